@@ -1,0 +1,297 @@
+"""Thin ctypes binding of libbi (include/bi.h).
+
+Argument marshalling only: every step of the forward path runs in the CUDA
+library.  PyTorch provides device memory and streams.  Importing this module
+loads ``_build/libbi.so`` and raises if it has not been built — there is no
+fallback path.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+
+import torch
+
+from . import build as _build
+
+BI_OK, BI_ERR_INVALID, BI_ERR_SHAPE, BI_ERR_UNSUPPORTED, BI_ERR_CUDA, BI_ERR_TIMEOUT, BI_ERR_DEVICE, \
+    BI_ERR_WORKSPACE = range(8)
+INVARIANT, VARIANT = 0, 1
+BF16, F32 = 0, 1
+EP_NONE, EP_RESIDUAL, EP_SWIGLU = 0, 1, 2
+KV_CHUNK, PAGE = 256, 16
+
+_STATUS_NAMES = {0: "BI_OK", 1: "BI_ERR_INVALID", 2: "BI_ERR_SHAPE", 3: "BI_ERR_UNSUPPORTED", 4: "BI_ERR_CUDA",
+                 5: "BI_ERR_TIMEOUT", 6: "BI_ERR_DEVICE", 7: "BI_ERR_WORKSPACE"}
+
+
+class BIError(RuntimeError):
+    def __init__(self, status: int, msg: str):
+        super().__init__(f"{_STATUS_NAMES.get(status, status)}: {msg}")
+        self.status = status
+
+
+def _load():
+    path = _build.LIB
+    if not os.path.exists(path):
+        raise ImportError(f"libbi.so is not built ({path}); run invariant_fixed_order_gb300.build.build()")
+    return ctypes.CDLL(path)
+
+
+_lib = _load()
+LIB_PATH = _build.LIB
+
+_vp, _i32, _i64, _f32, _f64, _sz = (ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_float,
+                                    ctypes.c_double, ctypes.c_size_t)
+_i32p = ctypes.POINTER(ctypes.c_int32)
+
+
+class ModelConfigC(ctypes.Structure):
+    _fields_ = [("d", _i32), ("H", _i32), ("Hkv", _i32), ("Dh", _i32), ("F", _i32), ("V", _i32),
+                ("n_layers", _i32), ("eps", _f32), ("rope_theta", _f64), ("max_pos", _i32)]
+
+
+class ModelWeightsC(ctypes.Structure):
+    _fields_ = [("embed", _vp), ("gamma_final", _vp), ("w_lm", _vp), ("gamma_attn", ctypes.POINTER(_vp)),
+                ("w_qkv", ctypes.POINTER(_vp)), ("w_o", ctypes.POINTER(_vp)), ("gamma_ffn", ctypes.POINTER(_vp)),
+                ("w_gu", ctypes.POINTER(_vp)), ("w_down", ctypes.POINTER(_vp))]
+
+
+class KVCacheC(ctypes.Structure):
+    _fields_ = [("k", ctypes.POINTER(_vp)), ("v", ctypes.POINTER(_vp)), ("num_pages", _i32)]
+
+
+class BatchC(ctypes.Structure):
+    _fields_ = [("B", _i32), ("q_len", _i32p), ("pos0", _i32p), ("token_ids", _vp), ("page_table", _vp),
+                ("max_pages", _i32), ("R", _i32), ("logit_rows", _i32p)]
+
+
+def _proto(name, restype, *args):
+    f = getattr(_lib, name)
+    f.restype = restype
+    f.argtypes = list(args)
+    return f
+
+
+_proto("bi_last_error", ctypes.c_char_p)
+_proto("bi_version", _i32)
+_proto("bi_check_status", _i32, _vp, _vp)
+_proto("bi_reset_status", _i32, _vp, _vp)
+_proto("bi_rmsnorm", _i32, _vp, _vp, _vp, _i64, _i32, _f32, _vp)
+_proto("bi_gemm_workspace_size", _sz, _i64, _i32, _i32, _i32)
+_proto("bi_gemm", _i32, _vp, _vp, _vp, _i32, _vp, _i32, _i64, _i32, _i32, _i32, _vp, _sz, _vp, _vp)
+_proto("bi_pack_gate_up", _i32, _vp, _vp, _vp, _i32, _i32, _vp)
+_proto("bi_rope_kv_append", _i32, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
+       _i32, _vp, _vp)
+_proto("bi_rope_table", _i32, _vp, _vp, _i32, _i32, _f64)
+_proto("bi_decode_attention_workspace_size", _sz, _i32, _i32, _i32, _i32, _i32)
+_proto("bi_decode_attention", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+       _f32, _i32, _vp, _sz, _vp, _vp)
+_proto("bi_prefill_attention", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+       _i32, _f32, _vp, _vp)
+_proto("bi_argmax", _i32, _vp, _vp, _i32, _i32, _vp)
+_proto("bi_embed", _i32, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp)
+_proto("bi_model_create", _i32, ctypes.POINTER(ModelConfigC), ctypes.POINTER(ModelWeightsC),
+       ctypes.POINTER(_vp))
+_proto("bi_model_destroy", None, _vp)
+_proto("bi_forward_workspace_size", _sz, ctypes.POINTER(ModelConfigC), _i32, _i32, _i32, _i32)
+_proto("bi_forward_step", _i32, _vp, ctypes.POINTER(BatchC), ctypes.POINTER(KVCacheC), _vp, _vp, _vp, _i32, _vp,
+       _sz, _vp, _vp)
+
+
+def _check(rc: int) -> None:
+    if rc != BI_OK:
+        raise BIError(rc, _lib.bi_last_error().decode(errors="replace"))
+
+
+def _p(t):
+    return None if t is None else ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream=None):
+    s = torch.cuda.current_stream() if stream is None else stream
+    return ctypes.c_void_p(s.cuda_stream)
+
+
+def version() -> int:
+    return int(_lib.bi_version())
+
+
+def new_status(device="cuda") -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device)
+
+
+def check_status(status: torch.Tensor, stream=None) -> None:
+    _check(_lib.bi_check_status(_p(status), _stream(stream)))
+
+
+def reset_status(status: torch.Tensor, stream=None) -> None:
+    _check(_lib.bi_reset_status(_p(status), _stream(stream)))
+
+
+def _bf16_bits(t: torch.Tensor):
+    assert t.dtype == torch.bfloat16 and t.is_contiguous(), "expected a contiguous bf16 tensor"
+    return _p(t)
+
+
+# ---- kernels ------------------------------------------------------------------
+
+def rmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-5, out: torch.Tensor | None = None,
+            stream=None) -> torch.Tensor:
+    d = x.shape[-1]
+    out = torch.empty_like(x) if out is None else out
+    _check(_lib.bi_rmsnorm(_bf16_bits(x), _bf16_bits(gamma), _bf16_bits(out), x.numel() // d, d, eps,
+                           _stream(stream)))
+    return out
+
+
+def gemm_workspace_size(M: int, N: int, K: int, mode: int = INVARIANT) -> int:
+    return int(_lib.bi_gemm_workspace_size(M, N, K, mode))
+
+
+def gemm(A: torch.Tensor, W: torch.Tensor, out: torch.Tensor | None = None, c_dtype: int = BF16,
+         residual: torch.Tensor | None = None, ep: int = EP_NONE, mode: int = INVARIANT,
+         ws: torch.Tensor | None = None, status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    M, K = A.shape
+    N = W.shape[0]
+    if out is None:
+        ncol = N // 2 if ep == EP_SWIGLU else N
+        out = torch.empty(M, ncol, device=A.device, dtype=torch.float32 if c_dtype == F32 else torch.bfloat16)
+    need = gemm_workspace_size(M, N, K, mode)
+    if need and (ws is None or ws.numel() < need):
+        ws = torch.empty(need, dtype=torch.uint8, device=A.device)
+    _check(_lib.bi_gemm(_p(A), _p(W), _p(out), c_dtype, _p(residual), ep, M, N, K, mode, _p(ws),
+                        0 if ws is None else ws.numel(), _p(status), _stream(stream)))
+    return out
+
+
+def pack_gate_up(w_gate: torch.Tensor, w_up: torch.Tensor, stream=None) -> torch.Tensor:
+    F, d = w_gate.shape
+    out = torch.empty(2 * F, d, dtype=torch.bfloat16, device=w_gate.device)
+    _check(_lib.bi_pack_gate_up(_p(w_gate), _p(w_up), _p(out), F, d, _stream(stream)))
+    return out
+
+
+def rope_table(n_pos: int, Dh: int, theta: float):
+    c = torch.empty(n_pos, Dh // 2, dtype=torch.float32)
+    s = torch.empty(n_pos, Dh // 2, dtype=torch.float32)
+    _check(_lib.bi_rope_table(_p(c), _p(s), n_pos, Dh, theta))
+    return c, s
+
+
+def rope_kv_append(qkv, tok_req, tok_pos, rope_cos, rope_sin, q_out, k_cache, v_cache, page_table, H, Hkv, Dh,
+                   status, stream=None):
+    T = qkv.shape[0]
+    _check(_lib.bi_rope_kv_append(_p(qkv), _p(tok_req), _p(tok_pos), _p(rope_cos), _p(rope_sin),
+                                  rope_cos.shape[0], _p(q_out), _p(k_cache), _p(v_cache), _p(page_table),
+                                  page_table.shape[-1], k_cache.shape[0], T, H, Hkv, Dh, _p(status),
+                                  _stream(stream)))
+
+
+def decode_attention_workspace_size(B: int, H: int, Dh: int, max_seq_len: int, mode: int = INVARIANT) -> int:
+    return int(_lib.bi_decode_attention_workspace_size(B, H, Dh, max_seq_len, mode))
+
+
+def decode_attention(q, k_cache, v_cache, page_table, seq_lens, max_seq_len: int, out_dtype: int = BF16,
+                     mode: int = INVARIANT, scale: float | None = None, ws=None, status=None, out=None,
+                     stream=None) -> torch.Tensor:
+    B, H, Dh = q.shape
+    Hkv = k_cache.shape[1]
+    if scale is None:
+        scale = float(torch.tensor(1.0, dtype=torch.float32) / torch.sqrt(torch.tensor(float(Dh))))
+    if out is None:
+        out = torch.empty(B, H, Dh, device=q.device, dtype=torch.float32 if out_dtype == F32 else torch.bfloat16)
+    need = decode_attention_workspace_size(B, H, Dh, max_seq_len, mode)
+    if ws is None or ws.numel() < need:
+        ws = torch.empty(need, dtype=torch.uint8, device=q.device)
+    _check(_lib.bi_decode_attention(_p(q), _p(k_cache), _p(v_cache), _p(page_table), _p(seq_lens), _p(out),
+                                    out_dtype, B, H, Hkv, Dh, page_table.shape[-1], k_cache.shape[0], max_seq_len,
+                                    scale, mode, _p(ws), ws.numel(), _p(status), _stream(stream)))
+    return out
+
+
+def prefill_attention(q, cu_q, q_pos0, k_cache, v_cache, page_table, out_dtype: int = BF16,
+                      scale: float | None = None, status=None, out=None, stream=None) -> torch.Tensor:
+    T, H, Dh = q.shape
+    B = cu_q.shape[0] - 1
+    Hkv = k_cache.shape[1]
+    if scale is None:
+        scale = float(torch.tensor(1.0, dtype=torch.float32) / torch.sqrt(torch.tensor(float(Dh))))
+    if out is None:
+        out = torch.empty(T, H, Dh, device=q.device, dtype=torch.float32 if out_dtype == F32 else torch.bfloat16)
+    _check(_lib.bi_prefill_attention(_p(q), _p(cu_q), _p(q_pos0), _p(k_cache), _p(v_cache), _p(page_table),
+                                     _p(out), out_dtype, B, T, H, Hkv, Dh, page_table.shape[-1], k_cache.shape[0],
+                                     scale, _p(status), _stream(stream)))
+    return out
+
+
+def argmax(logits: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    R, V = logits.shape
+    out = torch.empty(R, dtype=torch.int32, device=logits.device) if out is None else out
+    _check(_lib.bi_argmax(_p(logits), _p(out), R, V, _stream(stream)))
+    return out
+
+
+def embed(E: torch.Tensor, ids: torch.Tensor, status=None, out=None, stream=None) -> torch.Tensor:
+    V, d = E.shape
+    T = ids.shape[0]
+    out = torch.empty(T, d, dtype=torch.bfloat16, device=E.device) if out is None else out
+    _check(_lib.bi_embed(_p(E), _p(ids), _p(out), T, V, d, _p(status), _stream(stream)))
+    return out
+
+
+# ---- model ----------------------------------------------------------------------
+
+def _ptr_array(tensors):
+    arr = (_vp * len(tensors))(*[t.data_ptr() for t in tensors])
+    return arr
+
+
+class Model:
+    """Owns nothing but the library's model handle; the weight tensors are
+    borrowed (kept referenced here so they outlive the handle)."""
+
+    def __init__(self, cfg, layers: list, head: dict, max_pos: int):
+        self.cfg = cfg
+        self.layers = layers
+        self.head = head
+        self.max_pos = max_pos
+        self._c = ModelConfigC(cfg.d, cfg.H, cfg.Hkv, cfg.Dh, cfg.F, cfg.V, cfg.n_layers, cfg.eps, cfg.rope_theta,
+                               max_pos)
+        self._arrays = {k: _ptr_array([L[k] for L in layers])
+                        for k in ("gamma_attn", "w_qkv", "w_o", "gamma_ffn", "w_gu", "w_down")}
+        w = ModelWeightsC(head["embed"].data_ptr(), head["gamma_final"].data_ptr(), head["w_lm"].data_ptr(),
+                          self._arrays["gamma_attn"], self._arrays["w_qkv"], self._arrays["w_o"],
+                          self._arrays["gamma_ffn"], self._arrays["w_gu"], self._arrays["w_down"])
+        h = ctypes.c_void_p()
+        _check(_lib.bi_model_create(ctypes.byref(self._c), ctypes.byref(w), ctypes.byref(h)))
+        self._h = h
+
+    def close(self):
+        if getattr(self, "_h", None) is not None and self._h.value:
+            _lib.bi_model_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+    def workspace_size(self, max_T: int, max_B: int, max_R: int, max_seq: int) -> int:
+        return int(_lib.bi_forward_workspace_size(ctypes.byref(self._c), max_T, max_B, max_R, max_seq))
+
+    def forward_step(self, q_len, pos0, token_ids: torch.Tensor, page_table: torch.Tensor, kv_k: list, kv_v: list,
+                     logit_rows, ws: torch.Tensor, status: torch.Tensor, logits_out=None, tokens_out=None,
+                     hidden_out=None, mode: int = INVARIANT, stream=None):
+        """One ragged step.  q_len / pos0 / logit_rows are host int sequences."""
+        B = len(q_len)
+        ql = (ctypes.c_int32 * B)(*[int(v) for v in q_len])
+        p0 = (ctypes.c_int32 * B)(*[int(v) for v in pos0])
+        R = len(logit_rows)
+        rows = (ctypes.c_int32 * max(R, 1))(*[int(v) for v in logit_rows])
+        batch = BatchC(B, ql, p0, token_ids.data_ptr(), page_table.data_ptr(), page_table.shape[-1], R, rows)
+        ka, va = _ptr_array(kv_k), _ptr_array(kv_v)
+        kv = KVCacheC(ka, va, kv_k[0].shape[0])
+        _check(_lib.bi_forward_step(self._h, ctypes.byref(batch), ctypes.byref(kv), _p(logits_out), _p(tokens_out),
+                                    _p(hidden_out), mode, _p(ws), ws.numel(), _p(status), _stream(stream)))

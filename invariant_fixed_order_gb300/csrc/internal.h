@@ -1,0 +1,80 @@
+// Host-side declarations shared by the translation units of libbi.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include <string>
+
+#include "../../include/bi.h"
+
+namespace bi {
+
+// thread-local error message (api.cu)
+void set_error(const std::string& msg);
+bi_status fail(bi_status s, const std::string& msg);
+bi_status cuda_fail(cudaError_t e, const char* what);
+int num_sms();
+
+// ---- elementwise / row kernels (k_rows.cu) ----
+cudaError_t launch_rmsnorm(const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y, int64_t rows,
+                           int32_t d, float eps, cudaStream_t s);
+cudaError_t launch_embed(const bi_bf16* E, const int32_t* ids, bi_bf16* x, int32_t T, int32_t V,
+                         int32_t d, int32_t* status, cudaStream_t s);
+cudaError_t launch_rope_kv_append(const float* qkv, const int32_t* tok_req, const int32_t* tok_pos,
+                                  const float* rc, const float* rs, int32_t max_pos, bi_bf16* q_out,
+                                  bi_bf16* kc, bi_bf16* vc, const int32_t* page_table,
+                                  int32_t max_pages, int32_t num_pages, int32_t T, int32_t H,
+                                  int32_t Hkv, int32_t Dh, int32_t* status, cudaStream_t s);
+cudaError_t launch_argmax(const float* logits, int32_t* out, int32_t R, int32_t V, cudaStream_t s);
+cudaError_t launch_pack_gate_up(const bi_bf16* g, const bi_bf16* u, bi_bf16* gu, int32_t F,
+                                int32_t d, cudaStream_t s);
+cudaError_t launch_gather_rows(const bi_bf16* x, const int32_t* rows, bi_bf16* out, int32_t R,
+                               int32_t d, cudaStream_t s);
+
+// ---- attention (k_attention.cu) ----
+// How a work entry e maps to (query/output row t, request r, position p).
+struct EntryMap {
+    int32_t kind;            // 0: decode by request, 1: token list, 2: ragged cu_q
+    const int32_t* a;        // kind 0: seq_lens[B]; kind 1: list[n]; kind 2: cu_q[B+1]
+    const int32_t* b;        // kind 1: tok_req[T];  kind 2: q_pos0[B]
+    const int32_t* c;        // kind 1: tok_pos[T]
+    int32_t nreq;            // kind 2: B
+};
+
+struct AttnGeom {
+    const bi_bf16* q;        // [rows, H, Dh]
+    const bi_bf16* kc;       // [num_pages, Hkv, 16, Dh]
+    const bi_bf16* vc;
+    const int32_t* page_table;
+    void* out;               // [rows, H, Dh]
+    int32_t out_f32;
+    int32_t H, Hkv, Dh, max_pages, num_pages;
+    float scale;
+    int32_t* status;
+};
+
+// split size: 0 -> fixed BI_KV_CHUNK chunks; >0 -> variant rule with chunk2
+size_t decode_ws_bytes(int32_t n_entries, int32_t H, int32_t Dh, int32_t max_splits);
+int32_t invariant_max_splits(int32_t max_seq);
+// variant occupancy rule: fills chunk2 and the bound on splits per request
+void variant_split_plan(int32_t B, int32_t H, int32_t Hkv, int32_t max_seq, int32_t* chunk2,
+                        int32_t* max_splits);
+cudaError_t launch_decode_attention(const AttnGeom& g, const EntryMap& em, int32_t n_entries,
+                                    int32_t max_splits, int32_t variant_chunk2, float* ws_o,
+                                    float* ws_ml, cudaStream_t s);
+cudaError_t launch_prefill_attention(const AttnGeom& g, const EntryMap& em, int32_t n_entries,
+                                     cudaStream_t s);
+bool attention_supported(int32_t H, int32_t Hkv, int32_t Dh);
+
+// ---- GEMM (k_gemm.cu) ----
+struct GemmPlan {
+    int32_t splits;          // 1 = invariant path
+};
+GemmPlan gemm_plan(int64_t M, int32_t N, int32_t K, bi_mode mode);
+size_t gemm_ws_bytes(int64_t M, int32_t N, int32_t K, bi_mode mode);
+bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype,
+                   const bi_bf16* residual, bi_epilogue ep, int64_t M, int32_t N, int32_t K,
+                   bi_mode mode, void* ws, size_t ws_bytes, int32_t* status, cudaStream_t s);
+
+}  // namespace bi

@@ -1,0 +1,254 @@
+// Row-wise kernels: RMSNorm, embedding gather, RoPE + paged KV append, greedy
+// argmax, gate/up packing, row gather.
+#include "common.cuh"
+#include "internal.h"
+
+namespace bi {
+
+// ---------------------------------------------------------------------------
+// RMSNorm: one warp per row ("Lockstep", "The fix": one fixed reduction order).
+// Lane l owns 16-byte chunks l, l+32, l+64, ... and adds their squares in
+// ascending element order with fused multiply-adds; the 32 lane sums then meet
+// in an xor-butterfly (16, 8, 4, 2, 1).  Addition is commutative, so every
+// lane ends with the same bits and the order depends on d only.
+// ---------------------------------------------------------------------------
+constexpr int kNormWarps = 8;
+
+__global__ void __launch_bounds__(kNormWarps * 32)
+rmsnorm_kernel(const uint4* x, const uint4* __restrict__ gamma, uint4* y, int64_t rows,
+               int32_t d8, float eps, float fd) {
+    const int64_t row = static_cast<int64_t>(blockIdx.x) * kNormWarps + threadIdx.x / 32;
+    const int lane = threadIdx.x & 31;
+    if (row >= rows) return;  // uniform per warp
+    const uint4* xr = x + row * d8;
+    float ss = 0.0f;
+    for (int c = lane; c < d8; c += 32) {
+        const uint4 v = xr[c];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float a = bf16_lo(w[e]);
+            ss = __fmaf_rn(a, a, ss);
+            const float b = bf16_hi(w[e]);
+            ss = __fmaf_rn(b, b, ss);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, off));
+    const float mean = __fdiv_rn(ss, fd);
+    const float rinv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
+    uint4* yr = y + row * d8;
+    for (int c = lane; c < d8; c += 32) {
+        const uint4 v = xr[c];
+        const uint4 g = gamma[c];
+        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+        const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
+        uint32_t o[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+            const float a = __fmul_rn(__fmul_rn(bf16_lo(w[e]), rinv), bf16_lo(gw[e]));
+            const float b = __fmul_rn(__fmul_rn(bf16_hi(w[e]), rinv), bf16_hi(gw[e]));
+            o[e] = pack_bf16x2(a, b);
+        }
+        yr[c] = make_uint4(o[0], o[1], o[2], o[3]);
+    }
+}
+
+cudaError_t launch_rmsnorm(const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y, int64_t rows,
+                           int32_t d, float eps, cudaStream_t s) {
+    if (rows <= 0) return cudaSuccess;
+    const int64_t blocks = (rows + kNormWarps - 1) / kNormWarps;
+    rmsnorm_kernel<<<static_cast<unsigned>(blocks), kNormWarps * 32, 0, s>>>(
+        reinterpret_cast<const uint4*>(x), reinterpret_cast<const uint4*>(gamma),
+        reinterpret_cast<uint4*>(y), rows, d / 8, eps, static_cast<float>(d));
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Embedding gather: x[t] = E[ids[t]].
+// ---------------------------------------------------------------------------
+__global__ void embed_kernel(const uint4* __restrict__ E, const int32_t* __restrict__ ids,
+                             uint4* __restrict__ x, int32_t V, int32_t d8, int32_t* status) {
+    const int32_t t = blockIdx.x;
+    const int32_t id = ids[t];
+    const bool ok = id >= 0 && id < V;
+    if (!ok && threadIdx.x == 0) report(status, BI_DEV_BAD_TOKEN);
+    for (int c = threadIdx.x; c < d8; c += blockDim.x)
+        x[static_cast<int64_t>(t) * d8 + c] = ok ? E[static_cast<int64_t>(id) * d8 + c] : make_uint4(0, 0, 0, 0);
+}
+
+cudaError_t launch_embed(const bi_bf16* E, const int32_t* ids, bi_bf16* x, int32_t T, int32_t V,
+                         int32_t d, int32_t* status, cudaStream_t s) {
+    if (T <= 0) return cudaSuccess;
+    embed_kernel<<<T, 128, 0, s>>>(reinterpret_cast<const uint4*>(E), ids,
+                                   reinterpret_cast<uint4*>(x), V, d / 8, status);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// RoPE (rotate-half) + KV append.  q and k heads are rotated in fp32 from the
+// fp32 projection, each output rounded once to bf16:
+//   out[i]        = x[i] * cos - x[i + Dh/2] * sin
+//   out[i + Dh/2] = x[i + Dh/2] * cos + x[i] * sin
+// (each product rounded, then the sum: no fused multiply-add).
+// ---------------------------------------------------------------------------
+__global__ void __launch_bounds__(256)
+rope_append_kernel(const float* __restrict__ qkv, const int32_t* __restrict__ tok_req,
+                   const int32_t* __restrict__ tok_pos, const float* __restrict__ rc,
+                   const float* __restrict__ rs, int32_t max_pos, uint16_t* __restrict__ q_out,
+                   uint16_t* __restrict__ kc, uint16_t* __restrict__ vc,
+                   const int32_t* __restrict__ page_table, int32_t max_pages, int32_t num_pages,
+                   int32_t H, int32_t Hkv, int32_t Dh, int32_t* status) {
+    const int32_t t = blockIdx.x;
+    const int32_t half = Dh / 2;
+    const int32_t pos = tok_pos[t];
+    const int32_t req = tok_req[t];
+    bool ok = pos >= 0 && pos < max_pos && (pos / BI_PAGE) < max_pages;
+    int32_t page = 0;
+    if (ok) {
+        page = page_table[static_cast<int64_t>(req) * max_pages + pos / BI_PAGE];
+        if (page < 0 || page >= num_pages) {
+            if (threadIdx.x == 0) report(status, BI_DEV_BAD_PAGE);
+            ok = false;
+        }
+    } else if (threadIdx.x == 0) {
+        report(status, BI_DEV_BAD_POSITION);
+    }
+    const int32_t slot = pos & (BI_PAGE - 1);
+    const int32_t nqkv = (H + 2 * Hkv) * Dh;
+    const float* row = qkv + static_cast<int64_t>(t) * nqkv;
+    const int32_t work = (H + 2 * Hkv) * half;
+    for (int32_t w = threadIdx.x; w < work; w += blockDim.x) {
+        const int32_t head = w / half;
+        const int32_t i = w - head * half;
+        const float x0 = row[head * Dh + i];
+        const float x1 = row[head * Dh + i + half];
+        float r0, r1;
+        if (head < H + Hkv) {
+            const float c = ok ? rc[static_cast<int64_t>(pos) * half + i] : 1.0f;
+            const float sn = ok ? rs[static_cast<int64_t>(pos) * half + i] : 0.0f;
+            r0 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, sn));
+            r1 = __fadd_rn(__fmul_rn(x1, c), __fmul_rn(x0, sn));
+        } else {
+            r0 = x0;
+            r1 = x1;
+        }
+        const uint16_t b0 = f32_to_bf16(r0), b1 = f32_to_bf16(r1);
+        if (head < H) {
+            uint16_t* qo = q_out + (static_cast<int64_t>(t) * H + head) * Dh;
+            qo[i] = b0;
+            qo[i + half] = b1;
+        } else if (ok) {
+            const bool is_k = head < H + Hkv;
+            const int32_t g = is_k ? head - H : head - H - Hkv;
+            uint16_t* dst = (is_k ? kc : vc) +
+                            ((static_cast<int64_t>(page) * Hkv + g) * BI_PAGE + slot) * Dh;
+            dst[i] = b0;
+            dst[i + half] = b1;
+        }
+    }
+}
+
+cudaError_t launch_rope_kv_append(const float* qkv, const int32_t* tok_req, const int32_t* tok_pos,
+                                  const float* rc, const float* rs, int32_t max_pos, bi_bf16* q_out,
+                                  bi_bf16* kc, bi_bf16* vc, const int32_t* page_table,
+                                  int32_t max_pages, int32_t num_pages, int32_t T, int32_t H,
+                                  int32_t Hkv, int32_t Dh, int32_t* status, cudaStream_t s) {
+    if (T <= 0) return cudaSuccess;
+    rope_append_kernel<<<T, 256, 0, s>>>(qkv, tok_req, tok_pos, rc, rs, max_pos, q_out, kc, vc,
+                                         page_table, max_pages, num_pages, H, Hkv, Dh, status);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Greedy argmax ("temperature=0 means deterministic").  (value, index) pairs
+// are totally ordered: a NaN beats every number, a larger number beats a
+// smaller one, and between equals (or two NaNs) the lower index wins.  The
+// winner of a totally ordered set does not depend on the reduction order.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ bool beats(float a, int32_t ia, float b, int32_t ib) {
+    const bool an = isnan(a), bn = isnan(b);
+    if (an != bn) return an;
+    if (!an && a != b) return a > b;
+    return ia < ib;
+}
+
+constexpr int kArgmaxThreads = 1024;
+
+__global__ void __launch_bounds__(kArgmaxThreads)
+argmax_kernel(const float* __restrict__ logits, int32_t* __restrict__ out, int32_t V) {
+    __shared__ float sv[kArgmaxThreads / 32];
+    __shared__ int32_t si[kArgmaxThreads / 32];
+    const float* row = logits + static_cast<int64_t>(blockIdx.x) * V;
+    float bv = -INFINITY;
+    int32_t bi = 0x7fffffff;
+    for (int32_t j = threadIdx.x; j < V; j += kArgmaxThreads) {
+        const float v = row[j];
+        if (beats(v, j, bv, bi)) { bv = v; bi = j; }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+        const int32_t oi = __shfl_xor_sync(0xffffffffu, bi, off);
+        if (beats(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+    }
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+    if (lane == 0) { sv[warp] = bv; si[warp] = bi; }
+    __syncthreads();
+    if (warp == 0) {
+        bv = sv[lane];
+        bi = si[lane];
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) {
+            const float ov = __shfl_xor_sync(0xffffffffu, bv, off);
+            const int32_t oi = __shfl_xor_sync(0xffffffffu, bi, off);
+            if (beats(ov, oi, bv, bi)) { bv = ov; bi = oi; }
+        }
+        if (lane == 0) out[blockIdx.x] = bi;
+    }
+}
+
+cudaError_t launch_argmax(const float* logits, int32_t* out, int32_t R, int32_t V, cudaStream_t s) {
+    if (R <= 0) return cudaSuccess;
+    argmax_kernel<<<R, kArgmaxThreads, 0, s>>>(logits, out, V);
+    return cudaGetLastError();
+}
+
+// ---------------------------------------------------------------------------
+// Gate/up interleave and row gather (plain copies).
+// ---------------------------------------------------------------------------
+__global__ void pack_gate_up_kernel(const uint4* __restrict__ g, const uint4* __restrict__ u,
+                                    uint4* __restrict__ gu, int32_t d8) {
+    const int32_t r = blockIdx.x;  // output row in [0, 2F)
+    const int32_t j = r / (2 * BI_SWIGLU_GROUP), w = r % (2 * BI_SWIGLU_GROUP);
+    const uint4* src = (w < BI_SWIGLU_GROUP ? g : u) +
+                       static_cast<int64_t>(j * BI_SWIGLU_GROUP + (w % BI_SWIGLU_GROUP)) * d8;
+    for (int c = threadIdx.x; c < d8; c += blockDim.x) gu[static_cast<int64_t>(r) * d8 + c] = src[c];
+}
+
+cudaError_t launch_pack_gate_up(const bi_bf16* g, const bi_bf16* u, bi_bf16* gu, int32_t F,
+                                int32_t d, cudaStream_t s) {
+    if (F <= 0) return cudaSuccess;
+    pack_gate_up_kernel<<<2 * F, 256, 0, s>>>(reinterpret_cast<const uint4*>(g),
+                                             reinterpret_cast<const uint4*>(u),
+                                             reinterpret_cast<uint4*>(gu), d / 8);
+    return cudaGetLastError();
+}
+
+__global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ rows,
+                                   uint4* __restrict__ out, int32_t d8) {
+    const int32_t r = blockIdx.x;
+    const int64_t src = rows[r];
+    for (int c = threadIdx.x; c < d8; c += blockDim.x)
+        out[static_cast<int64_t>(r) * d8 + c] = x[src * d8 + c];
+}
+
+cudaError_t launch_gather_rows(const bi_bf16* x, const int32_t* rows, bi_bf16* out, int32_t R,
+                               int32_t d, cudaStream_t s) {
+    if (R <= 0) return cudaSuccess;
+    gather_rows_kernel<<<R, 128, 0, s>>>(reinterpret_cast<const uint4*>(x), rows,
+                                         reinterpret_cast<uint4*>(out), d / 8);
+    return cudaGetLastError();
+}
+
+}  // namespace bi
