@@ -1,0 +1,448 @@
+"""Benchmark: batch-invariant decode step, Llama-3-8B shapes, one GB300 per rank.
+
+Workload (one step): a decode step of a ragged batch of B requests (B = 64 by
+default; contexts uniform in [128, 8192], paged KV with page 16, K/V ~ N(0, 1)
+bf16) through the whole path — embedding, one 8B-shaped decoder layer (d 4096,
+32/8 heads, head dim 128, SwiGLU 14336), final RMSNorm, the 128256-wide LM
+head in fp32 and greedy argmax — via bi_forward_step.  Weights are random
+N(0, 0.02) bf16 (synthetic data; no trained weights).  The step reads ~2.6 GB,
+far more than L2, so no flush is needed between steps.
+
+Prints one JSON line (rank 0).  `value` is decode tokens/s of the invariant
+mode at batch B, summed over ranks (each rank is an independent replica with
+its own batch: weak scaling, no collective on the data path).  `sweep` holds
+invariant vs variant tokens/s and the HBM-roofline fraction of the whole step
+for B in 1..64.  `roofline` is for the dominant kernel (the tcgen05 GEMM),
+timed with CUDA events on its launching stream.  `cpu_baseline` is the CPU
+oracle on a bounded sample of the same workload.
+
+--impl reference times the CPU oracle (the slow, plain definition) on the same
+workload as the reference arm.
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import os
+import statistics
+import subprocess
+import sys
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+METRIC = "decode tokens/s (8B-shape, bs 1-64, invariant vs variant); % HBM roofline"
+WORKLOAD = "llama3-8b-shape decode step: 1 decoder layer + final norm + LM head + argmax"
+CTX_LO, CTX_HI = 128, 8192
+DATA_SEED = 43          # 42 + config index
+WEIGHT_SEED = 1234
+
+
+def parse():
+    p = argparse.ArgumentParser()
+    p.add_argument("--gpus", type=int, default=1)
+    p.add_argument("--steps", type=int, default=20)
+    p.add_argument("--warmup", type=int, default=5)
+    p.add_argument("--batch", type=int, default=64)
+    p.add_argument("--impl", default="ours", choices=["ours", "reference"])
+    p.add_argument("--no-sweep", action="store_true")
+    p.add_argument("--no-cpu", action="store_true")
+    p.add_argument("--cpu-seconds", type=float, default=15.0)
+    return p.parse_args()
+
+
+def dist_env():
+    return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
+
+
+def peaks():
+    try:
+        with open(os.path.join(ROOT, "MEASURED_PEAKS.json")) as fh:
+            j = json.load(fh)
+        return float(j["hbm_gbs"]), float(j["bf16_tflops"]), "measured"
+    except Exception:
+        return 6800.0, 1900.0, "fallback"
+
+
+class ClockSampler:
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits", "-lms", "200",
+                 "-i", str(gpu_index)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except Exception:
+            self.proc = None
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"]}
+        time.sleep(0.25)
+        self.proc.terminate()
+        try:
+            out, _ = self.proc.communicate(timeout=5)
+        except Exception:
+            self.proc.kill()
+            out = ""
+        sm, mx, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in out.splitlines():
+            parts = [x.strip() for x in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                mx.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower().startswith("active"):
+                    reasons.add(n)
+        loaded = [s for s in sm if s > 0]
+        return {"sm_mhz": statistics.median(loaded) if loaded else None,
+                "sm_max_mhz": max(mx) if mx else None, "reasons": sorted(reasons), "samples": len(sm)}
+
+
+# ---------------------------------------------------------------------------
+# workload
+# ---------------------------------------------------------------------------
+
+def make_workload(B: int, rank: int):
+    from invariant_fixed_order_gb300 import synth
+    from invariant_fixed_order_gb300.config import LLAMA3_8B_1L
+    cfg = LLAMA3_8B_1L
+    ctx = synth.uniform_ints(B, CTX_LO, CTX_HI, DATA_SEED + 1000 * rank)
+    ids = synth.token_ids(B, cfg.V, DATA_SEED + 1000 * rank + 1)
+    return cfg, ctx, ids
+
+
+class GpuWorkload:
+    def __init__(self, B: int, rank: int, device: str):
+        import torch
+        from invariant_fixed_order_gb300 import synth
+        from invariant_fixed_order_gb300.engine import Engine
+        self.cfg, self.ctx, self.ids = make_workload(B, rank)
+        cfg = self.cfg
+        self.B = B
+        self.max_pages = CTX_HI // 16 + 1
+        pages_needed = int(sum((int(s) + 15) // 16 for s in self.ctx))
+        self.eng = Engine(cfg, seed=WEIGHT_SEED, num_pages=pages_needed + 64, max_pages=self.max_pages, max_T=B,
+                          max_B=B, max_R=B, max_seq=self.max_pages * 16, device=device)
+        # per-request pages and KV history (positions 0 .. s-2; the step appends s-1)
+        self.table = np.zeros((B, self.max_pages), np.int32)
+        for i, s in enumerate(self.ctx):
+            pages = self.eng.pool.alloc((int(s) + 15) // 16)
+            self.table[i, :len(pages)] = pages
+            n = int(s) - 1
+            if n > 0:
+                k, v = synth.kv_history(n, cfg.Hkv, cfg.Dh, DATA_SEED * 7919 + i, device=device)
+                pos = np.arange(n)
+                pg = torch.from_numpy(self.table[i, pos // 16].astype(np.int64)).to(device)
+                sl = torch.from_numpy((pos % 16).astype(np.int64)).to(device)
+                self.eng.k[0][pg, :, sl, :] = k
+                self.eng.v[0][pg, :, sl, :] = v
+        self.d_table = torch.from_numpy(self.table).to(device)
+        self.d_ids = torch.from_numpy(self.ids).to(device)
+        self.logits = torch.empty(B, cfg.V, dtype=torch.float32, device=device)
+        self.tokens = torch.empty(B, dtype=torch.int32, device=device)
+        torch.cuda.synchronize()
+
+    def step(self, b: int, mode: int, stream=None):
+        """Decode step over the first b requests."""
+        self.eng.step([1] * b, [int(s) - 1 for s in self.ctx[:b]], self.d_ids[:b], self.d_table[:b],
+                      list(range(b)), mode=mode, stream=stream, logits_out=self.logits[:b], tokens_out=self.tokens)
+
+    def step_bytes(self, b: int) -> int:
+        from invariant_fixed_order_gb300 import roofline
+        return roofline.decode_step_bytes(self.cfg, [int(s) for s in self.ctx[:b]])
+
+
+def time_steps(fn, steps: int, warmup: int, stream) -> float:
+    import torch
+    for _ in range(warmup):
+        fn()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(steps):
+        fn()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    return e0.elapsed_time(e1) / steps
+
+
+def gemm_roofline(w: GpuWorkload, steps: int, stream, hbm_peak: float) -> dict:
+    """Times every GEMM of the step standalone (same shapes, same weights) with
+    CUDA events on the launching stream; algorithmic bytes per launch are the
+    weights, the activations in and the outputs (plus the residual read)."""
+    import torch
+    from invariant_fixed_order_gb300 import bi
+    cfg, B = w.cfg, w.B
+    L = w.eng.layers[0]
+    dev = w.d_ids.device
+    x = torch.randn(B, cfg.d, device=dev).to(torch.bfloat16)
+    h = torch.randn(B, cfg.F, device=dev).to(torch.bfloat16)
+    qkv = torch.empty(B, cfg.qkv_dim, dtype=torch.float32, device=dev)
+    res = torch.randn(B, cfg.d, device=dev).to(torch.bfloat16)
+    hout = torch.empty(B, cfg.F, dtype=torch.bfloat16, device=dev)
+    logits = torch.empty(B, cfg.V, dtype=torch.float32, device=dev)
+    shapes = [
+        ("qkv", lambda: bi.gemm(x, L["w_qkv"], out=qkv, c_dtype=bi.F32, stream=stream),
+         cfg.qkv_dim * cfg.d * 2 + B * cfg.d * 2 + B * cfg.qkv_dim * 4),
+        ("o", lambda: bi.gemm(x, L["w_o"], out=res, residual=res, ep=bi.EP_RESIDUAL, stream=stream),
+         cfg.d * cfg.d * 2 + B * cfg.d * 2 + B * cfg.d * 4),
+        ("gate_up", lambda: bi.gemm(x, L["w_gu"], out=hout, ep=bi.EP_SWIGLU, stream=stream),
+         2 * cfg.F * cfg.d * 2 + B * cfg.d * 2 + B * cfg.F * 2),
+        ("down", lambda: bi.gemm(h, L["w_down"], out=res, residual=res, ep=bi.EP_RESIDUAL, stream=stream),
+         cfg.d * cfg.F * 2 + B * cfg.F * 2 + B * cfg.d * 4),
+        ("lm_head", lambda: bi.gemm(x, w.eng.head["w_lm"], out=logits, c_dtype=bi.F32, stream=stream),
+         cfg.V * cfg.d * 2 + B * cfg.d * 2 + B * cfg.V * 4),
+    ]
+    per = {}
+    tot_bytes, tot_ms = 0, 0.0
+    for name, fn, nbytes in shapes:
+        ms = time_steps(fn, max(steps, 10), 3, stream)
+        per[name] = {"us": round(ms * 1e3, 2), "GBps": round(nbytes / (ms * 1e-3) / 1e9, 1),
+                     "frac": round(nbytes / (ms * 1e-3) / 1e9 / hbm_peak, 3)}
+        tot_bytes += nbytes
+        tot_ms += ms
+    n = len(shapes)
+    achieved = (tot_bytes / n) / (tot_ms / n * 1e-3) / 1e9
+    return {"per_launch_bytes": tot_bytes / n, "per_launch_ms": tot_ms / n, "achieved": achieved, "per_gemm": per}
+
+
+def attention_time(w: GpuWorkload, steps: int, stream) -> dict:
+    import torch
+    from invariant_fixed_order_gb300 import bi
+    cfg, B = w.cfg, w.B
+    dev = w.d_ids.device
+    q = torch.randn(B, cfg.H, cfg.Dh, device=dev).to(torch.bfloat16)
+    sl = torch.from_numpy(np.asarray(w.ctx, np.int32)).to(dev)
+    ws = torch.empty(bi.decode_attention_workspace_size(B, cfg.H, cfg.Dh, w.max_pages * 16, bi.VARIANT),
+                     dtype=torch.uint8, device=dev)
+    out = torch.empty(B, cfg.H, cfg.Dh, dtype=torch.bfloat16, device=dev)
+    fn = lambda: bi.decode_attention(q, w.eng.k[0], w.eng.v[0], w.d_table, sl, int(max(w.ctx)), ws=ws, out=out,
+                                     stream=stream)
+    ms = time_steps(fn, max(steps, 10), 3, stream)
+    kv = sum(2 * int(s) * cfg.Hkv * cfg.Dh * 2 for s in w.ctx)
+    return {"us": round(ms * 1e3, 2), "GBps": round(kv / (ms * 1e-3) / 1e9, 1), "kv_bytes": kv}
+
+
+# ---------------------------------------------------------------------------
+# CPU oracle timing
+# ---------------------------------------------------------------------------
+
+class OracleSample:
+    """The CPU oracle on the same workload: shapes, contexts, token ids and
+    distributions as the GPU run (values drawn by the CPU generator)."""
+
+    def __init__(self, B: int, rank: int):
+        import oracle
+        import torch
+        from invariant_fixed_order_gb300 import synth
+        oracle.build()
+        self.cfg, self.ctx, self.ids = make_workload(B, rank)
+        cfg = self.cfg
+        wl = synth.layer_weights(cfg, WEIGHT_SEED, "cpu", 0)
+        hd = synth.head_weights(cfg, WEIGHT_SEED, "cpu")
+        self.w = {k: synth.to_f32_numpy(v) for k, v in wl.items()}
+        self.gamma_final = synth.to_f32_numpy(hd["gamma_final"])
+        self.w_lm = synth.to_f32_numpy(hd["w_lm"])
+        self.x = synth.to_f32_numpy(hd["embed"][torch.from_numpy(self.ids.astype(np.int64))])
+        del wl, hd
+        self.dims = oracle.Dims(cfg.d, cfg.H, cfg.Hkv, cfg.Dh, cfg.F, cfg.eps, cfg.rope_theta)
+        self.B = B
+        self.next = 0
+
+    def run(self, target_s: float) -> dict:
+        """One decode step (layer + LM head + argmax) per request, in request
+        order (wrapping around), until ~target_s of oracle time."""
+        import oracle
+        from invariant_fixed_order_gb300 import synth
+        cfg = self.cfg
+        done, t_total = 0, 0.0
+        while t_total < target_s and done < 4 * self.B:
+            i = self.next % self.B
+            self.next += 1
+            n = int(self.ctx[i]) - 1
+            k, v = synth.kv_history(max(n, 1), cfg.Hkv, cfg.Dh, DATA_SEED * 7919 + i, device="cpu")
+            kf, vf = synth.to_f32_numpy(k), synth.to_f32_numpy(v)
+            t0 = time.perf_counter()
+            x_out, _, _, _ = oracle.layer_forward(self.dims, self.w, [1], [n], [kf], [vf], self.x[i:i + 1])
+            oracle.lm_head(self.dims, self.gamma_final, self.w_lm, x_out, [0])
+            t_total += time.perf_counter() - t0
+            done += 1
+        return {"value": done / t_total, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
+                "sample": f"{done} decode steps (1 layer + LM head + argmax) of requests drawn in order from the "
+                          f"{self.B}-request batch, {t_total:.1f} s of oracle time"}
+
+
+# ---------------------------------------------------------------------------
+# arms
+# ---------------------------------------------------------------------------
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return
+    per_step = max(1.0, min(20.0, 150.0 / max(args.steps + args.warmup, 1)))
+    sample = OracleSample(args.batch, 0)
+    rates = []
+    for i in range(args.warmup + args.steps):
+        r = sample.run(per_step)
+        if i >= args.warmup:
+            rates.append(r)
+    value = statistics.median(x["value"] for x in rates)
+    line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+            "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * args.batch / value,
+            "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch": args.batch, "context": [CTX_LO, CTX_HI]},
+            "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": rates[0]["cores"], "kind": "oracle",
+                             "sample": rates[0]["sample"] + " per step"},
+            "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def run_ours(args):
+    import torch
+    rank, world, local_rank = dist_env()
+    torch.cuda.set_device(local_rank)
+    device = f"cuda:{local_rank}"
+    if world > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=torch.device(device))
+    from __graft_entry__ import build
+    build()
+    from invariant_fixed_order_gb300 import bi
+    hbm_peak, _, peak_kind = peaks()
+
+    stream = torch.cuda.current_stream()
+    sampler = ClockSampler(local_rank)
+    w = GpuWorkload(args.batch, rank, device)
+    B = args.batch
+
+    def barrier():
+        if world > 1:
+            torch.distributed.barrier()
+
+    # ---- main timed region: K invariant steps at batch B ----
+    for _ in range(max(args.warmup, 3)):
+        w.step(B, bi.INVARIANT)
+    torch.cuda.synchronize()
+    barrier()
+    torch.cuda.synchronize()
+    e0 = torch.cuda.Event(enable_timing=True)
+    e1 = torch.cuda.Event(enable_timing=True)
+    e0.record(stream)
+    for _ in range(args.steps):
+        w.step(B, bi.INVARIANT)
+    e1.record(stream)
+    torch.cuda.synchronize()
+    barrier()
+    ms = e0.elapsed_time(e1) / args.steps
+    if world > 1:
+        t = torch.tensor([ms], device=device)
+        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
+        ms = float(t.item())
+    w.eng.check()
+    value = world * B / (ms * 1e-3)
+    launches_per_step = 13  # embed, 2 rmsnorm, 4 GEMMs, rope, decode split, merge, gather, final norm, LM GEMM
+    launches_per_step += 1  # argmax
+
+    # ---- e2e: host buffers in, tokens back, through the public API ----
+    pin_ids = torch.from_numpy(w.ids).pin_memory()
+    pin_table = torch.from_numpy(w.table).pin_memory()
+    pin_tok = torch.empty(B, dtype=torch.int32).pin_memory()
+    d_ids = torch.empty_like(w.d_ids)
+    d_table = torch.empty_like(w.d_table)
+
+    def e2e_step():
+        d_ids.copy_(pin_ids, non_blocking=True)
+        d_table.copy_(pin_table, non_blocking=True)
+        w.eng.step([1] * B, [int(s) - 1 for s in w.ctx], d_ids, d_table, list(range(B)), mode=bi.INVARIANT,
+                   logits_out=w.logits, tokens_out=w.tokens)
+        pin_tok.copy_(w.tokens, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_step()
+    torch.cuda.synchronize()
+    e2e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    meta_bytes = (3 * B + B) * 4
+    h2d = pin_ids.numel() * 4 + pin_table.numel() * 4 + meta_bytes
+    d2h = B * 4
+
+    # ---- sweep: invariant vs variant over batch sizes ----
+    sweep = []
+    if not args.no_sweep:
+        for b in (1, 2, 4, 8, 16, 32, 64):
+            if b > B:
+                break
+            row = {"bs": b}
+            for name, mode in (("invariant", bi.INVARIANT), ("variant", bi.VARIANT)):
+                t = time_steps(lambda: w.step(b, mode), max(args.steps, 10), 3, stream)
+                row[name + "_tok_s"] = round(b / (t * 1e-3), 1)
+                row[name + "_us"] = round(t * 1e3, 1)
+                row[name + "_hbm_frac"] = round(w.step_bytes(b) / (t * 1e-3) / 1e9 / hbm_peak, 3)
+            sweep.append(row)
+    w.eng.check()
+
+    # ---- dominant kernel (GEMM) and attention, timed standalone with events ----
+    g = gemm_roofline(w, args.steps, stream, hbm_peak)
+    att = attention_time(w, args.steps, stream)
+    clocks = sampler.stop()
+    step_bytes = w.step_bytes(B)
+
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu:
+        cpu = OracleSample(B, rank).run(args.cpu_seconds)
+
+    if rank == 0:
+        line = {
+            "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
+            "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+            "config": {"workload": WORKLOAD, "batch_per_gpu": B, "context": [CTX_LO, CTX_HI],
+                       "mode": "invariant", "parallelism": f"replicas{world}",
+                       "l2": "inputs larger than L2 (step reads %.2f GB)" % (step_bytes / 1e9)},
+            "step_hbm_frac": round(step_bytes / (ms * 1e-3) / 1e9 / hbm_peak, 3),
+            "roofline": {"bound": "hbm", "kernel": "gemm_tc_kernel", "achieved": round(g["achieved"], 1),
+                         "peak": hbm_peak, "unit": "GB/s", "frac": round(g["achieved"] / hbm_peak, 3),
+                         "traffic": None, "peak_kind": peak_kind, "per_gemm": g["per_gemm"],
+                         "per_launch_bytes": int(g["per_launch_bytes"])},
+            "attention": att,
+            "e2e": {"value": round(world * B / (e2e_ms * 1e-3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
+                    "d2h_bytes_per_step": d2h},
+            "gpu_launches": launches_per_step * args.steps,
+            "clocks": clocks,
+            "sweep": sweep,
+        }
+        if cpu is not None:
+            line["cpu_baseline"] = cpu
+        print(json.dumps(line), flush=True)
+    w.eng.close()
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def main():
+    args = parse()
+    if args.impl == "reference":
+        run_reference(args)
+    else:
+        run_ours(args)
+
+
+if __name__ == "__main__":
+    main()

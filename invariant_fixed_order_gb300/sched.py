@@ -199,7 +199,7 @@ class FuzzConfig:
 
 
 def fuzz_continuous(runner: Runner, requests: list, n_decode: int, rng: np.random.Generator,
-                    cfg: FuzzConfig, teacher: dict | None = None):
+                    cfg: FuzzConfig, teacher: dict | None = None, all_prompt_logits: bool = True):
     """A randomised continuous-batching run.  Requests arrive at random steps,
     prefill in random chunks (within the token budget, co-scheduled with the
     decodes of running requests), may be evicted (pages freed) and readmitted
@@ -245,7 +245,8 @@ def fuzz_continuous(runner: Runner, requests: list, n_decode: int, rng: np.rando
             n = min(remaining, chunk, budget)
             if n <= 0:
                 continue
-            first_prefill = not produced_prompt[r.rid] and r.n_cached == 0 and not r.generated
+            first_prefill = (all_prompt_logits and not produced_prompt[r.rid] and r.n_cached == 0
+                             and not r.generated)
             items.append(StepItem(r, n, "all" if first_prefill else "last"))
             budget -= n
         if not items:

@@ -1,0 +1,304 @@
+"""Forward-step tests through bi_forward_step:
+
+* tiny single layer + LM head: oracle parity of every prompt position, and
+  bitwise invariance over all 1500 splits of 8 requests into batches of 1, 2,
+  4 and 8 (random in-batch order), prefill logits and decode logits;
+* chunked prefill: any chunking of a prompt gives the same bits;
+* the 8B-shaped layer: every request's layer output and logits bit-identical
+  to its bs=1 run over random batch compositions of every size 1..64, oracle
+  parity on a sample, and the batch-variant mode showing differences;
+* a mixed continuous-batching fuzz (chunked prefill co-scheduled with
+  decodes, arrival order, preemption, evict/readmit) on the 8B-shaped layer.
+"""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+from invariant_fixed_order_gb300 import synth
+from invariant_fixed_order_gb300.config import LLAMA3_8B_1L, TINY
+from tests.helpers import assert_logits_close, f32
+
+pytestmark = pytest.mark.gpu
+
+
+@pytest.fixture(scope="module")
+def mods():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from invariant_fixed_order_gb300 import bi, sched
+    from invariant_fixed_order_gb300.engine import Engine
+    return bi, sched, Engine
+
+
+# ---------------------------------------------------------------------------
+# tiny model
+# ---------------------------------------------------------------------------
+
+@pytest.fixture(scope="module")
+def tiny(mods):
+    bi, sched, Engine = mods
+    eng = Engine(TINY, num_pages=1024, max_pages=24, max_T=8 * 260, max_B=8, max_R=8 * 260, keep_logical=True)
+    lens = synth.uniform_ints(8, 1, 256, 42 + 0)
+    prompts = [synth.token_ids(int(n), TINY.V, 500 + i) for i, n in enumerate(lens)]
+    yield eng, prompts
+    eng.close()
+
+
+def run_block(sched, runner, prompts, rids, n_decode, rng=None, mode=None):
+    """Prefill the block's prompts in one ragged step (all-position logits), then
+    n_decode co-batched greedy decode steps.  Returns {rid: [positions, V]}."""
+    reqs = [sched.Request(rid, prompts[rid]) for rid in rids]
+    order = list(range(len(reqs))) if rng is None else list(rng.permutation(len(reqs)))
+    out = {r.rid: [] for r in reqs}
+    items = [sched.StepItem(reqs[i], len(reqs[i].prompt), "all") for i in order]
+    logits, tokens, sl = runner.step(items, mode=mode)
+    for it, s in zip(items, sl):
+        out[it.req.rid].append(logits[s])
+        it.req.generated.append(int(tokens[s][-1].item()))
+    for _ in range(n_decode):
+        order = list(range(len(reqs))) if rng is None else list(rng.permutation(len(reqs)))
+        items = [sched.StepItem(reqs[i], 1, "last") for i in order]
+        logits, tokens, sl = runner.step(items, mode=mode)
+        for it, s in zip(items, sl):
+            out[it.req.rid].append(logits[s])
+            it.req.generated.append(int(tokens[s][0].item()))
+    for r in reqs:
+        runner.evict(r)
+    return {rid: torch.cat(v) for rid, v in out.items()}
+
+
+def test_tiny_oracle_parity(mods, tiny):
+    bi, sched, _ = mods
+    eng, prompts = tiny
+    runner = sched.Runner(eng)
+    dims = oracle.Dims(TINY.d, TINY.H, TINY.Hkv, TINY.Dh, TINY.F, TINY.eps, TINY.rope_theta)
+    w = {k: f32(v) for k, v in eng.logical[0].items()}
+    head = {k: f32(v) for k, v in eng.head.items()}
+    got = run_block(sched, runner, prompts, list(range(8)), 0)
+    eng.check()
+    empty = [np.zeros((1, TINY.Hkv, TINY.Dh), np.float32)]
+    for rid, p in enumerate(prompts):
+        x = oracle.embed(head["embed"], p)
+        x_out, _, _, _ = oracle.layer_forward(dims, w, [len(p)], [0], empty, empty, x)
+        ref, ref_tok = oracle.lm_head(dims, head["gamma_final"], head["w_lm"], x_out, np.arange(len(p)))
+        assert_logits_close(got[rid].cpu().numpy(), ref)
+
+
+def test_tiny_all_partitions_bitwise(mods, tiny):
+    """Every split of the 8 requests into batches of sizes 1/2/4/8, random order inside each batch."""
+    bi, sched, _ = mods
+    eng, prompts = tiny
+    runner = sched.Runner(eng)
+    n_decode = 2
+    solo = {rid: run_block(sched, runner, prompts, [rid], n_decode)[rid] for rid in range(8)}
+    rng = np.random.default_rng(1000)
+    parts = list(sched.set_partitions_with_sizes(list(range(8)), {1, 2, 4, 8}))
+    assert len(parts) == 1500
+    ref = torch.cat([solo[r] for r in range(8)])
+    n_checked = 0
+    for part in parts:
+        got = {}
+        for block in part:
+            got.update(run_block(sched, runner, prompts, block, n_decode, rng=rng))
+        cat = torch.cat([got[r] for r in range(8)])
+        if not sched.bitwise_equal(cat, ref):
+            bad = [r for r in range(8) if not sched.bitwise_equal(got[r], solo[r])]
+            pytest.fail(f"partition {part}: requests {bad} differ from their solo run: "
+                        f"{[sched.diff_report(got[r], solo[r]) for r in bad]}")
+        n_checked += 1
+    eng.check()
+    assert n_checked == 1500
+
+
+def test_tiny_prefill_chunking_bitwise(mods, tiny):
+    bi, sched, _ = mods
+    eng, prompts = tiny
+    runner = sched.Runner(eng)
+    rid = int(np.argmax([len(p) for p in prompts]))
+    p = prompts[rid]
+    whole = run_block(sched, runner, prompts, [rid], 3)[rid]
+    rng = np.random.default_rng(7)
+    for trial in range(5):
+        cuts = sorted(set(int(c) for c in rng.integers(1, len(p), size=trial + 1)))
+        chunks = np.diff([0] + cuts + [len(p)]).tolist()
+        req = sched.Request(rid, p)
+        rows = []
+        for n in chunks:
+            logits, tokens, sl = runner.step([sched.StepItem(req, n, "all")])
+            rows.append(logits[sl[0]])
+        req.generated.append(int(tokens[sl[0]][-1].item()))
+        for _ in range(3):
+            logits, tokens, sl = runner.step([sched.StepItem(req, 1, "last")])
+            rows.append(logits[sl[0]])
+            req.generated.append(int(tokens[sl[0]][0].item()))
+        runner.evict(req)
+        assert sched.bitwise_equal(torch.cat(rows), whole), chunks
+
+
+# ---------------------------------------------------------------------------
+# 8B-shaped single layer (decode steps over random compositions)
+# ---------------------------------------------------------------------------
+
+class DecodeLayerCase:
+    """B requests with synthetic KV history (N(0,1)), contexts U[128, 8192]."""
+
+    def __init__(self, Engine, n_req=64, seed=43):
+        cfg = LLAMA3_8B_1L
+        self.cfg = cfg
+        self.ctx = synth.uniform_ints(n_req, 128, 8192, seed)
+        self.ids = synth.token_ids(n_req, cfg.V, seed + 1)
+        self.max_pages = 8192 // 16 + 1
+        pages = int(sum((int(s) + 15) // 16 for s in self.ctx))
+        self.eng = Engine(cfg, num_pages=pages + 64, max_pages=self.max_pages, max_T=n_req, max_B=n_req,
+                          max_R=n_req, keep_logical=True)
+        self.table = np.zeros((n_req, self.max_pages), np.int32)
+        self.hist = []
+        for i, s in enumerate(self.ctx):
+            pg = self.eng.pool.alloc((int(s) + 15) // 16)
+            self.table[i, :len(pg)] = pg
+            k, v = synth.kv_history(int(s) - 1, cfg.Hkv, cfg.Dh, 7919 * seed + i, device="cuda")
+            pos = np.arange(int(s) - 1)
+            pt = torch.from_numpy(self.table[i, pos // 16].astype(np.int64)).cuda()
+            sl = torch.from_numpy((pos % 16).astype(np.int64)).cuda()
+            self.eng.k[0][pt, :, sl, :] = k
+            self.eng.v[0][pt, :, sl, :] = v
+            self.hist.append((k, v))
+        self.d_table = torch.from_numpy(self.table).cuda()
+        self.d_ids = torch.from_numpy(self.ids).cuda()
+
+    def step(self, rows, mode):
+        rows = list(rows)
+        idx = torch.tensor(rows, device="cuda")
+        logits, tokens, hidden = self.eng.step([1] * len(rows), [int(self.ctx[r]) - 1 for r in rows],
+                                               self.d_ids[idx].contiguous(), self.d_table[idx].contiguous(),
+                                               list(range(len(rows))), mode=mode, want_hidden=True)
+        return logits, hidden
+
+
+@pytest.fixture(scope="module")
+def layer8b(mods):
+    bi, sched, Engine = mods
+    case = DecodeLayerCase(Engine)
+    yield case
+    case.eng.close()
+
+
+def test_8b_layer_compositions_bitwise(mods, layer8b):
+    """Every batch size 1..64, 200 random compositions each: each request's layer
+    output and logits are bit-identical to its bs=1 run."""
+    bi, sched, _ = mods
+    case = layer8b
+    n = len(case.ctx)
+    solo_l, solo_h = [], []
+    for r in range(n):
+        l, h = case.step([r], bi.INVARIANT)
+        solo_l.append(l[0].clone())
+        solo_h.append(h[0].clone())
+    solo_l = torch.stack(solo_l)
+    solo_h = torch.stack(solo_h)
+    rng = np.random.default_rng(1001)
+    bad = 0
+    for b in range(1, n + 1):
+        for _ in range(200):
+            rows = rng.choice(n, size=b, replace=False)
+            l, h = case.step(rows, bi.INVARIANT)
+            r = torch.from_numpy(rows).cuda()
+            if not (sched.bitwise_equal(l, solo_l[r]) and sched.bitwise_equal(h, solo_h[r])):
+                bad += 1
+    case.eng.check()
+    assert bad == 0, f"{bad} compositions differ from bs=1"
+
+
+def test_8b_layer_oracle_parity(mods, layer8b):
+    bi, sched, _ = mods
+    case = layer8b
+    cfg = case.cfg
+    dims = oracle.Dims(cfg.d, cfg.H, cfg.Hkv, cfg.Dh, cfg.F, cfg.eps, cfg.rope_theta)
+    w = {k: f32(v) for k, v in case.eng.logical[0].items()}
+    gamma_final, w_lm = f32(case.eng.head["gamma_final"]), f32(case.eng.head["w_lm"])
+    E = case.eng.head["embed"]
+    rows = [int(np.argmin(case.ctx)), 3, 17]
+    logits, hidden = case.step(rows, bi.INVARIANT)
+    for j, r in enumerate(rows):
+        k, v = case.hist[r]
+        x = f32(E[int(case.ids[r])])[None]
+        x_out, attn, _, _ = oracle.layer_forward(dims, w, [1], [int(case.ctx[r]) - 1], [f32(k)], [f32(v)], x)
+        ref_logits, ref_tok = oracle.lm_head(dims, gamma_final, w_lm, x_out, [0])
+        assert_logits_close(logits[j:j + 1].cpu().numpy(), ref_logits)
+        # the layer output (bf16 residual stream) within a few bf16 ulps
+        got_h = f32(hidden[j])
+        assert np.max(np.abs(got_h - x_out[0])) <= 4 * 2.0 ** -8 * (np.max(np.abs(x_out[0])) + 1)
+
+
+def test_8b_layer_variant_mode_negative_control(mods, layer8b):
+    """Variant mode must show at least one bit difference against bs=1 somewhere,
+    while staying within the parity tolerance."""
+    bi, sched, _ = mods
+    case = layer8b
+    n = len(case.ctx)
+    solo = [case.step([r], bi.VARIANT)[0][0].clone() for r in range(8)]
+    rng = np.random.default_rng(1002)
+    diffs = 0
+    for b in (2, 8, 16, 32, 64):
+        rows = np.concatenate([np.arange(8), rng.choice(np.arange(8, n), size=max(b - 8, 0), replace=False)])[:b]
+        l, _ = case.step(rows, bi.VARIANT)
+        for j, r in enumerate(rows[:8]):
+            if r < 8 and not sched.bitwise_equal(l[j], solo[r]):
+                diffs += 1
+                ref = solo[r].cpu().numpy()
+                assert np.max(np.abs(l[j].cpu().numpy() - ref)) <= 2e-2 * np.max(np.abs(ref))
+    assert diffs > 0, "batch-variant mode never differed: the harness would have no teeth"
+
+
+# ---------------------------------------------------------------------------
+# mixed continuous batching on the 8B-shaped layer
+# ---------------------------------------------------------------------------
+
+def test_8b_continuous_batching_fuzz(mods):
+    """Chunked prefill (256-2048) co-scheduled with decode requests, random
+    arrival order, preemption and evict/readmit: every produced logits row
+    equals the solo run bit for bit."""
+    bi, sched, Engine = mods
+    cfg = LLAMA3_8B_1L
+    rng = np.random.default_rng(1003)
+    long_lens = rng.integers(512, 12000, 3)
+    short_lens = rng.integers(256, 2048, 3)
+    lens = [int(x) for x in np.concatenate([long_lens, short_lens])]
+    prompts = [synth.token_ids(n, cfg.V, 900 + i) for i, n in enumerate(lens)]
+    n_decode = 4
+    max_pages = (max(lens) + n_decode + 15) // 16 + 1
+    eng = Engine(cfg, num_pages=sum(lens) // 16 + 64 * len(lens), max_pages=max_pages,
+                 max_T=max(max(lens), 4096) + 64, max_B=16, max_R=16)
+    runner = sched.Runner(eng)
+    solo = {}
+    teacher = {}
+    for rid, p in enumerate(prompts):
+        req = sched.Request(rid, p)
+        # solo: the whole prompt in one prefill, then greedy decode, alone
+        out = {}
+        logits, tokens, sl = runner.step([sched.StepItem(req, len(p), "last")])
+        out[len(p) - 1] = logits[sl[0]][0].clone()
+        for _ in range(n_decode):
+            req.generated.append(int(tokens[sl[0]][-1].item()))
+            if len(req.generated) > n_decode - 1:
+                break
+            logits, tokens, sl = runner.step([sched.StepItem(req, 1, "last")])
+            out[req.n_cached - 1] = logits[sl[0]][0].clone()
+        teacher[rid] = list(req.generated)
+        solo[rid] = out
+        runner.evict(req)
+    eng.check()
+    fz = sched.FuzzConfig(token_budget=4096, chunk_min=256, chunk_max=2048, p_evict=0.15, readmit_delay=(1, 3),
+                          arrival_span=4)
+    for trial in range(6):
+        reqs = [sched.Request(rid, p) for rid, p in enumerate(prompts)]
+        got = sched.fuzz_continuous(runner, reqs, n_decode, np.random.default_rng(2000 + trial), fz,
+                                    teacher=teacher, all_prompt_logits=False)
+        eng.check()
+        for rid in range(len(prompts)):
+            for pos, row in solo[rid].items():
+                assert pos in got[rid], (trial, rid, pos, sorted(got[rid]))
+                assert sched.bitwise_equal(got[rid][pos], row), (trial, rid, pos,
+                                                                  sched.diff_report(got[rid][pos], row))
+    eng.close()
