@@ -9,7 +9,7 @@
  * in one fixed order with split points that depend on the request alone:
  *   - RMSNorm: one warp per row, lane-serial over 16-byte chunks, then a fixed
  *     xor-butterfly;
- *   - GEMM: one tcgen05 MMA instruction shape (128x64x16, bf16 in, fp32
+ *   - GEMM: one tcgen05 MMA instruction shape (128x128x16, bf16 in, fp32
  *     accumulate in TMEM), one K tile (64), K loop in ascending order, no
  *     split-K, whatever M is;
  *   - attention: keys cut into chunks of BI_KV_CHUNK positions aligned to key 0
@@ -79,7 +79,7 @@ typedef enum {
 #define BI_KV_CHUNK 256      /* attention key chunk (positions) */
 #define BI_PAGE 16           /* KV page (positions) */
 #define BI_GEMM_BLOCK_M 128  /* MMA M */
-#define BI_GEMM_UMMA_N 64    /* MMA N */
+#define BI_GEMM_UMMA_N 128  /* MMA N */
 #define BI_GEMM_BLOCK_K 64   /* K tile */
 #define BI_SWIGLU_GROUP 32   /* gate/up interleave group (rows) */
 
@@ -123,11 +123,12 @@ bi_status bi_rmsnorm(const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y,
  * nn.Linear layout); C: DEVICE [M, N] (or [M, N/2] for BI_EP_SWIGLU) in c_dtype
  * (BI_EP_RESIDUAL and BI_EP_SWIGLU need BI_BF16); residual: DEVICE [M, N] bf16
  * for BI_EP_RESIDUAL, else NULL.
- * BI_INVARIANT: one tile configuration for every M; each element's K sum runs
- * in ascending 64-wide K tiles through 16-deep MMAs into one TMEM accumulator.
+ * BI_INVARIANT: every element's K sum, for every M, runs in ascending 64-wide K
+ * tiles through 16-deep MMAs (M=128, N=128) into one TMEM accumulator; only
+ * data movement (tile width, TMA box, ring depth) may follow M.
  * BI_VARIANT: when the output has fewer tiles than SMs, K is split over CTAs
  * into an fp32 workspace and the partials are added in split order.
- * Requires K % 64 == 0, N % 64 == 0, M >= 0, 16-byte aligned pointers.
+ * Requires K % 64 == 0, N % 128 == 0, M >= 0, 16-byte aligned pointers.
  * ws: DEVICE scratch of at least bi_gemm_workspace_size(M, N, K, mode) bytes
  * (0 in invariant mode; may then be NULL). */
 size_t bi_gemm_workspace_size(int64_t M, int32_t N, int32_t K, bi_mode mode);

@@ -93,7 +93,7 @@ static bi_status check_gemm_args(const bi_bf16* A, const bi_bf16* W, void* C, bi
                                  bi_mode mode) {
     if (M < 0 || N <= 0 || K <= 0) return fail(BI_ERR_SHAPE, "bi_gemm: need M >= 0, N > 0, K > 0");
     if (K % BI_GEMM_BLOCK_K != 0 || N % BI_GEMM_UMMA_N != 0)
-        return fail(BI_ERR_SHAPE, "bi_gemm: need K % 64 == 0 and N % 64 == 0");
+        return fail(BI_ERR_SHAPE, "bi_gemm: need K % 64 == 0 and N % 128 == 0");
     if (M > 0x7fffffffLL) return fail(BI_ERR_SHAPE, "bi_gemm: M too large");
     if (mode != BI_INVARIANT && mode != BI_VARIANT) return fail(BI_ERR_INVALID, "bi_gemm: bad mode");
     if (c_dtype != BI_BF16 && c_dtype != BI_F32) return fail(BI_ERR_INVALID, "bi_gemm: bad dtype");
@@ -268,8 +268,10 @@ extern "C" bi_status bi_model_create(const bi_model_config* cfg, const bi_model_
     const bi_model_config& c = *cfg;
     if (c.d <= 0 || c.H <= 0 || c.Hkv <= 0 || c.Dh <= 0 || c.F <= 0 || c.V <= 0 || c.n_layers <= 0 || c.max_pos <= 0)
         return fail(BI_ERR_SHAPE, "bi_model_create: nonpositive dimension");
-    if (c.d % 64 || c.F % 32 || (2 * c.F) % 64 || c.V % 64 || ((c.H + 2 * c.Hkv) * c.Dh) % 64 || (c.H * c.Dh) % 64)
-        return fail(BI_ERR_SHAPE, "bi_model_create: GEMM dimensions must be multiples of 64");
+    constexpr int n_mult = BI_GEMM_UMMA_N;
+    if (c.d % n_mult || c.F % 64 || c.V % n_mult || ((c.H + 2 * c.Hkv) * c.Dh) % n_mult || (c.H * c.Dh) % 64 ||
+        c.F % 64)
+        return fail(BI_ERR_SHAPE, "bi_model_create: GEMM widths must be multiples of 128 (K multiples of 64)");
     if (!attention_supported(c.H, c.Hkv, c.Dh)) return fail(BI_ERR_UNSUPPORTED, "bi_model_create: attention shape");
     if (!w->embed || !w->gamma_final || !w->w_lm || !w->gamma_attn || !w->w_qkv || !w->w_o || !w->gamma_ffn ||
         !w->w_gu || !w->w_down)

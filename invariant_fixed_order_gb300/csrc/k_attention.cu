@@ -22,12 +22,14 @@ namespace bi {
 
 constexpr int kAttnThreads = 128;
 constexpr int kMaxChunkPages = BI_KV_CHUNK / BI_PAGE + 1;  // a variant piece may straddle one more page
+constexpr int kSub = 64;                                   // keys per staged sub-chunk
+constexpr int kRing = 4;                                   // staged sub-chunks in flight
 
 template <int G, int DH>
 struct AttnSmem {
-    uint16_t v[BI_KV_CHUNK][DH];  // staged V rows of the chunk
+    uint16_t ring[kRing][kSub][DH];  // K or V rows of one sub-chunk per stage
     float q[G][DH];
-    float p[G][BI_KV_CHUNK];      // scores, then exp(score - m)
+    float p[G][BI_KV_CHUNK];         // scores, then exp(score - m)
     float m[G];
     float l[G];
     int32_t pages[kMaxChunkPages];
@@ -37,8 +39,7 @@ template <int G, int DH>
 struct AttnShape {
     static constexpr int kSlots = G * DH / 2;  // (head, dim pair) outputs
     static constexpr int kSlotsPerThread = (kSlots + kAttnThreads - 1) / kAttnThreads;
-    static constexpr int kDimsPerLane = DH / 8;  // 8 lanes per key
-    static constexpr int kVecPerLane = kDimsPerLane / 8;
+    static constexpr int kPieces = DH / 64;    // 16-byte pieces per lane per key (8 lanes per key)
 };
 
 struct Entry {
@@ -94,10 +95,14 @@ __device__ __forceinline__ void load_q(AttnSmem<G, DH>& sm, const uint16_t* q, i
 // fp32 queries sit in sm.q.  On return sm.m / sm.l hold each head's max score
 // and sum of exp(score - max); o[i][0..1] holds the thread's output slot i
 // (head = slot / (DH/2), dims 2*(slot % (DH/2)) + {0, 1}).
-//   score_j = (q . k_j) * scale: each of 8 lanes adds q[d] k_j[d] over its DH/8
-//             consecutive dims in ascending order (fused multiply-add), then
-//             an xor-butterfly over the 8 lanes (4, 2, 1);
-//   l = sum_j exp(score_j - m), o = sum_j exp(score_j - m) v_j, serial in j.
+//   score_j = (q . k_j) * scale: lane s (of the 8 lanes of key j) adds
+//             q[d] k_j[d] with fused multiply-adds over d = 64u + 8s .. 64u +
+//             8s + 7 for u = 0, 1, ... in that order, then the 8 lane sums meet
+//             in an xor-butterfly (4, 2, 1);
+//   m = max_j score_j;  l = sum_j exp(score_j - m), o = sum_j exp(score_j - m)
+//             v_j, both serial in j.
+// K and V rows stream through a ring of kRing shared-memory stages of kSub
+// keys each (cp.async), K sub-chunks first, then V sub-chunks.
 template <int G, int DH>
 __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH>& sm, const uint16_t* __restrict__ kc,
                                               const uint16_t* __restrict__ vc, const int32_t* page_row,
@@ -105,6 +110,7 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH>& sm, const uint16_
                                               int32_t max_pages, int32_t num_pages, int32_t* status,
                                               float (&o)[AttnShape<G, DH>::kSlotsPerThread][2]) {
     using S = AttnShape<G, DH>;
+    constexpr int kVecPerRow = DH / 8;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
     const int32_t lp0 = k0 / BI_PAGE;
     const int32_t np = (k0 + n - 1) / BI_PAGE - lp0 + 1;
@@ -119,102 +125,132 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH>& sm, const uint16_
     }
     __syncthreads();
 
-    // stage V rows of the chunk in shared memory while the scores are computed
-    constexpr int kVecPerRow = DH / 8;
-    for (int gi = tid; gi < n * kVecPerRow; gi += kAttnThreads) {
-        const int32_t jl = gi / kVecPerRow, part = gi % kVecPerRow;
-        const int32_t kp = k0 + jl;
-        const int32_t pg = sm.pages[kp / BI_PAGE - lp0];
-        const uint16_t* src = vc + ((static_cast<int64_t>(pg) * Hkv + g) * BI_PAGE + (kp & (BI_PAGE - 1))) * DH + part * 8;
-        cp_async16(&sm.v[jl][part * 8], src);
-    }
-    cp_async_commit();
-
-    // scores: warp w handles keys it*16 + w*4 + lane/8
-    {
-        const int kk = lane >> 3, sub = lane & 7;
-        float qr[G][S::kDimsPerLane];
-#pragma unroll
-        for (int h = 0; h < G; ++h)
-#pragma unroll
-            for (int d = 0; d < S::kDimsPerLane; ++d) qr[h][d] = sm.q[h][sub * S::kDimsPerLane + d];
-        const int iters = (n + 15) / 16;
-        for (int it = 0; it < iters; ++it) {
-            const int32_t jl = it * 16 + warp * 4 + kk;
-            const bool valid = jl < n;
-            uint4 kv[S::kVecPerLane];
-            if (valid) {
-                const int32_t kp = k0 + jl;
+    const int ns = (n + kSub - 1) / kSub;  // sub-chunks of K, then as many of V
+    auto issue = [&](int t) {
+        if (t < 2 * ns) {
+            const bool is_v = t >= ns;
+            const int sc = is_v ? t - ns : t;
+            const int32_t j0 = sc * kSub;
+            const int32_t nk = min(kSub, n - j0);
+            const uint16_t* base = is_v ? vc : kc;
+            uint16_t(*dst)[DH] = sm.ring[t % kRing];
+            for (int gi = tid; gi < nk * kVecPerRow; gi += kAttnThreads) {
+                const int32_t jl = gi / kVecPerRow, part = gi % kVecPerRow;
+                const int32_t kp = k0 + j0 + jl;
                 const int32_t pg = sm.pages[kp / BI_PAGE - lp0];
-                const uint16_t* kptr = kc + ((static_cast<int64_t>(pg) * Hkv + g) * BI_PAGE + (kp & (BI_PAGE - 1))) * DH +
-                                       sub * S::kDimsPerLane;
-#pragma unroll
-                for (int u = 0; u < S::kVecPerLane; ++u) kv[u] = ld_nc_v4(kptr + u * 8);
-            } else {
-#pragma unroll
-                for (int u = 0; u < S::kVecPerLane; ++u) kv[u] = make_uint4(0, 0, 0, 0);
-            }
-            float acc[G];
-#pragma unroll
-            for (int h = 0; h < G; ++h) acc[h] = 0.0f;
-#pragma unroll
-            for (int u = 0; u < S::kVecPerLane; ++u) {
-                const uint32_t w[4] = {kv[u].x, kv[u].y, kv[u].z, kv[u].w};
-#pragma unroll
-                for (int e = 0; e < 4; ++e) {
-                    const float k_lo = bf16_lo(w[e]), k_hi = bf16_hi(w[e]);
-#pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        acc[h] = __fmaf_rn(qr[h][u * 8 + 2 * e], k_lo, acc[h]);
-                        acc[h] = __fmaf_rn(qr[h][u * 8 + 2 * e + 1], k_hi, acc[h]);
-                    }
-                }
-            }
-#pragma unroll
-            for (int h = 0; h < G; ++h) {
-                acc[h] = __fadd_rn(acc[h], __shfl_xor_sync(0xffffffffu, acc[h], 4));
-                acc[h] = __fadd_rn(acc[h], __shfl_xor_sync(0xffffffffu, acc[h], 2));
-                acc[h] = __fadd_rn(acc[h], __shfl_xor_sync(0xffffffffu, acc[h], 1));
-            }
-            if (valid && sub == 0) {
-#pragma unroll
-                for (int h = 0; h < G; ++h) sm.p[h][jl] = __fmul_rn(acc[h], scale);
+                cp_async16(&dst[jl][part * 8],
+                           base + ((static_cast<int64_t>(pg) * Hkv + g) * BI_PAGE + (kp & (BI_PAGE - 1))) * DH + part * 8);
             }
         }
-    }
-    __syncthreads();
-
-    // per head: m = max score (exact, order-free), p = exp(score - m)
-    for (int h = warp; h < G; h += kAttnThreads / 32) {
-        float mx = -INFINITY;
-        for (int jl = lane; jl < n; jl += 32) mx = fmaxf(mx, sm.p[h][jl]);
+        cp_async_commit();  // possibly empty: keeps one group per sub-chunk slot
+    };
 #pragma unroll
-        for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-        for (int jl = lane; jl < n; jl += 32) sm.p[h][jl] = expf(__fsub_rn(sm.p[h][jl], mx));
-        if (lane == 0) sm.m[h] = mx;
+    for (int t = 0; t < kRing; ++t) issue(t);
+
+    const int kk = lane >> 3, sub = lane & 7;
+    float qr[G][S::kPieces * 8];
+#pragma unroll
+    for (int h = 0; h < G; ++h)
+#pragma unroll
+        for (int u = 0; u < S::kPieces; ++u)
+#pragma unroll
+            for (int d = 0; d < 8; ++d) qr[h][u * 8 + d] = sm.q[h][u * 64 + sub * 8 + d];
+
+    float oacc[S::kSlotsPerThread][2];
+    float lacc[S::kSlotsPerThread];
+#pragma unroll
+    for (int si = 0; si < S::kSlotsPerThread; ++si) {
+        oacc[si][0] = oacc[si][1] = 0.0f;
+        lacc[si] = 0.0f;
+    }
+
+    for (int t = 0; t < 2 * ns; ++t) {
+        asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 1) : "memory");
+        __syncthreads();
+        const uint16_t(*buf)[DH] = sm.ring[t % kRing];
+        if (t < ns) {
+            // scores of this sub-chunk's keys: warp w takes keys it*16 + w*4 + lane/8
+            const int32_t j0 = t * kSub;
+            const int32_t nk = min(kSub, n - j0);
+            for (int it = 0; it < (nk + 15) / 16; ++it) {
+                const int32_t jl = it * 16 + warp * 4 + kk;
+                const bool valid = jl < nk;
+                float acc[G];
+#pragma unroll
+                for (int h = 0; h < G; ++h) acc[h] = 0.0f;
+                if (valid) {
+#pragma unroll
+                    for (int u = 0; u < S::kPieces; ++u) {
+                        const uint4 kv = *reinterpret_cast<const uint4*>(&buf[jl][u * 64 + sub * 8]);
+                        const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float k_lo = bf16_lo(w[e]), k_hi = bf16_hi(w[e]);
+#pragma unroll
+                            for (int h = 0; h < G; ++h) {
+                                acc[h] = __fmaf_rn(qr[h][u * 8 + 2 * e], k_lo, acc[h]);
+                                acc[h] = __fmaf_rn(qr[h][u * 8 + 2 * e + 1], k_hi, acc[h]);
+                            }
+                        }
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+                    acc[h] = __fadd_rn(acc[h], __shfl_xor_sync(0xffffffffu, acc[h], 4));
+                    acc[h] = __fadd_rn(acc[h], __shfl_xor_sync(0xffffffffu, acc[h], 2));
+                    acc[h] = __fadd_rn(acc[h], __shfl_xor_sync(0xffffffffu, acc[h], 1));
+                }
+                if (valid && sub == 0) {
+#pragma unroll
+                    for (int h = 0; h < G; ++h) sm.p[h][j0 + jl] = __fmul_rn(acc[h], scale);
+                }
+            }
+            if (t == ns - 1) {
+                __syncthreads();
+                // per head: m = max score (exact, order-free), p = exp(score - m)
+                for (int h = warp; h < G; h += kAttnThreads / 32) {
+                    float mx = -INFINITY;
+                    for (int jl = lane; jl < n; jl += 32) mx = fmaxf(mx, sm.p[h][jl]);
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+                    for (int jl = lane; jl < n; jl += 32) sm.p[h][jl] = expf(__fsub_rn(sm.p[h][jl], mx));
+                    if (lane == 0) sm.m[h] = mx;
+                }
+            }
+        } else {
+            // o and l over this sub-chunk's keys, continuing the serial key order
+            const int32_t j0 = (t - ns) * kSub;
+            const int32_t nk = min(kSub, n - j0);
+#pragma unroll
+            for (int si = 0; si < S::kSlotsPerThread; ++si) {
+                const int slot = tid + si * kAttnThreads;
+                if (slot < S::kSlots) {
+                    const int h = slot / (DH / 2), dp = slot % (DH / 2);
+                    const float* ph = sm.p[h] + j0;
+                    float o0 = oacc[si][0], o1 = oacc[si][1], l = lacc[si];
+                    for (int jl = 0; jl < nk; ++jl) {
+                        const float pv = ph[jl];
+                        const uint32_t vv = *reinterpret_cast<const uint32_t*>(&buf[jl][2 * dp]);
+                        o0 = __fmaf_rn(pv, bf16_lo(vv), o0);
+                        o1 = __fmaf_rn(pv, bf16_hi(vv), o1);
+                        l = __fadd_rn(l, pv);
+                    }
+                    oacc[si][0] = o0;
+                    oacc[si][1] = o1;
+                    lacc[si] = l;
+                }
+            }
+        }
+        __syncthreads();
+        issue(t + kRing);
     }
     cp_async_wait_all();
-    __syncthreads();
-
-    // o and l: serial over the keys in ascending order
 #pragma unroll
     for (int si = 0; si < S::kSlotsPerThread; ++si) {
         const int slot = tid + si * kAttnThreads;
-        float o0 = 0.0f, o1 = 0.0f, l = 0.0f;
-        if (slot < S::kSlots) {
-            const int h = slot / (DH / 2), dp = slot % (DH / 2);
-            const float* ph = sm.p[h];
-            for (int jl = 0; jl < n; ++jl) {
-                const float pv = ph[jl];
-                const uint32_t vv = *reinterpret_cast<const uint32_t*>(&sm.v[jl][2 * dp]);
-                o0 = __fmaf_rn(pv, bf16_lo(vv), o0);
-                o1 = __fmaf_rn(pv, bf16_hi(vv), o1);
-                l = __fadd_rn(l, pv);
-            }
-            if (dp == 0) sm.l[h] = l;
-        }
-        o[si][0] = o0;
-        o[si][1] = o1;
+        if (slot < S::kSlots && slot % (DH / 2) == 0) sm.l[slot / (DH / 2)] = lacc[si];
+        o[si][0] = oacc[si][0];
+        o[si][1] = oacc[si][1];
     }
     __syncthreads();
 }

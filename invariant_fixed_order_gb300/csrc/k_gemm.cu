@@ -2,28 +2,41 @@
 //
 // "Batch invariance and reproducible inference", "2 · Cross-block
 // accumulation" and "3 · Kernel selection changing with shape": split-K and
-// M-dependent tile choice are what make a GEMM's per-element order follow the
-// batch.  Here every M runs the same configuration: 128-row M tiles, 64-column
-// N tiles, 64-deep K tiles loaded by TMA with 128-byte swizzle, and one
-// tcgen05.mma shape (M=128, N=64, K=16, bf16 in, fp32 accumulate in TMEM).  An
-// output element's K sum is always: K tiles in ascending order, within a tile
-// the four 16-deep MMAs in ascending order, accumulated in place in TMEM.
-// Nothing in that sequence depends on M, on the position of the row inside its
-// tile or on the other rows.
+// M-dependent kernel choice are what make a GEMM's per-element order follow
+// the batch.  Here every output element, for every M, is produced by the same
+// sequence: one tcgen05.mma shape (M=128, N=64, K=16; bf16 in, fp32
+// accumulated in TMEM), K tiles of 64 in ascending order, inside a K tile the
+// four 16-deep MMAs in ascending order, all into one accumulator.
 //
-// Warp roles (192 threads): warp 0 issues TMA loads into a ring of shared-
-// memory stages and owns the TMEM allocation; warp 1 issues the MMAs; warps
-// 2-5 read the accumulator back (warp w reads TMEM lanes 32*(w%4)..+31, i.e.
-// rows of the tile) and apply the fused epilogue.  Every wait is bounded: a
-// wait that runs out sets an abort flag and a device status code, every role
-// then winds down, in-flight copies and MMAs are drained, TMEM is freed.
+// What may follow M is only how that work is laid out, never the arithmetic
+// of an element:
+//   * the CTA tile is 128 x 64 (one MMA per 16-deep step) for small M, where
+//     the weights stream from HBM and many CTAs are wanted, and 128 x 256
+//     (four identical 64-wide MMAs per step, sharing A) for large M, where the
+//     tensor pipe must be fed from L2;
+//   * the TMA box of A covers the smallest power of two >= M rows (16..128);
+//     A stages are packed at that stride, so the MMA's rows past the box read
+//     neighbouring stages: those rows of the accumulator are never stored,
+//     and a row's result depends only on its own A row (pinned by the row-
+//     invariance tests);
+//   * ring depths.
+//
+// The kernel is persistent (one CTA per SM) with warp roles: warp 0 streams
+// weight tiles by TMA into a deep ring and owns the TMEM allocation, warp 2
+// streams activation tiles into a separate ring, warp 1 issues the MMAs
+// (one thread), warps 4-7 read the accumulator back (warp w: TMEM lanes
+// 32*(w%4)..+31) and run the fused epilogue.  The accumulator is double
+// buffered in TMEM so a tile's epilogue overlaps the next tile's main loop.
+// Every wait is bounded: a wait that runs out sets an abort flag and a device
+// status code, every role winds down, copies and MMAs in flight are drained
+// and TMEM is freed.
 //
 // BI_VARIANT splits K over CTAs into an fp32 workspace when the output has
-// fewer tiles than SMs (the fast path for small M) and adds the partials in
-// split order in a second kernel: deterministic run to run, but its order
-// depends on M.
+// fewer tiles than SMs and adds the partials in split order in a second
+// kernel: deterministic run to run, but its order depends on M.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <mutex>
 
 #include "internal.h"
@@ -32,17 +45,15 @@
 namespace bi {
 
 constexpr int kBM = BI_GEMM_BLOCK_M;   // 128
-constexpr int kBN = BI_GEMM_UMMA_N;    // 64
+constexpr int kUN = BI_GEMM_UMMA_N;    // N of one MMA
+constexpr int kEpi = 64;               // epilogue column chunk (a SwiGLU gate|up group pair)
 constexpr int kBK = BI_GEMM_BLOCK_K;   // 64
-constexpr int kStages = 8;
-constexpr int kGemmThreads = 192;
-constexpr int kABytes = kBM * kBK * 2;                // 16 KB
-constexpr int kBBytes = kBN * kBK * 2;                // 8 KB
-constexpr int kStageBytes = kABytes + kBBytes;        // 24 KB
-constexpr int kTmemCols = 64;                         // fp32 accumulator columns
-constexpr int kGroupM = 16;                           // M tiles per rasterisation band
-constexpr size_t kGemmSmem = 1024 + static_cast<size_t>(kStages) * kStageBytes + 256;
-constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBM, kBN);
+constexpr int kMaxStages = 16;
+constexpr int kGemmThreads = 256;
+constexpr int kAFull = kBM * kBK * 2;  // bytes the MMA reads for A per K tile (16 KB)
+constexpr int kGroupM = 16;            // M tiles per rasterisation band
+constexpr int kBarrierBytes = 1024;
+constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBM, kUN);
 
 struct GemmArgs {
     void* C;
@@ -53,8 +64,13 @@ struct GemmArgs {
     int32_t ep;
     int32_t kb_per_split;
     int32_t nkb_total;
-    int32_t m_tiles, n_tiles;
+    int32_t m_tiles, n_tiles, total_tiles;
     int64_t split_stride;  // elements between split partials (fp32), variant only
+    int32_t a_box_rows;    // rows of A per TMA box (16..128)
+    int32_t a_stride;      // bytes between A box slots (a_box_rows * 128)
+    int32_t a_region;      // bytes of the A region (slots + pad for the last window)
+    int32_t stages;        // ring stages
+    int32_t kps;           // 64-deep K tiles per stage
     int32_t* status;
 };
 
@@ -63,39 +79,119 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
     return __fmul_rn(s, u);
 }
 
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// Epilogue of one 64-column group (one MMA's worth) of one row: 64 fp32
+// accumulators in r, output columns n0 .. n0+63 of the GEMM.
+__device__ __forceinline__ void epilogue_group(const GemmArgs& args, int64_t row, int32_t n0, int32_t split,
+                                               const uint32_t (&r)[4][16]) {
+    if (args.ep == BI_EP_SWIGLU) {
+        // columns 0..31 gate, 32..63 up of the same 32 hidden units
+        uint32_t hv[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const int c0 = 2 * i, c1 = 2 * i + 1;
+            const float g0 = __uint_as_float(r[c0 / 16][c0 % 16]);
+            const float g1 = __uint_as_float(r[c1 / 16][c1 % 16]);
+            const float u0 = __uint_as_float(r[2 + c0 / 16][c0 % 16]);
+            const float u1 = __uint_as_float(r[2 + c1 / 16][c1 % 16]);
+            hv[i] = pack_bf16x2(silu_mul(g0, u0), silu_mul(g1, u1));
+        }
+        uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(args.C) + row * (args.N / 2) + n0 / 2);
+#pragma unroll
+        for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
+    } else if (args.c_f32) {
+        float* dst = reinterpret_cast<float*>(args.C) + split * args.split_stride + row * args.N + n0;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+#pragma unroll
+            for (int i = 0; i < 4; ++i)
+                reinterpret_cast<uint4*>(dst + c * 16)[i] =
+                    make_uint4(r[c][4 * i], r[c][4 * i + 1], r[c][4 * i + 2], r[c][4 * i + 3]);
+    } else {
+        uint16_t* dst = reinterpret_cast<uint16_t*>(args.C) + row * args.N + n0;
+        const uint16_t* res = args.ep == BI_EP_RESIDUAL ? args.residual + row * args.N + n0 : nullptr;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+            uint32_t rw[8];
+            if (res) {
+                const uint4 a = reinterpret_cast<const uint4*>(res + c * 16)[0];
+                const uint4 b = reinterpret_cast<const uint4*>(res + c * 16)[1];
+                rw[0] = a.x; rw[1] = a.y; rw[2] = a.z; rw[3] = a.w;
+                rw[4] = b.x; rw[5] = b.y; rw[6] = b.z; rw[7] = b.w;
+            }
+            uint32_t ov[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) {
+                float v0 = __uint_as_float(r[c][2 * i]);
+                float v1 = __uint_as_float(r[c][2 * i + 1]);
+                if (res) {
+                    v0 = __fadd_rn(v0, bf16_lo(rw[i]));
+                    v1 = __fadd_rn(v1, bf16_hi(rw[i]));
+                }
+                ov[i] = pack_bf16x2(v0, v1);
+            }
+            uint4* d4 = reinterpret_cast<uint4*>(dst + c * 16);
+            d4[0] = make_uint4(ov[0], ov[1], ov[2], ov[3]);
+            d4[1] = make_uint4(ov[4], ov[5], ov[6], ov[7]);
+        }
+    }
+}
+
+template <int BN>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, GemmArgs args) {
+    constexpr int kWBytes = BN * kBK * 2;
+    constexpr int kGroups = BN / kUN;   // MMAs per 16-deep step
+    constexpr int kChunks = BN / kEpi;  // epilogue chunks per tile
+    constexpr uint32_t kTmemCols = 2 * BN;  // two accumulator buffers
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-    uint64_t* full = reinterpret_cast<uint64_t*>(smem + kStages * kStageBytes);
-    uint64_t* empty = full + kStages;
-    uint64_t* accum = empty + kStages;
-    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(accum + 1);
+    uint8_t* sA = smem;
+    uint8_t* sW = smem + args.a_region;
+    uint64_t* full = reinterpret_cast<uint64_t*>(sW + args.stages * args.kps * kWBytes);
+    uint64_t* empty = full + kMaxStages;
+    uint64_t* acc_full = empty + kMaxStages;     // [2]
+    uint64_t* acc_empty = acc_full + 2;          // [2]
+    uint64_t* drain = acc_empty + 2;
+    uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
     volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_holder + 1);
 
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
-
-    // grouped rasterisation: bands of kGroupM M tiles sweep the N tiles together
-    const int32_t lin = blockIdx.x;
-    const int32_t band = kGroupM * args.n_tiles;
-    const int32_t first_m = (lin / band) * kGroupM;
-    const int32_t band_m = min(kGroupM, args.m_tiles - first_m);
-    const int32_t m_tile = first_m + (lin % band) % band_m;
-    const int32_t n_tile = (lin % band) / band_m;
     const int32_t split = blockIdx.y;
     const int32_t kb0 = split * args.kb_per_split;
     const int32_t nkb = min(args.kb_per_split, args.nkb_total - kb0);
+    const int S = args.stages, kps = args.kps;
+
+    auto tile_coords = [&](int32_t lin, int32_t& m_tile, int32_t& n_tile) {
+        const int32_t band = kGroupM * args.n_tiles;
+        const int32_t first_m = (lin / band) * kGroupM;
+        const int32_t band_m = min(kGroupM, args.m_tiles - first_m);
+        m_tile = first_m + (lin % band) % band_m;
+        n_tile = (lin % band) / band_m;
+    };
 
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tmA);
         ptx::prefetch_tmap(&tmW);
-        for (int s = 0; s < kStages; ++s) {
+        for (int s = 0; s < S; ++s) {
             ptx::mbar_init(&full[s], 1);
             ptx::mbar_init(&empty[s], 1);
         }
-        ptx::mbar_init(accum, 1);
+        for (int b = 0; b < 2; ++b) {
+            ptx::mbar_init(&acc_full[b], 1);
+            ptx::mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
+        }
+        ptx::mbar_init(drain, 1);
         *abort_flag = 0;
         ptx::fence_barrier_init();
+    }
+    if (warp >= 4) {
+        // the A region starts zeroed: rows no TMA box covers read as zero
+        uint4* z = reinterpret_cast<uint4*>(sA);
+        for (int i = threadIdx.x - 128; i < args.a_region / 16; i += 128) z[i] = make_uint4(0, 0, 0, 0);
         ptx::fence_proxy_async_smem();
     }
     if (warp == 0) {
@@ -110,37 +206,49 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---- TMA producer ----
+            // ---- TMA producer: per stage, kps K tiles of A and of W ----
             const uint64_t pol_w = ptx::policy_evict_first();  // weights stream through once
             const uint64_t pol_a = ptx::policy_evict_last();   // activations are re-read by every N tile
-            int32_t last_phase[kStages];
-            for (int s = 0; s < kStages; ++s) last_phase[s] = -1;
-            for (int32_t kb = 0; kb < nkb; ++kb) {
-                const int s = kb % kStages;
-                const uint32_t ph = static_cast<uint32_t>(kb / kStages) & 1u;
-                if (!ptx::mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag)) {
-                    if (!*abort_flag) report(args.status, BI_DEV_TIMEOUT_PRODUCER);
-                    *abort_flag = 1;
-                    break;
+            const uint32_t a_tx = static_cast<uint32_t>(args.a_box_rows) * kBK * 2;
+            uint32_t issued = 0;  // stages issued
+            int s = 0;            // stage and its phase, advanced incrementally
+            uint32_t ph = 0;
+            bool ok = true;
+            for (int32_t tile = blockIdx.x; tile < args.total_tiles && ok; tile += gridDim.x) {
+                int32_t m_tile, n_tile;
+                tile_coords(tile, m_tile, n_tile);
+                for (int32_t kb = 0; kb < nkb; kb += kps) {
+                    const int cnt = min(kps, nkb - kb);
+                    if (!ptx::mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag)) {
+                        if (!*abort_flag) report(args.status, BI_DEV_TIMEOUT_PRODUCER);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    ptx::mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(cnt) * (a_tx + kWBytes));
+                    for (int j = 0; j < cnt; ++j) {
+                        const int32_t kx = (kb0 + kb + j) * kBK;
+                        const int slot = s * kps + j;
+                        ptx::tma_load_2d(sA + slot * args.a_stride, &tmA, &full[s], kx, m_tile * kBM, pol_a);
+                        ptx::tma_load_2d(sW + slot * kWBytes, &tmW, &full[s], kx, n_tile * BN, pol_w);
+                    }
+                    ++issued;
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
-                uint8_t* sa = smem + s * kStageBytes;
-                ptx::mbar_arrive_expect_tx(&full[s], kStageBytes);
-                const int32_t kx = (kb0 + kb) * kBK;
-                ptx::tma_load_2d(sa, &tmA, &full[s], kx, m_tile * kBM, pol_a);
-                ptx::tma_load_2d(sa + kABytes, &tmW, &full[s], kx, n_tile * kBN, pol_w);
-                last_phase[s] = static_cast<int32_t>(ph);
             }
             // drain: every issued copy must land before the CTA may exit
-            for (int s = 0; s < kStages; ++s) {
-                if (last_phase[s] >= 0 &&
-                    !ptx::mbar_wait_bounded(&full[s], static_cast<uint32_t>(last_phase[s]), abort_flag)) {
-                    // the wait above also returns early on abort: wait once more without the abort exit
-                    const uint64_t t0 = globaltimer_ns();
-                    while (!ptx::mbar_try_wait(smem_u32(&full[s]), static_cast<uint32_t>(last_phase[s]))) {
-                        if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                            report(args.status, BI_DEV_TIMEOUT_DRAIN);
-                            break;
-                        }
+            const uint32_t first = issued > static_cast<uint32_t>(S) ? issued - S : 0u;
+            for (uint32_t q = first; q < issued; ++q) {
+                const int qs = static_cast<int>(q % S);
+                const uint32_t qph = (q / S) & 1u;
+                const uint64_t t0 = globaltimer_ns();
+                while (!ptx::mbar_try_wait(smem_u32(&full[qs]), qph)) {
+                    if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                        report(args.status, BI_DEV_TIMEOUT_DRAIN);
+                        break;
                     }
                 }
             }
@@ -148,101 +256,95 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     } else if (warp == 1) {
         if (lane == 0) {
             // ---- MMA issuer ----
-            for (int32_t kb = 0; kb < nkb; ++kb) {
-                const int s = kb % kStages;
-                const uint32_t ph = static_cast<uint32_t>(kb / kStages) & 1u;
-                if (!ptx::mbar_wait_bounded(&full[s], ph, abort_flag)) {
+            // Descriptors are built once; a slot or a 16-deep K step only moves
+            // the start-address field (16-byte units; shared memory < 256 KB so
+            // the 14-bit field never carries).
+            const uint64_t a_desc0 = ptx::smem_desc_sw128(smem_u32(sA));
+            const uint64_t w_desc0 = ptx::smem_desc_sw128(smem_u32(sW));
+            const uint32_t a_step = static_cast<uint32_t>(args.a_stride) >> 4;
+            constexpr uint32_t w_step = kWBytes >> 4;
+            constexpr uint32_t g_step = (kUN * kBK * 2) >> 4;
+            int s = 0;
+            uint32_t ph = 0;
+            int32_t i = 0;
+            bool ok = true;
+            for (int32_t tile = blockIdx.x; tile < args.total_tiles && ok; tile += gridDim.x, ++i) {
+                const int b = i & 1;
+                if (!ptx::mbar_wait_bounded(&acc_empty[b], ((static_cast<uint32_t>(i) >> 1) & 1u) ^ 1u, abort_flag)) {
                     if (!*abort_flag) report(args.status, BI_DEV_TIMEOUT_MMA);
                     *abort_flag = 1;
                     break;
                 }
                 ptx::tc_fence_after();
-                const uint32_t sa = smem_u32(smem + s * kStageBytes);
-                const uint32_t sb = sa + kABytes;
+                const uint32_t acc = tmem + static_cast<uint32_t>(b * BN);
+                for (int32_t kb = 0; kb < nkb; kb += kps) {
+                    const int cnt = min(kps, nkb - kb);
+                    if (!ptx::mbar_wait_bounded(&full[s], ph, abort_flag)) {
+                        if (!*abort_flag) report(args.status, BI_DEV_TIMEOUT_MMA);
+                        *abort_flag = 1;
+                        ok = false;
+                        break;
+                    }
+                    ptx::tc_fence_after();
+                    for (int j = 0; j < cnt; ++j) {
+                        const uint32_t slot = static_cast<uint32_t>(s * kps + j);
+                        const uint64_t ad = a_desc0 + slot * a_step;
+                        const uint64_t wd = w_desc0 + slot * w_step;
 #pragma unroll
-                for (int k = 0; k < kBK / 16; ++k) {
-                    const uint64_t ad = ptx::smem_desc_sw128(sa + k * 32);
-                    const uint64_t bd = ptx::smem_desc_sw128(sb + k * 32);
-                    ptx::tc_mma_f16(tmem, ad, bd, kIdesc, (kb > 0 || k > 0) ? 1u : 0u);
+                        for (int k = 0; k < kBK / 16; ++k) {
+#pragma unroll
+                            for (int g = 0; g < kGroups; ++g)
+                                ptx::tc_mma_f16(acc + g * kUN, ad + 2u * k, wd + g * g_step + 2u * k, kIdesc,
+                                                (kb + j > 0 || k > 0) ? 1u : 0u);
+                        }
+                    }
+                    ptx::tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
+                    if (++s == S) {
+                        s = 0;
+                        ph ^= 1u;
+                    }
                 }
-                ptx::tc_commit(&empty[s]);  // stage s is free once these MMAs have read it
+                if (ok) ptx::tc_commit(&acc_full[b]);
             }
-            ptx::tc_commit(accum);  // always: the epilogue and teardown wait on it
+            // no MMA may be in flight when TMEM is freed
+            ptx::tc_commit(drain);
+            const uint64_t t0 = globaltimer_ns();
+            while (!ptx::mbar_try_wait(smem_u32(drain), 0)) {
+                if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                    report(args.status, BI_DEV_TIMEOUT_DRAIN);
+                    break;
+                }
+            }
         }
-    } else {
-        // ---- epilogue: warps 2..5 ----
+    } else if (warp >= 4) {
+        // ---- epilogue: warps 4..7 ----
         const int q = warp & 3;
-        const int64_t row = static_cast<int64_t>(m_tile) * kBM + q * 32 + lane;
-        const bool ready = ptx::mbar_wait_bounded(accum, 0, abort_flag);
-        if (!ready && !*abort_flag) report(args.status, BI_DEV_TIMEOUT_EPILOGUE);
-        const bool go = __all_sync(0xffffffffu, ready && !*abort_flag && nkb > 0);
-        if (go) {
+        int32_t i = 0;
+        for (int32_t tile = blockIdx.x; tile < args.total_tiles; tile += gridDim.x, ++i) {
+            const int b = i & 1;
+            const bool ready = ptx::mbar_wait_bounded(&acc_full[b], (static_cast<uint32_t>(i) >> 1) & 1u, abort_flag);
+            if (!ready && !*abort_flag) report(args.status, BI_DEV_TIMEOUT_EPILOGUE);
+            if (!__all_sync(0xffffffffu, ready && !*abort_flag)) break;
             ptx::tc_fence_after();
-            uint32_t r[4][16];
-            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16);
+            int32_t m_tile, n_tile;
+            tile_coords(tile, m_tile, n_tile);
+            const int64_t row = static_cast<int64_t>(m_tile) * kBM + q * 32 + lane;
+            const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * BN);
+#pragma unroll 1
+            for (int j = 0; j < kChunks; ++j) {
+                uint32_t r[4][16];
 #pragma unroll
-            for (int c = 0; c < 4; ++c) ptx::tmem_ld16(taddr + c * 16, r[c]);
-            ptx::tmem_ld_wait();
-            if (row < args.M) {
-                const int32_t col0 = n_tile * kBN;
-                if (args.ep == BI_EP_SWIGLU) {
-                    // columns 0..31 gate, 32..63 up of the same 32 hidden units
-                    uint32_t hv[16];
-#pragma unroll
-                    for (int i = 0; i < 16; ++i) {
-                        const int c0 = 2 * i, c1 = 2 * i + 1;
-                        const float g0 = __uint_as_float(r[c0 / 16][c0 % 16]);
-                        const float g1 = __uint_as_float(r[c1 / 16][c1 % 16]);
-                        const float u0 = __uint_as_float(r[2 + c0 / 16][c0 % 16]);
-                        const float u1 = __uint_as_float(r[2 + c1 / 16][c1 % 16]);
-                        hv[i] = pack_bf16x2(silu_mul(g0, u0), silu_mul(g1, u1));
-                    }
-                    uint4* dst = reinterpret_cast<uint4*>(reinterpret_cast<uint16_t*>(args.C) +
-                                                          row * (args.N / 2) + col0 / 2);
-#pragma unroll
-                    for (int i = 0; i < 4; ++i) dst[i] = make_uint4(hv[4 * i], hv[4 * i + 1], hv[4 * i + 2], hv[4 * i + 3]);
-                } else if (args.c_f32) {
-                    float* dst = reinterpret_cast<float*>(args.C) + split * args.split_stride + row * args.N + col0;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c)
-#pragma unroll
-                        for (int i = 0; i < 4; ++i)
-                            reinterpret_cast<uint4*>(dst + c * 16)[i] =
-                                make_uint4(r[c][4 * i], r[c][4 * i + 1], r[c][4 * i + 2], r[c][4 * i + 3]);
-                } else {
-                    uint16_t* dst = reinterpret_cast<uint16_t*>(args.C) + row * args.N + col0;
-                    const uint16_t* res = args.ep == BI_EP_RESIDUAL ? args.residual + row * args.N + col0 : nullptr;
-#pragma unroll
-                    for (int c = 0; c < 4; ++c) {
-                        uint32_t rw[8];
-                        if (res) {
-                            const uint4 a = reinterpret_cast<const uint4*>(res + c * 16)[0];
-                            const uint4 b = reinterpret_cast<const uint4*>(res + c * 16)[1];
-                            rw[0] = a.x; rw[1] = a.y; rw[2] = a.z; rw[3] = a.w;
-                            rw[4] = b.x; rw[5] = b.y; rw[6] = b.z; rw[7] = b.w;
-                        }
-                        uint32_t ov[8];
-#pragma unroll
-                        for (int i = 0; i < 8; ++i) {
-                            float v0 = __uint_as_float(r[c][2 * i]);
-                            float v1 = __uint_as_float(r[c][2 * i + 1]);
-                            if (res) {
-                                v0 = __fadd_rn(v0, bf16_lo(rw[i]));
-                                v1 = __fadd_rn(v1, bf16_hi(rw[i]));
-                            }
-                            ov[i] = pack_bf16x2(v0, v1);
-                        }
-                        uint4* d4 = reinterpret_cast<uint4*>(dst + c * 16);
-                        d4[0] = make_uint4(ov[0], ov[1], ov[2], ov[3]);
-                        d4[1] = make_uint4(ov[4], ov[5], ov[6], ov[7]);
-                    }
-                }
+                for (int c = 0; c < 4; ++c) ptx::tmem_ld16(taddr + j * kEpi + c * 16, r[c]);
+                ptx::tmem_ld_wait();
+                if (row < args.M) epilogue_group(args, row, n_tile * BN + j * kEpi, split, r);
             }
+            ptx::tc_fence_before();
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&acc_empty[b]);
         }
     }
 
-    // teardown: all MMAs have completed once `accum` fired (or its wait gave
-    // up); warp 0 frees TMEM.
+    // teardown: MMAs drained by the issuer, copies drained by the producers
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 0) {
@@ -314,7 +416,7 @@ static bool make_kmajor_map(CUtensorMap* map, const void* base, uint64_t K, uint
 GemmPlan gemm_plan(int64_t M, int32_t N, int32_t K, bi_mode mode) {
     GemmPlan p{1};
     if (mode != BI_VARIANT || M <= 0) return p;
-    const int64_t tiles = ((M + kBM - 1) / kBM) * (N / kBN);
+    const int64_t tiles = ((M + kBM - 1) / kBM) * (N / kUN);
     const int sms = num_sms();
     if (tiles >= sms) return p;
     const int32_t nkb = K / kBK;
@@ -333,24 +435,67 @@ size_t gemm_ws_bytes(int64_t M, int32_t N, int32_t K, bi_mode mode) {
     return static_cast<size_t>(p.splits) * static_cast<size_t>(M) * N * sizeof(float) + 256;
 }
 
+namespace {
+
+struct Layout {
+    int32_t bn, a_box, a_stride, a_region, stages, kps;
+    size_t smem;
+};
+
+// Layout of one launch.  Only data movement depends on M here; the MMA
+// sequence of every output element is the same for all layouts.
+Layout choose_layout(int64_t M, int32_t N) {
+    Layout L{};
+    L.bn = (M > 2 * kBM && N % 256 == 0 && 256 % kUN == 0) ? 256 : kUN;
+    int32_t box = 16;
+    while (box < kBM && box < M) box *= 2;
+    if (L.bn == 256) box = kBM;
+    L.a_box = box;
+    L.a_stride = box * kBK * 2;
+    L.kps = L.bn == 256 ? 1 : 2;
+    const int32_t w_tile = L.bn * kBK * 2;
+    const int32_t pad = kAFull - L.a_stride;  // the last slot's 128-row window reaches this far past it
+    const int32_t budget = 212 * 1024 - pad;
+    int32_t stages = budget / (L.kps * (L.a_stride + w_tile));
+    stages = std::min(std::max(stages, 2), kMaxStages);
+    L.stages = stages;
+    L.a_region = stages * L.kps * L.a_stride + pad;
+    L.smem = 1024 + static_cast<size_t>(L.a_region) + static_cast<size_t>(stages) * L.kps * w_tile + kBarrierBytes;
+    return L;
+}
+
+template <int BN>
+cudaError_t launch_tiles(const CUtensorMap& tmA, const CUtensorMap& tmW, const GemmArgs& a, dim3 grid, size_t smem,
+                         cudaStream_t s) {
+    if constexpr (BN % kUN != 0) {
+        return cudaErrorInvalidValue;
+    } else {
+        static std::once_flag once;
+        static cudaError_t err = cudaSuccess;
+        std::call_once(once, [] {
+            err = cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       227 * 1024);
+        });
+        if (err != cudaSuccess) return err;
+        gemm_tc_kernel<BN><<<grid, kGemmThreads, smem, s>>>(tmA, tmW, a);
+        return cudaGetLastError();
+    }
+}
+
+}  // namespace
+
 bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype, const bi_bf16* residual,
                    bi_epilogue ep, int64_t M, int32_t N, int32_t K, bi_mode mode, void* ws, size_t ws_bytes,
                    int32_t* status, cudaStream_t s) {
     if (M == 0) return BI_OK;
-    static std::once_flag attr_once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(attr_once, [] {
-        attr_err = cudaFuncSetAttribute(gemm_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(kGemmSmem));
-    });
-    if (attr_err != cudaSuccess) return cuda_fail(attr_err, "cudaFuncSetAttribute(gemm)");
-
     const GemmPlan plan = gemm_plan(M, N, K, mode);
+    const Layout L = choose_layout(M, N);
+
     const int32_t nkb = K / kBK;
     const int32_t per = (nkb + plan.splits - 1) / plan.splits;
     CUtensorMap tmA, tmW;
-    if (!make_kmajor_map(&tmA, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), kBM) ||
-        !make_kmajor_map(&tmW, W, static_cast<uint64_t>(K), static_cast<uint64_t>(N), kBN))
+    if (!make_kmajor_map(&tmA, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), static_cast<uint32_t>(L.a_box)) ||
+        !make_kmajor_map(&tmW, W, static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint32_t>(L.bn)))
         return fail(BI_ERR_CUDA, "cuTensorMapEncodeTiled failed");
 
     GemmArgs a{};
@@ -360,7 +505,12 @@ bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype
     a.kb_per_split = per;
     a.nkb_total = nkb;
     a.m_tiles = static_cast<int32_t>((M + kBM - 1) / kBM);
-    a.n_tiles = N / kBN;
+    a.n_tiles = N / L.bn;
+    a.a_box_rows = L.a_box;
+    a.a_stride = L.a_stride;
+    a.a_region = L.a_region;
+    a.stages = L.stages;
+    a.kps = L.kps;
     a.status = status;
     if (plan.splits > 1) {
         if (ws == nullptr || ws_bytes < gemm_ws_bytes(M, N, K, mode))
@@ -379,9 +529,12 @@ bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype
     }
     const int64_t tiles = static_cast<int64_t>(a.m_tiles) * a.n_tiles;
     if (tiles > 0x7fffffffLL) return fail(BI_ERR_SHAPE, "bi_gemm: too many tiles");
-    dim3 grid(static_cast<unsigned>(tiles), plan.splits);
-    gemm_tc_kernel<<<grid, kGemmThreads, kGemmSmem, s>>>(tmA, tmW, a);
-    cudaError_t e = cudaGetLastError();
+    a.total_tiles = static_cast<int32_t>(tiles);
+    const int64_t ctas = std::min<int64_t>(tiles, std::max(1, num_sms() / plan.splits));
+    dim3 grid(static_cast<unsigned>(ctas), plan.splits);
+    cudaError_t e = L.bn == 256   ? launch_tiles<256>(tmA, tmW, a, grid, L.smem, s)
+                    : L.bn == 128 ? launch_tiles<128>(tmA, tmW, a, grid, L.smem, s)
+                                  : launch_tiles<64>(tmA, tmW, a, grid, L.smem, s);
     if (e != cudaSuccess) return cuda_fail(e, "gemm_tc_kernel launch");
     if (plan.splits > 1) {
         const int64_t n_out = ep == BI_EP_SWIGLU ? M * (N / 2) : M * N;

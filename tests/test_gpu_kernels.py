@@ -69,8 +69,8 @@ def test_rmsnorm_in_place(bi):
 # GEMM (tcgen05)
 # ---------------------------------------------------------------------------
 
-@pytest.mark.parametrize("M,N,K", [(1, 64, 64), (5, 128, 256), (128, 64, 4096), (129, 192, 1024),
-                                   (300, 64, 14336), (64, 512, 4096)])
+@pytest.mark.parametrize("M,N,K", [(1, 128, 64), (5, 128, 256), (128, 128, 4096), (129, 384, 1024),
+                                   (300, 256, 14336), (64, 512, 4096), (17, 640, 1984), (600, 768, 512)])
 def test_gemm_integer_valued_exact(bi, M, N, K):
     A = int_bf16((M, K), 100 + M)
     W = int_bf16((N, K), 200 + N)
@@ -161,7 +161,7 @@ def test_gemm_variant_mode_splits_k(bi):
 
 def test_gemm_rejects_bad_shapes(bi):
     A = torch.zeros(4, 100, dtype=torch.bfloat16, device="cuda")
-    W = torch.zeros(64, 100, dtype=torch.bfloat16, device="cuda")
+    W = torch.zeros(128, 100, dtype=torch.bfloat16, device="cuda")
     with pytest.raises(bi.BIError) as e:
         bi.gemm(A, W)
     assert e.value.status == bi.BI_ERR_SHAPE
