@@ -21,25 +21,27 @@
 namespace bi {
 
 constexpr int kAttnThreads = 128;
+constexpr int kWarps = kAttnThreads / 32;
 constexpr int kMaxChunkPages = BI_KV_CHUNK / BI_PAGE + 1;  // a variant piece may straddle one more page
 constexpr int kSub = 64;                                   // keys per staged sub-chunk
-constexpr int kRing = 4;                                   // staged sub-chunks in flight
-
-template <int G, int DH>
-struct AttnSmem {
-    uint16_t ring[kRing][kSub][DH];  // K or V rows of one sub-chunk per stage
-    float q[G][DH];
-    float p[G][BI_KV_CHUNK];         // scores, then exp(score - m)
-    float m[G];
-    float l[G];
-    int32_t pages[kMaxChunkPages];
-};
+constexpr int kRing = 3;                                   // staged sub-chunks in flight
 
 template <int G, int DH>
 struct AttnShape {
-    static constexpr int kSlots = G * DH / 2;  // (head, dim pair) outputs
-    static constexpr int kSlotsPerThread = (kSlots + kAttnThreads - 1) / kAttnThreads;
-    static constexpr int kPieces = DH / 64;    // 16-byte pieces per lane per key (8 lanes per key)
+    static_assert(G >= 1 && G <= 8, "a GQA group fills at most the 8 rows a0/a2 of an m16n8k16 tile");
+    static constexpr int kKSteps = DH / 16;           // 16-deep MMA steps over the head dim
+    static constexpr int kDimsPerWarp = DH / kWarps;  // PV: output dims per warp
+    static constexpr int kNB = kDimsPerWarp / 8;      // PV: 8-wide n-blocks per warp
+};
+
+template <int G, int DH>
+struct AttnSmem {
+    uint16_t ring[kRing][kSub][DH];  // K or V rows; 16-byte chunk c of row r sits at chunk c ^ (r & 7)
+    float p[G][BI_KV_CHUNK];         // scores, then exp(score - m)
+    float red[kWarps][G];            // per-warp partial sums of l
+    float m[G];
+    float l[G];
+    int32_t pages[kMaxChunkPages];
 };
 
 struct Entry {
@@ -83,24 +85,59 @@ __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait_all() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
 
-// Loads the G query heads of token t (bf16) into shared memory as fp32.
-template <int G, int DH>
-__device__ __forceinline__ void load_q(AttnSmem<G, DH>& sm, const uint16_t* q, int32_t t, int32_t H,
-                                       int32_t g) {
-    const uint16_t* src = q + (static_cast<int64_t>(t) * H + static_cast<int64_t>(g) * G) * DH;
-    for (int i = threadIdx.x; i < G * DH; i += kAttnThreads) sm.q[i / DH][i % DH] = bf16_to_f32(src[i]);
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
+    asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+                 : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
+                 : "r"(addr));
+}
+// d += A(16x16, rows 8..15 zero) * B(16x8), bf16 in, fp32 accumulate.
+__device__ __forceinline__ void mma_rows8(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
+    const uint32_t z = 0;
+    asm volatile(
+        "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
+        "{%0, %1, %2, %3};"
+        : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+        : "r"(a0), "r"(z), "r"(a2), "r"(z), "r"(b0), "r"(b1));
+}
+// Byte offset of (row, 16-byte chunk c) in a swizzled ring stage.
+template <int DH>
+__device__ __forceinline__ uint32_t ring_off(int row, int c) {
+    return static_cast<uint32_t>(row * DH * 2 + ((c ^ (row & 7)) << 4));
 }
 
-// Partial of keys [k0, k0 + n) (1 <= n <= BI_KV_CHUNK) for the G heads whose
-// fp32 queries sit in sm.q.  On return sm.m / sm.l hold each head's max score
-// and sum of exp(score - max); o[i][0..1] holds the thread's output slot i
-// (head = slot / (DH/2), dims 2*(slot % (DH/2)) + {0, 1}).
-//   score_j = (q . k_j) * scale: lane s (of the 8 lanes of key j) adds
-//             q[d] k_j[d] with fused multiply-adds over d = 64u + 8s .. 64u +
-//             8s + 7 for u = 0, 1, ... in that order, then the 8 lane sums meet
-//             in an xor-butterfly (4, 2, 1);
-//   m = max_j score_j;  l = sum_j exp(score_j - m), o = sum_j exp(score_j - m)
-//             v_j, both serial in j.
+// Query fragments of the GQA group: row h of the MMA's A operand is head h of
+// the group (rows >= G and 8..15 are zero); qa[ks] = {a0, a2} of 16-deep step ks.
+template <int G, int DH>
+__device__ __forceinline__ void load_q_frags(const uint16_t* q, int32_t t, int32_t H, int32_t g,
+                                             uint32_t (&qa)[DH / 16][2]) {
+    const int lane = threadIdx.x & 31, h = lane >> 2, c = 2 * (lane & 3);
+    const uint16_t* src = q + (static_cast<int64_t>(t) * H + static_cast<int64_t>(g) * G + h) * DH;
+#pragma unroll
+    for (int ks = 0; ks < DH / 16; ++ks) {
+        qa[ks][0] = h < G ? *reinterpret_cast<const uint32_t*>(src + ks * 16 + c) : 0u;
+        qa[ks][1] = h < G ? *reinterpret_cast<const uint32_t*>(src + ks * 16 + 8 + c) : 0u;
+    }
+}
+
+// Partial of keys [k0, k0 + n) (1 <= n <= BI_KV_CHUNK) for the G heads of
+// one GQA group.  On return sm.m / sm.l hold each head's max score and sum of
+// exp(score - max), and a thread with h = lane/4 < G holds in o[nb][0..1] the
+// unnormalised output of head h at dims 32w + 8nb + 2(lane%4) + {0,1} (w =
+// warp; DH/4 dims per warp).  The arithmetic, fixed for a given (n, G, DH):
+//   score_j = (q . k_j) * scale: q and k_j in bf16 multiplied on the tensor
+//             cores (m16n8k16, fp32 accumulate) over the head dim in 16-deep
+//             steps in ascending order, then one fp32 multiply by scale;
+//   m = max_j score_j;   p_j = exp(score_j - m);
+//   l = sum over the 4 warps in order of (xor-butterfly over the 32 lanes of
+//       (lane-serial sum of p_j over j = 32w + lane + 128i, i ascending));
+//   o = sum_j p_j v_j on the tensor cores: p_j split into bf16 hi = bf16(p_j)
+//       and lo = bf16(p_j - hi), for each 16-key step in ascending order the
+//       hi product then the lo product accumulated in fp32.
 // K and V rows stream through a ring of kRing shared-memory stages of kSub
 // keys each (cp.async), K sub-chunks first, then V sub-chunks.
 template <int G, int DH>
@@ -108,7 +145,8 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH>& sm, const uint16_
                                               const uint16_t* __restrict__ vc, const int32_t* page_row,
                                               int32_t g, int32_t Hkv, int32_t k0, int32_t n, float scale,
                                               int32_t max_pages, int32_t num_pages, int32_t* status,
-                                              float (&o)[AttnShape<G, DH>::kSlotsPerThread][2]) {
+                                              const uint32_t (&qa)[DH / 16][2],
+                                              float (&o)[AttnShape<G, DH>::kNB][2]) {
     using S = AttnShape<G, DH>;
     constexpr int kVecPerRow = DH / 8;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
@@ -126,20 +164,25 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH>& sm, const uint16_
     __syncthreads();
 
     const int ns = (n + kSub - 1) / kSub;  // sub-chunks of K, then as many of V
+    const int part = tid % kVecPerRow;     // this thread's 16-byte column of every row it copies
     auto issue = [&](int t) {
         if (t < 2 * ns) {
             const bool is_v = t >= ns;
-            const int sc = is_v ? t - ns : t;
-            const int32_t j0 = sc * kSub;
+            const int32_t j0 = (is_v ? t - ns : t) * kSub;
             const int32_t nk = min(kSub, n - j0);
-            const uint16_t* base = is_v ? vc : kc;
-            uint16_t(*dst)[DH] = sm.ring[t % kRing];
-            for (int gi = tid; gi < nk * kVecPerRow; gi += kAttnThreads) {
-                const int32_t jl = gi / kVecPerRow, part = gi % kVecPerRow;
+            const uint16_t* base = (is_v ? vc : kc) + static_cast<int64_t>(g) * BI_PAGE * DH + part * 8;
+            unsigned char* dst = reinterpret_cast<unsigned char*>(sm.ring[t % kRing]);
+            for (int jl = tid / kVecPerRow; jl < nk; jl += kAttnThreads / kVecPerRow) {
                 const int32_t kp = k0 + j0 + jl;
-                const int32_t pg = sm.pages[kp / BI_PAGE - lp0];
-                cp_async16(&dst[jl][part * 8],
-                           base + ((static_cast<int64_t>(pg) * Hkv + g) * BI_PAGE + (kp & (BI_PAGE - 1))) * DH + part * 8);
+                const int64_t pg = sm.pages[kp / BI_PAGE - lp0];
+                cp_async16(dst + ring_off<DH>(jl, part), base + (pg * Hkv * BI_PAGE + (kp & (BI_PAGE - 1))) * DH);
+            }
+            if (is_v) {
+                // V rows past the last key up to the 16-key step boundary are read by
+                // the MMA with p = 0: make them zero rather than stale
+                const int32_t pad_end = min(kSub, (nk + 15) & ~15);
+                for (int jl = nk + tid / kVecPerRow; jl < pad_end; jl += kAttnThreads / kVecPerRow)
+                    *reinterpret_cast<uint4*>(dst + ring_off<DH>(jl, part)) = make_uint4(0, 0, 0, 0);
             }
         }
         cp_async_commit();  // possibly empty: keeps one group per sub-chunk slot
@@ -147,97 +190,106 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH>& sm, const uint16_
 #pragma unroll
     for (int t = 0; t < kRing; ++t) issue(t);
 
-    const int kk = lane >> 3, sub = lane & 7;
-    float qr[G][S::kPieces * 8];
+    const int hrow = lane >> 2, cq = 2 * (lane & 3);
+    float oacc[S::kNB][4];
 #pragma unroll
-    for (int h = 0; h < G; ++h)
-#pragma unroll
-        for (int u = 0; u < S::kPieces; ++u)
-#pragma unroll
-            for (int d = 0; d < 8; ++d) qr[h][u * 8 + d] = sm.q[h][u * 64 + sub * 8 + d];
-
-    float oacc[S::kSlotsPerThread][2];
-    float lacc[S::kSlotsPerThread];
-#pragma unroll
-    for (int si = 0; si < S::kSlotsPerThread; ++si) {
-        oacc[si][0] = oacc[si][1] = 0.0f;
-        lacc[si] = 0.0f;
-    }
+    for (int nb = 0; nb < S::kNB; ++nb) oacc[nb][0] = oacc[nb][1] = oacc[nb][2] = oacc[nb][3] = 0.0f;
 
     for (int t = 0; t < 2 * ns; ++t) {
         asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 1) : "memory");
         __syncthreads();
-        const uint16_t(*buf)[DH] = sm.ring[t % kRing];
+        const uint32_t buf = smem_u32(sm.ring[t % kRing]);
         if (t < ns) {
-            // scores of this sub-chunk's keys: warp w takes keys it*16 + w*4 + lane/8
+            // scores: warp w takes keys 16w .. 16w+15 of the sub-chunk, 8 per MMA n-block
             const int32_t j0 = t * kSub;
             const int32_t nk = min(kSub, n - j0);
-            for (int it = 0; it < (nk + 15) / 16; ++it) {
-                const int32_t jl = it * 16 + warp * 4 + kk;
-                const bool valid = jl < nk;
-                float acc[G];
 #pragma unroll
-                for (int h = 0; h < G; ++h) acc[h] = 0.0f;
-                if (valid) {
+            for (int nb2 = 0; nb2 < 2; ++nb2) {
+                const int n0 = warp * 16 + nb2 * 8;
+                if (n0 >= nk) break;
+                float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
 #pragma unroll
-                    for (int u = 0; u < S::kPieces; ++u) {
-                        const uint4 kv = *reinterpret_cast<const uint4*>(&buf[jl][u * 64 + sub * 8]);
-                        const uint32_t w[4] = {kv.x, kv.y, kv.z, kv.w};
+                for (int ks = 0; ks < S::kKSteps; ks += 2) {
+                    uint32_t r[4];
+                    ldsm_x4(buf + ring_off<DH>(n0 + (lane & 7), 2 * ks + (lane >> 3)), r);
+                    mma_rows8(acc, qa[ks][0], qa[ks][1], r[0], r[1]);
+                    mma_rows8(acc, qa[ks + 1][0], qa[ks + 1][1], r[2], r[3]);
+                }
+                if (hrow < G) {
 #pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float k_lo = bf16_lo(w[e]), k_hi = bf16_hi(w[e]);
-#pragma unroll
-                            for (int h = 0; h < G; ++h) {
-                                acc[h] = __fmaf_rn(qr[h][u * 8 + 2 * e], k_lo, acc[h]);
-                                acc[h] = __fmaf_rn(qr[h][u * 8 + 2 * e + 1], k_hi, acc[h]);
-                            }
-                        }
+                    for (int c = 0; c < 2; ++c) {
+                        const int key = n0 + cq + c;
+                        if (key < nk) sm.p[hrow][j0 + key] = __fmul_rn(acc[c], scale);
                     }
-                }
-#pragma unroll
-                for (int h = 0; h < G; ++h) {
-                    acc[h] = __fadd_rn(acc[h], __shfl_xor_sync(0xffffffffu, acc[h], 4));
-                    acc[h] = __fadd_rn(acc[h], __shfl_xor_sync(0xffffffffu, acc[h], 2));
-                    acc[h] = __fadd_rn(acc[h], __shfl_xor_sync(0xffffffffu, acc[h], 1));
-                }
-                if (valid && sub == 0) {
-#pragma unroll
-                    for (int h = 0; h < G; ++h) sm.p[h][j0 + jl] = __fmul_rn(acc[h], scale);
                 }
             }
             if (t == ns - 1) {
                 __syncthreads();
-                // per head: m = max score (exact, order-free), p = exp(score - m)
-                for (int h = warp; h < G; h += kAttnThreads / 32) {
+                // m: exact max per head (order-free)
+                for (int h = warp; h < G; h += kWarps) {
                     float mx = -INFINITY;
-                    for (int jl = lane; jl < n; jl += 32) mx = fmaxf(mx, sm.p[h][jl]);
+                    for (int j = lane; j < n; j += 32) mx = fmaxf(mx, sm.p[h][j]);
 #pragma unroll
                     for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                    for (int jl = lane; jl < n; jl += 32) sm.p[h][jl] = expf(__fsub_rn(sm.p[h][jl], mx));
                     if (lane == 0) sm.m[h] = mx;
+                }
+                __syncthreads();
+                // p = exp(score - m) and the fixed-tree sum l
+                float ls[G];
+#pragma unroll
+                for (int h = 0; h < G; ++h) ls[h] = 0.0f;
+                for (int j = tid; j < n; j += kAttnThreads) {
+#pragma unroll
+                    for (int h = 0; h < G; ++h) {
+                        const float pv = expf(__fsub_rn(sm.p[h][j], sm.m[h]));
+                        sm.p[h][j] = pv;
+                        ls[h] = __fadd_rn(ls[h], pv);
+                    }
+                }
+#pragma unroll
+                for (int h = 0; h < G; ++h) {
+#pragma unroll
+                    for (int off = 16; off >= 1; off >>= 1)
+                        ls[h] = __fadd_rn(ls[h], __shfl_xor_sync(0xffffffffu, ls[h], off));
+                    if (lane == 0) sm.red[warp][h] = ls[h];
+                }
+                __syncthreads();
+                if (tid < G) {
+                    float l = sm.red[0][tid];
+#pragma unroll
+                    for (int w = 1; w < kWarps; ++w) l = __fadd_rn(l, sm.red[w][tid]);
+                    sm.l[tid] = l;
                 }
             }
         } else {
-            // o and l over this sub-chunk's keys, continuing the serial key order
+            // PV: warp w owns dims DH/4 * w .. ; 16-key steps in ascending order
             const int32_t j0 = (t - ns) * kSub;
             const int32_t nk = min(kSub, n - j0);
+            const int c0 = warp * S::kDimsPerWarp / 8;  // first 16-byte chunk of this warp's dims
+            for (int kk = 0; kk < nk; kk += 16) {
+                float pv[4];
 #pragma unroll
-            for (int si = 0; si < S::kSlotsPerThread; ++si) {
-                const int slot = tid + si * kAttnThreads;
-                if (slot < S::kSlots) {
-                    const int h = slot / (DH / 2), dp = slot % (DH / 2);
-                    const float* ph = sm.p[h] + j0;
-                    float o0 = oacc[si][0], o1 = oacc[si][1], l = lacc[si];
-                    for (int jl = 0; jl < nk; ++jl) {
-                        const float pv = ph[jl];
-                        const uint32_t vv = *reinterpret_cast<const uint32_t*>(&buf[jl][2 * dp]);
-                        o0 = __fmaf_rn(pv, bf16_lo(vv), o0);
-                        o1 = __fmaf_rn(pv, bf16_hi(vv), o1);
-                        l = __fadd_rn(l, pv);
-                    }
-                    oacc[si][0] = o0;
-                    oacc[si][1] = o1;
-                    lacc[si] = l;
+                for (int x = 0; x < 4; ++x) {
+                    const int key = kk + cq + (x & 1) + (x >> 1) * 8;
+                    pv[x] = (hrow < G && key < nk) ? sm.p[hrow][j0 + key] : 0.0f;
+                }
+                uint32_t hi[2], lo[2];
+#pragma unroll
+                for (int y = 0; y < 2; ++y) {
+                    const float h0 = __uint_as_float(static_cast<uint32_t>(f32_to_bf16(pv[2 * y])) << 16);
+                    const float h1 = __uint_as_float(static_cast<uint32_t>(f32_to_bf16(pv[2 * y + 1])) << 16);
+                    hi[y] = pack_bf16x2(h0, h1);
+                    lo[y] = pack_bf16x2(__fsub_rn(pv[2 * y], h0), __fsub_rn(pv[2 * y + 1], h1));
+                }
+#pragma unroll
+                for (int nb = 0; nb < S::kNB; nb += 2) {
+                    uint32_t r[4];
+                    const int i = lane >> 3;
+                    ldsm_x4_trans(buf + ring_off<DH>(kk + (i & 1) * 8 + (lane & 7), c0 + nb + (i >> 1)), r);
+                    mma_rows8(oacc[nb], hi[0], hi[1], r[0], r[1]);
+                    mma_rows8(oacc[nb], lo[0], lo[1], r[0], r[1]);
+                    mma_rows8(oacc[nb + 1], hi[0], hi[1], r[2], r[3]);
+                    mma_rows8(oacc[nb + 1], lo[0], lo[1], r[2], r[3]);
                 }
             }
         }
@@ -246,11 +298,9 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH>& sm, const uint16_
     }
     cp_async_wait_all();
 #pragma unroll
-    for (int si = 0; si < S::kSlotsPerThread; ++si) {
-        const int slot = tid + si * kAttnThreads;
-        if (slot < S::kSlots && slot % (DH / 2) == 0) sm.l[slot / (DH / 2)] = lacc[si];
-        o[si][0] = oacc[si][0];
-        o[si][1] = oacc[si][1];
+    for (int nb = 0; nb < S::kNB; ++nb) {
+        o[nb][0] = oacc[nb][0];
+        o[nb][1] = oacc[nb][1];
     }
     __syncthreads();
 }
@@ -304,21 +354,21 @@ decode_split_kernel(AttnGeom geo, EntryMap em, int32_t max_splits, int32_t chunk
     if (split >= count) return;
     const int32_t k0 = split * size;
     const int32_t n = min(size, s - k0);
-    load_q<G, DH>(sm, reinterpret_cast<const uint16_t*>(geo.q), en.t, geo.H, g);
-    __syncthreads();
-    float o[S::kSlotsPerThread][2];
+    uint32_t qa[DH / 16][2];
+    load_q_frags<G, DH>(reinterpret_cast<const uint16_t*>(geo.q), en.t, geo.H, g, qa);
+    float o[S::kNB][2];
     chunk_partial<G, DH>(sm, reinterpret_cast<const uint16_t*>(geo.kc), reinterpret_cast<const uint16_t*>(geo.vc),
                          geo.page_table + static_cast<int64_t>(en.r) * geo.max_pages, g, geo.Hkv, k0, n,
-                         geo.scale, geo.max_pages, geo.num_pages, geo.status, o);
+                         geo.scale, geo.max_pages, geo.num_pages, geo.status, qa, o);
+    const int lane = threadIdx.x & 31, warp = threadIdx.x / 32, h = lane >> 2;
+    if (h < G) {
+        const int64_t row = (static_cast<int64_t>(e) * geo.H + g * G + h) * max_splits + split;
 #pragma unroll
-    for (int si = 0; si < S::kSlotsPerThread; ++si) {
-        const int slot = threadIdx.x + si * kAttnThreads;
-        if (slot < S::kSlots) {
-            const int h = slot / (DH / 2), dp = slot % (DH / 2);
-            const int64_t row = (static_cast<int64_t>(e) * geo.H + g * G + h) * max_splits + split;
-            *reinterpret_cast<float2*>(ws_o + row * DH + 2 * dp) = make_float2(o[si][0], o[si][1]);
-            if (dp == 0) *reinterpret_cast<float2*>(ws_ml + row * 2) = make_float2(sm.m[h], sm.l[h]);
+        for (int nb = 0; nb < S::kNB; ++nb) {
+            const int d = warp * S::kDimsPerWarp + nb * 8 + 2 * (lane & 3);
+            *reinterpret_cast<float2*>(ws_o + row * DH + d) = make_float2(o[nb][0], o[nb][1]);
         }
+        if (warp == 0 && (lane & 3) == 0) *reinterpret_cast<float2*>(ws_ml + row * 2) = make_float2(sm.m[h], sm.l[h]);
     }
 }
 
@@ -361,53 +411,58 @@ prefill_kernel(AttnGeom geo, EntryMap em) {
     const Entry en = get_entry(em, e);
     const int32_t s = en.p + 1;
     const bool ok = en.p >= 0 && (s + BI_PAGE - 1) / BI_PAGE <= geo.max_pages;
+    const int lane = threadIdx.x & 31, warp = threadIdx.x / 32, h = lane >> 2;
     if (!ok) {
         if (threadIdx.x == 0) report(geo.status, BI_DEV_BAD_POSITION);
-#pragma unroll
-        for (int si = 0; si < S::kSlotsPerThread; ++si) {
-            const int slot = threadIdx.x + si * kAttnThreads;
-            if (slot < S::kSlots) {
-                const int h = slot / (DH / 2), dp = slot % (DH / 2);
-                store_out2(geo.out, geo.out_f32, (static_cast<int64_t>(en.t) * geo.H + g * G + h) * DH + 2 * dp, 0.f, 0.f);
-            }
-        }
+        if (h < G)
+            for (int nb = 0; nb < S::kNB; ++nb)
+                store_out2(geo.out, geo.out_f32,
+                           (static_cast<int64_t>(en.t) * geo.H + g * G + h) * DH + warp * S::kDimsPerWarp + nb * 8 +
+                               2 * (lane & 3),
+                           0.f, 0.f);
         return;
     }
-    load_q<G, DH>(sm, reinterpret_cast<const uint16_t*>(geo.q), en.t, geo.H, g);
-    __syncthreads();
-    float M[S::kSlotsPerThread], L[S::kSlotsPerThread], O[S::kSlotsPerThread][2];
+    uint32_t qa[DH / 16][2];
+    load_q_frags<G, DH>(reinterpret_cast<const uint16_t*>(geo.q), en.t, geo.H, g, qa);
+    const int hh = h < G ? h : 0;
+    float M = 0.0f, L = 0.0f, O[S::kNB][2];
     const int32_t count = (s + BI_KV_CHUNK - 1) / BI_KV_CHUNK;
     const int32_t* page_row = geo.page_table + static_cast<int64_t>(en.r) * geo.max_pages;
     for (int32_t j = 0; j < count; ++j) {
         const int32_t k0 = j * BI_KV_CHUNK;
         const int32_t n = min(BI_KV_CHUNK, s - k0);
-        float o[S::kSlotsPerThread][2];
+        float o[S::kNB][2];
         chunk_partial<G, DH>(sm, reinterpret_cast<const uint16_t*>(geo.kc), reinterpret_cast<const uint16_t*>(geo.vc),
-                             page_row, g, geo.Hkv, k0, n, geo.scale, geo.max_pages, geo.num_pages, geo.status, o);
+                             page_row, g, geo.Hkv, k0, n, geo.scale, geo.max_pages, geo.num_pages, geo.status, qa, o);
+        const float m = sm.m[hh], l = sm.l[hh];
+        if (j == 0) {
+            M = m;
+            L = l;
 #pragma unroll
-        for (int si = 0; si < S::kSlotsPerThread; ++si) {
-            const int slot = threadIdx.x + si * kAttnThreads;
-            const int h = slot < S::kSlots ? slot / (DH / 2) : 0;
-            const float m = sm.m[h], l = sm.l[h];
-            if (j == 0) {
-                M[si] = m;
-                L[si] = l;
-                O[si][0] = o[si][0];
-                O[si][1] = o[si][1];
-            } else {
-                fold_step(M[si], L[si], O[si][0], O[si][1], m, l, o[si][0], o[si][1]);
+            for (int nb = 0; nb < S::kNB; ++nb) {
+                O[nb][0] = o[nb][0];
+                O[nb][1] = o[nb][1];
+            }
+        } else {
+            // the same fold as the decode merge, one dim pair at a time
+            const float M0 = M, L0 = L;
+#pragma unroll
+            for (int nb = 0; nb < S::kNB; ++nb) {
+                float Mx = M0, Lx = L0;
+                fold_step(Mx, Lx, O[nb][0], O[nb][1], m, l, o[nb][0], o[nb][1]);
+                M = Mx;
+                L = Lx;
             }
         }
         __syncthreads();
     }
+    if (h < G) {
 #pragma unroll
-    for (int si = 0; si < S::kSlotsPerThread; ++si) {
-        const int slot = threadIdx.x + si * kAttnThreads;
-        if (slot < S::kSlots) {
-            const int h = slot / (DH / 2), dp = slot % (DH / 2);
-            store_out2(geo.out, geo.out_f32, (static_cast<int64_t>(en.t) * geo.H + g * G + h) * DH + 2 * dp,
-                       __fdiv_rn(O[si][0], L[si]), __fdiv_rn(O[si][1], L[si]));
-        }
+        for (int nb = 0; nb < S::kNB; ++nb)
+            store_out2(geo.out, geo.out_f32,
+                       (static_cast<int64_t>(en.t) * geo.H + g * G + h) * DH + warp * S::kDimsPerWarp + nb * 8 +
+                           2 * (lane & 3),
+                       __fdiv_rn(O[nb][0], L), __fdiv_rn(O[nb][1], L));
     }
 }
 
