@@ -201,6 +201,29 @@ bi_status bi_decode_attention(const bi_bf16* q, const bi_bf16* k_cache, const bi
                               float scale, bi_mode mode, void* ws, size_t ws_bytes,
                               int32_t* dev_status, bi_stream stream);
 
+/* bi_decode_attention_noalloc: bi_decode_attention for callers that cannot
+ * allocate device memory where they run it (an allocator that forbids new
+ * allocations once serving has started, a host that only hands over input
+ * and output pointers).  There is no counterpart on the pages; it is a
+ * packaging of the same kernels.  The split partials live in one static
+ * device array of 16 MiB (16777216 bytes) that every GPU loading this
+ * library holds until the process exits; the
+ * call allocates nothing and computes exactly what bi_decode_attention
+ * computes.  A batch whose partials need more
+ * (B * H * splits * (Dh + 2) * 4 bytes, splits = ceil(max_seq_len / 256) in
+ * invariant mode) is rejected with BI_ERR_WORKSPACE before any launch.
+ * The first call on each device looks up the array's device address; make
+ * that first call before any stream capture.  All calls share the one array:
+ * calls whose work overlaps on the GPU race and corrupt each other's
+ * partials, so keep them ordered (one stream, or events).  Nothing in the
+ * array needs to start at zero: each call writes every partial it reads. */
+bi_status bi_decode_attention_noalloc(const bi_bf16* q, const bi_bf16* k_cache, const bi_bf16* v_cache,
+                                      const int32_t* page_table, const int32_t* seq_lens,
+                                      void* out, bi_dtype out_dtype,
+                                      int32_t B, int32_t H, int32_t Hkv, int32_t Dh,
+                                      int32_t max_pages, int32_t num_pages, int32_t max_seq_len,
+                                      float scale, bi_mode mode, int32_t* dev_status, bi_stream stream);
+
 /* bi_prefill_attention: causal attention for ragged query blocks.  Request i
  * owns queries [cu_q[i], cu_q[i+1]) at positions q_pos0[i] + t (cu_q: DEVICE
  * [B+1], q_pos0: DEVICE [B]); its K/V for positions 0..q_pos0[i]+q_len-1 must

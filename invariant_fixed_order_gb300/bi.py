@@ -87,6 +87,8 @@ _proto("bi_rope_table", _i32, _vp, _vp, _i32, _i32, _f64)
 _proto("bi_decode_attention_workspace_size", _sz, _i32, _i32, _i32, _i32, _i32)
 _proto("bi_decode_attention", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
        _f32, _i32, _vp, _sz, _vp, _vp)
+_proto("bi_decode_attention_noalloc", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
+       _i32, _f32, _i32, _vp, _vp)
 _proto("bi_prefill_attention", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
        _i32, _f32, _vp, _vp)
 _proto("bi_argmax", _i32, _vp, _vp, _i32, _i32, _vp)
@@ -207,6 +209,26 @@ def decode_attention(q, k_cache, v_cache, page_table, seq_lens, max_seq_len: int
     _check(_lib.bi_decode_attention(_p(q), _p(k_cache), _p(v_cache), _p(page_table), _p(seq_lens), _p(out),
                                     out_dtype, B, H, Hkv, Dh, page_table.shape[-1], k_cache.shape[0], max_seq_len,
                                     scale, mode, _p(ws), ws.numel(), _p(status), _stream(stream)))
+    return out
+
+
+NOALLOC_SCRATCH_BYTES = 16 << 20
+
+
+def decode_attention_noalloc(q, k_cache, v_cache, page_table, seq_lens, max_seq_len: int, out_dtype: int = BF16,
+                             mode: int = INVARIANT, scale: float | None = None, status=None, out=None,
+                             stream=None) -> torch.Tensor:
+    """decode_attention without a workspace: the library's static device
+    scratch holds the split partials (for callers that cannot allocate)."""
+    B, H, Dh = q.shape
+    Hkv = k_cache.shape[1]
+    if scale is None:
+        scale = float(torch.tensor(1.0, dtype=torch.float32) / torch.sqrt(torch.tensor(float(Dh))))
+    if out is None:
+        out = torch.empty(B, H, Dh, device=q.device, dtype=torch.float32 if out_dtype == F32 else torch.bfloat16)
+    _check(_lib.bi_decode_attention_noalloc(_p(q), _p(k_cache), _p(v_cache), _p(page_table), _p(seq_lens), _p(out),
+                                            out_dtype, B, H, Hkv, Dh, page_table.shape[-1], k_cache.shape[0],
+                                            max_seq_len, scale, mode, _p(status), _stream(stream)))
     return out
 
 

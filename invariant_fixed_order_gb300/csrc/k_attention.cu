@@ -15,6 +15,9 @@
 // the two kernels.
 #include <math.h>
 
+#include <mutex>
+#include <string>
+
 #include "common.cuh"
 #include "internal.h"
 
@@ -566,3 +569,90 @@ cudaError_t launch_prefill_attention(const AttnGeom& g, const EntryMap& em, int3
 }
 
 }  // namespace bi
+
+// ===========================================================================
+// Allocation-free decode attention.
+//
+// Some callers cannot allocate device memory at the point where they run
+// decode attention: code running under an allocator that forbids new
+// allocations once serving has started, callers that own no memory pool of
+// their own, or hosts that only hand this library plain input and output
+// pointers.  bi_decode_attention_noalloc serves them with the same kernels as
+// bi_decode_attention, its fp32 split partials living in one statically sized
+// device array below instead of a caller workspace.
+// ===========================================================================
+
+namespace bi {
+
+// Scratch for the split partials of bi_decode_attention_noalloc.  Every GPU
+// that loads this library holds it until the process exits.
+constexpr size_t kNoAllocScratchBytes = static_cast<size_t>(16) << 20;  // 16 MiB
+static __device__ __align__(256) unsigned char g_noalloc_scratch[kNoAllocScratchBytes];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_noalloc_mutex;
+void* g_noalloc_ptr[kMaxDevices] = {};
+
+// Device address of the scratch array on the current device; looked up once
+// per device (the host-side symbol is only a stand-in, never a device address).
+bi_status noalloc_scratch(void** out) {
+    int dev = 0;
+    cudaError_t e = cudaGetDevice(&dev);
+    if (e != cudaSuccess) return cuda_fail(e, "bi_decode_attention_noalloc: cudaGetDevice");
+    if (dev < 0 || dev >= kMaxDevices) return fail(BI_ERR_UNSUPPORTED, "bi_decode_attention_noalloc: device index");
+    std::lock_guard<std::mutex> lock(g_noalloc_mutex);
+    if (g_noalloc_ptr[dev] == nullptr) {
+        void* p = nullptr;
+        e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
+        if (e != cudaSuccess) return cuda_fail(e, "bi_decode_attention_noalloc: cudaGetSymbolAddress");
+        g_noalloc_ptr[dev] = p;
+    }
+    *out = g_noalloc_ptr[dev];
+    return BI_OK;
+}
+}  // namespace
+
+}  // namespace bi
+
+extern "C" bi_status bi_decode_attention_noalloc(const bi_bf16* q, const bi_bf16* k_cache, const bi_bf16* v_cache,
+                                                 const int32_t* page_table, const int32_t* seq_lens, void* out,
+                                                 bi_dtype out_dtype, int32_t B, int32_t H, int32_t Hkv, int32_t Dh,
+                                                 int32_t max_pages, int32_t num_pages, int32_t max_seq_len,
+                                                 float scale, bi_mode mode, int32_t* dev_status, bi_stream stream) {
+    using namespace bi;
+    if (B < 0) return fail(BI_ERR_SHAPE, "bi_decode_attention_noalloc: B < 0");
+    if (B == 0) return BI_OK;
+    if (!attention_supported(H, Hkv, Dh))
+        return fail(BI_ERR_UNSUPPORTED, "bi_decode_attention_noalloc: need Dh in {64,128} and H/Hkv in {1,2,4,8}");
+    if (max_pages <= 0 || num_pages <= 0) return fail(BI_ERR_SHAPE, "bi_decode_attention_noalloc: need max_pages, num_pages > 0");
+    if (out_dtype != BI_BF16 && out_dtype != BI_F32) return fail(BI_ERR_INVALID, "bi_decode_attention_noalloc: bad dtype");
+    if (!q || !k_cache || !v_cache || !page_table || !seq_lens || !out)
+        return fail(BI_ERR_INVALID, "bi_decode_attention_noalloc: null pointer");
+    auto aligned16 = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+    if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+        return fail(BI_ERR_INVALID, "bi_decode_attention_noalloc: pointers must be 16-byte aligned");
+    if (max_seq_len <= 0 || max_seq_len > max_pages * BI_PAGE)
+        return fail(BI_ERR_SHAPE, "bi_decode_attention_noalloc: need 0 < max_seq_len <= max_pages * 16");
+    if (mode != BI_INVARIANT && mode != BI_VARIANT) return fail(BI_ERR_INVALID, "bi_decode_attention_noalloc: bad mode");
+    int32_t max_splits = invariant_max_splits(max_seq_len), chunk2 = 0;
+    if (mode == BI_VARIANT) variant_split_plan(B, H, Hkv, max_seq_len, &chunk2, &max_splits);
+    const size_t need = decode_ws_bytes(B, H, Dh, max_splits);
+    if (need > kNoAllocScratchBytes)
+        return fail(BI_ERR_WORKSPACE,
+                    "bi_decode_attention_noalloc: this batch needs " + std::to_string(need) +
+                        " bytes of split partials, more than the " + std::to_string(kNoAllocScratchBytes) +
+                        "-byte static scratch; use bi_decode_attention with a workspace");
+    void* scratch = nullptr;
+    bi_status st = noalloc_scratch(&scratch);
+    if (st != BI_OK) return st;
+    // every partial the merge reads is written earlier in this call: nothing in
+    // the scratch has to start at zero
+    float* ws_o = static_cast<float*>(scratch);
+    float* ws_ml = ws_o + static_cast<size_t>(B) * H * max_splits * Dh;
+    AttnGeom g{q, k_cache, v_cache, page_table, out, out_dtype == BI_F32, H, Hkv, Dh, max_pages, num_pages, scale,
+               dev_status};
+    EntryMap em{0, seq_lens, nullptr, nullptr, B};
+    cudaError_t e = launch_decode_attention(g, em, B, max_splits, chunk2, ws_o, ws_ml, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? BI_OK : cuda_fail(e, "bi_decode_attention_noalloc launch");
+}
