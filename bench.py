@@ -410,9 +410,8 @@ def run_ours(args):
     barrier()
     ms = e0.elapsed_time(e1) / args.steps
     if world > 1:
-        t = torch.tensor([ms], device=device)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        ms = float(t.item())
+        from invariant_fixed_order_gb300 import replicas
+        ms = replicas.max_over_ranks(ms, device=device)
     w.eng.check()
     value = world * B / (ms * 1e-3)
     launches_per_step = 13  # embed, 2 rmsnorm, 4 GEMMs, rope, decode split, merge, gather, final norm, LM GEMM

@@ -1,0 +1,109 @@
+"""System tests on multi-layer 8B-shaped models (random weights):
+
+* unique completions: every prompt decoded greedily under several randomised
+  continuous-batching schedules (random arrival, batch composition, chunked
+  prefill, evict/readmit) gives exactly one completion, equal to its solo run
+  (and the 95% rule-of-three bound on the divergence rate is reported);
+* decode-verify-rollback: the batch-variant fast path verified by invariant
+  replay commits exactly the pure invariant greedy tokens, including when the
+  fast path is forced to emit wrong candidates.
+
+Sizes are reduced from the full configurations so the suite stays within
+minutes; BI_SYSTEM_SCALE=full runs the full ones (32 layers, 64 prompts of
+128-4096 tokens, 256 generated tokens, 50 schedules)."""
+import os
+
+import numpy as np
+import pytest
+import torch
+
+from invariant_fixed_order_gb300 import synth
+from invariant_fixed_order_gb300.config import LLAMA3_8B
+
+pytestmark = pytest.mark.gpu
+
+FULL = os.environ.get("BI_SYSTEM_SCALE") == "full"
+
+
+@pytest.fixture(scope="module")
+def mods():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from invariant_fixed_order_gb300 import bi, dvr, sched
+    from invariant_fixed_order_gb300.engine import Engine
+    return bi, sched, dvr, Engine
+
+
+def greedy_solo(sched, runner, prompt, rid, n_new, mode):
+    req = sched.Request(rid, prompt)
+    logits, tokens, sl = runner.step([sched.StepItem(req, len(prompt), "last")], mode=mode)
+    req.generated.append(int(tokens[sl[0]][-1].item()))
+    while len(req.generated) < n_new:
+        logits, tokens, sl = runner.step([sched.StepItem(req, 1, "last")], mode=mode)
+        req.generated.append(int(tokens[sl[0]][0].item()))
+    runner.evict(req)
+    return list(req.generated)
+
+
+def test_unique_completions_under_random_schedules(mods):
+    bi, sched, dvr, Engine = mods
+    n_layers, n_prompts, lo, hi, n_new, n_sched = (32, 64, 128, 4096, 256, 50) if FULL else (16, 24, 128, 1024, 40, 6)
+    cfg = LLAMA3_8B.with_layers(n_layers)
+    lens = [int(x) for x in synth.uniform_ints(n_prompts, lo, hi, 42 + 4)]
+    prompts = [synth.token_ids(n, cfg.V, 4000 + i) for i, n in enumerate(lens)]
+    max_pages = (hi + n_new + 15) // 16 + 1
+    eng = Engine(cfg, num_pages=sum((n + n_new + 15) // 16 + 1 for n in lens) + 256, max_pages=max_pages,
+                 max_T=max(4096, hi) + n_prompts, max_B=n_prompts, max_R=n_prompts)
+    runner = sched.Runner(eng)
+    solo = {rid: greedy_solo(sched, runner, p, rid, n_new, bi.INVARIANT) for rid, p in enumerate(prompts)}
+    completions = {rid: {tuple(solo[rid])} for rid in solo}
+    fz = sched.FuzzConfig(token_budget=4096, chunk_min=256, chunk_max=2048, p_evict=0.05, readmit_delay=(1, 3),
+                          arrival_span=6)
+    for k in range(n_sched):
+        reqs = [sched.Request(rid, p) for rid, p in enumerate(prompts)]
+        sched.fuzz_continuous(runner, reqs, n_new, np.random.default_rng(1000 + k), fz, all_prompt_logits=False)
+        eng.check()
+        for r in reqs:
+            completions[r.rid].add(tuple(r.generated[:n_new]))
+    unique = {rid: len(c) for rid, c in completions.items()}
+    bound = sched.rule_of_three(n_prompts * n_sched)
+    print(f"unique completions per prompt: max {max(unique.values())}; rule-of-three bound {bound:.4f}")
+    assert all(u == 1 for u in unique.values()), unique
+    eng.close()
+
+
+def test_decode_verify_rollback_commits_the_invariant_greedy_tokens(mods):
+    bi, sched, dvr, Engine = mods
+    n_layers, n_prompts, n_new, window = (32, 64, 256, 64) if FULL else (8, 16, 96, 32)
+    cfg = LLAMA3_8B.with_layers(n_layers)
+    lens = [int(x) for x in synth.uniform_ints(n_prompts, 128, 1024, 42 + 5)]
+    prompts = [synth.token_ids(n, cfg.V, 5000 + i) for i, n in enumerate(lens)]
+    max_pages = (1024 + n_new + window + 15) // 16 + 1
+    eng = Engine(cfg, num_pages=n_prompts * max_pages + 64, max_pages=max_pages,
+                 max_T=max(8 * window, 8 * 1024) + 64, max_B=n_prompts, max_R=8 * window)
+    runner = sched.Runner(eng)
+    truth = {rid: greedy_solo(sched, runner, p, rid, n_new, bi.INVARIANT) for rid, p in enumerate(prompts)}
+
+    # plain run of the fast path
+    reqs = [sched.Request(rid, p) for rid, p in enumerate(prompts)]
+    st = dvr.dvr_generate(runner, reqs, n_new, window=window, verify_batch=8)
+    eng.check()
+    for r in reqs:
+        assert r.generated == truth[r.rid], r.rid
+        runner.evict(r)
+    assert st.committed == n_prompts * n_new
+    print("dvr:", st.as_dict())
+
+    # a fast path that emits wrong candidates at chosen positions: the verifier
+    # must catch each one, roll back and still commit exactly the greedy tokens
+    bad = {(rid, len(prompts[rid]) + 5 + 7 * rid) for rid in range(n_prompts)}
+    reqs = [sched.Request(rid, p) for rid, p in enumerate(prompts)]
+    st2 = dvr.dvr_generate(runner, reqs, n_new, window=window, verify_batch=8,
+                           corrupt=lambda rid, pos: (rid, pos) in bad)
+    eng.check()
+    for r in reqs:
+        assert r.generated == truth[r.rid], r.rid
+        runner.evict(r)
+    assert st2.mismatched_windows >= n_prompts
+    assert st2.rollback_rate > 0
+    eng.close()
