@@ -31,8 +31,9 @@
  *   - All work is enqueued on `stream` (a cudaStream_t; NULL = legacy default
  *     stream) and is asynchronous.  No call allocates device memory except
  *     bi_model_create (its RoPE table).  Workspaces are caller-owned, sized by
- *     the *_workspace_size functions, and only the call they are passed to may
- *     use them until that call's work has finished on the stream.
+ *     the *_workspace_size functions, 16-byte aligned (as cudaMalloc's are),
+ *     and only the call they are passed to may use them until that call's
+ *     work has finished on the stream.
  *   - Argument validation happens before any launch: on failure nothing is
  *     launched or written, the call returns a bi_status other than BI_OK and
  *     bi_last_error() describes it.

@@ -200,6 +200,7 @@ extern "C" bi_status bi_decode_attention(const bi_bf16* q, const bi_bf16* k_cach
     if (mode == BI_VARIANT) variant_split_plan(B, H, Hkv, max_seq_len, &chunk2, &max_splits);
     const size_t need = decode_ws_bytes(B, H, Dh, max_splits);
     if (!ws || ws_bytes < need) return fail(BI_ERR_WORKSPACE, "bi_decode_attention: workspace too small");
+    if (!aligned16(ws)) return fail(BI_ERR_INVALID, "bi_decode_attention: workspace must be 16-byte aligned");
     float* ws_o = static_cast<float*>(ws);
     float* ws_ml = ws_o + static_cast<size_t>(B) * H * max_splits * Dh;
     AttnGeom g{q, k_cache, v_cache, page_table, out, out_dtype == BI_F32, H, Hkv, Dh, max_pages, num_pages, scale,
@@ -323,7 +324,7 @@ extern "C" void bi_model_destroy(bi_model* m) {
 namespace {
 
 struct FwdLayout {
-    size_t x, y, qkv, q, attn, h, xr, yr, logits, meta, dec_ws, gemm_ws, total;
+    size_t x, y, qkv, q, attn, h, yr, logits, meta, dec_ws, gemm_ws, total;
     int32_t dec_splits;
 };
 
@@ -342,7 +343,6 @@ FwdLayout fwd_layout(const bi_model_config& c, int32_t T, int32_t B, int32_t R, 
     L.q = take(static_cast<size_t>(T) * c.H * c.Dh * 2);
     L.attn = take(static_cast<size_t>(T) * c.H * c.Dh * 2);
     L.h = take(static_cast<size_t>(T) * c.F * 2);
-    L.xr = take(static_cast<size_t>(R) * c.d * 2);
     L.yr = take(static_cast<size_t>(R) * c.d * 2);
     L.logits = take(static_cast<size_t>(R) * c.V * 4);
     L.meta = take((static_cast<size_t>(T) * 4 + R + 16) * 4);
@@ -410,6 +410,7 @@ extern "C" bi_status bi_forward_step(bi_model* m, const bi_batch* batch, const b
         if (b.logit_rows[r] < 0 || b.logit_rows[r] >= T) return fail(BI_ERR_SHAPE, "bi_forward_step: logit row out of range");
     const FwdLayout L = fwd_layout(c, T, b.B, b.R, max_seq);
     if (!ws || ws_bytes < L.total) return fail(BI_ERR_WORKSPACE, "bi_forward_step: workspace too small");
+    if (!aligned16(ws)) return fail(BI_ERR_INVALID, "bi_forward_step: workspace must be 16-byte aligned");
     if (!dev_status) return fail(BI_ERR_INVALID, "bi_forward_step: null dev_status");
 
     // pinned staging: [tok_req T][tok_pos T][dec_list nd][pre_list T-nd][logit_rows R]
@@ -499,11 +500,9 @@ extern "C" bi_status bi_forward_step(bi_model* m, const bi_batch* batch, const b
         BI_TRY_CUDA(cudaMemcpyAsync(hidden_out, x, static_cast<size_t>(T) * c.d * 2, cudaMemcpyDeviceToDevice, s),
                     "hidden copy");
     if (b.R > 0 && (logits_out || tokens_out)) {
-        bi_bf16* xr = reinterpret_cast<bi_bf16*>(base + L.xr);
         bi_bf16* yr = reinterpret_cast<bi_bf16*>(base + L.yr);
         float* logits = logits_out ? logits_out : reinterpret_cast<float*>(base + L.logits);
-        BI_TRY_CUDA(launch_gather_rows(x, d_rows, xr, b.R, c.d, s), "gather rows");
-        BI_TRY_CUDA(launch_rmsnorm(xr, m->gamma_final, yr, b.R, c.d, c.eps, s), "final rmsnorm");
+        BI_TRY_CUDA(launch_rmsnorm(x, m->gamma_final, yr, b.R, c.d, c.eps, s, d_rows), "final rmsnorm");
         BI_TRY(run_gemm(yr, m->w_lm, logits, BI_F32, nullptr, BI_EP_NONE, b.R, c.V, c.d, mode, gws, gws_bytes,
                         dev_status, s));
         if (tokens_out) BI_TRY_CUDA(launch_argmax(logits, tokens_out, b.R, c.V, s), "argmax");

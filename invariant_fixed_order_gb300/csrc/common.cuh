@@ -58,6 +58,19 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
     return r;
 }
 
+// ---------------------------------------------------------------------------
+// Programmatic dependent launch.  Every kernel of this library is launched so
+// that it may start while the kernel before it in the stream is finishing:
+// pdl_trigger() lets the next kernel start its own prologue, pdl_wait() blocks
+// until every kernel ordered before this one has completed with its writes
+// visible.  Each kernel runs pdl_wait() in every thread before it reads or
+// writes global memory that another kernel touches, and before it exits, so
+// completion of a kernel still implies completion of all earlier ones.  Both
+// are no-ops when the launch carries no such dependency.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ void pdl_trigger() { asm volatile("griddepcontrol.launch_dependents;" ::: "memory"); }
+__device__ __forceinline__ void pdl_wait() { asm volatile("griddepcontrol.wait;" ::: "memory"); }
+
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {
     return static_cast<uint32_t>(__cvta_generic_to_shared(p));
 }

@@ -10,6 +10,27 @@
 
 namespace bi {
 
+// Launch with programmatic stream serialisation: the kernel may begin while
+// the previous kernel in the stream drains, and synchronises with it through
+// griddepcontrol.wait (pdl_wait in common.cuh), which every kernel of this
+// library executes before touching shared global data.
+template <typename... P, typename... A>
+inline cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              A&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<A&&>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // thread-local error message (api.cu)
 void set_error(const std::string& msg);
 bi_status fail(bi_status s, const std::string& msg);
@@ -17,8 +38,9 @@ bi_status cuda_fail(cudaError_t e, const char* what);
 int num_sms();
 
 // ---- elementwise / row kernels (k_rows.cu) ----
+// rows: output rows; src_rows (device, optional): output row r normalises input row src_rows[r]
 cudaError_t launch_rmsnorm(const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y, int64_t rows,
-                           int32_t d, float eps, cudaStream_t s);
+                           int32_t d, float eps, cudaStream_t s, const int32_t* src_rows = nullptr);
 cudaError_t launch_embed(const bi_bf16* E, const int32_t* ids, bi_bf16* x, int32_t T, int32_t V,
                          int32_t d, int32_t* status, cudaStream_t s);
 cudaError_t launch_rope_kv_append(const float* qkv, const int32_t* tok_req, const int32_t* tok_pos,
@@ -29,8 +51,6 @@ cudaError_t launch_rope_kv_append(const float* qkv, const int32_t* tok_req, cons
 cudaError_t launch_argmax(const float* logits, int32_t* out, int32_t R, int32_t V, cudaStream_t s);
 cudaError_t launch_pack_gate_up(const bi_bf16* g, const bi_bf16* u, bi_bf16* gu, int32_t F,
                                 int32_t d, cudaStream_t s);
-cudaError_t launch_gather_rows(const bi_bf16* x, const int32_t* rows, bi_bf16* out, int32_t R,
-                               int32_t d, cudaStream_t s);
 
 // ---- attention (k_attention.cu) ----
 // How a work entry e maps to (query/output row t, request r, position p).

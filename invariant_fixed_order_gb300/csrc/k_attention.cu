@@ -341,6 +341,8 @@ template <int G, int DH>
 __global__ void __launch_bounds__(kAttnThreads)
 decode_split_kernel(AttnGeom geo, EntryMap em, int32_t max_splits, int32_t chunk2, float* __restrict__ ws_o,
                     float* __restrict__ ws_ml) {
+    pdl_trigger();
+    pdl_wait();
     using S = AttnShape<G, DH>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     AttnSmem<G, DH>& sm = *reinterpret_cast<AttnSmem<G, DH>*>(smem_raw);
@@ -375,11 +377,17 @@ decode_split_kernel(AttnGeom geo, EntryMap em, int32_t max_splits, int32_t chunk
     }
 }
 
-// Merge: grid (entries, H), DH/2 threads, each one dim pair; serial over splits.
+// Merge: grid (entries, H), DH/2 threads, each one dim pair; the fold runs
+// over splits in ascending order, its inputs fetched kMergeBatch splits at a
+// time so the loads of a batch are in flight together.
+constexpr int kMergeBatch = 8;
+
 template <int DH>
 __global__ void __launch_bounds__(DH / 2)
 decode_merge_kernel(AttnGeom geo, EntryMap em, int32_t max_splits, int32_t chunk2, const float* __restrict__ ws_o,
                     const float* __restrict__ ws_ml) {
+    pdl_trigger();
+    pdl_wait();
     const int32_t e = blockIdx.x, h = blockIdx.y, dp = threadIdx.x;
     const Entry en = get_entry(em, e);
     const int32_t s = en.p + 1;
@@ -392,11 +400,29 @@ decode_merge_kernel(AttnGeom geo, EntryMap em, int32_t max_splits, int32_t chunk
         return;
     }
     const int64_t row0 = (static_cast<int64_t>(e) * geo.H + h) * max_splits;
-    float M = ws_ml[row0 * 2], L = ws_ml[row0 * 2 + 1];
-    float O0 = ws_o[row0 * DH + 2 * dp], O1 = ws_o[row0 * DH + 2 * dp + 1];
-    for (int32_t j = 1; j < count; ++j) {
-        const int64_t r = row0 + j;
-        fold_step(M, L, O0, O1, ws_ml[r * 2], ws_ml[r * 2 + 1], ws_o[r * DH + 2 * dp], ws_o[r * DH + 2 * dp + 1]);
+    float M = 0.0f, L = 0.0f, O0 = 0.0f, O1 = 0.0f;
+    for (int32_t j0 = 0; j0 < count; j0 += kMergeBatch) {
+        float2 ml[kMergeBatch], o[kMergeBatch];
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+            const int64_t r = row0 + j0 + u;
+            if (j0 + u < count) {
+                ml[u] = *reinterpret_cast<const float2*>(ws_ml + r * 2);
+                o[u] = *reinterpret_cast<const float2*>(ws_o + r * DH + 2 * dp);
+            }
+        }
+#pragma unroll
+        for (int u = 0; u < kMergeBatch; ++u) {
+            if (j0 + u >= count) break;
+            if (j0 + u == 0) {
+                M = ml[u].x;
+                L = ml[u].y;
+                O0 = o[u].x;
+                O1 = o[u].y;
+            } else {
+                fold_step(M, L, O0, O1, ml[u].x, ml[u].y, o[u].x, o[u].y);
+            }
+        }
     }
     store_out2(geo.out, geo.out_f32, oidx, __fdiv_rn(O0, L), __fdiv_rn(O1, L));
 }
@@ -407,6 +433,8 @@ decode_merge_kernel(AttnGeom geo, EntryMap em, int32_t max_splits, int32_t chunk
 template <int G, int DH>
 __global__ void __launch_bounds__(kAttnThreads)
 prefill_kernel(AttnGeom geo, EntryMap em) {
+    pdl_trigger();
+    pdl_wait();
     using S = AttnShape<G, DH>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
     AttnSmem<G, DH>& sm = *reinterpret_cast<AttnSmem<G, DH>*>(smem_raw);
@@ -518,11 +546,11 @@ static cudaError_t launch_decode_t(const AttnGeom& g, const EntryMap& em, int32_
         attr_set = true;
     }
     dim3 grid(n, g.Hkv, max_splits);
-    decode_split_kernel<G, DH><<<grid, kAttnThreads, smem, s>>>(g, em, max_splits, chunk2, ws_o, ws_ml);
-    cudaError_t e = cudaGetLastError();
+    cudaError_t e = launch_pdl(decode_split_kernel<G, DH>, grid, dim3(kAttnThreads), smem, s, g, em, max_splits,
+                               chunk2, ws_o, ws_ml);
     if (e != cudaSuccess) return e;
-    decode_merge_kernel<DH><<<dim3(n, g.H), DH / 2, 0, s>>>(g, em, max_splits, chunk2, ws_o, ws_ml);
-    return cudaGetLastError();
+    return launch_pdl(decode_merge_kernel<DH>, dim3(n, g.H), dim3(DH / 2), 0, s, g, em, max_splits, chunk2,
+                      static_cast<const float*>(ws_o), static_cast<const float*>(ws_ml));
 }
 
 template <int G, int DH>
@@ -535,8 +563,7 @@ static cudaError_t launch_prefill_t(const AttnGeom& g, const EntryMap& em, int32
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    prefill_kernel<G, DH><<<dim3(n, g.Hkv), kAttnThreads, smem, s>>>(g, em);
-    return cudaGetLastError();
+    return launch_pdl(prefill_kernel<G, DH>, dim3(n, g.Hkv), dim3(kAttnThreads), smem, s, g, em);
 }
 
 #define BI_ATTN_DISPATCH(FN, ...)                                              \

@@ -4,32 +4,33 @@
 // accumulation" and "3 · Kernel selection changing with shape": split-K and
 // M-dependent kernel choice are what make a GEMM's per-element order follow
 // the batch.  Here every output element, for every M, is produced by the same
-// sequence: one tcgen05.mma shape (M=128, N=64, K=16; bf16 in, fp32
+// sequence: one tcgen05.mma shape (M=128, N=128, K=16; bf16 in, fp32
 // accumulated in TMEM), K tiles of 64 in ascending order, inside a K tile the
 // four 16-deep MMAs in ascending order, all into one accumulator.
 //
 // What may follow M is only how that work is laid out, never the arithmetic
 // of an element:
-//   * the CTA tile is 128 x 64 (one MMA per 16-deep step) for small M, where
-//     the weights stream from HBM and many CTAs are wanted, and 128 x 256
-//     (four identical 64-wide MMAs per step, sharing A) for large M, where the
-//     tensor pipe must be fed from L2;
+//   * the CTA tile is 128 x 128 (one MMA per 16-deep step) for M <= 256, and
+//     128 x 256 (two identical MMAs per step, sharing A) for larger M, where
+//     the tensor pipe must be fed from L2;
 //   * the TMA box of A covers the smallest power of two >= M rows (16..128);
 //     A stages are packed at that stride, so the MMA's rows past the box read
 //     neighbouring stages: those rows of the accumulator are never stored,
 //     and a row's result depends only on its own A row (pinned by the row-
 //     invariance tests);
-//   * ring depths.
+//   * ring depth and K tiles per ring stage.
 //
-// The kernel is persistent (one CTA per SM) with warp roles: warp 0 streams
-// weight tiles by TMA into a deep ring and owns the TMEM allocation, warp 2
-// streams activation tiles into a separate ring, warp 1 issues the MMAs
-// (one thread), warps 4-7 read the accumulator back (warp w: TMEM lanes
-// 32*(w%4)..+31) and run the fused epilogue.  The accumulator is double
-// buffered in TMEM so a tile's epilogue overlaps the next tile's main loop.
-// Every wait is bounded: a wait that runs out sets an abort flag and a device
-// status code, every role winds down, copies and MMAs in flight are drained
-// and TMEM is freed.
+// The kernel is persistent (at most one CTA per SM) with warp roles: warp 0
+// streams K tiles of A and W by TMA into one ring and owns the TMEM
+// allocation, warp 1 issues the MMAs (one thread), warps 4-7 read the
+// accumulator back (warp w: TMEM lanes 32*(w%4)..+31) and run the fused
+// epilogue.  The accumulator is double buffered in TMEM so a tile's epilogue
+// overlaps the next tile's main loop.  Weights do not depend on the kernel
+// before this one in the stream, so while that kernel finishes the producer
+// already pulls the first tile's weight slab into L2; activations are read
+// only after the dependency wait.  Every wait is bounded: a wait that runs
+// out sets an abort flag and a device status code, every role winds down,
+// copies and MMAs in flight are drained and TMEM is freed.
 //
 // BI_VARIANT splits K over CTAs into an fp32 workspace when the output has
 // fewer tiles than SMs and adds the partials in split order in a second
@@ -54,6 +55,10 @@ constexpr int kAFull = kBM * kBK * 2;  // bytes the MMA reads for A per K tile (
 constexpr int kGroupM = 16;            // M tiles per rasterisation band
 constexpr int kBarrierBytes = 1024;
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBM, kUN);
+// L2 prefetch of weights before the dependency wait: at most this many bytes
+// per CTA, and at most kPrefetchTotal over the grid (L2 holds 126 MB).
+constexpr int64_t kPrefetchPerCta = 1 << 20;
+constexpr int64_t kPrefetchTotal = 64ll << 20;
 
 struct GemmArgs {
     void* C;
@@ -173,6 +178,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         n_tile = (lin % band) / band_m;
     };
 
+    pdl_trigger();
     if (warp == 0 && lane == 0) {
         ptx::prefetch_tmap(&tmA);
         ptx::prefetch_tmap(&tmW);
@@ -203,6 +209,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+
+    if (warp == 0 && lane == 0 && static_cast<int32_t>(blockIdx.x) < args.total_tiles) {
+        // weights of the first tile into L2 while the previous kernel drains
+        int32_t m_tile, n_tile;
+        tile_coords(blockIdx.x, m_tile, n_tile);
+        const int64_t budget = min(kPrefetchPerCta, kPrefetchTotal / (static_cast<int64_t>(gridDim.x) * gridDim.y));
+        const int32_t nk = static_cast<int32_t>(budget / kWBytes < nkb ? budget / kWBytes : nkb);
+        for (int32_t kb = 0; kb < nk; ++kb) ptx::tma_prefetch_l2_2d(&tmW, (kb0 + kb) * kBK, n_tile * BN);
+    }
+    pdl_wait();
 
     if (warp == 0) {
         if (lane == 0) {
@@ -357,6 +373,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 // Split-K reduction (variant mode): partials added in split order, then the epilogue.
 __global__ void splitk_reduce_kernel(const float* __restrict__ ws, int32_t splits, int64_t split_stride, int64_t M,
                                      int32_t N, void* C, int32_t c_f32, const uint16_t* residual, int32_t ep) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t idx = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x;
     if (ep == BI_EP_SWIGLU) {
         const int32_t nout = N / 2;
@@ -477,8 +495,7 @@ cudaError_t launch_tiles(const CUtensorMap& tmA, const CUtensorMap& tmW, const G
                                        227 * 1024);
         });
         if (err != cudaSuccess) return err;
-        gemm_tc_kernel<BN><<<grid, kGemmThreads, smem, s>>>(tmA, tmW, a);
-        return cudaGetLastError();
+        return launch_pdl(gemm_tc_kernel<BN>, grid, dim3(kGemmThreads), smem, s, tmA, tmW, a);
     }
 }
 
@@ -513,8 +530,8 @@ bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype
     a.kps = L.kps;
     a.status = status;
     if (plan.splits > 1) {
-        if (ws == nullptr || ws_bytes < gemm_ws_bytes(M, N, K, mode))
-            return fail(BI_ERR_WORKSPACE, "bi_gemm: variant split-K workspace too small");
+        if (ws == nullptr || ws_bytes < gemm_ws_bytes(M, N, K, mode) || (reinterpret_cast<uintptr_t>(ws) & 15u))
+            return fail(BI_ERR_WORKSPACE, "bi_gemm: variant split-K workspace too small or not 16-byte aligned");
         a.C = ws;
         a.c_f32 = 1;
         a.ep = BI_EP_NONE;
@@ -540,10 +557,9 @@ bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype
         const int64_t n_out = ep == BI_EP_SWIGLU ? M * (N / 2) : M * N;
         const int threads = 256;
         const int64_t blocks = (n_out + threads - 1) / threads;
-        splitk_reduce_kernel<<<static_cast<unsigned>(blocks), threads, 0, s>>>(
-            reinterpret_cast<const float*>(ws), plan.splits, M * N, M, N, C, c_dtype == BI_F32,
-            reinterpret_cast<const uint16_t*>(residual), ep);
-        e = cudaGetLastError();
+        e = launch_pdl(splitk_reduce_kernel, dim3(static_cast<unsigned>(blocks)), dim3(threads), 0, s,
+                       static_cast<const float*>(ws), plan.splits, M * N, M, N, C, static_cast<int32_t>(c_dtype == BI_F32),
+                       reinterpret_cast<const uint16_t*>(residual), static_cast<int32_t>(ep));
         if (e != cudaSuccess) return cuda_fail(e, "splitk_reduce_kernel launch");
     }
     return BI_OK;

@@ -1,5 +1,5 @@
-// Row-wise kernels: RMSNorm, embedding gather, RoPE + paged KV append, greedy
-// argmax, gate/up packing, row gather.
+// Row-wise kernels: RMSNorm (optionally of gathered rows), embedding gather,
+// RoPE + paged KV append, greedy argmax, gate/up packing.
 #include "common.cuh"
 #include "internal.h"
 
@@ -11,57 +11,105 @@ namespace bi {
 // ascending element order with fused multiply-adds; the 32 lane sums then meet
 // in an xor-butterfly (16, 8, 4, 2, 1).  Addition is commutative, so every
 // lane ends with the same bits and the order depends on d only.
+//
+// A lane issues all loads of a block of CPL chunks (and of their gains)
+// before it uses any, so a row costs one memory latency rather than one per
+// chunk; when the row fits one block (d <= 256 * CPL) it stays in registers
+// for the second pass.  Blocking changes when values arrive, not the order in
+// which they are added.
 // ---------------------------------------------------------------------------
-constexpr int kNormWarps = 8;
+constexpr int kNormWarps = 4;
 
+template <int CPL>
 __global__ void __launch_bounds__(kNormWarps * 32)
-rmsnorm_kernel(const uint4* x, const uint4* __restrict__ gamma, uint4* y, int64_t rows,
-               int32_t d8, float eps, float fd) {
+rmsnorm_kernel(const uint4* x, const uint4* __restrict__ gamma, uint4* y, int64_t rows, int32_t d8, float eps,
+               float fd, const int32_t* __restrict__ src_rows) {
+    pdl_trigger();
+    pdl_wait();
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kNormWarps + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;  // uniform per warp
-    const uint4* xr = x + row * d8;
-    float ss = 0.0f;
-    for (int c = lane; c < d8; c += 32) {
-        const uint4 v = xr[c];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
+    const int64_t src = src_rows != nullptr ? static_cast<int64_t>(src_rows[row]) : row;
+    const uint4* xr = x + src * d8;
+    uint4* yr = y + row * d8;
+    constexpr int kBlock = 32 * CPL;
+    uint4 v[CPL], g[CPL];
+    auto load_block = [&](int base, bool with_gamma) {
 #pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float a = bf16_lo(w[e]);
-            ss = __fmaf_rn(a, a, ss);
-            const float b = bf16_hi(w[e]);
-            ss = __fmaf_rn(b, b, ss);
+        for (int i = 0; i < CPL; ++i) {
+            const int c = base + lane + 32 * i;
+            if (c < d8) {
+                v[i] = xr[c];
+                if (with_gamma) g[i] = gamma[c];
+            }
+        }
+    };
+    auto store_block = [&](int base, float rinv) {
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+            const int c = base + lane + 32 * i;
+            if (c < d8) {
+                const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+                const uint32_t gw[4] = {g[i].x, g[i].y, g[i].z, g[i].w};
+                uint32_t o[4];
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float a = __fmul_rn(__fmul_rn(bf16_lo(w[e]), rinv), bf16_lo(gw[e]));
+                    const float b = __fmul_rn(__fmul_rn(bf16_hi(w[e]), rinv), bf16_hi(gw[e]));
+                    o[e] = pack_bf16x2(a, b);
+                }
+                yr[c] = make_uint4(o[0], o[1], o[2], o[3]);
+            }
+        }
+    };
+    const bool cached = d8 <= kBlock;
+    float ss = 0.0f;
+    for (int base = 0; base < d8; base += kBlock) {
+        load_block(base, cached);
+#pragma unroll
+        for (int i = 0; i < CPL; ++i) {
+            if (base + lane + 32 * i < d8) {
+                const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float a = bf16_lo(w[e]);
+                    ss = __fmaf_rn(a, a, ss);
+                    const float b = bf16_hi(w[e]);
+                    ss = __fmaf_rn(b, b, ss);
+                }
+            }
         }
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, off));
     const float mean = __fdiv_rn(ss, fd);
     const float rinv = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, eps)));
-    uint4* yr = y + row * d8;
-    for (int c = lane; c < d8; c += 32) {
-        const uint4 v = xr[c];
-        const uint4 g = gamma[c];
-        const uint32_t w[4] = {v.x, v.y, v.z, v.w};
-        const uint32_t gw[4] = {g.x, g.y, g.z, g.w};
-        uint32_t o[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-            const float a = __fmul_rn(__fmul_rn(bf16_lo(w[e]), rinv), bf16_lo(gw[e]));
-            const float b = __fmul_rn(__fmul_rn(bf16_hi(w[e]), rinv), bf16_hi(gw[e]));
-            o[e] = pack_bf16x2(a, b);
+    if (cached) {
+        store_block(0, rinv);
+    } else {
+        for (int base = 0; base < d8; base += kBlock) {
+            load_block(base, true);
+            store_block(base, rinv);
         }
-        yr[c] = make_uint4(o[0], o[1], o[2], o[3]);
     }
 }
 
-cudaError_t launch_rmsnorm(const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y, int64_t rows,
-                           int32_t d, float eps, cudaStream_t s) {
+cudaError_t launch_rmsnorm(const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y, int64_t rows, int32_t d, float eps,
+                           cudaStream_t s, const int32_t* src_rows) {
     if (rows <= 0) return cudaSuccess;
-    const int64_t blocks = (rows + kNormWarps - 1) / kNormWarps;
-    rmsnorm_kernel<<<static_cast<unsigned>(blocks), kNormWarps * 32, 0, s>>>(
-        reinterpret_cast<const uint4*>(x), reinterpret_cast<const uint4*>(gamma),
-        reinterpret_cast<uint4*>(y), rows, d / 8, eps, static_cast<float>(d));
-    return cudaGetLastError();
+    const dim3 grid(static_cast<unsigned>((rows + kNormWarps - 1) / kNormWarps));
+    const dim3 block(kNormWarps * 32);
+    const int32_t d8 = d / 8;
+    auto go = [&](auto kernel) {
+        return launch_pdl(kernel, grid, block, 0, s, reinterpret_cast<const uint4*>(x),
+                          reinterpret_cast<const uint4*>(gamma), reinterpret_cast<uint4*>(y), rows, d8, eps,
+                          static_cast<float>(d), src_rows);
+    };
+    if (d8 <= 32) return go(rmsnorm_kernel<1>);
+    if (d8 <= 64) return go(rmsnorm_kernel<2>);
+    if (d8 <= 128) return go(rmsnorm_kernel<4>);
+    if (d8 <= 256) return go(rmsnorm_kernel<8>);
+    return go(rmsnorm_kernel<16>);
 }
 
 // ---------------------------------------------------------------------------
@@ -69,6 +117,8 @@ cudaError_t launch_rmsnorm(const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y, i
 // ---------------------------------------------------------------------------
 __global__ void embed_kernel(const uint4* __restrict__ E, const int32_t* __restrict__ ids,
                              uint4* __restrict__ x, int32_t V, int32_t d8, int32_t* status) {
+    pdl_trigger();
+    pdl_wait();
     const int32_t t = blockIdx.x;
     const int32_t id = ids[t];
     const bool ok = id >= 0 && id < V;
@@ -80,9 +130,8 @@ __global__ void embed_kernel(const uint4* __restrict__ E, const int32_t* __restr
 cudaError_t launch_embed(const bi_bf16* E, const int32_t* ids, bi_bf16* x, int32_t T, int32_t V,
                          int32_t d, int32_t* status, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
-    embed_kernel<<<T, 128, 0, s>>>(reinterpret_cast<const uint4*>(E), ids,
-                                   reinterpret_cast<uint4*>(x), V, d / 8, status);
-    return cudaGetLastError();
+    return launch_pdl(embed_kernel, dim3(T), dim3(128), 0, s, reinterpret_cast<const uint4*>(E), ids,
+                      reinterpret_cast<uint4*>(x), V, d / 8, status);
 }
 
 // ---------------------------------------------------------------------------
@@ -92,15 +141,23 @@ cudaError_t launch_embed(const bi_bf16* E, const int32_t* ids, bi_bf16* x, int32
 //   out[i + Dh/2] = x[i + Dh/2] * cos + x[i] * sin
 // (each product rounded, then the sum: no fused multiply-add).
 // ---------------------------------------------------------------------------
-__global__ void __launch_bounds__(256)
+// One thread per rotated pair: grid (T, ceil((H + 2 Hkv) * Dh/2 / 128)).
+constexpr int kRopeThreads = 128;
+
+__global__ void __launch_bounds__(kRopeThreads)
 rope_append_kernel(const float* __restrict__ qkv, const int32_t* __restrict__ tok_req,
                    const int32_t* __restrict__ tok_pos, const float* __restrict__ rc,
                    const float* __restrict__ rs, int32_t max_pos, uint16_t* __restrict__ q_out,
                    uint16_t* __restrict__ kc, uint16_t* __restrict__ vc,
                    const int32_t* __restrict__ page_table, int32_t max_pages, int32_t num_pages,
                    int32_t H, int32_t Hkv, int32_t Dh, int32_t* status) {
+    pdl_trigger();
+    pdl_wait();
     const int32_t t = blockIdx.x;
     const int32_t half = Dh / 2;
+    const int32_t w = static_cast<int32_t>(blockIdx.y) * kRopeThreads + threadIdx.x;
+    if (w >= (H + 2 * Hkv) * half) return;
+    const bool reporter = blockIdx.y == 0 && threadIdx.x == 0;
     const int32_t pos = tok_pos[t];
     const int32_t req = tok_req[t];
     bool ok = pos >= 0 && pos < max_pos && (pos / BI_PAGE) < max_pages;
@@ -108,44 +165,39 @@ rope_append_kernel(const float* __restrict__ qkv, const int32_t* __restrict__ to
     if (ok) {
         page = page_table[static_cast<int64_t>(req) * max_pages + pos / BI_PAGE];
         if (page < 0 || page >= num_pages) {
-            if (threadIdx.x == 0) report(status, BI_DEV_BAD_PAGE);
+            if (reporter) report(status, BI_DEV_BAD_PAGE);
             ok = false;
         }
-    } else if (threadIdx.x == 0) {
+    } else if (reporter) {
         report(status, BI_DEV_BAD_POSITION);
     }
     const int32_t slot = pos & (BI_PAGE - 1);
-    const int32_t nqkv = (H + 2 * Hkv) * Dh;
-    const float* row = qkv + static_cast<int64_t>(t) * nqkv;
-    const int32_t work = (H + 2 * Hkv) * half;
-    for (int32_t w = threadIdx.x; w < work; w += blockDim.x) {
-        const int32_t head = w / half;
-        const int32_t i = w - head * half;
-        const float x0 = row[head * Dh + i];
-        const float x1 = row[head * Dh + i + half];
-        float r0, r1;
-        if (head < H + Hkv) {
-            const float c = ok ? rc[static_cast<int64_t>(pos) * half + i] : 1.0f;
-            const float sn = ok ? rs[static_cast<int64_t>(pos) * half + i] : 0.0f;
-            r0 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, sn));
-            r1 = __fadd_rn(__fmul_rn(x1, c), __fmul_rn(x0, sn));
-        } else {
-            r0 = x0;
-            r1 = x1;
-        }
-        const uint16_t b0 = f32_to_bf16(r0), b1 = f32_to_bf16(r1);
-        if (head < H) {
-            uint16_t* qo = q_out + (static_cast<int64_t>(t) * H + head) * Dh;
-            qo[i] = b0;
-            qo[i + half] = b1;
-        } else if (ok) {
-            const bool is_k = head < H + Hkv;
-            const int32_t g = is_k ? head - H : head - H - Hkv;
-            uint16_t* dst = (is_k ? kc : vc) +
-                            ((static_cast<int64_t>(page) * Hkv + g) * BI_PAGE + slot) * Dh;
-            dst[i] = b0;
-            dst[i + half] = b1;
-        }
+    const int32_t head = w / half;
+    const int32_t i = w - head * half;
+    const float* row = qkv + static_cast<int64_t>(t) * ((H + 2 * Hkv) * Dh);
+    const float x0 = row[head * Dh + i];
+    const float x1 = row[head * Dh + i + half];
+    float r0, r1;
+    if (head < H + Hkv) {
+        const float c = ok ? rc[static_cast<int64_t>(pos) * half + i] : 1.0f;
+        const float sn = ok ? rs[static_cast<int64_t>(pos) * half + i] : 0.0f;
+        r0 = __fsub_rn(__fmul_rn(x0, c), __fmul_rn(x1, sn));
+        r1 = __fadd_rn(__fmul_rn(x1, c), __fmul_rn(x0, sn));
+    } else {
+        r0 = x0;
+        r1 = x1;
+    }
+    const uint16_t b0 = f32_to_bf16(r0), b1 = f32_to_bf16(r1);
+    if (head < H) {
+        uint16_t* qo = q_out + (static_cast<int64_t>(t) * H + head) * Dh;
+        qo[i] = b0;
+        qo[i + half] = b1;
+    } else if (ok) {
+        const bool is_k = head < H + Hkv;
+        const int32_t g = is_k ? head - H : head - H - Hkv;
+        uint16_t* dst = (is_k ? kc : vc) + ((static_cast<int64_t>(page) * Hkv + g) * BI_PAGE + slot) * Dh;
+        dst[i] = b0;
+        dst[i + half] = b1;
     }
 }
 
@@ -155,9 +207,10 @@ cudaError_t launch_rope_kv_append(const float* qkv, const int32_t* tok_req, cons
                                   int32_t max_pages, int32_t num_pages, int32_t T, int32_t H,
                                   int32_t Hkv, int32_t Dh, int32_t* status, cudaStream_t s) {
     if (T <= 0) return cudaSuccess;
-    rope_append_kernel<<<T, 256, 0, s>>>(qkv, tok_req, tok_pos, rc, rs, max_pos, q_out, kc, vc,
-                                         page_table, max_pages, num_pages, H, Hkv, Dh, status);
-    return cudaGetLastError();
+    const int32_t work = (H + 2 * Hkv) * (Dh / 2);
+    const dim3 grid(T, (work + kRopeThreads - 1) / kRopeThreads);
+    return launch_pdl(rope_append_kernel, grid, dim3(kRopeThreads), 0, s, qkv, tok_req, tok_pos, rc, rs, max_pos,
+                      q_out, kc, vc, page_table, max_pages, num_pages, H, Hkv, Dh, status);
 }
 
 // ---------------------------------------------------------------------------
@@ -174,15 +227,38 @@ __device__ __forceinline__ bool beats(float a, int32_t ia, float b, int32_t ib) 
 }
 
 constexpr int kArgmaxThreads = 1024;
+constexpr int kArgmaxUnroll = 8;  // 16-byte loads in flight per thread
 
 __global__ void __launch_bounds__(kArgmaxThreads)
-argmax_kernel(const float* __restrict__ logits, int32_t* __restrict__ out, int32_t V) {
+argmax_kernel(const float* __restrict__ logits, int32_t* __restrict__ out, int32_t V, int32_t nv) {
+    pdl_trigger();
+    pdl_wait();
     __shared__ float sv[kArgmaxThreads / 32];
     __shared__ int32_t si[kArgmaxThreads / 32];
     const float* row = logits + static_cast<int64_t>(blockIdx.x) * V;
     float bv = -INFINITY;
     int32_t bi = 0x7fffffff;
-    for (int32_t j = threadIdx.x; j < V; j += kArgmaxThreads) {
+    // nv > 0: the row is read as nv aligned float4s, then the V - 4 nv tail
+    const float4* row4 = reinterpret_cast<const float4*>(row);
+    for (int32_t base = 0; base < nv; base += kArgmaxUnroll * kArgmaxThreads) {
+        float4 a[kArgmaxUnroll];
+#pragma unroll
+        for (int u = 0; u < kArgmaxUnroll; ++u) {
+            const int32_t q = base + u * kArgmaxThreads + static_cast<int32_t>(threadIdx.x);
+            if (q < nv) a[u] = row4[q];
+        }
+#pragma unroll
+        for (int u = 0; u < kArgmaxUnroll; ++u) {
+            const int32_t q = base + u * kArgmaxThreads + static_cast<int32_t>(threadIdx.x);
+            if (q < nv) {
+                const float v4[4] = {a[u].x, a[u].y, a[u].z, a[u].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e)
+                    if (beats(v4[e], 4 * q + e, bv, bi)) { bv = v4[e]; bi = 4 * q + e; }
+            }
+        }
+    }
+    for (int32_t j = 4 * nv + static_cast<int32_t>(threadIdx.x); j < V; j += kArgmaxThreads) {
         const float v = row[j];
         if (beats(v, j, bv, bi)) { bv = v; bi = j; }
     }
@@ -210,15 +286,18 @@ argmax_kernel(const float* __restrict__ logits, int32_t* __restrict__ out, int32
 
 cudaError_t launch_argmax(const float* logits, int32_t* out, int32_t R, int32_t V, cudaStream_t s) {
     if (R <= 0) return cudaSuccess;
-    argmax_kernel<<<R, kArgmaxThreads, 0, s>>>(logits, out, V);
-    return cudaGetLastError();
+    // every row starts 16-byte aligned when the base is and V % 4 == 0
+    const bool vec = (reinterpret_cast<uintptr_t>(logits) & 15u) == 0 && V % 4 == 0;
+    return launch_pdl(argmax_kernel, dim3(R), dim3(kArgmaxThreads), 0, s, logits, out, V, vec ? V / 4 : 0);
 }
 
 // ---------------------------------------------------------------------------
-// Gate/up interleave and row gather (plain copies).
+// Gate/up interleave (a plain copy).
 // ---------------------------------------------------------------------------
 __global__ void pack_gate_up_kernel(const uint4* __restrict__ g, const uint4* __restrict__ u,
                                     uint4* __restrict__ gu, int32_t d8) {
+    pdl_trigger();
+    pdl_wait();
     const int32_t r = blockIdx.x;  // output row in [0, 2F)
     const int32_t j = r / (2 * BI_SWIGLU_GROUP), w = r % (2 * BI_SWIGLU_GROUP);
     const uint4* src = (w < BI_SWIGLU_GROUP ? g : u) +
@@ -229,26 +308,8 @@ __global__ void pack_gate_up_kernel(const uint4* __restrict__ g, const uint4* __
 cudaError_t launch_pack_gate_up(const bi_bf16* g, const bi_bf16* u, bi_bf16* gu, int32_t F,
                                 int32_t d, cudaStream_t s) {
     if (F <= 0) return cudaSuccess;
-    pack_gate_up_kernel<<<2 * F, 256, 0, s>>>(reinterpret_cast<const uint4*>(g),
-                                             reinterpret_cast<const uint4*>(u),
-                                             reinterpret_cast<uint4*>(gu), d / 8);
-    return cudaGetLastError();
-}
-
-__global__ void gather_rows_kernel(const uint4* __restrict__ x, const int32_t* __restrict__ rows,
-                                   uint4* __restrict__ out, int32_t d8) {
-    const int32_t r = blockIdx.x;
-    const int64_t src = rows[r];
-    for (int c = threadIdx.x; c < d8; c += blockDim.x)
-        out[static_cast<int64_t>(r) * d8 + c] = x[src * d8 + c];
-}
-
-cudaError_t launch_gather_rows(const bi_bf16* x, const int32_t* rows, bi_bf16* out, int32_t R,
-                               int32_t d, cudaStream_t s) {
-    if (R <= 0) return cudaSuccess;
-    gather_rows_kernel<<<R, 128, 0, s>>>(reinterpret_cast<const uint4*>(x), rows,
-                                         reinterpret_cast<uint4*>(out), d / 8);
-    return cudaGetLastError();
+    return launch_pdl(pack_gate_up_kernel, dim3(2 * F), dim3(256), 0, s, reinterpret_cast<const uint4*>(g),
+                      reinterpret_cast<const uint4*>(u), reinterpret_cast<uint4*>(gu), d / 8);
 }
 
 }  // namespace bi
