@@ -469,11 +469,14 @@ extern "C" bi_status bi_forward_step(bi_model* m, const bi_batch* batch, const b
     if (dec_splits > L.dec_splits) return fail(BI_ERR_SHAPE, "bi_forward_step: split plan exceeds workspace");
     float* dec_ml = dec_o + static_cast<size_t>(std::max(nd, 1)) * c.H * dec_splits * c.Dh;
 
-    BI_TRY_CUDA(launch_embed(m->embed, b.token_ids, x, T, c.V, c.d, dev_status, s), "embed");
+    // The step's first kernel waits for all earlier work on the stream; every
+    // later kernel of the step starts after it, so weights (never written
+    // within a step) may be fetched before each kernel's dependency wait.
+    BI_TRY_CUDA(launch_embed(m->embed, b.token_ids, x, T, c.V, c.d, dev_status, s, /*after_all=*/true), "embed");
     for (int l = 0; l < c.n_layers; ++l) {
         BI_TRY_CUDA(launch_rmsnorm(x, m->gamma_attn[l], y, T, c.d, c.eps, s), "rmsnorm");
         BI_TRY(run_gemm(y, m->w_qkv[l], qkv, BI_F32, nullptr, BI_EP_NONE, T, nqkv, c.d, mode, gws, gws_bytes,
-                        dev_status, s));
+                        dev_status, s, true));
         BI_TRY_CUDA(launch_rope_kv_append(qkv, d_req, d_pos, m->rope_cos, m->rope_sin, c.max_pos, q, kv->k[l],
                                           kv->v[l], b.page_table, b.max_pages, kv->num_pages, T, c.H, c.Hkv, c.Dh,
                                           dev_status, s),
@@ -489,12 +492,12 @@ extern "C" bi_status bi_forward_step(bi_model* m, const bi_batch* batch, const b
             BI_TRY_CUDA(launch_prefill_attention(g, em, T - nd, s), "prefill attention");
         }
         BI_TRY(run_gemm(attn, m->w_o[l], x, BI_BF16, x, BI_EP_RESIDUAL, T, c.d, c.H * c.Dh, mode, gws, gws_bytes,
-                        dev_status, s));
+                        dev_status, s, true));
         BI_TRY_CUDA(launch_rmsnorm(x, m->gamma_ffn[l], y, T, c.d, c.eps, s), "rmsnorm");
         BI_TRY(run_gemm(y, m->w_gu[l], h, BI_BF16, nullptr, BI_EP_SWIGLU, T, 2 * c.F, c.d, mode, gws, gws_bytes,
-                        dev_status, s));
+                        dev_status, s, true));
         BI_TRY(run_gemm(h, m->w_down[l], x, BI_BF16, x, BI_EP_RESIDUAL, T, c.d, c.F, mode, gws, gws_bytes,
-                        dev_status, s));
+                        dev_status, s, true));
     }
     if (hidden_out)
         BI_TRY_CUDA(cudaMemcpyAsync(hidden_out, x, static_cast<size_t>(T) * c.d * 2, cudaMemcpyDeviceToDevice, s),
@@ -504,7 +507,7 @@ extern "C" bi_status bi_forward_step(bi_model* m, const bi_batch* batch, const b
         float* logits = logits_out ? logits_out : reinterpret_cast<float*>(base + L.logits);
         BI_TRY_CUDA(launch_rmsnorm(x, m->gamma_final, yr, b.R, c.d, c.eps, s, d_rows), "final rmsnorm");
         BI_TRY(run_gemm(yr, m->w_lm, logits, BI_F32, nullptr, BI_EP_NONE, b.R, c.V, c.d, mode, gws, gws_bytes,
-                        dev_status, s));
+                        dev_status, s, true));
         if (tokens_out) BI_TRY_CUDA(launch_argmax(logits, tokens_out, b.R, c.V, s), "argmax");
     }
     return BI_OK;

@@ -15,8 +15,8 @@ namespace bi {
 // griddepcontrol.wait (pdl_wait in common.cuh), which every kernel of this
 // library executes before touching shared global data.
 template <typename... P, typename... A>
-inline cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
-                              A&&... args) {
+inline cudaError_t launch_k(bool pdl, void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                            A&&... args) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = grid;
     cfg.blockDim = block;
@@ -26,9 +26,14 @@ inline cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_
     attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
     attr[0].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = attr;
-    cfg.numAttrs = 1;
+    cfg.numAttrs = pdl ? 1 : 0;
     const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<A&&>(args)...);
     return e != cudaSuccess ? e : cudaGetLastError();
+}
+template <typename... P, typename... A>
+inline cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                              A&&... args) {
+    return launch_k(true, kernel, grid, block, smem, s, static_cast<A&&>(args)...);
 }
 
 // thread-local error message (api.cu)
@@ -41,8 +46,11 @@ int num_sms();
 // rows: output rows; src_rows (device, optional): output row r normalises input row src_rows[r]
 cudaError_t launch_rmsnorm(const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y, int64_t rows,
                            int32_t d, float eps, cudaStream_t s, const int32_t* src_rows = nullptr);
+// after_all: launch without programmatic serialisation, so the kernel (and
+// every kernel chained after it) starts only once all earlier work on the
+// stream has finished.
 cudaError_t launch_embed(const bi_bf16* E, const int32_t* ids, bi_bf16* x, int32_t T, int32_t V,
-                         int32_t d, int32_t* status, cudaStream_t s);
+                         int32_t d, int32_t* status, cudaStream_t s, bool after_all = false);
 cudaError_t launch_rope_kv_append(const float* qkv, const int32_t* tok_req, const int32_t* tok_pos,
                                   const float* rc, const float* rs, int32_t max_pos, bi_bf16* q_out,
                                   bi_bf16* kc, bi_bf16* vc, const int32_t* page_table,
@@ -93,8 +101,12 @@ struct GemmPlan {
 };
 GemmPlan gemm_plan(int64_t M, int32_t N, int32_t K, bi_mode mode);
 size_t gemm_ws_bytes(int64_t M, int32_t N, int32_t K, bi_mode mode);
+// weights_settled: no kernel that may still be running when this one starts
+// writes W (true inside bi_forward_step, whose first kernel waits for all
+// earlier work on the stream), so W may be fetched before the dependency wait.
 bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype,
                    const bi_bf16* residual, bi_epilogue ep, int64_t M, int32_t N, int32_t K,
-                   bi_mode mode, void* ws, size_t ws_bytes, int32_t* status, cudaStream_t s);
+                   bi_mode mode, void* ws, size_t ws_bytes, int32_t* status, cudaStream_t s,
+                   bool weights_settled = false);
 
 }  // namespace bi

@@ -54,11 +54,9 @@ constexpr int kGemmThreads = 256;
 constexpr int kAFull = kBM * kBK * 2;  // bytes the MMA reads for A per K tile (16 KB)
 constexpr int kGroupM = 16;            // M tiles per rasterisation band
 constexpr int kBarrierBytes = 1024;
+constexpr int kRingBudget = 212 * 1024;  // shared memory for the A and W rings
+constexpr int kMaxSmem = 227 * 1024;
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBM, kUN);
-// L2 prefetch of weights before the dependency wait: at most this many bytes
-// per CTA, and at most kPrefetchTotal over the grid (L2 holds 126 MB).
-constexpr int64_t kPrefetchPerCta = 1 << 20;
-constexpr int64_t kPrefetchTotal = 64ll << 20;
 
 struct GemmArgs {
     void* C;
@@ -76,6 +74,7 @@ struct GemmArgs {
     int32_t a_region;      // bytes of the A region (slots + pad for the last window)
     int32_t stages;        // ring stages
     int32_t kps;           // 64-deep K tiles per stage
+    int32_t w_early;       // 1: W may be read before the dependency wait (no earlier kernel writes it)
     int32_t* status;
 };
 
@@ -209,23 +208,32 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
-
-    if (warp == 0 && lane == 0 && static_cast<int32_t>(blockIdx.x) < args.total_tiles) {
-        // weights of the first tile into L2 while the previous kernel drains
-        int32_t m_tile, n_tile;
-        tile_coords(blockIdx.x, m_tile, n_tile);
-        const int64_t budget = min(kPrefetchPerCta, kPrefetchTotal / (static_cast<int64_t>(gridDim.x) * gridDim.y));
-        const int32_t nk = static_cast<int32_t>(budget / kWBytes < nkb ? budget / kWBytes : nkb);
-        for (int32_t kb = 0; kb < nk; ++kb) ptx::tma_prefetch_l2_2d(&tmW, (kb0 + kb) * kBK, n_tile * BN);
-    }
-    pdl_wait();
+    if (!(warp == 0 && lane == 0)) pdl_wait();  // the producer waits in its role below
 
     if (warp == 0) {
         if (lane == 0) {
-            // ---- TMA producer: per stage, kps K tiles of A and of W ----
+            // ---- TMA producer: per stage one box of A and one of W, each kps K tiles deep ----
             const uint64_t pol_w = ptx::policy_evict_first();  // weights stream through once
             const uint64_t pol_a = ptx::policy_evict_last();   // activations are re-read by every N tile
-            const uint32_t a_tx = static_cast<uint32_t>(args.a_box_rows) * kBK * 2;
+            // a box always lands whole (out-of-range rows and K tiles are zero-filled)
+            const uint32_t stage_tx = static_cast<uint32_t>(kps) * (static_cast<uint32_t>(args.a_stride) + kWBytes);
+            // Weights do not depend on the kernel before this one: when the
+            // caller guarantees that nothing still in flight writes them, the
+            // first tile's first stages of W are requested before the
+            // dependency wait and only A waits for the previous kernel.
+            uint32_t pre = 0;
+            if (args.w_early && static_cast<int32_t>(blockIdx.x) < args.total_tiles) {
+                int32_t m_tile, n_tile;
+                tile_coords(blockIdx.x, m_tile, n_tile);
+                const int32_t first_stages = (nkb + kps - 1) / kps;
+                pre = static_cast<uint32_t>(min(S, first_stages));
+                for (uint32_t q = 0; q < pre; ++q) {
+                    ptx::mbar_arrive_expect_tx(&full[q], stage_tx);
+                    ptx::tma_load_3d(sW + q * kps * kWBytes, &tmW, &full[q], 0, n_tile * BN,
+                                     kb0 + static_cast<int32_t>(q) * kps, pol_w);
+                }
+            }
+            pdl_wait();
             uint32_t issued = 0;  // stages issued
             int s = 0;            // stage and its phase, advanced incrementally
             uint32_t ph = 0;
@@ -234,19 +242,21 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 int32_t m_tile, n_tile;
                 tile_coords(tile, m_tile, n_tile);
                 for (int32_t kb = 0; kb < nkb; kb += kps) {
-                    const int cnt = min(kps, nkb - kb);
-                    if (!ptx::mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag)) {
-                        if (!*abort_flag) report(args.status, BI_DEV_TIMEOUT_PRODUCER);
-                        *abort_flag = 1;
-                        ok = false;
-                        break;
-                    }
-                    ptx::mbar_arrive_expect_tx(&full[s], static_cast<uint32_t>(cnt) * (a_tx + kWBytes));
-                    for (int j = 0; j < cnt; ++j) {
-                        const int32_t kx = (kb0 + kb + j) * kBK;
-                        const int slot = s * kps + j;
-                        ptx::tma_load_2d(sA + slot * args.a_stride, &tmA, &full[s], kx, m_tile * kBM, pol_a);
-                        ptx::tma_load_2d(sW + slot * kWBytes, &tmW, &full[s], kx, n_tile * BN, pol_w);
+                    if (issued < pre) {
+                        // armed, W already requested: only A is missing
+                        ptx::tma_load_3d(sA + s * kps * args.a_stride, &tmA, &full[s], 0, m_tile * kBM, kb0 + kb,
+                                         pol_a);
+                    } else {
+                        if (!ptx::mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag)) {
+                            if (!*abort_flag) report(args.status, BI_DEV_TIMEOUT_PRODUCER);
+                            *abort_flag = 1;
+                            ok = false;
+                            break;
+                        }
+                        ptx::mbar_arrive_expect_tx(&full[s], stage_tx);
+                        ptx::tma_load_3d(sA + s * kps * args.a_stride, &tmA, &full[s], 0, m_tile * kBM, kb0 + kb,
+                                         pol_a);
+                        ptx::tma_load_3d(sW + s * kps * kWBytes, &tmW, &full[s], 0, n_tile * BN, kb0 + kb, pol_w);
                     }
                     ++issued;
                     if (++s == S) {
@@ -418,15 +428,21 @@ static PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
     return fn;
 }
 
-// Row-major [rows, K] bf16 matrix, box of box_rows x 64 with 128-byte swizzle.
-static bool make_kmajor_map(CUtensorMap* map, const void* base, uint64_t K, uint64_t rows, uint32_t box_rows) {
+// Row-major [rows, K] bf16 matrix seen as three dimensions (64 elements of a
+// K tile, row, K tile), so that one box of (64, box_rows, depth) brings
+// `depth` consecutive K tiles of box_rows rows, each tile laid out as rows of
+// 128 bytes with the 128-byte swizzle (the layout the MMA descriptors read).
+// One large copy per operand and ring stage keeps enough bytes in flight per
+// SM; small copies are limited by how fast one thread can re-arm and issue.
+static bool make_kslab_map(CUtensorMap* map, const void* base, uint64_t K, uint64_t rows, uint32_t box_rows,
+                           uint32_t depth) {
     auto fn = encode_fn();
     if (!fn) return false;
-    cuuint64_t dims[2] = {K, rows};
-    cuuint64_t strides[1] = {K * 2};
-    cuuint32_t box[2] = {static_cast<cuuint32_t>(kBK), box_rows};
-    cuuint32_t estr[2] = {1, 1};
-    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(kBK), rows, K / kBK};
+    cuuint64_t strides[2] = {K * 2, static_cast<cuuint64_t>(kBK) * 2};
+    cuuint32_t box[3] = {static_cast<cuuint32_t>(kBK), box_rows, depth};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
               CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -462,7 +478,7 @@ struct Layout {
 
 // Layout of one launch.  Only data movement depends on M here; the MMA
 // sequence of every output element is the same for all layouts.
-Layout choose_layout(int64_t M, int32_t N) {
+Layout choose_layout(int64_t M, int32_t N, int32_t K) {
     Layout L{};
     L.bn = (M > 2 * kBM && N % 256 == 0 && 256 % kUN == 0) ? 256 : kUN;
     int32_t box = 16;
@@ -470,11 +486,13 @@ Layout choose_layout(int64_t M, int32_t N) {
     if (L.bn == 256) box = kBM;
     L.a_box = box;
     L.a_stride = box * kBK * 2;
-    L.kps = L.bn == 256 ? 1 : 2;
     const int32_t w_tile = L.bn * kBK * 2;
     const int32_t pad = kAFull - L.a_stride;  // the last slot's 128-row window reaches this far past it
-    const int32_t budget = 212 * 1024 - pad;
-    int32_t stages = budget / (L.kps * (L.a_stride + w_tile));
+    const int32_t budget = kRingBudget - pad;
+    const int32_t per_k = L.a_stride + w_tile;  // bytes of one K tile of A and W
+    // deep stages (one large copy per operand) while at least two still fit
+    L.kps = std::max(1, std::min({L.bn == 256 ? 2 : 4, K / kBK, budget / (2 * per_k)}));
+    int32_t stages = budget / (L.kps * per_k);
     stages = std::min(std::max(stages, 2), kMaxStages);
     L.stages = stages;
     L.a_region = stages * L.kps * L.a_stride + pad;
@@ -491,8 +509,7 @@ cudaError_t launch_tiles(const CUtensorMap& tmA, const CUtensorMap& tmW, const G
         static std::once_flag once;
         static cudaError_t err = cudaSuccess;
         std::call_once(once, [] {
-            err = cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       227 * 1024);
+            err = cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
         });
         if (err != cudaSuccess) return err;
         return launch_pdl(gemm_tc_kernel<BN>, grid, dim3(kGemmThreads), smem, s, tmA, tmW, a);
@@ -503,16 +520,19 @@ cudaError_t launch_tiles(const CUtensorMap& tmA, const CUtensorMap& tmW, const G
 
 bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype, const bi_bf16* residual,
                    bi_epilogue ep, int64_t M, int32_t N, int32_t K, bi_mode mode, void* ws, size_t ws_bytes,
-                   int32_t* status, cudaStream_t s) {
+                   int32_t* status, cudaStream_t s, bool weights_settled) {
     if (M == 0) return BI_OK;
     const GemmPlan plan = gemm_plan(M, N, K, mode);
-    const Layout L = choose_layout(M, N);
+    const Layout L = choose_layout(M, N, K);
 
+    if (L.smem > static_cast<size_t>(kMaxSmem)) return fail(BI_ERR_UNSUPPORTED, "bi_gemm: no ring layout fits");
     const int32_t nkb = K / kBK;
     const int32_t per = (nkb + plan.splits - 1) / plan.splits;
     CUtensorMap tmA, tmW;
-    if (!make_kmajor_map(&tmA, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), static_cast<uint32_t>(L.a_box)) ||
-        !make_kmajor_map(&tmW, W, static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint32_t>(L.bn)))
+    if (!make_kslab_map(&tmA, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), static_cast<uint32_t>(L.a_box),
+                        static_cast<uint32_t>(L.kps)) ||
+        !make_kslab_map(&tmW, W, static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint32_t>(L.bn),
+                        static_cast<uint32_t>(L.kps)))
         return fail(BI_ERR_CUDA, "cuTensorMapEncodeTiled failed");
 
     GemmArgs a{};
@@ -528,6 +548,7 @@ bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype
     a.a_region = L.a_region;
     a.stages = L.stages;
     a.kps = L.kps;
+    a.w_early = weights_settled ? 1 : 0;
     a.status = status;
     if (plan.splits > 1) {
         if (ws == nullptr || ws_bytes < gemm_ws_bytes(M, N, K, mode) || (reinterpret_cast<uintptr_t>(ws) & 15u))

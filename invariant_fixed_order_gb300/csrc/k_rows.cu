@@ -128,10 +128,10 @@ __global__ void embed_kernel(const uint4* __restrict__ E, const int32_t* __restr
 }
 
 cudaError_t launch_embed(const bi_bf16* E, const int32_t* ids, bi_bf16* x, int32_t T, int32_t V,
-                         int32_t d, int32_t* status, cudaStream_t s) {
+                         int32_t d, int32_t* status, cudaStream_t s, bool after_all) {
     if (T <= 0) return cudaSuccess;
-    return launch_pdl(embed_kernel, dim3(T), dim3(128), 0, s, reinterpret_cast<const uint4*>(E), ids,
-                      reinterpret_cast<uint4*>(x), V, d / 8, status);
+    return launch_k(!after_all, embed_kernel, dim3(T), dim3(128), 0, s, reinterpret_cast<const uint4*>(E), ids,
+                    reinterpret_cast<uint4*>(x), V, d / 8, status);
 }
 
 // ---------------------------------------------------------------------------
