@@ -324,7 +324,7 @@ extern "C" void bi_model_destroy(bi_model* m) {
 namespace {
 
 struct FwdLayout {
-    size_t x, y, qkv, q, attn, h, yr, logits, meta, dec_ws, gemm_ws, total;
+    size_t x, y, qkv, q, attn, h, yr, logits, am_keys, am_counter, meta, dec_ws, gemm_ws, total;
     int32_t dec_splits;
 };
 
@@ -345,6 +345,8 @@ FwdLayout fwd_layout(const bi_model_config& c, int32_t T, int32_t B, int32_t R, 
     L.h = take(static_cast<size_t>(T) * c.F * 2);
     L.yr = take(static_cast<size_t>(R) * c.d * 2);
     L.logits = take(static_cast<size_t>(R) * c.V * 4);
+    L.am_keys = take(static_cast<size_t>(R) * 8);
+    L.am_counter = take(16);
     L.meta = take((static_cast<size_t>(T) * 4 + R + 16) * 4);
     L.dec_splits = std::max(invariant_max_splits(max_seq), 16);
     L.dec_ws = take(decode_ws_bytes(B, c.H, c.Dh, L.dec_splits));
@@ -504,11 +506,17 @@ extern "C" bi_status bi_forward_step(bi_model* m, const bi_batch* batch, const b
                     "hidden copy");
     if (b.R > 0 && (logits_out || tokens_out)) {
         bi_bf16* yr = reinterpret_cast<bi_bf16*>(base + L.yr);
-        float* logits = logits_out ? logits_out : reinterpret_cast<float*>(base + L.logits);
-        BI_TRY_CUDA(launch_rmsnorm(x, m->gamma_final, yr, b.R, c.d, c.eps, s, d_rows), "final rmsnorm");
+        // greedy tokens come straight out of the LM head's epilogue unless the
+        // batch-variant plan splits its K (then the argmax reads stored logits)
+        const bool fuse = tokens_out != nullptr && gemm_plan(b.R, c.V, c.d, mode).splits == 1;
+        ArgmaxFuse am{reinterpret_cast<unsigned long long*>(base + L.am_keys), tokens_out,
+                      reinterpret_cast<unsigned int*>(base + L.am_counter)};
+        float* logits = logits_out ? logits_out : fuse ? nullptr : reinterpret_cast<float*>(base + L.logits);
+        BI_TRY_CUDA(launch_rmsnorm(x, m->gamma_final, yr, b.R, c.d, c.eps, s, d_rows, fuse ? &am : nullptr),
+                    "final rmsnorm");
         BI_TRY(run_gemm(yr, m->w_lm, logits, BI_F32, nullptr, BI_EP_NONE, b.R, c.V, c.d, mode, gws, gws_bytes,
-                        dev_status, s, true));
-        if (tokens_out) BI_TRY_CUDA(launch_argmax(logits, tokens_out, b.R, c.V, s), "argmax");
+                        dev_status, s, true, fuse ? &am : nullptr));
+        if (tokens_out && !fuse) BI_TRY_CUDA(launch_argmax(logits, tokens_out, b.R, c.V, s), "argmax");
     }
     return BI_OK;
 }

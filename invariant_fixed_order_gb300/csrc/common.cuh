@@ -59,6 +59,26 @@ __device__ __forceinline__ uint4 ld_nc_v4(const void* p) {
 }
 
 // ---------------------------------------------------------------------------
+// Greedy argmax as a 64-bit key ("temperature=0 means deterministic").
+// (value, index) pairs are totally ordered: a NaN beats every number, a
+// larger number beats a smaller one, and between equal values (-0 equals +0)
+// or two NaNs the lower index wins.  argmax_key maps a pair to an unsigned
+// key whose minimum over a row is the winner, so the winner can be taken
+// with atomicMin in any order and still be unique.
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ unsigned long long argmax_key(float v, int32_t idx) {
+    uint32_t hi = 0u;  // NaN
+    if (!isnan(v)) {
+        uint32_t b = __float_as_uint(v);
+        if (b == 0x80000000u) b = 0u;
+        const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);  // grows with v
+        hi = ~ord;  // in [1, 0xfffffffe] for every number
+    }
+    return (static_cast<unsigned long long>(hi) << 32) | static_cast<uint32_t>(idx);
+}
+constexpr unsigned long long kArgmaxKeyNone = ~0ull;  // worse than every candidate
+
+// ---------------------------------------------------------------------------
 // Programmatic dependent launch.  Every kernel of this library is launched so
 // that it may start while the kernel before it in the stream is finishing:
 // pdl_trigger() lets the next kernel start its own prologue, pdl_wait() blocks

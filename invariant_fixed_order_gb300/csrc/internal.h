@@ -43,9 +43,20 @@ bi_status cuda_fail(cudaError_t e, const char* what);
 int num_sms();
 
 // ---- elementwise / row kernels (k_rows.cu) ----
-// rows: output rows; src_rows (device, optional): output row r normalises input row src_rows[r]
+// Greedy argmax fused into an fp32 GEMM epilogue: keys[rows] (set to
+// kArgmaxKeyNone and counter to 0 before the GEMM) receive each row's winning
+// key; the last CTA writes tokens[row] and resets the counter.
+struct ArgmaxFuse {
+    unsigned long long* keys;
+    int32_t* tokens;
+    unsigned int* counter;
+};
+
+// rows: output rows; src_rows (device, optional): output row r normalises input row src_rows[r];
+// am (optional): initialise its keys[0, rows) and counter for a fused argmax that follows
 cudaError_t launch_rmsnorm(const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y, int64_t rows,
-                           int32_t d, float eps, cudaStream_t s, const int32_t* src_rows = nullptr);
+                           int32_t d, float eps, cudaStream_t s, const int32_t* src_rows = nullptr,
+                           const ArgmaxFuse* am = nullptr);
 // after_all: launch without programmatic serialisation, so the kernel (and
 // every kernel chained after it) starts only once all earlier work on the
 // stream has finished.
@@ -104,9 +115,11 @@ size_t gemm_ws_bytes(int64_t M, int32_t N, int32_t K, bi_mode mode);
 // weights_settled: no kernel that may still be running when this one starts
 // writes W (true inside bi_forward_step, whose first kernel waits for all
 // earlier work on the stream), so W may be fetched before the dependency wait.
+// am (optional, fp32 output, no epilogue, plan without split-K): fused greedy
+// argmax over each row's N outputs; C may then be null (outputs not stored).
 bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype,
                    const bi_bf16* residual, bi_epilogue ep, int64_t M, int32_t N, int32_t K,
                    bi_mode mode, void* ws, size_t ws_bytes, int32_t* status, cudaStream_t s,
-                   bool weights_settled = false);
+                   bool weights_settled = false, const ArgmaxFuse* am = nullptr);
 
 }  // namespace bi

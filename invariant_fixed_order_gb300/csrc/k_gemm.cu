@@ -55,7 +55,7 @@ constexpr int kAFull = kBM * kBK * 2;  // bytes the MMA reads for A per K tile (
 constexpr int kGroupM = 16;            // M tiles per rasterisation band
 constexpr int kBarrierBytes = 1024;
 constexpr int kRingBudget = 212 * 1024;  // shared memory for the A and W rings
-constexpr int kMaxSmem = 227 * 1024;
+constexpr int kMaxSmem = 226 * 1024;  // dynamic shared memory; the kernel's few static bytes fit beside it
 constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBM, kUN);
 
 struct GemmArgs {
@@ -75,6 +75,9 @@ struct GemmArgs {
     int32_t stages;        // ring stages
     int32_t kps;           // 64-deep K tiles per stage
     int32_t w_early;       // 1: W may be read before the dependency wait (no earlier kernel writes it)
+    unsigned long long* am_keys;  // fused greedy argmax (fp32 output only): per-row winning key, or null
+    int32_t* am_tokens;
+    unsigned int* am_counter;
     int32_t* status;
 };
 
@@ -356,14 +359,26 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             tile_coords(tile, m_tile, n_tile);
             const int64_t row = static_cast<int64_t>(m_tile) * kBM + q * 32 + lane;
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * BN);
+            unsigned long long best = kArgmaxKeyNone;
 #pragma unroll 1
             for (int j = 0; j < kChunks; ++j) {
                 uint32_t r[4][16];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) ptx::tmem_ld16(taddr + j * kEpi + c * 16, r[c]);
                 ptx::tmem_ld_wait();
-                if (row < args.M) epilogue_group(args, row, n_tile * BN + j * kEpi, split, r);
+                const int32_t n0 = n_tile * BN + j * kEpi;
+                if (row < args.M && args.C != nullptr) epilogue_group(args, row, n0, split, r);
+                if (args.am_keys != nullptr) {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c)
+#pragma unroll
+                        for (int e = 0; e < 16; ++e) {
+                            const unsigned long long key = argmax_key(__uint_as_float(r[c][e]), n0 + c * 16 + e);
+                            best = key < best ? key : best;
+                        }
+                }
             }
+            if (args.am_keys != nullptr && row < args.M) atomicMin(args.am_keys + row, best);
             ptx::tc_fence_before();
             __syncwarp();
             if (lane == 0) mbar_arrive(&acc_empty[b]);
@@ -371,12 +386,28 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
 
     // teardown: MMAs drained by the issuer, copies drained by the producers
+    if (args.am_keys != nullptr) __threadfence();  // this CTA's argmax keys before its count below
     ptx::tc_fence_before();
     __syncthreads();
     if (warp == 0) {
         __syncwarp();
         ptx::tc_fence_after();
         ptx::tmem_dealloc(tmem, kTmemCols);
+    }
+    if (args.am_keys != nullptr) {
+        // the last CTA to finish turns every row's key into its token id
+        __shared__ uint32_t am_last;
+        if (threadIdx.x == 0) {
+            const unsigned int done = atomicAdd(args.am_counter, 1u);
+            am_last = done == gridDim.x * gridDim.y - 1u ? 1u : 0u;
+        }
+        __syncthreads();
+        if (am_last) {
+            __threadfence();
+            for (int64_t r = threadIdx.x; r < args.M; r += blockDim.x)
+                args.am_tokens[r] = static_cast<int32_t>(__ldcg(args.am_keys + r) & 0xffffffffull);
+            if (threadIdx.x == 0) *args.am_counter = 0u;
+        }
     }
 }
 
@@ -520,7 +551,7 @@ cudaError_t launch_tiles(const CUtensorMap& tmA, const CUtensorMap& tmW, const G
 
 bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype, const bi_bf16* residual,
                    bi_epilogue ep, int64_t M, int32_t N, int32_t K, bi_mode mode, void* ws, size_t ws_bytes,
-                   int32_t* status, cudaStream_t s, bool weights_settled) {
+                   int32_t* status, cudaStream_t s, bool weights_settled, const ArgmaxFuse* am) {
     if (M == 0) return BI_OK;
     const GemmPlan plan = gemm_plan(M, N, K, mode);
     const Layout L = choose_layout(M, N, K);
@@ -550,6 +581,15 @@ bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype
     a.kps = L.kps;
     a.w_early = weights_settled ? 1 : 0;
     a.status = status;
+    if (am != nullptr) {
+        if (plan.splits != 1 || c_dtype != BI_F32 || ep != BI_EP_NONE)
+            return fail(BI_ERR_INVALID, "fused argmax needs an fp32 GEMM without epilogue or split-K");
+        a.am_keys = am->keys;
+        a.am_tokens = am->tokens;
+        a.am_counter = am->counter;
+    } else if (C == nullptr) {
+        return fail(BI_ERR_INVALID, "bi_gemm: null output");
+    }
     if (plan.splits > 1) {
         if (ws == nullptr || ws_bytes < gemm_ws_bytes(M, N, K, mode) || (reinterpret_cast<uintptr_t>(ws) & 15u))
             return fail(BI_ERR_WORKSPACE, "bi_gemm: variant split-K workspace too small or not 16-byte aligned");

@@ -23,12 +23,16 @@ constexpr int kNormWarps = 4;
 template <int CPL>
 __global__ void __launch_bounds__(kNormWarps * 32)
 rmsnorm_kernel(const uint4* x, const uint4* __restrict__ gamma, uint4* y, int64_t rows, int32_t d8, float eps,
-               float fd, const int32_t* __restrict__ src_rows) {
+               float fd, const int32_t* __restrict__ src_rows, unsigned long long* am_keys, unsigned int* am_counter) {
     pdl_trigger();
     pdl_wait();
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kNormWarps + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;  // uniform per warp
+    if (am_keys != nullptr && lane == 0) {
+        am_keys[row] = kArgmaxKeyNone;
+        if (row == 0) *am_counter = 0u;
+    }
     const int64_t src = src_rows != nullptr ? static_cast<int64_t>(src_rows[row]) : row;
     const uint4* xr = x + src * d8;
     uint4* yr = y + row * d8;
@@ -95,7 +99,7 @@ rmsnorm_kernel(const uint4* x, const uint4* __restrict__ gamma, uint4* y, int64_
 }
 
 cudaError_t launch_rmsnorm(const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y, int64_t rows, int32_t d, float eps,
-                           cudaStream_t s, const int32_t* src_rows) {
+                           cudaStream_t s, const int32_t* src_rows, const ArgmaxFuse* am) {
     if (rows <= 0) return cudaSuccess;
     const dim3 grid(static_cast<unsigned>((rows + kNormWarps - 1) / kNormWarps));
     const dim3 block(kNormWarps * 32);
@@ -103,7 +107,7 @@ cudaError_t launch_rmsnorm(const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y, i
     auto go = [&](auto kernel) {
         return launch_pdl(kernel, grid, block, 0, s, reinterpret_cast<const uint4*>(x),
                           reinterpret_cast<const uint4*>(gamma), reinterpret_cast<uint4*>(y), rows, d8, eps,
-                          static_cast<float>(d), src_rows);
+                          static_cast<float>(d), src_rows, am ? am->keys : nullptr, am ? am->counter : nullptr);
     };
     if (d8 <= 32) return go(rmsnorm_kernel<1>);
     if (d8 <= 64) return go(rmsnorm_kernel<2>);

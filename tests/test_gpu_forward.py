@@ -136,6 +136,42 @@ def test_tiny_prefill_chunking_bitwise(mods, tiny):
         assert sched.bitwise_equal(torch.cat(rows), whole), chunks
 
 
+def test_tiny_greedy_tokens_follow_total_order(mods, tiny):
+    """Greedy tokens of a forward step equal the total-order argmax of its
+    logits, including exact ties (all LM-head rows equal: token 0) and NaN
+    logits (two NaN rows: the lower index)."""
+    bi, sched, _ = mods
+    eng, prompts = tiny
+    runner = sched.Runner(eng)
+    w_lm = eng.head["w_lm"]
+    saved = w_lm.clone()
+    try:
+        def run(rids):
+            reqs = [sched.Request(rid, prompts[rid]) for rid in rids]
+            items = [sched.StepItem(r, len(r.prompt), "all") for r in reqs]
+            logits, tokens, _ = runner.step(items)
+            out = (logits.clone(), tokens.clone())
+            for r in reqs:
+                runner.evict(r)
+            return out
+        logits, tokens = run([0, 3, 5])
+        assert np.array_equal(tokens.cpu().numpy(), oracle.argmax_rows(logits.cpu().numpy()))
+        w_lm.copy_(saved[7].expand_as(w_lm))
+        logits, tokens = run([1, 2])
+        assert bool((logits == logits[:, :1]).all())
+        assert int(tokens.abs().sum()) == 0
+        nan_row = saved[7].clone()
+        nan_row[3] = float("nan")
+        w_lm[700] = nan_row
+        w_lm[1500] = nan_row
+        logits, tokens = run([4])
+        assert bool(torch.isnan(logits[:, 700]).all()) and bool(torch.isnan(logits[:, 1500]).all())
+        assert bool((tokens == 700).all())
+    finally:
+        w_lm.copy_(saved)
+        torch.cuda.synchronize()
+
+
 # ---------------------------------------------------------------------------
 # 8B-shaped single layer (decode steps over random compositions)
 # ---------------------------------------------------------------------------
@@ -173,6 +209,7 @@ class DecodeLayerCase:
         logits, tokens, hidden = self.eng.step([1] * len(rows), [int(self.ctx[r]) - 1 for r in rows],
                                                self.d_ids[idx].contiguous(), self.d_table[idx].contiguous(),
                                                list(range(len(rows))), mode=mode, want_hidden=True)
+        self.last_tokens = tokens
         return logits, hidden
 
 
@@ -190,13 +227,17 @@ def test_8b_layer_compositions_bitwise(mods, layer8b):
     bi, sched, _ = mods
     case = layer8b
     n = len(case.ctx)
-    solo_l, solo_h = [], []
+    solo_l, solo_h, solo_t = [], [], []
     for r in range(n):
         l, h = case.step([r], bi.INVARIANT)
         solo_l.append(l[0].clone())
         solo_h.append(h[0].clone())
+        solo_t.append(case.last_tokens[0].clone())
     solo_l = torch.stack(solo_l)
     solo_h = torch.stack(solo_h)
+    solo_t = torch.stack(solo_t)
+    # the greedy tokens (taken inside the LM head's epilogue) are the argmax of the logits
+    assert np.array_equal(solo_t.cpu().numpy(), oracle.argmax_rows(solo_l.cpu().numpy()))
     rng = np.random.default_rng(1001)
     bad = 0
     for b in range(1, n + 1):
@@ -204,7 +245,8 @@ def test_8b_layer_compositions_bitwise(mods, layer8b):
             rows = rng.choice(n, size=b, replace=False)
             l, h = case.step(rows, bi.INVARIANT)
             r = torch.from_numpy(rows).cuda()
-            if not (sched.bitwise_equal(l, solo_l[r]) and sched.bitwise_equal(h, solo_h[r])):
+            if not (sched.bitwise_equal(l, solo_l[r]) and sched.bitwise_equal(h, solo_h[r])
+                    and torch.equal(case.last_tokens[:b], solo_t[r])):
                 bad += 1
     case.eng.check()
     assert bad == 0, f"{bad} compositions differ from bs=1"
