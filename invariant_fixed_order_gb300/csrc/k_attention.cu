@@ -27,7 +27,7 @@ constexpr int kAttnThreads = 128;
 constexpr int kWarps = kAttnThreads / 32;
 constexpr int kMaxChunkPages = BI_KV_CHUNK / BI_PAGE + 1;  // a variant piece may straddle one more page
 constexpr int kSub = 64;                                   // keys per staged sub-chunk
-constexpr int kRing = 3;                                   // staged sub-chunks in flight
+constexpr int kRing = 2;  // staged sub-chunks in flight (a shallow ring fits 6 CTAs per SM)
 
 template <int G, int DH>
 struct AttnShape {
