@@ -26,24 +26,38 @@ namespace bi {
 constexpr int kAttnThreads = 128;
 constexpr int kWarps = kAttnThreads / 32;
 constexpr int kMaxChunkPages = BI_KV_CHUNK / BI_PAGE + 1;  // a variant piece may straddle one more page
-constexpr int kSub = 64;                                   // keys per staged sub-chunk
-constexpr int kRing = 2;  // staged sub-chunks in flight (a shallow ring fits 6 CTAs per SM)
+constexpr int kSub = 64;  // keys per staged sub-chunk
+constexpr int kRing = 2;  // staged sub-chunks in flight (a shallow ring fits several CTAs per SM)
 
-template <int G, int DH>
+// The MMAs are transposed with respect to the usual attention tiling: the 16
+// rows of an m16n8k16 tile are keys (scores) or head dims (PV), and its 8
+// columns are (query token, head) pairs, token-major.  A decode CTA has one
+// token, so its columns are the G heads of one GQA group; a prefill CTA has
+// NT consecutive tokens of one request sharing every K/V load.
+template <int G, int DH, int NT>
 struct AttnShape {
-    static_assert(G >= 1 && G <= 8, "a GQA group fills at most the 8 rows a0/a2 of an m16n8k16 tile");
-    static constexpr int kKSteps = DH / 16;           // 16-deep MMA steps over the head dim
-    static constexpr int kDimsPerWarp = DH / kWarps;  // PV: output dims per warp
-    static constexpr int kNB = kDimsPerWarp / 8;      // PV: 8-wide n-blocks per warp
+    static_assert(G >= 1 && G <= 8 && NT >= 1, "unsupported group");
+    static constexpr int kCols = NT * G;            // live columns
+    static constexpr int kNB = (kCols + 7) / 8;     // 8-wide column blocks
+    static constexpr int kKSteps = DH / 16;         // 16-deep MMA steps over the head dim
+    static constexpr int kDimsPerWarp = DH / kWarps;
+    static constexpr int kMT = kDimsPerWarp / 16;   // PV: 16-dim row tiles per warp
+    static_assert(kMT >= 1, "head dim too small");
 };
 
-template <int G, int DH>
+template <int G, int DH, int NT>
 struct AttnSmem {
+    using S = AttnShape<G, DH, NT>;
     uint16_t ring[kRing][kSub][DH];  // K or V rows; 16-byte chunk c of row r sits at chunk c ^ (r & 7)
-    float p[G][BI_KV_CHUNK];         // scores, then exp(score - m)
-    float red[kWarps][G];            // per-warp partial sums of l
-    float m[G];
-    float l[G];
+    float p[S::kCols][BI_KV_CHUNK];  // scores, then exp(score - m); after PV, the outputs being stored
+    float red[kWarps][S::kCols];     // per-warp partial sums of l
+    float m[S::kCols];
+    float l[S::kCols];
+    float fold_a[S::kCols];          // prefill fold: weights of the running state and of the chunk
+    float fold_b[S::kCols];
+    float M[S::kCols];               // prefill fold: running max and sum
+    float L[S::kCols];
+    int32_t ncol[S::kCols];          // keys of the current chunk each column attends to
     int32_t pages[kMaxChunkPages];
 };
 
@@ -98,14 +112,13 @@ __device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t (&r)[4]) {
                  : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3])
                  : "r"(addr));
 }
-// d += A(16x16, rows 8..15 zero) * B(16x8), bf16 in, fp32 accumulate.
-__device__ __forceinline__ void mma_rows8(float (&d)[4], uint32_t a0, uint32_t a2, uint32_t b0, uint32_t b1) {
-    const uint32_t z = 0;
+// d += A(16x16) * B(16x8), bf16 in, fp32 accumulate.
+__device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4], uint32_t b0, uint32_t b1) {
     asm volatile(
         "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, {%4, %5, %6, %7}, {%8, %9}, "
         "{%0, %1, %2, %3};"
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
-        : "r"(a0), "r"(z), "r"(a2), "r"(z), "r"(b0), "r"(b1));
+        : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
 // Byte offset of (row, 16-byte chunk c) in a swizzled ring stage.
 template <int DH>
@@ -113,48 +126,60 @@ __device__ __forceinline__ uint32_t ring_off(int row, int c) {
     return static_cast<uint32_t>(row * DH * 2 + ((c ^ (row & 7)) << 4));
 }
 
-// Query fragments of the GQA group: row h of the MMA's A operand is head h of
-// the group (rows >= G and 8..15 are zero); qa[ks] = {a0, a2} of 16-deep step ks.
-template <int G, int DH>
-__device__ __forceinline__ void load_q_frags(const uint16_t* q, int32_t t, int32_t H, int32_t g,
-                                             uint32_t (&qa)[DH / 16][2]) {
-    const int lane = threadIdx.x & 31, h = lane >> 2, c = 2 * (lane & 3);
-    const uint16_t* src = q + (static_cast<int64_t>(t) * H + static_cast<int64_t>(g) * G + h) * DH;
+// Query fragments as the B operand of the score MMAs: column c = nb*8 + lane/4
+// is head c % G of the c / G-th token of the CTA (tok[] gives its row in q;
+// -1 or c >= kCols: zero); qb[nb][ks] = {b0, b1} of 16-deep step ks.
+template <int G, int DH, int NT>
+__device__ __forceinline__ void load_q_cols(const uint16_t* q, const int32_t (&tok)[NT], int32_t H, int32_t g,
+                                            uint32_t (&qb)[AttnShape<G, DH, NT>::kNB][DH / 16][2]) {
+    using S = AttnShape<G, DH, NT>;
+    const int lane = threadIdx.x & 31, c8 = lane >> 2, k2 = 2 * (lane & 3);
 #pragma unroll
-    for (int ks = 0; ks < DH / 16; ++ks) {
-        qa[ks][0] = h < G ? *reinterpret_cast<const uint32_t*>(src + ks * 16 + c) : 0u;
-        qa[ks][1] = h < G ? *reinterpret_cast<const uint32_t*>(src + ks * 16 + 8 + c) : 0u;
+    for (int nb = 0; nb < S::kNB; ++nb) {
+        const int c = nb * 8 + c8;
+        const int32_t t = c < S::kCols ? tok[c / G] : -1;
+        const uint16_t* src = q + (static_cast<int64_t>(t) * H + static_cast<int64_t>(g) * G + c % G) * DH;
+#pragma unroll
+        for (int ks = 0; ks < DH / 16; ++ks) {
+            qb[nb][ks][0] = t >= 0 ? *reinterpret_cast<const uint32_t*>(src + ks * 16 + k2) : 0u;
+            qb[nb][ks][1] = t >= 0 ? *reinterpret_cast<const uint32_t*>(src + ks * 16 + 8 + k2) : 0u;
+        }
     }
 }
 
-// Partial of keys [k0, k0 + n) (1 <= n <= BI_KV_CHUNK) for the G heads of
-// one GQA group.  On return sm.m / sm.l hold each head's max score and sum of
-// exp(score - max), and a thread with h = lane/4 < G holds in o[nb][0..1] the
-// unnormalised output of head h at dims 32w + 8nb + 2(lane%4) + {0,1} (w =
-// warp; DH/4 dims per warp).  The arithmetic, fixed for a given (n, G, DH):
-//   score_j = (q . k_j) * scale: q and k_j in bf16 multiplied on the tensor
-//             cores (m16n8k16, fp32 accumulate) over the head dim in 16-deep
-//             steps in ascending order, then one fp32 multiply by scale;
+// Partial of keys [k0, k0 + n_max) (1 <= n_max <= BI_KV_CHUNK) for every
+// column; column c attends to the first sm.ncol[c] of them (set by the caller
+// before a barrier; 0 = none).  On return sm.m / sm.l hold each column's max
+// score and sum of exp(score - max), and oacc[mt][nb] holds, in the m16n8
+// accumulator layout, the unnormalised output of columns nb*8 + 2(lane%4)
+// + {0,1} at head dims 32w + 16mt + lane/4 + {0, 8} (w = warp; DH/4 dims per
+// warp).  The arithmetic of one column, fixed for a given number of keys:
+//   score_j = (k_j . q) * scale: bf16 products on the tensor cores (m16n8k16,
+//             fp32 accumulate) over the head dim in 16-deep steps in
+//             ascending order, then one fp32 multiply by scale;
 //   m = max_j score_j;   p_j = exp(score_j - m);
 //   l = sum over the 4 warps in order of (xor-butterfly over the 32 lanes of
 //       (lane-serial sum of p_j over j = 32w + lane + 128i, i ascending));
 //   o = sum_j p_j v_j on the tensor cores: p_j split into bf16 hi = bf16(p_j)
 //       and lo = bf16(p_j - hi), for each 16-key step in ascending order the
 //       hi product then the lo product accumulated in fp32.
-// K and V rows stream through a ring of kRing shared-memory stages of kSub
-// keys each (cp.async), K sub-chunks first, then V sub-chunks.
-template <int G, int DH>
-__device__ __forceinline__ void chunk_partial(AttnSmem<G, DH>& sm, const uint16_t* __restrict__ kc,
+// A key a column does not attend to gets p = 0, which adds exact zeros, so a
+// column's bits do not depend on the other columns of its CTA.  K and V rows
+// stream through a ring of kRing shared-memory stages of kSub keys each
+// (cp.async), K sub-chunks first, then V sub-chunks.
+template <int G, int DH, int NT>
+__device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uint16_t* __restrict__ kc,
                                               const uint16_t* __restrict__ vc, const int32_t* page_row,
-                                              int32_t g, int32_t Hkv, int32_t k0, int32_t n, float scale,
+                                              int32_t g, int32_t Hkv, int32_t k0, int32_t n_max, float scale,
                                               int32_t max_pages, int32_t num_pages, int32_t* status,
-                                              const uint32_t (&qa)[DH / 16][2],
-                                              float (&o)[AttnShape<G, DH>::kNB][2]) {
-    using S = AttnShape<G, DH>;
+                                              const uint32_t (&qb)[AttnShape<G, DH, NT>::kNB][DH / 16][2],
+                                              float (&oacc)[AttnShape<G, DH, NT>::kMT][AttnShape<G, DH, NT>::kNB][4]) {
+    using S = AttnShape<G, DH, NT>;
     constexpr int kVecPerRow = DH / 8;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
+    const int c8 = lane >> 2, k2 = 2 * (lane & 3);
     const int32_t lp0 = k0 / BI_PAGE;
-    const int32_t np = (k0 + n - 1) / BI_PAGE - lp0 + 1;
+    const int32_t np = (k0 + n_max - 1) / BI_PAGE - lp0 + 1;
     if (tid < np) {
         const int32_t lp = lp0 + tid;
         int32_t pg = lp < max_pages ? page_row[lp] : -1;
@@ -166,13 +191,13 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH>& sm, const uint16_
     }
     __syncthreads();
 
-    const int ns = (n + kSub - 1) / kSub;  // sub-chunks of K, then as many of V
-    const int part = tid % kVecPerRow;     // this thread's 16-byte column of every row it copies
+    const int ns = (n_max + kSub - 1) / kSub;  // sub-chunks of K, then as many of V
+    const int part = tid % kVecPerRow;         // this thread's 16-byte column of every row it copies
     auto issue = [&](int t) {
         if (t < 2 * ns) {
             const bool is_v = t >= ns;
             const int32_t j0 = (is_v ? t - ns : t) * kSub;
-            const int32_t nk = min(kSub, n - j0);
+            const int32_t nk = min(kSub, n_max - j0);
             const uint16_t* base = (is_v ? vc : kc) + static_cast<int64_t>(g) * BI_PAGE * DH + part * 8;
             unsigned char* dst = reinterpret_cast<unsigned char*>(sm.ring[t % kRing]);
             for (int jl = tid / kVecPerRow; jl < nk; jl += kAttnThreads / kVecPerRow) {
@@ -180,84 +205,83 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH>& sm, const uint16_
                 const int64_t pg = sm.pages[kp / BI_PAGE - lp0];
                 cp_async16(dst + ring_off<DH>(jl, part), base + (pg * Hkv * BI_PAGE + (kp & (BI_PAGE - 1))) * DH);
             }
-            if (is_v) {
-                // V rows past the last key up to the 16-key step boundary are read by
-                // the MMA with p = 0: make them zero rather than stale
-                const int32_t pad_end = min(kSub, (nk + 15) & ~15);
-                for (int jl = nk + tid / kVecPerRow; jl < pad_end; jl += kAttnThreads / kVecPerRow)
-                    *reinterpret_cast<uint4*>(dst + ring_off<DH>(jl, part)) = make_uint4(0, 0, 0, 0);
-            }
+            // rows past the last key up to the 16-key step boundary are read by
+            // the MMAs (K: scores never stored; V: times p = 0): zero, not stale
+            const int32_t pad_end = min(kSub, (nk + 15) & ~15);
+            for (int jl = nk + tid / kVecPerRow; jl < pad_end; jl += kAttnThreads / kVecPerRow)
+                *reinterpret_cast<uint4*>(dst + ring_off<DH>(jl, part)) = make_uint4(0, 0, 0, 0);
         }
         cp_async_commit();  // possibly empty: keeps one group per sub-chunk slot
     };
 #pragma unroll
     for (int t = 0; t < kRing; ++t) issue(t);
 
-    const int hrow = lane >> 2, cq = 2 * (lane & 3);
-    float oacc[S::kNB][4];
 #pragma unroll
-    for (int nb = 0; nb < S::kNB; ++nb) oacc[nb][0] = oacc[nb][1] = oacc[nb][2] = oacc[nb][3] = 0.0f;
+    for (int mt = 0; mt < S::kMT; ++mt)
+#pragma unroll
+        for (int nb = 0; nb < S::kNB; ++nb) oacc[mt][nb][0] = oacc[mt][nb][1] = oacc[mt][nb][2] = oacc[mt][nb][3] = 0.0f;
 
     for (int t = 0; t < 2 * ns; ++t) {
         asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 1) : "memory");
         __syncthreads();
         const uint32_t buf = smem_u32(sm.ring[t % kRing]);
         if (t < ns) {
-            // scores: warp w takes keys 16w .. 16w+15 of the sub-chunk, 8 per MMA n-block
+            // scores: warp w takes keys 16w .. 16w+15 of the sub-chunk as the MMA rows
             const int32_t j0 = t * kSub;
-            const int32_t nk = min(kSub, n - j0);
+            const int32_t nk = min(kSub, n_max - j0);
+            if (warp * 16 < nk) {
+                float acc[S::kNB][4];
 #pragma unroll
-            for (int nb2 = 0; nb2 < 2; ++nb2) {
-                const int n0 = warp * 16 + nb2 * 8;
-                if (n0 >= nk) break;
-                float acc[4] = {0.0f, 0.0f, 0.0f, 0.0f};
+                for (int nb = 0; nb < S::kNB; ++nb) acc[nb][0] = acc[nb][1] = acc[nb][2] = acc[nb][3] = 0.0f;
 #pragma unroll
-                for (int ks = 0; ks < S::kKSteps; ks += 2) {
-                    uint32_t r[4];
-                    ldsm_x4(buf + ring_off<DH>(n0 + (lane & 7), 2 * ks + (lane >> 3)), r);
-                    mma_rows8(acc, qa[ks][0], qa[ks][1], r[0], r[1]);
-                    mma_rows8(acc, qa[ks + 1][0], qa[ks + 1][1], r[2], r[3]);
+                for (int ks = 0; ks < S::kKSteps; ++ks) {
+                    uint32_t a[4];
+                    ldsm_x4(buf + ring_off<DH>(warp * 16 + (lane & 7) + ((lane >> 3) & 1) * 8, 2 * ks + (lane >> 4)), a);
+#pragma unroll
+                    for (int nb = 0; nb < S::kNB; ++nb) mma_16816(acc[nb], a, qb[nb][ks][0], qb[nb][ks][1]);
                 }
-                if (hrow < G) {
 #pragma unroll
-                    for (int c = 0; c < 2; ++c) {
-                        const int key = n0 + cq + c;
-                        if (key < nk) sm.p[hrow][j0 + key] = __fmul_rn(acc[c], scale);
+                for (int nb = 0; nb < S::kNB; ++nb)
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        const int c = nb * 8 + k2 + (x & 1);
+                        const int32_t key = j0 + warp * 16 + c8 + (x >> 1) * 8;
+                        if (c < S::kCols && key < n_max)
+                            sm.p[c][key] = key < sm.ncol[c] ? __fmul_rn(acc[nb][x], scale) : -INFINITY;
                     }
-                }
             }
             if (t == ns - 1) {
                 __syncthreads();
-                // m: exact max per head (order-free)
-                for (int h = warp; h < G; h += kWarps) {
+                // m: exact max per column (order-free); a column without keys gets 0
+                for (int c = warp; c < S::kCols; c += kWarps) {
                     float mx = -INFINITY;
-                    for (int j = lane; j < n; j += 32) mx = fmaxf(mx, sm.p[h][j]);
+                    for (int j = lane; j < n_max; j += 32) mx = fmaxf(mx, sm.p[c][j]);
 #pragma unroll
                     for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
-                    if (lane == 0) sm.m[h] = mx;
+                    if (lane == 0) sm.m[c] = sm.ncol[c] > 0 ? mx : 0.0f;
                 }
                 __syncthreads();
-                // p = exp(score - m) and the fixed-tree sum l
-                float ls[G];
+                // p = exp(score - m) (exp(-inf) = 0 for keys a column skips) and the fixed-tree sum l
+                float ls[S::kCols];
 #pragma unroll
-                for (int h = 0; h < G; ++h) ls[h] = 0.0f;
-                for (int j = tid; j < n; j += kAttnThreads) {
+                for (int c = 0; c < S::kCols; ++c) ls[c] = 0.0f;
+                for (int j = tid; j < n_max; j += kAttnThreads) {
 #pragma unroll
-                    for (int h = 0; h < G; ++h) {
-                        const float pv = expf(__fsub_rn(sm.p[h][j], sm.m[h]));
-                        sm.p[h][j] = pv;
-                        ls[h] = __fadd_rn(ls[h], pv);
+                    for (int c = 0; c < S::kCols; ++c) {
+                        const float pv = expf(__fsub_rn(sm.p[c][j], sm.m[c]));
+                        sm.p[c][j] = pv;
+                        ls[c] = __fadd_rn(ls[c], pv);
                     }
                 }
 #pragma unroll
-                for (int h = 0; h < G; ++h) {
+                for (int c = 0; c < S::kCols; ++c) {
 #pragma unroll
                     for (int off = 16; off >= 1; off >>= 1)
-                        ls[h] = __fadd_rn(ls[h], __shfl_xor_sync(0xffffffffu, ls[h], off));
-                    if (lane == 0) sm.red[warp][h] = ls[h];
+                        ls[c] = __fadd_rn(ls[c], __shfl_xor_sync(0xffffffffu, ls[c], off));
+                    if (lane == 0) sm.red[warp][c] = ls[c];
                 }
                 __syncthreads();
-                if (tid < G) {
+                if (tid < S::kCols) {
                     float l = sm.red[0][tid];
 #pragma unroll
                     for (int w = 1; w < kWarps; ++w) l = __fadd_rn(l, sm.red[w][tid]);
@@ -265,34 +289,35 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH>& sm, const uint16_
                 }
             }
         } else {
-            // PV: warp w owns dims DH/4 * w .. ; 16-key steps in ascending order
+            // PV: warp w owns head dims DH/4 * w ..; 16-key steps in ascending order
             const int32_t j0 = (t - ns) * kSub;
-            const int32_t nk = min(kSub, n - j0);
-            const int c0 = warp * S::kDimsPerWarp / 8;  // first 16-byte chunk of this warp's dims
+            const int32_t nk = min(kSub, n_max - j0);
             for (int kk = 0; kk < nk; kk += 16) {
-                float pv[4];
+                uint32_t bh[S::kNB][2], bl[S::kNB][2];
 #pragma unroll
-                for (int x = 0; x < 4; ++x) {
-                    const int key = kk + cq + (x & 1) + (x >> 1) * 8;
-                    pv[x] = (hrow < G && key < nk) ? sm.p[hrow][j0 + key] : 0.0f;
+                for (int nb = 0; nb < S::kNB; ++nb) {
+                    const int c = nb * 8 + c8;
+#pragma unroll
+                    for (int y = 0; y < 2; ++y) {
+                        const int32_t key = j0 + kk + k2 + 8 * y;
+                        const float p0 = (c < S::kCols && key < n_max) ? sm.p[c][key] : 0.0f;
+                        const float p1 = (c < S::kCols && key + 1 < n_max) ? sm.p[c][key + 1] : 0.0f;
+                        const float h0 = __uint_as_float(static_cast<uint32_t>(f32_to_bf16(p0)) << 16);
+                        const float h1 = __uint_as_float(static_cast<uint32_t>(f32_to_bf16(p1)) << 16);
+                        bh[nb][y] = pack_bf16x2(h0, h1);
+                        bl[nb][y] = pack_bf16x2(__fsub_rn(p0, h0), __fsub_rn(p1, h1));
+                    }
                 }
-                uint32_t hi[2], lo[2];
 #pragma unroll
-                for (int y = 0; y < 2; ++y) {
-                    const float h0 = __uint_as_float(static_cast<uint32_t>(f32_to_bf16(pv[2 * y])) << 16);
-                    const float h1 = __uint_as_float(static_cast<uint32_t>(f32_to_bf16(pv[2 * y + 1])) << 16);
-                    hi[y] = pack_bf16x2(h0, h1);
-                    lo[y] = pack_bf16x2(__fsub_rn(pv[2 * y], h0), __fsub_rn(pv[2 * y + 1], h1));
-                }
+                for (int mt = 0; mt < S::kMT; ++mt) {
+                    uint32_t a[4];
+                    const int c0 = (warp * S::kDimsPerWarp + mt * 16) / 8;
+                    ldsm_x4_trans(buf + ring_off<DH>(kk + (lane & 7) + (lane >> 4) * 8, c0 + ((lane >> 3) & 1)), a);
 #pragma unroll
-                for (int nb = 0; nb < S::kNB; nb += 2) {
-                    uint32_t r[4];
-                    const int i = lane >> 3;
-                    ldsm_x4_trans(buf + ring_off<DH>(kk + (i & 1) * 8 + (lane & 7), c0 + nb + (i >> 1)), r);
-                    mma_rows8(oacc[nb], hi[0], hi[1], r[0], r[1]);
-                    mma_rows8(oacc[nb], lo[0], lo[1], r[0], r[1]);
-                    mma_rows8(oacc[nb + 1], hi[0], hi[1], r[2], r[3]);
-                    mma_rows8(oacc[nb + 1], lo[0], lo[1], r[2], r[3]);
+                    for (int nb = 0; nb < S::kNB; ++nb) {
+                        mma_16816(oacc[mt][nb], a, bh[nb][0], bh[nb][1]);
+                        mma_16816(oacc[mt][nb], a, bl[nb][0], bl[nb][1]);
+                    }
                 }
             }
         }
@@ -300,12 +325,26 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH>& sm, const uint16_
         issue(t + kRing);
     }
     cp_async_wait_all();
-#pragma unroll
-    for (int nb = 0; nb < S::kNB; ++nb) {
-        o[nb][0] = oacc[nb][0];
-        o[nb][1] = oacc[nb][1];
-    }
     __syncthreads();
+}
+
+// Writes a thread's accumulator elements (oacc layout above), each through
+// f(column, dim, value).
+template <int G, int DH, int NT, typename F>
+__device__ __forceinline__ void for_each_out(const float (&oacc)[AttnShape<G, DH, NT>::kMT][AttnShape<G, DH, NT>::kNB][4],
+                                             F&& f) {
+    using S = AttnShape<G, DH, NT>;
+    const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
+#pragma unroll
+    for (int mt = 0; mt < S::kMT; ++mt)
+#pragma unroll
+        for (int nb = 0; nb < S::kNB; ++nb)
+#pragma unroll
+            for (int x = 0; x < 4; ++x) {
+                const int c = nb * 8 + 2 * (lane & 3) + (x & 1);
+                const int d = warp * S::kDimsPerWarp + mt * 16 + (lane >> 2) + (x >> 1) * 8;
+                if (c < S::kCols) f(c, d, oacc[mt][nb][x]);
+            }
 }
 
 // Ascending-order merge step of two partials (M, L, O) and (m, l, o).
@@ -335,7 +374,7 @@ __device__ __forceinline__ void pieces(int32_t s, int32_t chunk2, int32_t& size,
 }
 
 // ---------------------------------------------------------------------------
-// Decode: grid (entries, Hkv, max_splits).
+// Decode: grid (entries, Hkv, max_splits); one token, its G heads as columns.
 // ---------------------------------------------------------------------------
 template <int G, int DH>
 __global__ void __launch_bounds__(kAttnThreads)
@@ -343,9 +382,9 @@ decode_split_kernel(AttnGeom geo, EntryMap em, int32_t max_splits, int32_t chunk
                     float* __restrict__ ws_ml) {
     pdl_trigger();
     pdl_wait();
-    using S = AttnShape<G, DH>;
+    using S = AttnShape<G, DH, 1>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    AttnSmem<G, DH>& sm = *reinterpret_cast<AttnSmem<G, DH>*>(smem_raw);
+    AttnSmem<G, DH, 1>& sm = *reinterpret_cast<AttnSmem<G, DH, 1>*>(smem_raw);
     const int32_t e = blockIdx.x, g = blockIdx.y, split = blockIdx.z;
     const Entry en = get_entry(em, e);
     const int32_t s = en.p + 1;
@@ -359,21 +398,28 @@ decode_split_kernel(AttnGeom geo, EntryMap em, int32_t max_splits, int32_t chunk
     if (split >= count) return;
     const int32_t k0 = split * size;
     const int32_t n = min(size, s - k0);
-    uint32_t qa[DH / 16][2];
-    load_q_frags<G, DH>(reinterpret_cast<const uint16_t*>(geo.q), en.t, geo.H, g, qa);
-    float o[S::kNB][2];
-    chunk_partial<G, DH>(sm, reinterpret_cast<const uint16_t*>(geo.kc), reinterpret_cast<const uint16_t*>(geo.vc),
-                         geo.page_table + static_cast<int64_t>(en.r) * geo.max_pages, g, geo.Hkv, k0, n,
-                         geo.scale, geo.max_pages, geo.num_pages, geo.status, qa, o);
-    const int lane = threadIdx.x & 31, warp = threadIdx.x / 32, h = lane >> 2;
-    if (h < G) {
-        const int64_t row = (static_cast<int64_t>(e) * geo.H + g * G + h) * max_splits + split;
-#pragma unroll
-        for (int nb = 0; nb < S::kNB; ++nb) {
-            const int d = warp * S::kDimsPerWarp + nb * 8 + 2 * (lane & 3);
-            *reinterpret_cast<float2*>(ws_o + row * DH + d) = make_float2(o[nb][0], o[nb][1]);
-        }
-        if (warp == 0 && (lane & 3) == 0) *reinterpret_cast<float2*>(ws_ml + row * 2) = make_float2(sm.m[h], sm.l[h]);
+    if (threadIdx.x < S::kCols) sm.ncol[threadIdx.x] = n;
+    const int32_t tok[1] = {en.t};
+    uint32_t qb[S::kNB][DH / 16][2];
+    load_q_cols<G, DH, 1>(reinterpret_cast<const uint16_t*>(geo.q), tok, geo.H, g, qb);
+    float oacc[S::kMT][S::kNB][4];
+    chunk_partial<G, DH, 1>(sm, reinterpret_cast<const uint16_t*>(geo.kc), reinterpret_cast<const uint16_t*>(geo.vc),
+                            geo.page_table + static_cast<int64_t>(en.r) * geo.max_pages, g, geo.Hkv, k0, n,
+                            geo.scale, geo.max_pages, geo.num_pages, geo.status, qb, oacc);
+    // stage the partials through the score buffer, then write whole rows
+    float* stage = &sm.p[0][0];  // [kCols][DH]
+    for_each_out<G, DH, 1>(oacc, [&](int c, int d, float v) { stage[c * DH + d] = v; });
+    __syncthreads();
+    const int64_t row0 = (static_cast<int64_t>(e) * geo.H + static_cast<int64_t>(g) * G) * max_splits + split;
+    for (int i = threadIdx.x; i < S::kCols * (DH / 4); i += kAttnThreads) {
+        const int c = i / (DH / 4), d4 = i % (DH / 4);
+        reinterpret_cast<float4*>(ws_o + (row0 + static_cast<int64_t>(c) * max_splits) * DH)[d4] =
+            reinterpret_cast<const float4*>(stage + c * DH)[d4];
+    }
+    if (threadIdx.x < S::kCols) {
+        const int c = threadIdx.x;
+        *reinterpret_cast<float2*>(ws_ml + (row0 + static_cast<int64_t>(c) * max_splits) * 2) =
+            make_float2(sm.m[c], sm.l[c]);
     }
 }
 
@@ -428,72 +474,105 @@ decode_merge_kernel(AttnGeom geo, EntryMap em, int32_t max_splits, int32_t chunk
 }
 
 // ---------------------------------------------------------------------------
-// Prefill: grid (entries, Hkv); each CTA walks its query's chunks in order.
+// Prefill: grid (ceil(entries / NT), Hkv).  A CTA takes NT consecutive
+// entries; each run of them that belongs to one request shares its K/V loads,
+// walks the chunks in order and folds them in registers with the decode
+// merge's arithmetic, column by column.
 // ---------------------------------------------------------------------------
-template <int G, int DH>
+template <int G, int DH, int NT>
 __global__ void __launch_bounds__(kAttnThreads)
-prefill_kernel(AttnGeom geo, EntryMap em) {
+prefill_kernel(AttnGeom geo, EntryMap em, int32_t n_entries) {
     pdl_trigger();
     pdl_wait();
-    using S = AttnShape<G, DH>;
+    using S = AttnShape<G, DH, NT>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    AttnSmem<G, DH>& sm = *reinterpret_cast<AttnSmem<G, DH>*>(smem_raw);
-    const int32_t e = blockIdx.x, g = blockIdx.y;
-    const Entry en = get_entry(em, e);
-    const int32_t s = en.p + 1;
-    const bool ok = en.p >= 0 && (s + BI_PAGE - 1) / BI_PAGE <= geo.max_pages;
-    const int lane = threadIdx.x & 31, warp = threadIdx.x / 32, h = lane >> 2;
-    if (!ok) {
-        if (threadIdx.x == 0) report(geo.status, BI_DEV_BAD_POSITION);
-        if (h < G)
-            for (int nb = 0; nb < S::kNB; ++nb)
-                store_out2(geo.out, geo.out_f32,
-                           (static_cast<int64_t>(en.t) * geo.H + g * G + h) * DH + warp * S::kDimsPerWarp + nb * 8 +
-                               2 * (lane & 3),
-                           0.f, 0.f);
-        return;
-    }
-    uint32_t qa[DH / 16][2];
-    load_q_frags<G, DH>(reinterpret_cast<const uint16_t*>(geo.q), en.t, geo.H, g, qa);
-    const int hh = h < G ? h : 0;
-    float M = 0.0f, L = 0.0f, O[S::kNB][2];
-    const int32_t count = (s + BI_KV_CHUNK - 1) / BI_KV_CHUNK;
-    const int32_t* page_row = geo.page_table + static_cast<int64_t>(en.r) * geo.max_pages;
-    for (int32_t j = 0; j < count; ++j) {
-        const int32_t k0 = j * BI_KV_CHUNK;
-        const int32_t n = min(BI_KV_CHUNK, s - k0);
-        float o[S::kNB][2];
-        chunk_partial<G, DH>(sm, reinterpret_cast<const uint16_t*>(geo.kc), reinterpret_cast<const uint16_t*>(geo.vc),
-                             page_row, g, geo.Hkv, k0, n, geo.scale, geo.max_pages, geo.num_pages, geo.status, qa, o);
-        const float m = sm.m[hh], l = sm.l[hh];
-        if (j == 0) {
-            M = m;
-            L = l;
+    AttnSmem<G, DH, NT>& sm = *reinterpret_cast<AttnSmem<G, DH, NT>*>(smem_raw);
+    const int32_t g = blockIdx.y;
+    const int32_t e_begin = static_cast<int32_t>(blockIdx.x) * NT;
+    const int32_t e_end = min(e_begin + NT, n_entries);
+    const int tid = threadIdx.x;
+    for (int32_t e0 = e_begin; e0 < e_end;) {
+        const Entry first = get_entry(em, e0);
+        int32_t e1 = e0 + 1;
+        while (e1 < e_end && get_entry(em, e1).r == first.r) ++e1;
+        int32_t tok[NT], keys[NT];
+        int32_t s_max = 0;
 #pragma unroll
-            for (int nb = 0; nb < S::kNB; ++nb) {
-                O[nb][0] = o[nb][0];
-                O[nb][1] = o[nb][1];
-            }
-        } else {
-            // the same fold as the decode merge, one dim pair at a time
-            const float M0 = M, L0 = L;
-#pragma unroll
-            for (int nb = 0; nb < S::kNB; ++nb) {
-                float Mx = M0, Lx = L0;
-                fold_step(Mx, Lx, O[nb][0], O[nb][1], m, l, o[nb][0], o[nb][1]);
-                M = Mx;
-                L = Lx;
+        for (int i = 0; i < NT; ++i) {
+            tok[i] = -1;
+            keys[i] = 0;
+            if (e0 + i < e1) {
+                const Entry en = get_entry(em, e0 + i);
+                const int32_t s = en.p + 1;
+                const bool ok = en.p >= 0 && (s + BI_PAGE - 1) / BI_PAGE <= geo.max_pages;
+                if (!ok && tid == 0) report(geo.status, BI_DEV_BAD_POSITION);
+                tok[i] = en.t;
+                keys[i] = ok ? s : 0;
+                s_max = max(s_max, keys[i]);
             }
         }
-        __syncthreads();
-    }
-    if (h < G) {
+        uint32_t qb[S::kNB][DH / 16][2];
+        load_q_cols<G, DH, NT>(reinterpret_cast<const uint16_t*>(geo.q), tok, geo.H, g, qb);
+        float O[S::kMT][S::kNB][4];
+        const int32_t count = (s_max + BI_KV_CHUNK - 1) / BI_KV_CHUNK;
+        const int32_t* page_row = geo.page_table + static_cast<int64_t>(first.r) * geo.max_pages;
+        for (int32_t j = 0; j < count; ++j) {
+            const int32_t k0 = j * BI_KV_CHUNK;
+            if (tid < S::kCols) sm.ncol[tid] = min(max(keys[tid / G] - k0, 0), BI_KV_CHUNK);
+            float o[S::kMT][S::kNB][4];
+            chunk_partial<G, DH, NT>(sm, reinterpret_cast<const uint16_t*>(geo.kc),
+                                     reinterpret_cast<const uint16_t*>(geo.vc), page_row, g, geo.Hkv, k0,
+                                     min(BI_KV_CHUNK, s_max - k0), geo.scale, geo.max_pages, geo.num_pages,
+                                     geo.status, qb, o);
+            // the decode merge's fold (fold_step), one column's (M, L) at a time
+            if (tid < S::kCols && sm.ncol[tid] > 0) {
+                const float m = sm.m[tid], l = sm.l[tid];
+                if (j == 0) {
+                    sm.M[tid] = m;
+                    sm.L[tid] = l;
+                } else {
+                    const float M = sm.M[tid];
+                    const float Mn = fmaxf(M, m);
+                    const float a = expf(__fsub_rn(M, Mn));
+                    const float b = expf(__fsub_rn(m, Mn));
+                    sm.L[tid] = __fadd_rn(__fmul_rn(sm.L[tid], a), __fmul_rn(l, b));
+                    sm.M[tid] = Mn;
+                    sm.fold_a[tid] = a;
+                    sm.fold_b[tid] = b;
+                }
+            }
+            __syncthreads();
+            const int lane = tid & 31;
 #pragma unroll
-        for (int nb = 0; nb < S::kNB; ++nb)
-            store_out2(geo.out, geo.out_f32,
-                       (static_cast<int64_t>(en.t) * geo.H + g * G + h) * DH + warp * S::kDimsPerWarp + nb * 8 +
-                           2 * (lane & 3),
-                       __fdiv_rn(O[nb][0], L), __fdiv_rn(O[nb][1], L));
+            for (int mt = 0; mt < S::kMT; ++mt)
+#pragma unroll
+                for (int nb = 0; nb < S::kNB; ++nb)
+#pragma unroll
+                    for (int x = 0; x < 4; ++x) {
+                        const int c = nb * 8 + 2 * (lane & 3) + (x & 1);
+                        if (c < S::kCols && sm.ncol[c] > 0)
+                            O[mt][nb][x] = j == 0 ? o[mt][nb][x]
+                                                  : __fadd_rn(__fmul_rn(O[mt][nb][x], sm.fold_a[c]),
+                                                              __fmul_rn(o[mt][nb][x], sm.fold_b[c]));
+                    }
+            __syncthreads();
+        }
+        // out = O / L, staged through the score buffer; a token without keys gets zeros
+        float* stage = &sm.p[0][0];  // [kCols][DH]
+        for_each_out<G, DH, NT>(O, [&](int c, int d, float v) {
+            stage[c * DH + d] = keys[c / G] > 0 ? __fdiv_rn(v, sm.L[c]) : 0.0f;
+        });
+        __syncthreads();
+        for (int i = tid; i < S::kCols * (DH / 2); i += kAttnThreads) {
+            const int c = i / (DH / 2), dp = i % (DH / 2);
+            const int ti = c / G;
+            if (e0 + ti < e1)
+                store_out2(geo.out, geo.out_f32,
+                           (static_cast<int64_t>(tok[ti]) * geo.H + static_cast<int64_t>(g) * G + c % G) * DH + 2 * dp,
+                           stage[c * DH + 2 * dp], stage[c * DH + 2 * dp + 1]);
+        }
+        __syncthreads();
+        e0 = e1;
     }
 }
 
@@ -537,7 +616,7 @@ size_t decode_ws_bytes(int32_t n_entries, int32_t H, int32_t Dh, int32_t max_spl
 template <int G, int DH>
 static cudaError_t launch_decode_t(const AttnGeom& g, const EntryMap& em, int32_t n, int32_t max_splits,
                                    int32_t chunk2, float* ws_o, float* ws_ml, cudaStream_t s) {
-    const size_t smem = sizeof(AttnSmem<G, DH>);
+    const size_t smem = sizeof(AttnSmem<G, DH, 1>);
     static bool attr_set = false;
     if (!attr_set) {
         cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<G, DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -553,17 +632,23 @@ static cudaError_t launch_decode_t(const AttnGeom& g, const EntryMap& em, int32_
                       static_cast<const float*>(ws_o), static_cast<const float*>(ws_ml));
 }
 
+// Query tokens per prefill CTA: 16 (token, head) columns.
+template <int G>
+constexpr int prefill_tokens() { return 16 / G; }
+
 template <int G, int DH>
 static cudaError_t launch_prefill_t(const AttnGeom& g, const EntryMap& em, int32_t n, cudaStream_t s) {
-    const size_t smem = sizeof(AttnSmem<G, DH>);
+    constexpr int NT = prefill_tokens<G>();
+    const size_t smem = sizeof(AttnSmem<G, DH, NT>);
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<G, DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<G, DH, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                              static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    return launch_pdl(prefill_kernel<G, DH>, dim3(n, g.Hkv), dim3(kAttnThreads), smem, s, g, em);
+    return launch_pdl(prefill_kernel<G, DH, NT>, dim3((n + NT - 1) / NT, g.Hkv), dim3(kAttnThreads), smem, s, g, em,
+                      n);
 }
 
 #define BI_ATTN_DISPATCH(FN, ...)                                              \
