@@ -51,7 +51,7 @@ def parse():
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
-    p.add_argument("--ncu-target", choices=["gemm-decode64", "gemm-prefill8192"], default=None,
+    p.add_argument("--ncu-target", choices=["gemm-decode64", "gemm-prefill8192", "prefill-attn16"], default=None,
                    help="launch only the named GEMMs (twice: warm-up, then the pass to capture) for an ncu "
                         "capture; prints no measurement")
     return p.parse_args()
@@ -267,6 +267,13 @@ def prefill_measure(device: str, steps: int, bf16_peak: float, stream) -> dict:
     eng.check()
     gemm_fl = roofline.layer_flops(cfg, T) + roofline.gemm_flops(64, cfg.V, cfg.d)
     attn_fl = 4 * cfg.H * cfg.Dh * sum(L * (L + 1) // 2 for L in lens)
+    # the step's causal attention alone, on the K/V the step just appended
+    q = (torch.randn(T, cfg.H, cfg.Dh, device=device) * 0.5).to(torch.bfloat16)
+    cu_q = torch.from_numpy(np.concatenate([[0], np.cumsum(lens)]).astype(np.int32)).to(device)
+    pos0 = torch.zeros(64, dtype=torch.int32, device=device)
+    aout = torch.empty(T, cfg.H, cfg.Dh, dtype=torch.bfloat16, device=device)
+    ams = time_steps(lambda: bi.prefill_attention(q, cu_q, pos0, eng.k[0], eng.v[0], d_table, out=aout,
+                                                  stream=stream), 3, 1, stream)
     # the step's largest GEMM alone: gate/up over all T tokens
     y = torch.randn(T, cfg.d, device=device).to(torch.bfloat16)
     hbuf = torch.empty(T, cfg.F, dtype=torch.bfloat16, device=device)
@@ -277,6 +284,7 @@ def prefill_measure(device: str, steps: int, bf16_peak: float, stream) -> dict:
     return {"requests": 64, "tokens": T, "chunk": [256, 2048], "ms_per_step": round(ms, 3),
             "tokens_per_s": round(T / (ms * 1e-3), 1), "gemm_tflop": round(gemm_fl / 1e12, 2),
             "attention_tflop": round(attn_fl / 1e12, 3),
+            "attention": {"us": round(ams * 1e3, 1), "tflops": round(attn_fl / (ams * 1e-3) / 1e12, 1)},
             "gate_up_gemm": {"us": round(gms * 1e3, 1), "tflops": round(gu_tf, 1),
                              "frac": round(gu_tf / bf16_peak, 3), "peak_tflops": bf16_peak}}
 
@@ -517,6 +525,29 @@ def ncu_target(which: str) -> None:
     def rnd(*shape, std=1.0):
         return (torch.randn(*shape, device="cuda", generator=g) * std).to(torch.bfloat16)
 
+    if which == "prefill-attn16":
+        # causal prefill attention of 16 prompts of U[256, 2048] tokens on random K/V (launched twice)
+        from invariant_fixed_order_gb300 import synth
+        lens = [int(x) for x in synth.uniform_ints(16, 256, 2048, DATA_SEED + 1)]
+        T = sum(lens)
+        max_pages = 2048 // 16 + 1
+        n_pages = sum((L + 15) // 16 for L in lens)
+        kc = rnd(n_pages, c.Hkv, 16, c.Dh)
+        vc = rnd(n_pages, c.Hkv, 16, c.Dh)
+        table = torch.zeros(16, max_pages, dtype=torch.int32, device="cuda")
+        p0 = 0
+        for i, L in enumerate(lens):
+            n = (L + 15) // 16
+            table[i, :n] = torch.arange(p0, p0 + n, dtype=torch.int32, device="cuda")
+            p0 += n
+        q = rnd(T, c.H, c.Dh)
+        cu_q = torch.tensor([0] + list(np.cumsum(lens)), dtype=torch.int32, device="cuda")
+        pos0 = torch.zeros(16, dtype=torch.int32, device="cuda")
+        for _ in range(2):
+            bi.prefill_attention(q, cu_q, pos0, kc, vc, table)
+        torch.cuda.synchronize()
+        print(json.dumps({"ncu_target": which, "done": True}))
+        return
     if which == "gemm-decode64":
         shapes = [(c.qkv_dim, c.d, bi.F32, bi.EP_NONE), (c.d, c.H * c.Dh, bi.BF16, bi.EP_RESIDUAL),
                   (2 * c.F, c.d, bi.BF16, bi.EP_SWIGLU), (c.d, c.F, bi.BF16, bi.EP_RESIDUAL),

@@ -28,6 +28,10 @@ constexpr int kWarps = kAttnThreads / 32;
 constexpr int kMaxChunkPages = BI_KV_CHUNK / BI_PAGE + 1;  // a variant piece may straddle one more page
 constexpr int kSub = 64;  // keys per staged sub-chunk
 constexpr int kRing = 2;  // staged sub-chunks in flight (a shallow ring fits several CTAs per SM)
+// Row strides chosen for conflict-free shared-memory access patterns of the
+// MMA fragments: scores (fp32), the bf16 hi/lo parts of p, staged outputs.
+constexpr int kPStride = BI_KV_CHUNK + 4;
+constexpr int kHStride = BI_KV_CHUNK + 8;
 
 // The MMAs are transposed with respect to the usual attention tiling: the 16
 // rows of an m16n8k16 tile are keys (scores) or head dims (PV), and its 8
@@ -49,7 +53,8 @@ template <int G, int DH, int NT>
 struct AttnSmem {
     using S = AttnShape<G, DH, NT>;
     uint16_t ring[kRing][kSub][DH];  // K or V rows; 16-byte chunk c of row r sits at chunk c ^ (r & 7)
-    float p[S::kCols][BI_KV_CHUNK];  // scores, then exp(score - m); after PV, the outputs being stored
+    float p[S::kCols][kPStride];     // scores, then exp(score - m); after PV, the outputs being stored
+    uint16_t ph[2][S::kCols][kHStride];  // bf16 hi = bf16(p) and lo = bf16(p - hi), the PV operand
     float red[kWarps][S::kCols];     // per-warp partial sums of l
     float m[S::kCols];
     float l[S::kCols];
@@ -221,6 +226,15 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
 #pragma unroll
         for (int nb = 0; nb < S::kNB; ++nb) oacc[mt][nb][0] = oacc[mt][nb][1] = oacc[mt][nb][2] = oacc[mt][nb][3] = 0.0f;
 
+    int32_t ncol_r[S::kNB][2];  // keys of this thread's score columns
+#pragma unroll
+    for (int nb = 0; nb < S::kNB; ++nb)
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            const int c = nb * 8 + k2 + x;
+            ncol_r[nb][x] = c < S::kCols ? sm.ncol[c] : 0;
+        }
+
     for (int t = 0; t < 2 * ns; ++t) {
         asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 1) : "memory");
         __syncthreads();
@@ -247,7 +261,7 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
                         const int c = nb * 8 + k2 + (x & 1);
                         const int32_t key = j0 + warp * 16 + c8 + (x >> 1) * 8;
                         if (c < S::kCols && key < n_max)
-                            sm.p[c][key] = key < sm.ncol[c] ? __fmul_rn(acc[nb][x], scale) : -INFINITY;
+                            sm.p[c][key] = key < ncol_r[nb][x & 1] ? __fmul_rn(acc[nb][x], scale) : -INFINITY;
                     }
             }
             if (t == ns - 1) {
@@ -269,10 +283,16 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
 #pragma unroll
                     for (int c = 0; c < S::kCols; ++c) {
                         const float pv = expf(__fsub_rn(sm.p[c][j], sm.m[c]));
-                        sm.p[c][j] = pv;
+                        const uint16_t hb = f32_to_bf16(pv);
+                        sm.ph[0][c][j] = hb;
+                        sm.ph[1][c][j] = f32_to_bf16(__fsub_rn(pv, bf16_to_f32(hb)));
                         ls[c] = __fadd_rn(ls[c], pv);
                     }
                 }
+                // keys past n_max up to the 16-key step boundary enter PV with p = 0
+                for (int j = n_max + tid; j < ((n_max + 15) & ~15); j += kAttnThreads)
+#pragma unroll
+                    for (int c = 0; c < S::kCols; ++c) sm.ph[0][c][j] = sm.ph[1][c][j] = 0;
 #pragma unroll
                 for (int c = 0; c < S::kCols; ++c) {
 #pragma unroll
@@ -300,12 +320,8 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
 #pragma unroll
                     for (int y = 0; y < 2; ++y) {
                         const int32_t key = j0 + kk + k2 + 8 * y;
-                        const float p0 = (c < S::kCols && key < n_max) ? sm.p[c][key] : 0.0f;
-                        const float p1 = (c < S::kCols && key + 1 < n_max) ? sm.p[c][key + 1] : 0.0f;
-                        const float h0 = __uint_as_float(static_cast<uint32_t>(f32_to_bf16(p0)) << 16);
-                        const float h1 = __uint_as_float(static_cast<uint32_t>(f32_to_bf16(p1)) << 16);
-                        bh[nb][y] = pack_bf16x2(h0, h1);
-                        bl[nb][y] = pack_bf16x2(__fsub_rn(p0, h0), __fsub_rn(p1, h1));
+                        bh[nb][y] = c < S::kCols ? *reinterpret_cast<const uint32_t*>(&sm.ph[0][c][key]) : 0u;
+                        bl[nb][y] = c < S::kCols ? *reinterpret_cast<const uint32_t*>(&sm.ph[1][c][key]) : 0u;
                     }
                 }
 #pragma unroll
@@ -407,14 +423,15 @@ decode_split_kernel(AttnGeom geo, EntryMap em, int32_t max_splits, int32_t chunk
                             geo.page_table + static_cast<int64_t>(en.r) * geo.max_pages, g, geo.Hkv, k0, n,
                             geo.scale, geo.max_pages, geo.num_pages, geo.status, qb, oacc);
     // stage the partials through the score buffer, then write whole rows
-    float* stage = &sm.p[0][0];  // [kCols][DH]
-    for_each_out<G, DH, 1>(oacc, [&](int c, int d, float v) { stage[c * DH + d] = v; });
+    constexpr int kOStride = DH + 4;
+    float* stage = &sm.p[0][0];  // [kCols][kOStride]
+    for_each_out<G, DH, 1>(oacc, [&](int c, int d, float v) { stage[c * kOStride + d] = v; });
     __syncthreads();
     const int64_t row0 = (static_cast<int64_t>(e) * geo.H + static_cast<int64_t>(g) * G) * max_splits + split;
     for (int i = threadIdx.x; i < S::kCols * (DH / 4); i += kAttnThreads) {
         const int c = i / (DH / 4), d4 = i % (DH / 4);
         reinterpret_cast<float4*>(ws_o + (row0 + static_cast<int64_t>(c) * max_splits) * DH)[d4] =
-            reinterpret_cast<const float4*>(stage + c * DH)[d4];
+            reinterpret_cast<const float4*>(stage + c * kOStride)[d4];
     }
     if (threadIdx.x < S::kCols) {
         const int c = threadIdx.x;
@@ -558,9 +575,10 @@ prefill_kernel(AttnGeom geo, EntryMap em, int32_t n_entries) {
             __syncthreads();
         }
         // out = O / L, staged through the score buffer; a token without keys gets zeros
-        float* stage = &sm.p[0][0];  // [kCols][DH]
+        constexpr int kOStride = DH + 4;
+        float* stage = &sm.p[0][0];  // [kCols][kOStride]
         for_each_out<G, DH, NT>(O, [&](int c, int d, float v) {
-            stage[c * DH + d] = keys[c / G] > 0 ? __fdiv_rn(v, sm.L[c]) : 0.0f;
+            stage[c * kOStride + d] = keys[c / G] > 0 ? __fdiv_rn(v, sm.L[c]) : 0.0f;
         });
         __syncthreads();
         for (int i = tid; i < S::kCols * (DH / 2); i += kAttnThreads) {
@@ -569,7 +587,7 @@ prefill_kernel(AttnGeom geo, EntryMap em, int32_t n_entries) {
             if (e0 + ti < e1)
                 store_out2(geo.out, geo.out_f32,
                            (static_cast<int64_t>(tok[ti]) * geo.H + static_cast<int64_t>(g) * G + c % G) * DH + 2 * dp,
-                           stage[c * DH + 2 * dp], stage[c * DH + 2 * dp + 1]);
+                           stage[c * kOStride + 2 * dp], stage[c * kOStride + 2 * dp + 1]);
         }
         __syncthreads();
         e0 = e1;
