@@ -172,6 +172,29 @@ def test_tiny_greedy_tokens_follow_total_order(mods, tiny):
         torch.cuda.synchronize()
 
 
+def test_tiny_bad_token_reports_status(mods, tiny):
+    """A token id outside the vocabulary is reported through the device status
+    word (the embedding gather reads it as a zero row) and does not disturb
+    the other requests of the step."""
+    bi, sched, _ = mods
+    eng, prompts = tiny
+    good = [int(t) for t in prompts[2][:5]]
+    table = np.zeros((2, eng.max_pages), np.int32)
+    table[0, 0], table[1, 0] = eng.pool.alloc(1)[0], eng.pool.alloc(1)[0]
+    try:
+        ref, _, _ = eng.step([5], [0], good, table[:1], [4])
+        ref = ref.clone()
+        eng.check()
+        logits, _, _ = eng.step([5, 3], [0, 0], good + [7, TINY.V + 3, 9], table, [4, 7])
+        torch.cuda.synchronize()
+        with pytest.raises(bi.BIError):
+            eng.check()
+        bi.reset_status(eng.status)
+        assert torch.equal(logits[0], ref[0])
+    finally:
+        eng.pool.free([int(table[0, 0]), int(table[1, 0])])
+
+
 # ---------------------------------------------------------------------------
 # 8B-shaped single layer (decode steps over random compositions)
 # ---------------------------------------------------------------------------

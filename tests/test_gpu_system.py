@@ -72,6 +72,45 @@ def test_unique_completions_under_random_schedules(mods):
     eng.close()
 
 
+def test_decode_throughput_invariant_vs_variant(mods):
+    """Greedy decode throughput of the multi-layer model at batch 64 (and 1),
+    invariant vs batch-variant mode (reported; variant is the faster one)."""
+    bi, sched, dvr, Engine = mods
+    n_layers, n_prompts, n_steps = (32, 64, 64) if FULL else (8, 64, 16)
+    cfg = LLAMA3_8B.with_layers(n_layers)
+    lens = [int(x) for x in synth.uniform_ints(n_prompts, 128, 4096, 42 + 6)]
+    max_pages = (4096 + n_steps + 15) // 16 + 1
+    eng = Engine(cfg, num_pages=sum((n + n_steps + 15) // 16 + 1 for n in lens) + 64, max_pages=max_pages,
+                 max_T=max(lens) + 64, max_B=n_prompts, max_R=n_prompts)
+    runner = sched.Runner(eng)
+    out = {}
+    for mode_name, mode in (("invariant", bi.INVARIANT), ("variant", bi.VARIANT)):
+        for b in (1, n_prompts):
+            reqs = [sched.Request(i, synth.token_ids(lens[i], cfg.V, 6000 + i)) for i in range(b)]
+            for r in reqs:  # prompts prefilled one by one (not timed)
+                logits, tokens, sl = runner.step([sched.StepItem(r, len(r.prompt), "last")], mode=mode)
+                r.generated.append(int(tokens[sl[0]][-1].item()))
+            torch.cuda.synchronize()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record()
+            for _ in range(n_steps):
+                items = [sched.StepItem(r, 1, "last") for r in reqs]
+                logits, tokens, sl = runner.step(items, mode=mode)
+                tok = tokens.tolist()
+                for r, s_ in zip(reqs, sl):
+                    r.generated.append(tok[s_.start])
+            e1.record()
+            torch.cuda.synchronize()
+            ms = e0.elapsed_time(e1) / n_steps
+            out[f"{mode_name}_bs{b}"] = {"ms_per_step": round(ms, 3), "tok_s": round(b / (ms * 1e-3), 1)}
+            for r in reqs:
+                runner.evict(r)
+    eng.check()
+    print(f"decode throughput, {n_layers} layers (host scheduler in the loop):", out)
+    assert out[f"variant_bs{n_prompts}"]["tok_s"] > 0 and out[f"invariant_bs{n_prompts}"]["tok_s"] > 0
+    eng.close()
+
+
 def test_decode_verify_rollback_commits_the_invariant_greedy_tokens(mods):
     bi, sched, dvr, Engine = mods
     n_layers, n_prompts, n_new, window = (32, 64, 256, 64) if FULL else (8, 16, 96, 32)
