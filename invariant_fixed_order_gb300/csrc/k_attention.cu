@@ -49,12 +49,30 @@ struct AttnShape {
     static_assert(kMT >= 1, "head dim too small");
 };
 
+// Scores (fp32; after PV, the outputs being stored) and the bf16 hi = bf16(p)
+// and lo = bf16(p - hi) parts of p that the PV MMAs read.  With few columns
+// (decode) the two share storage, which keeps a CTA small enough for six per
+// SM; with many (prefill) they are separate, which keeps registers down.
+template <int C, bool kShared>
+struct ScoreStore;
+template <int C>
+struct ScoreStore<C, true> {
+    union {
+        float p[C][kPStride];
+        uint16_t ph[2][C][kHStride];
+    };
+};
+template <int C>
+struct ScoreStore<C, false> {
+    float p[C][kPStride];
+    uint16_t ph[2][C][kHStride];
+};
+
 template <int G, int DH, int NT>
-struct AttnSmem {
+struct AttnSmem : ScoreStore<AttnShape<G, DH, NT>::kCols, (AttnShape<G, DH, NT>::kCols <= 8)> {
     using S = AttnShape<G, DH, NT>;
+    static constexpr bool kSharedScores = S::kCols <= 8;
     uint16_t ring[kRing][kSub][DH];  // K or V rows; 16-byte chunk c of row r sits at chunk c ^ (r & 7)
-    float p[S::kCols][kPStride];     // scores, then exp(score - m); after PV, the outputs being stored
-    uint16_t ph[2][S::kCols][kHStride];  // bf16 hi = bf16(p) and lo = bf16(p - hi), the PV operand
     float red[kWarps][S::kCols];     // per-warp partial sums of l
     float m[S::kCols];
     float l[S::kCols];
@@ -279,14 +297,47 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
                 float ls[S::kCols];
 #pragma unroll
                 for (int c = 0; c < S::kCols; ++c) ls[c] = 0.0f;
-                for (int j = tid; j < n_max; j += kAttnThreads) {
+                if constexpr (AttnSmem<G, DH, NT>::kSharedScores) {
+                    // the hi/lo parts overwrite the scores: each thread first takes
+                    // all of its scores (j = tid + 128i) into registers
+                    constexpr int kJ = BI_KV_CHUNK / kAttnThreads;
+                    uint32_t hl[kJ][S::kCols];  // hi | lo << 16
 #pragma unroll
-                    for (int c = 0; c < S::kCols; ++c) {
-                        const float pv = expf(__fsub_rn(sm.p[c][j], sm.m[c]));
-                        const uint16_t hb = f32_to_bf16(pv);
-                        sm.ph[0][c][j] = hb;
-                        sm.ph[1][c][j] = f32_to_bf16(__fsub_rn(pv, bf16_to_f32(hb)));
-                        ls[c] = __fadd_rn(ls[c], pv);
+                    for (int i = 0; i < kJ; ++i) {
+                        const int j = tid + i * kAttnThreads;
+                        if (j < n_max) {
+#pragma unroll
+                            for (int c = 0; c < S::kCols; ++c) {
+                                const float pv = expf(__fsub_rn(sm.p[c][j], sm.m[c]));
+                                const uint16_t hb = f32_to_bf16(pv);
+                                const uint16_t lb = f32_to_bf16(__fsub_rn(pv, bf16_to_f32(hb)));
+                                hl[i][c] = static_cast<uint32_t>(hb) | (static_cast<uint32_t>(lb) << 16);
+                                ls[c] = __fadd_rn(ls[c], pv);
+                            }
+                        }
+                    }
+                    __syncthreads();
+#pragma unroll
+                    for (int i = 0; i < kJ; ++i) {
+                        const int j = tid + i * kAttnThreads;
+                        if (j < n_max) {
+#pragma unroll
+                            for (int c = 0; c < S::kCols; ++c) {
+                                sm.ph[0][c][j] = static_cast<uint16_t>(hl[i][c] & 0xffffu);
+                                sm.ph[1][c][j] = static_cast<uint16_t>(hl[i][c] >> 16);
+                            }
+                        }
+                    }
+                } else {
+                    for (int j = tid; j < n_max; j += kAttnThreads) {
+#pragma unroll
+                        for (int c = 0; c < S::kCols; ++c) {
+                            const float pv = expf(__fsub_rn(sm.p[c][j], sm.m[c]));
+                            const uint16_t hb = f32_to_bf16(pv);
+                            sm.ph[0][c][j] = hb;
+                            sm.ph[1][c][j] = f32_to_bf16(__fsub_rn(pv, bf16_to_f32(hb)));
+                            ls[c] = __fadd_rn(ls[c], pv);
+                        }
                     }
                 }
                 // keys past n_max up to the 16-key step boundary enter PV with p = 0
