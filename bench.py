@@ -162,6 +162,15 @@ class GpuWorkload:
         self.eng.step([1] * b, [int(s) - 1 for s in self.ctx[:b]], self.d_ids[:b], self.d_table[:b],
                       list(range(b)), mode=mode, stream=stream, logits_out=self.logits[:b], tokens_out=self.tokens)
 
+    def step_layer(self, b: int, mode: int, stream=None):
+        """The layer alone (embedding + layer, no logit rows) over the first b requests."""
+        self.eng.step([1] * b, [int(s) - 1 for s in self.ctx[:b]], self.d_ids[:b], self.d_table[:b], [],
+                      mode=mode, stream=stream, want_logits=False)
+
+    def layer_bytes(self, b: int) -> int:
+        from invariant_fixed_order_gb300 import roofline
+        return roofline.decode_layer_bytes(self.cfg, [int(s) for s in self.ctx[:b]])
+
     def step_bytes(self, b: int) -> int:
         from invariant_fixed_order_gb300 import roofline
         return roofline.decode_step_bytes(self.cfg, [int(s) for s in self.ctx[:b]])
@@ -464,6 +473,10 @@ def run_ours(args):
                 row[name + "_tok_s"] = round(b / (t * 1e-3), 1)
                 row[name + "_us"] = round(t * 1e3, 1)
                 row[name + "_hbm_frac"] = round(w.step_bytes(b) / (t * 1e-3) / 1e9 / hbm_peak, 3)
+            # the layer alone against the layer's own bytes (weights once + this batch's KV + activations)
+            t = time_steps(lambda: w.step_layer(b, bi.INVARIANT), max(args.steps, 10), 3, stream)
+            row["invariant_layer_us"] = round(t * 1e3, 1)
+            row["invariant_layer_hbm_frac"] = round(w.layer_bytes(b) / (t * 1e-3) / 1e9 / hbm_peak, 3)
             sweep.append(row)
     w.eng.check()
 
