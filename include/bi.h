@@ -90,6 +90,7 @@ typedef enum {
 #define BI_DEV_TIMEOUT_MMA 0x102
 #define BI_DEV_TIMEOUT_EPILOGUE 0x103
 #define BI_DEV_TIMEOUT_DRAIN 0x104
+#define BI_DEV_TIMEOUT_ATTENTION 0x105  /* a K/V copy into an attention CTA did not land in time */
 #define BI_DEV_BAD_PAGE 0x201
 #define BI_DEV_BAD_POSITION 0x202
 #define BI_DEV_BAD_TOKEN 0x203

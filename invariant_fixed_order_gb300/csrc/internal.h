@@ -1,6 +1,7 @@
 // Host-side declarations shared by the translation units of libbi.
 #pragma once
 
+#include <cuda.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -105,6 +106,11 @@ cudaError_t launch_decode_attention(const AttnGeom& g, const EntryMap& em, int32
 cudaError_t launch_prefill_attention(const AttnGeom& g, const EntryMap& em, int32_t n_entries,
                                      cudaStream_t s);
 bool attention_supported(int32_t H, int32_t Hkv, int32_t Dh);
+
+// Tensor map over a paged K or V cache [num_pages, Hkv, 16, Dh] seen as rows
+// of Dh bf16 (row (page * Hkv + head) * 16 + slot), boxes of 16 rows x 64
+// elements with the 128-byte swizzle (k_gemm.cu owns the driver entry point).
+bool encode_kv_map(CUtensorMap* map, const bi_bf16* cache, int64_t num_pages, int32_t Hkv, int32_t Dh);
 
 // ---- GEMM (k_gemm.cu) ----
 struct GemmPlan {

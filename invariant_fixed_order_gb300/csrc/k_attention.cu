@@ -20,6 +20,7 @@
 
 #include "common.cuh"
 #include "internal.h"
+#include "tc_ptx.cuh"
 
 namespace bi {
 
@@ -68,11 +69,18 @@ struct ScoreStore<C, false> {
     uint16_t ph[2][C][kHStride];
 };
 
+// A ring stage holds kSub keys of K or V in the layout a 128-byte-swizzled TMA
+// box writes: per 64-element half of the head dim, kSub rows of 128 bytes, the
+// 16-byte chunk c of row r at chunk c ^ (r & 7).  The ring comes first so a
+// 1024-byte aligned dynamic shared memory base keeps every stage aligned.
 template <int G, int DH, int NT>
-struct AttnSmem : ScoreStore<AttnShape<G, DH, NT>::kCols, (AttnShape<G, DH, NT>::kCols <= 8)> {
+struct AttnSmem {
     using S = AttnShape<G, DH, NT>;
     static constexpr bool kSharedScores = S::kCols <= 8;
-    uint16_t ring[kRing][kSub][DH];  // K or V rows; 16-byte chunk c of row r sits at chunk c ^ (r & 7)
+    uint8_t ring[kRing][kSub * DH * 2];
+    ScoreStore<S::kCols, kSharedScores> sc;
+    uint64_t full[kRing];            // TMA completion per ring stage
+    int32_t abort;                   // a copy did not land: issue no more
     float red[kWarps][S::kCols];     // per-warp partial sums of l
     float m[S::kCols];
     float l[S::kCols];
@@ -143,10 +151,31 @@ __device__ __forceinline__ void mma_16816(float (&d)[4], const uint32_t (&a)[4],
         : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
         : "r"(a[0]), "r"(a[1]), "r"(a[2]), "r"(a[3]), "r"(b0), "r"(b1));
 }
-// Byte offset of (row, 16-byte chunk c) in a swizzled ring stage.
+// Byte offset of (row, 16-byte chunk c) in a ring stage (layout above).
 template <int DH>
 __device__ __forceinline__ uint32_t ring_off(int row, int c) {
-    return static_cast<uint32_t>(row * DH * 2 + ((c ^ (row & 7)) << 4));
+    return static_cast<uint32_t>((c >> 3) * (kSub * 128) + row * 128 + (((c & 7) ^ (row & 7)) << 4));
+}
+
+// One-time setup of a CTA's ring barriers (thread 0; a barrier must follow).
+template <typename Sm>
+__device__ __forceinline__ void ring_init(Sm& sm) {
+    if (threadIdx.x == 0) {
+        for (int s = 0; s < kRing; ++s) ptx::mbar_init(&sm.full[s], 1);
+        sm.abort = 0;
+        ptx::fence_barrier_init();
+    }
+}
+
+// Bounded wait for a ring stage's TMA copies (every thread waits).
+__device__ __forceinline__ bool wait_stage(uint64_t* bar, uint32_t parity) {
+    const uint32_t a = smem_u32(bar);
+    if (ptx::mbar_try_wait(a, parity)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (uint32_t i = 1;; ++i) {
+        if (ptx::mbar_try_wait(a, parity)) return true;
+        if ((i & 255u) == 0u && globaltimer_ns() - t0 > kWaitLimitNs) return false;
+    }
 }
 
 // Query fragments as the B operand of the score MMAs: column c = nb*8 + lane/4
@@ -188,11 +217,15 @@ __device__ __forceinline__ void load_q_cols(const uint16_t* q, const int32_t (&t
 //       hi product then the lo product accumulated in fp32.
 // A key a column does not attend to gets p = 0, which adds exact zeros, so a
 // column's bits do not depend on the other columns of its CTA.  K and V rows
-// stream through a ring of kRing shared-memory stages of kSub keys each
-// (cp.async), K sub-chunks first, then V sub-chunks.
+// stream through a ring of kRing shared-memory stages of kSub keys each, K
+// sub-chunks first, then V sub-chunks: as TMA boxes of one 16-key page of the
+// KV head (two boxes per page at DH = 128) when the chunk starts on a page,
+// else by cp.async into the same layout.  phase tracks the stages' mbarrier
+// parities across calls.
 template <int G, int DH, int NT>
 __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uint16_t* __restrict__ kc,
-                                              const uint16_t* __restrict__ vc, const int32_t* page_row,
+                                              const uint16_t* __restrict__ vc, const CUtensorMap* tmK,
+                                              const CUtensorMap* tmV, uint32_t& phase, const int32_t* page_row,
                                               int32_t g, int32_t Hkv, int32_t k0, int32_t n_max, float scale,
                                               int32_t max_pages, int32_t num_pages, int32_t* status,
                                               const uint32_t (&qb)[AttnShape<G, DH, NT>::kNB][DH / 16][2],
@@ -216,25 +249,52 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
 
     const int ns = (n_max + kSub - 1) / kSub;  // sub-chunks of K, then as many of V
     const int part = tid % kVecPerRow;         // this thread's 16-byte column of every row it copies
+    // TMA boxes start on a page; the ring must sit on a 1024-byte boundary for the swizzle
+    const bool use_tma = (k0 & (BI_PAGE - 1)) == 0 && (smem_u32(&sm.ring[0][0]) & 1023u) == 0;
+    constexpr int kHalves = DH / 64;
+    // Stages with a TMA copy still to be waited for.  Every thread derives it
+    // from the same values (sm.abort is only read after a barrier), so every
+    // thread waits on the same stages and tracks the same barrier parities.
+    uint32_t issued = 0;
     auto issue = [&](int t) {
         if (t < 2 * ns) {
             const bool is_v = t >= ns;
             const int32_t j0 = (is_v ? t - ns : t) * kSub;
             const int32_t nk = min(kSub, n_max - j0);
-            const uint16_t* base = (is_v ? vc : kc) + static_cast<int64_t>(g) * BI_PAGE * DH + part * 8;
-            unsigned char* dst = reinterpret_cast<unsigned char*>(sm.ring[t % kRing]);
-            for (int jl = tid / kVecPerRow; jl < nk; jl += kAttnThreads / kVecPerRow) {
-                const int32_t kp = k0 + j0 + jl;
-                const int64_t pg = sm.pages[kp / BI_PAGE - lp0];
-                cp_async16(dst + ring_off<DH>(jl, part), base + (pg * Hkv * BI_PAGE + (kp & (BI_PAGE - 1))) * DH);
+            uint8_t* dst = sm.ring[t % kRing];
+            if (use_tma) {
+                if (sm.abort) return;
+                issued |= 1u << (t % kRing);
+                if (tid == 0) {
+                    const int npg = (nk + BI_PAGE - 1) / BI_PAGE;
+                    const CUtensorMap* map = is_v ? tmV : tmK;
+                    uint64_t* bar = &sm.full[t % kRing];
+                    ptx::fence_proxy_async_smem();  // earlier generic writes to the stage before the copy
+                    ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(npg * kHalves * BI_PAGE * 128));
+                    for (int i = 0; i < npg; ++i) {
+                        const int32_t pg = sm.pages[(k0 + j0) / BI_PAGE - lp0 + i];
+                        const int32_t y = (pg * Hkv + g) * BI_PAGE;
+#pragma unroll
+                        for (int h = 0; h < kHalves; ++h)
+                            ptx::tma_load_2d(dst + h * (kSub * 128) + i * (BI_PAGE * 128), map, bar, h * 64, y);
+                    }
+                }
+            } else {
+                const uint16_t* base = (is_v ? vc : kc) + static_cast<int64_t>(g) * BI_PAGE * DH + part * 8;
+                for (int jl = tid / kVecPerRow; jl < nk; jl += kAttnThreads / kVecPerRow) {
+                    const int32_t kp = k0 + j0 + jl;
+                    const int64_t pg = sm.pages[kp / BI_PAGE - lp0];
+                    cp_async16(dst + ring_off<DH>(jl, part),
+                               base + (pg * Hkv * BI_PAGE + (kp & (BI_PAGE - 1))) * DH);
+                }
+                // rows past the last key up to the 16-key step boundary are read by
+                // the MMAs (K: scores never stored; V: times p = 0): zero, not stale
+                const int32_t pad_end = min(kSub, (nk + 15) & ~15);
+                for (int jl = nk + tid / kVecPerRow; jl < pad_end; jl += kAttnThreads / kVecPerRow)
+                    *reinterpret_cast<uint4*>(dst + ring_off<DH>(jl, part)) = make_uint4(0, 0, 0, 0);
             }
-            // rows past the last key up to the 16-key step boundary are read by
-            // the MMAs (K: scores never stored; V: times p = 0): zero, not stale
-            const int32_t pad_end = min(kSub, (nk + 15) & ~15);
-            for (int jl = nk + tid / kVecPerRow; jl < pad_end; jl += kAttnThreads / kVecPerRow)
-                *reinterpret_cast<uint4*>(dst + ring_off<DH>(jl, part)) = make_uint4(0, 0, 0, 0);
         }
-        cp_async_commit();  // possibly empty: keeps one group per sub-chunk slot
+        if (!use_tma) cp_async_commit();  // possibly empty: keeps one group per sub-chunk slot
     };
 #pragma unroll
     for (int t = 0; t < kRing; ++t) issue(t);
@@ -254,9 +314,32 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
         }
 
     for (int t = 0; t < 2 * ns; ++t) {
-        asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 1) : "memory");
+        const int st = t % kRing;
+        if (use_tma) {
+            if (issued & (1u << st)) {
+                issued &= ~(1u << st);
+                if (!wait_stage(&sm.full[st], (phase >> st) & 1u)) {
+                    report(status, BI_DEV_TIMEOUT_ATTENTION);
+                    sm.abort = 1;
+                }
+                phase ^= 1u << st;
+                // a page box also brings the rows past the last key: in V they
+                // meet p = 0 in the MMAs, so they must be zeros, not stale values
+                const int32_t j0 = (t - ns) * kSub;
+                const int32_t nk = min(kSub, n_max - j0);
+                if (t >= ns && (nk & 15)) {
+                    const int32_t pad_end = (nk + 15) & ~15;
+                    for (int i = tid; i < (pad_end - nk) * kVecPerRow; i += kAttnThreads)
+                        *reinterpret_cast<uint4*>(sm.ring[st] + ring_off<DH>(nk + i / kVecPerRow, i % kVecPerRow)) =
+                            make_uint4(0, 0, 0, 0);
+                    ptx::fence_proxy_async_smem();  // before the stage's next TMA write
+                }
+            }
+        } else {
+            asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 1) : "memory");
+        }
         __syncthreads();
-        const uint32_t buf = smem_u32(sm.ring[t % kRing]);
+        const uint32_t buf = smem_u32(sm.ring[st]);
         if (t < ns) {
             // scores: warp w takes keys 16w .. 16w+15 of the sub-chunk as the MMA rows
             const int32_t j0 = t * kSub;
@@ -279,7 +362,7 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
                         const int c = nb * 8 + k2 + (x & 1);
                         const int32_t key = j0 + warp * 16 + c8 + (x >> 1) * 8;
                         if (c < S::kCols && key < n_max)
-                            sm.p[c][key] = key < ncol_r[nb][x & 1] ? __fmul_rn(acc[nb][x], scale) : -INFINITY;
+                            sm.sc.p[c][key] = key < ncol_r[nb][x & 1] ? __fmul_rn(acc[nb][x], scale) : -INFINITY;
                     }
             }
             if (t == ns - 1) {
@@ -287,7 +370,7 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
                 // m: exact max per column (order-free); a column without keys gets 0
                 for (int c = warp; c < S::kCols; c += kWarps) {
                     float mx = -INFINITY;
-                    for (int j = lane; j < n_max; j += 32) mx = fmaxf(mx, sm.p[c][j]);
+                    for (int j = lane; j < n_max; j += 32) mx = fmaxf(mx, sm.sc.p[c][j]);
 #pragma unroll
                     for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
                     if (lane == 0) sm.m[c] = sm.ncol[c] > 0 ? mx : 0.0f;
@@ -308,7 +391,7 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
                         if (j < n_max) {
 #pragma unroll
                             for (int c = 0; c < S::kCols; ++c) {
-                                const float pv = expf(__fsub_rn(sm.p[c][j], sm.m[c]));
+                                const float pv = expf(__fsub_rn(sm.sc.p[c][j], sm.m[c]));
                                 const uint16_t hb = f32_to_bf16(pv);
                                 const uint16_t lb = f32_to_bf16(__fsub_rn(pv, bf16_to_f32(hb)));
                                 hl[i][c] = static_cast<uint32_t>(hb) | (static_cast<uint32_t>(lb) << 16);
@@ -323,8 +406,8 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
                         if (j < n_max) {
 #pragma unroll
                             for (int c = 0; c < S::kCols; ++c) {
-                                sm.ph[0][c][j] = static_cast<uint16_t>(hl[i][c] & 0xffffu);
-                                sm.ph[1][c][j] = static_cast<uint16_t>(hl[i][c] >> 16);
+                                sm.sc.ph[0][c][j] = static_cast<uint16_t>(hl[i][c] & 0xffffu);
+                                sm.sc.ph[1][c][j] = static_cast<uint16_t>(hl[i][c] >> 16);
                             }
                         }
                     }
@@ -332,10 +415,10 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
                     for (int j = tid; j < n_max; j += kAttnThreads) {
 #pragma unroll
                         for (int c = 0; c < S::kCols; ++c) {
-                            const float pv = expf(__fsub_rn(sm.p[c][j], sm.m[c]));
+                            const float pv = expf(__fsub_rn(sm.sc.p[c][j], sm.m[c]));
                             const uint16_t hb = f32_to_bf16(pv);
-                            sm.ph[0][c][j] = hb;
-                            sm.ph[1][c][j] = f32_to_bf16(__fsub_rn(pv, bf16_to_f32(hb)));
+                            sm.sc.ph[0][c][j] = hb;
+                            sm.sc.ph[1][c][j] = f32_to_bf16(__fsub_rn(pv, bf16_to_f32(hb)));
                             ls[c] = __fadd_rn(ls[c], pv);
                         }
                     }
@@ -343,7 +426,7 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
                 // keys past n_max up to the 16-key step boundary enter PV with p = 0
                 for (int j = n_max + tid; j < ((n_max + 15) & ~15); j += kAttnThreads)
 #pragma unroll
-                    for (int c = 0; c < S::kCols; ++c) sm.ph[0][c][j] = sm.ph[1][c][j] = 0;
+                    for (int c = 0; c < S::kCols; ++c) sm.sc.ph[0][c][j] = sm.sc.ph[1][c][j] = 0;
 #pragma unroll
                 for (int c = 0; c < S::kCols; ++c) {
 #pragma unroll
@@ -371,8 +454,8 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
 #pragma unroll
                     for (int y = 0; y < 2; ++y) {
                         const int32_t key = j0 + kk + k2 + 8 * y;
-                        bh[nb][y] = c < S::kCols ? *reinterpret_cast<const uint32_t*>(&sm.ph[0][c][key]) : 0u;
-                        bl[nb][y] = c < S::kCols ? *reinterpret_cast<const uint32_t*>(&sm.ph[1][c][key]) : 0u;
+                        bh[nb][y] = c < S::kCols ? *reinterpret_cast<const uint32_t*>(&sm.sc.ph[0][c][key]) : 0u;
+                        bl[nb][y] = c < S::kCols ? *reinterpret_cast<const uint32_t*>(&sm.sc.ph[1][c][key]) : 0u;
                     }
                 }
 #pragma unroll
@@ -391,7 +474,7 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
         __syncthreads();
         issue(t + kRing);
     }
-    cp_async_wait_all();
+    if (!use_tma) cp_async_wait_all();
     __syncthreads();
 }
 
@@ -444,8 +527,9 @@ __device__ __forceinline__ void pieces(int32_t s, int32_t chunk2, int32_t& size,
 // Decode: grid (entries, Hkv, max_splits); one token, its G heads as columns.
 // ---------------------------------------------------------------------------
 template <int G, int DH>
-__global__ void __launch_bounds__(kAttnThreads)
-decode_split_kernel(AttnGeom geo, EntryMap em, int32_t max_splits, int32_t chunk2, float* __restrict__ ws_o,
+__global__ void __launch_bounds__(kAttnThreads, 6)
+decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnGeom geo,
+                    EntryMap em, int32_t max_splits, int32_t chunk2, float* __restrict__ ws_o,
                     float* __restrict__ ws_ml) {
     pdl_trigger();
     pdl_wait();
@@ -466,16 +550,19 @@ decode_split_kernel(AttnGeom geo, EntryMap em, int32_t max_splits, int32_t chunk
     const int32_t k0 = split * size;
     const int32_t n = min(size, s - k0);
     if (threadIdx.x < S::kCols) sm.ncol[threadIdx.x] = n;
+    ring_init(sm);
+    uint32_t phase = 0;
     const int32_t tok[1] = {en.t};
     uint32_t qb[S::kNB][DH / 16][2];
     load_q_cols<G, DH, 1>(reinterpret_cast<const uint16_t*>(geo.q), tok, geo.H, g, qb);
     float oacc[S::kMT][S::kNB][4];
     chunk_partial<G, DH, 1>(sm, reinterpret_cast<const uint16_t*>(geo.kc), reinterpret_cast<const uint16_t*>(geo.vc),
-                            geo.page_table + static_cast<int64_t>(en.r) * geo.max_pages, g, geo.Hkv, k0, n,
+                            &tmK, &tmV, phase, geo.page_table + static_cast<int64_t>(en.r) * geo.max_pages, g,
+                            geo.Hkv, k0, n,
                             geo.scale, geo.max_pages, geo.num_pages, geo.status, qb, oacc);
     // stage the partials through the score buffer, then write whole rows
     constexpr int kOStride = DH + 4;
-    float* stage = &sm.p[0][0];  // [kCols][kOStride]
+    float* stage = &sm.sc.p[0][0];  // [kCols][kOStride]
     for_each_out<G, DH, 1>(oacc, [&](int c, int d, float v) { stage[c * kOStride + d] = v; });
     __syncthreads();
     const int64_t row0 = (static_cast<int64_t>(e) * geo.H + static_cast<int64_t>(g) * G) * max_splits + split;
@@ -549,7 +636,8 @@ decode_merge_kernel(AttnGeom geo, EntryMap em, int32_t max_splits, int32_t chunk
 // ---------------------------------------------------------------------------
 template <int G, int DH, int NT>
 __global__ void __launch_bounds__(kAttnThreads)
-prefill_kernel(AttnGeom geo, EntryMap em, int32_t n_entries) {
+prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnGeom geo,
+               EntryMap em, int32_t n_entries) {
     pdl_trigger();
     pdl_wait();
     using S = AttnShape<G, DH, NT>;
@@ -559,6 +647,8 @@ prefill_kernel(AttnGeom geo, EntryMap em, int32_t n_entries) {
     const int32_t e_begin = static_cast<int32_t>(blockIdx.x) * NT;
     const int32_t e_end = min(e_begin + NT, n_entries);
     const int tid = threadIdx.x;
+    ring_init(sm);
+    uint32_t phase = 0;
     for (int32_t e0 = e_begin; e0 < e_end;) {
         const Entry first = get_entry(em, e0);
         int32_t e1 = e0 + 1;
@@ -589,7 +679,8 @@ prefill_kernel(AttnGeom geo, EntryMap em, int32_t n_entries) {
             if (tid < S::kCols) sm.ncol[tid] = min(max(keys[tid / G] - k0, 0), BI_KV_CHUNK);
             float o[S::kMT][S::kNB][4];
             chunk_partial<G, DH, NT>(sm, reinterpret_cast<const uint16_t*>(geo.kc),
-                                     reinterpret_cast<const uint16_t*>(geo.vc), page_row, g, geo.Hkv, k0,
+                                     reinterpret_cast<const uint16_t*>(geo.vc), &tmK, &tmV, phase, page_row, g,
+                                     geo.Hkv, k0,
                                      min(BI_KV_CHUNK, s_max - k0), geo.scale, geo.max_pages, geo.num_pages,
                                      geo.status, qb, o);
             // the decode merge's fold (fold_step), one column's (M, L) at a time
@@ -627,7 +718,7 @@ prefill_kernel(AttnGeom geo, EntryMap em, int32_t n_entries) {
         }
         // out = O / L, staged through the score buffer; a token without keys gets zeros
         constexpr int kOStride = DH + 4;
-        float* stage = &sm.p[0][0];  // [kCols][kOStride]
+        float* stage = &sm.sc.p[0][0];  // [kCols][kOStride]
         for_each_out<G, DH, NT>(O, [&](int c, int d, float v) {
             stage[c * kOStride + d] = keys[c / G] > 0 ? __fdiv_rn(v, sm.L[c]) : 0.0f;
         });
@@ -693,9 +784,12 @@ static cudaError_t launch_decode_t(const AttnGeom& g, const EntryMap& em, int32_
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
+    CUtensorMap tmK, tmV;
+    if (!encode_kv_map(&tmK, g.kc, g.num_pages, g.Hkv, DH) || !encode_kv_map(&tmV, g.vc, g.num_pages, g.Hkv, DH))
+        return cudaErrorInvalidValue;
     dim3 grid(n, g.Hkv, max_splits);
-    cudaError_t e = launch_pdl(decode_split_kernel<G, DH>, grid, dim3(kAttnThreads), smem, s, g, em, max_splits,
-                               chunk2, ws_o, ws_ml);
+    cudaError_t e = launch_pdl(decode_split_kernel<G, DH>, grid, dim3(kAttnThreads), smem, s, tmK, tmV, g, em,
+                               max_splits, chunk2, ws_o, ws_ml);
     if (e != cudaSuccess) return e;
     return launch_pdl(decode_merge_kernel<DH>, dim3(n, g.H), dim3(DH / 2), 0, s, g, em, max_splits, chunk2,
                       static_cast<const float*>(ws_o), static_cast<const float*>(ws_ml));
@@ -716,8 +810,11 @@ static cudaError_t launch_prefill_t(const AttnGeom& g, const EntryMap& em, int32
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
-    return launch_pdl(prefill_kernel<G, DH, NT>, dim3((n + NT - 1) / NT, g.Hkv), dim3(kAttnThreads), smem, s, g, em,
-                      n);
+    CUtensorMap tmK, tmV;
+    if (!encode_kv_map(&tmK, g.kc, g.num_pages, g.Hkv, DH) || !encode_kv_map(&tmV, g.vc, g.num_pages, g.Hkv, DH))
+        return cudaErrorInvalidValue;
+    return launch_pdl(prefill_kernel<G, DH, NT>, dim3((n + NT - 1) / NT, g.Hkv), dim3(kAttnThreads), smem, s, tmK,
+                      tmV, g, em, n);
 }
 
 #define BI_ATTN_DISPATCH(FN, ...)                                              \

@@ -478,6 +478,18 @@ static bool make_kslab_map(CUtensorMap* map, const void* base, uint64_t K, uint6
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_kv_map(CUtensorMap* map, const bi_bf16* cache, int64_t num_pages, int32_t Hkv, int32_t Dh) {
+    auto fn = encode_fn();
+    if (!fn) return false;
+    cuuint64_t dims[2] = {static_cast<cuuint64_t>(Dh), static_cast<cuuint64_t>(num_pages) * Hkv * BI_PAGE};
+    cuuint64_t strides[1] = {static_cast<cuuint64_t>(Dh) * 2};
+    cuuint32_t box[2] = {64, BI_PAGE};
+    cuuint32_t estr[2] = {1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<bi_bf16*>(cache), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 GemmPlan gemm_plan(int64_t M, int32_t N, int32_t K, bi_mode mode) {
     GemmPlan p{1};
     if (mode != BI_VARIANT || M <= 0) return p;

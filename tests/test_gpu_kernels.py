@@ -246,9 +246,11 @@ def test_decode_variant_mode_differs_somewhere(bi):
         assert same == (mode == bi.INVARIANT)
 
 
-def test_prefill_matches_decode_bitwise(bi):
-    """The output at position p is the same bits from prefill (any chunking) and from decode at s = p + 1."""
-    H, Hkv, Dh = 32, 8, 128
+@pytest.mark.parametrize("H,Hkv,Dh", [(32, 8, 128), (8, 8, 128), (4, 2, 64), (16, 2, 128), (8, 1, 64)])
+def test_prefill_matches_decode_bitwise(bi, H, Hkv, Dh):
+    """The output at position p is the same bits from prefill (any chunking) and from decode at s = p + 1
+    (GQA groups of 1, 2, 4 and 8 heads: 16, 8, 4 and 2 query tokens per prefill CTA)."""
+    G = H // Hkv
     n = 600
     kv, hist, _ = make_decode_case([n], H, Hkv, Dh, seed=6)
     q = synth.normal_bf16((n, H, Dh), 1.0, 77, "cuda")
@@ -274,8 +276,8 @@ def test_prefill_matches_decode_bitwise(bi):
     qf = f32(q)
     pre_f = pre.view(np.float32)
     for p in (0, 255, 256, 599):
-        for h in (0, 5, 31):
-            g = h // 4
+        for h in (0, H // 2 + 1, H - 1):
+            g = h // G
             ref = oracle.attention_head(qf[p, h], k[:p + 1, g], v[:p + 1, g])
             assert np.max(np.abs(pre_f[p, h] - ref)) <= ATTN_MAX_ABS
 
