@@ -171,12 +171,17 @@ bi_status bi_rope_table(float* cos_out, float* sin_out, int32_t n_pos, int32_t D
  * attention reductions") -----------------------------------------------------
  * For query head h (kv head h / (H/Hkv)) of a token at position p: keys
  * 0..p of its request, cut into chunks [256j, min(256j + 256, p + 1)).  Per
- * chunk, in fp32: s = (q . k) * scale (each dot product: 16 (or Dh/8)
- * elements per lane in order, then an xor-butterfly over 8 lanes), m = max s,
- * l = sum_key exp(s - m) and o = sum_key exp(s - m) v, both in ascending key
- * order.  Chunks merge in ascending order: state (M, L, O) starts at chunk 0;
- * each next chunk gives M' = max(M, m), L' = L e^(M-M') + l e^(m-M'),
- * O' = O e^(M-M') + o e^(m-M'); the output is O / L.
+ * chunk, in fp32: s_j = (k_j . q) * scale, the dot product on the tensor
+ * cores (bf16 products, fp32 accumulation over 16-deep steps of the head dim
+ * in ascending order); m = max_j s_j; p_j = exp(s_j - m); l = sum_j p_j in a
+ * fixed tree (per thread t of 128 the serial sum over j = t, t + 128, then an
+ * xor-butterfly over each warp's 32 lanes, then the 4 warps in order);
+ * o = sum_j p_j v_j on the tensor cores with p_j split into bf16 hi and lo
+ * parts, 16-key steps in ascending order.  Chunks merge in ascending order:
+ * state (M, L, O) starts at chunk 0; each next chunk gives M' = max(M, m),
+ * L' = L e^(M-M') + l e^(m-M'), O' = O e^(M-M') + o e^(m-M'); the output is
+ * O / L.  Decode and prefill run the same per-chunk arithmetic and the same
+ * merge, so a position's output has the same bits from either.
  * Supported: Dh in {64, 128}, H / Hkv in {1, 2, 4, 8}.
  *
  * bi_decode_attention: one query per request at position seq_lens[i] - 1
@@ -308,11 +313,16 @@ size_t bi_forward_workspace_size(const bi_model_config* cfg, int32_t max_T, int3
 
 /* Embedding -> n_layers x (RMSNorm, QKV GEMM, RoPE + KV append, attention,
  * O GEMM + residual, RMSNorm, gate/up GEMM + SwiGLU, down GEMM + residual) ->
- * final RMSNorm of the logit rows -> LM head (fp32) -> greedy argmax.
- * logits_out: DEVICE [R, V] fp32 or NULL; tokens_out: DEVICE [R] or NULL;
- * hidden_out: DEVICE [T, d] bf16 residual stream after the last layer, or NULL.
+ * final RMSNorm of the logit rows -> LM head (fp32) -> greedy argmax (taken in
+ * the LM head's epilogue: the same tokens as bi_argmax of the logits).
+ * logits_out: DEVICE [R, V] fp32 or NULL (then no logits are stored when
+ * tokens_out is given); tokens_out: DEVICE [R] or NULL; hidden_out: DEVICE
+ * [T, d] bf16 residual stream after the last layer, or NULL.  ws: DEVICE
+ * scratch of bi_forward_workspace_size bytes, 16-byte aligned.
  * Copies the step's small metadata (token positions and lists) host to device
- * on `stream`. */
+ * on `stream`.  The step's first kernel waits for all earlier work on
+ * `stream`; the weights must not be written by work still in flight on other
+ * streams while a step runs. */
 bi_status bi_forward_step(bi_model* m, const bi_batch* batch, const bi_kv_cache* kv,
                           float* logits_out, int32_t* tokens_out, bi_bf16* hidden_out,
                           bi_mode mode, void* ws, size_t ws_bytes, int32_t* dev_status,
