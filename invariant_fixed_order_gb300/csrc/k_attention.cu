@@ -3,16 +3,17 @@
 // "1 · Split-K and segmented attention reductions": the split count is
 // ceil(seq_len / tile), a function of the request's own length).
 //
-// One device function computes the fp32 partial (m, l, o) of G query heads
-// (one GQA group) of one query against one chunk of keys.  Decode runs it in
-// one CTA per (query, kv head, chunk) and merges the partials in a second
-// kernel; prefill runs it chunk after chunk in one CTA per (query, kv head)
-// and folds as it goes.  Both use the same chunk boundaries (multiples of
-// BI_KV_CHUNK from key 0), the same partial and the same fold, so a token's
-// output has the same bits whichever path, batch or prefill chunking
-// produced it.  Every floating-point step below is an explicit round-to-
-// nearest intrinsic so the compiler cannot fuse or reorder it differently in
-// the two kernels.
+// One device function computes the fp32 partial (m, l, o) of one chunk of
+// keys for a set of (query, head) columns: the G heads of one GQA group of one
+// query (decode) or of 16/G consecutive queries of one request (prefill).
+// Decode runs it in one CTA per (query, kv head, chunk) and merges the
+// partials in a second kernel; prefill runs it chunk after chunk in one CTA
+// per (query block, kv head) and folds as it goes.  Both use the same chunk
+// boundaries (multiples of BI_KV_CHUNK from key 0), the same per-column
+// partial and the same fold, so a token's output has the same bits whichever
+// path, batch or prefill chunking produced it.  Every floating-point step
+// outside the MMAs is an explicit round-to-nearest intrinsic so the compiler
+// cannot fuse or reorder it differently in the two kernels.
 #include <math.h>
 
 #include <mutex>
