@@ -327,13 +327,14 @@ def test_8b_layer_variant_mode_negative_control(mods, layer8b):
 # ---------------------------------------------------------------------------
 
 def test_8b_continuous_batching_fuzz(mods):
-    """Chunked prefill (256-2048) co-scheduled with decode requests, random
-    arrival order, preemption and evict/readmit: every produced logits row
-    equals the solo run bit for bit."""
+    """Chunked prefill (256-2048) co-scheduled with decode requests (contexts
+    up to 32768), random arrival order, preemption and evict/readmit: every
+    produced logits row equals the solo run bit for bit."""
     bi, sched, Engine = mods
     cfg = LLAMA3_8B_1L
     rng = np.random.default_rng(1003)
-    long_lens = rng.integers(512, 12000, 3)
+    long_lens = rng.integers(512, 32768, 3)  # decode contexts up to 32768 positions
+    long_lens[0] = 32760
     short_lens = rng.integers(256, 2048, 3)
     lens = [int(x) for x in np.concatenate([long_lens, short_lens])]
     prompts = [synth.token_ids(n, cfg.V, 900 + i) for i, n in enumerate(lens)]

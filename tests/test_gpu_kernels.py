@@ -211,6 +211,30 @@ def test_decode_attention_parity(bi, H, Hkv, Dh):
     assert err <= ATTN_MAX_ABS, err
 
 
+def test_decode_attention_long_contexts(bi):
+    """Contexts up to 32768 positions (128 splits): oracle parity on sampled heads,
+    the same bits alone and batched, and the batch-variant plan within tolerance."""
+    H, Hkv, Dh = 32, 8, 128
+    seq_lens = [32768, 20001, 4097, 1]
+    kv, hist, q = make_decode_case(seq_lens, H, Hkv, Dh, seed=11)
+    table = kv.table_tensor()
+    sl = torch.tensor(seq_lens, dtype=torch.int32, device="cuda")
+    st = bi.new_status()
+    full = bi.decode_attention(q, kv.k[0], kv.v[0], table, sl, max(seq_lens), out_dtype=bi.F32, status=st)
+    bi.check_status(st)
+    qf, out = f32(q), f32(full)
+    for i in range(len(seq_lens)):
+        k, v = hist[i]
+        for h in (0, 13, 31):
+            ref = oracle.attention_head(qf[i, h], k[:, h // 4], v[:, h // 4])
+            assert np.max(np.abs(out[i, h] - ref)) <= ATTN_MAX_ABS, (i, h)
+    alone = bi.decode_attention(q[:1].contiguous(), kv.k[0], kv.v[0], table[:1].contiguous(), sl[:1].contiguous(),
+                                seq_lens[0], out_dtype=bi.F32)
+    assert np.array_equal(bits(alone)[0], bits(full)[0])
+    var = bi.decode_attention(q, kv.k[0], kv.v[0], table, sl, max(seq_lens), out_dtype=bi.F32, mode=bi.VARIANT)
+    assert np.max(np.abs(f32(var) - out)) <= 2 * ATTN_MAX_ABS
+
+
 def test_decode_attention_batch_invariance(bi):
     H, Hkv, Dh = 32, 8, 128
     rng = np.random.default_rng(9)
