@@ -523,7 +523,7 @@ struct Layout {
 // sequence of every output element is the same for all layouts.
 Layout choose_layout(int64_t M, int32_t N, int32_t K) {
     Layout L{};
-    L.bn = (M > 2 * kBM && N % 256 == 0 && 256 % kUN == 0) ? 256 : kUN;
+    L.bn = (M > 2 * kBM && N % 256 == 0) ? 256 : kUN;
     int32_t box = 16;
     while (box < kBM && box < M) box *= 2;
     if (L.bn == 256) box = kBM;
@@ -546,17 +546,14 @@ Layout choose_layout(int64_t M, int32_t N, int32_t K) {
 template <int BN>
 cudaError_t launch_tiles(const CUtensorMap& tmA, const CUtensorMap& tmW, const GemmArgs& a, dim3 grid, size_t smem,
                          cudaStream_t s) {
-    if constexpr (BN % kUN != 0) {
-        return cudaErrorInvalidValue;
-    } else {
-        static std::once_flag once;
-        static cudaError_t err = cudaSuccess;
-        std::call_once(once, [] {
-            err = cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
-        });
-        if (err != cudaSuccess) return err;
-        return launch_pdl(gemm_tc_kernel<BN>, grid, dim3(kGemmThreads), smem, s, tmA, tmW, a);
-    }
+    static_assert(BN % kUN == 0, "a CTA tile is a whole number of MMAs wide");
+    static std::once_flag once;
+    static cudaError_t err = cudaSuccess;
+    std::call_once(once, [] {
+        err = cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+    });
+    if (err != cudaSuccess) return err;
+    return launch_pdl(gemm_tc_kernel<BN>, grid, dim3(kGemmThreads), smem, s, tmA, tmW, a);
 }
 
 }  // namespace
@@ -622,9 +619,8 @@ bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype
     a.total_tiles = static_cast<int32_t>(tiles);
     const int64_t ctas = std::min<int64_t>(tiles, std::max(1, num_sms() / plan.splits));
     dim3 grid(static_cast<unsigned>(ctas), plan.splits);
-    cudaError_t e = L.bn == 256   ? launch_tiles<256>(tmA, tmW, a, grid, L.smem, s)
-                    : L.bn == 128 ? launch_tiles<128>(tmA, tmW, a, grid, L.smem, s)
-                                  : launch_tiles<64>(tmA, tmW, a, grid, L.smem, s);
+    cudaError_t e = L.bn == 256 ? launch_tiles<256>(tmA, tmW, a, grid, L.smem, s)
+                                : launch_tiles<kUN>(tmA, tmW, a, grid, L.smem, s);
     if (e != cudaSuccess) return cuda_fail(e, "gemm_tc_kernel launch");
     if (plan.splits > 1) {
         const int64_t n_out = ep == BI_EP_SWIGLU ? M * (N / 2) : M * N;
