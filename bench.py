@@ -57,6 +57,15 @@ def parse():
     return p.parse_args()
 
 
+def run_config(batch: int, world: int) -> dict:
+    """The workload both arms report (the same keys and values)."""
+    from invariant_fixed_order_gb300 import roofline
+    cfg, ctx, _ = make_workload(batch, 0)
+    step_gb = roofline.decode_step_bytes(cfg, [int(s) for s in ctx]) / 1e9
+    return {"workload": WORKLOAD, "batch_per_gpu": batch, "context": [CTX_LO, CTX_HI], "mode": "invariant",
+            "parallelism": f"replicas{world}", "l2": "inputs larger than L2 (step reads %.2f GB)" % step_gb}
+
+
 def dist_env():
     return int(os.environ.get("RANK", 0)), int(os.environ.get("WORLD_SIZE", 1)), int(os.environ.get("LOCAL_RANK", 0))
 
@@ -382,7 +391,7 @@ def run_reference(args):
     line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
             "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * args.batch / value,
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "batch": args.batch, "context": [CTX_LO, CTX_HI]},
+            "config": run_config(args.batch, args.gpus),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": rates[0]["cores"], "kind": "oracle",
                              "sample": rates[0]["sample"] + " per step"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
@@ -499,9 +508,7 @@ def run_ours(args):
             "metric": METRIC, "value": round(value, 1), "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
             "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True, "scaling": "weak",
             "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-            "config": {"workload": WORKLOAD, "batch_per_gpu": B, "context": [CTX_LO, CTX_HI],
-                       "mode": "invariant", "parallelism": f"replicas{world}",
-                       "l2": "inputs larger than L2 (step reads %.2f GB)" % (step_bytes / 1e9)},
+            "config": run_config(B, world),
             "step_hbm_frac": round(step_bytes / (ms * 1e-3) / 1e9 / hbm_peak, 3),
             "roofline": {"bound": "hbm", "kernel": "gemm_tc_kernel", "achieved": round(g["achieved"], 1),
                          "peak": hbm_peak, "unit": "GB/s", "frac": round(g["achieved"] / hbm_peak, 3),
