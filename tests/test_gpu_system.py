@@ -45,6 +45,23 @@ def greedy_solo(sched, runner, prompt, rid, n_new, mode):
     return list(req.generated)
 
 
+def greedy_batched(sched, runner, prompts, n_new, mode):
+    """Greedy decoding of all prompts together (prompts prefilled one by one)."""
+    reqs = [sched.Request(rid, p) for rid, p in enumerate(prompts)]
+    for r in reqs:
+        logits, tokens, sl = runner.step([sched.StepItem(r, len(r.prompt), "last")], mode=mode)
+        r.generated.append(int(tokens[sl[0]][-1].item()))
+    while len(reqs[0].generated) < n_new:
+        logits, tokens, sl = runner.step([sched.StepItem(r, 1, "last") for r in reqs], mode=mode)
+        tok = tokens.tolist()
+        for r, s_ in zip(reqs, sl):
+            r.generated.append(tok[s_.start])
+    out = {r.rid: list(r.generated) for r in reqs}
+    for r in reqs:
+        runner.evict(r)
+    return out
+
+
 def test_unique_completions_under_random_schedules(mods):
     bi, sched, dvr, Engine = mods
     n_layers, n_prompts, lo, hi, n_new, n_sched = (32, 64, 128, 4096, 256, 50) if FULL else (16, 24, 128, 1024, 40, 6)
@@ -57,14 +74,19 @@ def test_unique_completions_under_random_schedules(mods):
     runner = sched.Runner(eng)
     solo = {rid: greedy_solo(sched, runner, p, rid, n_new, bi.INVARIANT) for rid, p in enumerate(prompts)}
     completions = {rid: {tuple(solo[rid])} for rid in solo}
-    fz = sched.FuzzConfig(token_budget=4096, chunk_min=256, chunk_max=2048, p_evict=0.05, readmit_delay=(1, 3),
-                          arrival_span=6)
+    # at full size an eviction recomputes up to 4k positions through 32 layers: evict less often
+    fz = sched.FuzzConfig(token_budget=4096, chunk_min=256, chunk_max=2048, p_evict=0.002 if FULL else 0.05,
+                          readmit_delay=(1, 3), arrival_span=6)
+    print(f"unique completions: {n_layers} layers, {n_prompts} prompts, {n_new} tokens, {n_sched} schedules",
+          flush=True)
     for k in range(n_sched):
         reqs = [sched.Request(rid, p) for rid, p in enumerate(prompts)]
         sched.fuzz_continuous(runner, reqs, n_new, np.random.default_rng(1000 + k), fz, all_prompt_logits=False)
         eng.check()
         for r in reqs:
             completions[r.rid].add(tuple(r.generated[:n_new]))
+        print(f"  schedule {k}: max completions per prompt so far {max(len(c) for c in completions.values())}",
+              flush=True)
     unique = {rid: len(c) for rid, c in completions.items()}
     bound = sched.rule_of_three(n_prompts * n_sched)
     print(f"unique completions per prompt: max {max(unique.values())}; rule-of-three bound {bound:.4f}")
@@ -121,7 +143,8 @@ def test_decode_verify_rollback_commits_the_invariant_greedy_tokens(mods):
     eng = Engine(cfg, num_pages=n_prompts * max_pages + 64, max_pages=max_pages,
                  max_T=max(8 * window, 8 * 1024) + 64, max_B=n_prompts, max_R=8 * window)
     runner = sched.Runner(eng)
-    truth = {rid: greedy_solo(sched, runner, p, rid, n_new, bi.INVARIANT) for rid, p in enumerate(prompts)}
+    # pure invariant greedy decoding (batched: invariant mode gives every request its solo bits)
+    truth = greedy_batched(sched, runner, prompts, n_new, bi.INVARIANT)
 
     # plain run of the fast path
     reqs = [sched.Request(rid, p) for rid, p in enumerate(prompts)]
@@ -131,7 +154,8 @@ def test_decode_verify_rollback_commits_the_invariant_greedy_tokens(mods):
         assert r.generated == truth[r.rid], r.rid
         runner.evict(r)
     assert st.committed == n_prompts * n_new
-    print("dvr:", st.as_dict())
+    print(f"dvr ({n_layers} layers, {n_prompts} prompts, {n_new} tokens, window {window}):", st.as_dict(),
+          flush=True)
 
     # a fast path that emits wrong candidates at chosen positions: the verifier
     # must catch each one, roll back and still commit exactly the greedy tokens
