@@ -316,6 +316,7 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
 
     for (int t = 0; t < 2 * ns; ++t) {
         const int st = t % kRing;
+        bool padded = false;  // (uniform) rows of this stage were just zeroed by several threads
         if (use_tma) {
             if (issued & (1u << st)) {
                 issued &= ~(1u << st);
@@ -329,6 +330,7 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
                 const int32_t j0 = (t - ns) * kSub;
                 const int32_t nk = min(kSub, n_max - j0);
                 if (t >= ns && (nk & 15)) {
+                    padded = true;
                     const int32_t pad_end = (nk + 15) & ~15;
                     for (int i = tid; i < (pad_end - nk) * kVecPerRow; i += kAttnThreads)
                         *reinterpret_cast<uint4*>(sm.ring[st] + ring_off<DH>(nk + i / kVecPerRow, i % kVecPerRow)) =
@@ -339,7 +341,9 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
         } else {
             asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 1) : "memory");
         }
-        __syncthreads();
+        // a thread's own mbarrier wait makes a TMA stage visible to it; cp.async
+        // stages and zero-padded rows need the CTA barrier
+        if (!use_tma || padded) __syncthreads();
         const uint32_t buf = smem_u32(sm.ring[st]);
         if (t < ns) {
             // scores: warp w takes keys 16w .. 16w+15 of the sub-chunk as the MMA rows
