@@ -9,8 +9,10 @@
  * in one fixed order with split points that depend on the request alone:
  *   - RMSNorm: one warp per row, lane-serial over 16-byte chunks, then a fixed
  *     xor-butterfly;
- *   - GEMM: one tcgen05 MMA instruction shape (128x128x16, bf16 in, fp32
- *     accumulate in TMEM), one K tile (64), K loop in ascending order, no
+ *   - GEMM: per weight matrix one tcgen05 MMA instruction form, chosen by
+ *     the matrix's width N alone (N <= 65536: the two-SM pair form
+ *     256x128x16; wider: the single-SM form 128x128x16), bf16 in, fp32
+ *     accumulate in TMEM, one K tile (64), K loop in ascending order, no
  *     split-K, whatever M is;
  *   - attention: keys cut into chunks of BI_KV_CHUNK positions aligned to key 0
  *     ("Batch invariance and reproducible inference", "1 · Split-K and
@@ -79,7 +81,7 @@ typedef enum {
 /* Fixed constants of the method (never functions of a batch). */
 #define BI_KV_CHUNK 256      /* attention key chunk (positions) */
 #define BI_PAGE 16           /* KV page (positions) */
-#define BI_GEMM_BLOCK_M 128  /* MMA M */
+#define BI_GEMM_BLOCK_M 128  /* accumulator rows per CTA (a pair MMA spans two CTAs: M = 256) */
 #define BI_GEMM_UMMA_N 128  /* MMA N */
 #define BI_GEMM_BLOCK_K 64   /* K tile */
 #define BI_SWIGLU_GROUP 32   /* gate/up interleave group (rows) */
@@ -91,6 +93,7 @@ typedef enum {
 #define BI_DEV_TIMEOUT_EPILOGUE 0x103
 #define BI_DEV_TIMEOUT_DRAIN 0x104
 #define BI_DEV_TIMEOUT_ATTENTION 0x105  /* a K/V copy into an attention CTA did not land in time */
+#define BI_DEV_PAIR_TMEM 0x106  /* the two CTAs of a GEMM pair were given different tensor-memory columns */
 #define BI_DEV_BAD_PAGE 0x201
 #define BI_DEV_BAD_POSITION 0x202
 #define BI_DEV_BAD_TOKEN 0x203

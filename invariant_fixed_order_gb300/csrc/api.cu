@@ -64,6 +64,7 @@ extern "C" bi_status bi_check_status(const int32_t* dev_status, bi_stream stream
     char buf[96];
     snprintf(buf, sizeof buf, "device status 0x%x", v);
     if (v >= BI_DEV_TIMEOUT_PRODUCER && v <= BI_DEV_TIMEOUT_ATTENTION) return fail(BI_ERR_TIMEOUT, buf);
+    if (v == BI_DEV_PAIR_TMEM) return fail(BI_ERR_CUDA, buf);
     return fail(BI_ERR_DEVICE, buf);
 }
 

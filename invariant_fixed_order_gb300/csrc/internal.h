@@ -37,6 +37,29 @@ inline cudaError_t launch_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_
     return launch_k(true, kernel, grid, block, smem, s, static_cast<A&&>(args)...);
 }
 
+// As launch_pdl, in clusters of two CTAs along x (grid.x even): the CTA pairs
+// of the tensor-core GEMM.
+template <typename... P, typename... A>
+inline cudaError_t launch_pair_pdl(void (*kernel)(P...), dim3 grid, dim3 block, size_t smem, cudaStream_t s,
+                                   A&&... args) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = s;
+    cudaLaunchAttribute attr[2];
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    attr[1].id = cudaLaunchAttributeClusterDimension;
+    attr[1].val.clusterDim.x = 2;
+    attr[1].val.clusterDim.y = 1;
+    attr[1].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 2;
+    const cudaError_t e = cudaLaunchKernelEx(&cfg, kernel, static_cast<A&&>(args)...);
+    return e != cudaSuccess ? e : cudaGetLastError();
+}
+
 // thread-local error message (api.cu)
 void set_error(const std::string& msg);
 bi_status fail(bi_status s, const std::string& msg);

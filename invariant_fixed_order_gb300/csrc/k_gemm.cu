@@ -3,38 +3,53 @@
 // "Batch invariance and reproducible inference", "2 · Cross-block
 // accumulation" and "3 · Kernel selection changing with shape": split-K and
 // M-dependent kernel choice are what make a GEMM's per-element order follow
-// the batch.  Here every output element, for every M, is produced by the same
-// sequence: one tcgen05.mma shape (M=128, N=128, K=16; bf16 in, fp32
-// accumulated in TMEM), K tiles of 64 in ascending order, inside a K tile the
-// four 16-deep MMAs in ascending order, all into one accumulator.
+// the batch.  Here every output element of a weight matrix, for every M, is
+// produced by the same sequence: one tcgen05.mma instruction form (bf16 in,
+// fp32 accumulated in TMEM, N = 128, K = 16), K tiles of 64 in ascending
+// order, inside a K tile the four 16-deep MMAs in ascending order, all into
+// one accumulator.  The form is fixed by the matrix's width N alone:
+//   * N <= 65536 (the projections of a layer): the CTA-pair form, M = 256
+//     over a cluster of two CTAs on two SMs.  The pair's MMA takes 128 rows of
+//     A from each CTA's shared memory and 64 of its 128 weight rows from
+//     each, so a layer projection with only 32-48 output tiles of 128 columns
+//     keeps twice the SMs busy, and a prefill GEMM's tensor cores read less
+//     shared memory per multiply-add (measured: ~55 ns per pair MMA against
+//     ~65 ns for a single-CTA 128x128x16 MMA);
+//   * N > 65536 (a vocabulary projection): the single-CTA form, M = 128.
+//     Its hundreds of tiles fill every SM many times over, and one SM then
+//     consumes 4 KB of weights per MMA instead of the pair's 2 KB, which is
+//     what lets the weight stream run at the copy bandwidth.
 //
 // What may follow M is only how that work is laid out, never the arithmetic
 // of an element:
-//   * the CTA tile is 128 x 128 (one MMA per 16-deep step) for M <= 256, and
-//     128 x 256 (two identical MMAs per step, sharing A) for larger M, where
-//     the tensor pipe must be fed from L2;
-//   * the TMA box of A covers the smallest power of two >= M rows (16..128);
-//     A stages are packed at that stride, so the MMA's rows past the box read
-//     neighbouring stages: those rows of the accumulator are never stored,
-//     and a row's result depends only on its own A row (pinned by the row-
-//     invariance tests);
+//   * tile width: 128 columns (one MMA per 16-deep step) for M <= 256, and
+//     256 columns (two MMAs per step sharing A) for larger M;
+//   * the TMA box of A covers the smallest power of two >= min(M, 128) rows
+//     (16..128); A stages are packed at that stride, so the MMA's rows past
+//     the box read neighbouring stages: those rows of the accumulator are
+//     never stored, and a row's result depends only on its own A row (pinned
+//     by the row-invariance tests);
 //   * ring depth and K tiles per ring stage.
 //
-// The kernel is persistent (at most one CTA per SM) with warp roles: warp 0
-// streams K tiles of A and W by TMA into one ring and owns the TMEM
-// allocation, warp 1 issues the MMAs (one thread), warps 4-7 read the
-// accumulator back (warp w: TMEM lanes 32*(w%4)..+31) and run the fused
-// epilogue.  The accumulator is double buffered in TMEM so a tile's epilogue
-// overlaps the next tile's main loop.  Weights do not depend on the kernel
-// before this one in the stream, so while that kernel finishes the producer
-// already pulls the first tile's weight slab into L2; activations are read
-// only after the dependency wait.  Every wait is bounded: a wait that runs
-// out sets an abort flag and a device status code, every role winds down,
-// copies and MMAs in flight are drained and TMEM is freed.
+// The kernel is persistent (one CTA per SM) with warp roles: warp 0 of each
+// CTA streams its K tiles of A and W by TMA into its own ring, counting the
+// bytes of the whole group on the issuing CTA's barrier, and owns the TMEM
+// allocation; warp 1 of the issuing CTA (the even CTA of a pair) issues the
+// MMAs (one thread) and commits each consumed ring stage to every producer;
+// warps 4-7 of each CTA read that CTA's 128 accumulator rows back (warp w:
+// TMEM lanes 32*(w%4)..+31), run the fused epilogue and release the
+// accumulator to the MMA issuer.  The accumulator is double buffered in TMEM
+// so a tile's epilogue overlaps the next tile's main loop.  Weights do not
+// depend on the kernel before this one in the stream, so while that kernel
+// finishes the producers already pull the first tile's weight slab;
+// activations are read only after the dependency wait.  Every wait is
+// bounded: a wait that runs out sets an abort flag in every CTA of the group
+// and a device status code, every role winds down, copies and MMAs in flight
+// are drained and TMEM is freed.
 //
 // BI_VARIANT splits K over CTAs into an fp32 workspace when the output has
-// fewer tiles than SMs and adds the partials in split order in a second
-// kernel: deterministic run to run, but its order depends on M.
+// fewer 128x128 tiles than SMs and adds the partials in split order in a
+// second kernel: deterministic run to run, but its order depends on M.
 #include <cudaTypedefs.h>
 
 #include <algorithm>
@@ -45,18 +60,17 @@
 
 namespace bi {
 
-constexpr int kBM = BI_GEMM_BLOCK_M;   // 128
-constexpr int kUN = BI_GEMM_UMMA_N;    // N of one MMA
+constexpr int kBM = BI_GEMM_BLOCK_M;   // 128: accumulator rows of one CTA
+constexpr int kUN = BI_GEMM_UMMA_N;    // 128: N of one MMA
 constexpr int kEpi = 64;               // epilogue column chunk (a SwiGLU gate|up group pair)
 constexpr int kBK = BI_GEMM_BLOCK_K;   // 64
 constexpr int kMaxStages = 16;
 constexpr int kGemmThreads = 256;
-constexpr int kAFull = kBM * kBK * 2;  // bytes the MMA reads for A per K tile (16 KB)
+constexpr int kAFull = kBM * kBK * 2;  // bytes the MMA reads for A per K tile in one CTA (16 KB)
 constexpr int kGroupM = 16;            // M tiles per rasterisation band
 constexpr int kBarrierBytes = 1024;
 constexpr int kRingBudget = 212 * 1024;  // shared memory for the A and W rings
 constexpr int kMaxSmem = 226 * 1024;  // dynamic shared memory; the kernel's few static bytes fit beside it
-constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kBM, kUN);
 
 struct GemmArgs {
     void* C;
@@ -147,14 +161,20 @@ __device__ __forceinline__ void epilogue_group(const GemmArgs& args, int64_t row
     }
 }
 
-template <int BN>
+template <int BN, int CG>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, GemmArgs args) {
-    constexpr int kWBytes = BN * kBK * 2;
-    constexpr int kGroups = BN / kUN;   // MMAs per 16-deep step
-    constexpr int kChunks = BN / kEpi;  // epilogue chunks per tile
-    constexpr uint32_t kTmemCols = 2 * BN;  // two accumulator buffers
+    static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair");
+    constexpr int kTileM = CG * kBM;           // rows of a tile (the MMA's M)
+    constexpr int kGroups = BN / kUN;          // MMAs per 16-deep step
+    constexpr int kWRows = BN / CG;            // W rows (output columns) this CTA holds per K tile
+    constexpr int kWBytes = kWRows * kBK * 2;  // bytes of one K tile of W in this CTA
+    constexpr int kChunks = BN / kEpi;         // epilogue chunks per tile
+    constexpr uint32_t kTmemCols = 2 * BN;     // two accumulator buffers
+    constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM, kUN);
     extern __shared__ __align__(1024) uint8_t smem_raw[];
+    // both CTAs of a pair use identical offsets: the MMA descriptors and the
+    // cluster addresses below name the same offset in either CTA
     uint8_t* smem = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     uint8_t* sA = smem;
     uint8_t* sW = smem + args.a_region;
@@ -164,8 +184,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint64_t* acc_empty = acc_full + 2;          // [2]
     uint64_t* drain = acc_empty + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
-    volatile int32_t* abort_flag = reinterpret_cast<volatile int32_t*>(tmem_holder + 1);
+    int32_t* abort_word = reinterpret_cast<int32_t*>(tmem_holder + 1);
+    volatile int32_t* abort_flag = abort_word;
 
+    uint32_t rank = 0;  // 0: the CTA that issues the MMAs (the even CTA of a pair)
+    if constexpr (CG == 2) rank = ptx::cluster_ctarank();
+    const uint32_t peer = rank ^ 1u;
+    const int32_t unit = static_cast<int32_t>(blockIdx.x) / CG;  // this CTA's pair (or the CTA itself)
+    const int32_t nunits = static_cast<int32_t>(gridDim.x) / CG;
     const int warp = threadIdx.x / 32, lane = threadIdx.x & 31;
     const int32_t split = blockIdx.y;
     const int32_t kb0 = split * args.kb_per_split;
@@ -179,6 +205,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         m_tile = first_m + (lin % band) % band_m;
         n_tile = (lin % band) / band_m;
     };
+    // a role that gives up stops every CTA of the group
+    auto raise_abort = [&]() {
+        *abort_flag = 1;
+        if constexpr (CG == 2) ptx::st_shared_cluster_u32(ptx::mapa_shared(smem_u32(abort_word), peer), 1u);
+    };
 
     pdl_trigger();
     if (warp == 0 && lane == 0) {
@@ -190,7 +221,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&acc_full[b], 1);
-            ptx::mbar_init(&acc_empty[b], 4);  // one arrival per epilogue warp
+            ptx::mbar_init(&acc_empty[b], 4 * CG);  // one arrival per epilogue warp of the group
         }
         ptx::mbar_init(drain, 1);
         *abort_flag = 0;
@@ -204,36 +235,57 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     }
     if (warp == 0) {
         __syncwarp();
-        ptx::tmem_alloc(tmem_holder, kTmemCols);
-        ptx::tmem_relinquish();
+        ptx::tmem_alloc<CG>(tmem_holder, kTmemCols);
+        ptx::tmem_relinquish<CG>();
     }
     ptx::tc_fence_before();
-    __syncthreads();
+    if constexpr (CG == 2)
+        ptx::cluster_sync();  // barriers initialised and TMEM allocated in both CTAs
+    else
+        __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = *tmem_holder;
+    bool tmem_ok = true;
+    // a pair's MMAs write the even CTA's column address in both CTAs
+    if constexpr (CG == 2) tmem_ok = ptx::ld_shared_cluster_u32(ptx::mapa_shared(smem_u32(tmem_holder), peer)) == tmem;
     if (!(warp == 0 && lane == 0)) pdl_wait();  // the producer waits in its role below
 
-    if (warp == 0) {
+    if (!tmem_ok) {
+        if (warp == 0 && lane == 0) {
+            pdl_wait();
+            if (rank == 0) report(args.status, BI_DEV_PAIR_TMEM);
+        }
+    } else if (warp == 0) {
         if (lane == 0) {
-            // ---- TMA producer: per stage one box of A and one of W, each kps K tiles deep ----
+            // ---- TMA producer (every CTA): per stage one box of A and one of W, each kps K tiles deep ----
             const uint64_t pol_w = ptx::policy_evict_first();  // weights stream through once
             const uint64_t pol_a = ptx::policy_evict_last();   // activations are re-read by every N tile
-            // a box always lands whole (out-of-range rows and K tiles are zero-filled)
-            const uint32_t stage_tx = static_cast<uint32_t>(kps) * (static_cast<uint32_t>(args.a_stride) + kWBytes);
+            // boxes always land whole (out-of-range rows and K tiles are zero-filled); the
+            // issuing CTA's full barrier counts the bytes of every CTA of the group
+            const uint32_t stage_tx =
+                static_cast<uint32_t>(CG * kps) * (static_cast<uint32_t>(args.a_stride) + kWBytes);
+            const int32_t a_row0 = static_cast<int32_t>(rank) * kBM;     // this CTA's rows of the tile
+            const int32_t w_row0 = static_cast<int32_t>(rank) * kWRows;  // this CTA's W rows of the tile
+            auto load = [&](void* dst, const CUtensorMap* map, int s_, int32_t y, int32_t z, uint64_t pol) {
+                if constexpr (CG == 2)
+                    ptx::tma_load_3d_pair(dst, map, ptx::mapa_shared(smem_u32(&full[s_]), 0), 0, y, z, pol);
+                else
+                    ptx::tma_load_3d(dst, map, &full[s_], 0, y, z, pol);
+            };
             // Weights do not depend on the kernel before this one: when the
             // caller guarantees that nothing still in flight writes them, the
             // first tile's first stages of W are requested before the
             // dependency wait and only A waits for the previous kernel.
             uint32_t pre = 0;
-            if (args.w_early && static_cast<int32_t>(blockIdx.x) < args.total_tiles) {
+            if (args.w_early && unit < args.total_tiles) {
                 int32_t m_tile, n_tile;
-                tile_coords(blockIdx.x, m_tile, n_tile);
+                tile_coords(unit, m_tile, n_tile);
                 const int32_t first_stages = (nkb + kps - 1) / kps;
                 pre = static_cast<uint32_t>(min(S, first_stages));
                 for (uint32_t q = 0; q < pre; ++q) {
-                    ptx::mbar_arrive_expect_tx(&full[q], stage_tx);
-                    ptx::tma_load_3d(sW + q * kps * kWBytes, &tmW, &full[q], 0, n_tile * BN,
-                                     kb0 + static_cast<int32_t>(q) * kps, pol_w);
+                    if (rank == 0) ptx::mbar_arrive_expect_tx(&full[q], stage_tx);
+                    load(sW + q * kps * kWBytes, &tmW, static_cast<int>(q), n_tile * BN + w_row0,
+                         kb0 + static_cast<int32_t>(q) * kps, pol_w);
                 }
             }
             pdl_wait();
@@ -241,25 +293,24 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             int s = 0;            // stage and its phase, advanced incrementally
             uint32_t ph = 0;
             bool ok = true;
-            for (int32_t tile = blockIdx.x; tile < args.total_tiles && ok; tile += gridDim.x) {
+            for (int32_t tile = unit; tile < args.total_tiles && ok; tile += nunits) {
                 int32_t m_tile, n_tile;
                 tile_coords(tile, m_tile, n_tile);
+                const int32_t a_row = m_tile * kTileM + a_row0;
                 for (int32_t kb = 0; kb < nkb; kb += kps) {
                     if (issued < pre) {
                         // armed, W already requested: only A is missing
-                        ptx::tma_load_3d(sA + s * kps * args.a_stride, &tmA, &full[s], 0, m_tile * kBM, kb0 + kb,
-                                         pol_a);
+                        load(sA + s * kps * args.a_stride, &tmA, s, a_row, kb0 + kb, pol_a);
                     } else {
                         if (!ptx::mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag)) {
                             if (!*abort_flag) report(args.status, BI_DEV_TIMEOUT_PRODUCER);
-                            *abort_flag = 1;
+                            raise_abort();
                             ok = false;
                             break;
                         }
-                        ptx::mbar_arrive_expect_tx(&full[s], stage_tx);
-                        ptx::tma_load_3d(sA + s * kps * args.a_stride, &tmA, &full[s], 0, m_tile * kBM, kb0 + kb,
-                                         pol_a);
-                        ptx::tma_load_3d(sW + s * kps * kWBytes, &tmW, &full[s], 0, n_tile * BN, kb0 + kb, pol_w);
+                        if (rank == 0) ptx::mbar_arrive_expect_tx(&full[s], stage_tx);
+                        load(sA + s * kps * args.a_stride, &tmA, s, a_row, kb0 + kb, pol_a);
+                        load(sW + s * kps * kWBytes, &tmW, s, n_tile * BN + w_row0, kb0 + kb, pol_w);
                     }
                     ++issued;
                     if (++s == S) {
@@ -268,23 +319,26 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                 }
             }
-            // drain: every issued copy must land before the CTA may exit
-            const uint32_t first = issued > static_cast<uint32_t>(S) ? issued - S : 0u;
-            for (uint32_t q = first; q < issued; ++q) {
-                const int qs = static_cast<int>(q % S);
-                const uint32_t qph = (q / S) & 1u;
-                const uint64_t t0 = globaltimer_ns();
-                while (!ptx::mbar_try_wait(smem_u32(&full[qs]), qph)) {
-                    if (globaltimer_ns() - t0 > kWaitLimitNs) {
-                        report(args.status, BI_DEV_TIMEOUT_DRAIN);
-                        break;
+            // drain: every issued copy of the group lands on the issuing CTA's
+            // barriers, and must land before any CTA of the group may exit
+            if (rank == 0) {
+                const uint32_t first = issued > static_cast<uint32_t>(S) ? issued - S : 0u;
+                for (uint32_t q = first; q < issued; ++q) {
+                    const int qs = static_cast<int>(q % S);
+                    const uint32_t qph = (q / S) & 1u;
+                    const uint64_t t0 = globaltimer_ns();
+                    while (!ptx::mbar_try_wait(smem_u32(&full[qs]), qph)) {
+                        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                            report(args.status, BI_DEV_TIMEOUT_DRAIN);
+                            break;
+                        }
                     }
                 }
             }
         }
     } else if (warp == 1) {
-        if (lane == 0) {
-            // ---- MMA issuer ----
+        if (lane == 0 && rank == 0) {
+            // ---- MMA issuer (one thread of the issuing CTA) ----
             // Descriptors are built once; a slot or a 16-deep K step only moves
             // the start-address field (16-byte units; shared memory < 256 KB so
             // the 14-bit field never carries).
@@ -292,16 +346,16 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint64_t w_desc0 = ptx::smem_desc_sw128(smem_u32(sW));
             const uint32_t a_step = static_cast<uint32_t>(args.a_stride) >> 4;
             constexpr uint32_t w_step = kWBytes >> 4;
-            constexpr uint32_t g_step = (kUN * kBK * 2) >> 4;
+            constexpr uint32_t g_step = ((kUN / CG) * kBK * 2) >> 4;  // the next MMA's W rows in each CTA
             int s = 0;
             uint32_t ph = 0;
             int32_t i = 0;
             bool ok = true;
-            for (int32_t tile = blockIdx.x; tile < args.total_tiles && ok; tile += gridDim.x, ++i) {
+            for (int32_t tile = unit; tile < args.total_tiles && ok; tile += nunits, ++i) {
                 const int b = i & 1;
                 if (!ptx::mbar_wait_bounded(&acc_empty[b], ((static_cast<uint32_t>(i) >> 1) & 1u) ^ 1u, abort_flag)) {
                     if (!*abort_flag) report(args.status, BI_DEV_TIMEOUT_MMA);
-                    *abort_flag = 1;
+                    raise_abort();
                     break;
                 }
                 ptx::tc_fence_after();
@@ -310,7 +364,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     const int cnt = min(kps, nkb - kb);
                     if (!ptx::mbar_wait_bounded(&full[s], ph, abort_flag)) {
                         if (!*abort_flag) report(args.status, BI_DEV_TIMEOUT_MMA);
-                        *abort_flag = 1;
+                        raise_abort();
                         ok = false;
                         break;
                     }
@@ -323,20 +377,22 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         for (int k = 0; k < kBK / 16; ++k) {
 #pragma unroll
                             for (int g = 0; g < kGroups; ++g)
-                                ptx::tc_mma_f16(acc + g * kUN, ad + 2u * k, wd + g * g_step + 2u * k, kIdesc,
-                                                (kb + j > 0 || k > 0) ? 1u : 0u);
+                                ptx::tc_mma_f16<CG>(acc + g * kUN, ad + 2u * k, wd + g * g_step + 2u * k, kIdesc,
+                                                    (kb + j > 0 || k > 0) ? 1u : 0u);
                         }
                     }
-                    ptx::tc_commit(&empty[s]);  // the stage is free once these MMAs have read it
+                    ptx::tc_commit<CG>(&empty[s]);  // the stage is free (in every CTA) once read
                     if (++s == S) {
                         s = 0;
                         ph ^= 1u;
                     }
                 }
-                if (ok) ptx::tc_commit(&acc_full[b]);
+                if (ok) ptx::tc_commit<CG>(&acc_full[b]);
             }
-            // no MMA may be in flight when TMEM is freed
-            ptx::tc_commit(drain);
+            // no MMA may be in flight when any CTA frees TMEM or exits
+            ptx::tc_commit<CG>(drain);
+        }
+        if (lane == 0) {
             const uint64_t t0 = globaltimer_ns();
             while (!ptx::mbar_try_wait(smem_u32(drain), 0)) {
                 if (globaltimer_ns() - t0 > kWaitLimitNs) {
@@ -346,10 +402,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             }
         }
     } else if (warp >= 4) {
-        // ---- epilogue: warps 4..7 ----
+        // ---- epilogue: warps 4..7 of each CTA, on that CTA's 128 rows ----
         const int q = warp & 3;
         int32_t i = 0;
-        for (int32_t tile = blockIdx.x; tile < args.total_tiles; tile += gridDim.x, ++i) {
+        for (int32_t tile = unit; tile < args.total_tiles; tile += nunits, ++i) {
             const int b = i & 1;
             const bool ready = ptx::mbar_wait_bounded(&acc_full[b], (static_cast<uint32_t>(i) >> 1) & 1u, abort_flag);
             if (!ready && !*abort_flag) report(args.status, BI_DEV_TIMEOUT_EPILOGUE);
@@ -357,7 +413,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             ptx::tc_fence_after();
             int32_t m_tile, n_tile;
             tile_coords(tile, m_tile, n_tile);
-            const int64_t row = static_cast<int64_t>(m_tile) * kBM + q * 32 + lane;
+            const int64_t row = static_cast<int64_t>(m_tile) * kTileM + rank * kBM + q * 32 + lane;
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * BN);
             unsigned long long best = kArgmaxKeyNone;
 #pragma unroll 1
@@ -366,7 +422,10 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
                 for (int c = 0; c < 4; ++c) ptx::tmem_ld16(taddr + j * kEpi + c * 16, r[c]);
                 ptx::tmem_ld_wait();
-                const int32_t n0 = n_tile * BN + j * kEpi;
+                // accumulator columns 64j..64j+63 are MMA j/2's columns 64(j%2)..; in a
+                // pair, an MMA's columns 0-63 are W rows held by the even CTA, 64-127 by the odd
+                const int32_t n0 = CG == 2 ? n_tile * BN + (j & 1) * (BN / 2) + (j >> 1) * kEpi
+                                           : n_tile * BN + j * kEpi;
                 if (row < args.M && args.C != nullptr) epilogue_group(args, row, n0, split, r);
                 if (args.am_keys != nullptr) {
 #pragma unroll
@@ -381,18 +440,28 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             if (args.am_keys != nullptr && row < args.M) atomicMin(args.am_keys + row, best);
             ptx::tc_fence_before();
             __syncwarp();
-            if (lane == 0) mbar_arrive(&acc_empty[b]);
+            if (lane == 0) {
+                if (rank == 0)
+                    mbar_arrive(&acc_empty[b]);
+                else
+                    ptx::mbar_arrive_cluster(ptx::mapa_shared(smem_u32(&acc_empty[b]), 0));
+            }
         }
     }
 
-    // teardown: MMAs drained by the issuer, copies drained by the producers
+    // teardown: MMAs drained (every CTA saw the drain commit), copies drained
+    // by the issuing CTA's producer; after the (cluster) barrier no CTA
+    // touches another's shared or tensor memory
     if (args.am_keys != nullptr) __threadfence();  // this CTA's argmax keys before its count below
     ptx::tc_fence_before();
-    __syncthreads();
+    if constexpr (CG == 2)
+        ptx::cluster_sync();
+    else
+        __syncthreads();
     if (warp == 0) {
         __syncwarp();
         ptx::tc_fence_after();
-        ptx::tmem_dealloc(tmem, kTmemCols);
+        ptx::tmem_dealloc<CG>(tmem, kTmemCols);
     }
     if (args.am_keys != nullptr) {
         // the last CTA to finish turns every row's key into its token id
@@ -515,21 +584,34 @@ size_t gemm_ws_bytes(int64_t M, int32_t N, int32_t K, bi_mode mode) {
 namespace {
 
 struct Layout {
-    int32_t bn, a_box, a_stride, a_region, stages, kps;
+    int32_t cg, bn, a_box, a_stride, a_region, stages, kps;
     size_t smem;
 };
+
+// The MMA instruction form of a weight matrix, from its width alone (never
+// from M): weight matrices up to kPairMaxN columns have few enough 128-wide
+// output tiles that a tile must be spread over two SMs to use the GPU, and
+// take the pair form (256x128x16 over two SMs, 2 KB of weights per SM per
+// MMA); wider ones (a vocabulary projection) fill every SM many times over
+// and are bound by how fast the tensor cores consume weights, which the
+// single-CTA form (128x128x16, 4 KB of weights per MMA) does faster.
+constexpr int32_t kPairMaxN = 65536;
+int mma_group(int32_t N) { return N <= kPairMaxN ? 2 : 1; }
 
 // Layout of one launch.  Only data movement depends on M here; the MMA
 // sequence of every output element is the same for all layouts.
 Layout choose_layout(int64_t M, int32_t N, int32_t K) {
     Layout L{};
+    L.cg = mma_group(N);
+    // 256-wide tiles (two MMAs per step sharing the A slice, half the A
+    // re-reads from L2) for M > 256; for fewer rows 128-wide tiles spread the
+    // output over twice the tiles
     L.bn = (M > 2 * kBM && N % 256 == 0) ? 256 : kUN;
     int32_t box = 16;
     while (box < kBM && box < M) box *= 2;
-    if (L.bn == 256) box = kBM;
     L.a_box = box;
     L.a_stride = box * kBK * 2;
-    const int32_t w_tile = L.bn * kBK * 2;
+    const int32_t w_tile = (L.bn / L.cg) * kBK * 2;  // one K tile of this CTA's W rows
     const int32_t pad = kAFull - L.a_stride;  // the last slot's 128-row window reaches this far past it
     const int32_t budget = kRingBudget - pad;
     const int32_t per_k = L.a_stride + w_tile;  // bytes of one K tile of A and W
@@ -543,17 +625,58 @@ Layout choose_layout(int64_t M, int32_t N, int32_t K) {
     return L;
 }
 
-template <int BN>
-cudaError_t launch_tiles(const CUtensorMap& tmA, const CUtensorMap& tmW, const GemmArgs& a, dim3 grid, size_t smem,
-                         cudaStream_t s) {
-    static_assert(BN % kUN == 0, "a CTA tile is a whole number of MMAs wide");
+template <int BN, int CG>
+cudaError_t prepare_tiles() {
+    static_assert(BN % kUN == 0, "a tile is a whole number of MMAs wide");
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
-        err = cudaFuncSetAttribute(gemm_tc_kernel<BN>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+        err = cudaFuncSetAttribute(gemm_tc_kernel<BN, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
     });
-    if (err != cudaSuccess) return err;
-    return launch_pdl(gemm_tc_kernel<BN>, grid, dim3(kGemmThreads), smem, s, tmA, tmW, a);
+    return err;
+}
+
+// Pairs of CTAs that fit on the GPU at once (one CTA per SM).
+int resident_pairs() {
+    static int pairs = 0;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        int n = 0;
+        cudaLaunchConfig_t cfg{};
+        cfg.gridDim = dim3(2);
+        cfg.blockDim = dim3(kGemmThreads);
+        cfg.dynamicSmemBytes = kMaxSmem;
+        cudaLaunchAttribute attr[1];
+        attr[0].id = cudaLaunchAttributeClusterDimension;
+        attr[0].val.clusterDim.x = 2;
+        attr[0].val.clusterDim.y = 1;
+        attr[0].val.clusterDim.z = 1;
+        cfg.attrs = attr;
+        cfg.numAttrs = 1;
+        if (prepare_tiles<kUN, 2>() != cudaSuccess ||
+            cudaOccupancyMaxActiveClusters(&n, gemm_tc_kernel<kUN, 2>, &cfg) != cudaSuccess || n <= 0) {
+            (void)cudaGetLastError();
+            n = num_sms() / 2;
+        }
+        pairs = std::max(1, std::min(n, num_sms() / 2));
+    });
+    return pairs;
+}
+
+template <int BN, int CG>
+cudaError_t launch_tiles(const CUtensorMap& tmA, const CUtensorMap& tmW, const GemmArgs& a, int64_t tiles,
+                         int splits, size_t smem, cudaStream_t s) {
+    cudaError_t e = prepare_tiles<BN, CG>();
+    if (e != cudaSuccess) return e;
+    if constexpr (CG == 2) {
+        const int64_t pairs = std::min<int64_t>(tiles, std::max(1, resident_pairs() / splits));
+        return launch_pair_pdl(gemm_tc_kernel<BN, CG>, dim3(static_cast<unsigned>(2 * pairs), splits),
+                               dim3(kGemmThreads), smem, s, tmA, tmW, a);
+    } else {
+        const int64_t ctas = std::min<int64_t>(tiles, std::max(1, num_sms() / splits));
+        return launch_pdl(gemm_tc_kernel<BN, CG>, dim3(static_cast<unsigned>(ctas), splits), dim3(kGemmThreads),
+                          smem, s, tmA, tmW, a);
+    }
 }
 
 }  // namespace
@@ -571,8 +694,8 @@ bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype
     CUtensorMap tmA, tmW;
     if (!make_kslab_map(&tmA, A, static_cast<uint64_t>(K), static_cast<uint64_t>(M), static_cast<uint32_t>(L.a_box),
                         static_cast<uint32_t>(L.kps)) ||
-        !make_kslab_map(&tmW, W, static_cast<uint64_t>(K), static_cast<uint64_t>(N), static_cast<uint32_t>(L.bn),
-                        static_cast<uint32_t>(L.kps)))
+        !make_kslab_map(&tmW, W, static_cast<uint64_t>(K), static_cast<uint64_t>(N),
+                        static_cast<uint32_t>(L.bn / L.cg), static_cast<uint32_t>(L.kps)))
         return fail(BI_ERR_CUDA, "cuTensorMapEncodeTiled failed");
 
     GemmArgs a{};
@@ -581,7 +704,7 @@ bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype
     a.K = K;
     a.kb_per_split = per;
     a.nkb_total = nkb;
-    a.m_tiles = static_cast<int32_t>((M + kBM - 1) / kBM);
+    a.m_tiles = static_cast<int32_t>((M + L.cg * kBM - 1) / (L.cg * kBM));
     a.n_tiles = N / L.bn;
     a.a_box_rows = L.a_box;
     a.a_stride = L.a_stride;
@@ -617,10 +740,13 @@ bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype
     const int64_t tiles = static_cast<int64_t>(a.m_tiles) * a.n_tiles;
     if (tiles > 0x7fffffffLL) return fail(BI_ERR_SHAPE, "bi_gemm: too many tiles");
     a.total_tiles = static_cast<int32_t>(tiles);
-    const int64_t ctas = std::min<int64_t>(tiles, std::max(1, num_sms() / plan.splits));
-    dim3 grid(static_cast<unsigned>(ctas), plan.splits);
-    cudaError_t e = L.bn == 256 ? launch_tiles<256>(tmA, tmW, a, grid, L.smem, s)
-                                : launch_tiles<kUN>(tmA, tmW, a, grid, L.smem, s);
+    cudaError_t e;
+    if (L.cg == 2)
+        e = L.bn == 256 ? launch_tiles<256, 2>(tmA, tmW, a, tiles, plan.splits, L.smem, s)
+                        : launch_tiles<kUN, 2>(tmA, tmW, a, tiles, plan.splits, L.smem, s);
+    else
+        e = L.bn == 256 ? launch_tiles<256, 1>(tmA, tmW, a, tiles, plan.splits, L.smem, s)
+                        : launch_tiles<kUN, 1>(tmA, tmW, a, tiles, plan.splits, L.smem, s);
     if (e != cudaSuccess) return cuda_fail(e, "gemm_tc_kernel launch");
     if (plan.splits > 1) {
         const int64_t n_out = ep == BI_EP_SWIGLU ? M * (N / 2) : M * N;

@@ -70,7 +70,8 @@ def test_rmsnorm_in_place(bi):
 # ---------------------------------------------------------------------------
 
 @pytest.mark.parametrize("M,N,K", [(1, 128, 64), (5, 128, 256), (128, 128, 4096), (129, 384, 1024),
-                                   (300, 256, 14336), (64, 512, 4096), (17, 640, 1984), (600, 768, 512)])
+                                   (300, 256, 14336), (64, 512, 4096), (17, 640, 1984), (600, 768, 512),
+                                   (3, 25600, 128), (520, 8192, 128), (3, 65664, 128), (300, 65792, 64)])
 def test_gemm_integer_valued_exact(bi, M, N, K):
     A = int_bf16((M, K), 100 + M)
     W = int_bf16((N, K), 200 + N)
@@ -140,6 +141,18 @@ def test_gemm_row_invariance(bi):
     perm = torch.randperm(300, generator=torch.Generator().manual_seed(5))
     got = bits(bi.gemm(A[perm.cuda()].contiguous(), W, c_dtype=bi.F32))
     assert np.array_equal(got, full[perm.numpy()])
+
+
+def test_gemm_row_invariance_across_tile_widths(bi):
+    """Both MMA forms take 256-wide tiles for M > 256 and 128-wide tiles otherwise: here a vocabulary-wide
+    matrix (N > 65536, single-CTA form).  Same MMA sequence per element, so the same bits."""
+    K, N = 128, 65792
+    A = rand_bf16((520, K), 1.0, 610)
+    W = rand_bf16((N, K), 0.02, 611)
+    full = bits(bi.gemm(A, W, c_dtype=bi.F32))
+    for rows in ([0], [519], list(range(256, 512)), [7, 300, 2, 450]):
+        got = bits(bi.gemm(A[rows].contiguous(), W, c_dtype=bi.F32))
+        assert np.array_equal(got, full[rows]), rows
 
 
 def test_gemm_variant_mode_splits_k(bi):
