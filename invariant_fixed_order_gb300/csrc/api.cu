@@ -488,7 +488,9 @@ extern "C" bi_status bi_forward_step(bi_model* m, const bi_batch* batch, const b
                    scale, dev_status};
         if (nd > 0) {
             EntryMap em{1, d_dec, d_req, d_pos, b.B};
-            BI_TRY_CUDA(launch_decode_attention(g, em, nd, dec_splits, chunk2, dec_o, dec_ml, s), "decode attention");
+            // a decode entry's only new key (its last position) was appended just before
+            BI_TRY_CUDA(launch_decode_attention(g, em, nd, dec_splits, chunk2, dec_o, dec_ml, s, /*early_kv=*/true),
+                        "decode attention");
         }
         if (T - nd > 0) {
             EntryMap em{1, d_pre, d_req, d_pos, b.B};

@@ -123,9 +123,13 @@ int32_t invariant_max_splits(int32_t max_seq);
 // variant occupancy rule: fills chunk2 and the bound on splits per request
 void variant_split_plan(int32_t B, int32_t H, int32_t Hkv, int32_t max_seq, int32_t* chunk2,
                         int32_t* max_splits);
+// early_kv: the caller guarantees that of each entry's keys only the last
+// position was written since the kernels before this one in the stream began
+// (the forward step's decode entries); chunks before it then request their
+// K/V copies before the dependency wait.
 cudaError_t launch_decode_attention(const AttnGeom& g, const EntryMap& em, int32_t n_entries,
                                     int32_t max_splits, int32_t variant_chunk2, float* ws_o,
-                                    float* ws_ml, cudaStream_t s);
+                                    float* ws_ml, cudaStream_t s, bool early_kv = false);
 cudaError_t launch_prefill_attention(const AttnGeom& g, const EntryMap& em, int32_t n_entries,
                                      cudaStream_t s);
 bool attention_supported(int32_t H, int32_t Hkv, int32_t Dh);

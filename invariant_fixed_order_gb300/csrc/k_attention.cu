@@ -29,7 +29,12 @@ constexpr int kAttnThreads = 128;
 constexpr int kWarps = kAttnThreads / 32;
 constexpr int kMaxChunkPages = BI_KV_CHUNK / BI_PAGE + 1;  // a variant piece may straddle one more page
 constexpr int kSub = 64;  // keys per staged sub-chunk
-constexpr int kRing = 2;  // staged sub-chunks in flight (a shallow ring fits several CTAs per SM)
+// Staged sub-chunks in flight: a shallow ring (2) fits six CTAs per SM and
+// serves many CTAs; a decode grid that fits the GPU in one wave at three
+// CTAs per SM takes a deep one (4: all K sub-chunks of a chunk at once), so a
+// CTA's copies overlap instead of queueing behind each other.
+constexpr int kRing = 2;
+constexpr int kDeepRing = 4;
 // Row strides chosen for conflict-free shared-memory access patterns of the
 // MMA fragments: scores (fp32), the bf16 hi/lo parts of p, staged outputs.
 constexpr int kPStride = BI_KV_CHUNK + 4;
@@ -74,13 +79,14 @@ struct ScoreStore<C, false> {
 // box writes: per 64-element half of the head dim, kSub rows of 128 bytes, the
 // 16-byte chunk c of row r at chunk c ^ (r & 7).  The ring comes first so a
 // 1024-byte aligned dynamic shared memory base keeps every stage aligned.
-template <int G, int DH, int NT>
+template <int G, int DH, int NT, int RING = kRing>
 struct AttnSmem {
     using S = AttnShape<G, DH, NT>;
     static constexpr bool kSharedScores = S::kCols <= 8;
-    uint8_t ring[kRing][kSub * DH * 2];
+    static constexpr int kStages = RING;
+    uint8_t ring[RING][kSub * DH * 2];
     ScoreStore<S::kCols, kSharedScores> sc;
-    uint64_t full[kRing];            // TMA completion per ring stage
+    uint64_t full[RING];             // TMA completion per ring stage
     int32_t abort;                   // a copy did not land: issue no more
     float red[kWarps][S::kCols];     // per-warp partial sums of l
     float m[S::kCols];
@@ -162,7 +168,7 @@ __device__ __forceinline__ uint32_t ring_off(int row, int c) {
 template <typename Sm>
 __device__ __forceinline__ void ring_init(Sm& sm) {
     if (threadIdx.x == 0) {
-        for (int s = 0; s < kRing; ++s) ptx::mbar_init(&sm.full[s], 1);
+        for (int s = 0; s < Sm::kStages; ++s) ptx::mbar_init(&sm.full[s], 1);
         sm.abort = 0;
         ptx::fence_barrier_init();
     }
@@ -218,19 +224,21 @@ __device__ __forceinline__ void load_q_cols(const uint16_t* q, const int32_t (&t
 //       hi product then the lo product accumulated in fp32.
 // A key a column does not attend to gets p = 0, which adds exact zeros, so a
 // column's bits do not depend on the other columns of its CTA.  K and V rows
-// stream through a ring of kRing shared-memory stages of kSub keys each, K
+// stream through a ring of RING shared-memory stages of kSub keys each, K
 // sub-chunks first, then V sub-chunks: as TMA boxes of one 16-key page of the
 // KV head (two boxes per page at DH = 128) when the chunk starts on a page,
 // else by cp.async into the same layout.  phase tracks the stages' mbarrier
-// parities across calls.
-template <int G, int DH, int NT>
-__device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uint16_t* __restrict__ kc,
+// parities across calls.  ready() runs once the first stages are requested
+// and before the query fragments qb are read (decode loads them there).
+template <int G, int DH, int NT, int RING, typename Ready>
+__device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT, RING>& sm, const uint16_t* __restrict__ kc,
                                               const uint16_t* __restrict__ vc, const CUtensorMap* tmK,
                                               const CUtensorMap* tmV, uint32_t& phase, const int32_t* page_row,
                                               int32_t g, int32_t Hkv, int32_t k0, int32_t n_max, float scale,
                                               int32_t max_pages, int32_t num_pages, int32_t* status,
-                                              const uint32_t (&qb)[AttnShape<G, DH, NT>::kNB][DH / 16][2],
-                                              float (&oacc)[AttnShape<G, DH, NT>::kMT][AttnShape<G, DH, NT>::kNB][4]) {
+                                              uint32_t (&qb)[AttnShape<G, DH, NT>::kNB][DH / 16][2],
+                                              float (&oacc)[AttnShape<G, DH, NT>::kMT][AttnShape<G, DH, NT>::kNB][4],
+                                              Ready&& ready) {
     using S = AttnShape<G, DH, NT>;
     constexpr int kVecPerRow = DH / 8;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
@@ -262,14 +270,14 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
             const bool is_v = t >= ns;
             const int32_t j0 = (is_v ? t - ns : t) * kSub;
             const int32_t nk = min(kSub, n_max - j0);
-            uint8_t* dst = sm.ring[t % kRing];
+            uint8_t* dst = sm.ring[t % RING];
             if (use_tma) {
                 if (sm.abort) return;
-                issued |= 1u << (t % kRing);
+                issued |= 1u << (t % RING);
                 if (tid == 0) {
                     const int npg = (nk + BI_PAGE - 1) / BI_PAGE;
                     const CUtensorMap* map = is_v ? tmV : tmK;
-                    uint64_t* bar = &sm.full[t % kRing];
+                    uint64_t* bar = &sm.full[t % RING];
                     ptx::fence_proxy_async_smem();  // earlier generic writes to the stage before the copy
                     ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(npg * kHalves * BI_PAGE * 128));
                     for (int i = 0; i < npg; ++i) {
@@ -298,7 +306,8 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
         if (!use_tma) cp_async_commit();  // possibly empty: keeps one group per sub-chunk slot
     };
 #pragma unroll
-    for (int t = 0; t < kRing; ++t) issue(t);
+    for (int t = 0; t < RING; ++t) issue(t);
+    ready();
 
 #pragma unroll
     for (int mt = 0; mt < S::kMT; ++mt)
@@ -315,7 +324,7 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
         }
 
     for (int t = 0; t < 2 * ns; ++t) {
-        const int st = t % kRing;
+        const int st = t % RING;
         bool padded = false;  // (uniform) rows of this stage were just zeroed by several threads
         if (use_tma) {
             if (issued & (1u << st)) {
@@ -339,7 +348,7 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
                 }
             }
         } else {
-            asm volatile("cp.async.wait_group %0;" ::"n"(kRing - 1) : "memory");
+            asm volatile("cp.async.wait_group %0;" ::"n"(RING - 1) : "memory");
         }
         // a thread's own mbarrier wait makes a TMA stage visible to it; cp.async
         // stages and zero-padded rows need the CTA barrier
@@ -385,7 +394,7 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
                 float ls[S::kCols];
 #pragma unroll
                 for (int c = 0; c < S::kCols; ++c) ls[c] = 0.0f;
-                if constexpr (AttnSmem<G, DH, NT>::kSharedScores) {
+                if constexpr (AttnSmem<G, DH, NT, RING>::kSharedScores) {
                     // the hi/lo parts overwrite the scores: each thread first takes
                     // all of its scores (j = tid + 128i) into registers
                     constexpr int kJ = BI_KV_CHUNK / kAttnThreads;
@@ -477,7 +486,7 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT>& sm, const uin
             }
         }
         __syncthreads();
-        issue(t + kRing);
+        issue(t + RING);
     }
     if (!use_tma) cp_async_wait_all();
     __syncthreads();
@@ -531,40 +540,49 @@ __device__ __forceinline__ void pieces(int32_t s, int32_t chunk2, int32_t& size,
 // ---------------------------------------------------------------------------
 // Decode: grid (entries, Hkv, max_splits); one token, its G heads as columns.
 // ---------------------------------------------------------------------------
-template <int G, int DH>
+template <int G, int DH, int RING>
 __global__ void __launch_bounds__(kAttnThreads, 6)
 decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnGeom geo,
                     EntryMap em, int32_t max_splits, int32_t chunk2, float* __restrict__ ws_o,
-                    float* __restrict__ ws_ml) {
+                    float* __restrict__ ws_ml, int32_t early_kv) {
     pdl_trigger();
-    pdl_wait();
     using S = AttnShape<G, DH, 1>;
     extern __shared__ __align__(16) unsigned char smem_raw[];
-    AttnSmem<G, DH, 1>& sm = *reinterpret_cast<AttnSmem<G, DH, 1>*>(smem_raw);
+    AttnSmem<G, DH, 1, RING>& sm = *reinterpret_cast<AttnSmem<G, DH, 1, RING>*>(smem_raw);
+    // The entry map and the page table are written before the kernels that
+    // precede this one in the stream start (host copies); q and this step's
+    // keys are written by the kernel just before it.
     const int32_t e = blockIdx.x, g = blockIdx.y, split = blockIdx.z;
     const Entry en = get_entry(em, e);
     const int32_t s = en.p + 1;
     int32_t size, count;
     pieces(s > 0 ? s : 1, chunk2, size, count);
     const bool ok = en.p >= 0 && (s + BI_PAGE - 1) / BI_PAGE <= geo.max_pages && count <= max_splits;
-    if (!ok) {
-        if (split == 0 && g == 0 && threadIdx.x == 0) report(geo.status, BI_DEV_BAD_POSITION);
+    if (!ok || split >= count) {
+        pdl_wait();
+        if (!ok && split == 0 && g == 0 && threadIdx.x == 0) report(geo.status, BI_DEV_BAD_POSITION);
         return;
     }
-    if (split >= count) return;
     const int32_t k0 = split * size;
     const int32_t n = min(size, s - k0);
+    // With early_kv the caller guarantees that only each request's last
+    // position was written in this step: a chunk before it may then request
+    // its K/V copies before the dependency wait.
+    const bool settled = early_kv != 0 && k0 + n < s;
+    if (!settled) pdl_wait();
     if (threadIdx.x < S::kCols) sm.ncol[threadIdx.x] = n;
     ring_init(sm);
     uint32_t phase = 0;
     const int32_t tok[1] = {en.t};
     uint32_t qb[S::kNB][DH / 16][2];
-    load_q_cols<G, DH, 1>(reinterpret_cast<const uint16_t*>(geo.q), tok, geo.H, g, qb);
     float oacc[S::kMT][S::kNB][4];
-    chunk_partial<G, DH, 1>(sm, reinterpret_cast<const uint16_t*>(geo.kc), reinterpret_cast<const uint16_t*>(geo.vc),
-                            &tmK, &tmV, phase, geo.page_table + static_cast<int64_t>(en.r) * geo.max_pages, g,
-                            geo.Hkv, k0, n,
-                            geo.scale, geo.max_pages, geo.num_pages, geo.status, qb, oacc);
+    chunk_partial<G, DH, 1, RING>(
+        sm, reinterpret_cast<const uint16_t*>(geo.kc), reinterpret_cast<const uint16_t*>(geo.vc), &tmK, &tmV, phase,
+        geo.page_table + static_cast<int64_t>(en.r) * geo.max_pages, g, geo.Hkv, k0, n, geo.scale, geo.max_pages,
+        geo.num_pages, geo.status, qb, oacc, [&] {
+            if (settled) pdl_wait();
+            load_q_cols<G, DH, 1>(reinterpret_cast<const uint16_t*>(geo.q), tok, geo.H, g, qb);
+        });
     // stage the partials through the score buffer, then write whole rows
     constexpr int kOStride = DH + 4;
     float* stage = &sm.sc.p[0][0];  // [kCols][kOStride]
@@ -687,7 +705,7 @@ prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ 
                                      reinterpret_cast<const uint16_t*>(geo.vc), &tmK, &tmV, phase, page_row, g,
                                      geo.Hkv, k0,
                                      min(BI_KV_CHUNK, s_max - k0), geo.scale, geo.max_pages, geo.num_pages,
-                                     geo.status, qb, o);
+                                     geo.status, qb, o, [] {});
             // the decode merge's fold (fold_step), one column's (M, L) at a time
             if (tid < S::kCols && sm.ncol[tid] > 0) {
                 const float m = sm.m[tid], l = sm.l[tid];
@@ -778,14 +796,14 @@ size_t decode_ws_bytes(int32_t n_entries, int32_t H, int32_t Dh, int32_t max_spl
     return rows * (Dh + 2) * sizeof(float) + 256;
 }
 
-template <int G, int DH>
-static cudaError_t launch_decode_t(const AttnGeom& g, const EntryMap& em, int32_t n, int32_t max_splits,
-                                   int32_t chunk2, float* ws_o, float* ws_ml, cudaStream_t s) {
-    const size_t smem = sizeof(AttnSmem<G, DH, 1>);
+template <int G, int DH, int RING>
+static cudaError_t launch_decode_ring(const AttnGeom& g, const EntryMap& em, int32_t n, int32_t max_splits,
+                                      int32_t chunk2, float* ws_o, float* ws_ml, bool early_kv, cudaStream_t s) {
+    const size_t smem = sizeof(AttnSmem<G, DH, 1, RING>);
     static bool attr_set = false;
     if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<G, DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
+        cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<G, DH, RING>,
+                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
         if (e != cudaSuccess) return e;
         attr_set = true;
     }
@@ -793,11 +811,21 @@ static cudaError_t launch_decode_t(const AttnGeom& g, const EntryMap& em, int32_
     if (!encode_kv_map(&tmK, g.kc, g.num_pages, g.Hkv, DH) || !encode_kv_map(&tmV, g.vc, g.num_pages, g.Hkv, DH))
         return cudaErrorInvalidValue;
     dim3 grid(n, g.Hkv, max_splits);
-    cudaError_t e = launch_pdl(decode_split_kernel<G, DH>, grid, dim3(kAttnThreads), smem, s, tmK, tmV, g, em,
-                               max_splits, chunk2, ws_o, ws_ml);
+    cudaError_t e = launch_pdl(decode_split_kernel<G, DH, RING>, grid, dim3(kAttnThreads), smem, s, tmK, tmV, g, em,
+                               max_splits, chunk2, ws_o, ws_ml, static_cast<int32_t>(early_kv));
     if (e != cudaSuccess) return e;
     return launch_pdl(decode_merge_kernel<DH>, dim3(n, g.H), dim3(DH / 2), 0, s, g, em, max_splits, chunk2,
                       static_cast<const float*>(ws_o), static_cast<const float*>(ws_ml));
+}
+
+template <int G, int DH>
+static cudaError_t launch_decode_t(const AttnGeom& g, const EntryMap& em, int32_t n, int32_t max_splits,
+                                   int32_t chunk2, float* ws_o, float* ws_ml, bool early_kv, cudaStream_t s) {
+    // ring depth moves data only: the arithmetic of a chunk is the same for both
+    const int64_t ctas = static_cast<int64_t>(n) * g.Hkv * max_splits;
+    if (ctas <= 3ll * num_sms())
+        return launch_decode_ring<G, DH, kDeepRing>(g, em, n, max_splits, chunk2, ws_o, ws_ml, early_kv, s);
+    return launch_decode_ring<G, DH, kRing>(g, em, n, max_splits, chunk2, ws_o, ws_ml, early_kv, s);
 }
 
 // Query tokens per prefill CTA: 16 (token, head) columns.
@@ -841,9 +869,9 @@ static cudaError_t launch_prefill_t(const AttnGeom& g, const EntryMap& em, int32
 
 cudaError_t launch_decode_attention(const AttnGeom& g, const EntryMap& em, int32_t n_entries,
                                     int32_t max_splits, int32_t variant_chunk2, float* ws_o, float* ws_ml,
-                                    cudaStream_t s) {
+                                    cudaStream_t s, bool early_kv) {
     if (n_entries <= 0) return cudaSuccess;
-    BI_ATTN_DISPATCH(launch_decode_t, g, em, n_entries, max_splits, variant_chunk2, ws_o, ws_ml, s);
+    BI_ATTN_DISPATCH(launch_decode_t, g, em, n_entries, max_splits, variant_chunk2, ws_o, ws_ml, early_kv, s);
 }
 
 cudaError_t launch_prefill_attention(const AttnGeom& g, const EntryMap& em, int32_t n_entries, cudaStream_t s) {

@@ -663,6 +663,7 @@ int resident_pairs() {
     return pairs;
 }
 
+// Units (pairs or CTAs) launched: one per tile up to what fits at once.
 template <int BN, int CG>
 cudaError_t launch_tiles(const CUtensorMap& tmA, const CUtensorMap& tmW, const GemmArgs& a, int64_t tiles,
                          int splits, size_t smem, cudaStream_t s) {
