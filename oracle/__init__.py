@@ -85,6 +85,14 @@ def lib():
             L.orc_argmax.restype = i32
             L.orc_argmax.argtypes = [f32p, i32]
             L.orc_argmax_rows.argtypes = [f32p, i32p, i64, i32]
+            f64p, u32p, u8p = (ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_uint32),
+                               ctypes.POINTER(ctypes.c_uint8))
+            L.orc_log_softmax_rows.argtypes = [f32p, f64p, i64, i32]
+            L.orc_murmur3_32.restype = ctypes.c_uint32
+            L.orc_murmur3_32.argtypes = [u8p, i32, ctypes.c_uint32]
+            L.orc_sample_gumbel.restype = ctypes.c_int32
+            L.orc_sample_gumbel.argtypes = [f32p, i32, ctypes.c_uint32, i32, ctypes.c_float]
+            L.orc_sample_gumbel_rows.argtypes = [f32p, u32p, i32p, f32p, i32p, i64, i32]
             L.orc_rope_table.argtypes = [f32p, f32p, i32, i32, ctypes.c_double]
             L.orc_rope_apply.argtypes = [f32p, i32p, i64, i32, f32p, f32p, i32]
             L.orc_attention_head.argtypes = [f32p, f32p, f32p, i32, i64, i32, ctypes.c_float, f32p]
@@ -181,6 +189,40 @@ def argmax_rows(x) -> np.ndarray:
     rows, n = x.shape
     out = np.empty(rows, np.int32)
     _check(lib().orc_argmax_rows(_ptr(x), _ptr(out, ctypes.c_int32), rows, n), "argmax_rows")
+    return out
+
+
+def log_softmax_rows(x) -> np.ndarray:
+    """float64 logprobs of each row of fp32 logits (the definition)."""
+    x = _f32(np.atleast_2d(x))
+    rows, n = x.shape
+    out = np.empty((rows, n), np.float64)
+    _check(lib().orc_log_softmax_rows(_ptr(x), _ptr(out, ctypes.c_double), rows, n), "log_softmax_rows")
+    return out
+
+
+def murmur3_32(key: bytes, seed: int) -> int:
+    buf = np.frombuffer(key, np.uint8).copy() if key else np.zeros(1, np.uint8)
+    return int(lib().orc_murmur3_32(_ptr(buf, ctypes.c_uint8), len(key), seed & 0xffffffff))
+
+
+def sample_gumbel(x, seed: int, pos: int, t: float) -> int:
+    x = _f32(np.ravel(x))
+    r = int(lib().orc_sample_gumbel(_ptr(x), x.size, seed & 0xffffffff, pos, t))
+    if r < 0:
+        raise ValueError("oracle sample_gumbel: bad arguments")
+    return r
+
+
+def sample_gumbel_rows(x, seeds, pos, t) -> np.ndarray:
+    x = _f32(np.atleast_2d(x))
+    rows, n = x.shape
+    seeds = np.ascontiguousarray(np.asarray(seeds, dtype=np.uint32).reshape(rows))
+    pos = _i32(np.asarray(pos).reshape(rows))
+    t = _f32(np.asarray(t).reshape(rows))
+    out = np.empty(rows, np.int32)
+    _check(lib().orc_sample_gumbel_rows(_ptr(x), _ptr(seeds, ctypes.c_uint32), _ptr(pos, ctypes.c_int32), _ptr(t),
+                                        _ptr(out, ctypes.c_int32), rows, n), "sample_gumbel_rows")
     return out
 
 

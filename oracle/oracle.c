@@ -158,6 +158,111 @@ int orc_argmax_rows(const float* x, int32_t* out, int64_t rows, int32_t n) {
 }
 
 /* ------------------------------------------------------------------------ */
+/* Logprobs and seeded sampling                                               */
+/* ------------------------------------------------------------------------ */
+
+/* "Mathematically equivalent is not bitwise equivalent": logprobs are the
+ * log_softmax of the logits.  The definition, row by row, in float64. */
+int orc_log_softmax_rows(const float* x, double* lp, int64_t rows, int32_t n) {
+    if (!x || !lp || rows < 0 || n <= 0) return -1;
+#pragma omp parallel for schedule(static)
+    for (int64_t r = 0; r < rows; ++r) {
+        const float* xr = x + r * (int64_t)n;
+        double m = (double)xr[0];
+        for (int32_t j = 1; j < n; ++j) if ((double)xr[j] > m) m = (double)xr[j];
+        double z = 0.0;
+        for (int32_t j = 0; j < n; ++j) z += exp((double)xr[j] - m);
+        const double lz = log(z);
+        for (int32_t j = 0; j < n; ++j) lp[r * (int64_t)n + j] = ((double)xr[j] - m) - lz;
+    }
+    return 0;
+}
+
+static uint32_t rotl32(uint32_t v, int r) { return (v << r) | (v >> (32 - r)); }
+
+/* MurmurHash3_x86_32 (Austin Appleby's public-domain hash): 4-byte blocks
+ * read little-endian, each scrambled and mixed into h; the 1-3 tail bytes
+ * scrambled into h; then the length and the final avalanche. */
+uint32_t orc_murmur3_32(const uint8_t* key, int32_t len, uint32_t seed) {
+    const uint32_t c1 = 0xcc9e2d51u, c2 = 0x1b873593u;
+    uint32_t h = seed;
+    const int32_t nblocks = len / 4;
+    for (int32_t i = 0; i < nblocks; ++i) {
+        uint32_t k = (uint32_t)key[4 * i] | ((uint32_t)key[4 * i + 1] << 8) | ((uint32_t)key[4 * i + 2] << 16) |
+                     ((uint32_t)key[4 * i + 3] << 24);
+        k *= c1;
+        k = rotl32(k, 15);
+        k *= c2;
+        h ^= k;
+        h = rotl32(h, 13);
+        h = h * 5u + 0xe6546b64u;
+    }
+    const uint8_t* tail = key + 4 * nblocks;
+    uint32_t k = 0;
+    switch (len & 3) {
+        case 3: k ^= (uint32_t)tail[2] << 16; /* fall through */
+        case 2: k ^= (uint32_t)tail[1] << 8;  /* fall through */
+        case 1:
+            k ^= (uint32_t)tail[0];
+            k *= c1;
+            k = rotl32(k, 15);
+            k *= c2;
+            h ^= k;
+    }
+    h ^= (uint32_t)len;
+    h ^= h >> 16;
+    h *= 0x85ebca6bu;
+    h ^= h >> 13;
+    h *= 0xc2b2ae35u;
+    h ^= h >> 16;
+    return h;
+}
+
+/* "The weaker guarantees, which are usually enough": a request's draws come
+ * from its own seed, position and the column, not from a global stream. */
+int32_t orc_sample_gumbel(const float* x, int32_t n, uint32_t seed, int32_t pos, float t) {
+    if (!x || n <= 0) return -1;
+    if (!(t > 0.0f)) return orc_argmax(x, n); /* temperature 0 (or not positive): greedy */
+    int32_t best = -1;
+    double best_s = 0.0;
+    for (int32_t j = 0; j < n; ++j) {
+        uint8_t key[8];
+        const uint32_t p = (uint32_t)pos, c = (uint32_t)j;
+        for (int b = 0; b < 4; ++b) {
+            key[b] = (uint8_t)(p >> (8 * b));
+            key[4 + b] = (uint8_t)(c >> (8 * b));
+        }
+        const uint32_t h = orc_murmur3_32(key, 8, seed);
+        const double u = ((double)h + 0.5) / 4294967296.0;
+        const double g = -log(-log(u));
+        const double sc = (double)x[j] / (double)t + g;
+        if (best < 0) {
+            best = j;
+            best_s = sc;
+            continue;
+        }
+        if (isnan(best_s)) break; /* first NaN already holds */
+        if (isnan(sc) || sc > best_s) {
+            best = j;
+            best_s = sc;
+        }
+    }
+    return best;
+}
+
+int orc_sample_gumbel_rows(const float* x, const uint32_t* seeds, const int32_t* pos, const float* t,
+                           int32_t* out, int64_t rows, int32_t n) {
+    if (!x || !seeds || !pos || !t || !out || rows < 0 || n <= 0) return -1;
+    int bad = 0;
+#pragma omp parallel for schedule(static) reduction(| : bad)
+    for (int64_t r = 0; r < rows; ++r) {
+        out[r] = orc_sample_gumbel(x + r * (int64_t)n, n, seeds[r], pos[r], t[r]);
+        bad |= out[r] < 0;
+    }
+    return bad ? -2 : 0;
+}
+
+/* ------------------------------------------------------------------------ */
 /* Rotary embedding                                                          */
 /* ------------------------------------------------------------------------ */
 

@@ -58,6 +58,27 @@ int orc_swiglu(const float* g, const float* u, float* h, int64_t n, int round_bf
 int32_t orc_argmax(const float* x, int32_t n);
 int orc_argmax_rows(const float* x, int32_t* out, int64_t rows, int32_t n);
 
+/* ---- logprobs and seeded sampling ---------------------------------------
+ * "The weaker guarantees, which are usually enough" (per-request sampling
+ * determinism: Gumbel noise from murmur_hash32(seed, position, column) in
+ * float64) and "Mathematically equivalent is not bitwise equivalent"
+ * (logprobs from a log_softmax kernel, never log(softmax)). */
+
+/* lp[r,j] = x[r,j] - m_r - log(sum_i exp(x[r,i] - m_r)), m_r = max_i x[r,i]; in float64 */
+int orc_log_softmax_rows(const float* x, double* lp, int64_t rows, int32_t n);
+
+/* MurmurHash3, x86 32-bit variant, of len bytes with a 32-bit seed */
+uint32_t orc_murmur3_32(const uint8_t* key, int32_t len, uint32_t seed);
+
+/* Gumbel-max draw of one row at temperature t > 0, all in float64:
+ *   h_j = murmur3_32(le32(pos) || le32(j), seed), u_j = (h_j + 0.5) / 2^32,
+ *   g_j = -log(-log(u_j)), token = argmax_j (x_j / t + g_j)
+ * ties to the lowest index, a NaN score larger than every number.  A row with
+ * t <= 0 (or NaN) is decoded greedily (orc_argmax). */
+int32_t orc_sample_gumbel(const float* x, int32_t n, uint32_t seed, int32_t pos, float t);
+int orc_sample_gumbel_rows(const float* x, const uint32_t* seeds, const int32_t* pos, const float* t,
+                           int32_t* out, int64_t rows, int32_t n);
+
 /* ---- rotary embedding (rotate-half) ------------------------------------ */
 /* cos/sin tables [n_pos, Dh/2]: angle = pos * theta^(-2i/Dh) in float64, then
  * cos and sin in float64 rounded to float. */

@@ -396,3 +396,97 @@ def test_lm_head_matches_float64_and_argmax():
 def test_embed_gathers_rows():
     E = np.arange(40, dtype=np.float32).reshape(10, 4)
     assert np.array_equal(oracle.embed(E, [3, 0, 9]), E[[3, 0, 9]])
+
+
+# ---------------------------------------------------------------------------
+# "Mathematically equivalent is not bitwise equivalent": logprobs are the
+# log_softmax of the logits
+# ---------------------------------------------------------------------------
+
+@pytest.mark.parametrize("n", [1, 7, 128256])
+def test_log_softmax_uniform_row_is_minus_log_n(n):
+    lp = oracle.log_softmax_rows(np.full((1, n), 3.25, np.float32))
+    assert np.allclose(lp, -np.log(n), rtol=0, atol=1e-12)
+
+
+def test_log_softmax_two_columns_closed_form():
+    a, b = np.float32(1.5), np.float32(-2.25)
+    lp = oracle.log_softmax_rows(np.array([[a, b]], np.float32))[0]
+    d = float(b) - float(a)
+    assert abs(lp[0] - (-np.log1p(np.exp(d)))) < 1e-14
+    assert abs(lp[1] - (d - np.log1p(np.exp(d)))) < 1e-14
+
+
+def test_log_softmax_matches_library_and_invariants():
+    rng = np.random.default_rng(11)
+    # multiples of 2^-10 below 32 in magnitude: adding 64 below is exact in binary32
+    x = np.clip(np.round(rng.standard_normal((5, 3000)) * 4 * 1024) / 1024, -31, 31).astype(np.float32)
+    lp = oracle.log_softmax_rows(x)
+    ref = scipy.special.log_softmax(x.astype(np.float64), axis=1)
+    assert np.max(np.abs(lp - ref)) < 1e-10
+    assert np.allclose(np.exp(lp).sum(axis=1), 1.0, atol=1e-12)
+    assert np.all(lp <= 0)
+    assert np.array_equal(np.argmax(lp, axis=1), np.argmax(x, axis=1))
+    # shifting a row by a constant (exact in binary32 here) leaves its logprobs unchanged
+    lp2 = oracle.log_softmax_rows(x + np.float32(64.0))
+    assert np.max(np.abs(lp2 - lp)) < 1e-12
+    # each row on its own gives the same values as in the batch
+    assert np.array_equal(oracle.log_softmax_rows(x[2:3]), lp[2:3])
+
+
+# ---------------------------------------------------------------------------
+# "The weaker guarantees, which are usually enough": seeded Gumbel sampling
+# ---------------------------------------------------------------------------
+
+# MurmurHash3 x86_32 verification values published with the reference
+# implementation of the hash (key, seed, hash).
+MURMUR3_VECTORS = [(b"", 0, 0x00000000), (b"", 1, 0x514E28B7), (b"", 0xFFFFFFFF, 0x81F16F39),
+                   (b"\0\0\0\0", 0, 0x2362F9DE), (b"aaaa", 0x9747B28C, 0x5A97808A), (b"abc", 0, 0xB3DD93FA),
+                   (b"Hello, world!", 0x9747B28C, 0x24884CBA),
+                   (b"The quick brown fox jumps over the lazy dog", 0x9747B28C, 0x2FA826CD)]
+
+
+@pytest.mark.parametrize("key,seed,expect", MURMUR3_VECTORS)
+def test_murmur3_published_vectors(key, seed, expect):
+    assert oracle.murmur3_32(key, seed) == expect
+
+
+@pytest.mark.parametrize("t", [0.5, 1.0, 2.0])
+def test_gumbel_sampling_frequencies_follow_softmax(t):
+    """Over many positions the draws follow softmax(x / t) (chi-square, 3 degrees of freedom): pins the
+    sign of the Gumbel transform, the temperature's use and the uniform mapping."""
+    x = np.array([0.0, 1.0, 2.0, 0.5], np.float32)
+    n = 20000
+    rows = np.tile(x, (n, 1))
+    tok = oracle.sample_gumbel_rows(rows, np.full(n, 7), np.arange(n), np.full(n, t))
+    counts = np.bincount(tok, minlength=4)
+    p = scipy.special.softmax(x.astype(np.float64) / t)
+    chi2 = float(np.sum((counts - n * p) ** 2 / (n * p)))
+    assert chi2 < 30.0, (counts, n * p)
+
+
+def test_gumbel_sampling_depends_on_seed_position_and_logits_only():
+    rng = np.random.default_rng(3)
+    x = rng.standard_normal(500).astype(np.float32)
+    a = [oracle.sample_gumbel(x, 11, p, 1.0) for p in range(64)]
+    assert a == [oracle.sample_gumbel(x, 11, p, 1.0) for p in range(64)]   # reproducible
+    assert a != [oracle.sample_gumbel(x, 12, p, 1.0) for p in range(64)]   # the seed matters
+    assert len(set(a)) > 20                                                  # positions draw afresh
+    # a column far above the rest always wins (Gumbel noise lies within [-3.2, 23.2])
+    y = x.copy()
+    y[123] = 60.0
+    assert all(oracle.sample_gumbel(y, 5, p, 1.0) == 123 for p in range(32))
+    # lowering a column that did not win leaves the winner (the draws are per column)
+    for p in range(16):
+        w = oracle.sample_gumbel(x, 9, p, 1.0)
+        z = x.copy()
+        z[(w + 1) % x.size] = -1e30
+        assert oracle.sample_gumbel(z, 9, p, 1.0) == w
+
+
+def test_gumbel_sampling_special_rows():
+    x = np.array([0.5, np.nan, 3.0, np.nan], np.float32)
+    assert oracle.sample_gumbel(x, 1, 0, 1.0) == 1          # a NaN beats every number, first NaN wins
+    y = np.array([1.0, 4.0, 4.0, -2.0], np.float32)
+    assert oracle.sample_gumbel(y, 1, 0, 0.0) == 1          # temperature 0: greedy, lowest index of ties
+    assert oracle.sample_gumbel(y, 1, 0, -1.0) == 1
