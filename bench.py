@@ -257,6 +257,31 @@ def attention_time(w: GpuWorkload, steps: int, stream) -> dict:
     return {"us": round(ms * 1e3, 2), "GBps": round(kv / (ms * 1e-3) / 1e9, 1), "kv_bytes": kv}
 
 
+def logits_ops_time(w: GpuWorkload, steps: int, stream, hbm_peak: float) -> dict:
+    """Logprobs (log_softmax) and seeded sampling over the step's B logit rows, standalone with CUDA events.
+    log_softmax algorithmic bytes: the logits read once and the logprobs written once."""
+    import torch
+    from invariant_fixed_order_gb300 import bi
+    cfg, B = w.cfg, w.B
+    dev = w.d_ids.device
+    x = (torch.randn(B, cfg.V, device=dev) * 3.0).float()
+    lp = torch.empty_like(x)
+    ms_ls = time_steps(lambda: bi.log_softmax(x, out=lp, stream=stream), max(steps, 10), 3, stream)
+    g = torch.Generator().manual_seed(DATA_SEED)
+    seeds = torch.randint(0, 2 ** 31 - 1, (B,), generator=g, dtype=torch.int32).to(dev)
+    pos = torch.from_numpy(np.asarray(w.ctx, np.int32)).to(dev)
+    temps = torch.full((B,), 0.8, device=dev)
+    tok = torch.empty(B, dtype=torch.int32, device=dev)
+    ws = torch.empty(bi.sample_workspace_size(B, cfg.V), dtype=torch.uint8, device=dev)
+    ms_s = time_steps(lambda: bi.sample(x, seeds, pos, temps, out=tok, ws=ws, stream=stream), max(steps, 10), 3,
+                      stream)
+    ls_bytes = 2 * B * cfg.V * 4
+    return {"rows": B, "V": cfg.V,
+            "log_softmax": {"us": round(ms_ls * 1e3, 2), "GBps": round(ls_bytes / (ms_ls * 1e-3) / 1e9, 1),
+                            "frac": round(ls_bytes / (ms_ls * 1e-3) / 1e9 / hbm_peak, 3)},
+            "sample": {"us": round(ms_s * 1e3, 2), "Gcols_per_s": round(B * cfg.V / (ms_s * 1e-3) / 1e9, 2)}}
+
+
 def prefill_measure(device: str, steps: int, bf16_peak: float, stream) -> dict:
     """One prefill step of 64 requests (chunks of 256-2048 tokens, contexts from
     position 0) through the same 1-layer + LM-head path, plus the gate/up GEMM
@@ -492,6 +517,7 @@ def run_ours(args):
     # ---- dominant kernel (GEMM) and attention, timed standalone with events ----
     g = gemm_roofline(w, args.steps, stream, hbm_peak)
     att = attention_time(w, args.steps, stream)
+    lops = logits_ops_time(w, args.steps, stream, hbm_peak)
     step_bytes = w.step_bytes(B)
     del w
     torch.cuda.empty_cache()
@@ -516,6 +542,7 @@ def run_ours(args):
                          "per_gemm": g["per_gemm"],
                          "per_launch_bytes": int(g["per_launch_bytes"])},
             "attention": att,
+            "logits_ops": lops,
             "e2e": {"value": round(world * B / (e2e_ms * 1e-3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,

@@ -253,6 +253,34 @@ bi_status bi_prefill_attention(const bi_bf16* q, const int32_t* cu_q, const int3
  * any number (the first NaN wins).  logits DEVICE [R, V] fp32; out DEVICE [R]. */
 bi_status bi_argmax(const float* logits, int32_t* out, int32_t R, int32_t V, bi_stream stream);
 
+/* ---- Logprobs ("Batch invariance and reproducible inference", "Mathematically
+ * equivalent is not bitwise equivalent": logprobs come from one log_softmax
+ * kernel, never log(softmax); "The replacement kernels are deliberately dull":
+ * one thread block per row) -------------------------------------------------
+ * logprobs[r, j] = (logits[r, j] - m_r) - log(z_r), m_r = max_j logits[r, j],
+ * z_r = sum_j exp(logits[r, j] - m_r), fp32, summed in one fixed order that
+ * depends on V alone: a row's logprobs are bitwise the same whatever rows
+ * share the call.  A NaN logit makes its row NaN.  logits and logprobs DEVICE
+ * [R, V] fp32 (may not overlap). */
+bi_status bi_log_softmax(const float* logits, float* logprobs, int32_t R, int32_t V, bi_stream stream);
+
+/* ---- Seeded sampling ("Batch invariance and reproducible inference", "The
+ * weaker guarantees, which are usually enough": Gumbel noise from
+ * murmur_hash32(seed, position, column) in float64) -------------------------
+ * tokens[r] = argmax_j (logits[r, j] / t_r + g_j) in float64, where
+ *   h_j = MurmurHash3_x86_32(le32(positions[r]) || le32(j), seeds[r]),
+ *   u_j = (h_j + 0.5) / 2^32,  g_j = -log(-log(u_j)),  t_r = temperatures[r];
+ * ties go to the lowest index and a NaN score beats every number.  A row with
+ * t_r <= 0 (or NaN) takes the greedy argmax of its logits (as bi_argmax).  A
+ * row's token depends only on its logits, seed, position and temperature.
+ * logits DEVICE [R, V] fp32; seeds DEVICE [R] uint32; positions DEVICE [R]
+ * int32; temperatures DEVICE [R] fp32; tokens DEVICE [R] int32; ws DEVICE
+ * scratch of bi_sample_workspace_size(R, V) bytes, 16-byte aligned. */
+size_t bi_sample_workspace_size(int32_t R, int32_t V);
+bi_status bi_sample(const float* logits, const uint32_t* seeds, const int32_t* positions,
+                    const float* temperatures, int32_t* tokens, int32_t R, int32_t V,
+                    void* ws, size_t ws_bytes, bi_stream stream);
+
 /* ---- Embedding gather -----------------------------------------------------
  * x[t] = E[ids[t]]; E DEVICE [V, d] bf16, ids DEVICE [T], x DEVICE [T, d].
  * Requires d % 8 == 0.  Out-of-range ids report BI_DEV_BAD_TOKEN and write 0. */

@@ -92,6 +92,9 @@ _proto("bi_decode_attention_noalloc", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, 
 _proto("bi_prefill_attention", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
        _i32, _f32, _vp, _vp)
 _proto("bi_argmax", _i32, _vp, _vp, _i32, _i32, _vp)
+_proto("bi_log_softmax", _i32, _vp, _vp, _i32, _i32, _vp)
+_proto("bi_sample_workspace_size", _sz, _i32, _i32)
+_proto("bi_sample", _i32, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _sz, _vp)
 _proto("bi_embed", _i32, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp)
 _proto("bi_model_create", _i32, ctypes.POINTER(ModelConfigC), ctypes.POINTER(ModelWeightsC),
        ctypes.POINTER(_vp))
@@ -251,6 +254,31 @@ def argmax(logits: torch.Tensor, out: torch.Tensor | None = None, stream=None) -
     R, V = logits.shape
     out = torch.empty(R, dtype=torch.int32, device=logits.device) if out is None else out
     _check(_lib.bi_argmax(_p(logits), _p(out), R, V, _stream(stream)))
+    return out
+
+
+def log_softmax(logits: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    R, V = logits.shape
+    out = torch.empty(R, V, dtype=torch.float32, device=logits.device) if out is None else out
+    _check(_lib.bi_log_softmax(_p(logits), _p(out), R, V, _stream(stream)))
+    return out
+
+
+def sample_workspace_size(R: int, V: int) -> int:
+    return int(_lib.bi_sample_workspace_size(R, V))
+
+
+def sample(logits: torch.Tensor, seeds: torch.Tensor, positions: torch.Tensor, temperatures: torch.Tensor,
+           out: torch.Tensor | None = None, ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    """Seeded Gumbel-max tokens; seeds uint32 (or int32 holding the same bits), positions int32,
+    temperatures fp32, all DEVICE [R]."""
+    R, V = logits.shape
+    out = torch.empty(R, dtype=torch.int32, device=logits.device) if out is None else out
+    need = sample_workspace_size(R, V)
+    if ws is None or ws.numel() < need:
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=logits.device)
+    _check(_lib.bi_sample(_p(logits), _p(seeds), _p(positions), _p(temperatures), _p(out), R, V, _p(ws),
+                          ws.numel(), _stream(stream)))
     return out
 
 

@@ -236,6 +236,33 @@ extern "C" bi_status bi_argmax(const float* logits, int32_t* out, int32_t R, int
     return e == cudaSuccess ? BI_OK : cuda_fail(e, "bi_argmax launch");
 }
 
+extern "C" bi_status bi_log_softmax(const float* logits, float* logprobs, int32_t R, int32_t V, bi_stream stream) {
+    if (R < 0 || V <= 0) return fail(BI_ERR_SHAPE, "bi_log_softmax: need R >= 0, V > 0");
+    if (R == 0) return BI_OK;
+    if (!logits || !logprobs) return fail(BI_ERR_INVALID, "bi_log_softmax: null pointer");
+    const char* a = reinterpret_cast<const char*>(logits);
+    const char* b = reinterpret_cast<const char*>(logprobs);
+    const size_t n = static_cast<size_t>(R) * V * sizeof(float);
+    if (a < b + n && b < a + n) return fail(BI_ERR_INVALID, "bi_log_softmax: logits and logprobs overlap");
+    cudaError_t e = launch_log_softmax(logits, logprobs, R, V, static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? BI_OK : cuda_fail(e, "bi_log_softmax launch");
+}
+
+extern "C" size_t bi_sample_workspace_size(int32_t R, int32_t V) { return sample_ws_bytes(R, V); }
+
+extern "C" bi_status bi_sample(const float* logits, const uint32_t* seeds, const int32_t* positions,
+                               const float* temperatures, int32_t* tokens, int32_t R, int32_t V, void* ws,
+                               size_t ws_bytes, bi_stream stream) {
+    if (R < 0 || V <= 0) return fail(BI_ERR_SHAPE, "bi_sample: need R >= 0, V > 0");
+    if (R == 0) return BI_OK;
+    if (!logits || !seeds || !positions || !temperatures || !tokens) return fail(BI_ERR_INVALID, "bi_sample: null pointer");
+    if (!ws || ws_bytes < sample_ws_bytes(R, V) || !aligned16(ws))
+        return fail(BI_ERR_WORKSPACE, "bi_sample: workspace too small or not 16-byte aligned");
+    cudaError_t e = launch_sample(logits, seeds, positions, temperatures, tokens, R, V, ws,
+                                  static_cast<cudaStream_t>(stream));
+    return e == cudaSuccess ? BI_OK : cuda_fail(e, "bi_sample launch");
+}
+
 extern "C" bi_status bi_embed(const bi_bf16* E, const int32_t* ids, bi_bf16* x, int32_t T, int32_t V, int32_t d,
                               int32_t* dev_status, bi_stream stream) {
     if (T < 0 || V <= 0 || d <= 0 || d % 8) return fail(BI_ERR_SHAPE, "bi_embed: need d % 8 == 0");

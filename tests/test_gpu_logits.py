@@ -1,0 +1,138 @@
+"""Logprobs (bi_log_softmax) and seeded sampling (bi_sample) on the GPU against
+the CPU oracle: float64 definitions of "Mathematically equivalent is not
+bitwise equivalent" (log_softmax) and "The weaker guarantees, which are
+usually enough" (Gumbel noise from MurmurHash3 of position and column)."""
+import numpy as np
+import pytest
+import torch
+
+import oracle
+
+pytestmark = pytest.mark.gpu
+
+# |lp_gpu - lp_ref| <= ATOL + RTOL * |lp_ref|: the GPU sums z in fp32 in a fixed
+# order (relative error well below 1e-5 for 128256 terms) and rounds x - m and
+# (x - m) - log z once each (at most 2 ulp of values below 2^7).
+LS_ATOL, LS_RTOL = 1e-4, 1e-6
+
+
+@pytest.fixture(scope="module")
+def bi():
+    if not torch.cuda.is_available():
+        pytest.skip("no GPU")
+    from invariant_fixed_order_gb300 import bi as b
+    return b
+
+
+def logits_rows(R, V, scale, seed):
+    g = torch.Generator().manual_seed(seed)
+    return (torch.randn(R, V, generator=g) * scale).float()
+
+
+@pytest.mark.parametrize("R,V,scale", [(1, 1, 1.0), (3, 7, 2.0), (5, 1000, 4.0), (4, 1001, 3.0), (8, 128256, 3.0),
+                                       (2, 128256, 30.0)])
+def test_log_softmax_parity(bi, R, V, scale):
+    x = logits_rows(R, V, scale, 100 + V)
+    got = bi.log_softmax(x.cuda()).cpu().numpy().astype(np.float64)
+    ref = oracle.log_softmax_rows(x.numpy())
+    err = np.abs(got - ref)
+    assert np.all(err <= LS_ATOL + LS_RTOL * np.abs(ref)), float(err.max())
+
+
+def test_log_softmax_rows_do_not_depend_on_the_batch(bi):
+    x = logits_rows(16, 128256, 3.0, 7).cuda()
+    full = bi.log_softmax(x)
+    for rows in ([0], [15], [3, 9, 1], list(range(8, 16))):
+        alone = bi.log_softmax(x[rows].contiguous())
+        assert torch.equal(alone.view(torch.int32), full[rows].view(torch.int32)), rows
+    perm = torch.randperm(16, generator=torch.Generator().manual_seed(2)).cuda()
+    assert torch.equal(bi.log_softmax(x[perm].contiguous()).view(torch.int32), full[perm].view(torch.int32))
+
+
+def test_log_softmax_special_rows(bi):
+    V = 4096
+    x = torch.zeros(4, V)
+    x[0] = 2.5                      # uniform row: -log V
+    x[1, 17] = float("nan")         # a NaN makes its row NaN
+    x[2, :100] = float("-inf")      # excluded columns: -inf
+    x[3] = torch.arange(V, dtype=torch.float32) * 1e-3
+    got = bi.log_softmax(x.cuda()).cpu()
+    assert torch.allclose(got[0], torch.full((V,), -float(np.log(V))), atol=1e-6)
+    assert torch.isnan(got[1]).all()
+    assert torch.isinf(got[2, :100]).all() and (got[2, :100] < 0).all()
+    ref = oracle.log_softmax_rows(x[2:].numpy())
+    assert np.allclose(got[2, 100:].numpy(), ref[0, 100:], atol=LS_ATOL)
+    assert np.allclose(got[3].numpy(), ref[1], atol=LS_ATOL)
+
+
+def sample_inputs(R, seed):
+    rng = np.random.default_rng(seed)
+    seeds = rng.integers(0, 2 ** 32, R, dtype=np.uint64).astype(np.uint32)
+    pos = rng.integers(0, 40000, R).astype(np.int32)
+    temps = rng.choice(np.array([0.6, 1.0, 1.4, 0.0], np.float32), R)
+    return seeds, pos, temps
+
+
+def run_sample(bi, x, seeds, pos, temps):
+    return bi.sample(x.cuda(), torch.from_numpy(seeds.view(np.int32)).cuda(), torch.from_numpy(pos).cuda(),
+                     torch.from_numpy(temps).cuda()).cpu().numpy()
+
+
+def gumbel_scores(x_row, seed, pos, t, cols):
+    """float64 scores of a few columns, from the oracle's own hash (for a near-tie check)."""
+    out = []
+    for j in cols:
+        h = oracle.murmur3_32(np.array([pos, j], np.uint32).tobytes(), int(seed))
+        u = (h + 0.5) / 2.0 ** 32
+        out.append(float(x_row[j]) / float(t) - np.log(-np.log(u)))
+    return out
+
+
+@pytest.mark.parametrize("R,V,scale", [(64, 128256, 3.0), (16, 5000, 1.0), (8, 4097, 10.0)])
+def test_sample_matches_oracle(bi, R, V, scale):
+    x = logits_rows(R, V, scale, 300 + V)
+    seeds, pos, temps = sample_inputs(R, V)
+    got = run_sample(bi, x, seeds, pos, temps)
+    ref = oracle.sample_gumbel_rows(x.numpy(), seeds, pos, temps)
+    for r in np.nonzero(got != ref)[0]:
+        # both sides take the decision in float64; a difference can only be a near-tie of two columns
+        # whose scores agree to the last bits (the two float64 log implementations may differ by an ulp)
+        a, b = gumbel_scores(x[r].numpy(), seeds[r], pos[r], temps[r], [got[r], ref[r]])
+        assert temps[r] > 0 and abs(a - b) <= 1e-12 * max(1.0, abs(a)), (r, got[r], ref[r], a, b)
+    assert np.mean(got == ref) >= 0.99
+
+
+def test_sample_rows_do_not_depend_on_the_batch(bi):
+    R, V = 32, 128256
+    x = logits_rows(R, V, 3.0, 11)
+    seeds, pos, temps = sample_inputs(R, 12)
+    full = run_sample(bi, x, seeds, pos, temps)
+    for rows in ([0], [31], [5, 2, 20], list(range(10, 30))):
+        rows = np.array(rows)
+        got = run_sample(bi, x[rows].contiguous(), seeds[rows], pos[rows], temps[rows])
+        assert np.array_equal(got, full[rows]), rows
+
+
+def test_sample_frequencies_and_special_rows(bi):
+    # many positions of one 4-column row: the GPU draws are the oracle's draws (which follow softmax(x/t))
+    n = 20000
+    x = torch.tensor([[0.0, 1.0, 2.0, 0.5]]).repeat(n, 1)
+    seeds = np.full(n, 7, np.uint32)
+    pos = np.arange(n, dtype=np.int32)
+    temps = np.full(n, 1.0, np.float32)
+    got = run_sample(bi, x, seeds, pos, temps)
+    assert np.array_equal(got, oracle.sample_gumbel_rows(x.numpy(), seeds, pos, temps))
+    # NaN beats every number (first NaN); temperature 0 is the greedy argmax with ties to the lowest index
+    y = torch.tensor([[0.5, float("nan"), 3.0, float("nan")], [1.0, 4.0, 4.0, -2.0], [1.0, 4.0, 4.0, -2.0]])
+    got = run_sample(bi, y, np.array([1, 1, 1], np.uint32), np.array([0, 0, 0], np.int32),
+                     np.array([1.0, 0.0, -1.0], np.float32))
+    assert got.tolist() == [1, 1, 1]
+
+
+def test_sample_rejects_small_workspace(bi):
+    x = torch.zeros(2, 100, device="cuda")
+    z = torch.zeros(2, dtype=torch.int32, device="cuda")
+    t = torch.ones(2, device="cuda")
+    with pytest.raises(bi.BIError) as e:
+        bi._check(bi._lib.bi_sample(bi._p(x), bi._p(z), bi._p(z), bi._p(t), bi._p(z), 2, 100, None, 0, None))
+    assert e.value.status == bi.BI_ERR_WORKSPACE
