@@ -266,7 +266,8 @@ def logits_ops_time(w: GpuWorkload, steps: int, stream, hbm_peak: float) -> dict
     dev = w.d_ids.device
     x = (torch.randn(B, cfg.V, device=dev) * 3.0).float()
     lp = torch.empty_like(x)
-    ms_ls = time_steps(lambda: bi.log_softmax(x, out=lp, stream=stream), max(steps, 10), 3, stream)
+    lws = torch.empty(bi.log_softmax_workspace_size(B, cfg.V), dtype=torch.uint8, device=dev)
+    ms_ls = time_steps(lambda: bi.log_softmax(x, out=lp, ws=lws, stream=stream), max(steps, 10), 3, stream)
     g = torch.Generator().manual_seed(DATA_SEED)
     seeds = torch.randint(0, 2 ** 31 - 1, (B,), generator=g, dtype=torch.int32).to(dev)
     pos = torch.from_numpy(np.asarray(w.ctx, np.int32)).to(dev)

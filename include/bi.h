@@ -256,13 +256,17 @@ bi_status bi_argmax(const float* logits, int32_t* out, int32_t R, int32_t V, bi_
 /* ---- Logprobs ("Batch invariance and reproducible inference", "Mathematically
  * equivalent is not bitwise equivalent": logprobs come from one log_softmax
  * kernel, never log(softmax); "The replacement kernels are deliberately dull":
- * one thread block per row) -------------------------------------------------
+ * no reduction whose order follows the batch) ------------------------------
  * logprobs[r, j] = (logits[r, j] - m_r) - log(z_r), m_r = max_j logits[r, j],
  * z_r = sum_j exp(logits[r, j] - m_r), fp32, summed in one fixed order that
- * depends on V alone: a row's logprobs are bitwise the same whatever rows
- * share the call.  A NaN logit makes its row NaN.  logits and logprobs DEVICE
- * [R, V] fp32 (may not overlap). */
-bi_status bi_log_softmax(const float* logits, float* logprobs, int32_t R, int32_t V, bi_stream stream);
+ * depends on V alone (segments of 4096 columns, each reduced in a fixed tree,
+ * merged in segment order): a row's logprobs are bitwise the same whatever
+ * rows share the call.  A NaN logit makes its row NaN.  logits and logprobs
+ * DEVICE [R, V] fp32 (may not overlap); ws DEVICE scratch of
+ * bi_log_softmax_workspace_size(R, V) bytes, 16-byte aligned. */
+size_t bi_log_softmax_workspace_size(int32_t R, int32_t V);
+bi_status bi_log_softmax(const float* logits, float* logprobs, int32_t R, int32_t V,
+                         void* ws, size_t ws_bytes, bi_stream stream);
 
 /* ---- Seeded sampling ("Batch invariance and reproducible inference", "The
  * weaker guarantees, which are usually enough": Gumbel noise from
@@ -330,6 +334,21 @@ typedef struct {
     int32_t max_pages;
     int32_t R;                  /* rows that need logits */
     const int32_t* logit_rows;  /* HOST [R] token indices in 0..T-1 */
+    /* DEVICE [3T + R] or NULL.  NULL: the step derives its per-token metadata
+     * from q_len, pos0 and logit_rows and copies it host to device through a
+     * pinned staging buffer.  Non-NULL: the caller has written it on the
+     * device: [request of token t, T][position of token t, T][tokens with
+     * q_len 1 in token order, nd][the other tokens in order, T - nd][logit
+     * rows, R].  The step then reads no host memory after the call and calls
+     * nothing that synchronises, so it can be captured in a CUDA graph
+     * (programmatic dependent launch and cluster launches are captured as
+     * graph edges and nodes) and replayed with new contents of meta,
+     * token_ids and page_table.  q_len, pos0 and logit_rows still give the
+     * shapes (T, nd, R) and bounds: a replayed position must not exceed the
+     * captured pos0[i] + q_len[i] - 1 of its request slot (the attention split
+     * count and workspace were sized from it); larger positions are reported
+     * as BI_DEV_BAD_POSITION. */
+    const int32_t* meta;
 } bi_batch;
 
 typedef struct bi_model bi_model;

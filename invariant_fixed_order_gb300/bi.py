@@ -63,7 +63,7 @@ class KVCacheC(ctypes.Structure):
 
 class BatchC(ctypes.Structure):
     _fields_ = [("B", _i32), ("q_len", _i32p), ("pos0", _i32p), ("token_ids", _vp), ("page_table", _vp),
-                ("max_pages", _i32), ("R", _i32), ("logit_rows", _i32p)]
+                ("max_pages", _i32), ("R", _i32), ("logit_rows", _i32p), ("meta", _vp)]
 
 
 def _proto(name, restype, *args):
@@ -92,7 +92,8 @@ _proto("bi_decode_attention_noalloc", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, 
 _proto("bi_prefill_attention", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
        _i32, _f32, _vp, _vp)
 _proto("bi_argmax", _i32, _vp, _vp, _i32, _i32, _vp)
-_proto("bi_log_softmax", _i32, _vp, _vp, _i32, _i32, _vp)
+_proto("bi_log_softmax_workspace_size", _sz, _i32, _i32)
+_proto("bi_log_softmax", _i32, _vp, _vp, _i32, _i32, _vp, _sz, _vp)
 _proto("bi_sample_workspace_size", _sz, _i32, _i32)
 _proto("bi_sample", _i32, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _vp, _sz, _vp)
 _proto("bi_embed", _i32, _vp, _vp, _vp, _i32, _i32, _i32, _vp, _vp)
@@ -257,10 +258,18 @@ def argmax(logits: torch.Tensor, out: torch.Tensor | None = None, stream=None) -
     return out
 
 
-def log_softmax(logits: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+def log_softmax_workspace_size(R: int, V: int) -> int:
+    return int(_lib.bi_log_softmax_workspace_size(R, V))
+
+
+def log_softmax(logits: torch.Tensor, out: torch.Tensor | None = None, ws: torch.Tensor | None = None,
+                stream=None) -> torch.Tensor:
     R, V = logits.shape
     out = torch.empty(R, V, dtype=torch.float32, device=logits.device) if out is None else out
-    _check(_lib.bi_log_softmax(_p(logits), _p(out), R, V, _stream(stream)))
+    need = log_softmax_workspace_size(R, V)
+    if ws is None or ws.numel() < need:
+        ws = torch.empty(max(need, 1), dtype=torch.uint8, device=logits.device)
+    _check(_lib.bi_log_softmax(_p(logits), _p(out), R, V, _p(ws), ws.numel(), _stream(stream)))
     return out
 
 
@@ -333,14 +342,16 @@ class Model:
 
     def forward_step(self, q_len, pos0, token_ids: torch.Tensor, page_table: torch.Tensor, kv_k: list, kv_v: list,
                      logit_rows, ws: torch.Tensor, status: torch.Tensor, logits_out=None, tokens_out=None,
-                     hidden_out=None, mode: int = INVARIANT, stream=None):
-        """One ragged step.  q_len / pos0 / logit_rows are host int sequences."""
+                     hidden_out=None, mode: int = INVARIANT, stream=None, meta: torch.Tensor | None = None):
+        """One ragged step.  q_len / pos0 / logit_rows are host int sequences; meta (optional) is the
+        step's per-token metadata already on the device (the layout bi_batch documents)."""
         B = len(q_len)
         ql = (ctypes.c_int32 * B)(*[int(v) for v in q_len])
         p0 = (ctypes.c_int32 * B)(*[int(v) for v in pos0])
         R = len(logit_rows)
         rows = (ctypes.c_int32 * max(R, 1))(*[int(v) for v in logit_rows])
-        batch = BatchC(B, ql, p0, token_ids.data_ptr(), page_table.data_ptr(), page_table.shape[-1], R, rows)
+        batch = BatchC(B, ql, p0, token_ids.data_ptr(), page_table.data_ptr(), page_table.shape[-1], R, rows,
+                       None if meta is None else meta.data_ptr())
         ka, va = _ptr_array(kv_k), _ptr_array(kv_v)
         kv = KVCacheC(ka, va, kv_k[0].shape[0])
         _check(_lib.bi_forward_step(self._h, ctypes.byref(batch), ctypes.byref(kv), _p(logits_out), _p(tokens_out),

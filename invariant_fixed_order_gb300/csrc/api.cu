@@ -236,7 +236,10 @@ extern "C" bi_status bi_argmax(const float* logits, int32_t* out, int32_t R, int
     return e == cudaSuccess ? BI_OK : cuda_fail(e, "bi_argmax launch");
 }
 
-extern "C" bi_status bi_log_softmax(const float* logits, float* logprobs, int32_t R, int32_t V, bi_stream stream) {
+extern "C" size_t bi_log_softmax_workspace_size(int32_t R, int32_t V) { return log_softmax_ws_bytes(R, V); }
+
+extern "C" bi_status bi_log_softmax(const float* logits, float* logprobs, int32_t R, int32_t V, void* ws,
+                                    size_t ws_bytes, bi_stream stream) {
     if (R < 0 || V <= 0) return fail(BI_ERR_SHAPE, "bi_log_softmax: need R >= 0, V > 0");
     if (R == 0) return BI_OK;
     if (!logits || !logprobs) return fail(BI_ERR_INVALID, "bi_log_softmax: null pointer");
@@ -244,7 +247,9 @@ extern "C" bi_status bi_log_softmax(const float* logits, float* logprobs, int32_
     const char* b = reinterpret_cast<const char*>(logprobs);
     const size_t n = static_cast<size_t>(R) * V * sizeof(float);
     if (a < b + n && b < a + n) return fail(BI_ERR_INVALID, "bi_log_softmax: logits and logprobs overlap");
-    cudaError_t e = launch_log_softmax(logits, logprobs, R, V, static_cast<cudaStream_t>(stream));
+    if (!ws || ws_bytes < log_softmax_ws_bytes(R, V) || !aligned16(ws))
+        return fail(BI_ERR_WORKSPACE, "bi_log_softmax: workspace too small or not 16-byte aligned");
+    cudaError_t e = launch_log_softmax(logits, logprobs, R, V, ws, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? BI_OK : cuda_fail(e, "bi_log_softmax launch");
 }
 
@@ -445,37 +450,42 @@ extern "C" bi_status bi_forward_step(bi_model* m, const bi_batch* batch, const b
 
     // pinned staging: [tok_req T][tok_pos T][dec_list nd][pre_list T-nd][logit_rows R]
     const size_t meta_n = static_cast<size_t>(T) * 3 + b.R;
-    int slot = m->stage_next;
-    m->stage_next ^= 1;
-    BI_TRY_CUDA(cudaEventSynchronize(m->stage_done[slot]), "bi_forward_step: staging event");
-    if (m->stage_cap[slot] < meta_n) {
-        if (m->stage[slot]) cudaFreeHost(m->stage[slot]);
-        m->stage[slot] = nullptr;
-        m->stage_cap[slot] = 0;
-        const size_t cap = std::max<size_t>(meta_n * 2, 4096);
-        BI_TRY_CUDA(cudaHostAlloc(&m->stage[slot], cap * sizeof(int32_t), cudaHostAllocDefault), "cudaHostAlloc");
-        m->stage_cap[slot] = cap;
-    }
-    int32_t* hm = m->stage[slot];
-    int32_t* h_req = hm;
-    int32_t* h_pos = hm + T;
-    int32_t* h_dec = hm + 2 * static_cast<size_t>(T);
-    int32_t* h_pre = h_dec + nd;
-    int32_t* h_rows = hm + 3 * static_cast<size_t>(T);
-    {
-        int32_t t = 0, di = 0, pi = 0;
-        for (int32_t i = 0; i < b.B; ++i)
-            for (int32_t j = 0; j < b.q_len[i]; ++j, ++t) {
-                h_req[t] = i;
-                h_pos[t] = b.pos0[i] + j;
-                if (b.q_len[i] == 1) h_dec[di++] = t; else h_pre[pi++] = t;
-            }
-        std::memcpy(h_rows, b.logit_rows, sizeof(int32_t) * b.R);
-    }
     char* base = static_cast<char*>(ws);
-    int32_t* d_meta = reinterpret_cast<int32_t*>(base + L.meta);
-    BI_TRY_CUDA(cudaMemcpyAsync(d_meta, hm, meta_n * sizeof(int32_t), cudaMemcpyHostToDevice, s), "metadata copy");
-    BI_TRY_CUDA(cudaEventRecord(m->stage_done[slot], s), "cudaEventRecord");
+    const int32_t* d_meta = b.meta;
+    if (d_meta == nullptr) {
+        // the step derives the metadata on the host and copies it through pinned staging
+        int slot = m->stage_next;
+        m->stage_next ^= 1;
+        BI_TRY_CUDA(cudaEventSynchronize(m->stage_done[slot]), "bi_forward_step: staging event");
+        if (m->stage_cap[slot] < meta_n) {
+            if (m->stage[slot]) cudaFreeHost(m->stage[slot]);
+            m->stage[slot] = nullptr;
+            m->stage_cap[slot] = 0;
+            const size_t cap = std::max<size_t>(meta_n * 2, 4096);
+            BI_TRY_CUDA(cudaHostAlloc(&m->stage[slot], cap * sizeof(int32_t), cudaHostAllocDefault), "cudaHostAlloc");
+            m->stage_cap[slot] = cap;
+        }
+        int32_t* hm = m->stage[slot];
+        int32_t* h_req = hm;
+        int32_t* h_pos = hm + T;
+        int32_t* h_dec = hm + 2 * static_cast<size_t>(T);
+        int32_t* h_pre = h_dec + nd;
+        int32_t* h_rows = hm + 3 * static_cast<size_t>(T);
+        {
+            int32_t t = 0, di = 0, pi = 0;
+            for (int32_t i = 0; i < b.B; ++i)
+                for (int32_t j = 0; j < b.q_len[i]; ++j, ++t) {
+                    h_req[t] = i;
+                    h_pos[t] = b.pos0[i] + j;
+                    if (b.q_len[i] == 1) h_dec[di++] = t; else h_pre[pi++] = t;
+                }
+            std::memcpy(h_rows, b.logit_rows, sizeof(int32_t) * b.R);
+        }
+        int32_t* d_stage = reinterpret_cast<int32_t*>(base + L.meta);
+        BI_TRY_CUDA(cudaMemcpyAsync(d_stage, hm, meta_n * sizeof(int32_t), cudaMemcpyHostToDevice, s), "metadata copy");
+        BI_TRY_CUDA(cudaEventRecord(m->stage_done[slot], s), "cudaEventRecord");
+        d_meta = d_stage;
+    }
     const int32_t* d_req = d_meta;
     const int32_t* d_pos = d_meta + T;
     const int32_t* d_dec = d_meta + 2 * static_cast<size_t>(T);

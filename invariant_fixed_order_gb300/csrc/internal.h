@@ -94,7 +94,8 @@ cudaError_t launch_rope_kv_append(const float* qkv, const int32_t* tok_req, cons
 cudaError_t launch_argmax(const float* logits, int32_t* out, int32_t R, int32_t V, cudaStream_t s);
 
 // ---- logprobs and seeded sampling (k_logits.cu) ----
-cudaError_t launch_log_softmax(const float* logits, float* out, int32_t R, int32_t V, cudaStream_t s);
+size_t log_softmax_ws_bytes(int32_t R, int32_t V);
+cudaError_t launch_log_softmax(const float* logits, float* out, int32_t R, int32_t V, void* ws, cudaStream_t s);
 size_t sample_ws_bytes(int32_t R, int32_t V);
 cudaError_t launch_sample(const float* logits, const uint32_t* seeds, const int32_t* positions, const float* temps,
                           int32_t* tokens, int32_t R, int32_t V, void* ws, cudaStream_t s);

@@ -1,11 +1,13 @@
 // Logprobs and seeded sampling over rows of fp32 logits.
 //
 // "Mathematically equivalent is not bitwise equivalent": logprobs come from
-// one log_softmax kernel, whichever step (prefill rescoring or decode)
-// produced the logits.  The kernel runs one CTA per row and reduces the row
-// in one fixed order that depends on V alone ("The replacement kernels are
-// deliberately dull": a block per row, no cross-block reduction), so a row's
-// logprobs are bitwise the same whatever other rows share the launch.
+// one log_softmax kernel pair, whichever step (prefill rescoring or decode)
+// produced the logits.  A row is cut into segments of kSeg columns (a
+// function of V alone); each segment's max and sum of exponentials are
+// reduced in one fixed order, and the segments' partials are merged in
+// segment order, so a row's logprobs are bitwise the same whatever other rows
+// share the launch ("The replacement kernels are deliberately dull": no
+// reduction whose order follows the batch).
 //
 // "The weaker guarantees, which are usually enough": a request's draw depends
 // only on its own seed, its position and the column: Gumbel noise from
@@ -13,7 +15,11 @@
 // in float64, and the token is the argmax of logit / temperature + noise.
 // The argmax is a total order (a NaN beats every number, ties go to the
 // lowest index), so segments of a row may be searched by separate CTAs and
-// combined in any order without changing the winner.
+// combined in any order without changing the winner.  float64 is slow on
+// this GPU, so every score is first computed in fp32 with a proven error
+// bound; only the columns whose fp32 score lies within the bounds of their
+// segment's best fp32 score can be that segment's float64 winner, and only
+// they are scored in float64.  The token is the float64 argmax exactly.
 #include <math.h>
 
 #include "common.cuh"
@@ -21,39 +27,37 @@
 
 namespace bi {
 
-constexpr int kLsThreads = 512;
-constexpr int kLsWarps = kLsThreads / 32;
-constexpr int kSampleSeg = 4096;     // columns per sampling CTA
-constexpr int kSampleThreads = 256;
+constexpr int kSeg = 4096;            // columns per segment (log_softmax and sampling)
+constexpr int kSegThreads = 256;
+constexpr int kPerThread = kSeg / kSegThreads;  // 16 columns per thread: j = seg * kSeg + tid + 256 k
+
+int32_t logit_segments(int32_t V) { return (V + kSeg - 1) / kSeg; }
 
 // ---------------------------------------------------------------------------
 // log_softmax: lp_j = (x_j - m) - log(z), m = max_j x_j, z = sum_j exp(x_j - m)
-// Fixed order of z: thread t sums its columns serially in ascending order
-// (vector path: float4 q = t + 512 i, its 4 lanes in order; scalar path:
-// column t + 512 i), then an xor butterfly inside each warp, then the warps'
-// sums in warp order.
+// Pass 1 (one CTA per segment s): m_s = max over the segment, z_s = sum of
+// exp(x_j - m_s) in a fixed order: each thread's 16 columns in ascending k,
+// an xor butterfly inside each warp, the 8 warps' sums in warp order (a
+// segment without a finite maximum contributes z_s = 0).  Pass 2: every CTA
+// of the row merges the row's partials in segment order, m = max_s m_s,
+// z = sum_s z_s * exp(m_s - m), and writes its segment's logprobs.
 // ---------------------------------------------------------------------------
-template <bool kVec4>
-__global__ void __launch_bounds__(kLsThreads)
-log_softmax_kernel(const float* __restrict__ x, float* __restrict__ out, int32_t V) {
+__global__ void __launch_bounds__(kSegThreads)
+log_softmax_partial_kernel(const float* __restrict__ x, int32_t V, int32_t nseg, float2* __restrict__ part) {
     pdl_trigger();
     pdl_wait();
-    __shared__ float red[kLsWarps];
+    __shared__ float red[kSegThreads / 32];
     __shared__ float bc;
     const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
-    const float* xr = x + static_cast<int64_t>(blockIdx.x) * V;
-    float* orow = out + static_cast<int64_t>(blockIdx.x) * V;
-    const int32_t nq = kVec4 ? V / 4 : V;
-
-    // max (order-free; NaN never wins fmaxf, but reaches z below and makes the row NaN)
+    const int32_t seg = blockIdx.x, r = blockIdx.y;
+    const float* xr = x + static_cast<int64_t>(r) * V;
+    float v[kPerThread];
     float mx = -INFINITY;
-    for (int32_t q = tid; q < nq; q += kLsThreads) {
-        if constexpr (kVec4) {
-            const float4 v = reinterpret_cast<const float4*>(xr)[q];
-            mx = fmaxf(mx, fmaxf(fmaxf(v.x, v.y), fmaxf(v.z, v.w)));
-        } else {
-            mx = fmaxf(mx, xr[q]);
-        }
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+        const int32_t j = seg * kSeg + tid + kSegThreads * k;
+        v[k] = j < V ? xr[j] : -INFINITY;
+        mx = fmaxf(mx, v[k]);
     }
 #pragma unroll
     for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
@@ -61,23 +65,17 @@ log_softmax_kernel(const float* __restrict__ x, float* __restrict__ out, int32_t
     __syncthreads();
     if (tid == 0) {
         float m = red[0];
-        for (int w = 1; w < kLsWarps; ++w) m = fmaxf(m, red[w]);
+        for (int w = 1; w < kSegThreads / 32; ++w) m = fmaxf(m, red[w]);
         bc = m;
     }
     __syncthreads();
     const float m = bc;
-
-    // z in the fixed order above
     float z = 0.0f;
-    for (int32_t q = tid; q < nq; q += kLsThreads) {
-        if constexpr (kVec4) {
-            const float4 v = reinterpret_cast<const float4*>(xr)[q];
-            z = __fadd_rn(z, expf(__fsub_rn(v.x, m)));
-            z = __fadd_rn(z, expf(__fsub_rn(v.y, m)));
-            z = __fadd_rn(z, expf(__fsub_rn(v.z, m)));
-            z = __fadd_rn(z, expf(__fsub_rn(v.w, m)));
-        } else {
-            z = __fadd_rn(z, expf(__fsub_rn(xr[q], m)));
+    if (m != -INFINITY) {
+#pragma unroll
+        for (int k = 0; k < kPerThread; ++k) {
+            const int32_t j = seg * kSeg + tid + kSegThreads * k;
+            if (j < V) z = __fadd_rn(z, expf(__fsub_rn(v[k], m)));
         }
     }
 #pragma unroll
@@ -86,31 +84,53 @@ log_softmax_kernel(const float* __restrict__ x, float* __restrict__ out, int32_t
     if (lane == 0) red[warp] = z;
     __syncthreads();
     if (tid == 0) {
-        float s = red[0];
-        for (int w = 1; w < kLsWarps; ++w) s = __fadd_rn(s, red[w]);
-        bc = logf(s);
-    }
-    __syncthreads();
-    const float lz = bc;
-
-    for (int32_t q = tid; q < nq; q += kLsThreads) {
-        if constexpr (kVec4) {
-            const float4 v = reinterpret_cast<const float4*>(xr)[q];
-            reinterpret_cast<float4*>(orow)[q] =
-                make_float4(__fsub_rn(__fsub_rn(v.x, m), lz), __fsub_rn(__fsub_rn(v.y, m), lz),
-                            __fsub_rn(__fsub_rn(v.z, m), lz), __fsub_rn(__fsub_rn(v.w, m), lz));
-        } else {
-            orow[q] = __fsub_rn(__fsub_rn(xr[q], m), lz);
-        }
+        float t = red[0];
+        for (int w = 1; w < kSegThreads / 32; ++w) t = __fadd_rn(t, red[w]);
+        part[static_cast<int64_t>(r) * nseg + seg] = make_float2(m, t);
     }
 }
 
-cudaError_t launch_log_softmax(const float* logits, float* out, int32_t R, int32_t V, cudaStream_t s) {
+__global__ void __launch_bounds__(kSegThreads)
+log_softmax_write_kernel(const float* __restrict__ x, int32_t V, int32_t nseg, const float2* __restrict__ part,
+                         float* __restrict__ out) {
+    pdl_trigger();
+    pdl_wait();
+    __shared__ float2 ml;
+    const int tid = threadIdx.x;
+    const int32_t seg = blockIdx.x, r = blockIdx.y;
+    if (tid == 0) {
+        const float2* pr = part + static_cast<int64_t>(r) * nseg;
+        float m = pr[0].x;
+        for (int32_t q = 1; q < nseg; ++q) m = fmaxf(m, pr[q].x);
+        float z = 0.0f;
+        for (int32_t q = 0; q < nseg; ++q) z = __fadd_rn(z, __fmul_rn(pr[q].y, expf(__fsub_rn(pr[q].x, m))));
+        ml = make_float2(m, logf(z));
+    }
+    __syncthreads();
+    const float m = ml.x, lz = ml.y;
+    const float* xr = x + static_cast<int64_t>(r) * V;
+    float* orow = out + static_cast<int64_t>(r) * V;
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+        const int32_t j = seg * kSeg + tid + kSegThreads * k;
+        if (j < V) orow[j] = __fsub_rn(__fsub_rn(xr[j], m), lz);
+    }
+}
+
+size_t log_softmax_ws_bytes(int32_t R, int32_t V) {
+    if (R <= 0 || V <= 0) return 0;
+    return static_cast<size_t>(R) * logit_segments(V) * sizeof(float2) + 256;
+}
+
+cudaError_t launch_log_softmax(const float* logits, float* out, int32_t R, int32_t V, void* ws, cudaStream_t s) {
     if (R <= 0) return cudaSuccess;
-    const bool vec = (V % 4 == 0) && (reinterpret_cast<uintptr_t>(logits) & 15u) == 0 &&
-                     (reinterpret_cast<uintptr_t>(out) & 15u) == 0;
-    if (vec) return launch_pdl(log_softmax_kernel<true>, dim3(R), dim3(kLsThreads), 0, s, logits, out, V);
-    return launch_pdl(log_softmax_kernel<false>, dim3(R), dim3(kLsThreads), 0, s, logits, out, V);
+    const int32_t nseg = logit_segments(V);
+    float2* part = static_cast<float2*>(ws);
+    cudaError_t e = launch_pdl(log_softmax_partial_kernel, dim3(nseg, R), dim3(kSegThreads), 0, s, logits, V, nseg,
+                               part);
+    if (e != cudaSuccess) return e;
+    return launch_pdl(log_softmax_write_kernel, dim3(nseg, R), dim3(kSegThreads), 0, s, logits, V, nseg,
+                      static_cast<const float2*>(part), out);
 }
 
 // ---------------------------------------------------------------------------
@@ -147,36 +167,104 @@ __device__ __forceinline__ bool beats(double a, int32_t ia, double b, int32_t ib
     return a > b || (a == b && ia < ib);
 }
 
-// grid (segments, rows): the best (score, column) of one row's segment.
-__global__ void __launch_bounds__(kSampleThreads)
+// The float64 score of column j (the definition): x_j / t + g_j, or x_j for
+// a greedy row.
+__device__ __forceinline__ double score64(float x, double td, bool greedy, uint32_t h) {
+    if (greedy) return static_cast<double>(x);
+    const double u = (static_cast<double>(h) + 0.5) * 0x1p-32;  // exact: (0, 1)
+    return __dadd_rn(__ddiv_rn(static_cast<double>(x), td), -log(-log(u)));
+}
+
+// fp32 estimate of score64 and the bound on their difference.  With
+// u = (h + 0.5) / 2^32: w = -log(u) from u itself when u < 1/2 (w >= ln 2),
+// else from 1 - u = (2^32 - 1 - h + 0.5) / 2^32 through log1pf, so neither
+// loses digits to cancellation; the arguments carry a relative error below
+// 1e-7.  __logf is within 2^-21.41 absolute on [0.5, 2] and 3 ulp elsewhere,
+// log1pf within 1 ulp: |w32 - w| / w < 9e-6 and |g32 - g| < 1e-5 over the
+// whole range of g ([-3.2, 22.2]).  x * (1/t) and the sum add 3 * 2^-24 of
+// |x / t| and of |s|.  delta(s) = 1e-4 + 1e-6 (|s| + 48) covers all of it
+// with a margin of five or more (|x / t| <= |s| + 24).  A greedy row is exact
+// in fp32 (delta = 0).
+__device__ __forceinline__ float score32(float x, float rt, bool greedy, uint32_t h) {
+    if (greedy) return x;
+    float w;
+    if (h < 0x80000000u) {
+        const float u = __fmul_rn(__fadd_rn(static_cast<float>(h), 0.5f), 0x1p-32f);
+        w = -__logf(u);
+    } else {
+        const float v = __fmul_rn(__fadd_rn(static_cast<float>(0xffffffffu - h), 0.5f), 0x1p-32f);
+        w = -log1pf(-v);
+    }
+    return __fadd_rn(__fmul_rn(x, rt), -__logf(w));
+}
+__device__ __forceinline__ float score_bound(float s, bool greedy) {
+    return greedy ? 0.0f : __fadd_rn(1e-4f, __fmul_rn(1e-6f, __fadd_rn(fabsf(s), 48.0f)));
+}
+
+// grid (segments, rows): the float64 winner of one segment of a row.  Every
+// column's fp32 score is kept in registers; with M the segment's best fp32
+// score (reached at column k), the segment's float64 winner w satisfies
+// s32_w + delta_w >= s64_w >= s64_k >= M - delta(M), so only such columns
+// (and any non-finite score or maximum: a NaN beats every number, an
+// overflow leaves no bound) are scored in float64.  The row's winner is the
+// float64 winner of its own segment, so the merge below is exact.
+__global__ void __launch_bounds__(kSegThreads)
 sample_segment_kernel(const float* __restrict__ x, const uint32_t* __restrict__ seeds,
                       const int32_t* __restrict__ positions, const float* __restrict__ temps, int32_t V,
                       int32_t nseg, double* __restrict__ ws_score, int32_t* __restrict__ ws_idx) {
     pdl_trigger();
     pdl_wait();
-    __shared__ double s_sc[kSampleThreads / 32];
-    __shared__ int32_t s_ix[kSampleThreads / 32];
-    const int32_t seg = blockIdx.x, r = blockIdx.y;
+    __shared__ float red[kSegThreads / 32];
+    __shared__ float s_thr;
+    __shared__ double s_sc[kSegThreads / 32];
+    __shared__ int32_t s_ix[kSegThreads / 32];
     const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
+    const int32_t seg = blockIdx.x, r = blockIdx.y;
     const float* xr = x + static_cast<int64_t>(r) * V;
     const float t = temps[r];
     const bool greedy = !(t > 0.0f);  // temperature 0 (or not positive): the greedy argmax of the logits
+    const float rt = greedy ? 1.0f : __frcp_rn(t);
     const double td = static_cast<double>(t);
     const uint32_t seed = seeds[r], pos = static_cast<uint32_t>(positions[r]);
-    const int32_t j0 = seg * kSampleSeg, j1 = min(V, j0 + kSampleSeg);
+    float s32[kPerThread];
+    float mx = -INFINITY;
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+        const int32_t j = seg * kSeg + tid + kSegThreads * k;
+        s32[k] = -INFINITY;
+        if (j < V) {
+            const uint32_t h = greedy ? 0u : murmur3_pos_col(pos, static_cast<uint32_t>(j), seed);
+            s32[k] = score32(xr[j], rt, greedy, h);
+            mx = fmaxf(mx, s32[k]);
+        }
+    }
+#pragma unroll
+    for (int off = 16; off >= 1; off >>= 1) mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, off));
+    if (lane == 0) red[warp] = mx;
+    __syncthreads();
+    if (tid == 0) {
+        float m = red[0];
+        for (int w = 1; w < kSegThreads / 32; ++w) m = fmaxf(m, red[w]);
+        s_thr = isfinite(m) ? __fsub_rn(m, score_bound(m, greedy)) : -INFINITY;
+    }
+    __syncthreads();
+    const float thr = s_thr;
     double best = 0.0;
     int32_t bi = -1;
-    for (int32_t j = j0 + tid; j < j1; j += kSampleThreads) {
-        double sc = static_cast<double>(xr[j]);
-        if (!greedy) {
-            const uint32_t h = murmur3_pos_col(pos, static_cast<uint32_t>(j), seed);
-            const double u = (static_cast<double>(h) + 0.5) * 0x1p-32;  // exact: (0, 1)
-            const double g = -log(-log(u));
-            sc = __dadd_rn(__ddiv_rn(sc, td), g);
-        }
-        if (bi < 0 || beats(sc, j, best, bi)) {
-            best = sc;
-            bi = j;
+#pragma unroll
+    for (int k = 0; k < kPerThread; ++k) {
+        const int32_t j = seg * kSeg + tid + kSegThreads * k;
+        if (j < V) {
+            const bool cand = !isfinite(s32[k]) || !(thr > -INFINITY) ||
+                              __fadd_rn(s32[k], score_bound(s32[k], greedy)) >= thr;
+            if (cand) {
+                const uint32_t h = greedy ? 0u : murmur3_pos_col(pos, static_cast<uint32_t>(j), seed);
+                const double sc = score64(xr[j], td, greedy, h);
+                if (bi < 0 || beats(sc, j, best, bi)) {
+                    best = sc;
+                    bi = j;
+                }
+            }
         }
     }
 #pragma unroll
@@ -194,7 +282,7 @@ sample_segment_kernel(const float* __restrict__ x, const uint32_t* __restrict__ 
     }
     __syncthreads();
     if (tid == 0) {
-        for (int w = 1; w < kSampleThreads / 32; ++w)
+        for (int w = 1; w < kSegThreads / 32; ++w)
             if (s_ix[w] >= 0 && (bi < 0 || beats(s_sc[w], s_ix[w], best, bi))) {
                 best = s_sc[w];
                 bi = s_ix[w];
@@ -234,21 +322,20 @@ sample_merge_kernel(const double* __restrict__ ws_score, const int32_t* __restri
     if (lane == 0) tokens[r] = bi;
 }
 
-int32_t sample_segments(int32_t V) { return (V + kSampleSeg - 1) / kSampleSeg; }
-
 size_t sample_ws_bytes(int32_t R, int32_t V) {
     if (R <= 0 || V <= 0) return 0;
-    const size_t n = static_cast<size_t>(R) * sample_segments(V);
-    return n * sizeof(double) + n * sizeof(int32_t) + 256;
+    const size_t n = static_cast<size_t>(R) * logit_segments(V);
+    return n * (sizeof(double) + sizeof(int32_t)) + 256;
 }
 
 cudaError_t launch_sample(const float* logits, const uint32_t* seeds, const int32_t* positions, const float* temps,
                           int32_t* tokens, int32_t R, int32_t V, void* ws, cudaStream_t s) {
     if (R <= 0) return cudaSuccess;
-    const int32_t nseg = sample_segments(V);
+    const int32_t nseg = logit_segments(V);
+    const size_t n = static_cast<size_t>(R) * nseg;
     double* ws_score = static_cast<double*>(ws);
-    int32_t* ws_idx = reinterpret_cast<int32_t*>(ws_score + static_cast<size_t>(R) * nseg);
-    cudaError_t e = launch_pdl(sample_segment_kernel, dim3(nseg, R), dim3(kSampleThreads), 0, s, logits, seeds,
+    int32_t* ws_idx = reinterpret_cast<int32_t*>(ws_score + n);
+    cudaError_t e = launch_pdl(sample_segment_kernel, dim3(nseg, R), dim3(kSegThreads), 0, s, logits, seeds,
                                positions, temps, V, nseg, ws_score, ws_idx);
     if (e != cudaSuccess) return e;
     return launch_pdl(sample_merge_kernel, dim3(R), dim3(32), 0, s, static_cast<const double*>(ws_score),

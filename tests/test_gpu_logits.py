@@ -102,6 +102,19 @@ def test_sample_matches_oracle(bi, R, V, scale):
     assert np.mean(got == ref) >= 0.99
 
 
+def test_sample_extreme_temperatures_match_oracle(bi):
+    """The fp32 pre-pass prunes columns by a proven error bound; rows where |x / t| is large (low
+    temperature), where x / t overflows fp32 (no bound: every column is scored in float64) or where the
+    noise dominates (high temperature) must still give the float64 winner."""
+    R, V = 24, 128256
+    x = logits_rows(R, V, 30.0, 77)
+    seeds, pos, _ = sample_inputs(R, 78)
+    temps = np.array([0.05, 1e-30, 50.0, 0.5, 1e-3, 3.0] * 4, np.float32)
+    got = run_sample(bi, x, seeds, pos, temps)
+    ref = oracle.sample_gumbel_rows(x.numpy(), seeds, pos, temps)
+    assert np.array_equal(got, ref), np.nonzero(got != ref)
+
+
 def test_sample_rows_do_not_depend_on_the_batch(bi):
     R, V = 32, 128256
     x = logits_rows(R, V, 3.0, 11)
