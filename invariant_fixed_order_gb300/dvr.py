@@ -8,6 +8,11 @@ schedule (here: BI_INVARIANT mode, teacher-forced prefill of the window) in
 groups of requests; tokens that match are committed, the first mismatching
 one is replaced and the rest are discarded.
 
+"Per-Request Opt-In and Mixed Workloads": only requests marked
+is_deterministic are verified (their prompts are prefilled in invariant
+mode); the others share the fast path's batches and commit its tokens as they
+come, so the verifier's work follows the deterministic share of the traffic.
+
 Reading of the rollback step (the page says only that the system rolls back
 to the last verified consistent position): at the first mismatch the
 verifier's own token at that position is committed too, as in speculative
@@ -21,7 +26,7 @@ is only a matter of truncating the request's length.
 from __future__ import annotations
 
 import time
-from dataclasses import dataclass
+from dataclasses import dataclass, field
 
 import torch
 
@@ -38,6 +43,7 @@ class DvrStats:
     t_prefill: float = 0.0
     t_decode: float = 0.0
     t_verify: float = 0.0
+    verified: set = field(default_factory=set)  # request ids whose windows were verified
 
     @property
     def rollback_rate(self) -> float:
@@ -76,10 +82,14 @@ def dvr_generate(runner: Runner, reqs: list, n_new: int, window: int = 64, verif
     st = DvrStats()
     V = runner.eng.cfg.V
     t0 = _now()
-    # prompts: invariant prefill, in groups; the first token comes from the prefill
-    for group in _groups(reqs, verify_batch):
+    # prompts, in groups; the first token comes from the prefill: invariant for
+    # deterministic requests, the fast path for the others
+    det = [r for r in reqs if r.is_deterministic]
+    free = [r for r in reqs if not r.is_deterministic]
+    for group, mode in [(g, bi.INVARIANT) for g in _groups(det, verify_batch)] + \
+                       [(g, fast_mode) for g in _groups(free, verify_batch)]:
         items = [StepItem(r, len(r.prompt), "last") for r in group]
-        logits, tokens, sl = runner.step(items, mode=bi.INVARIANT)
+        logits, tokens, sl = runner.step(items, mode=mode)
         toks = tokens.cpu().tolist()
         for it, s in zip(items, sl):
             it.req.generated.append(int(toks[s][-1] if isinstance(toks[s], list) else toks[s.stop - 1]))
@@ -104,7 +114,7 @@ def dvr_generate(runner: Runner, reqs: list, n_new: int, window: int = 64, verif
         t1 = _now()
         st.t_decode += t1 - t0
         # ---- verify: invariant teacher-forced prefill of the window, in groups ----
-        for group in _groups(active, verify_batch):
+        for group in _groups([r for r in active if r.is_deterministic], verify_batch):
             items = []
             for r in group:
                 L = start[r.rid]
@@ -119,6 +129,7 @@ def dvr_generate(runner: Runner, reqs: list, n_new: int, window: int = 64, verif
                 cand = r.tokens[L:L + W].tolist()
                 k = next((j for j in range(W) if verified[j] != cand[j]), None)
                 st.windows += 1
+                st.verified.add(r.rid)
                 n_prompt = len(r.prompt)
                 if k is None:
                     r.n_cached = L + W - 1
@@ -128,6 +139,9 @@ def dvr_generate(runner: Runner, reqs: list, n_new: int, window: int = 64, verif
                     r.generated = r.generated[:L + k - n_prompt] + [int(verified[k])]
                     r.n_cached = L + k
         st.t_verify += _now() - t1
+        for r in active:
+            if not r.is_deterministic:
+                r.n_cached = len(r.tokens) - 1   # fast-path tokens are committed as decoded
         active = [r for r in active if len(r.generated) < n_new]
     for r in reqs:
         del r.generated[n_new:]

@@ -100,6 +100,10 @@ class Request:
     generated: list = field(default_factory=list)
     pages: list = field(default_factory=list)
     n_cached: int = 0
+    # "Per-Request Opt-In and Mixed Workloads": a deterministic request's
+    # committed tokens must not depend on the batch; the others may take the
+    # batch-variant fast path unverified
+    is_deterministic: bool = True
 
     @property
     def tokens(self) -> np.ndarray:

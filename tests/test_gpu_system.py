@@ -170,3 +170,37 @@ def test_decode_verify_rollback_commits_the_invariant_greedy_tokens(mods):
     assert st2.mismatched_windows >= n_prompts
     assert st2.rollback_rate > 0
     eng.close()
+
+
+def test_dvr_per_request_opt_in_and_tuning(mods):
+    """"Per-Request Opt-In and Mixed Workloads": only requests marked deterministic are verified; they
+    commit exactly the pure invariant greedy tokens while sharing fast-path batches with unverified
+    requests, and the verifier's work covers only them.  Window and verify-batch sizes are swept
+    ("The window size and verify batch size are tunable parameters")."""
+    bi, sched, dvr, Engine = mods
+    n_layers, n_prompts, n_new = (8, 16, 48)
+    cfg = LLAMA3_8B.with_layers(n_layers)
+    lens = [int(x) for x in synth.uniform_ints(n_prompts, 128, 768, 42 + 7)]
+    prompts = [synth.token_ids(n, cfg.V, 6000 + i) for i, n in enumerate(lens)]
+    max_pages = (768 + n_new + 64 + 15) // 16 + 1
+    eng = Engine(cfg, num_pages=n_prompts * max_pages + 64, max_pages=max_pages,
+                 max_T=16 * 768 + 64, max_B=n_prompts, max_R=16 * 64)
+    runner = sched.Runner(eng)
+    truth = greedy_batched(sched, runner, prompts, n_new, bi.INVARIANT)
+    det = {rid for rid in range(n_prompts) if rid % 2 == 0}
+    results = {}
+    for window, vb in ((16, 4), (32, 8), (48, 16)):
+        reqs = [sched.Request(rid, p, is_deterministic=rid in det) for rid, p in enumerate(prompts)]
+        st = dvr.dvr_generate(runner, reqs, n_new, window=window, verify_batch=vb)
+        eng.check()
+        for r in reqs:
+            assert len(r.generated) == n_new, r.rid
+            if r.is_deterministic:
+                assert r.generated == truth[r.rid], r.rid
+            runner.evict(r)
+        # every verified window belongs to a deterministic request
+        assert st.verified == det, st.verified
+        assert st.windows >= len(det) * (-(-(n_new - 1) // window))
+        results[(window, vb)] = st.as_dict()
+    print("dvr opt-in (8 layers, 16 prompts, half deterministic):", results, flush=True)
+    eng.close()
