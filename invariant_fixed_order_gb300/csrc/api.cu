@@ -515,12 +515,21 @@ extern "C" bi_status bi_forward_step(bi_model* m, const bi_batch* batch, const b
     BI_TRY_CUDA(launch_embed(m->embed, b.token_ids, x, T, c.V, c.d, dev_status, s, /*after_all=*/true), "embed");
     for (int l = 0; l < c.n_layers; ++l) {
         BI_TRY_CUDA(launch_rmsnorm(x, m->gamma_attn[l], y, T, c.d, c.eps, s), "rmsnorm");
-        BI_TRY(run_gemm(y, m->w_qkv[l], qkv, BI_F32, nullptr, BI_EP_NONE, T, nqkv, c.d, mode, gws, gws_bytes,
-                        dev_status, s, true));
-        BI_TRY_CUDA(launch_rope_kv_append(qkv, d_req, d_pos, m->rope_cos, m->rope_sin, c.max_pos, q, kv->k[l],
-                                          kv->v[l], b.page_table, b.max_pages, kv->num_pages, T, c.H, c.Hkv, c.Dh,
-                                          dev_status, s),
-                    "rope_kv_append");
+        if (gemm_can_fuse_rope(T, nqkv, c.d, mode, c.Dh)) {
+            // RoPE and the K/V append run in the QKV GEMM's epilogue (no fp32 qkv round trip)
+            const RopeFuse rf{d_req, d_pos, m->rope_cos, m->rope_sin, reinterpret_cast<uint16_t*>(q),
+                              reinterpret_cast<uint16_t*>(kv->k[l]), reinterpret_cast<uint16_t*>(kv->v[l]),
+                              b.page_table, c.max_pos, b.max_pages, kv->num_pages, c.H, c.Hkv, c.Dh};
+            BI_TRY(run_gemm(y, m->w_qkv[l], nullptr, BI_F32, nullptr, BI_EP_NONE, T, nqkv, c.d, mode, gws,
+                            gws_bytes, dev_status, s, true, nullptr, &rf));
+        } else {
+            BI_TRY(run_gemm(y, m->w_qkv[l], qkv, BI_F32, nullptr, BI_EP_NONE, T, nqkv, c.d, mode, gws, gws_bytes,
+                            dev_status, s, true));
+            BI_TRY_CUDA(launch_rope_kv_append(qkv, d_req, d_pos, m->rope_cos, m->rope_sin, c.max_pos, q, kv->k[l],
+                                              kv->v[l], b.page_table, b.max_pages, kv->num_pages, T, c.H, c.Hkv,
+                                              c.Dh, dev_status, s),
+                        "rope_kv_append");
+        }
         AttnGeom g{q, kv->k[l], kv->v[l], b.page_table, attn, 0, c.H, c.Hkv, c.Dh, b.max_pages, kv->num_pages,
                    scale, dev_status};
         if (nd > 0) {

@@ -76,6 +76,21 @@ struct ArgmaxFuse {
     unsigned int* counter;
 };
 
+// RoPE + KV append fused into the QKV GEMM's epilogue (the arithmetic of
+// rope_append_kernel on the fp32 accumulator instead of a stored fp32 qkv):
+// GEMM row t is token t; its columns are q heads, then k heads, then v heads.
+struct RopeFuse {
+    const int32_t* tok_req;
+    const int32_t* tok_pos;
+    const float* rc;
+    const float* rs;
+    uint16_t* q_out;
+    uint16_t* kc;
+    uint16_t* vc;
+    const int32_t* page_table;
+    int32_t max_pos, max_pages, num_pages, H, Hkv, Dh;
+};
+
 // rows: output rows; src_rows (device, optional): output row r normalises input row src_rows[r];
 // am (optional): initialise its keys[0, rows) and counter for a fused argmax that follows
 cudaError_t launch_rmsnorm(const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y, int64_t rows,
@@ -160,6 +175,9 @@ size_t gemm_ws_bytes(int64_t M, int32_t N, int32_t K, bi_mode mode);
 bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype,
                    const bi_bf16* residual, bi_epilogue ep, int64_t M, int32_t N, int32_t K,
                    bi_mode mode, void* ws, size_t ws_bytes, int32_t* status, cudaStream_t s,
-                   bool weights_settled = false, const ArgmaxFuse* am = nullptr);
+                   bool weights_settled = false, const ArgmaxFuse* am = nullptr,
+                   const RopeFuse* rope = nullptr);
+// whether run_gemm can fuse RoPE + KV append for this shape and mode
+bool gemm_can_fuse_rope(int64_t M, int32_t N, int32_t K, bi_mode mode, int32_t Dh);
 
 }  // namespace bi

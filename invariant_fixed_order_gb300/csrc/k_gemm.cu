@@ -92,6 +92,8 @@ struct GemmArgs {
     unsigned long long* am_keys;  // fused greedy argmax (fp32 output only): per-row winning key, or null
     int32_t* am_tokens;
     unsigned int* am_counter;
+    int32_t rope_on;       // 1: the epilogue applies RoPE and appends K/V (rope) instead of storing C
+    RopeFuse rope;
     int32_t* status;
 };
 
@@ -157,6 +159,108 @@ __device__ __forceinline__ void epilogue_group(const GemmArgs& args, int64_t row
             uint4* d4 = reinterpret_cast<uint4*>(dst + c * 16);
             d4[0] = make_uint4(ov[0], ov[1], ov[2], ov[3]);
             d4[1] = make_uint4(ov[4], ov[5], ov[6], ov[7]);
+        }
+    }
+}
+
+// Accumulator column (within a tile's TMEM buffer) of output column o of the
+// tile: in a pair, an MMA's columns 0-63 are the even CTA's W rows (output
+// columns g*64.. of the tile's first half), 64-127 the odd CTA's (second half).
+template <int BN, int CG>
+__device__ __forceinline__ uint32_t acc_col(int32_t o) {
+    if constexpr (CG == 2) {
+        const int32_t hi = o >= BN / 2 ? 1 : 0;
+        const int32_t oo = o - hi * (BN / 2);
+        return static_cast<uint32_t>((oo / 64) * 128 + hi * 64 + (oo % 64));
+    } else {
+        return static_cast<uint32_t>(o);
+    }
+}
+
+// RoPE + KV append of one GEMM row (token) over the heads of one tile, the
+// arithmetic of rope_append_kernel: rotate-half pairs (i, i + Dh/2) of q and
+// k heads as r0 = x0 c - x1 s, r1 = x1 c + x0 s in fp32, one bf16 rounding;
+// q to q_out, k and v to the token's page slot.  Every lane loads (the TMEM
+// loads are warp-wide); only rows < M store.
+template <int BN, int CG>
+__device__ __forceinline__ void rope_epilogue(const GemmArgs& args, uint32_t taddr, int64_t row, int32_t n_tile) {
+    const RopeFuse& rp = args.rope;
+    const int32_t Dh = rp.Dh, half = Dh / 2;
+    const bool live = row < args.M;
+    int32_t pos = 0, page = 0;
+    bool ok = false;
+    if (live) {
+        pos = rp.tok_pos[row];
+        const int32_t req = rp.tok_req[row];
+        ok = pos >= 0 && pos < rp.max_pos && (pos / BI_PAGE) < rp.max_pages;
+        if (ok) {
+            page = rp.page_table[static_cast<int64_t>(req) * rp.max_pages + pos / BI_PAGE];
+            if (page < 0 || page >= rp.num_pages) {
+                report(args.status, BI_DEV_BAD_PAGE);
+                ok = false;
+            }
+        } else {
+            report(args.status, BI_DEV_BAD_POSITION);
+        }
+    }
+    const int32_t slot = pos & (BI_PAGE - 1);
+    const float* crow = rp.rc + static_cast<int64_t>(ok ? pos : 0) * half;
+    const float* srow = rp.rs + static_cast<int64_t>(ok ? pos : 0) * half;
+#pragma unroll 1
+    for (int32_t hs = 0; hs < BN / Dh; ++hs) {
+        const int32_t head = (n_tile * BN + hs * Dh) / Dh;
+        const bool rot = head < rp.H + rp.Hkv;
+        uint16_t* dst = nullptr;
+        if (head < rp.H) {
+            dst = rp.q_out + (row * rp.H + head) * Dh;
+        } else if (ok) {
+            const bool is_k = head < rp.H + rp.Hkv;
+            const int32_t g = is_k ? head - rp.H : head - rp.H - rp.Hkv;
+            dst = (is_k ? rp.kc : rp.vc) + ((static_cast<int64_t>(page) * rp.Hkv + g) * BI_PAGE + slot) * Dh;
+        }
+        const uint32_t ta = acc_col<BN, CG>(hs * Dh), tb = acc_col<BN, CG>(hs * Dh + half);
+#pragma unroll 1
+        for (int32_t c = 0; c < half; c += 16) {
+            uint32_t ra[16], rb[16];
+            ptx::tmem_ld16(taddr + ta + c, ra);
+            ptx::tmem_ld16(taddr + tb + c, rb);
+            ptx::tmem_ld_wait();
+            if (live && dst != nullptr) {
+                float cs16[16], sn16[16];
+#pragma unroll
+                for (int v = 0; v < 4; ++v) {
+                    const float4 cv = ok ? reinterpret_cast<const float4*>(crow + c)[v] : make_float4(1.f, 1.f, 1.f, 1.f);
+                    const float4 sv = ok ? reinterpret_cast<const float4*>(srow + c)[v] : make_float4(0.f, 0.f, 0.f, 0.f);
+                    cs16[4 * v] = cv.x; cs16[4 * v + 1] = cv.y; cs16[4 * v + 2] = cv.z; cs16[4 * v + 3] = cv.w;
+                    sn16[4 * v] = sv.x; sn16[4 * v + 1] = sv.y; sn16[4 * v + 2] = sv.z; sn16[4 * v + 3] = sv.w;
+                }
+                uint32_t o0[8], o1[8];
+#pragma unroll
+                for (int e = 0; e < 16; e += 2) {
+                    float r0[2], r1[2];
+#pragma unroll
+                    for (int u = 0; u < 2; ++u) {
+                        const float x0 = __uint_as_float(ra[e + u]), x1 = __uint_as_float(rb[e + u]);
+                        if (rot) {
+                            const float cs = cs16[e + u];
+                            const float sn = sn16[e + u];
+                            r0[u] = __fsub_rn(__fmul_rn(x0, cs), __fmul_rn(x1, sn));
+                            r1[u] = __fadd_rn(__fmul_rn(x1, cs), __fmul_rn(x0, sn));
+                        } else {
+                            r0[u] = x0;
+                            r1[u] = x1;
+                        }
+                    }
+                    o0[e / 2] = pack_bf16x2(r0[0], r0[1]);
+                    o1[e / 2] = pack_bf16x2(r1[0], r1[1]);
+                }
+                uint4* d0 = reinterpret_cast<uint4*>(dst + c);
+                uint4* d1 = reinterpret_cast<uint4*>(dst + half + c);
+                d0[0] = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+                d0[1] = make_uint4(o0[4], o0[5], o0[6], o0[7]);
+                d1[0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+                d1[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
+            }
         }
     }
 }
@@ -407,17 +511,31 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         int32_t i = 0;
         for (int32_t tile = unit; tile < args.total_tiles; tile += nunits, ++i) {
             const int b = i & 1;
+            int32_t m_tile, n_tile;
+            tile_coords(tile, m_tile, n_tile);
+            const int64_t row = static_cast<int64_t>(m_tile) * kTileM + rank * kBM + q * 32 + lane;
+            if (args.rope_on && row < args.M) {
+                // the row's cos/sin table rows are read after the MMAs: fetch them into L1 meanwhile
+                const int32_t pos = args.rope.tok_pos[row];
+                if (pos >= 0 && pos < args.rope.max_pos) {
+                    const int32_t half = args.rope.Dh / 2;
+                    const char* cp = reinterpret_cast<const char*>(args.rope.rc + static_cast<int64_t>(pos) * half);
+                    const char* sp = reinterpret_cast<const char*>(args.rope.rs + static_cast<int64_t>(pos) * half);
+                    for (int32_t o = 0; o < half * 4; o += 128) {
+                        asm volatile("prefetch.global.L1 [%0];" ::"l"(cp + o));
+                        asm volatile("prefetch.global.L1 [%0];" ::"l"(sp + o));
+                    }
+                }
+            }
             const bool ready = ptx::mbar_wait_bounded(&acc_full[b], (static_cast<uint32_t>(i) >> 1) & 1u, abort_flag);
             if (!ready && !*abort_flag) report(args.status, BI_DEV_TIMEOUT_EPILOGUE);
             if (!__all_sync(0xffffffffu, ready && !*abort_flag)) break;
             ptx::tc_fence_after();
-            int32_t m_tile, n_tile;
-            tile_coords(tile, m_tile, n_tile);
-            const int64_t row = static_cast<int64_t>(m_tile) * kTileM + rank * kBM + q * 32 + lane;
             const uint32_t taddr = tmem + (static_cast<uint32_t>(q * 32) << 16) + static_cast<uint32_t>(b * BN);
             unsigned long long best = kArgmaxKeyNone;
+            if (args.rope_on) rope_epilogue<BN, CG>(args, taddr, row, n_tile);
 #pragma unroll 1
-            for (int j = 0; j < kChunks; ++j) {
+            for (int j = 0; j < (args.rope_on ? 0 : kChunks); ++j) {
                 uint32_t r[4][16];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) ptx::tmem_ld16(taddr + j * kEpi + c * 16, r[c]);
@@ -682,9 +800,15 @@ cudaError_t launch_tiles(const CUtensorMap& tmA, const CUtensorMap& tmW, const G
 
 }  // namespace
 
+bool gemm_can_fuse_rope(int64_t M, int32_t N, int32_t K, bi_mode mode, int32_t Dh) {
+    // tiles (128 or 256 columns, at multiples of their width) then hold whole heads
+    return M > 0 && N > 0 && gemm_plan(M, N, K, mode).splits == 1 && (Dh == 64 || Dh == 128);
+}
+
 bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype, const bi_bf16* residual,
                    bi_epilogue ep, int64_t M, int32_t N, int32_t K, bi_mode mode, void* ws, size_t ws_bytes,
-                   int32_t* status, cudaStream_t s, bool weights_settled, const ArgmaxFuse* am) {
+                   int32_t* status, cudaStream_t s, bool weights_settled, const ArgmaxFuse* am,
+                   const RopeFuse* rope) {
     if (M == 0) return BI_OK;
     const GemmPlan plan = gemm_plan(M, N, K, mode);
     const Layout L = choose_layout(M, N, K);
@@ -714,7 +838,13 @@ bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype
     a.kps = L.kps;
     a.w_early = weights_settled ? 1 : 0;
     a.status = status;
-    if (am != nullptr) {
+    if (rope != nullptr) {
+        if (!gemm_can_fuse_rope(M, N, K, mode, rope->Dh) || am != nullptr || ep != BI_EP_NONE ||
+            N != (rope->H + 2 * rope->Hkv) * rope->Dh)
+            return fail(BI_ERR_INVALID, "fused RoPE needs a pair-form QKV GEMM without split-K or other epilogue");
+        a.rope_on = 1;
+        a.rope = *rope;
+    } else if (am != nullptr) {
         if (plan.splits != 1 || c_dtype != BI_F32 || ep != BI_EP_NONE)
             return fail(BI_ERR_INVALID, "fused argmax needs an fp32 GEMM without epilogue or split-K");
         a.am_keys = am->keys;
