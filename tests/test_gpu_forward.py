@@ -283,8 +283,10 @@ def test_8b_layer_oracle_parity(mods, layer8b):
     w = {k: f32(v) for k, v in case.eng.logical[0].items()}
     gamma_final, w_lm = f32(case.eng.head["gamma_final"]), f32(case.eng.head["w_lm"])
     E = case.eng.head["embed"]
-    rows = [int(np.argmin(case.ctx)), 3, 17]
-    logits, hidden = case.step(rows, bi.INVARIANT)
+    rows = [int(np.argmin(case.ctx)), int(np.argmax(case.ctx)), 3, 17]
+    # the full 64-request step, as the bench runs it; sampled rows checked one by one
+    logits_all, hidden_all = case.step(range(len(case.ctx)), bi.INVARIANT)
+    logits, hidden = logits_all[rows], hidden_all[rows]
     for j, r in enumerate(rows):
         k, v = case.hist[r]
         x = f32(E[int(case.ids[r])])[None]

@@ -149,3 +149,91 @@ def test_sample_rejects_small_workspace(bi):
     with pytest.raises(bi.BIError) as e:
         bi._check(bi._lib.bi_sample(bi._p(x), bi._p(z), bi._p(z), bi._p(t), bi._p(z), 2, 100, None, 0, None))
     assert e.value.status == bi.BI_ERR_WORKSPACE
+
+
+# ---------------------------------------------------------------------------
+# Through the forward step
+# ---------------------------------------------------------------------------
+
+def tiny_engine(bi):
+    from invariant_fixed_order_gb300.config import TINY
+    from invariant_fixed_order_gb300.engine import Engine
+    return Engine(TINY, num_pages=256, max_pages=32, max_T=512, max_B=16, max_R=512)
+
+
+def test_prefill_rescore_logprobs_equal_generation_logprobs(bi):
+    """"Logprobs from a prefill rescore and logprobs from generation must come from the same kernel or
+    they will not match": a prompt decoded token by token, then rescored by one prefill of the whole
+    sequence, gives the same logprobs bit for bit at every generated position."""
+    from invariant_fixed_order_gb300 import synth
+    eng = tiny_engine(bi)
+    cfg = eng.cfg
+    prompt = synth.token_ids(37, cfg.V, 900)
+    pages = eng.pool.alloc(8)
+    table = np.zeros((1, 32), np.int32)
+    table[0, :8] = pages
+    logits, tok, _ = eng.step([37], [0], prompt, table, [36])
+    seq, gen_lp = list(prompt), []
+    for i in range(12):
+        seq.append(int(tok[0].item()))
+        gen_lp.append(bi.log_softmax(logits[:1].contiguous()).clone())
+        logits, tok, _ = eng.step([1], [len(seq) - 1], np.array(seq[-1:], np.int32), table, [0])
+    # rescore: one prefill of prompt + generated tokens into fresh pages, all positions
+    pages2 = eng.pool.alloc(8)
+    table2 = np.zeros((1, 32), np.int32)
+    table2[0, :8] = pages2
+    n = len(seq)
+    logits_all, _, _ = eng.step([n], [0], np.array(seq, np.int32), table2, list(range(n)))
+    resc = bi.log_softmax(logits_all)
+    for i, lp in enumerate(gen_lp):
+        row = 36 + i  # the position whose logits predicted generated token i
+        assert torch.equal(resc[row].view(torch.int32), lp[0].view(torch.int32)), i
+    eng.check()
+    eng.close()
+
+
+def test_seeded_sampling_is_batch_invariant_end_to_end(bi):
+    """Sampled continuations (seeded, temperature 0.8) are the same tokens whether a request decodes alone
+    or in a batch with others in any order: its logits are the same bits and its draws depend only on its
+    seed and positions."""
+    from invariant_fixed_order_gb300 import synth
+    eng = tiny_engine(bi)
+    cfg = eng.cfg
+    n_req, n_new = 6, 10
+    prompts = [synth.token_ids(5 + 7 * i, cfg.V, 950 + i) for i in range(n_req)]
+    seeds = np.array([11 + 1000 * i for i in range(n_req)], np.uint32)
+
+    def run(order):
+        tables = np.zeros((n_req, 32), np.int32)
+        for i in range(n_req):
+            tables[i, :4] = eng.pool.alloc(4)
+        seqs = {i: list(prompts[i]) for i in range(n_req)}
+        for i in order:   # prompts one by one, then sampled decode of the whole group in this order
+            logits, _, _ = eng.step([len(prompts[i])], [0], prompts[i], tables[i:i + 1], [len(prompts[i]) - 1])
+            t = bi.sample(logits, torch.tensor([int(seeds[i])], dtype=torch.int32).view(torch.int32).cuda(),
+                          torch.tensor([len(prompts[i])], dtype=torch.int32).cuda(),
+                          torch.tensor([0.8]).cuda())
+            seqs[i].append(int(t[0].item()))
+        for _ in range(n_new - 1):
+            ids = np.array([seqs[i][-1] for i in order], np.int32)
+            pos = [len(seqs[i]) - 1 for i in order]
+            logits, _, _ = eng.step([1] * len(order), pos, ids, tables[list(order)], list(range(len(order))))
+            t = bi.sample(logits, torch.from_numpy(seeds[list(order)].view(np.int32)).cuda(),
+                          torch.tensor([p + 1 for p in pos], dtype=torch.int32).cuda(),
+                          torch.full((len(order),), 0.8).cuda())
+            for k, i in enumerate(order):
+                seqs[i].append(int(t[k].item()))
+        for i in range(n_req):
+            eng.pool.free(tables[i, :4].tolist())
+        return {i: seqs[i][len(prompts[i]):] for i in order}
+
+    solo = {}
+    for i in range(n_req):
+        solo.update(run([i]))
+    rng = np.random.default_rng(4)
+    for _ in range(3):
+        order = [int(x) for x in rng.permutation(n_req)]
+        assert run(order) == solo
+    assert len({tuple(v) for v in solo.values()}) == n_req
+    eng.check()
+    eng.close()
