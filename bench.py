@@ -466,9 +466,10 @@ def run_ours(args):
         ms = replicas.max_over_ranks(ms, device=device)
     w.eng.check()
     value = world * B / (ms * 1e-3)
-    # embed, 2 rmsnorm, 4 GEMMs, rope, decode split, merge, final norm of the gathered rows, LM GEMM (greedy
-    # argmax fused into its epilogue)
-    launches_per_step = 12
+    # embed, 2 rmsnorm, 4 GEMMs (RoPE + K/V append inside the QKV GEMM's epilogue), decode split, merge, final
+    # norm of the gathered rows, LM GEMM (greedy argmax fused into its epilogue): the ncu launch list of this
+    # step shows the same 11
+    launches_per_step = 11
 
     # ---- e2e: host buffers in, tokens back, through the public API ----
     pin_ids = torch.from_numpy(w.ids).pin_memory()
