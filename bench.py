@@ -240,6 +240,25 @@ def gemm_roofline(w: GpuWorkload, steps: int, stream, hbm_peak: float) -> dict:
     return {"per_launch_bytes": tot_bytes / n, "per_launch_ms": tot_ms / n, "achieved": achieved, "per_gemm": per}
 
 
+def graph_times(w: GpuWorkload, steps: int, sizes) -> dict:
+    """The same decode step replayed from a CUDA graph (graphs.DecodeGraphs, one bucket per size, inputs
+    written once): device time per step with CUDA events on the replay stream."""
+    import torch
+    from invariant_fixed_order_gb300 import bi
+    from invariant_fixed_order_gb300.graphs import DecodeGraphs
+    sizes = sorted({b for b in sizes if b <= w.B})
+    g = DecodeGraphs(w.eng, int(max(w.ctx)), ladder=tuple(sizes), mode=bi.INVARIANT)
+    out = {}
+    for b in sizes:
+        g.step(w.ids[:b], [int(s) - 1 for s in w.ctx[:b]], w.table[:b], bucket=b)
+        graph = g.buckets[b][0]
+        ms = time_steps(graph.replay, max(steps, 10), 3, torch.cuda.current_stream())
+        out[f"bs{b}_us"] = round(ms * 1e3, 1)
+    torch.cuda.synchronize()
+    g.close()
+    return out
+
+
 def attention_time(w: GpuWorkload, steps: int, stream) -> dict:
     import torch
     from invariant_fixed_order_gb300 import bi
@@ -519,6 +538,7 @@ def run_ours(args):
     # ---- dominant kernel (GEMM) and attention, timed standalone with events ----
     g = gemm_roofline(w, args.steps, stream, hbm_peak)
     att = attention_time(w, args.steps, stream)
+    graphs = graph_times(w, args.steps, (1, 16, B))
     lops = logits_ops_time(w, args.steps, stream, hbm_peak)
     step_bytes = w.step_bytes(B)
     del w
@@ -545,6 +565,7 @@ def run_ours(args):
                          "per_launch_bytes": int(g["per_launch_bytes"])},
             "attention": att,
             "logits_ops": lops,
+            "graph_replay": graphs,
             "e2e": {"value": round(world * B / (e2e_ms * 1e-3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
                     "d2h_bytes_per_step": d2h},
             "gpu_launches": launches_per_step * args.steps,
