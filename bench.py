@@ -474,10 +474,10 @@ def run_ours(args):
         ms = replicas.max_over_ranks(ms, device=device)
     w.eng.check()
     value = world * B / (ms * 1e-3)
-    # embed, 2 rmsnorm, 4 GEMMs (RoPE + K/V append inside the QKV GEMM's epilogue), decode split, merge, final
-    # norm of the gathered rows, LM GEMM (greedy argmax fused into its epilogue): the ncu launch list of this
-    # step shows the same 11 (a graph replay launches the same kernels)
-    launches_per_step = 11
+    # embedding gather + first norm, FFN norm, 4 GEMMs (RoPE + K/V append inside the QKV GEMM's epilogue),
+    # decode split, merge, final norm of the gathered rows, LM GEMM (greedy argmax fused into its epilogue):
+    # 10 kernels per step (a graph replay launches the same kernels)
+    launches_per_step = 10
     # the same step launched eagerly through bi_forward_step, for comparison
     eager_ms = time_steps(lambda: w.step(B, bi.INVARIANT), max(args.steps, 10), 3, stream)
 

@@ -512,9 +512,12 @@ extern "C" bi_status bi_forward_step(bi_model* m, const bi_batch* batch, const b
     // The step's first kernel waits for all earlier work on the stream; every
     // later kernel of the step starts after it, so weights (never written
     // within a step) may be fetched before each kernel's dependency wait.
-    BI_TRY_CUDA(launch_embed(m->embed, b.token_ids, x, T, c.V, c.d, dev_status, s, /*after_all=*/true), "embed");
+    // the embedding gather and the first norm in one kernel (it also writes the residual stream x)
+    BI_TRY_CUDA(launch_embed_rmsnorm(m->embed, b.token_ids, c.V, m->gamma_attn[0], x, y, T, c.d, c.eps, dev_status,
+                                     s),
+                "embed + rmsnorm");
     for (int l = 0; l < c.n_layers; ++l) {
-        BI_TRY_CUDA(launch_rmsnorm(x, m->gamma_attn[l], y, T, c.d, c.eps, s), "rmsnorm");
+        if (l > 0) BI_TRY_CUDA(launch_rmsnorm(x, m->gamma_attn[l], y, T, c.d, c.eps, s), "rmsnorm");
         if (gemm_can_fuse_rope(T, nqkv, c.d, mode, c.Dh)) {
             // RoPE and the K/V append run in the QKV GEMM's epilogue (no fp32 qkv round trip)
             const RopeFuse rf{d_req, d_pos, m->rope_cos, m->rope_sin, reinterpret_cast<uint16_t*>(q),

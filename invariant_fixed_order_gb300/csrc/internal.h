@@ -99,6 +99,9 @@ cudaError_t launch_rmsnorm(const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y, i
 // after_all: launch without programmatic serialisation, so the kernel (and
 // every kernel chained after it) starts only once all earlier work on the
 // stream has finished.
+// x[t] = E[ids[t]] and y[t] = rmsnorm(x[t]) in one kernel (the norm's arithmetic), waiting for all earlier work
+cudaError_t launch_embed_rmsnorm(const bi_bf16* E, const int32_t* ids, int32_t V, const bi_bf16* gamma, bi_bf16* x,
+                                 bi_bf16* y, int32_t T, int32_t d, float eps, int32_t* status, cudaStream_t s);
 cudaError_t launch_embed(const bi_bf16* E, const int32_t* ids, bi_bf16* x, int32_t T, int32_t V,
                          int32_t d, int32_t* status, cudaStream_t s, bool after_all = false);
 cudaError_t launch_rope_kv_append(const float* qkv, const int32_t* tok_req, const int32_t* tok_pos,

@@ -20,10 +20,14 @@ namespace bi {
 // ---------------------------------------------------------------------------
 constexpr int kNormWarps = 4;
 
-template <int CPL>
+// kEmbed: the row is the embedding row E[ids[row]] (the step's first norm);
+// the warp also writes it to x_out, the residual stream (an id outside the
+// vocabulary reports BI_DEV_BAD_TOKEN and reads as zeros, as embed_kernel).
+template <int CPL, bool kEmbed>
 __global__ void __launch_bounds__(kNormWarps * 32)
 rmsnorm_kernel(const uint4* x, const uint4* __restrict__ gamma, uint4* y, int64_t rows, int32_t d8, float eps,
-               float fd, const int32_t* __restrict__ src_rows, unsigned long long* am_keys, unsigned int* am_counter) {
+               float fd, const int32_t* __restrict__ src_rows, unsigned long long* am_keys, unsigned int* am_counter,
+               const int32_t* __restrict__ ids, int32_t V, uint4* x_out, int32_t* status) {
     pdl_trigger();
     pdl_wait();
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kNormWarps + threadIdx.x / 32;
@@ -33,8 +37,17 @@ rmsnorm_kernel(const uint4* x, const uint4* __restrict__ gamma, uint4* y, int64_
         am_keys[row] = kArgmaxKeyNone;
         if (row == 0) *am_counter = 0u;
     }
-    const int64_t src = src_rows != nullptr ? static_cast<int64_t>(src_rows[row]) : row;
-    const uint4* xr = x + src * d8;
+    const uint4* xr;
+    bool zero = false;
+    if constexpr (kEmbed) {
+        const int32_t id = ids[row];
+        zero = !(id >= 0 && id < V);
+        if (zero && lane == 0) report(status, BI_DEV_BAD_TOKEN);
+        xr = x + static_cast<int64_t>(zero ? 0 : id) * d8;
+    } else {
+        const int64_t src = src_rows != nullptr ? static_cast<int64_t>(src_rows[row]) : row;
+        xr = x + src * d8;
+    }
     uint4* yr = y + row * d8;
     constexpr int kBlock = 32 * CPL;
     uint4 v[CPL], g[CPL];
@@ -43,7 +56,7 @@ rmsnorm_kernel(const uint4* x, const uint4* __restrict__ gamma, uint4* y, int64_
         for (int i = 0; i < CPL; ++i) {
             const int c = base + lane + 32 * i;
             if (c < d8) {
-                v[i] = xr[c];
+                v[i] = zero ? make_uint4(0, 0, 0, 0) : xr[c];
                 if (with_gamma) g[i] = gamma[c];
             }
         }
@@ -70,6 +83,13 @@ rmsnorm_kernel(const uint4* x, const uint4* __restrict__ gamma, uint4* y, int64_
     float ss = 0.0f;
     for (int base = 0; base < d8; base += kBlock) {
         load_block(base, cached);
+        if constexpr (kEmbed) {
+#pragma unroll
+            for (int i = 0; i < CPL; ++i) {
+                const int c = base + lane + 32 * i;
+                if (c < d8) x_out[row * d8 + c] = v[i];
+            }
+        }
 #pragma unroll
         for (int i = 0; i < CPL; ++i) {
             if (base + lane + 32 * i < d8) {
@@ -98,22 +118,37 @@ rmsnorm_kernel(const uint4* x, const uint4* __restrict__ gamma, uint4* y, int64_
     }
 }
 
-cudaError_t launch_rmsnorm(const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y, int64_t rows, int32_t d, float eps,
-                           cudaStream_t s, const int32_t* src_rows, const ArgmaxFuse* am) {
+template <bool kEmbed>
+static cudaError_t launch_rmsnorm_t(bool pdl, const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y, int64_t rows,
+                                    int32_t d, float eps, cudaStream_t s, const int32_t* src_rows,
+                                    const ArgmaxFuse* am, const int32_t* ids, int32_t V, bi_bf16* x_out,
+                                    int32_t* status) {
     if (rows <= 0) return cudaSuccess;
     const dim3 grid(static_cast<unsigned>((rows + kNormWarps - 1) / kNormWarps));
     const dim3 block(kNormWarps * 32);
     const int32_t d8 = d / 8;
     auto go = [&](auto kernel) {
-        return launch_pdl(kernel, grid, block, 0, s, reinterpret_cast<const uint4*>(x),
-                          reinterpret_cast<const uint4*>(gamma), reinterpret_cast<uint4*>(y), rows, d8, eps,
-                          static_cast<float>(d), src_rows, am ? am->keys : nullptr, am ? am->counter : nullptr);
+        return launch_k(pdl, kernel, grid, block, 0, s, reinterpret_cast<const uint4*>(x),
+                        reinterpret_cast<const uint4*>(gamma), reinterpret_cast<uint4*>(y), rows, d8, eps,
+                        static_cast<float>(d), src_rows, am ? am->keys : nullptr, am ? am->counter : nullptr, ids, V,
+                        reinterpret_cast<uint4*>(x_out), status);
     };
-    if (d8 <= 32) return go(rmsnorm_kernel<1>);
-    if (d8 <= 64) return go(rmsnorm_kernel<2>);
-    if (d8 <= 128) return go(rmsnorm_kernel<4>);
-    if (d8 <= 256) return go(rmsnorm_kernel<8>);
-    return go(rmsnorm_kernel<16>);
+    if (d8 <= 32) return go(rmsnorm_kernel<1, kEmbed>);
+    if (d8 <= 64) return go(rmsnorm_kernel<2, kEmbed>);
+    if (d8 <= 128) return go(rmsnorm_kernel<4, kEmbed>);
+    if (d8 <= 256) return go(rmsnorm_kernel<8, kEmbed>);
+    return go(rmsnorm_kernel<16, kEmbed>);
+}
+
+cudaError_t launch_rmsnorm(const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y, int64_t rows, int32_t d, float eps,
+                           cudaStream_t s, const int32_t* src_rows, const ArgmaxFuse* am) {
+    return launch_rmsnorm_t<false>(true, x, gamma, y, rows, d, eps, s, src_rows, am, nullptr, 0, nullptr, nullptr);
+}
+
+cudaError_t launch_embed_rmsnorm(const bi_bf16* E, const int32_t* ids, int32_t V, const bi_bf16* gamma, bi_bf16* x,
+                                 bi_bf16* y, int32_t T, int32_t d, float eps, int32_t* status, cudaStream_t s) {
+    // the step's first kernel: launched without programmatic serialisation, so it waits for all earlier work
+    return launch_rmsnorm_t<true>(false, E, gamma, y, T, d, eps, s, nullptr, nullptr, ids, V, x, status);
 }
 
 // ---------------------------------------------------------------------------
