@@ -604,7 +604,7 @@ decode_split_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_consta
 // Merge: grid (entries, H), DH/2 threads, each one dim pair; the fold runs
 // over splits in ascending order, its inputs fetched kMergeBatch splits at a
 // time so the loads of a batch are in flight together.
-constexpr int kMergeBatch = 8;
+constexpr int kMergeBatch = 32;
 
 template <int DH>
 __global__ void __launch_bounds__(DH / 2)
