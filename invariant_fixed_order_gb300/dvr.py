@@ -67,7 +67,8 @@ def _groups(seq, n):
 
 
 def _now():
-    torch.cuda.synchronize()
+    if torch.cuda.is_available():
+        torch.cuda.synchronize()  # device work counts towards the phase it was issued in
     return time.perf_counter()
 
 
