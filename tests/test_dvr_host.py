@@ -10,48 +10,9 @@ verify groups, the rollback and cache truncation, and the per-request opt-in.
 """
 import numpy as np
 import pytest
-import torch
 
 from invariant_fixed_order_gb300 import dvr, sched
-from invariant_fixed_order_gb300.engine import PagePool
-
-INVARIANT, VARIANT = 0, 1
-V = 997
-PAGE = 16
-
-
-def rule(history, mode):
-    h = 7
-    for t in history:
-        h = (h * 1000003 + int(t) + 1) % 2147483647
-    tok = h % V
-    if mode == VARIANT and (h >> 7) % 10 == 0:
-        tok = (tok + 1) % V
-    return tok
-
-
-class FakeEngine:
-    class cfg:
-        V = V
-
-    def __init__(self, num_pages=4096, max_pages=64):
-        self.max_pages = max_pages
-        self.pool = PagePool(num_pages, seed=0)
-        self.cache = {}
-
-    def step(self, q_len, pos0, ids, table, rows, mode=INVARIANT):
-        out, t = [], 0
-        for i, (n, p0) in enumerate(zip(q_len, pos0)):
-            for j in range(n):
-                p = p0 + j
-                self.cache[(int(table[i][p // PAGE]), p % PAGE)] = int(ids[t + j])
-            for j in range(n):
-                p = p0 + j
-                hist = [self.cache[(int(table[i][q // PAGE]), q % PAGE)] for q in range(p + 1)]
-                out.append(rule(hist, mode))
-            t += n
-        tokens = torch.tensor([out[r] for r in rows], dtype=torch.int32)
-        return None, tokens, None
+from tests.standin import INVARIANT, VARIANT, V, StandInEngine as FakeEngine, rule
 
 
 def greedy(prompt, n_new, mode):
