@@ -800,13 +800,13 @@ template <int G, int DH, int RING>
 static cudaError_t launch_decode_ring(const AttnGeom& g, const EntryMap& em, int32_t n, int32_t max_splits,
                                       int32_t chunk2, float* ws_o, float* ws_ml, bool early_kv, cudaStream_t s) {
     const size_t smem = sizeof(AttnSmem<G, DH, 1, RING>);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<G, DH, RING>,
-                                             cudaFuncAttributeMaxDynamicSharedMemorySize, static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [smem] {
+        attr_err = cudaFuncSetAttribute(decode_split_kernel<G, DH, RING>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(smem));
+    });
+    if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap tmK, tmV;
     if (!encode_kv_map(&tmK, g.kc, g.num_pages, g.Hkv, DH) || !encode_kv_map(&tmV, g.vc, g.num_pages, g.Hkv, DH))
         return cudaErrorInvalidValue;
@@ -836,13 +836,13 @@ template <int G, int DH>
 static cudaError_t launch_prefill_t(const AttnGeom& g, const EntryMap& em, int32_t n, cudaStream_t s) {
     constexpr int NT = prefill_tokens<G>();
     const size_t smem = sizeof(AttnSmem<G, DH, NT>);
-    static bool attr_set = false;
-    if (!attr_set) {
-        cudaError_t e = cudaFuncSetAttribute(prefill_kernel<G, DH, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                             static_cast<int>(smem));
-        if (e != cudaSuccess) return e;
-        attr_set = true;
-    }
+    static std::once_flag once;
+    static cudaError_t attr_err = cudaSuccess;
+    std::call_once(once, [smem] {
+        attr_err = cudaFuncSetAttribute(prefill_kernel<G, DH, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                        static_cast<int>(smem));
+    });
+    if (attr_err != cudaSuccess) return attr_err;
     CUtensorMap tmK, tmV;
     if (!encode_kv_map(&tmK, g.kc, g.num_pages, g.Hkv, DH) || !encode_kv_map(&tmV, g.vc, g.num_pages, g.Hkv, DH))
         return cudaErrorInvalidValue;

@@ -6,8 +6,9 @@ bench's CPU-baseline leg may import this package.  The product path
 product package: the two share no code.
 
 The C source is the plain definition of a Llama-style decoder step in binary32
-with no fused multiply-add; see ``oracle.h`` for the page and section each
-function follows ("Lockstep"; "Batch invariance and reproducible inference").
+with no fused multiply-add, plus logprobs and seeded Gumbel-max sampling in
+float64; see ``oracle.h`` for the page and section each function follows
+("Lockstep"; "Batch invariance and reproducible inference").
 All tensors cross this wrapper as float32 numpy arrays; bf16 tensors are passed
 as float32 arrays holding bf16-representable values.
 """

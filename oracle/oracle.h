@@ -8,7 +8,8 @@
  *
  * Every function is the plain definition of one step of a Llama-style decoder
  * step, written as serial loops in binary32 (`float`), compiled with
- * -ffp-contract=off so that no multiply-add is fused.  Values that the GPU
+ * -ffp-contract=off so that no multiply-add is fused; logprobs and the seeded
+ * sampler are written in float64 (the sampler's decision is the pages').  Values that the GPU
  * stores in bf16 are rounded to bf16 (round to nearest even) at exactly those
  * storage points when `round_bf16` is non-zero; with it zero the oracle is a
  * pure fp32 computation (used by the float64 brute-force pin).
