@@ -394,8 +394,9 @@ class OracleSample:
             t_total += time.perf_counter() - t0
             done += 1
         return {"value": done / t_total, "unit": "tokens/s", "cores": oracle.num_threads(), "kind": "oracle",
-                "sample": f"{done} decode steps (1 layer + LM head + argmax) of requests drawn in order from the "
-                          f"{self.B}-request batch, {t_total:.1f} s of oracle time"}
+                "sample": f"{done} single-request decode steps (1 layer + LM head + argmax) of requests drawn in "
+                          f"order from the {self.B}-request batch, {t_total:.1f} s of oracle time; ms_per_step is "
+                          f"a whole {self.B}-request step at that rate"}
 
 
 # ---------------------------------------------------------------------------
@@ -419,7 +420,7 @@ def run_reference(args):
             "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f32", "data": "synthetic",
             "config": run_config(args.batch, args.gpus),
             "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": rates[0]["cores"], "kind": "oracle",
-                             "sample": rates[0]["sample"] + " per step"},
+                             "sample": rates[0]["sample"] + " (one timed step)"},
             "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
     print(json.dumps(line), flush=True)
 
