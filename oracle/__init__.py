@@ -64,49 +64,54 @@ class _LayerW(ctypes.Structure):
                 ("w_gate", _FP), ("w_up", _FP), ("w_down", _FP)]
 
 
+def bind(path: str) -> ctypes.CDLL:
+    """Load a compiled oracle library from ``path`` and declare its functions'
+    argument types (the functions of oracle.h)."""
+    L = ctypes.CDLL(path)
+    f32p, i32p, i64p = _FP, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)
+    i64, i32 = ctypes.c_int64, ctypes.c_int32
+    L.orc_bf16_round.restype = ctypes.c_float
+    L.orc_bf16_round.argtypes = [ctypes.c_float]
+    L.orc_bf16_round_array.argtypes = [f32p, f32p, i64]
+    L.orc_sum_serial.restype = ctypes.c_float
+    L.orc_sum_serial.argtypes = [f32p, i64]
+    L.orc_sum_pairwise.restype = ctypes.c_float
+    L.orc_sum_pairwise.argtypes = [f32p, i64]
+    L.orc_rmsnorm.argtypes = [f32p, f32p, f32p, i64, i32, ctypes.c_float, ctypes.c_int]
+    L.orc_matmul.argtypes = [f32p, f32p, f32p, i64, i32, i32]
+    L.orc_softmax.argtypes = [f32p, f32p, i32]
+    L.orc_swiglu.argtypes = [f32p, f32p, f32p, i64, ctypes.c_int]
+    L.orc_argmax.restype = i32
+    L.orc_argmax.argtypes = [f32p, i32]
+    L.orc_argmax_rows.argtypes = [f32p, i32p, i64, i32]
+    f64p, u32p, u8p = (ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_uint32),
+                       ctypes.POINTER(ctypes.c_uint8))
+    L.orc_log_softmax_rows.argtypes = [f32p, f64p, i64, i32]
+    L.orc_murmur3_32.restype = ctypes.c_uint32
+    L.orc_murmur3_32.argtypes = [u8p, i32, ctypes.c_uint32]
+    L.orc_sample_gumbel.restype = ctypes.c_int32
+    L.orc_sample_gumbel.argtypes = [f32p, i32, ctypes.c_uint32, i32, ctypes.c_float]
+    L.orc_sample_gumbel_rows.argtypes = [f32p, u32p, i32p, f32p, i32p, i64, i32]
+    L.orc_rope_table.argtypes = [f32p, f32p, i32, i32, ctypes.c_double]
+    L.orc_rope_apply.argtypes = [f32p, i32p, i64, i32, f32p, f32p, i32]
+    L.orc_attention_head.argtypes = [f32p, f32p, f32p, i32, i64, i32, ctypes.c_float, f32p]
+    L.orc_attention_head_split.argtypes = [f32p, f32p, f32p, i32, i64, i32,
+                                           ctypes.c_float, i32, f32p]
+    L.orc_layer_forward.argtypes = [ctypes.POINTER(_Dims), ctypes.POINTER(_LayerW), i32,
+                                    i32p, i32p, i64p, f32p, f32p, f32p, f32p, f32p]
+    L.orc_lm_head.argtypes = [ctypes.POINTER(_Dims), f32p, f32p, i32, f32p, i32p, i32,
+                              f32p, i32p]
+    L.orc_embed.argtypes = [f32p, i32, i32, i32p, i64, f32p]
+    L.orc_num_threads.restype = ctypes.c_int
+    L.orc_set_num_threads.argtypes = [ctypes.c_int]
+    return L
+
+
 def lib():
     global _lib
     with _lock:
         if _lib is None:
-            path = build()
-            L = ctypes.CDLL(path)
-            f32p, i32p, i64p = _FP, ctypes.POINTER(ctypes.c_int32), ctypes.POINTER(ctypes.c_int64)
-            i64, i32 = ctypes.c_int64, ctypes.c_int32
-            L.orc_bf16_round.restype = ctypes.c_float
-            L.orc_bf16_round.argtypes = [ctypes.c_float]
-            L.orc_bf16_round_array.argtypes = [f32p, f32p, i64]
-            L.orc_sum_serial.restype = ctypes.c_float
-            L.orc_sum_serial.argtypes = [f32p, i64]
-            L.orc_sum_pairwise.restype = ctypes.c_float
-            L.orc_sum_pairwise.argtypes = [f32p, i64]
-            L.orc_rmsnorm.argtypes = [f32p, f32p, f32p, i64, i32, ctypes.c_float, ctypes.c_int]
-            L.orc_matmul.argtypes = [f32p, f32p, f32p, i64, i32, i32]
-            L.orc_softmax.argtypes = [f32p, f32p, i32]
-            L.orc_swiglu.argtypes = [f32p, f32p, f32p, i64, ctypes.c_int]
-            L.orc_argmax.restype = i32
-            L.orc_argmax.argtypes = [f32p, i32]
-            L.orc_argmax_rows.argtypes = [f32p, i32p, i64, i32]
-            f64p, u32p, u8p = (ctypes.POINTER(ctypes.c_double), ctypes.POINTER(ctypes.c_uint32),
-                               ctypes.POINTER(ctypes.c_uint8))
-            L.orc_log_softmax_rows.argtypes = [f32p, f64p, i64, i32]
-            L.orc_murmur3_32.restype = ctypes.c_uint32
-            L.orc_murmur3_32.argtypes = [u8p, i32, ctypes.c_uint32]
-            L.orc_sample_gumbel.restype = ctypes.c_int32
-            L.orc_sample_gumbel.argtypes = [f32p, i32, ctypes.c_uint32, i32, ctypes.c_float]
-            L.orc_sample_gumbel_rows.argtypes = [f32p, u32p, i32p, f32p, i32p, i64, i32]
-            L.orc_rope_table.argtypes = [f32p, f32p, i32, i32, ctypes.c_double]
-            L.orc_rope_apply.argtypes = [f32p, i32p, i64, i32, f32p, f32p, i32]
-            L.orc_attention_head.argtypes = [f32p, f32p, f32p, i32, i64, i32, ctypes.c_float, f32p]
-            L.orc_attention_head_split.argtypes = [f32p, f32p, f32p, i32, i64, i32,
-                                                   ctypes.c_float, i32, f32p]
-            L.orc_layer_forward.argtypes = [ctypes.POINTER(_Dims), ctypes.POINTER(_LayerW), i32,
-                                            i32p, i32p, i64p, f32p, f32p, f32p, f32p, f32p]
-            L.orc_lm_head.argtypes = [ctypes.POINTER(_Dims), f32p, f32p, i32, f32p, i32p, i32,
-                                      f32p, i32p]
-            L.orc_embed.argtypes = [f32p, i32, i32, i32p, i64, f32p]
-            L.orc_num_threads.restype = ctypes.c_int
-            L.orc_set_num_threads.argtypes = [ctypes.c_int]
-            _lib = L
+            _lib = bind(build())
     return _lib
 
 

@@ -75,7 +75,10 @@ uint32_t orc_murmur3_32(const uint8_t* key, int32_t len, uint32_t seed);
  *   h_j = murmur3_32(le32(pos) || le32(j), seed), u_j = (h_j + 0.5) / 2^32,
  *   g_j = -log(-log(u_j)), token = argmax_j (x_j / t + g_j)
  * ties to the lowest index, a NaN score larger than every number.  A row with
- * t <= 0 (or NaN) is decoded greedily (orc_argmax). */
+ * t <= 0 (or NaN) is decoded greedily (orc_argmax).
+ * Parity unpinned in one detail: the byte layout of the hash key (position
+ * first, then column) is a reading.  The pages name the hash's inputs but
+ * print no hash or token that would fix their order. */
 int32_t orc_sample_gumbel(const float* x, int32_t n, uint32_t seed, int32_t pos, float t);
 int orc_sample_gumbel_rows(const float* x, const uint32_t* seeds, const int32_t* pos, const float* t,
                            int32_t* out, int64_t rows, int32_t n);

@@ -138,6 +138,19 @@ def test_softmax_rows_sum_to_one(n):
     np.testing.assert_allclose(p, scipy.special.softmax(s.astype(np.float64)), rtol=1e-5, atol=1e-9)
 
 
+def test_softmax_is_shift_invariant_beyond_the_exp_range():
+    """softmax(s + c) = softmax(s): with s on a 2^-10 grid the shift by 512 is exact in binary32, so the
+    values must agree bit for bit although e^512 is far beyond binary32's range."""
+    rng = np.random.default_rng(15)
+    s = (np.round(rng.standard_normal(300) * 4 * 1024) / 1024).astype(np.float32)
+    p = oracle.softmax(s)
+    assert np.array_equal(oracle.softmax(s + np.float32(512.0)), p)
+    assert np.array_equal(oracle.softmax(s - np.float32(512.0)), p)
+    # two logits 100 apart: the larger takes all the mass to binary32 precision
+    p2 = oracle.softmax(np.float32([0.0, 100.0]))
+    assert p2[1] == np.float32(1.0) and 0.0 <= p2[0] < 1e-40
+
+
 @pytest.mark.parametrize("n", [1, 3, 256, 700])
 def test_attention_identical_keys_returns_mean_of_v(n):
     rng = np.random.default_rng(6)
@@ -415,6 +428,13 @@ def test_log_softmax_two_columns_closed_form():
     d = float(b) - float(a)
     assert abs(lp[0] - (-np.log1p(np.exp(d)))) < 1e-14
     assert abs(lp[1] - (d - np.log1p(np.exp(d)))) < 1e-14
+
+
+def test_log_softmax_beyond_the_float64_exp_range():
+    """Logits 1000 apart: e^1000 overflows float64, but the logprobs are [-1000 - log1p(e^-1000), -log1p(...)]
+    = [-1000, 0] exactly (e^-1000 underflows to 0)."""
+    lp = oracle.log_softmax_rows(np.float32([[0.0, 1000.0], [1000.0, 0.0], [-1000.0, 1000.0]]))
+    assert np.array_equal(lp, [[-1000.0, 0.0], [0.0, -1000.0], [-2000.0, 0.0]])
 
 
 def test_log_softmax_matches_library_and_invariants():
