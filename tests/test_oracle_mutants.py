@@ -8,11 +8,11 @@ against it, and at least one pin must fail.  A mutant that survives means a
 mistake of that kind could sit in the oracle unnoticed.
 """
 import importlib
+import importlib.util
 import inspect
 import os
 import shutil
 import subprocess
-
 
 import oracle
 
@@ -90,6 +90,27 @@ UNPINNED = [
 ]
 
 
+# Mistakes planted in the oracle's Python wrapper (argument marshalling): the
+# mutated copy of the package reuses the unmutated compiled library.
+PY_MUTANTS = [
+    ("history rows shifted by one position",
+     "k_pool[row0[i]:row0[i] + pos0[i]] = k_hist[i][:pos0[i]]",
+     "k_pool[row0[i]:row0[i] + pos0[i]] = np.roll(k_hist[i][:pos0[i]], 1, axis=0)"),
+    ("pool offsets from query lengths, not context lengths",
+     "row0[1:] = np.cumsum(rows)[:-1]", "row0[1:] = np.cumsum(q_lens)[:-1]"),
+    ("returned caches start one row late",
+     "k_new = [k_pool[row0[i]:row0[i] + rows[i]] for i in range(B)]",
+     "k_new = [k_pool[row0[i] + 1:row0[i] + rows[i] + 1] for i in range(B)]"),
+    ("default attention scale 1/Dh",
+     "scale = np.float32(1.0) / np.sqrt(np.float32(Dh)) if scale is None else scale\n    out = np.empty(Dh, np.float32)\n"
+     "    _check(lib().orc_attention_head(",
+     "scale = np.float32(1.0) / np.float32(Dh) if scale is None else scale\n    out = np.empty(Dh, np.float32)\n"
+     "    _check(lib().orc_attention_head("),
+    ("rope table one position short", "n_pos = int(pos.max()) + 1 if pos.size else 1",
+     "n_pos = int(pos.max()) if pos.size else 1"),
+]
+
+
 def _pin_cases():
     """Every (pin, arguments) of test_oracle_pins, parametrisations expanded."""
     mod = importlib.import_module("tests.test_oracle_pins")
@@ -127,6 +148,15 @@ def _compile(tmp, text, repl):
     return so
 
 
+def _killed(cases) -> bool:
+    for _, fn, kw in cases:
+        try:
+            fn(**kw)
+        except Exception:  # an assertion, or the oracle reporting an error
+            return True
+    return False
+
+
 def _survivors(mutants, tmp_path, monkeypatch):
     cases = _pin_cases()
     assert len(cases) > 40
@@ -134,17 +164,26 @@ def _survivors(mutants, tmp_path, monkeypatch):
     for i, (name, text, repl) in enumerate(mutants):
         so = _compile(str(tmp_path / str(i)), text, repl)
         monkeypatch.setattr(oracle, "_lib", oracle.bind(so))
-        killed = None
-        for pin, fn, kw in cases:
-            try:
-                fn(**kw)
-            except Exception:  # an assertion, or the oracle reporting an error
-                killed = pin
-                break
-        if killed is None:
+        if not _killed(cases):
             survivors.append(name)
     monkeypatch.undo()
     return survivors
+
+
+def _py_mutant(tmp, name, text, repl):
+    """A copy of the oracle package with one wrapper mistake, bound to the unmutated library."""
+    src = open(os.path.join(ROOT, "oracle", "__init__.py")).read()
+    assert src.count(text) == 1, text
+    d = os.path.join(tmp, "pkg")
+    os.makedirs(d, exist_ok=True)
+    path = os.path.join(d, "__init__.py")
+    with open(path, "w") as fh:
+        fh.write(src.replace(text, repl))
+    spec = importlib.util.spec_from_file_location(f"oracle_mutant_{abs(hash(name))}", path)
+    mod = importlib.util.module_from_spec(spec)
+    spec.loader.exec_module(mod)
+    mod._lib = mod.bind(oracle.build())  # its own handle: argument types name the copy's structures
+    return mod
 
 
 def test_unmutated_oracle_passes_every_pin():
@@ -153,6 +192,9 @@ def test_unmutated_oracle_passes_every_pin():
 
 
 def test_every_mutant_fails_a_pin(tmp_path, monkeypatch):
+    # control: an unchanged copy built the way the mutants are passes every pin
+    text = MUTANTS[0][1]
+    assert _survivors([("copy", text, text)], tmp_path / "copy", monkeypatch) == ["copy"]
     survivors = _survivors(MUTANTS, tmp_path, monkeypatch)
     assert not survivors, f"mutants no pin catches: {survivors}"
 
@@ -160,3 +202,19 @@ def test_every_mutant_fails_a_pin(tmp_path, monkeypatch):
 def test_unpinned_readings_are_still_unpinned(tmp_path, monkeypatch):
     """If a pin comes to catch one of these, move it to MUTANTS and drop its "parity unpinned" notes."""
     assert _survivors(UNPINNED, tmp_path, monkeypatch) == [m[0] for m in UNPINNED]
+
+
+def test_every_wrapper_mutant_fails_a_pin(tmp_path, monkeypatch):
+    pins = importlib.import_module("tests.test_oracle_pins")
+    cases = _pin_cases()
+    text = PY_MUTANTS[0][1]
+    monkeypatch.setattr(pins, "oracle", _py_mutant(str(tmp_path / "copy"), "copy", text, text))
+    assert not _killed(cases), "an unmutated copy of the wrapper fails a pin"
+    monkeypatch.undo()
+    survivors = []
+    for i, (name, text, repl) in enumerate(PY_MUTANTS):
+        monkeypatch.setattr(pins, "oracle", _py_mutant(str(tmp_path / str(i)), name, text, repl))
+        if not _killed(cases):
+            survivors.append(name)
+        monkeypatch.undo()
+    assert not survivors, f"wrapper mutants no pin catches: {survivors}"
