@@ -65,11 +65,15 @@ def attention_flops(cfg: ModelConfig, q_positions) -> int:
 def decode_layer_bytes(cfg: ModelConfig, seq_lens) -> int:
     """Algorithmic HBM bytes of one layer of one decode step over a batch whose
     requests have the given context lengths (the current token included):
-    weights once, each request's KV once, activations (residual in/out, qkv,
-    attention, ffn hidden) per token."""
+    weights once, each request's KV once, and per token the activations the
+    step stores and reads back: the residual stream and the two norm outputs
+    (six d-vectors), the rotated q and the appended k and v (written once by
+    the QKV GEMM's epilogue; the fp32 projection is never stored), q read by
+    attention, the attention output written and read, the SwiGLU output
+    written and read."""
     B = len(seq_lens)
     kv = sum(kv_bytes_per_layer(cfg, int(s)) for s in seq_lens)
-    act = B * (cfg.d * BF16 * 6 + cfg.qkv_dim * F32 * 2 + cfg.H * cfg.Dh * BF16 * 3
+    act = B * (cfg.d * BF16 * 6 + cfg.qkv_dim * BF16 + cfg.H * cfg.Dh * BF16 * 3
                + cfg.F * BF16 * 2)
     return layer_weight_bytes(cfg) + kv + act
 
