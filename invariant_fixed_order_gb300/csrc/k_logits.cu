@@ -178,10 +178,11 @@ __device__ __forceinline__ double score64(float x, double td, bool greedy, uint3
 // fp32 estimate of score64 and the bound on their difference.  With
 // u = (h + 0.5) / 2^32: w = -log(u) from u itself when u < 1/2 (w >= ln 2),
 // else from 1 - u = (2^32 - 1 - h + 0.5) / 2^32 through log1pf, so neither
-// loses digits to cancellation; the arguments carry a relative error below
-// 1e-7.  __logf is within 2^-21.41 absolute on [0.5, 2] and 3 ulp elsewhere,
-// log1pf within 1 ulp: |w32 - w| / w < 9e-6 and |g32 - g| < 1e-5 over the
-// whole range of g ([-3.2, 22.2]).  x * (1/t) and the sum add 3 * 2^-24 of
+// loses digits to cancellation; the arguments carry a relative error of at
+// most 2^-23 (two roundings).  __logf is within 2^-21.41 absolute on [0.5, 2]
+// and 3 ulp elsewhere, log1pf within 1 ulp: |w32 - w| / w < 9e-6 and
+// |g32 - g| < 1e-5 over the whole range of g ([-3.14, 22.9], its ends at
+// h = 0 and h = 2^32 - 1).  x * (1/t) and the sum add 3 * 2^-24 of
 // |x / t| and of |s|.  delta(s) = 1e-4 + 1e-6 (|s| + 48) covers all of it
 // with a margin of five or more (|x / t| <= |s| + 24).  A greedy row is exact
 // in fp32 (delta = 0).
