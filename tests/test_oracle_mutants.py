@@ -11,8 +11,11 @@ import importlib
 import importlib.util
 import inspect
 import os
+import pathlib
 import shutil
 import subprocess
+
+import pytest
 
 import oracle
 
@@ -111,6 +114,16 @@ PY_MUTANTS = [
 ]
 
 
+@pytest.fixture
+def build_dir(request):
+    """Where this test's copies are built: the oracle's own (git-ignored) build folder, emptied afterwards."""
+    d = pathlib.Path(ROOT) / "oracle" / "_build" / "mutants" / request.node.name
+    shutil.rmtree(d, ignore_errors=True)
+    d.mkdir(parents=True)
+    yield d
+    shutil.rmtree(d, ignore_errors=True)
+
+
 def _pin_cases():
     """Every (pin, arguments) of test_oracle_pins, parametrisations expanded."""
     mod = importlib.import_module("tests.test_oracle_pins")
@@ -157,12 +170,12 @@ def _killed(cases) -> bool:
     return False
 
 
-def _survivors(mutants, tmp_path, monkeypatch):
+def _survivors(mutants, folder, monkeypatch):
     cases = _pin_cases()
     assert len(cases) > 40
     survivors = []
     for i, (name, text, repl) in enumerate(mutants):
-        so = _compile(str(tmp_path / str(i)), text, repl)
+        so = _compile(str(folder / str(i)), text, repl)
         monkeypatch.setattr(oracle, "_lib", oracle.bind(so))
         if not _killed(cases):
             survivors.append(name)
@@ -191,29 +204,29 @@ def test_unmutated_oracle_passes_every_pin():
         fn(**kw)
 
 
-def test_every_mutant_fails_a_pin(tmp_path, monkeypatch):
+def test_every_mutant_fails_a_pin(build_dir, monkeypatch):
     # control: an unchanged copy built the way the mutants are passes every pin
     text = MUTANTS[0][1]
-    assert _survivors([("copy", text, text)], tmp_path / "copy", monkeypatch) == ["copy"]
-    survivors = _survivors(MUTANTS, tmp_path, monkeypatch)
+    assert _survivors([("copy", text, text)], build_dir / "copy", monkeypatch) == ["copy"]
+    survivors = _survivors(MUTANTS, build_dir, monkeypatch)
     assert not survivors, f"mutants no pin catches: {survivors}"
 
 
-def test_unpinned_readings_are_still_unpinned(tmp_path, monkeypatch):
+def test_unpinned_readings_are_still_unpinned(build_dir, monkeypatch):
     """If a pin comes to catch one of these, move it to MUTANTS and drop its "parity unpinned" notes."""
-    assert _survivors(UNPINNED, tmp_path, monkeypatch) == [m[0] for m in UNPINNED]
+    assert _survivors(UNPINNED, build_dir, monkeypatch) == [m[0] for m in UNPINNED]
 
 
-def test_every_wrapper_mutant_fails_a_pin(tmp_path, monkeypatch):
+def test_every_wrapper_mutant_fails_a_pin(build_dir, monkeypatch):
     pins = importlib.import_module("tests.test_oracle_pins")
     cases = _pin_cases()
     text = PY_MUTANTS[0][1]
-    monkeypatch.setattr(pins, "oracle", _py_mutant(str(tmp_path / "copy"), "copy", text, text))
+    monkeypatch.setattr(pins, "oracle", _py_mutant(str(build_dir / "copy"), "copy", text, text))
     assert not _killed(cases), "an unmutated copy of the wrapper fails a pin"
     monkeypatch.undo()
     survivors = []
     for i, (name, text, repl) in enumerate(PY_MUTANTS):
-        monkeypatch.setattr(pins, "oracle", _py_mutant(str(tmp_path / str(i)), name, text, repl))
+        monkeypatch.setattr(pins, "oracle", _py_mutant(str(build_dir / str(i)), name, text, repl))
         if not _killed(cases):
             survivors.append(name)
         monkeypatch.undo()
