@@ -9,7 +9,6 @@ a small "logits" row.  With batch_dependent=True the logits also depend on
 the number of rows in the step, as a batch-variant kernel's would: the
 comparators must catch it.
 """
-import numpy as np
 import torch
 
 from invariant_fixed_order_gb300.engine import PagePool
