@@ -128,16 +128,36 @@ def new_status(device="cuda") -> torch.Tensor:
 
 
 def check_status(status: torch.Tensor, stream=None) -> None:
-    _check(_lib.bi_check_status(_p(status), _stream(stream)))
+    _check(_lib.bi_check_status(_d(status, "status", _I32), _stream(stream)))
 
 
 def reset_status(status: torch.Tensor, stream=None) -> None:
-    _check(_lib.bi_reset_status(_p(status), _stream(stream)))
+    _check(_lib.bi_reset_status(_d(status, "status", _I32), _stream(stream)))
 
 
-def _bf16_bits(t: torch.Tensor):
-    assert t.dtype == torch.bfloat16 and t.is_contiguous(), "expected a contiguous bf16 tensor"
+_BF16, _F32, _I32 = (torch.bfloat16,), (torch.float32,), (torch.int32,)
+_U32 = (torch.int32,) + ((torch.uint32,) if hasattr(torch, "uint32") else ())
+
+
+def _d(t, name: str, dtypes=None, optional: bool = False):
+    """The device pointer of a dense CUDA tensor (the C ABI reads it as a flat
+    row-major array), after checking that it is one; None stays NULL when the
+    argument is optional."""
+    if t is None:
+        if optional:
+            return None
+        raise ValueError(f"{name}: a CUDA tensor is required")
+    if not isinstance(t, torch.Tensor) or not t.is_cuda:
+        raise ValueError(f"{name}: expected a CUDA tensor")
+    if not t.is_contiguous():
+        raise ValueError(f"{name}: expected a contiguous tensor (the library reads it as a dense row-major array)")
+    if dtypes is not None and t.dtype not in dtypes:
+        raise ValueError(f"{name}: expected dtype {' or '.join(str(d) for d in dtypes)}, got {t.dtype}")
     return _p(t)
+
+
+def _out_dt(c_dtype: int):
+    return _F32 if c_dtype == F32 else _BF16
 
 
 # ---- kernels ------------------------------------------------------------------
@@ -146,8 +166,8 @@ def rmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-5, out: torch.
             stream=None) -> torch.Tensor:
     d = x.shape[-1]
     out = torch.empty_like(x) if out is None else out
-    _check(_lib.bi_rmsnorm(_bf16_bits(x), _bf16_bits(gamma), _bf16_bits(out), x.numel() // d, d, eps,
-                           _stream(stream)))
+    _check(_lib.bi_rmsnorm(_d(x, "x", _BF16), _d(gamma, "gamma", _BF16), _d(out, "out", _BF16), x.numel() // d, d,
+                           eps, _stream(stream)))
     return out
 
 
@@ -166,15 +186,18 @@ def gemm(A: torch.Tensor, W: torch.Tensor, out: torch.Tensor | None = None, c_dt
     need = gemm_workspace_size(M, N, K, mode)
     if need and (ws is None or ws.numel() < need):
         ws = torch.empty(need, dtype=torch.uint8, device=A.device)
-    _check(_lib.bi_gemm(_p(A), _p(W), _p(out), c_dtype, _p(residual), ep, M, N, K, mode, _p(ws),
-                        0 if ws is None else ws.numel(), _p(status), _stream(stream)))
+    _check(_lib.bi_gemm(_d(A, "A", _BF16), _d(W, "W", _BF16), _d(out, "out", _out_dt(c_dtype)), c_dtype,
+                        _d(residual, "residual", _BF16, optional=True), ep, M, N, K, mode,
+                        _d(ws, "ws", optional=True), 0 if ws is None else ws.numel() * ws.element_size(),
+                        _d(status, "status", _I32, optional=True), _stream(stream)))
     return out
 
 
 def pack_gate_up(w_gate: torch.Tensor, w_up: torch.Tensor, stream=None) -> torch.Tensor:
     F, d = w_gate.shape
     out = torch.empty(2 * F, d, dtype=torch.bfloat16, device=w_gate.device)
-    _check(_lib.bi_pack_gate_up(_p(w_gate), _p(w_up), _p(out), F, d, _stream(stream)))
+    _check(_lib.bi_pack_gate_up(_d(w_gate, "w_gate", _BF16), _d(w_up, "w_up", _BF16), _d(out, "out", _BF16), F, d,
+                                _stream(stream)))
     return out
 
 
@@ -188,9 +211,12 @@ def rope_table(n_pos: int, Dh: int, theta: float):
 def rope_kv_append(qkv, tok_req, tok_pos, rope_cos, rope_sin, q_out, k_cache, v_cache, page_table, H, Hkv, Dh,
                    status, stream=None):
     T = qkv.shape[0]
-    _check(_lib.bi_rope_kv_append(_p(qkv), _p(tok_req), _p(tok_pos), _p(rope_cos), _p(rope_sin),
-                                  rope_cos.shape[0], _p(q_out), _p(k_cache), _p(v_cache), _p(page_table),
-                                  page_table.shape[-1], k_cache.shape[0], T, H, Hkv, Dh, _p(status),
+    _check(_lib.bi_rope_kv_append(_d(qkv, "qkv", _F32), _d(tok_req, "tok_req", _I32), _d(tok_pos, "tok_pos", _I32),
+                                  _d(rope_cos, "rope_cos", _F32), _d(rope_sin, "rope_sin", _F32),
+                                  rope_cos.shape[0], _d(q_out, "q_out", _BF16), _d(k_cache, "k_cache", _BF16),
+                                  _d(v_cache, "v_cache", _BF16), _d(page_table, "page_table", _I32),
+                                  page_table.shape[-1], k_cache.shape[0], T, H, Hkv, Dh,
+                                  _d(status, "status", _I32, optional=True),
                                   _stream(stream)))
 
 
@@ -210,9 +236,12 @@ def decode_attention(q, k_cache, v_cache, page_table, seq_lens, max_seq_len: int
     need = decode_attention_workspace_size(B, H, Dh, max_seq_len, mode)
     if ws is None or ws.numel() < need:
         ws = torch.empty(need, dtype=torch.uint8, device=q.device)
-    _check(_lib.bi_decode_attention(_p(q), _p(k_cache), _p(v_cache), _p(page_table), _p(seq_lens), _p(out),
-                                    out_dtype, B, H, Hkv, Dh, page_table.shape[-1], k_cache.shape[0], max_seq_len,
-                                    scale, mode, _p(ws), ws.numel(), _p(status), _stream(stream)))
+    _check(_lib.bi_decode_attention(_d(q, "q", _BF16), _d(k_cache, "k_cache", _BF16), _d(v_cache, "v_cache", _BF16),
+                                    _d(page_table, "page_table", _I32), _d(seq_lens, "seq_lens", _I32),
+                                    _d(out, "out", _out_dt(out_dtype)), out_dtype, B, H, Hkv, Dh,
+                                    page_table.shape[-1], k_cache.shape[0], max_seq_len, scale, mode,
+                                    _d(ws, "ws"), ws.numel() * ws.element_size(),
+                                    _d(status, "status", _I32, optional=True), _stream(stream)))
     return out
 
 
@@ -230,9 +259,12 @@ def decode_attention_noalloc(q, k_cache, v_cache, page_table, seq_lens, max_seq_
         scale = float(torch.tensor(1.0, dtype=torch.float32) / torch.sqrt(torch.tensor(float(Dh))))
     if out is None:
         out = torch.empty(B, H, Dh, device=q.device, dtype=torch.float32 if out_dtype == F32 else torch.bfloat16)
-    _check(_lib.bi_decode_attention_noalloc(_p(q), _p(k_cache), _p(v_cache), _p(page_table), _p(seq_lens), _p(out),
+    _check(_lib.bi_decode_attention_noalloc(_d(q, "q", _BF16), _d(k_cache, "k_cache", _BF16),
+                                            _d(v_cache, "v_cache", _BF16), _d(page_table, "page_table", _I32),
+                                            _d(seq_lens, "seq_lens", _I32), _d(out, "out", _out_dt(out_dtype)),
                                             out_dtype, B, H, Hkv, Dh, page_table.shape[-1], k_cache.shape[0],
-                                            max_seq_len, scale, mode, _p(status), _stream(stream)))
+                                            max_seq_len, scale, mode, _d(status, "status", _I32, optional=True),
+                                            _stream(stream)))
     return out
 
 
@@ -245,16 +277,18 @@ def prefill_attention(q, cu_q, q_pos0, k_cache, v_cache, page_table, out_dtype: 
         scale = float(torch.tensor(1.0, dtype=torch.float32) / torch.sqrt(torch.tensor(float(Dh))))
     if out is None:
         out = torch.empty(T, H, Dh, device=q.device, dtype=torch.float32 if out_dtype == F32 else torch.bfloat16)
-    _check(_lib.bi_prefill_attention(_p(q), _p(cu_q), _p(q_pos0), _p(k_cache), _p(v_cache), _p(page_table),
-                                     _p(out), out_dtype, B, T, H, Hkv, Dh, page_table.shape[-1], k_cache.shape[0],
-                                     scale, _p(status), _stream(stream)))
+    _check(_lib.bi_prefill_attention(_d(q, "q", _BF16), _d(cu_q, "cu_q", _I32), _d(q_pos0, "q_pos0", _I32),
+                                     _d(k_cache, "k_cache", _BF16), _d(v_cache, "v_cache", _BF16),
+                                     _d(page_table, "page_table", _I32), _d(out, "out", _out_dt(out_dtype)), out_dtype,
+                                     B, T, H, Hkv, Dh, page_table.shape[-1], k_cache.shape[0], scale,
+                                     _d(status, "status", _I32, optional=True), _stream(stream)))
     return out
 
 
 def argmax(logits: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     R, V = logits.shape
     out = torch.empty(R, dtype=torch.int32, device=logits.device) if out is None else out
-    _check(_lib.bi_argmax(_p(logits), _p(out), R, V, _stream(stream)))
+    _check(_lib.bi_argmax(_d(logits, "logits", _F32), _d(out, "out", _I32), R, V, _stream(stream)))
     return out
 
 
@@ -269,7 +303,8 @@ def log_softmax(logits: torch.Tensor, out: torch.Tensor | None = None, ws: torch
     need = log_softmax_workspace_size(R, V)
     if ws is None or ws.numel() < need:
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=logits.device)
-    _check(_lib.bi_log_softmax(_p(logits), _p(out), R, V, _p(ws), ws.numel(), _stream(stream)))
+    _check(_lib.bi_log_softmax(_d(logits, "logits", _F32), _d(out, "out", _F32), R, V, _d(ws, "ws"),
+                               ws.numel() * ws.element_size(), _stream(stream)))
     return out
 
 
@@ -286,8 +321,9 @@ def sample(logits: torch.Tensor, seeds: torch.Tensor, positions: torch.Tensor, t
     need = sample_workspace_size(R, V)
     if ws is None or ws.numel() < need:
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=logits.device)
-    _check(_lib.bi_sample(_p(logits), _p(seeds), _p(positions), _p(temperatures), _p(out), R, V, _p(ws),
-                          ws.numel(), _stream(stream)))
+    _check(_lib.bi_sample(_d(logits, "logits", _F32), _d(seeds, "seeds", _U32), _d(positions, "positions", _I32),
+                          _d(temperatures, "temperatures", _F32), _d(out, "out", _I32), R, V, _d(ws, "ws"),
+                          ws.numel() * ws.element_size(), _stream(stream)))
     return out
 
 
@@ -295,7 +331,8 @@ def embed(E: torch.Tensor, ids: torch.Tensor, status=None, out=None, stream=None
     V, d = E.shape
     T = ids.shape[0]
     out = torch.empty(T, d, dtype=torch.bfloat16, device=E.device) if out is None else out
-    _check(_lib.bi_embed(_p(E), _p(ids), _p(out), T, V, d, _p(status), _stream(stream)))
+    _check(_lib.bi_embed(_d(E, "E", _BF16), _d(ids, "ids", _I32), _d(out, "out", _BF16), T, V, d,
+                         _d(status, "status", _I32, optional=True), _stream(stream)))
     return out
 
 
@@ -317,6 +354,11 @@ class Model:
         self.max_pos = max_pos
         self._c = ModelConfigC(cfg.d, cfg.H, cfg.Hkv, cfg.Dh, cfg.F, cfg.V, cfg.n_layers, cfg.eps, cfg.rope_theta,
                                max_pos)
+        for i, L in enumerate(layers):
+            for k in ("gamma_attn", "w_qkv", "w_o", "gamma_ffn", "w_gu", "w_down"):
+                _d(L[k], f"layers[{i}][{k}]", _BF16)
+        for k in ("embed", "gamma_final", "w_lm"):
+            _d(head[k], f"head[{k}]", _BF16)
         self._arrays = {k: _ptr_array([L[k] for L in layers])
                         for k in ("gamma_attn", "w_qkv", "w_o", "gamma_ffn", "w_gu", "w_down")}
         w = ModelWeightsC(head["embed"].data_ptr(), head["gamma_final"].data_ptr(), head["w_lm"].data_ptr(),
@@ -350,9 +392,16 @@ class Model:
         p0 = (ctypes.c_int32 * B)(*[int(v) for v in pos0])
         R = len(logit_rows)
         rows = (ctypes.c_int32 * max(R, 1))(*[int(v) for v in logit_rows])
-        batch = BatchC(B, ql, p0, token_ids.data_ptr(), page_table.data_ptr(), page_table.shape[-1], R, rows,
-                       None if meta is None else meta.data_ptr())
+        batch = BatchC(B, ql, p0, _d(token_ids, "token_ids", _I32).value, _d(page_table, "page_table", _I32).value,
+                       page_table.shape[-1], R, rows,
+                       None if meta is None else _d(meta, "meta", _I32).value)
+        for name, caches in (("kv_k", kv_k), ("kv_v", kv_v)):
+            for i, t in enumerate(caches):
+                _d(t, f"{name}[{i}]", _BF16)
         ka, va = _ptr_array(kv_k), _ptr_array(kv_v)
         kv = KVCacheC(ka, va, kv_k[0].shape[0])
-        _check(_lib.bi_forward_step(self._h, ctypes.byref(batch), ctypes.byref(kv), _p(logits_out), _p(tokens_out),
-                                    _p(hidden_out), mode, _p(ws), ws.numel(), _p(status), _stream(stream)))
+        _check(_lib.bi_forward_step(self._h, ctypes.byref(batch), ctypes.byref(kv),
+                                    _d(logits_out, "logits_out", _F32, optional=True),
+                                    _d(tokens_out, "tokens_out", _I32, optional=True),
+                                    _d(hidden_out, "hidden_out", _BF16, optional=True), mode, _d(ws, "ws"),
+                                    ws.numel() * ws.element_size(), _d(status, "status", _I32), _stream(stream)))
