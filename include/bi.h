@@ -200,7 +200,8 @@ bi_status bi_rope_table(float* cos_out, float* sin_out, int32_t n_pos, int32_t D
  *   n_i     = max(ceil(s_i / 256), ceil(s_i / chunk2)),
  * and request i's keys are cut into pieces of ceil(s_i / n_i) positions from
  * key 0; so the pieces depend on the batch.  max_s = max_seq_len.
- * ws: DEVICE scratch of bi_decode_attention_workspace_size bytes. */
+ * ws: DEVICE scratch of bi_decode_attention_workspace_size bytes.
+ * scale <= 0 (or NaN) selects the default fl32(1 / fl32(sqrt(Dh))). */
 size_t bi_decode_attention_workspace_size(int32_t B, int32_t H, int32_t Dh, int32_t max_seq_len,
                                           bi_mode mode);
 bi_status bi_decode_attention(const bi_bf16* q, const bi_bf16* k_cache, const bi_bf16* v_cache,
@@ -222,11 +223,13 @@ bi_status bi_decode_attention(const bi_bf16* q, const bi_bf16* k_cache, const bi
  * computes.  A batch whose partials need more
  * (B * H * splits * (Dh + 2) * 4 bytes, splits = ceil(max_seq_len / 256) in
  * invariant mode) is rejected with BI_ERR_WORKSPACE before any launch.
- * The first call on each device looks up the array's device address; make
+ * The first call on each device (and the first after a device reset, which
+ * gives the array a new address) looks up the array's device address; make
  * that first call before any stream capture.  All calls share the one array:
  * calls whose work overlaps on the GPU race and corrupt each other's
  * partials, so keep them ordered (one stream, or events).  Nothing in the
- * array needs to start at zero: each call writes every partial it reads. */
+ * array needs to start at zero: each call writes every partial it reads.
+ * scale <= 0 (or NaN) selects the default, as in bi_decode_attention. */
 bi_status bi_decode_attention_noalloc(const bi_bf16* q, const bi_bf16* k_cache, const bi_bf16* v_cache,
                                       const int32_t* page_table, const int32_t* seq_lens,
                                       void* out, bi_dtype out_dtype,
@@ -238,13 +241,28 @@ bi_status bi_decode_attention_noalloc(const bi_bf16* q, const bi_bf16* k_cache, 
  * owns queries [cu_q[i], cu_q[i+1]) at positions q_pos0[i] + t (cu_q: DEVICE
  * [B+1], q_pos0: DEVICE [B]); its K/V for positions 0..q_pos0[i]+q_len-1 must
  * already be in the cache.  q: DEVICE [T, H, Dh] bf16; out: DEVICE [T, H, Dh].
- * Same per-(query, chunk) arithmetic and merge as bi_decode_attention, so a
- * token gets the same bits from either call. */
+ * max_seq_len: HOST upper bound on q_pos0[i] + q_len_i (0 < max_seq_len <=
+ * max_pages * 16).
+ * BI_INVARIANT: the same per-(query, chunk) arithmetic and merge as
+ * bi_decode_attention, so a token gets the same bits from either call and
+ * from any cutting of its prompt into calls ("Batch invariance and
+ * reproducible inference", "Mathematically equivalent is not bitwise
+ * equivalent": prefill and decode must reduce alike).  The products run on
+ * tcgen05 tensor cores with the accumulators in tensor memory; no workspace
+ * (ws may be NULL).
+ * BI_VARIANT: every query's keys are cut by the occupancy rule documented at
+ * bi_decode_attention, with num_seq = B and max_s = max_seq_len, and the
+ * pieces merged in order: the split then depends on the batch (the negative
+ * control).  Its fp32 partials live in ws.
+ * ws: DEVICE scratch of bi_prefill_attention_workspace_size bytes, 16-byte
+ * aligned.  scale <= 0 (or NaN) selects the default fl32(1 / fl32(sqrt(Dh))). */
+size_t bi_prefill_attention_workspace_size(int32_t T, int32_t H, int32_t Dh, int32_t max_seq_len, bi_mode mode);
 bi_status bi_prefill_attention(const bi_bf16* q, const int32_t* cu_q, const int32_t* q_pos0,
                                const bi_bf16* k_cache, const bi_bf16* v_cache,
                                const int32_t* page_table, void* out, bi_dtype out_dtype,
                                int32_t B, int32_t T, int32_t H, int32_t Hkv, int32_t Dh,
-                               int32_t max_pages, int32_t num_pages, float scale,
+                               int32_t max_pages, int32_t num_pages, int32_t max_seq_len, float scale,
+                               bi_mode mode, void* ws, size_t ws_bytes,
                                int32_t* dev_status, bi_stream stream);
 
 /* ---- Greedy argmax ("Batch invariance and reproducible inference",

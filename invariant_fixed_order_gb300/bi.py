@@ -89,8 +89,9 @@ _proto("bi_decode_attention", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i
        _f32, _i32, _vp, _sz, _vp, _vp)
 _proto("bi_decode_attention_noalloc", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
        _i32, _f32, _i32, _vp, _vp)
+_proto("bi_prefill_attention_workspace_size", _sz, _i32, _i32, _i32, _i32, _i32)
 _proto("bi_prefill_attention", _i32, _vp, _vp, _vp, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32, _i32, _i32,
-       _i32, _f32, _vp, _vp)
+       _i32, _i32, _f32, _i32, _vp, _sz, _vp, _vp)
 _proto("bi_argmax", _i32, _vp, _vp, _i32, _i32, _vp)
 _proto("bi_log_softmax_workspace_size", _sz, _i32, _i32)
 _proto("bi_log_softmax", _i32, _vp, _vp, _i32, _i32, _vp, _sz, _vp)
@@ -156,6 +157,25 @@ def _d(t, name: str, dtypes=None, optional: bool = False):
     return _p(t)
 
 
+def _shape(t, name: str, *dims, optional: bool = False, min_rows: bool = False):
+    """Checks t's shape against the sizes passed to the C ABI (None: any), before any pointer is taken: the
+    library builds its copies and stores from those sizes, so a tensor of another shape would be read or
+    written out of bounds.  min_rows: the first dimension may be larger (rows past it are never touched)."""
+    if t is None:
+        if optional:
+            return
+        raise ValueError(f"{name}: a CUDA tensor is required")
+    if not isinstance(t, torch.Tensor):
+        raise ValueError(f"{name}: expected a CUDA tensor")
+    got = tuple(int(x) for x in t.shape)
+    want = tuple(dims)
+    ok = len(got) == len(want) and all(w is None or g == w or (min_rows and i == 0 and g >= w)
+                                       for i, (g, w) in enumerate(zip(got, want)))
+    if not ok:
+        shown = "(" + ", ".join("*" if w is None else str(w) for w in want) + ("," if len(want) == 1 else "") + ")"
+        raise ValueError(f"{name}: expected shape {shown}{' (or more rows)' if min_rows else ''}, got {got}")
+
+
 def _out_dt(c_dtype: int):
     return _F32 if c_dtype == F32 else _BF16
 
@@ -166,6 +186,8 @@ def rmsnorm(x: torch.Tensor, gamma: torch.Tensor, eps: float = 1e-5, out: torch.
             stream=None) -> torch.Tensor:
     d = x.shape[-1]
     out = torch.empty_like(x) if out is None else out
+    _shape(gamma, "gamma", d)
+    _shape(out, "out", *x.shape)
     _check(_lib.bi_rmsnorm(_d(x, "x", _BF16), _d(gamma, "gamma", _BF16), _d(out, "out", _BF16), x.numel() // d, d,
                            eps, _stream(stream)))
     return out
@@ -178,11 +200,15 @@ def gemm_workspace_size(M: int, N: int, K: int, mode: int = INVARIANT) -> int:
 def gemm(A: torch.Tensor, W: torch.Tensor, out: torch.Tensor | None = None, c_dtype: int = BF16,
          residual: torch.Tensor | None = None, ep: int = EP_NONE, mode: int = INVARIANT,
          ws: torch.Tensor | None = None, status: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    _shape(A, "A", None, None)
     M, K = A.shape
+    _shape(W, "W", None, K)
     N = W.shape[0]
+    ncol = N // 2 if ep == EP_SWIGLU else N
     if out is None:
-        ncol = N // 2 if ep == EP_SWIGLU else N
         out = torch.empty(M, ncol, device=A.device, dtype=torch.float32 if c_dtype == F32 else torch.bfloat16)
+    _shape(out, "out", M, ncol)
+    _shape(residual, "residual", M, N, optional=True)
     need = gemm_workspace_size(M, N, K, mode)
     if need and (ws is None or ws.numel() < need):
         ws = torch.empty(need, dtype=torch.uint8, device=A.device)
@@ -194,7 +220,9 @@ def gemm(A: torch.Tensor, W: torch.Tensor, out: torch.Tensor | None = None, c_dt
 
 
 def pack_gate_up(w_gate: torch.Tensor, w_up: torch.Tensor, stream=None) -> torch.Tensor:
+    _shape(w_gate, "w_gate", None, None)
     F, d = w_gate.shape
+    _shape(w_up, "w_up", F, d)
     out = torch.empty(2 * F, d, dtype=torch.bfloat16, device=w_gate.device)
     _check(_lib.bi_pack_gate_up(_d(w_gate, "w_gate", _BF16), _d(w_up, "w_up", _BF16), _d(out, "out", _BF16), F, d,
                                 _stream(stream)))
@@ -210,7 +238,16 @@ def rope_table(n_pos: int, Dh: int, theta: float):
 
 def rope_kv_append(qkv, tok_req, tok_pos, rope_cos, rope_sin, q_out, k_cache, v_cache, page_table, H, Hkv, Dh,
                    status, stream=None):
+    _shape(qkv, "qkv", None, (H + 2 * Hkv) * Dh)
     T = qkv.shape[0]
+    _shape(tok_req, "tok_req", T)
+    _shape(tok_pos, "tok_pos", T)
+    _shape(rope_cos, "rope_cos", None, Dh // 2)
+    _shape(rope_sin, "rope_sin", rope_cos.shape[0], Dh // 2)
+    _shape(q_out, "q_out", T, H, Dh)
+    _shape(k_cache, "k_cache", None, Hkv, PAGE, Dh)
+    _shape(v_cache, "v_cache", *k_cache.shape)
+    _shape(page_table, "page_table", None, None)
     _check(_lib.bi_rope_kv_append(_d(qkv, "qkv", _F32), _d(tok_req, "tok_req", _I32), _d(tok_pos, "tok_pos", _I32),
                                   _d(rope_cos, "rope_cos", _F32), _d(rope_sin, "rope_sin", _F32),
                                   rope_cos.shape[0], _d(q_out, "q_out", _BF16), _d(k_cache, "k_cache", _BF16),
@@ -224,22 +261,36 @@ def decode_attention_workspace_size(B: int, H: int, Dh: int, max_seq_len: int, m
     return int(_lib.bi_decode_attention_workspace_size(B, H, Dh, max_seq_len, mode))
 
 
+def _attn_shapes(q, k_cache, v_cache, page_table, rows: int):
+    _shape(q, "q", rows, None, None)
+    _, H, Dh = q.shape
+    _shape(k_cache, "k_cache", None, None, PAGE, Dh)
+    _shape(v_cache, "v_cache", *k_cache.shape)
+    _shape(page_table, "page_table", None, None)
+    return H, k_cache.shape[1]
+
+
 def decode_attention(q, k_cache, v_cache, page_table, seq_lens, max_seq_len: int, out_dtype: int = BF16,
                      mode: int = INVARIANT, scale: float | None = None, ws=None, status=None, out=None,
                      stream=None) -> torch.Tensor:
+    """scale None: the library's default fl32(1 / fl32(sqrt(Dh)))."""
+    _shape(q, "q", None, None, None)
     B, H, Dh = q.shape
+    _attn_shapes(q, k_cache, v_cache, page_table, B)
     Hkv = k_cache.shape[1]
-    if scale is None:
-        scale = float(torch.tensor(1.0, dtype=torch.float32) / torch.sqrt(torch.tensor(float(Dh))))
+    _shape(page_table, "page_table", B, None)
+    _shape(seq_lens, "seq_lens", B)
     if out is None:
         out = torch.empty(B, H, Dh, device=q.device, dtype=torch.float32 if out_dtype == F32 else torch.bfloat16)
+    _shape(out, "out", B, H, Dh)
     need = decode_attention_workspace_size(B, H, Dh, max_seq_len, mode)
     if ws is None or ws.numel() < need:
         ws = torch.empty(need, dtype=torch.uint8, device=q.device)
     _check(_lib.bi_decode_attention(_d(q, "q", _BF16), _d(k_cache, "k_cache", _BF16), _d(v_cache, "v_cache", _BF16),
                                     _d(page_table, "page_table", _I32), _d(seq_lens, "seq_lens", _I32),
                                     _d(out, "out", _out_dt(out_dtype)), out_dtype, B, H, Hkv, Dh,
-                                    page_table.shape[-1], k_cache.shape[0], max_seq_len, scale, mode,
+                                    page_table.shape[-1], k_cache.shape[0], max_seq_len,
+                                    0.0 if scale is None else scale, mode,
                                     _d(ws, "ws"), ws.numel() * ws.element_size(),
                                     _d(status, "status", _I32, optional=True), _stream(stream)))
     return out
@@ -253,41 +304,64 @@ def decode_attention_noalloc(q, k_cache, v_cache, page_table, seq_lens, max_seq_
                              stream=None) -> torch.Tensor:
     """decode_attention without a workspace: the library's static device
     scratch holds the split partials (for callers that cannot allocate)."""
+    _shape(q, "q", None, None, None)
     B, H, Dh = q.shape
+    _attn_shapes(q, k_cache, v_cache, page_table, B)
     Hkv = k_cache.shape[1]
-    if scale is None:
-        scale = float(torch.tensor(1.0, dtype=torch.float32) / torch.sqrt(torch.tensor(float(Dh))))
+    _shape(page_table, "page_table", B, None)
+    _shape(seq_lens, "seq_lens", B)
     if out is None:
         out = torch.empty(B, H, Dh, device=q.device, dtype=torch.float32 if out_dtype == F32 else torch.bfloat16)
+    _shape(out, "out", B, H, Dh)
     _check(_lib.bi_decode_attention_noalloc(_d(q, "q", _BF16), _d(k_cache, "k_cache", _BF16),
                                             _d(v_cache, "v_cache", _BF16), _d(page_table, "page_table", _I32),
                                             _d(seq_lens, "seq_lens", _I32), _d(out, "out", _out_dt(out_dtype)),
                                             out_dtype, B, H, Hkv, Dh, page_table.shape[-1], k_cache.shape[0],
-                                            max_seq_len, scale, mode, _d(status, "status", _I32, optional=True),
-                                            _stream(stream)))
+                                            max_seq_len, 0.0 if scale is None else scale, mode,
+                                            _d(status, "status", _I32, optional=True), _stream(stream)))
     return out
 
 
+def prefill_attention_workspace_size(T: int, H: int, Dh: int, max_seq_len: int, mode: int = INVARIANT) -> int:
+    return int(_lib.bi_prefill_attention_workspace_size(T, H, Dh, max_seq_len, mode))
+
+
 def prefill_attention(q, cu_q, q_pos0, k_cache, v_cache, page_table, out_dtype: int = BF16,
-                      scale: float | None = None, status=None, out=None, stream=None) -> torch.Tensor:
+                      scale: float | None = None, status=None, out=None, stream=None, mode: int = INVARIANT,
+                      max_seq_len: int | None = None, ws=None) -> torch.Tensor:
+    """Causal attention of ragged query blocks.  max_seq_len None: the page table's capacity (a bound the
+    caller need not compute); scale None: the library's default."""
+    _shape(q, "q", None, None, None)
     T, H, Dh = q.shape
+    _shape(cu_q, "cu_q", None)
     B = cu_q.shape[0] - 1
+    _attn_shapes(q, k_cache, v_cache, page_table, T)
     Hkv = k_cache.shape[1]
-    if scale is None:
-        scale = float(torch.tensor(1.0, dtype=torch.float32) / torch.sqrt(torch.tensor(float(Dh))))
+    _shape(q_pos0, "q_pos0", B)
+    _shape(page_table, "page_table", B, None)
+    if max_seq_len is None:
+        max_seq_len = page_table.shape[-1] * PAGE
     if out is None:
         out = torch.empty(T, H, Dh, device=q.device, dtype=torch.float32 if out_dtype == F32 else torch.bfloat16)
+    _shape(out, "out", T, H, Dh)
+    need = prefill_attention_workspace_size(T, H, Dh, max_seq_len, mode)
+    if need and (ws is None or ws.numel() < need):
+        ws = torch.empty(need, dtype=torch.uint8, device=q.device)
     _check(_lib.bi_prefill_attention(_d(q, "q", _BF16), _d(cu_q, "cu_q", _I32), _d(q_pos0, "q_pos0", _I32),
                                      _d(k_cache, "k_cache", _BF16), _d(v_cache, "v_cache", _BF16),
                                      _d(page_table, "page_table", _I32), _d(out, "out", _out_dt(out_dtype)), out_dtype,
-                                     B, T, H, Hkv, Dh, page_table.shape[-1], k_cache.shape[0], scale,
+                                     B, T, H, Hkv, Dh, page_table.shape[-1], k_cache.shape[0], max_seq_len,
+                                     0.0 if scale is None else scale, mode, _d(ws, "ws", optional=True),
+                                     0 if ws is None else ws.numel() * ws.element_size(),
                                      _d(status, "status", _I32, optional=True), _stream(stream)))
     return out
 
 
 def argmax(logits: torch.Tensor, out: torch.Tensor | None = None, stream=None) -> torch.Tensor:
+    _shape(logits, "logits", None, None)
     R, V = logits.shape
     out = torch.empty(R, dtype=torch.int32, device=logits.device) if out is None else out
+    _shape(out, "out", R)
     _check(_lib.bi_argmax(_d(logits, "logits", _F32), _d(out, "out", _I32), R, V, _stream(stream)))
     return out
 
@@ -298,8 +372,10 @@ def log_softmax_workspace_size(R: int, V: int) -> int:
 
 def log_softmax(logits: torch.Tensor, out: torch.Tensor | None = None, ws: torch.Tensor | None = None,
                 stream=None) -> torch.Tensor:
+    _shape(logits, "logits", None, None)
     R, V = logits.shape
     out = torch.empty(R, V, dtype=torch.float32, device=logits.device) if out is None else out
+    _shape(out, "out", R, V)
     need = log_softmax_workspace_size(R, V)
     if ws is None or ws.numel() < need:
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=logits.device)
@@ -316,8 +392,11 @@ def sample(logits: torch.Tensor, seeds: torch.Tensor, positions: torch.Tensor, t
            out: torch.Tensor | None = None, ws: torch.Tensor | None = None, stream=None) -> torch.Tensor:
     """Seeded Gumbel-max tokens; seeds uint32 (or int32 holding the same bits), positions int32,
     temperatures fp32, all DEVICE [R]."""
+    _shape(logits, "logits", None, None)
     R, V = logits.shape
     out = torch.empty(R, dtype=torch.int32, device=logits.device) if out is None else out
+    for name, t in (("seeds", seeds), ("positions", positions), ("temperatures", temperatures), ("out", out)):
+        _shape(t, name, R)
     need = sample_workspace_size(R, V)
     if ws is None or ws.numel() < need:
         ws = torch.empty(max(need, 1), dtype=torch.uint8, device=logits.device)
@@ -328,9 +407,12 @@ def sample(logits: torch.Tensor, seeds: torch.Tensor, positions: torch.Tensor, t
 
 
 def embed(E: torch.Tensor, ids: torch.Tensor, status=None, out=None, stream=None) -> torch.Tensor:
+    _shape(E, "E", None, None)
     V, d = E.shape
+    _shape(ids, "ids", None)
     T = ids.shape[0]
     out = torch.empty(T, d, dtype=torch.bfloat16, device=E.device) if out is None else out
+    _shape(out, "out", T, d)
     _check(_lib.bi_embed(_d(E, "E", _BF16), _d(ids, "ids", _I32), _d(out, "out", _BF16), T, V, d,
                          _d(status, "status", _I32, optional=True), _stream(stream)))
     return out
@@ -354,10 +436,17 @@ class Model:
         self.max_pos = max_pos
         self._c = ModelConfigC(cfg.d, cfg.H, cfg.Hkv, cfg.Dh, cfg.F, cfg.V, cfg.n_layers, cfg.eps, cfg.rope_theta,
                                max_pos)
+        if len(layers) != cfg.n_layers:
+            raise ValueError(f"layers: expected {cfg.n_layers}, got {len(layers)}")
+        qkv = (cfg.H + 2 * cfg.Hkv) * cfg.Dh
+        want = {"gamma_attn": (cfg.d,), "w_qkv": (qkv, cfg.d), "w_o": (cfg.d, cfg.H * cfg.Dh), "gamma_ffn": (cfg.d,),
+                "w_gu": (2 * cfg.F, cfg.d), "w_down": (cfg.d, cfg.F)}
         for i, L in enumerate(layers):
             for k in ("gamma_attn", "w_qkv", "w_o", "gamma_ffn", "w_gu", "w_down"):
+                _shape(L[k], f"layers[{i}][{k}]", *want[k])
                 _d(L[k], f"layers[{i}][{k}]", _BF16)
-        for k in ("embed", "gamma_final", "w_lm"):
+        for k, shp in (("embed", (cfg.V, cfg.d)), ("gamma_final", (cfg.d,)), ("w_lm", (cfg.V, cfg.d))):
+            _shape(head[k], f"head[{k}]", *shp)
             _d(head[k], f"head[{k}]", _BF16)
         self._arrays = {k: _ptr_array([L[k] for L in layers])
                         for k in ("gamma_attn", "w_qkv", "w_o", "gamma_ffn", "w_gu", "w_down")}
@@ -388,10 +477,25 @@ class Model:
         """One ragged step.  q_len / pos0 / logit_rows are host int sequences; meta (optional) is the
         step's per-token metadata already on the device (the layout bi_batch documents)."""
         B = len(q_len)
+        if len(pos0) != B:
+            raise ValueError(f"pos0: expected {B} entries, got {len(pos0)}")
         ql = (ctypes.c_int32 * B)(*[int(v) for v in q_len])
         p0 = (ctypes.c_int32 * B)(*[int(v) for v in pos0])
         R = len(logit_rows)
         rows = (ctypes.c_int32 * max(R, 1))(*[int(v) for v in logit_rows])
+        T = sum(int(v) for v in q_len)
+        c = self.cfg
+        _shape(token_ids, "token_ids", T)
+        _shape(page_table, "page_table", B, None, min_rows=True)
+        _shape(meta, "meta", 3 * T + R, optional=True)
+        _shape(logits_out, "logits_out", R, c.V, optional=True, min_rows=True)
+        _shape(tokens_out, "tokens_out", R, optional=True, min_rows=True)
+        _shape(hidden_out, "hidden_out", T, c.d, optional=True, min_rows=True)
+        if len(kv_k) != c.n_layers or len(kv_v) != c.n_layers:
+            raise ValueError(f"kv_k / kv_v: expected {c.n_layers} layers")
+        for name, caches in (("kv_k", kv_k), ("kv_v", kv_v)):
+            for i, t in enumerate(caches):
+                _shape(t, f"{name}[{i}]", kv_k[0].shape[0], c.Hkv, PAGE, c.Dh)
         batch = BatchC(B, ql, p0, _d(token_ids, "token_ids", _I32).value, _d(page_table, "page_table", _I32).value,
                        page_table.shape[-1], R, rows,
                        None if meta is None else _d(meta, "meta", _I32).value)

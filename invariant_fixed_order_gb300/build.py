@@ -19,7 +19,7 @@ CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build")
 LIB = os.path.join(BUILD, "libbi.so")
 UNITS = ["api.cu", "k_rows.cu", "k_attention.cu", "k_gemm.cu", "k_logits.cu"]
-HEADERS = ["common.cuh", "internal.h", "tc_ptx.cuh"]
+HEADERS = ["common.cuh", "internal.h", "tc_ptx.cuh", "prefill_tc.cuh"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 FLAGS = ["-O3", "-std=c++17", "-lineinfo", "-Xcompiler", "-fPIC", "-Xcompiler", "-O2"]
 

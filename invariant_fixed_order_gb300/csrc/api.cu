@@ -42,6 +42,11 @@ static bool aligned16(const void* p) { return (reinterpret_cast<uintptr_t>(p) & 
 
 static size_t align_up(size_t v, size_t a = 256) { return (v + a - 1) / a * a; }
 
+// The attention scale fl32(1 / fl32(sqrt(Dh))) unless the caller gives a positive one.
+float default_scale(float scale, int32_t Dh) {
+    return scale > 0.0f ? scale : 1.0f / sqrtf(static_cast<float>(Dh));
+}
+
 }  // namespace bi
 
 using namespace bi;
@@ -204,27 +209,51 @@ extern "C" bi_status bi_decode_attention(const bi_bf16* q, const bi_bf16* k_cach
     if (!aligned16(ws)) return fail(BI_ERR_INVALID, "bi_decode_attention: workspace must be 16-byte aligned");
     float* ws_o = static_cast<float*>(ws);
     float* ws_ml = ws_o + static_cast<size_t>(B) * H * max_splits * Dh;
-    AttnGeom g{q, k_cache, v_cache, page_table, out, out_dtype == BI_F32, H, Hkv, Dh, max_pages, num_pages, scale,
-               dev_status};
+    AttnGeom g{q, k_cache, v_cache, page_table, out, out_dtype == BI_F32, H, Hkv, Dh, max_pages, num_pages,
+               default_scale(scale, Dh), dev_status};
     EntryMap em{0, seq_lens, nullptr, nullptr, B};
     cudaError_t e = launch_decode_attention(g, em, B, max_splits, chunk2, ws_o, ws_ml, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? BI_OK : cuda_fail(e, "bi_decode_attention launch");
+}
+
+extern "C" size_t bi_prefill_attention_workspace_size(int32_t T, int32_t H, int32_t Dh, int32_t max_seq_len,
+                                                      bi_mode mode) {
+    if (T <= 0 || H <= 0 || Dh <= 0 || mode != BI_VARIANT) return 0;
+    // the occupancy rule never cuts a context into more than max(ceil(s / 256), 16) pieces
+    return decode_ws_bytes(T, H, Dh, std::max(invariant_max_splits(max_seq_len), 16));
 }
 
 extern "C" bi_status bi_prefill_attention(const bi_bf16* q, const int32_t* cu_q, const int32_t* q_pos0,
                                           const bi_bf16* k_cache, const bi_bf16* v_cache, const int32_t* page_table,
                                           void* out, bi_dtype out_dtype, int32_t B, int32_t T, int32_t H,
                                           int32_t Hkv, int32_t Dh, int32_t max_pages, int32_t num_pages,
-                                          float scale, int32_t* dev_status, bi_stream stream) {
+                                          int32_t max_seq_len, float scale, bi_mode mode, void* ws,
+                                          size_t ws_bytes, int32_t* dev_status, bi_stream stream) {
     if (B < 0 || T < 0) return fail(BI_ERR_SHAPE, "bi_prefill_attention: negative size");
     if (B == 0 || T == 0) return BI_OK;
     bi_status st = check_attn(q, k_cache, v_cache, page_table, out, out_dtype, H, Hkv, Dh, max_pages, num_pages);
     if (st != BI_OK) return st;
     if (!cu_q || !q_pos0) return fail(BI_ERR_INVALID, "bi_prefill_attention: null cu_q / q_pos0");
-    AttnGeom g{q, k_cache, v_cache, page_table, out, out_dtype == BI_F32, H, Hkv, Dh, max_pages, num_pages, scale,
-               dev_status};
+    if (max_seq_len <= 0 || max_seq_len > max_pages * BI_PAGE)
+        return fail(BI_ERR_SHAPE, "bi_prefill_attention: need 0 < max_seq_len <= max_pages * 16");
+    if (mode != BI_INVARIANT && mode != BI_VARIANT) return fail(BI_ERR_INVALID, "bi_prefill_attention: bad mode");
+    AttnGeom g{q, k_cache, v_cache, page_table, out, out_dtype == BI_F32, H, Hkv, Dh, max_pages, num_pages,
+               default_scale(scale, Dh), dev_status};
     EntryMap em{2, cu_q, q_pos0, nullptr, B};
-    cudaError_t e = launch_prefill_attention(g, em, T, static_cast<cudaStream_t>(stream));
+    cudaError_t e;
+    if (mode == BI_INVARIANT) {
+        e = launch_prefill_attention(g, em, T, static_cast<cudaStream_t>(stream));
+    } else {
+        // every query as a decode entry whose pieces follow the occupancy rule of this batch
+        int32_t max_splits = 0, chunk2 = 0;
+        variant_split_plan(B, H, Hkv, max_seq_len, &chunk2, &max_splits);
+        const size_t need = decode_ws_bytes(T, H, Dh, max_splits);
+        if (!ws || ws_bytes < need) return fail(BI_ERR_WORKSPACE, "bi_prefill_attention: workspace too small");
+        if (!aligned16(ws)) return fail(BI_ERR_INVALID, "bi_prefill_attention: workspace must be 16-byte aligned");
+        float* ws_o = static_cast<float*>(ws);
+        float* ws_ml = ws_o + static_cast<size_t>(T) * H * max_splits * Dh;
+        e = launch_decode_attention(g, em, T, max_splits, chunk2, ws_o, ws_ml, static_cast<cudaStream_t>(stream));
+    }
     return e == cudaSuccess ? BI_OK : cuda_fail(e, "bi_prefill_attention launch");
 }
 
@@ -502,7 +531,7 @@ extern "C" bi_status bi_forward_step(bi_model* m, const bi_batch* batch, const b
     void* gws = base + L.gemm_ws;
     const size_t gws_bytes = static_cast<size_t>(num_sms()) * BI_GEMM_BLOCK_M * BI_GEMM_UMMA_N * 4 + 4096;
     const int32_t nqkv = (c.H + 2 * c.Hkv) * c.Dh;
-    const float scale = 1.0f / sqrtf(static_cast<float>(c.Dh));
+    const float scale = default_scale(0.0f, c.Dh);
 
     int32_t dec_splits = invariant_max_splits(max_seq_dec), chunk2 = 0;
     if (mode == BI_VARIANT) variant_split_plan(b.B, c.H, c.Hkv, max_seq, &chunk2, &dec_splits);

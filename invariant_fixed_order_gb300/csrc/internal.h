@@ -65,6 +65,8 @@ void set_error(const std::string& msg);
 bi_status fail(bi_status s, const std::string& msg);
 bi_status cuda_fail(cudaError_t e, const char* what);
 int num_sms();
+// the attention scale: the caller's when positive, else fl32(1 / fl32(sqrt(Dh)))
+float default_scale(float scale, int32_t Dh);
 
 // ---- elementwise / row kernels (k_rows.cu) ----
 // Greedy argmax fused into an fp32 GEMM epilogue: keys[rows] (set to

@@ -3,17 +3,17 @@
 // "1 · Split-K and segmented attention reductions": the split count is
 // ceil(seq_len / tile), a function of the request's own length).
 //
-// One device function computes the fp32 partial (m, l, o) of one chunk of
-// keys for a set of (query, head) columns: the G heads of one GQA group of one
-// query (decode) or of 16/G consecutive queries of one request (prefill).
-// Decode runs it in one CTA per (query, kv head, chunk) and merges the
-// partials in a second kernel; prefill runs it chunk after chunk in one CTA
-// per (query block, kv head) and folds as it goes.  Both use the same chunk
-// boundaries (multiples of BI_KV_CHUNK from key 0), the same per-column
-// partial and the same fold, so a token's output has the same bits whichever
-// path, batch or prefill chunking produced it.  Every floating-point step
-// outside the MMAs is an explicit round-to-nearest intrinsic so the compiler
-// cannot fuse or reorder it differently in the two kernels.
+// Decode: one device function computes the fp32 partial (m, l, o) of one
+// chunk of keys for the G heads of one GQA group of one query, in one CTA per
+// (query, kv head, chunk); a second kernel merges the partials in ascending
+// chunk order.  Prefill (prefill_tc.cuh) runs the same per-chunk arithmetic on
+// the tcgen05 tensor cores for 128 (token, head) rows at a time and folds the
+// chunks in order as it goes.  Both use the same chunk boundaries (multiples
+// of BI_KV_CHUNK from key 0), the same per-row partial and the same fold, so
+// a token's output has the same bits whichever path, batch or prefill
+// chunking produced it.  Every floating-point step outside the MMAs is an
+// explicit round-to-nearest intrinsic so the compiler cannot fuse or reorder
+// it differently in the two kernels.
 #include <math.h>
 
 #include <mutex>
@@ -42,9 +42,9 @@ constexpr int kHStride = BI_KV_CHUNK + 8;
 
 // The MMAs are transposed with respect to the usual attention tiling: the 16
 // rows of an m16n8k16 tile are keys (scores) or head dims (PV), and its 8
-// columns are (query token, head) pairs, token-major.  A decode CTA has one
-// token, so its columns are the G heads of one GQA group; a prefill CTA has
-// NT consecutive tokens of one request sharing every K/V load.
+// columns are (query token, head) pairs, token-major: NT tokens of one
+// request sharing every K/V load.  A decode CTA has one token (NT = 1), so its
+// columns are the G heads of one GQA group.
 template <int G, int DH, int NT>
 struct AttnShape {
     static_assert(G >= 1 && G <= 8 && NT >= 1, "unsupported group");
@@ -59,7 +59,7 @@ struct AttnShape {
 // Scores (fp32; after PV, the outputs being stored) and the bf16 hi = bf16(p)
 // and lo = bf16(p - hi) parts of p that the PV MMAs read.  With few columns
 // (decode) the two share storage, which keeps a CTA small enough for six per
-// SM; with many (prefill) they are separate, which keeps registers down.
+// SM; with many they are separate, which keeps registers down.
 template <int C, bool kShared>
 struct ScoreStore;
 template <int C>
@@ -91,10 +91,6 @@ struct AttnSmem {
     float red[kWarps][S::kCols];     // per-warp partial sums of l
     float m[S::kCols];
     float l[S::kCols];
-    float fold_a[S::kCols];          // prefill fold: weights of the running state and of the chunk
-    float fold_b[S::kCols];
-    float M[S::kCols];               // prefill fold: running max and sum
-    float L[S::kCols];
     int32_t ncol[S::kCols];          // keys of the current chunk each column attends to
     int32_t pages[kMaxChunkPages];
 };
@@ -652,114 +648,6 @@ decode_merge_kernel(AttnGeom geo, EntryMap em, int32_t max_splits, int32_t chunk
 }
 
 // ---------------------------------------------------------------------------
-// Prefill: grid (ceil(entries / NT), Hkv).  A CTA takes NT consecutive
-// entries; each run of them that belongs to one request shares its K/V loads,
-// walks the chunks in order and folds them in registers with the decode
-// merge's arithmetic, column by column.
-// ---------------------------------------------------------------------------
-template <int G, int DH, int NT>
-__global__ void __launch_bounds__(kAttnThreads)
-prefill_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnGeom geo,
-               EntryMap em, int32_t n_entries) {
-    pdl_trigger();
-    pdl_wait();
-    using S = AttnShape<G, DH, NT>;
-    extern __shared__ __align__(16) unsigned char smem_raw[];
-    AttnSmem<G, DH, NT>& sm = *reinterpret_cast<AttnSmem<G, DH, NT>*>(smem_raw);
-    const int32_t g = blockIdx.y;
-    const int32_t e_begin = static_cast<int32_t>(blockIdx.x) * NT;
-    const int32_t e_end = min(e_begin + NT, n_entries);
-    const int tid = threadIdx.x;
-    ring_init(sm);
-    uint32_t phase = 0;
-    for (int32_t e0 = e_begin; e0 < e_end;) {
-        const Entry first = get_entry(em, e0);
-        int32_t e1 = e0 + 1;
-        while (e1 < e_end && get_entry(em, e1).r == first.r) ++e1;
-        int32_t tok[NT], keys[NT];
-        int32_t s_max = 0;
-#pragma unroll
-        for (int i = 0; i < NT; ++i) {
-            tok[i] = -1;
-            keys[i] = 0;
-            if (e0 + i < e1) {
-                const Entry en = get_entry(em, e0 + i);
-                const int32_t s = en.p + 1;
-                const bool ok = en.p >= 0 && (s + BI_PAGE - 1) / BI_PAGE <= geo.max_pages;
-                if (!ok && tid == 0) report(geo.status, BI_DEV_BAD_POSITION);
-                tok[i] = en.t;
-                keys[i] = ok ? s : 0;
-                s_max = max(s_max, keys[i]);
-            }
-        }
-        uint32_t qb[S::kNB][DH / 16][2];
-        load_q_cols<G, DH, NT>(reinterpret_cast<const uint16_t*>(geo.q), tok, geo.H, g, qb);
-        float O[S::kMT][S::kNB][4];
-        const int32_t count = (s_max + BI_KV_CHUNK - 1) / BI_KV_CHUNK;
-        const int32_t* page_row = geo.page_table + static_cast<int64_t>(first.r) * geo.max_pages;
-        for (int32_t j = 0; j < count; ++j) {
-            const int32_t k0 = j * BI_KV_CHUNK;
-            if (tid < S::kCols) sm.ncol[tid] = min(max(keys[tid / G] - k0, 0), BI_KV_CHUNK);
-            float o[S::kMT][S::kNB][4];
-            chunk_partial<G, DH, NT>(sm, reinterpret_cast<const uint16_t*>(geo.kc),
-                                     reinterpret_cast<const uint16_t*>(geo.vc), &tmK, &tmV, phase, page_row, g,
-                                     geo.Hkv, k0,
-                                     min(BI_KV_CHUNK, s_max - k0), geo.scale, geo.max_pages, geo.num_pages,
-                                     geo.status, qb, o, [] {});
-            // the decode merge's fold (fold_step), one column's (M, L) at a time
-            if (tid < S::kCols && sm.ncol[tid] > 0) {
-                const float m = sm.m[tid], l = sm.l[tid];
-                if (j == 0) {
-                    sm.M[tid] = m;
-                    sm.L[tid] = l;
-                } else {
-                    const float M = sm.M[tid];
-                    const float Mn = fmaxf(M, m);
-                    const float a = expf(__fsub_rn(M, Mn));
-                    const float b = expf(__fsub_rn(m, Mn));
-                    sm.L[tid] = __fadd_rn(__fmul_rn(sm.L[tid], a), __fmul_rn(l, b));
-                    sm.M[tid] = Mn;
-                    sm.fold_a[tid] = a;
-                    sm.fold_b[tid] = b;
-                }
-            }
-            __syncthreads();
-            const int lane = tid & 31;
-#pragma unroll
-            for (int mt = 0; mt < S::kMT; ++mt)
-#pragma unroll
-                for (int nb = 0; nb < S::kNB; ++nb)
-#pragma unroll
-                    for (int x = 0; x < 4; ++x) {
-                        const int c = nb * 8 + 2 * (lane & 3) + (x & 1);
-                        if (c < S::kCols && sm.ncol[c] > 0)
-                            O[mt][nb][x] = j == 0 ? o[mt][nb][x]
-                                                  : __fadd_rn(__fmul_rn(O[mt][nb][x], sm.fold_a[c]),
-                                                              __fmul_rn(o[mt][nb][x], sm.fold_b[c]));
-                    }
-            __syncthreads();
-        }
-        // out = O / L, staged through the score buffer; a token without keys gets zeros
-        constexpr int kOStride = DH + 4;
-        float* stage = &sm.sc.p[0][0];  // [kCols][kOStride]
-        for_each_out<G, DH, NT>(O, [&](int c, int d, float v) {
-            stage[c * kOStride + d] = keys[c / G] > 0 ? __fdiv_rn(v, sm.L[c]) : 0.0f;
-        });
-        __syncthreads();
-        for (int i = tid; i < S::kCols * (DH / 2); i += kAttnThreads) {
-            const int c = i / (DH / 2), dp = i % (DH / 2);
-            const int ti = c / G;
-            if (e0 + ti < e1)
-                store_out2(geo.out, geo.out_f32,
-                           (static_cast<int64_t>(tok[ti]) * geo.H + static_cast<int64_t>(g) * G + c % G) * DH + 2 * dp,
-                           stage[c * kOStride + 2 * dp], stage[c * kOStride + 2 * dp + 1]);
-        }
-        __syncthreads();
-        e0 = e1;
-    }
-}
-
-// ---------------------------------------------------------------------------
 // Host side
 // ---------------------------------------------------------------------------
 bool attention_supported(int32_t H, int32_t Hkv, int32_t Dh) {
@@ -828,28 +716,6 @@ static cudaError_t launch_decode_t(const AttnGeom& g, const EntryMap& em, int32_
     return launch_decode_ring<G, DH, kRing>(g, em, n, max_splits, chunk2, ws_o, ws_ml, early_kv, s);
 }
 
-// Query tokens per prefill CTA: 16 (token, head) columns.
-template <int G>
-constexpr int prefill_tokens() { return 16 / G; }
-
-template <int G, int DH>
-static cudaError_t launch_prefill_t(const AttnGeom& g, const EntryMap& em, int32_t n, cudaStream_t s) {
-    constexpr int NT = prefill_tokens<G>();
-    const size_t smem = sizeof(AttnSmem<G, DH, NT>);
-    static std::once_flag once;
-    static cudaError_t attr_err = cudaSuccess;
-    std::call_once(once, [smem] {
-        attr_err = cudaFuncSetAttribute(prefill_kernel<G, DH, NT>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                        static_cast<int>(smem));
-    });
-    if (attr_err != cudaSuccess) return attr_err;
-    CUtensorMap tmK, tmV;
-    if (!encode_kv_map(&tmK, g.kc, g.num_pages, g.Hkv, DH) || !encode_kv_map(&tmV, g.vc, g.num_pages, g.Hkv, DH))
-        return cudaErrorInvalidValue;
-    return launch_pdl(prefill_kernel<G, DH, NT>, dim3((n + NT - 1) / NT, g.Hkv), dim3(kAttnThreads), smem, s, tmK,
-                      tmV, g, em, n);
-}
-
 #define BI_ATTN_DISPATCH(FN, ...)                                              \
     do {                                                                       \
         const int32_t G_ = g.H / g.Hkv;                                        \
@@ -874,9 +740,15 @@ cudaError_t launch_decode_attention(const AttnGeom& g, const EntryMap& em, int32
     BI_ATTN_DISPATCH(launch_decode_t, g, em, n_entries, max_splits, variant_chunk2, ws_o, ws_ml, early_kv, s);
 }
 
+}  // namespace bi
+
+#include "prefill_tc.cuh"
+
+namespace bi {
+
 cudaError_t launch_prefill_attention(const AttnGeom& g, const EntryMap& em, int32_t n_entries, cudaStream_t s) {
     if (n_entries <= 0) return cudaSuccess;
-    BI_ATTN_DISPATCH(launch_prefill_t, g, em, n_entries, s);
+    BI_ATTN_DISPATCH(tc_prefill::launch_prefill_tc_t, g, em, n_entries, s);
 }
 
 }  // namespace bi
@@ -904,20 +776,58 @@ namespace {
 constexpr int kMaxDevices = 64;
 std::mutex g_noalloc_mutex;
 void* g_noalloc_ptr[kMaxDevices] = {};
+unsigned long long g_noalloc_ctx[kMaxDevices] = {};  // the context the address was taken in
 
-// Device address of the scratch array on the current device; looked up once
-// per device (the host-side symbol is only a stand-in, never a device address).
+using CtxGetCurrentFn = CUresult (*)(CUcontext*);
+using CtxGetIdFn = CUresult (*)(CUcontext, unsigned long long*);
+
+// Unique id of the context current on this thread (ids are never reused, so
+// a context re-created after a device reset gets a new one); false when no
+// context is current or the driver offers no such query.
+bool current_ctx_id(unsigned long long* id) {
+    static CtxGetCurrentFn get_current = nullptr;
+    static CtxGetIdFn get_id = nullptr;
+    static std::once_flag once;
+    std::call_once(once, [] {
+        void* p = nullptr;
+        cudaDriverEntryPointQueryResult q;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetCurrent", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_current = reinterpret_cast<CtxGetCurrentFn>(p);
+        p = nullptr;
+        if (cudaGetDriverEntryPointByVersion("cuCtxGetId", &p, 12000, cudaEnableDefault, &q) == cudaSuccess &&
+            q == cudaDriverEntryPointSuccess)
+            get_id = reinterpret_cast<CtxGetIdFn>(p);
+    });
+    if (!get_current || !get_id) return false;
+    CUcontext ctx = nullptr;
+    if (get_current(&ctx) != CUDA_SUCCESS || ctx == nullptr) return false;
+    return get_id(ctx, id) == CUDA_SUCCESS;
+}
+
+// Device address of the scratch array in the current device's context (the
+// host-side symbol is only a stand-in, never a device address).  Looked up
+// once per device and context: after a device reset the library's module is
+// loaded again in a new context, the array gets a new address, and the next
+// call looks it up anew.
 bi_status noalloc_scratch(void** out) {
     int dev = 0;
     cudaError_t e = cudaGetDevice(&dev);
     if (e != cudaSuccess) return cuda_fail(e, "bi_decode_attention_noalloc: cudaGetDevice");
     if (dev < 0 || dev >= kMaxDevices) return fail(BI_ERR_UNSUPPORTED, "bi_decode_attention_noalloc: device index");
+    unsigned long long ctx = 0;
+    const bool known = current_ctx_id(&ctx);
     std::lock_guard<std::mutex> lock(g_noalloc_mutex);
-    if (g_noalloc_ptr[dev] == nullptr) {
+    if (!known || g_noalloc_ptr[dev] == nullptr || g_noalloc_ctx[dev] != ctx) {
         void* p = nullptr;
         e = cudaGetSymbolAddress(&p, g_noalloc_scratch);
         if (e != cudaSuccess) return cuda_fail(e, "bi_decode_attention_noalloc: cudaGetSymbolAddress");
-        g_noalloc_ptr[dev] = p;
+        // the lookup makes the device's primary context current if none was
+        unsigned long long now = 0;
+        g_noalloc_ptr[dev] = current_ctx_id(&now) ? p : nullptr;  // no id: look it up again next call
+        g_noalloc_ctx[dev] = now;
+        *out = p;
+        return BI_OK;
     }
     *out = g_noalloc_ptr[dev];
     return BI_OK;
@@ -961,8 +871,8 @@ extern "C" bi_status bi_decode_attention_noalloc(const bi_bf16* q, const bi_bf16
     // the scratch has to start at zero
     float* ws_o = static_cast<float*>(scratch);
     float* ws_ml = ws_o + static_cast<size_t>(B) * H * max_splits * Dh;
-    AttnGeom g{q, k_cache, v_cache, page_table, out, out_dtype == BI_F32, H, Hkv, Dh, max_pages, num_pages, scale,
-               dev_status};
+    AttnGeom g{q, k_cache, v_cache, page_table, out, out_dtype == BI_F32, H, Hkv, Dh, max_pages, num_pages,
+               default_scale(scale, Dh), dev_status};
     EntryMap em{0, seq_lens, nullptr, nullptr, B};
     cudaError_t e = launch_decode_attention(g, em, B, max_splits, chunk2, ws_o, ws_ml, static_cast<cudaStream_t>(stream));
     return e == cudaSuccess ? BI_OK : cuda_fail(e, "bi_decode_attention_noalloc launch");

@@ -298,6 +298,61 @@ def test_8b_layer_oracle_parity(mods, layer8b):
         assert np.max(np.abs(got_h - x_out[0])) <= 4 * 2.0 ** -8 * (np.max(np.abs(x_out[0])) + 1)
 
 
+def test_8b_prefill_chunk_with_decodes_oracle_parity(mods, layer8b):
+    """A 300-token prompt prefilled in the same step as four decode requests of the 8B-shaped layer (T = 304:
+    256-wide GEMM tiles, RoPE over many positions in the QKV epilogue, tcgen05 prefill attention over two
+    chunks): the logits of every prompt position and of the decode rows, and the layer output of every token,
+    against the oracle."""
+    bi, sched, _ = mods
+    case = layer8b
+    cfg = case.cfg
+    dims = oracle.Dims(cfg.d, cfg.H, cfg.Hkv, cfg.Dh, cfg.F, cfg.eps, cfg.rope_theta)
+    w = {k: f32(v) for k, v in case.eng.logical[0].items()}
+    gamma_final, w_lm = f32(case.eng.head["gamma_final"]), f32(case.eng.head["w_lm"])
+    E = case.eng.head["embed"]
+    n = 300
+    T = n + 4
+    prompt = synth.token_ids(n, cfg.V, 777)
+    pages = case.eng.pool.alloc((n + 15) // 16)
+    ws_small = case.eng.ws
+    case.eng.ws = torch.empty(case.eng.model.workspace_size(T, 5, T, case.eng.max_seq), dtype=torch.uint8,
+                              device="cuda")
+    try:
+        prow = np.zeros(case.max_pages, np.int32)
+        prow[:len(pages)] = pages
+        dec = [3, int(np.argmin(case.ctx)), 17, int(np.argmax(case.ctx))]
+        # decode, decode, the prompt, decode, decode
+        q_len = [1, 1, n, 1, 1]
+        pos0 = [int(case.ctx[dec[0]]) - 1, int(case.ctx[dec[1]]) - 1, 0, int(case.ctx[dec[2]]) - 1,
+                int(case.ctx[dec[3]]) - 1]
+        ids = np.concatenate([case.ids[dec[:2]], prompt, case.ids[dec[2:]]]).astype(np.int32)
+        table = np.stack([case.table[dec[0]], case.table[dec[1]], prow, case.table[dec[2]], case.table[dec[3]]])
+        logits, _, hidden = case.eng.step(q_len, pos0, ids, table, list(range(T)), want_hidden=True)
+        case.eng.check()
+        logits, hidden = logits.cpu().numpy(), f32(hidden)
+        # the prompt: every position
+        x = f32(E[torch.from_numpy(prompt.astype(np.int64)).cuda()])
+        empty = [np.zeros((1, cfg.Hkv, cfg.Dh), np.float32)]
+        x_out, _, _, _ = oracle.layer_forward(dims, w, [n], [0], empty, empty, x)
+        ref_logits, _ = oracle.lm_head(dims, gamma_final, w_lm, x_out, np.arange(n))
+        got = logits[2:2 + n]
+        assert_logits_close(got, ref_logits)
+        row_err = np.max(np.abs(got - ref_logits), axis=1)
+        assert np.all(row_err <= 2e-2 * np.max(np.abs(ref_logits), axis=1))
+        assert np.max(np.abs(hidden[2:2 + n] - x_out)) <= 4 * 2.0 ** -8 * (np.max(np.abs(x_out)) + 1)
+        # the decode rows
+        for j, (r, t) in enumerate(zip(dec, (0, 1, n + 2, n + 3))):
+            k, v = case.hist[r]
+            xd = f32(E[int(case.ids[r])])[None]
+            xd_out, _, _, _ = oracle.layer_forward(dims, w, [1], [int(case.ctx[r]) - 1], [f32(k)], [f32(v)], xd)
+            ref_d, _ = oracle.lm_head(dims, gamma_final, w_lm, xd_out, [0])
+            assert_logits_close(logits[t:t + 1], ref_d)
+            assert np.max(np.abs(hidden[t] - xd_out[0])) <= 4 * 2.0 ** -8 * (np.max(np.abs(xd_out[0])) + 1)
+    finally:
+        case.eng.ws = ws_small
+        case.eng.pool.free(pages)
+
+
 def test_8b_layer_variant_mode_negative_control(mods, layer8b):
     """Variant mode must show bit differences against bs=1 somewhere (the
     harness has teeth), stay within the parity tolerance, and repeat itself on

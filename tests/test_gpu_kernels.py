@@ -105,6 +105,9 @@ def test_gemm_bf16_and_residual_epilogue(bi):
     assert np.array_equal(bits(C), bits(expect))
     ref = oracle.bf16_round(oracle.matmul(f32(A), f32(W)) + f32(R))
     assert np.mean(f32(C) == ref) > 0.98
+    # every element within one bf16 rounding of the oracle's (|acc| < 2, so the two fp32 sums of 1024 products
+    # differ by well under 3e-4 before the residual add and the rounding)
+    assert np.all(np.abs(f32(C) - ref) <= 2.0 ** -7 * np.abs(ref) + 3e-4)
     # in place (output aliases the residual)
     Rc = R.clone()
     bi.gemm(A, W, out=Rc, residual=Rc, ep=bi.EP_RESIDUAL)
@@ -317,6 +320,84 @@ def test_prefill_matches_decode_bitwise(bi, H, Hkv, Dh):
             g = h // G
             ref = oracle.attention_head(qf[p, h], k[:p + 1, g], v[:p + 1, g])
             assert np.max(np.abs(pre_f[p, h] - ref)) <= ATTN_MAX_ABS
+
+
+def test_prefill_dense_oracle_parity(bi):
+    """Every position of a 600-token prompt (three chunks, the last one partial), for heads of four different
+    KV groups, against the oracle's unsplit softmax attention."""
+    H, Hkv, Dh = 32, 8, 128
+    G = H // Hkv
+    n = 600
+    kv, hist, _ = make_decode_case([n], H, Hkv, Dh, seed=16)
+    q = synth.normal_bf16((n, H, Dh), 1.0, 78, "cuda")
+    cu = torch.tensor([0, n], dtype=torch.int32, device="cuda")
+    p0 = torch.tensor([0], dtype=torch.int32, device="cuda")
+    got = f32(bi.prefill_attention(q, cu, p0, kv.k[0], kv.v[0], kv.table_tensor(), out_dtype=bi.F32))
+    k, v = hist[0]
+    qf = f32(q)
+    worst = 0.0
+    for h in (0, 5, 13, 31):
+        g = h // G
+        for p in range(n):
+            ref = oracle.attention_head(qf[p, h], k[:p + 1, g], v[:p + 1, g])
+            worst = max(worst, float(np.max(np.abs(got[p, h] - ref))))
+    assert worst <= ATTN_MAX_ABS, worst
+
+
+def ragged_prefill_case(H, Hkv, Dh, seed):
+    """Five requests, each continuing a cached prefix: q_len [5, 37, 300, 1, 130] at q_pos0
+    [0, 250, 17, 600, 256] (chunk boundaries inside blocks, blocks that start mid-chunk, a one-token block,
+    CTAs whose 128 rows straddle requests)."""
+    q_len = [5, 37, 300, 1, 130]
+    q_pos0 = [0, 250, 17, 600, 256]
+    ctx = [a + b for a, b in zip(q_len, q_pos0)]
+    kv, hist, _ = make_decode_case(ctx, H, Hkv, Dh, seed=seed)
+    T = sum(q_len)
+    q = synth.normal_bf16((T, H, Dh), 1.0, seed + 5, "cuda")
+    cu = torch.tensor(np.concatenate([[0], np.cumsum(q_len)]), dtype=torch.int32, device="cuda")
+    p0 = torch.tensor(q_pos0, dtype=torch.int32, device="cuda")
+    tok_req = np.repeat(np.arange(len(q_len)), q_len)
+    tok_pos = np.concatenate([np.arange(a, a + b) for a, b in zip(q_pos0, q_len)])
+    return kv, hist, q, cu, p0, tok_req, tok_pos
+
+
+@pytest.mark.parametrize("H,Hkv,Dh", [(32, 8, 128), (8, 1, 64), (16, 16, 128), (4, 2, 64)])
+def test_prefill_ragged_batch_equals_decode(bi, H, Hkv, Dh):
+    """A ragged batch of five prompt blocks: each token's output is the bits decode gives it alone."""
+    kv, hist, q, cu, p0, tok_req, tok_pos = ragged_prefill_case(H, Hkv, Dh, seed=21)
+    table = kv.table_tensor()
+    st = bi.new_status()
+    pre = bits(bi.prefill_attention(q, cu, p0, kv.k[0], kv.v[0], table, out_dtype=bi.F32, status=st))
+    bi.check_status(st)
+    idx = torch.from_numpy(tok_req.astype(np.int64)).cuda()
+    dec = bits(bi.decode_attention(q, kv.k[0], kv.v[0], table[idx].contiguous(),
+                                   torch.from_numpy((tok_pos + 1).astype(np.int32)).cuda(), int(tok_pos.max()) + 1,
+                                   out_dtype=bi.F32))
+    assert np.array_equal(pre, dec)
+    # bf16 output: the same values rounded once
+    pre16 = bi.prefill_attention(q, cu, p0, kv.k[0], kv.v[0], table)
+    assert np.array_equal(bits(pre16), bits(torch.from_numpy(pre.view(np.float32)).to(torch.bfloat16)))
+
+
+def test_prefill_variant_mode_negative_control(bi):
+    """Batch-variant prefill cuts every query's keys by the occupancy rule of its batch: within the parity
+    tolerance of the invariant result, the same bits on a repeat, and different bits somewhere (the split
+    follows the batch)."""
+    H, Hkv, Dh = 32, 8, 128
+    kv, hist, q, cu, p0, tok_req, tok_pos = ragged_prefill_case(H, Hkv, Dh, seed=22)
+    table = kv.table_tensor()
+    inv = bi.prefill_attention(q, cu, p0, kv.k[0], kv.v[0], table, out_dtype=bi.F32)
+    var = bi.prefill_attention(q, cu, p0, kv.k[0], kv.v[0], table, out_dtype=bi.F32, mode=bi.VARIANT)
+    again = bi.prefill_attention(q, cu, p0, kv.k[0], kv.v[0], table, out_dtype=bi.F32, mode=bi.VARIANT)
+    assert np.array_equal(bits(var), bits(again))
+    assert float((var - inv).abs().max()) <= ATTN_MAX_ABS
+    assert not np.array_equal(bits(var), bits(inv))
+    # one query checked against the oracle directly
+    t = int(np.argmax(tok_pos))
+    r, p = int(tok_req[t]), int(tok_pos[t])
+    k, v = hist[r]
+    ref = oracle.attention_head(f32(q)[t, 3], k[:p + 1, 0], v[:p + 1, 0])
+    assert np.max(np.abs(f32(var)[t, 3] - ref)) <= ATTN_MAX_ABS
 
 
 def test_attention_bad_page_reports_status(bi):
