@@ -130,6 +130,17 @@ __host__ __device__ __forceinline__ int32_t variant_piece(int32_t s, int32_t chu
     return (s + n - 1) / n;
 }
 
+// e^x of the attention softmax and its merge, as 2^(x * log2 e) on the
+// special-function unit (ex2.approx, subnormal results flushed to zero: at
+// most ~2^-22 relative error, plus |x| * 2^-24 from rounding the product).
+// Every kernel whose results must agree bit for bit (decode's chunk partials
+// and merge, prefill's chunk softmax and fold) calls this one function.
+__device__ __forceinline__ float attn_exp(float x) {
+    float y;
+    asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(__fmul_rn(x, 1.44269504088896341f)));
+    return y;
+}
+
 __device__ __forceinline__ void cp_async16(void* dst, const void* src) {
     asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
@@ -401,7 +412,7 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT, RING>& sm, con
                         if (j < n_max) {
 #pragma unroll
                             for (int c = 0; c < S::kCols; ++c) {
-                                const float pv = expf(__fsub_rn(sm.sc.p[c][j], sm.m[c]));
+                                const float pv = attn_exp(__fsub_rn(sm.sc.p[c][j], sm.m[c]));
                                 const uint16_t hb = f32_to_bf16(pv);
                                 const uint16_t lb = f32_to_bf16(__fsub_rn(pv, bf16_to_f32(hb)));
                                 hl[i][c] = static_cast<uint32_t>(hb) | (static_cast<uint32_t>(lb) << 16);
@@ -425,7 +436,7 @@ __device__ __forceinline__ void chunk_partial(AttnSmem<G, DH, NT, RING>& sm, con
                     for (int j = tid; j < n_max; j += kAttnThreads) {
 #pragma unroll
                         for (int c = 0; c < S::kCols; ++c) {
-                            const float pv = expf(__fsub_rn(sm.sc.p[c][j], sm.m[c]));
+                            const float pv = attn_exp(__fsub_rn(sm.sc.p[c][j], sm.m[c]));
                             const uint16_t hb = f32_to_bf16(pv);
                             sm.sc.ph[0][c][j] = hb;
                             sm.sc.ph[1][c][j] = f32_to_bf16(__fsub_rn(pv, bf16_to_f32(hb)));
@@ -511,8 +522,8 @@ __device__ __forceinline__ void for_each_out(const float (&oacc)[AttnShape<G, DH
 __device__ __forceinline__ void fold_step(float& M, float& L, float& O0, float& O1, float m, float l,
                                           float o0, float o1) {
     const float Mn = fmaxf(M, m);
-    const float a = expf(__fsub_rn(M, Mn));
-    const float b = expf(__fsub_rn(m, Mn));
+    const float a = attn_exp(__fsub_rn(M, Mn));
+    const float b = attn_exp(__fsub_rn(m, Mn));
     L = __fadd_rn(__fmul_rn(L, a), __fmul_rn(l, b));
     O0 = __fadd_rn(__fmul_rn(O0, a), __fmul_rn(o0, b));
     O1 = __fadd_rn(__fmul_rn(O1, a), __fmul_rn(o1, b));

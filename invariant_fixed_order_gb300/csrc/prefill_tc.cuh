@@ -2,23 +2,32 @@
 // bitwise aligned with the decode routine of k_attention.cu.
 //
 // One CTA = 128 (query token, head) rows of one request and one KV head
-// (128 / G consecutive tokens x the G heads of the group), 128 threads; thread
-// t owns row t, which is also TMEM lane t.  Chunks of 256 keys from key 0,
-// walked in order; per chunk:
-//   S = Q K^T            tcgen05, M = 128 rows, N = 256 keys, K = Dh in 16-steps,
-//                        A = Q (K-major SW128, loaded once), B = the chunk's K
-//                        pages (K-major SW128, TMA page boxes) -> TMEM cols [0, 256)
-//   softmax per row      thread-local: score = fl(acc * scale) or -inf past the
-//                        row's keys; m = max; p = exp(score - m); hi = bf16(p),
-//                        lo = bf16(p - hi); l summed in the decode routine's tree
-//                        (lane-serial pairs j, j + 128; xor-butterfly over 32
-//                        keys; the four 32-key groups in order); hi/lo packed
-//                        into TMEM in place of the scores (A operand of PV)
+// (128 / G consecutive tokens x the G heads of the group).  Row r is tensor
+// memory lane r; two threads share it (warps w and w + 4 reach the same lane
+// quarter), each taking half of the row's keys and half of its head dims.
+// Chunks of 256 keys from key 0 are walked in order; per chunk:
+//   S = Q K^T            tcgen05, M = 128 rows, N = 256 keys, K = Dh in 16-deep
+//                        steps; A = Q (K-major, 128-byte swizzle, loaded once per
+//                        run of tokens), B = the chunk's K pages (TMA page boxes)
+//                        -> TMEM columns [0, 256)
+//   softmax per row      score = fl(acc * scale) (or -inf past the row's keys);
+//                        m = max; p = exp(score - m); hi = bf16(p), lo =
+//                        bf16(p - hi); l summed in the decode routine's tree:
+//                        per 32-key group b the pairs (32b + i, 32b + 128 + i)
+//                        added to 0 in that order, an xor-butterfly 16, 8, 4, 2,
+//                        1 over i, then the four groups in order.  The thread of
+//                        the lower half takes groups 0 and 1 (keys 0-63 and
+//                        128-191), the other groups 2 and 3; the partial maxima
+//                        and group sums meet in shared memory.  hi/lo pairs go
+//                        back into TMEM in place of the scores, as the A operand
+//                        of the next product
 //   o = P V              tcgen05, A = P (TMEM), B = the chunk's V pages read
-//                        MN-major (dims contiguous), per 16-key step hi then lo,
-//                        into a zeroed accumulator -> TMEM cols [256, 256 + Dh)
-//   fold                 the decode merge's expressions into the running
-//                        (M, L) in registers and O in TMEM cols [384, 384 + Dh)
+//                        MN-major (head dims contiguous), per 16-key step the hi
+//                        then the lo product, into an accumulator that starts
+//                        at zero -> TMEM columns [256, 256 + Dh)
+//   fold                 the decode merge's expressions into the running (M, L)
+//                        in registers and O in TMEM columns [384, 384 + Dh)
+// The next chunk's S product runs on the tensor cores while the fold runs.
 // Outside the MMAs every step repeats the decode routine's arithmetic.  Inside
 // them, a tcgen05 kind::f16 chain of 16-deep K steps gives the same fp32 bits
 // as the decode routine's mma.sync m16n8k16 chain over the same steps, for
@@ -27,11 +36,13 @@
 // kernel and from decode.
 #pragma once
 
+#include <limits.h>
+
 namespace bi {
 namespace tc_prefill {
 
-constexpr int kRows = 128;                 // rows per CTA = TMEM lanes = threads
-constexpr int kThreads = 128;
+constexpr int kRows = 128;                 // rows per CTA = TMEM lanes
+constexpr int kThreads = 256;              // two threads per row
 constexpr int kChunk = BI_KV_CHUNK;        // 256 keys
 constexpr int kKeyRegion = kChunk * 128;   // one 64-dim SW128 region of a chunk's K or V (32 KB)
 constexpr int kQRegion = kRows * 128;      // one 64-dim SW128 region of Q (16 KB)
@@ -43,6 +54,7 @@ constexpr uint32_t kColRun = 384;          // running O
 // A bf16 pair packed into one 32-bit TMEM column of an A operand holds the
 // even k in its low half (measured: the other order reproduces nothing).
 constexpr bool kLowHalfEvenK = true;
+static_assert(kLowHalfEvenK, "pack_p below writes the even key into the low half");
 
 template <int DH>
 struct Smem {
@@ -53,7 +65,11 @@ struct Smem {
     uint64_t k_full, v_full, s_done, pv_done;
     uint32_t tmem_base;
     int32_t abort;
-    int32_t pages[kChunk / BI_PAGE];
+    float xmax[2][kRows];                  // each half's partial row maximum
+    float xsum[2][kRows];                  // the upper half's group sums (groups 2 and 3)
+    float xL[kRows];                       // the row's final L, for the upper half's output
+    int32_t red_max[kThreads / 32];
+    int32_t red_min[kThreads / 32];
 };
 
 // Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled region.
@@ -83,8 +99,31 @@ __device__ __forceinline__ void mma_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_
         : "memory");
 }
 
-// Each thread writes 16 consecutive 32-bit columns of its own lane.
-__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16]) {
+// Each thread reads / writes 32 consecutive 32-bit columns of its own lane.
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, uint32_t* r) {
+    asm volatile(
+        "tcgen05.ld.sync.aligned.32x32b.x32.b32 "
+        "{%0, %1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, "
+        "%16, %17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31}, [%32];"
+        : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+          "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15]),
+          "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]), "=r"(r[22]), "=r"(r[23]),
+          "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]), "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+        : "r"(taddr)
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const uint32_t* v) {
+    asm volatile(
+        "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], "
+        "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16, "
+        "%17, %18, %19, %20, %21, %22, %23, %24, %25, %26, %27, %28, %29, %30, %31, %32};" ::"r"(taddr),
+        "r"(v[0]), "r"(v[1]), "r"(v[2]), "r"(v[3]), "r"(v[4]), "r"(v[5]), "r"(v[6]), "r"(v[7]), "r"(v[8]),
+        "r"(v[9]), "r"(v[10]), "r"(v[11]), "r"(v[12]), "r"(v[13]), "r"(v[14]), "r"(v[15]), "r"(v[16]),
+        "r"(v[17]), "r"(v[18]), "r"(v[19]), "r"(v[20]), "r"(v[21]), "r"(v[22]), "r"(v[23]), "r"(v[24]),
+        "r"(v[25]), "r"(v[26]), "r"(v[27]), "r"(v[28]), "r"(v[29]), "r"(v[30]), "r"(v[31])
+        : "memory");
+}
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
     asm volatile(
         "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], "
         "{%1, %2, %3, %4, %5, %6, %7, %8, %9, %10, %11, %12, %13, %14, %15, %16};" ::"r"(taddr),
@@ -94,122 +133,119 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t (&v)[16
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
-// TMEM address of column col of this thread's warp's lane quarter.
-__device__ __forceinline__ uint32_t lane_addr(uint32_t base, uint32_t col) {
-    return base + (static_cast<uint32_t>((threadIdx.x / 32) * 32) << 16) + col;
-}
-
-__device__ __forceinline__ uint32_t pack_pair(uint16_t even_k, uint16_t odd_k) {
-    return kLowHalfEvenK ? (static_cast<uint32_t>(even_k) | (static_cast<uint32_t>(odd_k) << 16))
-                         : (static_cast<uint32_t>(odd_k) | (static_cast<uint32_t>(even_k) << 16));
-}
-
-// Softmax of one chunk for this thread's row, in TMEM.  ncol = keys of the
-// chunk the row attends to (0..256).  On return m, l are the row's partial and
-// TMEM columns [16 g, 16 g + 16) hold key group g's p as the PV A operand:
-// 8 packed hi pairs, then 8 packed lo pairs.
-// n_max (the chunk's keys, the same in every thread) bounds the warp-collective
-// TMEM reads; ncol masks this thread's row.
-__device__ __forceinline__ void softmax_chunk(uint32_t tmem, int32_t n_max, int32_t ncol, float scale, float& m_out,
-                                              float& l_out) {
-    // m: exact max of the row's scores (order-free); a row without keys gets 0
-    float mx = -INFINITY;
-    for (int c0 = 0; c0 < n_max; c0 += 16) {
-        uint32_t r[16];
-        ptx::tmem_ld16(lane_addr(tmem, kColS + c0), r);
-        ptx::tmem_ld_wait();
-#pragma unroll
-        for (int j = 0; j < 16; ++j)
-            if (c0 + j < ncol) mx = fmaxf(mx, __fmul_rn(__uint_as_float(r[j]), scale));
-    }
-    const float m = ncol > 0 ? mx : 0.0f;
-    // p, its hi/lo parts, and l in the decode routine's tree: for each 32-key
-    // group b (keys 32b + L and 32b + 128 + L), lane-serial pairs, then the
-    // xor-butterfly 16, 8, 4, 2, 1 over L; the groups added in order
-    float l = 0.0f;
-#pragma unroll 1
-    for (int b = 0; b < 4; ++b) {
-        float u[32];
-#pragma unroll
-        for (int half = 0; half < 2; ++half) {       // keys 32b.. then 32b + 128..
-#pragma unroll
-            for (int q = 0; q < 2; ++q) {            // two 16-key groups of 32
-                const int c0 = 32 * b + 128 * half + 16 * q;
-                uint32_t r[16];
-                ptx::tmem_ld16(lane_addr(tmem, kColS + c0), r);
-                ptx::tmem_ld_wait();
-                uint32_t w[16];
-#pragma unroll
-                for (int j = 0; j < 16; j += 2) {
-                    float pv[2];
-                    uint16_t hb[2], lb[2];
-#pragma unroll
-                    for (int x = 0; x < 2; ++x) {
-                        const int key = c0 + j + x;
-                        const float sc = key < ncol ? __fmul_rn(__uint_as_float(r[j + x]), scale) : -INFINITY;
-                        pv[x] = expf(__fsub_rn(sc, m));
-                        hb[x] = f32_to_bf16(pv[x]);
-                        lb[x] = f32_to_bf16(__fsub_rn(pv[x], bf16_to_f32(hb[x])));
-                        const int L = 16 * q + j + x;
-                        u[L] = half == 0 ? __fadd_rn(0.0f, pv[x]) : __fadd_rn(u[L], pv[x]);
-                    }
-                    w[j / 2] = pack_pair(hb[0], hb[1]);
-                    w[8 + j / 2] = pack_pair(lb[0], lb[1]);
-                }
-                tmem_st16(lane_addr(tmem, kColS + c0), w);
-            }
-        }
-#pragma unroll
-        for (int off = 16; off >= 1; off >>= 1)
-#pragma unroll
-            for (int L = 0; L < off; ++L) u[L] = __fadd_rn(u[L], u[L + off]);
-        l = b == 0 ? u[0] : __fadd_rn(l, u[0]);
-    }
-    m_out = m;
-    l_out = l;
-}
-
-// Zeroes Dh columns of this thread's lane from col.
-template <int DH>
-__device__ __forceinline__ void tmem_zero(uint32_t tmem, uint32_t col) {
+// Writes zeros into N consecutive columns of this thread's lane from taddr.
+template <int N>
+__device__ __forceinline__ void zero_cols(uint32_t taddr) {
     uint32_t z[16];
 #pragma unroll
-    for (int j = 0; j < 16; ++j) z[j] = 0u;
+    for (int i = 0; i < 16; ++i) z[i] = 0u;
 #pragma unroll
-    for (int c0 = 0; c0 < DH; c0 += 16) tmem_st16(lane_addr(tmem, col + c0), z);
+    for (int c = 0; c < N; c += 16) tmem_st16(taddr + c, z);
 }
 
-// The decode merge's fold of this chunk's (m, l, o) into the running (M, L, O);
-// the first chunk copies.  Every thread of the CTA calls it (the TMEM accesses
-// are warp-collective; first is the same everywhere); a row that attends to no
-// key of the chunk (active false) keeps its state.
-template <int DH>
-__device__ __forceinline__ void fold_chunk(uint32_t tmem, bool first, bool active, float m, float l, float& M,
-                                           float& L) {
-    float a = 1.0f, b = 1.0f;
-    if (!active) {
-    } else if (!first) {
-        const float Mn = fmaxf(M, m);
-        a = expf(__fsub_rn(M, Mn));
-        b = expf(__fsub_rn(m, Mn));
-        L = __fadd_rn(__fmul_rn(L, a), __fmul_rn(l, b));
-        M = Mn;
-    } else {
-        M = m;
-        L = l;
-    }
-#pragma unroll 1
-    for (int c0 = 0; c0 < DH; c0 += 16) {
-        uint32_t o[16], O[16];
-        ptx::tmem_ld16(lane_addr(tmem, kColO + c0), o);
-        if (!first) ptx::tmem_ld16(lane_addr(tmem, kColRun + c0), O);
-        ptx::tmem_ld_wait();
-        if (!first && active)
+// TMEM address of column col of this thread's lane quarter.
+__device__ __forceinline__ uint32_t lane_addr(uint32_t base, uint32_t col) {
+    return base + (static_cast<uint32_t>(((threadIdx.x / 32) & 3) * 32) << 16) + col;
+}
+
+// p of two consecutive keys (the even one first) as packed bf16 hi and lo
+// pairs: hi = bf16(p) and lo = bf16(p - hi), rounded to nearest even as the
+// decode routine rounds them.
+__device__ __forceinline__ void pack_p(float p0, float p1, uint32_t& hi, uint32_t& lo) {
+    __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);  // .x (low half) = p0
+    hi = *reinterpret_cast<uint32_t*>(&h);
+    const float r0 = __fsub_rn(p0, __uint_as_float(hi << 16));
+    const float r1 = __fsub_rn(p1, __uint_as_float(hi & 0xffff0000u));
+    __nv_bfloat162 l = __floats2bfloat162_rn(r0, r1);
+    lo = *reinterpret_cast<uint32_t*>(&l);
+}
+
+// Softmax of one chunk for this thread's half of its row.  ncol = keys of the
+// chunk the row attends to (0..256); n_max = the chunk's keys (the same in
+// every thread, so the warp-collective TMEM accesses stay uniform).  kMask:
+// some row of the CTA attends to fewer than all 256 keys of the chunk.  On
+// return m is the row's maximum, and w01 (lower half) the sum of groups 0 and
+// 1; the upper half has left groups 2 and 3 in xsum.  P sits in TMEM columns
+// [16 c, 16 c + 16) for key group c of 16 keys: 8 packed hi pairs, then 8 lo.
+// The maximum is taken over the raw dot products and scaled once: rounding
+// is monotone and scale > 0, so max_j fl(s_j * scale) = fl(max_j s_j * scale).
+template <bool kMask, int DH>
+__device__ __forceinline__ void softmax_half(Smem<DH>& sm, uint32_t tmem, int half, int row, int32_t n_max,
+                                             int32_t ncol, float scale, float& m_out, float& w01) {
+    const int c_lo = 64 * half, c_hi = 128 + 64 * half;  // this thread's key ranges (64 keys each)
+    const uint32_t base = lane_addr(tmem, kColS);
+    // pass 1: the row's maximum over its keys
+    float mx = -INFINITY;
 #pragma unroll
-            for (int j = 0; j < 16; ++j)
-                O[j] = __float_as_uint(__fadd_rn(__fmul_rn(__uint_as_float(O[j]), a),
-                                                 __fmul_rn(__uint_as_float(o[j]), b)));
-        tmem_st16(lane_addr(tmem, kColRun + c0), first ? o : O);
+    for (int rg = 0; rg < 2; ++rg) {
+        const int c0 = rg == 0 ? c_lo : c_hi;
+        if (c0 < n_max) {
+            uint32_t r[64];
+            tmem_ld32(base + c0, r);
+            tmem_ld32(base + c0 + 32, r + 32);
+            ptx::tmem_ld_wait();
+#pragma unroll
+            for (int i = 0; i < 64; ++i)
+                if (!kMask || c0 + i < ncol) mx = fmaxf(mx, __uint_as_float(r[i]));
+        }
+    }
+    sm.xmax[half][row] = mx;
+    __syncthreads();
+    const float m = ncol > 0 ? __fmul_rn(fmaxf(sm.xmax[0][row], sm.xmax[1][row]), scale) : 0.0f;
+    // pass 2: p, its hi/lo pairs and the group sums, 16 keys of each range at a time
+    float w0 = 0.0f, w1 = 0.0f;
+#pragma unroll 1
+    for (int gi = 0; gi < 2; ++gi) {
+        const int b = 2 * half + gi;  // key group: keys 32b + i and 128 + 32b + i
+        float u[16];                  // after the second 16 keys: the butterfly's first level (i, i + 16)
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+            const int ca = 32 * b + 16 * q, cb = 128 + 32 * b + 16 * q;
+            uint32_t ra[16], rb[16];
+            if (ca < n_max) ptx::tmem_ld16(base + ca, ra);
+            if (cb < n_max) ptx::tmem_ld16(base + cb, rb);
+            ptx::tmem_ld_wait();
+            uint32_t wa[16], wb[16];  // P words of keys ca .. ca + 15 and cb .. cb + 15
+#pragma unroll
+            for (int j = 0; j < 16; j += 2) {
+                float pa[2], pb[2];
+#pragma unroll
+                for (int x = 0; x < 2; ++x) {
+                    const int i = j + x;
+                    float sa = ca < n_max ? __fmul_rn(__uint_as_float(ra[i]), scale) : -INFINITY;
+                    float sb = cb < n_max ? __fmul_rn(__uint_as_float(rb[i]), scale) : -INFINITY;
+                    if (kMask) {
+                        if (ca + i >= ncol) sa = -INFINITY;
+                        if (cb + i >= ncol) sb = -INFINITY;
+                    }
+                    pa[x] = attn_exp(__fsub_rn(sa, m));
+                    pb[x] = attn_exp(__fsub_rn(sb, m));
+                    // decode adds both to 0; p >= 0 is never -0, so 0 + p = p exactly
+                    const float pair = __fadd_rn(pa[x], pb[x]);
+                    u[i] = q == 0 ? pair : __fadd_rn(u[i], pair);
+                }
+                pack_p(pa[0], pa[1], wa[j / 2], wa[8 + j / 2]);
+                pack_p(pb[0], pb[1], wb[j / 2], wb[8 + j / 2]);
+            }
+            if (ca < n_max) tmem_st16(base + ca, wa);
+            if (cb < n_max) tmem_st16(base + cb, wb);
+        }
+#pragma unroll
+        for (int off = 8; off >= 1; off >>= 1)
+#pragma unroll
+            for (int i = 0; i < off; ++i) u[i] = __fadd_rn(u[i], u[i + off]);
+        if (gi == 0)
+            w0 = u[0];
+        else
+            w1 = u[0];
+    }
+    m_out = m;
+    if (half == 0) {
+        w01 = __fadd_rn(w0, w1);
+    } else {
+        sm.xsum[0][row] = w0;
+        sm.xsum[1][row] = w1;
+        w01 = 0.0f;
     }
 }
 
@@ -245,8 +281,8 @@ __device__ __forceinline__ void issue_chunk(uint8_t (*dst)[kKeyRegion], const CU
 }
 
 // Every thread: bounded wait on bar's phase; the outcome is the same in every
-// thread (a failure anywhere fails the block).
-// The phase advances only on success, so a later drain waits on the same one.
+// thread (a failure anywhere fails the block).  The phase advances only on
+// success, so a later drain waits on the same one.
 __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t& phase, volatile int32_t* abort) {
     const bool ok = __syncthreads_or(!ptx::mbar_wait_bounded(bar, phase, abort)) == 0;
     if (ok) phase ^= 1u;
@@ -261,13 +297,15 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     pdl_wait();
     constexpr int NT = kRows / G;
     constexpr int kRegions = DH / 64;
+    constexpr int kHalfDims = DH / 2;  // head dims of o and O per thread
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     Smem<DH>& sm = *reinterpret_cast<Smem<DH>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
+    const int half = warp >> 2;                  // which half of the row's keys and dims
+    const int row = 32 * (warp & 3) + lane;      // the row, = its TMEM lane
     const int32_t g = blockIdx.y;
     const int32_t e_begin = static_cast<int32_t>(blockIdx.x) * NT;
     const int32_t e_end = min(e_begin + NT, n_entries);
-    __shared__ int32_t red[kThreads / 32];
     if (tid == 0) {
         sm.abort = 0;
         ptx::mbar_init(&sm.k_full, 1);
@@ -286,16 +324,27 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     const uint32_t tmem = sm.tmem_base;
     const uint32_t idesc_s = ptx::idesc_bf16_f32(kRows, kChunk);
     const uint32_t idesc_pv = ptx::idesc_bf16_f32(kRows, DH) | (1u << 16);  // B (V) MN-major
+    const uint32_t col_o = kColO + half * kHalfDims, col_run = kColRun + half * kHalfDims;
     uint32_t ph_k = 0, ph_v = 0, ph_s = 0, ph_pv = 0;
     // outstanding asynchronous work, tracked alike in every thread
     bool k_pending = false, v_pending = false, s_pending = false, pv_pending = false;
     bool ok = true;
 
+    auto issue_s = [&]() {  // thread 0: S = Q K^T of the chunk in sm.k
+#pragma unroll
+        for (int ks = 0; ks < DH / 16; ++ks) {
+            const uint32_t step = static_cast<uint32_t>((ks % 4) * 32);
+            ptx::tc_mma_f16<1>(tmem + kColS, desc(smem_u32(&sm.q[ks / 4][0]) + step, 16, 1024),
+                               desc(smem_u32(&sm.k[ks / 4][0]) + step, 16, 1024), idesc_s, ks > 0);
+        }
+        ptx::tc_commit<1>(&sm.s_done);
+    };
+
     for (int32_t e0 = e_begin; e0 < e_end && ok;) {
         // a run of consecutive entries of one request; this thread's row is
-        // token e0 + tid / G, head tid % G
+        // token e0 + row / G, head row % G
         const Entry first = get_entry(em, e0);
-        const int32_t ti = tid / G;
+        const int32_t ti = row / G;
         Entry en{-1, -1, -1};
         if (e0 + ti < e_end) en = get_entry(em, e0 + ti);
         const bool mine = e0 + ti < e_end && en.r == first.r;
@@ -303,25 +352,39 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         if (mine) {
             const int32_t s_len = en.p + 1;
             const bool valid = en.p >= 0 && (s_len + BI_PAGE - 1) / BI_PAGE <= geo.max_pages;
-            if (!valid && tid % G == 0) report(geo.status, BI_DEV_BAD_POSITION);
+            if (!valid && half == 0 && row % G == 0) report(geo.status, BI_DEV_BAD_POSITION);
             keys = valid ? s_len : 0;
         }
-        const int32_t run_tokens = __syncthreads_count(mine && tid % G == 0);
+        const int32_t run_tokens = __syncthreads_count(mine && half == 0 && row % G == 0);
         const int32_t wmax = __reduce_max_sync(0xffffffffu, keys);
-        if (lane == 0) red[warp] = wmax;
-        // Q rows, K-major with the 128-byte swizzle (rows outside the run: zeros)
-        const uint16_t* qrow = reinterpret_cast<const uint16_t*>(geo.q) +
-                               (static_cast<int64_t>(mine ? en.t : 0) * geo.H + static_cast<int64_t>(g) * G + tid % G) * DH;
-#pragma unroll
-        for (int c = 0; c < DH / 8; ++c) {
-            const uint4 v = mine ? *reinterpret_cast<const uint4*>(qrow + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(&sm.q[c >> 3][sw128(tid, c)]) = v;
+        const int32_t wmin = __reduce_min_sync(0xffffffffu, mine ? keys : INT_MAX);
+        if (lane == 0) {
+            sm.red_max[warp] = wmax;
+            sm.red_min[warp] = wmin;
         }
-        ptx::fence_proxy_async_smem();
-        __syncthreads();
-        int32_t s_max = red[0];
+        // Q rows, K-major with the 128-byte swizzle (rows outside the run:
+        // zeros); this thread writes its half of the row's dims
+        const uint16_t* qrow = reinterpret_cast<const uint16_t*>(geo.q) +
+                               (static_cast<int64_t>(mine ? en.t : 0) * geo.H + static_cast<int64_t>(g) * G + row % G) * DH;
 #pragma unroll
-        for (int w = 1; w < kThreads / 32; ++w) s_max = max(s_max, red[w]);
+        for (int cc = 0; cc < DH / 16; ++cc) {
+            const int c = half * (DH / 16) + cc;
+            const uint4 v = mine ? *reinterpret_cast<const uint4*>(qrow + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
+            *reinterpret_cast<uint4*>(&sm.q[c >> 3][sw128(row, c)]) = v;
+        }
+        // this chunk's o starts at zero
+        zero_cols<kHalfDims>(lane_addr(tmem, col_o));
+        ptx::fence_proxy_async_smem();
+        tmem_st_wait();
+        ptx::tc_fence_before();
+        __syncthreads();
+        ptx::tc_fence_after();
+        int32_t s_max = sm.red_max[0], s_min = sm.red_min[0];
+#pragma unroll
+        for (int w = 1; w < kThreads / 32; ++w) {
+            s_max = max(s_max, sm.red_max[w]);
+            s_min = min(s_min, sm.red_min[w]);
+        }
         const int32_t count = (s_max + kChunk - 1) / kChunk;
         const int32_t* page_row = geo.page_table + static_cast<int64_t>(first.r) * geo.max_pages;
         if (tid == 0 && count > 0) {
@@ -329,25 +392,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             issue_chunk<DH>(sm.v, &tmV, &sm.v_full, page_row, 0, min(kChunk, s_max), g, geo);
         }
         k_pending = v_pending = count > 0;
+        if (count > 0) {
+            if (!(ok = wait_all(&sm.k_full, ph_k, &sm.abort))) break;
+            k_pending = false;
+            ptx::tc_fence_after();
+            if (tid == 0) issue_s();
+            s_pending = true;
+        }
         float M = 0.0f, L = 0.0f;
         for (int32_t j = 0; j < count && ok; ++j) {
             const int32_t k0 = j * kChunk;
             const int32_t n_max = min(kChunk, s_max - k0);
             const int32_t ncol = mine ? min(max(keys - k0, 0), kChunk) : 0;
-            // S = Q K^T over the chunk's 256 key rows (rows past n_max are masked below)
-            if (!(ok = wait_all(&sm.k_full, ph_k, &sm.abort))) break;
-            k_pending = false;
-            ptx::tc_fence_after();
-            if (tid == 0) {
-#pragma unroll
-                for (int ks = 0; ks < DH / 16; ++ks) {
-                    const uint32_t step = static_cast<uint32_t>((ks % 4) * 32);
-                    ptx::tc_mma_f16<1>(tmem + kColS, desc(smem_u32(&sm.q[ks / 4][0]) + step, 16, 1024),
-                                       desc(smem_u32(&sm.k[ks / 4][0]) + step, 16, 1024), idesc_s, ks > 0);
-                }
-                ptx::tc_commit<1>(&sm.s_done);
-            }
-            s_pending = true;
+            const bool masked = k0 + kChunk > s_min;  // some row of the run stops inside this chunk
             if (!(ok = wait_all(&sm.s_done, ph_s, &sm.abort))) break;
             s_pending = false;
             ptx::tc_fence_after();
@@ -356,9 +413,11 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 issue_chunk<DH>(sm.k, &tmK, &sm.k_full, page_row, k0 + kChunk, min(kChunk, s_max - k0 - kChunk), g,
                                 geo);
             k_pending = j + 1 < count;
-            float m, l;
-            softmax_chunk(tmem, n_max, ncol, geo.scale, m, l);
-            tmem_zero<DH>(tmem, kColO);
+            float m, w01;
+            if (masked)
+                softmax_half<true, DH>(sm, tmem, half, row, n_max, ncol, geo.scale, m, w01);
+            else
+                softmax_half<false, DH>(sm, tmem, half, row, n_max, ncol, geo.scale, m, w01);
             if (!(ok = wait_all(&sm.v_full, ph_v, &sm.abort))) break;
             v_pending = false;
             // V rows past the last key up to the 16-key step meet p = 0 in the MMAs:
@@ -375,6 +434,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             ptx::tc_fence_before();
             __syncthreads();
             ptx::tc_fence_after();
+            // l in the decode routine's order: ((group 0 + group 1) + group 2) + group 3
+            const float l = half == 0 ? __fadd_rn(__fadd_rn(w01, sm.xsum[0][row]), sm.xsum[1][row]) : 0.0f;
             // o = P V: per 16-key step the hi part, then the lo part
             if (tid == 0) {
                 const int steps = (n_max + 15) / 16;
@@ -389,32 +450,77 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             if (!(ok = wait_all(&sm.pv_done, ph_pv, &sm.abort))) break;
             pv_pending = false;
             ptx::tc_fence_after();
-            // the V buffer is free: the next chunk's V pages
+            // the V buffer is free: the next chunk's V pages; the S buffer is
+            // free: the next chunk's scores while this chunk is folded
             if (tid == 0 && j + 1 < count)
                 issue_chunk<DH>(sm.v, &tmV, &sm.v_full, page_row, k0 + kChunk, min(kChunk, s_max - k0 - kChunk), g,
                                 geo);
             v_pending = j + 1 < count;
-            fold_chunk<DH>(tmem, j == 0, ncol > 0, m, l, M, L);
+            if (j + 1 < count) {
+                if (!(ok = wait_all(&sm.k_full, ph_k, &sm.abort))) break;
+                k_pending = false;
+                ptx::tc_fence_after();
+                if (tid == 0) issue_s();
+                s_pending = true;
+            }
+            // the decode merge's fold; a row without keys in this chunk keeps its state
+            const bool active = ncol > 0;
+            float a = 1.0f, bw = 1.0f;
+            if (active) {
+                if (j == 0) {
+                    M = m;
+                    L = l;
+                } else {
+                    const float Mn = fmaxf(M, m);
+                    a = attn_exp(__fsub_rn(M, Mn));
+                    bw = attn_exp(__fsub_rn(m, Mn));
+                    L = __fadd_rn(__fmul_rn(L, a), __fmul_rn(l, bw));
+                    M = Mn;
+                }
+            }
+#pragma unroll
+            for (int c0 = 0; c0 < kHalfDims; c0 += 32) {
+                uint32_t o[32], O[32];
+                tmem_ld32(lane_addr(tmem, col_o + c0), o);
+                if (j > 0) tmem_ld32(lane_addr(tmem, col_run + c0), O);
+                ptx::tmem_ld_wait();
+                if (j > 0) {
+                    if (active)
+#pragma unroll
+                        for (int x = 0; x < 32; ++x)
+                            O[x] = __float_as_uint(__fadd_rn(__fmul_rn(__uint_as_float(O[x]), a),
+                                                             __fmul_rn(__uint_as_float(o[x]), bw)));
+                    tmem_st32(lane_addr(tmem, col_run + c0), O);
+                } else {
+                    tmem_st32(lane_addr(tmem, col_run + c0), o);
+                }
+            }
+            zero_cols<kHalfDims>(lane_addr(tmem, col_o));  // the next chunk's o starts at zero
             tmem_st_wait();
             ptx::tc_fence_before();
         }
-        if (ok) {
-            // out = O / L; a row without keys gets zeros
-            ptx::tc_fence_after();
-            const int64_t obase = (static_cast<int64_t>(mine ? en.t : 0) * geo.H + static_cast<int64_t>(g) * G + tid % G) * DH;
-#pragma unroll 1
-            for (int c0 = 0; c0 < DH; c0 += 16) {
-                uint32_t O[16];
-                ptx::tmem_ld16(lane_addr(tmem, kColRun + c0), O);
-                ptx::tmem_ld_wait();
-                if (mine)
+        if (!ok) break;
+        // out = O / L (the lower half's L); a row without keys gets zeros
+        if (half == 0) sm.xL[row] = L;
+        ptx::tc_fence_before();
+        __syncthreads();
+        ptx::tc_fence_after();
+        const float Lr = sm.xL[row];
+        const int64_t obase = (static_cast<int64_t>(mine ? en.t : 0) * geo.H + static_cast<int64_t>(g) * G + row % G) * DH +
+                              half * kHalfDims;
 #pragma unroll
-                    for (int j = 0; j < 16; j += 2) {
-                        const float a = keys > 0 && count > 0 ? __fdiv_rn(__uint_as_float(O[j]), L) : 0.0f;
-                        const float b = keys > 0 && count > 0 ? __fdiv_rn(__uint_as_float(O[j + 1]), L) : 0.0f;
-                        store_out2(geo.out, geo.out_f32, obase + c0 + j, a, b);
-                    }
-            }
+        for (int c0 = 0; c0 < kHalfDims; c0 += 32) {
+            uint32_t O[32];
+            tmem_ld32(lane_addr(tmem, col_run + c0), O);
+            ptx::tmem_ld_wait();
+            if (mine)
+#pragma unroll
+                for (int x = 0; x < 32; x += 2) {
+                    const bool has = keys > 0 && count > 0;
+                    const float o0 = has ? __fdiv_rn(__uint_as_float(O[x]), Lr) : 0.0f;
+                    const float o1 = has ? __fdiv_rn(__uint_as_float(O[x + 1]), Lr) : 0.0f;
+                    store_out2(geo.out, geo.out_f32, obase + c0 + x, o0, o1);
+                }
         }
         ptx::tc_fence_before();
         __syncthreads();
