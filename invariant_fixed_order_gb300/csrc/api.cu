@@ -242,7 +242,7 @@ extern "C" bi_status bi_prefill_attention(const bi_bf16* q, const int32_t* cu_q,
     EntryMap em{2, cu_q, q_pos0, nullptr, B};
     cudaError_t e;
     if (mode == BI_INVARIANT) {
-        e = launch_prefill_attention(g, em, T, static_cast<cudaStream_t>(stream));
+        e = launch_prefill_attention(g, em, T, T, static_cast<cudaStream_t>(stream));
     } else {
         // every query as a decode entry whose pieces follow the occupancy rule of this batch
         int32_t max_splits = 0, chunk2 = 0;
@@ -572,7 +572,7 @@ extern "C" bi_status bi_forward_step(bi_model* m, const bi_batch* batch, const b
         }
         if (T - nd > 0) {
             EntryMap em{1, d_pre, d_req, d_pos, b.B};
-            BI_TRY_CUDA(launch_prefill_attention(g, em, T - nd, s), "prefill attention");
+            BI_TRY_CUDA(launch_prefill_attention(g, em, T - nd, T, s), "prefill attention");
         }
         BI_TRY(run_gemm(attn, m->w_o[l], x, BI_BF16, x, BI_EP_RESIDUAL, T, c.d, c.H * c.Dh, mode, gws, gws_bytes,
                         dev_status, s, true));

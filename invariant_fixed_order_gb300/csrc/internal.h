@@ -157,7 +157,8 @@ void variant_split_plan(int32_t B, int32_t H, int32_t Hkv, int32_t max_seq, int3
 cudaError_t launch_decode_attention(const AttnGeom& g, const EntryMap& em, int32_t n_entries,
                                     int32_t max_splits, int32_t variant_chunk2, float* ws_o,
                                     float* ws_ml, cudaStream_t s, bool early_kv = false);
-cudaError_t launch_prefill_attention(const AttnGeom& g, const EntryMap& em, int32_t n_entries,
+// q_rows: rows of g.q (every token index an entry names is below it)
+cudaError_t launch_prefill_attention(const AttnGeom& g, const EntryMap& em, int32_t n_entries, int32_t q_rows,
                                      cudaStream_t s);
 bool attention_supported(int32_t H, int32_t Hkv, int32_t Dh);
 
@@ -165,6 +166,11 @@ bool attention_supported(int32_t H, int32_t Hkv, int32_t Dh);
 // of Dh bf16 (row (page * Hkv + head) * 16 + slot), boxes of 16 rows x 64
 // elements with the 128-byte swizzle (k_gemm.cu owns the driver entry point).
 bool encode_kv_map(CUtensorMap* map, const bi_bf16* cache, int64_t num_pages, int32_t Hkv, int32_t Dh);
+// Tensor map over queries q [rows, H, Dh] seen as three dimensions (Dh, H,
+// rows): a box of 64 elements x G heads x 128/G tokens brings the 128
+// (token, head) rows of one GQA group of consecutive tokens, each row's 64
+// elements as 128 bytes with the 128-byte swizzle.
+bool encode_q_map(CUtensorMap* map, const bi_bf16* q, int64_t rows, int32_t H, int32_t Dh, int32_t G);
 
 // ---- GEMM (k_gemm.cu) ----
 struct GemmPlan {

@@ -757,9 +757,10 @@ cudaError_t launch_decode_attention(const AttnGeom& g, const EntryMap& em, int32
 
 namespace bi {
 
-cudaError_t launch_prefill_attention(const AttnGeom& g, const EntryMap& em, int32_t n_entries, cudaStream_t s) {
+cudaError_t launch_prefill_attention(const AttnGeom& g, const EntryMap& em, int32_t n_entries, int32_t q_rows,
+                                     cudaStream_t s) {
     if (n_entries <= 0) return cudaSuccess;
-    BI_ATTN_DISPATCH(tc_prefill::launch_prefill_tc_t, g, em, n_entries, s);
+    BI_ATTN_DISPATCH(tc_prefill::launch_prefill_tc_t, g, em, n_entries, q_rows, s);
 }
 
 }  // namespace bi

@@ -677,6 +677,18 @@ bool encode_kv_map(CUtensorMap* map, const bi_bf16* cache, int64_t num_pages, in
               CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+bool encode_q_map(CUtensorMap* map, const bi_bf16* q, int64_t rows, int32_t H, int32_t Dh, int32_t G) {
+    auto fn = encode_fn();
+    if (!fn || G <= 0 || 128 % G != 0 || rows <= 0) return false;
+    cuuint64_t dims[3] = {static_cast<cuuint64_t>(Dh), static_cast<cuuint64_t>(H), static_cast<cuuint64_t>(rows)};
+    cuuint64_t strides[2] = {static_cast<cuuint64_t>(Dh) * 2, static_cast<cuuint64_t>(H) * Dh * 2};
+    cuuint32_t box[3] = {64, static_cast<cuuint32_t>(G), static_cast<cuuint32_t>(128 / G)};
+    cuuint32_t estr[3] = {1, 1, 1};
+    return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<bi_bf16*>(q), dims, strides, box, estr,
+              CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 GemmPlan gemm_plan(int64_t M, int32_t N, int32_t K, bi_mode mode) {
     GemmPlan p{1};
     if (mode != BI_VARIANT || M <= 0) return p;

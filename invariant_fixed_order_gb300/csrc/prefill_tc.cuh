@@ -7,9 +7,10 @@
 // quarter), each taking half of the row's keys and half of its head dims.
 // Chunks of 256 keys from key 0 are walked in order; per chunk:
 //   S = Q K^T            tcgen05, M = 128 rows, N = 256 keys, K = Dh in 16-deep
-//                        steps; A = Q (K-major, 128-byte swizzle, loaded once per
-//                        run of tokens), B = the chunk's K pages (TMA page boxes)
-//                        -> TMEM columns [0, 256)
+//                        steps; A = Q (K-major, 128-byte swizzle, one TMA box per
+//                        64 dims and run of tokens), B = the chunk's keys (K-major,
+//                        128-byte swizzle, gathered from their pages by 16-byte
+//                        cp.async copies of every thread) -> TMEM columns [0, 256)
 //   softmax per row      score = fl(acc * scale) (or -inf past the row's keys);
 //                        m = max; p = exp(score - m); hi = bf16(p), lo =
 //                        bf16(p - hi); l summed in the decode routine's tree:
@@ -21,13 +22,16 @@
 //                        and group sums meet in shared memory.  hi/lo pairs go
 //                        back into TMEM in place of the scores, as the A operand
 //                        of the next product
-//   o = P V              tcgen05, A = P (TMEM), B = the chunk's V pages read
-//                        MN-major (head dims contiguous), per 16-key step the hi
+//   o = P V              tcgen05, A = P (TMEM), B = the chunk's values (gathered
+//                        like K) read MN-major (head dims contiguous), per 16-key step the hi
 //                        then the lo product, into an accumulator that starts
 //                        at zero -> TMEM columns [256, 256 + Dh)
 //   fold                 the decode merge's expressions into the running (M, L)
 //                        in registers and O in TMEM columns [384, 384 + Dh)
-// The next chunk's S product runs on the tensor cores while the fold runs.
+// The next chunk's S product runs on the tensor cores while the fold runs;
+// the next chunk's K and V copies fly during the softmax and the products.
+// CTAs are persistent: a run's first copies fly while the previous run's
+// output is written.
 // Outside the MMAs every step repeats the decode routine's arithmetic.  Inside
 // them, a tcgen05 kind::f16 chain of 16-deep K steps gives the same fp32 bits
 // as the decode routine's mma.sync m16n8k16 chain over the same steps, for
@@ -62,7 +66,8 @@ struct Smem {
     uint8_t k[kRegions][kKeyRegion];       // 1024-aligned (first)
     uint8_t v[kRegions][kKeyRegion];
     uint8_t q[kRegions][kQRegion];
-    uint64_t k_full, v_full, s_done, pv_done;
+    uint8_t stage[kRows * DH * 2];         // output staging: bf16 rows, or half of the fp32 dims
+    uint64_t q_full, s_done, pv_done;
     uint32_t tmem_base;
     int32_t abort;
     float xmax[2][kRows];                  // each half's partial row maximum
@@ -70,6 +75,7 @@ struct Smem {
     float xL[kRows];                       // the row's final L, for the upper half's output
     int32_t red_max[kThreads / 32];
     int32_t red_min[kThreads / 32];
+    int32_t pg[4][kChunk / BI_PAGE];       // page-table entries of chunks c (slot c % 4), read ahead
 };
 
 // Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled region.
@@ -133,6 +139,14 @@ __device__ __forceinline__ void tmem_st16(uint32_t taddr, const uint32_t* v) {
 }
 __device__ __forceinline__ void tmem_st_wait() { asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory"); }
 
+// After tcgen05.wait::ld: ties each loaded register to that point, so no use
+// of it can be scheduled before the wait (the load writes it asynchronously).
+template <int N>
+__device__ __forceinline__ void reg_fence(uint32_t* r) {
+#pragma unroll
+    for (int i = 0; i < N; ++i) asm volatile("" : "+r"(r[i]));
+}
+
 // Writes zeros into N consecutive columns of this thread's lane from taddr.
 template <int N>
 __device__ __forceinline__ void zero_cols(uint32_t taddr) {
@@ -169,12 +183,65 @@ __device__ __forceinline__ void pack_p(float p0, float p1, uint32_t& hi, uint32_
 // [16 c, 16 c + 16) for key group c of 16 keys: 8 packed hi pairs, then 8 lo.
 // The maximum is taken over the raw dot products and scaled once: rounding
 // is monotone and scale > 0, so max_j fl(s_j * scale) = fl(max_j s_j * scale).
+// Reads one block of this thread's scores: keys ca .. ca + 15 and
+// ca + 128 .. ca + 143 (ca = 32 (2 half + gi) + 16 q); columns at or past n_max
+// are not read (zeros).  Completes at the next tcgen05.wait::ld.
+__device__ __forceinline__ void load_block(uint32_t base, int half, int gi, int q, int32_t n_max, uint32_t (&ra)[16],
+                                           uint32_t (&rb)[16]) {
+    const int ca = 32 * (2 * half + gi) + 16 * q, cb = 128 + ca;
+    if (ca < n_max) {
+        ptx::tmem_ld16(base + ca, ra);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) ra[i] = 0u;
+    }
+    if (cb < n_max) {
+        ptx::tmem_ld16(base + cb, rb);
+    } else {
+#pragma unroll
+        for (int i = 0; i < 16; ++i) rb[i] = 0u;
+    }
+}
+
+// p of one block (see load_block): P words back to TMEM in place of the
+// scores, pair sums p_i + p_(i+128) into u (kFirst: u = the pair sums; else
+// u += them, the butterfly's first level).
+template <bool kMask, bool kFirst>
+__device__ __forceinline__ void p_block(uint32_t base, int half, int gi, int q, int32_t n_max, int32_t ncol, float scale,
+                                        float m, const uint32_t (&ra)[16], const uint32_t (&rb)[16], float (&u)[16]) {
+    const int ca = 32 * (2 * half + gi) + 16 * q, cb = 128 + ca;
+    uint32_t wa[16], wb[16];  // P words of keys ca .. ca + 15 and cb .. cb + 15
+#pragma unroll
+    for (int j = 0; j < 16; j += 2) {
+        float pa[2], pb[2];
+#pragma unroll
+        for (int x = 0; x < 2; ++x) {
+            const int i = j + x;
+            float sa = ca < n_max ? __fmul_rn(__uint_as_float(ra[i]), scale) : -INFINITY;
+            float sb = cb < n_max ? __fmul_rn(__uint_as_float(rb[i]), scale) : -INFINITY;
+            if (kMask) {
+                if (ca + i >= ncol) sa = -INFINITY;
+                if (cb + i >= ncol) sb = -INFINITY;
+            }
+            pa[x] = attn_exp(__fsub_rn(sa, m));
+            pb[x] = attn_exp(__fsub_rn(sb, m));
+            // decode adds both to 0; p >= 0 is never -0, so 0 + p = p exactly
+            const float pair = __fadd_rn(pa[x], pb[x]);
+            u[i] = kFirst ? pair : __fadd_rn(u[i], pair);
+        }
+        pack_p(pa[0], pa[1], wa[j / 2], wa[8 + j / 2]);
+        pack_p(pb[0], pb[1], wb[j / 2], wb[8 + j / 2]);
+    }
+    if (ca < n_max) tmem_st16(base + ca, wa);
+    if (cb < n_max) tmem_st16(base + cb, wb);
+}
+
 template <bool kMask, int DH>
 __device__ __forceinline__ void softmax_half(Smem<DH>& sm, uint32_t tmem, int half, int row, int32_t n_max,
                                              int32_t ncol, float scale, float& m_out, float& w01) {
     const int c_lo = 64 * half, c_hi = 128 + 64 * half;  // this thread's key ranges (64 keys each)
     const uint32_t base = lane_addr(tmem, kColS);
-    // pass 1: the row's maximum over its keys
+    // pass 1: the row's maximum over its keys, 64 at a time
     float mx = -INFINITY;
 #pragma unroll
     for (int rg = 0; rg < 2; ++rg) {
@@ -184,6 +251,7 @@ __device__ __forceinline__ void softmax_half(Smem<DH>& sm, uint32_t tmem, int ha
             tmem_ld32(base + c0, r);
             tmem_ld32(base + c0 + 32, r + 32);
             ptx::tmem_ld_wait();
+            reg_fence<64>(r);
 #pragma unroll
             for (int i = 0; i < 64; ++i)
                 if (!kMask || c0 + i < ncol) mx = fmaxf(mx, __uint_as_float(r[i]));
@@ -192,44 +260,24 @@ __device__ __forceinline__ void softmax_half(Smem<DH>& sm, uint32_t tmem, int ha
     sm.xmax[half][row] = mx;
     __syncthreads();
     const float m = ncol > 0 ? __fmul_rn(fmaxf(sm.xmax[0][row], sm.xmax[1][row]), scale) : 0.0f;
-    // pass 2: p, its hi/lo pairs and the group sums, 16 keys of each range at a time
+    // pass 2: p, its hi/lo pairs and the group sums, 16 keys of each range at
+    // a time; the next block's scores are read while this block is computed
     float w0 = 0.0f, w1 = 0.0f;
+    uint32_t xa[16], xb[16], ya[16], yb[16];  // two blocks of scores: keys ca.. and cb..
+    load_block(base, half, 0, 0, n_max, xa, xb);
 #pragma unroll 1
     for (int gi = 0; gi < 2; ++gi) {
-        const int b = 2 * half + gi;  // key group: keys 32b + i and 128 + 32b + i
-        float u[16];                  // after the second 16 keys: the butterfly's first level (i, i + 16)
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-            const int ca = 32 * b + 16 * q, cb = 128 + 32 * b + 16 * q;
-            uint32_t ra[16], rb[16];
-            if (ca < n_max) ptx::tmem_ld16(base + ca, ra);
-            if (cb < n_max) ptx::tmem_ld16(base + cb, rb);
-            ptx::tmem_ld_wait();
-            uint32_t wa[16], wb[16];  // P words of keys ca .. ca + 15 and cb .. cb + 15
-#pragma unroll
-            for (int j = 0; j < 16; j += 2) {
-                float pa[2], pb[2];
-#pragma unroll
-                for (int x = 0; x < 2; ++x) {
-                    const int i = j + x;
-                    float sa = ca < n_max ? __fmul_rn(__uint_as_float(ra[i]), scale) : -INFINITY;
-                    float sb = cb < n_max ? __fmul_rn(__uint_as_float(rb[i]), scale) : -INFINITY;
-                    if (kMask) {
-                        if (ca + i >= ncol) sa = -INFINITY;
-                        if (cb + i >= ncol) sb = -INFINITY;
-                    }
-                    pa[x] = attn_exp(__fsub_rn(sa, m));
-                    pb[x] = attn_exp(__fsub_rn(sb, m));
-                    // decode adds both to 0; p >= 0 is never -0, so 0 + p = p exactly
-                    const float pair = __fadd_rn(pa[x], pb[x]);
-                    u[i] = q == 0 ? pair : __fadd_rn(u[i], pair);
-                }
-                pack_p(pa[0], pa[1], wa[j / 2], wa[8 + j / 2]);
-                pack_p(pb[0], pb[1], wb[j / 2], wb[8 + j / 2]);
-            }
-            if (ca < n_max) tmem_st16(base + ca, wa);
-            if (cb < n_max) tmem_st16(base + cb, wb);
-        }
+        float u[16];  // after the second block: the butterfly's first level (i, i + 16)
+        ptx::tmem_ld_wait();
+        reg_fence<16>(xa);
+        reg_fence<16>(xb);
+        load_block(base, half, gi, 1, n_max, ya, yb);
+        p_block<kMask, true>(base, half, gi, 0, n_max, ncol, scale, m, xa, xb, u);
+        ptx::tmem_ld_wait();
+        reg_fence<16>(ya);
+        reg_fence<16>(yb);
+        if (gi == 0) load_block(base, half, 1, 0, n_max, xa, xb);
+        p_block<kMask, false>(base, half, gi, 1, n_max, ncol, scale, m, ya, yb, u);
 #pragma unroll
         for (int off = 8; off >= 1; off >>= 1)
 #pragma unroll
@@ -257,27 +305,50 @@ __device__ __forceinline__ void softmax_half(Smem<DH>& sm, uint32_t tmem, int ha
 constexpr uint32_t kVLbo = kKeyRegion;
 constexpr uint32_t kVSbo = 1024;
 
-// Thread 0: TMA page boxes of keys [k0, k0 + n) of KV head g into a chunk
-// buffer (one box per 16-key page and 64-dim region), counted on bar.
+// Every thread: its share of the 16-byte copies (cp.async) that bring keys
+// [k0, k0 + n) of KV head g into a chunk buffer, in the 128-byte-swizzled
+// layout of a TMA page box (rows of 64 dims, regions of 64 dims kKeyRegion
+// apart); committed as one group.  pages: the chunk's page-table entries (in
+// shared memory, read ahead).  Sixteen consecutive threads copy one key's row,
+// so each read is a contiguous 256-byte (DH = 128) run of its page.  Keys past
+// n are not copied.
 template <int DH>
-__device__ __forceinline__ void issue_chunk(uint8_t (*dst)[kKeyRegion], const CUtensorMap* map, uint64_t* bar,
-                                            const int32_t* page_row, int32_t k0, int32_t n, int32_t g,
-                                            const AttnGeom& geo) {
-    constexpr int kRegions = DH / 64;
-    const int32_t np = (n + BI_PAGE - 1) / BI_PAGE;
-    ptx::fence_proxy_async_smem();  // earlier generic writes to the buffer before the copies
-    ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(np * kRegions * BI_PAGE * 128));
-    for (int i = 0; i < np; ++i) {
-        const int32_t lp = k0 / BI_PAGE + i;
-        int32_t pg = lp < geo.max_pages ? page_row[lp] : -1;
-        if (pg < 0 || pg >= geo.num_pages) {
-            report(geo.status, BI_DEV_BAD_PAGE);
-            pg = 0;
-        }
-        const int32_t y = (pg * geo.Hkv + g) * BI_PAGE;
+__device__ __forceinline__ void load_chunk(uint8_t (*dst)[kKeyRegion], const uint16_t* __restrict__ cache,
+                                           const int32_t* pages, int32_t k0, int32_t n, int32_t g,
+                                           const AttnGeom& geo) {
+    constexpr int kCPR = DH / 8;                 // 16-byte chunks per key row
+    constexpr int kIters = kChunk * kCPR / kThreads;
 #pragma unroll
-        for (int h = 0; h < kRegions; ++h) ptx::tma_load_2d(&dst[h][i * BI_PAGE * 128], map, bar, h * 64, y);
+    for (int it = 0; it < kIters; ++it) {
+        const int i = static_cast<int>(threadIdx.x) + it * kThreads;
+        const int key = i / kCPR, c = i % kCPR;
+        if (key < n) {
+            int32_t pg = pages[key / BI_PAGE];
+            if (pg < 0 || pg >= geo.num_pages) {
+                report(geo.status, BI_DEV_BAD_PAGE);
+                pg = 0;
+            }
+            const uint16_t* src =
+                cache + ((static_cast<int64_t>(pg) * geo.Hkv + g) * BI_PAGE + ((k0 + key) & (BI_PAGE - 1))) * DH + c * 8;
+            cp_async16(&dst[c >> 3][sw128(key, c & 7)], src);
+        }
     }
+    cp_async_commit();
+}
+
+// Page-table entry lp of a request's row (raw; checked where it is used), or
+// -1 past the row.
+__device__ __forceinline__ int32_t read_page(const int32_t* page_row, int32_t lp, int32_t max_pages) {
+    return lp < max_pages ? __ldg(page_row + lp) : -1;
+}
+
+// The copies of this thread's groups older than the newest `newer` are
+// complete; after the barrier that follows, every thread's are, and the
+// tensor cores may read them.
+template <int kNewer>
+__device__ __forceinline__ void copies_landed() {
+    asm volatile("cp.async.wait_group %0;" ::"n"(kNewer) : "memory");
+    ptx::fence_proxy_async_smem();  // generic-proxy writes before the MMAs read them
 }
 
 // Every thread: bounded wait on bar's phase; the outcome is the same in every
@@ -289,10 +360,75 @@ __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t& phase, volatil
     return ok;
 }
 
+// A finished run whose output is still in tensor memory (running O).
+struct PendingOut {
+    bool on;
+    int32_t t0, tokens, g;  // first token, tokens of the run, KV head
+};
+
+// out = O / L of a finished run, staged through shared memory and written
+// with 16-byte stores.  Every thread takes part: each writes its half of its
+// row (a row without keys: zeros), then all copy whole rows out.  bf16 rows
+// fit the stage at once, fp32 rows in two passes of half the dims.
+template <int G, int DH>
+__device__ __forceinline__ void write_out(Smem<DH>& sm, uint32_t tmem, const AttnGeom& geo, const PendingOut& po,
+                                          int half, int row, bool has, float L_lower) {
+    constexpr int kHalfDims = DH / 2;
+    constexpr int kCPR = DH / 8;  // 16-byte chunks per stage row (DH * 2 bytes)
+    const float L = half == 0 ? L_lower : sm.xL[row];
+    const int passes = geo.out_f32 ? 2 : 1;
+    const int esize = geo.out_f32 ? 4 : 2;
+    for (int p = 0; p < passes; ++p) {
+        if (!geo.out_f32 || half == p) {
+#pragma unroll
+            for (int c0 = 0; c0 < kHalfDims; c0 += 32) {
+                uint32_t O[32];
+                tmem_ld32(lane_addr(tmem, kColRun + half * kHalfDims + c0), O);
+                ptx::tmem_ld_wait();
+                reg_fence<32>(O);
+                float val[32];
+#pragma unroll
+                for (int x = 0; x < 32; ++x) val[x] = has ? __fdiv_rn(__uint_as_float(O[x]), L) : 0.0f;
+                if (geo.out_f32) {
+#pragma unroll
+                    for (int c = 0; c < 8; ++c) {
+                        const int cc = c0 / 4 + c;
+                        *reinterpret_cast<uint4*>(&sm.stage[row * DH * 2 + ((cc ^ (row % kCPR)) << 4)]) =
+                            make_uint4(__float_as_uint(val[4 * c]), __float_as_uint(val[4 * c + 1]),
+                                       __float_as_uint(val[4 * c + 2]), __float_as_uint(val[4 * c + 3]));
+                    }
+                } else {
+#pragma unroll
+                    for (int c = 0; c < 4; ++c) {
+                        const int cc = half * (kHalfDims / 8) + c0 / 8 + c;
+                        *reinterpret_cast<uint4*>(&sm.stage[row * DH * 2 + ((cc ^ (row % kCPR)) << 4)]) =
+                            make_uint4(pack_bf16x2(val[8 * c], val[8 * c + 1]),
+                                       pack_bf16x2(val[8 * c + 2], val[8 * c + 3]),
+                                       pack_bf16x2(val[8 * c + 4], val[8 * c + 5]),
+                                       pack_bf16x2(val[8 * c + 6], val[8 * c + 7]));
+                    }
+                }
+            }
+        }
+        __syncthreads();
+        for (int k = threadIdx.x; k < kRows * kCPR; k += kThreads) {
+            const int r = k / kCPR, c = k % kCPR;
+            const int ti = r / G;
+            if (ti < po.tokens) {
+                const int64_t orow = static_cast<int64_t>(po.t0 + ti) * geo.H + static_cast<int64_t>(po.g) * G + r % G;
+                char* dst = reinterpret_cast<char*>(geo.out) + (orow * DH) * esize + p * (DH / 2) * 4 + c * 16;
+                *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&sm.stage[r * DH * 2 + ((c ^ (r % kCPR)) << 4)]);
+            }
+        }
+        __syncthreads();
+    }
+}
+
+// Persistent CTAs over tiles of (NT consecutive entries, one KV head); a
+// tile's entries are walked as runs of one request each.
 template <int G, int DH>
 __global__ void __launch_bounds__(kThreads, 1)
-prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV, AttnGeom geo,
-                  EntryMap em, int32_t n_entries) {
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, AttnGeom geo, EntryMap em, int32_t n_entries) {
     pdl_trigger();
     pdl_wait();
     constexpr int NT = kRows / G;
@@ -303,13 +439,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
     const int half = warp >> 2;                  // which half of the row's keys and dims
     const int row = 32 * (warp & 3) + lane;      // the row, = its TMEM lane
-    const int32_t g = blockIdx.y;
-    const int32_t e_begin = static_cast<int32_t>(blockIdx.x) * NT;
-    const int32_t e_end = min(e_begin + NT, n_entries);
+    const int32_t n_blocks = (n_entries + NT - 1) / NT;
+    const int32_t n_tiles = n_blocks * geo.Hkv;
     if (tid == 0) {
         sm.abort = 0;
-        ptx::mbar_init(&sm.k_full, 1);
-        ptx::mbar_init(&sm.v_full, 1);
+        ptx::prefetch_tmap(&tmQ);
+        ptx::mbar_init(&sm.q_full, 1);
         ptx::mbar_init(&sm.s_done, 1);
         ptx::mbar_init(&sm.pv_done, 1);
         ptx::fence_barrier_init();
@@ -325,10 +460,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     const uint32_t idesc_s = ptx::idesc_bf16_f32(kRows, kChunk);
     const uint32_t idesc_pv = ptx::idesc_bf16_f32(kRows, DH) | (1u << 16);  // B (V) MN-major
     const uint32_t col_o = kColO + half * kHalfDims, col_run = kColRun + half * kHalfDims;
-    uint32_t ph_k = 0, ph_v = 0, ph_s = 0, ph_pv = 0;
-    // outstanding asynchronous work, tracked alike in every thread
-    bool k_pending = false, v_pending = false, s_pending = false, pv_pending = false;
+    zero_cols<kHalfDims>(lane_addr(tmem, col_o));  // o starts at zero (and is zeroed after every fold)
+    const uint16_t* kc = reinterpret_cast<const uint16_t*>(geo.kc);
+    const uint16_t* vc = reinterpret_cast<const uint16_t*>(geo.vc);
+    uint32_t ph_q = 0, ph_s = 0, ph_pv = 0;
+    // outstanding asynchronous work, tracked alike in every thread (the K and V
+    // copies are cp.async groups of each thread, waited for in commit order)
+    bool q_pending = false, s_pending = false, pv_pending = false;
     bool ok = true;
+    PendingOut po{false, 0, 0, 0};
+    bool po_has = false;  // this thread's row of the pending run has keys
+    float po_L = 0.0f;
 
     auto issue_s = [&]() {  // thread 0: S = Q K^T of the chunk in sm.k
 #pragma unroll
@@ -340,18 +482,37 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         ptx::tc_commit<1>(&sm.s_done);
     };
 
-    for (int32_t e0 = e_begin; e0 < e_end && ok;) {
-        // a run of consecutive entries of one request; this thread's row is
-        // token e0 + row / G, head row % G
+    int32_t tile = blockIdx.x;
+    int32_t e0 = 0, e_end = 0, g = 0;
+    if (tile < n_tiles) {
+        g = tile % geo.Hkv;
+        e0 = (tile / geo.Hkv) * NT;
+        e_end = min(e0 + NT, n_entries);
+    }
+    while (tile < n_tiles && ok) {
+        // ---- a run of consecutive entries of one request: token first.t + row / G, head row % G ----
         const Entry first = get_entry(em, e0);
+        const int32_t* page_row = geo.page_table + static_cast<int64_t>(first.r) * geo.max_pages;
+        // the page-table entries of the run's first two chunks, in flight during the lookups below
+        const int32_t pg_first = tid < 2 * (kChunk / BI_PAGE) ? read_page(page_row, tid, geo.max_pages) : 0;
         const int32_t ti = row / G;
         Entry en{-1, -1, -1};
-        if (e0 + ti < e_end) en = get_entry(em, e0 + ti);
-        const bool mine = e0 + ti < e_end && en.r == first.r;
+        bool mine = false;
+        if (e0 + ti < e_end) {
+            if (em.kind == 2) {
+                // entries are tokens; the request's tokens end at cu_q[r + 1]
+                mine = e0 + ti < em.a[first.r + 1];
+                en = Entry{e0 + ti, first.r, first.p + ti};
+            } else {
+                en = get_entry(em, e0 + ti);
+                mine = en.r == first.r;
+            }
+        }
         int32_t keys = 0;
         if (mine) {
             const int32_t s_len = en.p + 1;
-            const bool valid = en.p >= 0 && (s_len + BI_PAGE - 1) / BI_PAGE <= geo.max_pages;
+            // the queries are read as one box of consecutive tokens from first.t
+            const bool valid = en.p >= 0 && (s_len + BI_PAGE - 1) / BI_PAGE <= geo.max_pages && en.t == first.t + ti;
             if (!valid && half == 0 && row % G == 0) report(geo.status, BI_DEV_BAD_POSITION);
             keys = valid ? s_len : 0;
         }
@@ -362,23 +523,8 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             sm.red_max[warp] = wmax;
             sm.red_min[warp] = wmin;
         }
-        // Q rows, K-major with the 128-byte swizzle (rows outside the run:
-        // zeros); this thread writes its half of the row's dims
-        const uint16_t* qrow = reinterpret_cast<const uint16_t*>(geo.q) +
-                               (static_cast<int64_t>(mine ? en.t : 0) * geo.H + static_cast<int64_t>(g) * G + row % G) * DH;
-#pragma unroll
-        for (int cc = 0; cc < DH / 16; ++cc) {
-            const int c = half * (DH / 16) + cc;
-            const uint4 v = mine ? *reinterpret_cast<const uint4*>(qrow + 8 * c) : make_uint4(0u, 0u, 0u, 0u);
-            *reinterpret_cast<uint4*>(&sm.q[c >> 3][sw128(row, c)]) = v;
-        }
-        // this chunk's o starts at zero
-        zero_cols<kHalfDims>(lane_addr(tmem, col_o));
-        ptx::fence_proxy_async_smem();
-        tmem_st_wait();
-        ptx::tc_fence_before();
+        if (tid < 2 * (kChunk / BI_PAGE)) sm.pg[tid / (kChunk / BI_PAGE)][tid % (kChunk / BI_PAGE)] = pg_first;
         __syncthreads();
-        ptx::tc_fence_after();
         int32_t s_max = sm.red_max[0], s_min = sm.red_min[0];
 #pragma unroll
         for (int w = 1; w < kThreads / 32; ++w) {
@@ -386,15 +532,28 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             s_min = min(s_min, sm.red_min[w]);
         }
         const int32_t count = (s_max + kChunk - 1) / kChunk;
-        const int32_t* page_row = geo.page_table + static_cast<int64_t>(first.r) * geo.max_pages;
-        if (tid == 0 && count > 0) {
-            issue_chunk<DH>(sm.k, &tmK, &sm.k_full, page_row, 0, min(kChunk, s_max), g, geo);
-            issue_chunk<DH>(sm.v, &tmV, &sm.v_full, page_row, 0, min(kChunk, s_max), g, geo);
-        }
-        k_pending = v_pending = count > 0;
+        // this run's queries and first chunk: the buffers are free (the last
+        // products of the previous run have completed)
         if (count > 0) {
-            if (!(ok = wait_all(&sm.k_full, ph_k, &sm.abort))) break;
-            k_pending = false;
+            if (tid == 0) {
+                ptx::mbar_arrive_expect_tx(&sm.q_full, static_cast<uint32_t>(kRegions * kQRegion));
+#pragma unroll
+                for (int h = 0; h < kRegions; ++h)
+                    ptx::tma_load_3d(&sm.q[h][0], &tmQ, &sm.q_full, h * 64, g * G, first.t, ptx::policy_evict_first());
+            }
+            load_chunk<DH>(sm.k, kc, sm.pg[0], 0, min(kChunk, s_max), g, geo);
+            load_chunk<DH>(sm.v, vc, sm.pg[0], 0, min(kChunk, s_max), g, geo);
+            q_pending = true;
+        }
+        // the previous run's output, while this run's first copies are in flight
+        if (po.on) {
+            write_out<G, DH>(sm, tmem, geo, po, half, row, po_has, po_L);
+            po.on = false;
+        }
+        if (count > 0) {
+            copies_landed<1>();  // K (V is the newer group)
+            if (!(ok = wait_all(&sm.q_full, ph_q, &sm.abort))) break;
+            q_pending = false;
             ptx::tc_fence_after();
             if (tid == 0) issue_s();
             s_pending = true;
@@ -408,18 +567,19 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             if (!(ok = wait_all(&sm.s_done, ph_s, &sm.abort))) break;
             s_pending = false;
             ptx::tc_fence_after();
-            // the K buffer is free: the next chunk's K pages
-            if (tid == 0 && j + 1 < count)
-                issue_chunk<DH>(sm.k, &tmK, &sm.k_full, page_row, k0 + kChunk, min(kChunk, s_max - k0 - kChunk), g,
-                                geo);
-            k_pending = j + 1 < count;
+            // the K buffer is free: the next chunk's keys
+            if (j + 1 < count)
+                load_chunk<DH>(sm.k, kc, sm.pg[(j + 1) & 3], k0 + kChunk, min(kChunk, s_max - k0 - kChunk), g, geo);
             float m, w01;
             if (masked)
                 softmax_half<true, DH>(sm, tmem, half, row, n_max, ncol, geo.scale, m, w01);
             else
                 softmax_half<false, DH>(sm, tmem, half, row, n_max, ncol, geo.scale, m, w01);
-            if (!(ok = wait_all(&sm.v_full, ph_v, &sm.abort))) break;
-            v_pending = false;
+            // this chunk's V (the next chunk's K, if requested, is the newer group)
+            if (j + 1 < count)
+                copies_landed<1>();
+            else
+                copies_landed<0>();
             // V rows past the last key up to the 16-key step meet p = 0 in the MMAs:
             // zeros, not whatever the page holds there
             if (n_max & 15) {
@@ -450,15 +610,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             if (!(ok = wait_all(&sm.pv_done, ph_pv, &sm.abort))) break;
             pv_pending = false;
             ptx::tc_fence_after();
-            // the V buffer is free: the next chunk's V pages; the S buffer is
+            // the V buffer is free: the next chunk's values; the S buffer is
             // free: the next chunk's scores while this chunk is folded
-            if (tid == 0 && j + 1 < count)
-                issue_chunk<DH>(sm.v, &tmV, &sm.v_full, page_row, k0 + kChunk, min(kChunk, s_max - k0 - kChunk), g,
-                                geo);
-            v_pending = j + 1 < count;
+            // the page-table entries of chunk j + 2, stored after the fold
+            const int32_t pg_ahead =
+                tid < kChunk / BI_PAGE && j + 2 < count ? read_page(page_row, (j + 2) * (kChunk / BI_PAGE) + tid,
+                                                                    geo.max_pages)
+                                                        : 0;
             if (j + 1 < count) {
-                if (!(ok = wait_all(&sm.k_full, ph_k, &sm.abort))) break;
-                k_pending = false;
+                load_chunk<DH>(sm.v, vc, sm.pg[(j + 1) & 3], k0 + kChunk, min(kChunk, s_max - k0 - kChunk), g, geo);
+                copies_landed<1>();  // the next chunk's K (its V is the newer group)
+                __syncthreads();
                 ptx::tc_fence_after();
                 if (tid == 0) issue_s();
                 s_pending = true;
@@ -484,7 +646,9 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 tmem_ld32(lane_addr(tmem, col_o + c0), o);
                 if (j > 0) tmem_ld32(lane_addr(tmem, col_run + c0), O);
                 ptx::tmem_ld_wait();
+                reg_fence<32>(o);
                 if (j > 0) {
+                    reg_fence<32>(O);
                     if (active)
 #pragma unroll
                         for (int x = 0; x < 32; ++x)
@@ -496,44 +660,37 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 }
             }
             zero_cols<kHalfDims>(lane_addr(tmem, col_o));  // the next chunk's o starts at zero
+            if (tid < kChunk / BI_PAGE && j + 2 < count) sm.pg[(j + 2) & 3][tid] = pg_ahead;
             tmem_st_wait();
             ptx::tc_fence_before();
         }
         if (!ok) break;
-        // out = O / L (the lower half's L); a row without keys gets zeros
+        // the run's output is written while the next run's first copies are in flight
         if (half == 0) sm.xL[row] = L;
-        ptx::tc_fence_before();
-        __syncthreads();
-        ptx::tc_fence_after();
-        const float Lr = sm.xL[row];
-        const int64_t obase = (static_cast<int64_t>(mine ? en.t : 0) * geo.H + static_cast<int64_t>(g) * G + row % G) * DH +
-                              half * kHalfDims;
-#pragma unroll
-        for (int c0 = 0; c0 < kHalfDims; c0 += 32) {
-            uint32_t O[32];
-            tmem_ld32(lane_addr(tmem, col_run + c0), O);
-            ptx::tmem_ld_wait();
-            if (mine)
-#pragma unroll
-                for (int x = 0; x < 32; x += 2) {
-                    const bool has = keys > 0 && count > 0;
-                    const float o0 = has ? __fdiv_rn(__uint_as_float(O[x]), Lr) : 0.0f;
-                    const float o1 = has ? __fdiv_rn(__uint_as_float(O[x + 1]), Lr) : 0.0f;
-                    store_out2(geo.out, geo.out_f32, obase + c0 + x, o0, o1);
-                }
-        }
-        ptx::tc_fence_before();
-        __syncthreads();
+        po = PendingOut{true, first.t, run_tokens, g};
+        po_has = keys > 0 && count > 0;
+        po_L = L;
+        // the next run: the rest of this tile, else this CTA's next tile
         e0 += run_tokens;
+        if (e0 >= e_end) {
+            tile += gridDim.x;
+            if (tile < n_tiles) {
+                g = tile % geo.Hkv;
+                e0 = (tile / geo.Hkv) * NT;
+                e_end = min(e0 + NT, n_entries);
+            }
+        }
+        __syncthreads();  // xL and the run's shared state before the next run reuses them
     }
+    if (ok && po.on) write_out<G, DH>(sm, tmem, geo, po, half, row, po_has, po_L);
 
     if (!ok) {
         // a copy or an MMA did not complete in time: report, issue nothing more,
         // wait (bounded) for what is still in flight before the memory is freed
         if (tid == 0) report(geo.status, BI_DEV_TIMEOUT_ATTENTION);
         volatile int32_t none = 0;
-        if (k_pending) wait_all(&sm.k_full, ph_k, &none);
-        if (v_pending) wait_all(&sm.v_full, ph_v, &none);
+        cp_async_wait_all();
+        if (q_pending) wait_all(&sm.q_full, ph_q, &none);
         if (s_pending) wait_all(&sm.s_done, ph_s, &none);
         if (pv_pending) wait_all(&sm.pv_done, ph_pv, &none);
     }
@@ -544,7 +701,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
 }
 
 template <int G, int DH>
-cudaError_t launch_prefill_tc_t(const AttnGeom& g, const EntryMap& em, int32_t n, cudaStream_t s) {
+cudaError_t launch_prefill_tc_t(const AttnGeom& g, const EntryMap& em, int32_t n, int32_t q_rows, cudaStream_t s) {
     constexpr int NT = kRows / G;
     const size_t smem = sizeof(Smem<DH>) + 1024;  // + alignment of the base to 1024 bytes
     static std::once_flag once;
@@ -554,11 +711,12 @@ cudaError_t launch_prefill_tc_t(const AttnGeom& g, const EntryMap& em, int32_t n
                                         static_cast<int>(smem));
     });
     if (attr_err != cudaSuccess) return attr_err;
-    CUtensorMap tmK, tmV;
-    if (!encode_kv_map(&tmK, g.kc, g.num_pages, g.Hkv, DH) || !encode_kv_map(&tmV, g.vc, g.num_pages, g.Hkv, DH))
-        return cudaErrorInvalidValue;
-    return launch_pdl(prefill_tc_kernel<G, DH>, dim3((n + NT - 1) / NT, g.Hkv), dim3(kThreads), smem, s, tmK, tmV,
-                      g, em, n);
+    CUtensorMap tmQ;
+    if (!encode_q_map(&tmQ, g.q, q_rows, g.H, DH, G)) return cudaErrorInvalidValue;
+    const int64_t tiles = static_cast<int64_t>((n + NT - 1) / NT) * g.Hkv;
+    const int64_t ctas = std::min<int64_t>(tiles, num_sms());
+    return launch_pdl(prefill_tc_kernel<G, DH>, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, s, tmQ, g,
+                      em, n);
 }
 
 }  // namespace tc_prefill
