@@ -46,7 +46,18 @@ namespace bi {
 namespace tc_prefill {
 
 constexpr int kRows = 128;                 // rows per CTA = TMEM lanes
-constexpr int kThreads = 256;              // two threads per row
+constexpr int kConsumers = 256;            // two threads per row: warps 0-7 (warpgroups 0 and 1)
+constexpr int kThreads = kConsumers + 128; // warpgroup 2: warp 8 produces, warps 9-11 only give registers back
+// Registers per thread: the launch gives every thread kLaunchRegs; the
+// producer warpgroup hands back down to kProducerRegs and the consumers take
+// up kConsumerRegs, so 128 * kProducerRegs + 256 * kConsumerRegs must not
+// exceed kThreads * kLaunchRegs (checked below) or the increase would wait
+// forever.
+constexpr int kLaunchRegs = 168;
+constexpr int kProducerRegs = 56;
+constexpr int kConsumerRegs = 224;
+static_assert(128 * kProducerRegs + kConsumers * kConsumerRegs <= kThreads * kLaunchRegs,
+              "register split exceeds what the launch provides");
 constexpr int kChunk = BI_KV_CHUNK;        // 256 keys
 constexpr int kKeyRegion = kChunk * 128;   // one 64-dim SW128 region of a chunk's K or V (32 KB)
 constexpr int kQRegion = kRows * 128;      // one 64-dim SW128 region of Q (16 KB)
@@ -60,6 +71,14 @@ constexpr uint32_t kColRun = 384;          // running O
 constexpr bool kLowHalfEvenK = true;
 static_assert(kLowHalfEvenK, "pack_p below writes the even key into the low half");
 
+// What the producer tells the consumers about a run: its tokens (-1: no
+// more runs), first token, KV head, request, largest and smallest context of
+// its rows, chunk count, and each row's context (0: no keys, or not in the run).
+struct RunDesc {
+    int32_t tokens, t0, g, r, s_max, s_min, count;
+    int32_t keys[kRows];
+};
+
 template <int DH>
 struct Smem {
     static constexpr int kRegions = DH / 64;
@@ -67,16 +86,38 @@ struct Smem {
     uint8_t v[kRegions][kKeyRegion];
     uint8_t q[kRegions][kQRegion];
     uint8_t stage[kRows * DH * 2];         // output staging: bf16 rows, or half of the fp32 dims
-    uint64_t q_full, s_done, pv_done;
+    uint64_t q_full, k_full, v_full;       // producer -> consumers: copies landed
+    uint64_t s_done, pv_done;              // products completed (also: K, V and Q buffers free)
+    uint64_t rd_full[2], rd_empty[2];      // run descriptors written / read
     uint32_t tmem_base;
     int32_t abort;
     float xmax[2][kRows];                  // each half's partial row maximum
     float xsum[2][kRows];                  // the upper half's group sums (groups 2 and 3)
     float xL[kRows];                       // the row's final L, for the upper half's output
-    int32_t red_max[kThreads / 32];
-    int32_t red_min[kThreads / 32];
-    int32_t pg[4][kChunk / BI_PAGE];       // page-table entries of chunks c (slot c % 4), read ahead
+    RunDesc rd[2];
 };
+
+// One arrival on a barrier of this CTA (release: the caller's earlier writes
+// are visible to whoever completes a wait on the phase).
+__device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
+    asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
+}
+
+// The consumer warps' own barrier (named barrier 1, 256 threads); the
+// producer warp never takes part.
+__device__ __forceinline__ void consumer_sync() { asm volatile("bar.sync 1, 256;" ::: "memory"); }
+__device__ __forceinline__ bool consumer_any(bool pred) {
+    uint32_t r;
+    asm volatile(
+        "{\n\t.reg .pred p, q;\n\t"
+        "setp.ne.u32 p, %1, 0;\n\t"
+        "bar.red.or.pred q, 1, 256, p;\n\t"
+        "selp.u32 %0, 1, 0, q;\n\t}"
+        : "=r"(r)
+        : "r"(static_cast<uint32_t>(pred))
+        : "memory");
+    return r != 0;
+}
 
 // Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled region.
 __device__ __forceinline__ uint32_t sw128(int r, int c) {
@@ -258,7 +299,7 @@ __device__ __forceinline__ void softmax_half(Smem<DH>& sm, uint32_t tmem, int ha
         }
     }
     sm.xmax[half][row] = mx;
-    __syncthreads();
+    consumer_sync();
     const float m = ncol > 0 ? __fmul_rn(fmaxf(sm.xmax[0][row], sm.xmax[1][row]), scale) : 0.0f;
     // pass 2: p, its hi/lo pairs and the group sums, 16 keys of each range at
     // a time; the next block's scores are read while this block is computed
@@ -305,59 +346,42 @@ __device__ __forceinline__ void softmax_half(Smem<DH>& sm, uint32_t tmem, int ha
 constexpr uint32_t kVLbo = kKeyRegion;
 constexpr uint32_t kVSbo = 1024;
 
-// Every thread: its share of the 16-byte copies (cp.async) that bring keys
-// [k0, k0 + n) of KV head g into a chunk buffer, in the 128-byte-swizzled
-// layout of a TMA page box (rows of 64 dims, regions of 64 dims kKeyRegion
-// apart); committed as one group.  pages: the chunk's page-table entries (in
-// shared memory, read ahead).  Sixteen consecutive threads copy one key's row,
-// so each read is a contiguous 256-byte (DH = 128) run of its page.  Keys past
-// n are not copied.
+// The producer warp (every lane calls it): TMA page boxes of keys
+// [k0, k0 + n) of KV head g into a chunk buffer (one box per 16-key page and
+// 64-dim region: rows of 128 bytes, 128-byte swizzle), counted on bar.  The
+// lanes read the chunk's page-table entries together; lane 0 issues.
 template <int DH>
-__device__ __forceinline__ void load_chunk(uint8_t (*dst)[kKeyRegion], const uint16_t* __restrict__ cache,
-                                           const int32_t* pages, int32_t k0, int32_t n, int32_t g,
-                                           const AttnGeom& geo) {
-    constexpr int kCPR = DH / 8;                 // 16-byte chunks per key row
-    constexpr int kIters = kChunk * kCPR / kThreads;
-#pragma unroll
-    for (int it = 0; it < kIters; ++it) {
-        const int i = static_cast<int>(threadIdx.x) + it * kThreads;
-        const int key = i / kCPR, c = i % kCPR;
-        if (key < n) {
-            int32_t pg = pages[key / BI_PAGE];
-            if (pg < 0 || pg >= geo.num_pages) {
-                report(geo.status, BI_DEV_BAD_PAGE);
-                pg = 0;
-            }
-            const uint16_t* src =
-                cache + ((static_cast<int64_t>(pg) * geo.Hkv + g) * BI_PAGE + ((k0 + key) & (BI_PAGE - 1))) * DH + c * 8;
-            cp_async16(&dst[c >> 3][sw128(key, c & 7)], src);
+__device__ __forceinline__ void issue_chunk(uint8_t (*dst)[kKeyRegion], const CUtensorMap* map, uint64_t* bar,
+                                            const int32_t* page_row, int32_t k0, int32_t n, int32_t g,
+                                            const AttnGeom& geo) {
+    constexpr int kRegions = DH / 64;
+    const int lane = threadIdx.x & 31;
+    const int32_t np = (n + BI_PAGE - 1) / BI_PAGE;  // <= 16
+    int32_t pg = 0;
+    if (lane < np) {
+        const int32_t lp = k0 / BI_PAGE + lane;
+        pg = lp < geo.max_pages ? __ldg(page_row + lp) : -1;
+        if (pg < 0 || pg >= geo.num_pages) {
+            report(geo.status, BI_DEV_BAD_PAGE);
+            pg = 0;
         }
     }
-    cp_async_commit();
+    if (lane == 0) ptx::mbar_arrive_expect_tx(bar, static_cast<uint32_t>(np * kRegions * BI_PAGE * 128));
+    for (int i = 0; i < np; ++i) {
+        const int32_t pi = __shfl_sync(0xffffffffu, pg, i);
+        if (lane == 0) {
+            const int32_t y = (pi * geo.Hkv + g) * BI_PAGE;
+#pragma unroll
+            for (int h = 0; h < kRegions; ++h) ptx::tma_load_2d(&dst[h][i * BI_PAGE * 128], map, bar, h * 64, y);
+        }
+    }
 }
 
-// Page-table entry lp of a request's row (raw; checked where it is used), or
-// -1 past the row.
-__device__ __forceinline__ int32_t read_page(const int32_t* page_row, int32_t lp, int32_t max_pages) {
-    return lp < max_pages ? __ldg(page_row + lp) : -1;
-}
-
-// The copies of this thread's groups older than the newest `newer` are
-// complete; after the barrier that follows, every thread's are, and the
-// tensor cores may read them.
-template <int kNewer>
-__device__ __forceinline__ void copies_landed() {
-    asm volatile("cp.async.wait_group %0;" ::"n"(kNewer) : "memory");
-    ptx::fence_proxy_async_smem();  // generic-proxy writes before the MMAs read them
-}
-
-// Every thread: bounded wait on bar's phase; the outcome is the same in every
-// thread (a failure anywhere fails the block).  The phase advances only on
-// success, so a later drain waits on the same one.
-__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t& phase, volatile int32_t* abort) {
-    const bool ok = __syncthreads_or(!ptx::mbar_wait_bounded(bar, phase, abort)) == 0;
-    if (ok) phase ^= 1u;
-    return ok;
+// Every consumer thread: bounded wait for the phase of bar with the given
+// parity; the outcome is the same in every consumer thread (a failure
+// anywhere fails them all).
+__device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, volatile int32_t* abort) {
+    return !consumer_any(!ptx::mbar_wait_bounded(bar, parity, abort));
 }
 
 // A finished run whose output is still in tensor memory (running O).
@@ -410,8 +434,8 @@ __device__ __forceinline__ void write_out(Smem<DH>& sm, uint32_t tmem, const Att
                 }
             }
         }
-        __syncthreads();
-        for (int k = threadIdx.x; k < kRows * kCPR; k += kThreads) {
+        consumer_sync();
+        for (int k = threadIdx.x; k < kRows * kCPR; k += kConsumers) {
             const int r = k / kCPR, c = k % kCPR;
             const int ti = r / G;
             if (ti < po.tokens) {
@@ -420,33 +444,179 @@ __device__ __forceinline__ void write_out(Smem<DH>& sm, uint32_t tmem, const Att
                 *reinterpret_cast<uint4*>(dst) = *reinterpret_cast<const uint4*>(&sm.stage[r * DH * 2 + ((c ^ (r % kCPR)) << 4)]);
             }
         }
-        __syncthreads();
+        consumer_sync();
     }
 }
 
-// Persistent CTAs over tiles of (NT consecutive entries, one KV head); a
-// tile's entries are walked as runs of one request each.
+// The producer warp: walks this CTA's tiles (NT consecutive entries of one
+// KV head; tiles strided by the grid) as runs of one request each, writes a
+// descriptor per run, and issues its copies as the buffers come free: the
+// queries and keys of a chunk once the previous chunk's scores are done, its
+// values once the previous chunk's PV product is done.  It runs up to two
+// runs ahead of the consumers (the descriptor ring) and a chunk ahead in the
+// copies.  Ends with a descriptor of -1 tokens, then waits (bounded) until
+// every copy it issued has landed.
 template <int G, int DH>
-__global__ void __launch_bounds__(kThreads, 1)
-prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, AttnGeom geo, EntryMap em, int32_t n_entries) {
-    pdl_trigger();
-    pdl_wait();
+__device__ __forceinline__ void produce(Smem<DH>& sm, const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                        const CUtensorMap* tmQ, const AttnGeom& geo, const EntryMap& em,
+                                        int32_t n_entries) {
     constexpr int NT = kRows / G;
     constexpr int kRegions = DH / 64;
+    const int lane = threadIdx.x & 31;
+    const int32_t n_tiles = ((n_entries + NT - 1) / NT) * geo.Hkv;
+    volatile int32_t* abort = &sm.abort;
+    uint32_t runs = 0, chunks = 0, q_runs = 0;  // descriptors written, chunks and queries issued
+    bool ok = true;
+    // lane 0 waits (bounded), the warp follows its outcome
+    auto wait = [&](uint64_t* bar, uint32_t parity) {
+        bool r = true;
+        if (lane == 0) r = ptx::mbar_wait_bounded(bar, parity, abort);
+        return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+    };
+    auto take_slot = [&]() {  // the descriptor slot for run `runs`, once its previous run was read
+        const int slot = runs & 1;
+        if (runs >= 2 && !wait(&sm.rd_empty[slot], ((runs >> 1) - 1) & 1u)) return -1;
+        return slot;
+    };
+    for (int32_t tile = blockIdx.x; tile < n_tiles && ok; tile += gridDim.x) {
+        const int32_t g = tile % geo.Hkv;
+        const int32_t e_begin = (tile / geo.Hkv) * NT;
+        const int32_t e_end = min(e_begin + NT, n_entries);
+        for (int32_t e0 = e_begin; e0 < e_end && ok;) {
+            const int slot = take_slot();
+            if (slot < 0) {
+                ok = false;
+                break;
+            }
+            RunDesc& rd = sm.rd[slot];
+            // the run: token first.t + i is query row i * G + head for the heads of group g
+            const Entry first = get_entry(em, e0);
+            int32_t tok = 0, kmax = 0, kmin = INT_MAX;
+            for (int i = lane; i < NT; i += 32) {
+                const int32_t e = e0 + i;
+                int32_t keys = 0;
+                bool mine = false;
+                if (e < e_end) {
+                    Entry en;
+                    if (em.kind == 2) {  // entries are tokens; the request's tokens end at cu_q[r + 1]
+                        mine = e < em.a[first.r + 1];
+                        en = Entry{e, first.r, first.p + i};
+                    } else {
+                        en = get_entry(em, e);
+                        mine = en.r == first.r;
+                    }
+                    if (mine) {
+                        const int32_t s_len = en.p + 1;
+                        // the queries are read as one box of consecutive tokens from first.t
+                        const bool valid =
+                            en.p >= 0 && (s_len + BI_PAGE - 1) / BI_PAGE <= geo.max_pages && en.t == first.t + i;
+                        if (!valid) report(geo.status, BI_DEV_BAD_POSITION);
+                        keys = valid ? s_len : 0;
+                    }
+                }
+#pragma unroll
+                for (int hh = 0; hh < G; ++hh) rd.keys[i * G + hh] = keys;
+                if (mine) {
+                    ++tok;
+                    kmax = max(kmax, keys);
+                    kmin = min(kmin, keys);
+                }
+            }
+            tok = __reduce_add_sync(0xffffffffu, tok);
+            kmax = __reduce_max_sync(0xffffffffu, kmax);
+            kmin = __reduce_min_sync(0xffffffffu, kmin);
+            const int32_t count = (kmax + kChunk - 1) / kChunk;
+            if (lane == 0) {
+                rd.tokens = tok;
+                rd.t0 = first.t;
+                rd.g = g;
+                rd.r = first.r;
+                rd.s_max = kmax;
+                rd.s_min = kmin;
+                rd.count = count;
+            }
+            __syncwarp();
+            if (lane == 0) mbar_arrive(&sm.rd_full[slot]);  // releases the descriptor
+            ++runs;
+            const int32_t* page_row = geo.page_table + static_cast<int64_t>(first.r) * geo.max_pages;
+            for (int32_t j = 0; j < count && ok; ++j) {
+                const int32_t k0 = j * kChunk, n = min(kChunk, kmax - k0);
+                // the K (and Q) buffer is free once the previous chunk's scores are done
+                if (chunks > 0 && !(ok = wait(&sm.s_done, (chunks - 1) & 1u))) break;
+                if (j == 0) {
+                    if (lane == 0) {
+                        ptx::mbar_arrive_expect_tx(&sm.q_full, static_cast<uint32_t>(kRegions * kQRegion));
+#pragma unroll
+                        for (int h = 0; h < kRegions; ++h)
+                            ptx::tma_load_3d(&sm.q[h][0], tmQ, &sm.q_full, h * 64, g * G, first.t,
+                                             ptx::policy_evict_first());
+                    }
+                    ++q_runs;
+                }
+                issue_chunk<DH>(sm.k, tmK, &sm.k_full, page_row, k0, n, g, geo);
+                // the V buffer is free once the previous chunk's PV product is done
+                if (chunks > 0 && !(ok = wait(&sm.pv_done, (chunks - 1) & 1u))) break;
+                issue_chunk<DH>(sm.v, tmV, &sm.v_full, page_row, k0, n, g, geo);
+                ++chunks;
+            }
+            e0 += tok;
+        }
+    }
+    if (ok) {
+        const int slot = take_slot();
+        if (slot >= 0) {
+            if (lane == 0) {
+                sm.rd[slot].tokens = -1;
+                mbar_arrive(&sm.rd_full[slot]);
+            }
+        } else {
+            ok = false;
+        }
+    }
+    if (!ok && lane == 0) {
+        report(geo.status, BI_DEV_TIMEOUT_ATTENTION);
+        *abort = 1;
+    }
+    // every copy issued has landed before the shared memory is released
+    volatile int32_t none = 0;
+    if (lane == 0) {
+        if (q_runs > 0) ptx::mbar_wait_bounded(&sm.q_full, (q_runs - 1) & 1u, &none);
+        if (chunks > 0) {
+            ptx::mbar_wait_bounded(&sm.k_full, (chunks - 1) & 1u, &none);
+            ptx::mbar_wait_bounded(&sm.v_full, (chunks - 1) & 1u, &none);
+        }
+    }
+    __syncwarp();
+}
+
+// Persistent CTAs, one per SM: warps 0-7 consume runs (two threads per query
+// row: softmax, fold, output; thread 0 issues the MMAs), warp 8 produces them
+// (descriptors and copies); warps 9-11 complete warp 8's warpgroup, whose
+// registers go to the consumers.
+template <int G, int DH>
+__global__ void __launch_bounds__(kThreads, 1)
+prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                  const __grid_constant__ CUtensorMap tmQ, AttnGeom geo, EntryMap em, int32_t n_entries) {
+    pdl_trigger();
+    pdl_wait();
     constexpr int kHalfDims = DH / 2;  // head dims of o and O per thread
     extern __shared__ __align__(1024) unsigned char smem_raw[];
     Smem<DH>& sm = *reinterpret_cast<Smem<DH>*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
     const int tid = threadIdx.x, warp = tid / 32, lane = tid & 31;
-    const int half = warp >> 2;                  // which half of the row's keys and dims
-    const int row = 32 * (warp & 3) + lane;      // the row, = its TMEM lane
-    const int32_t n_blocks = (n_entries + NT - 1) / NT;
-    const int32_t n_tiles = n_blocks * geo.Hkv;
     if (tid == 0) {
         sm.abort = 0;
+        ptx::prefetch_tmap(&tmK);
+        ptx::prefetch_tmap(&tmV);
         ptx::prefetch_tmap(&tmQ);
         ptx::mbar_init(&sm.q_full, 1);
+        ptx::mbar_init(&sm.k_full, 1);
+        ptx::mbar_init(&sm.v_full, 1);
         ptx::mbar_init(&sm.s_done, 1);
         ptx::mbar_init(&sm.pv_done, 1);
+        for (int i = 0; i < 2; ++i) {
+            ptx::mbar_init(&sm.rd_full[i], 1);
+            ptx::mbar_init(&sm.rd_empty[i], kConsumers);
+        }
         ptx::fence_barrier_init();
     }
     if (warp == 0) {
@@ -457,242 +627,174 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmQ, AttnGeom geo, EntryMa
     __syncthreads();
     ptx::tc_fence_after();
     const uint32_t tmem = sm.tmem_base;
-    const uint32_t idesc_s = ptx::idesc_bf16_f32(kRows, kChunk);
-    const uint32_t idesc_pv = ptx::idesc_bf16_f32(kRows, DH) | (1u << 16);  // B (V) MN-major
-    const uint32_t col_o = kColO + half * kHalfDims, col_run = kColRun + half * kHalfDims;
-    zero_cols<kHalfDims>(lane_addr(tmem, col_o));  // o starts at zero (and is zeroed after every fold)
-    const uint16_t* kc = reinterpret_cast<const uint16_t*>(geo.kc);
-    const uint16_t* vc = reinterpret_cast<const uint16_t*>(geo.vc);
-    uint32_t ph_q = 0, ph_s = 0, ph_pv = 0;
-    // outstanding asynchronous work, tracked alike in every thread (the K and V
-    // copies are cp.async groups of each thread, waited for in commit order)
-    bool q_pending = false, s_pending = false, pv_pending = false;
-    bool ok = true;
-    PendingOut po{false, 0, 0, 0};
-    bool po_has = false;  // this thread's row of the pending run has keys
-    float po_L = 0.0f;
+    if (warp >= kConsumers / 32) {
+        asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
+        if (warp == kConsumers / 32) produce<G, DH>(sm, &tmK, &tmV, &tmQ, geo, em, n_entries);
+    } else {
+        asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
+        const int half = warp >> 2;              // which half of the row's keys and dims
+        const int row = 32 * (warp & 3) + lane;  // the row, = its TMEM lane
+        const uint32_t idesc_s = ptx::idesc_bf16_f32(kRows, kChunk);
+        const uint32_t idesc_pv = ptx::idesc_bf16_f32(kRows, DH) | (1u << 16);  // B (V) MN-major
+        const uint32_t col_o = kColO + half * kHalfDims, col_run = kColRun + half * kHalfDims;
+        volatile int32_t* abort = &sm.abort;
+        zero_cols<kHalfDims>(lane_addr(tmem, col_o));  // o starts at zero (and is zeroed after every fold)
+        uint32_t runs = 0, chunks = 0, q_runs = 0;     // descriptors, chunks and queries consumed
+        bool s_pending = false, pv_pending = false;    // products in flight
+        bool ok = true;
+        PendingOut po{false, 0, 0, 0};
+        bool po_has = false;  // this thread's row of the pending run has keys
+        float po_L = 0.0f;
 
-    auto issue_s = [&]() {  // thread 0: S = Q K^T of the chunk in sm.k
+        auto issue_s = [&]() {  // thread 0: S = Q K^T of the chunk in sm.k
 #pragma unroll
-        for (int ks = 0; ks < DH / 16; ++ks) {
-            const uint32_t step = static_cast<uint32_t>((ks % 4) * 32);
-            ptx::tc_mma_f16<1>(tmem + kColS, desc(smem_u32(&sm.q[ks / 4][0]) + step, 16, 1024),
-                               desc(smem_u32(&sm.k[ks / 4][0]) + step, 16, 1024), idesc_s, ks > 0);
-        }
-        ptx::tc_commit<1>(&sm.s_done);
-    };
+            for (int ks = 0; ks < DH / 16; ++ks) {
+                const uint32_t step = static_cast<uint32_t>((ks % 4) * 32);
+                ptx::tc_mma_f16<1>(tmem + kColS, desc(smem_u32(&sm.q[ks / 4][0]) + step, 16, 1024),
+                                   desc(smem_u32(&sm.k[ks / 4][0]) + step, 16, 1024), idesc_s, ks > 0);
+            }
+            ptx::tc_commit<1>(&sm.s_done);
+        };
 
-    int32_t tile = blockIdx.x;
-    int32_t e0 = 0, e_end = 0, g = 0;
-    if (tile < n_tiles) {
-        g = tile % geo.Hkv;
-        e0 = (tile / geo.Hkv) * NT;
-        e_end = min(e0 + NT, n_entries);
-    }
-    while (tile < n_tiles && ok) {
-        // ---- a run of consecutive entries of one request: token first.t + row / G, head row % G ----
-        const Entry first = get_entry(em, e0);
-        const int32_t* page_row = geo.page_table + static_cast<int64_t>(first.r) * geo.max_pages;
-        // the page-table entries of the run's first two chunks, in flight during the lookups below
-        const int32_t pg_first = tid < 2 * (kChunk / BI_PAGE) ? read_page(page_row, tid, geo.max_pages) : 0;
-        const int32_t ti = row / G;
-        Entry en{-1, -1, -1};
-        bool mine = false;
-        if (e0 + ti < e_end) {
-            if (em.kind == 2) {
-                // entries are tokens; the request's tokens end at cu_q[r + 1]
-                mine = e0 + ti < em.a[first.r + 1];
-                en = Entry{e0 + ti, first.r, first.p + ti};
-            } else {
-                en = get_entry(em, e0 + ti);
-                mine = en.r == first.r;
-            }
-        }
-        int32_t keys = 0;
-        if (mine) {
-            const int32_t s_len = en.p + 1;
-            // the queries are read as one box of consecutive tokens from first.t
-            const bool valid = en.p >= 0 && (s_len + BI_PAGE - 1) / BI_PAGE <= geo.max_pages && en.t == first.t + ti;
-            if (!valid && half == 0 && row % G == 0) report(geo.status, BI_DEV_BAD_POSITION);
-            keys = valid ? s_len : 0;
-        }
-        const int32_t run_tokens = __syncthreads_count(mine && half == 0 && row % G == 0);
-        const int32_t wmax = __reduce_max_sync(0xffffffffu, keys);
-        const int32_t wmin = __reduce_min_sync(0xffffffffu, mine ? keys : INT_MAX);
-        if (lane == 0) {
-            sm.red_max[warp] = wmax;
-            sm.red_min[warp] = wmin;
-        }
-        if (tid < 2 * (kChunk / BI_PAGE)) sm.pg[tid / (kChunk / BI_PAGE)][tid % (kChunk / BI_PAGE)] = pg_first;
-        __syncthreads();
-        int32_t s_max = sm.red_max[0], s_min = sm.red_min[0];
-#pragma unroll
-        for (int w = 1; w < kThreads / 32; ++w) {
-            s_max = max(s_max, sm.red_max[w]);
-            s_min = min(s_min, sm.red_min[w]);
-        }
-        const int32_t count = (s_max + kChunk - 1) / kChunk;
-        // this run's queries and first chunk: the buffers are free (the last
-        // products of the previous run have completed)
-        if (count > 0) {
-            if (tid == 0) {
-                ptx::mbar_arrive_expect_tx(&sm.q_full, static_cast<uint32_t>(kRegions * kQRegion));
-#pragma unroll
-                for (int h = 0; h < kRegions; ++h)
-                    ptx::tma_load_3d(&sm.q[h][0], &tmQ, &sm.q_full, h * 64, g * G, first.t, ptx::policy_evict_first());
-            }
-            load_chunk<DH>(sm.k, kc, sm.pg[0], 0, min(kChunk, s_max), g, geo);
-            load_chunk<DH>(sm.v, vc, sm.pg[0], 0, min(kChunk, s_max), g, geo);
-            q_pending = true;
-        }
-        // the previous run's output, while this run's first copies are in flight
-        if (po.on) {
-            write_out<G, DH>(sm, tmem, geo, po, half, row, po_has, po_L);
-            po.on = false;
-        }
-        if (count > 0) {
-            copies_landed<1>();  // K (V is the newer group)
-            if (!(ok = wait_all(&sm.q_full, ph_q, &sm.abort))) break;
-            q_pending = false;
-            ptx::tc_fence_after();
-            if (tid == 0) issue_s();
-            s_pending = true;
-        }
-        float M = 0.0f, L = 0.0f;
-        for (int32_t j = 0; j < count && ok; ++j) {
-            const int32_t k0 = j * kChunk;
-            const int32_t n_max = min(kChunk, s_max - k0);
-            const int32_t ncol = mine ? min(max(keys - k0, 0), kChunk) : 0;
-            const bool masked = k0 + kChunk > s_min;  // some row of the run stops inside this chunk
-            if (!(ok = wait_all(&sm.s_done, ph_s, &sm.abort))) break;
-            s_pending = false;
-            ptx::tc_fence_after();
-            // the K buffer is free: the next chunk's keys
-            if (j + 1 < count)
-                load_chunk<DH>(sm.k, kc, sm.pg[(j + 1) & 3], k0 + kChunk, min(kChunk, s_max - k0 - kChunk), g, geo);
-            float m, w01;
-            if (masked)
-                softmax_half<true, DH>(sm, tmem, half, row, n_max, ncol, geo.scale, m, w01);
-            else
-                softmax_half<false, DH>(sm, tmem, half, row, n_max, ncol, geo.scale, m, w01);
-            // this chunk's V (the next chunk's K, if requested, is the newer group)
-            if (j + 1 < count)
-                copies_landed<1>();
-            else
-                copies_landed<0>();
-            // V rows past the last key up to the 16-key step meet p = 0 in the MMAs:
-            // zeros, not whatever the page holds there
-            if (n_max & 15) {
-                const int pad = ((n_max + 15) & ~15) - n_max;
-                for (int i = tid; i < pad * 8 * kRegions; i += kThreads) {
-                    const int r = n_max + i / (8 * kRegions), rem = i % (8 * kRegions);
-                    *reinterpret_cast<uint4*>(&sm.v[rem / 8][sw128(r, rem % 8)]) = make_uint4(0u, 0u, 0u, 0u);
-                }
-                ptx::fence_proxy_async_smem();
-            }
-            tmem_st_wait();
-            ptx::tc_fence_before();
-            __syncthreads();
-            ptx::tc_fence_after();
-            // l in the decode routine's order: ((group 0 + group 1) + group 2) + group 3
-            const float l = half == 0 ? __fadd_rn(__fadd_rn(w01, sm.xsum[0][row]), sm.xsum[1][row]) : 0.0f;
-            // o = P V: per 16-key step the hi part, then the lo part
-            if (tid == 0) {
-                const int steps = (n_max + 15) / 16;
-                for (int ks = 0; ks < steps; ++ks) {
-                    const uint64_t bd = desc(smem_u32(&sm.v[0][0]) + static_cast<uint32_t>(ks * 2048), kVLbo, kVSbo);
-                    mma_ts(tmem + kColO, tmem + kColS + 16 * ks, bd, idesc_pv, 1u);
-                    mma_ts(tmem + kColO, tmem + kColS + 16 * ks + 8, bd, idesc_pv, 1u);
-                }
-                ptx::tc_commit<1>(&sm.pv_done);
-            }
-            pv_pending = true;
-            if (!(ok = wait_all(&sm.pv_done, ph_pv, &sm.abort))) break;
-            pv_pending = false;
-            ptx::tc_fence_after();
-            // the V buffer is free: the next chunk's values; the S buffer is
-            // free: the next chunk's scores while this chunk is folded
-            // the page-table entries of chunk j + 2, stored after the fold
-            const int32_t pg_ahead =
-                tid < kChunk / BI_PAGE && j + 2 < count ? read_page(page_row, (j + 2) * (kChunk / BI_PAGE) + tid,
-                                                                    geo.max_pages)
-                                                        : 0;
-            if (j + 1 < count) {
-                load_chunk<DH>(sm.v, vc, sm.pg[(j + 1) & 3], k0 + kChunk, min(kChunk, s_max - k0 - kChunk), g, geo);
-                copies_landed<1>();  // the next chunk's K (its V is the newer group)
-                __syncthreads();
+        while (ok) {
+            // ---- the next run's descriptor ----
+            const int slot = runs & 1;
+            if (!(ok = wait_all(&sm.rd_full[slot], (runs >> 1) & 1u, abort))) break;
+            const RunDesc& rd = sm.rd[slot];
+            const int32_t tokens = rd.tokens;
+            if (tokens < 0) break;
+            const int32_t t0 = rd.t0, g = rd.g, s_max = rd.s_max, s_min = rd.s_min, count = rd.count;
+            const int32_t keys = rd.keys[row];
+            const bool mine = row / G < tokens;
+            mbar_arrive(&sm.rd_empty[slot]);
+            ++runs;
+            if (count > 0) {
+                if (!(ok = wait_all(&sm.q_full, q_runs & 1u, abort))) break;
+                ++q_runs;
+                if (!(ok = wait_all(&sm.k_full, chunks & 1u, abort))) break;
                 ptx::tc_fence_after();
                 if (tid == 0) issue_s();
                 s_pending = true;
             }
-            // the decode merge's fold; a row without keys in this chunk keeps its state
-            const bool active = ncol > 0;
-            float a = 1.0f, bw = 1.0f;
-            if (active) {
-                if (j == 0) {
-                    M = m;
-                    L = l;
-                } else {
-                    const float Mn = fmaxf(M, m);
-                    a = attn_exp(__fsub_rn(M, Mn));
-                    bw = attn_exp(__fsub_rn(m, Mn));
-                    L = __fadd_rn(__fmul_rn(L, a), __fmul_rn(l, bw));
-                    M = Mn;
+            // the previous run's output, while this run's first scores are computed
+            if (po.on) {
+                write_out<G, DH>(sm, tmem, geo, po, half, row, po_has, po_L);
+                po.on = false;
+            }
+            float M = 0.0f, L = 0.0f;
+            for (int32_t j = 0; j < count && ok; ++j, ++chunks) {
+                const int32_t k0 = j * kChunk;
+                const int32_t n_max = min(kChunk, s_max - k0);
+                const int32_t ncol = mine ? min(max(keys - k0, 0), kChunk) : 0;
+                const bool masked = k0 + kChunk > s_min;  // some row of the run stops inside this chunk
+                if (!(ok = wait_all(&sm.s_done, chunks & 1u, abort))) break;
+                s_pending = false;
+                ptx::tc_fence_after();
+                float m, w01;
+                if (masked)
+                    softmax_half<true, DH>(sm, tmem, half, row, n_max, ncol, geo.scale, m, w01);
+                else
+                    softmax_half<false, DH>(sm, tmem, half, row, n_max, ncol, geo.scale, m, w01);
+                if (!(ok = wait_all(&sm.v_full, chunks & 1u, abort))) break;
+                // V rows past the last key up to the 16-key step meet p = 0 in the MMAs:
+                // zeros, not whatever the page holds there
+                if (n_max & 15) {
+                    constexpr int kRegions = DH / 64;
+                    const int pad = ((n_max + 15) & ~15) - n_max;
+                    for (int i = tid; i < pad * 8 * kRegions; i += kConsumers) {
+                        const int r = n_max + i / (8 * kRegions), rem = i % (8 * kRegions);
+                        *reinterpret_cast<uint4*>(&sm.v[rem / 8][sw128(r, rem % 8)]) = make_uint4(0u, 0u, 0u, 0u);
+                    }
+                    ptx::fence_proxy_async_smem();
                 }
-            }
-#pragma unroll
-            for (int c0 = 0; c0 < kHalfDims; c0 += 32) {
-                uint32_t o[32], O[32];
-                tmem_ld32(lane_addr(tmem, col_o + c0), o);
-                if (j > 0) tmem_ld32(lane_addr(tmem, col_run + c0), O);
-                ptx::tmem_ld_wait();
-                reg_fence<32>(o);
-                if (j > 0) {
-                    reg_fence<32>(O);
-                    if (active)
-#pragma unroll
-                        for (int x = 0; x < 32; ++x)
-                            O[x] = __float_as_uint(__fadd_rn(__fmul_rn(__uint_as_float(O[x]), a),
-                                                             __fmul_rn(__uint_as_float(o[x]), bw)));
-                    tmem_st32(lane_addr(tmem, col_run + c0), O);
-                } else {
-                    tmem_st32(lane_addr(tmem, col_run + c0), o);
+                tmem_st_wait();
+                ptx::tc_fence_before();
+                consumer_sync();
+                ptx::tc_fence_after();
+                // l in the decode routine's order: ((group 0 + group 1) + group 2) + group 3
+                const float l = half == 0 ? __fadd_rn(__fadd_rn(w01, sm.xsum[0][row]), sm.xsum[1][row]) : 0.0f;
+                // o = P V: per 16-key step the hi part, then the lo part
+                if (tid == 0) {
+                    const int steps = (n_max + 15) / 16;
+                    for (int ks = 0; ks < steps; ++ks) {
+                        const uint64_t bd =
+                            desc(smem_u32(&sm.v[0][0]) + static_cast<uint32_t>(ks * 2048), kVLbo, kVSbo);
+                        mma_ts(tmem + kColO, tmem + kColS + 16 * ks, bd, idesc_pv, 1u);
+                        mma_ts(tmem + kColO, tmem + kColS + 16 * ks + 8, bd, idesc_pv, 1u);
+                    }
+                    ptx::tc_commit<1>(&sm.pv_done);
                 }
+                pv_pending = true;
+                if (!(ok = wait_all(&sm.pv_done, chunks & 1u, abort))) break;
+                pv_pending = false;
+                ptx::tc_fence_after();
+                // the next chunk's scores while this chunk is folded
+                if (j + 1 < count) {
+                    if (!(ok = wait_all(&sm.k_full, (chunks + 1) & 1u, abort))) break;
+                    ptx::tc_fence_after();
+                    if (tid == 0) issue_s();
+                    s_pending = true;
+                }
+                // the decode merge's fold; a row without keys in this chunk keeps its state
+                const bool active = ncol > 0;
+                float a = 1.0f, bw = 1.0f;
+                if (active) {
+                    if (j == 0) {
+                        M = m;
+                        L = l;
+                    } else {
+                        const float Mn = fmaxf(M, m);
+                        a = attn_exp(__fsub_rn(M, Mn));
+                        bw = attn_exp(__fsub_rn(m, Mn));
+                        L = __fadd_rn(__fmul_rn(L, a), __fmul_rn(l, bw));
+                        M = Mn;
+                    }
+                }
+#pragma unroll
+                for (int c0 = 0; c0 < kHalfDims; c0 += 32) {
+                    uint32_t o[32], O[32];
+                    tmem_ld32(lane_addr(tmem, col_o + c0), o);
+                    if (j > 0) tmem_ld32(lane_addr(tmem, col_run + c0), O);
+                    ptx::tmem_ld_wait();
+                    reg_fence<32>(o);
+                    if (j > 0) {
+                        reg_fence<32>(O);
+                        if (active)
+#pragma unroll
+                            for (int x = 0; x < 32; ++x)
+                                O[x] = __float_as_uint(__fadd_rn(__fmul_rn(__uint_as_float(O[x]), a),
+                                                                 __fmul_rn(__uint_as_float(o[x]), bw)));
+                        tmem_st32(lane_addr(tmem, col_run + c0), O);
+                    } else {
+                        tmem_st32(lane_addr(tmem, col_run + c0), o);
+                    }
+                }
+                zero_cols<kHalfDims>(lane_addr(tmem, col_o));  // the next chunk's o starts at zero
+                tmem_st_wait();
+                ptx::tc_fence_before();
             }
-            zero_cols<kHalfDims>(lane_addr(tmem, col_o));  // the next chunk's o starts at zero
-            if (tid < kChunk / BI_PAGE && j + 2 < count) sm.pg[(j + 2) & 3][tid] = pg_ahead;
-            tmem_st_wait();
-            ptx::tc_fence_before();
+            if (!ok) break;
+            // the run's output is written while the next run's first scores are computed
+            if (half == 0) sm.xL[row] = L;
+            po = PendingOut{true, t0, tokens, g};
+            po_has = keys > 0 && count > 0;
+            po_L = L;
         }
-        if (!ok) break;
-        // the run's output is written while the next run's first copies are in flight
-        if (half == 0) sm.xL[row] = L;
-        po = PendingOut{true, first.t, run_tokens, g};
-        po_has = keys > 0 && count > 0;
-        po_L = L;
-        // the next run: the rest of this tile, else this CTA's next tile
-        e0 += run_tokens;
-        if (e0 >= e_end) {
-            tile += gridDim.x;
-            if (tile < n_tiles) {
-                g = tile % geo.Hkv;
-                e0 = (tile / geo.Hkv) * NT;
-                e_end = min(e0 + NT, n_entries);
+        if (ok && po.on) {
+            consumer_sync();  // xL of the last run
+            write_out<G, DH>(sm, tmem, geo, po, half, row, po_has, po_L);
+        }
+        if (!ok) {
+            // a copy or an MMA did not complete in time: stop the producer,
+            // wait (bounded) for the products still in flight
+            if (tid == 0) {
+                report(geo.status, BI_DEV_TIMEOUT_ATTENTION);
+                *abort = 1;
             }
+            volatile int32_t none = 0;
+            if (s_pending) wait_all(&sm.s_done, chunks & 1u, &none);
+            if (pv_pending) wait_all(&sm.pv_done, chunks & 1u, &none);
         }
-        __syncthreads();  // xL and the run's shared state before the next run reuses them
-    }
-    if (ok && po.on) write_out<G, DH>(sm, tmem, geo, po, half, row, po_has, po_L);
-
-    if (!ok) {
-        // a copy or an MMA did not complete in time: report, issue nothing more,
-        // wait (bounded) for what is still in flight before the memory is freed
-        if (tid == 0) report(geo.status, BI_DEV_TIMEOUT_ATTENTION);
-        volatile int32_t none = 0;
-        cp_async_wait_all();
-        if (q_pending) wait_all(&sm.q_full, ph_q, &none);
-        if (s_pending) wait_all(&sm.s_done, ph_s, &none);
-        if (pv_pending) wait_all(&sm.pv_done, ph_pv, &none);
     }
     ptx::tc_fence_before();
     __syncthreads();
@@ -709,14 +811,21 @@ cudaError_t launch_prefill_tc_t(const AttnGeom& g, const EntryMap& em, int32_t n
     std::call_once(once, [smem] {
         attr_err = cudaFuncSetAttribute(prefill_tc_kernel<G, DH>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                         static_cast<int>(smem));
+        // the consumers' register increase relies on the launch giving every
+        // thread kLaunchRegs: refuse to launch a build that gives fewer
+        cudaFuncAttributes fa{};
+        if (attr_err == cudaSuccess) attr_err = cudaFuncGetAttributes(&fa, prefill_tc_kernel<G, DH>);
+        if (attr_err == cudaSuccess && fa.numRegs < kLaunchRegs) attr_err = cudaErrorInvalidConfiguration;
     });
     if (attr_err != cudaSuccess) return attr_err;
-    CUtensorMap tmQ;
-    if (!encode_q_map(&tmQ, g.q, q_rows, g.H, DH, G)) return cudaErrorInvalidValue;
+    CUtensorMap tmK, tmV, tmQ;
+    if (!encode_kv_map(&tmK, g.kc, g.num_pages, g.Hkv, DH) || !encode_kv_map(&tmV, g.vc, g.num_pages, g.Hkv, DH) ||
+        !encode_q_map(&tmQ, g.q, q_rows, g.H, DH, G))
+        return cudaErrorInvalidValue;
     const int64_t tiles = static_cast<int64_t>((n + NT - 1) / NT) * g.Hkv;
     const int64_t ctas = std::min<int64_t>(tiles, num_sms());
-    return launch_pdl(prefill_tc_kernel<G, DH>, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, s, tmQ, g,
-                      em, n);
+    return launch_pdl(prefill_tc_kernel<G, DH>, dim3(static_cast<unsigned>(ctas)), dim3(kThreads), smem, s, tmK, tmV,
+                      tmQ, g, em, n);
 }
 
 }  // namespace tc_prefill
