@@ -655,7 +655,8 @@ decode_merge_kernel(AttnGeom geo, EntryMap em, int32_t max_splits, int32_t chunk
             }
         }
     }
-    store_out2(geo.out, geo.out_f32, oidx, __fdiv_rn(O0, L), __fdiv_rn(O1, L));
+    const float rl = __frcp_rn(L);  // out = O * fl(1 / L) (prefill's output divides the same way)
+    store_out2(geo.out, geo.out_f32, oidx, __fmul_rn(O0, rl), __fmul_rn(O1, rl));
 }
 
 // ---------------------------------------------------------------------------

@@ -88,6 +88,8 @@ struct Smem {
     uint8_t stage[kRows * DH * 2];         // output staging: bf16 rows, or half of the fp32 dims
     uint64_t q_full, k_full, v_full;       // producer -> consumers: copies landed
     uint64_t s_done, pv_done;              // products completed (also: K, V and Q buffers free)
+    uint64_t pa_ready, pb_ready;           // consumers -> MMA thread: P of keys 0-127 / 128-255 written
+    uint64_t drain;                        // the MMA thread's last commit
     uint64_t rd_full[2], rd_empty[2];      // run descriptors written / read
     uint32_t tmem_base;
     int32_t abort;
@@ -224,62 +226,41 @@ __device__ __forceinline__ void pack_p(float p0, float p1, uint32_t& hi, uint32_
 // [16 c, 16 c + 16) for key group c of 16 keys: 8 packed hi pairs, then 8 lo.
 // The maximum is taken over the raw dot products and scaled once: rounding
 // is monotone and scale > 0, so max_j fl(s_j * scale) = fl(max_j s_j * scale).
-// Reads one block of this thread's scores: keys ca .. ca + 15 and
-// ca + 128 .. ca + 143 (ca = 32 (2 half + gi) + 16 q); columns at or past n_max
-// are not read (zeros).  Completes at the next tcgen05.wait::ld.
-__device__ __forceinline__ void load_block(uint32_t base, int half, int gi, int q, int32_t n_max, uint32_t (&ra)[16],
-                                           uint32_t (&rb)[16]) {
-    const int ca = 32 * (2 * half + gi) + 16 * q, cb = 128 + ca;
-    if (ca < n_max) {
-        ptx::tmem_ld16(base + ca, ra);
+// Reads 16 of this thread's scores, keys c0 .. c0 + 15 (columns at or past
+// n_max: zeros, not read).  Completes at the next tcgen05.wait::ld.
+__device__ __forceinline__ void load16(uint32_t base, int c0, int32_t n_max, uint32_t (&r)[16]) {
+    if (c0 < n_max) {
+        ptx::tmem_ld16(base + c0, r);
     } else {
 #pragma unroll
-        for (int i = 0; i < 16; ++i) ra[i] = 0u;
-    }
-    if (cb < n_max) {
-        ptx::tmem_ld16(base + cb, rb);
-    } else {
-#pragma unroll
-        for (int i = 0; i < 16; ++i) rb[i] = 0u;
+        for (int i = 0; i < 16; ++i) r[i] = 0u;
     }
 }
 
-// p of one block (see load_block): P words back to TMEM in place of the
-// scores, pair sums p_i + p_(i+128) into u (kFirst: u = the pair sums; else
-// u += them, the butterfly's first level).
-template <bool kMask, bool kFirst>
-__device__ __forceinline__ void p_block(uint32_t base, int half, int gi, int q, int32_t n_max, int32_t ncol, float scale,
-                                        float m, const uint32_t (&ra)[16], const uint32_t (&rb)[16], float (&u)[16]) {
-    const int ca = 32 * (2 * half + gi) + 16 * q, cb = 128 + ca;
-    uint32_t wa[16], wb[16];  // P words of keys ca .. ca + 15 and cb .. cb + 15
+// p of keys c0 .. c0 + 15 into p[off ..], and their P words back to TMEM in
+// place of the scores (8 packed hi pairs, then 8 lo pairs).
+template <bool kMask>
+__device__ __forceinline__ void p_block16(uint32_t base, int c0, int32_t n_max, int32_t ncol, float scale, float m,
+                                          const uint32_t (&r)[16], float (&p)[64], int off) {
+    uint32_t w[16];
 #pragma unroll
     for (int j = 0; j < 16; j += 2) {
-        float pa[2], pb[2];
+        float pv[2];
 #pragma unroll
         for (int x = 0; x < 2; ++x) {
-            const int i = j + x;
-            float sa = ca < n_max ? __fmul_rn(__uint_as_float(ra[i]), scale) : -INFINITY;
-            float sb = cb < n_max ? __fmul_rn(__uint_as_float(rb[i]), scale) : -INFINITY;
-            if (kMask) {
-                if (ca + i >= ncol) sa = -INFINITY;
-                if (cb + i >= ncol) sb = -INFINITY;
-            }
-            pa[x] = attn_exp(__fsub_rn(sa, m));
-            pb[x] = attn_exp(__fsub_rn(sb, m));
-            // decode adds both to 0; p >= 0 is never -0, so 0 + p = p exactly
-            const float pair = __fadd_rn(pa[x], pb[x]);
-            u[i] = kFirst ? pair : __fadd_rn(u[i], pair);
+            float sc = c0 < n_max ? __fmul_rn(__uint_as_float(r[j + x]), scale) : -INFINITY;
+            if (kMask && c0 + j + x >= ncol) sc = -INFINITY;
+            pv[x] = attn_exp(__fsub_rn(sc, m));
+            p[off + j + x] = pv[x];
         }
-        pack_p(pa[0], pa[1], wa[j / 2], wa[8 + j / 2]);
-        pack_p(pb[0], pb[1], wb[j / 2], wb[8 + j / 2]);
+        pack_p(pv[0], pv[1], w[j / 2], w[8 + j / 2]);
     }
-    if (ca < n_max) tmem_st16(base + ca, wa);
-    if (cb < n_max) tmem_st16(base + cb, wb);
+    if (c0 < n_max) tmem_st16(base + c0, w);
 }
 
 template <bool kMask, int DH>
-__device__ __forceinline__ void softmax_half(Smem<DH>& sm, uint32_t tmem, int half, int row, int32_t n_max,
-                                             int32_t ncol, float scale, float& m_out, float& w01) {
+__device__ __forceinline__ void softmax_lo(Smem<DH>& sm, uint32_t tmem, int half, int row, int32_t n_max,
+                                           int32_t ncol, float scale, float& m_out, float (&pa)[64]) {
     const int c_lo = 64 * half, c_hi = 128 + 64 * half;  // this thread's key ranges (64 keys each)
     const uint32_t base = lane_addr(tmem, kColS);
     // pass 1: the row's maximum over its keys, 64 at a time
@@ -301,39 +282,75 @@ __device__ __forceinline__ void softmax_half(Smem<DH>& sm, uint32_t tmem, int ha
     sm.xmax[half][row] = mx;
     consumer_sync();
     const float m = ncol > 0 ? __fmul_rn(fmaxf(sm.xmax[0][row], sm.xmax[1][row]), scale) : 0.0f;
-    // pass 2: p, its hi/lo pairs and the group sums, 16 keys of each range at
-    // a time; the next block's scores are read while this block is computed
-    float w0 = 0.0f, w1 = 0.0f;
-    uint32_t xa[16], xb[16], ya[16], yb[16];  // two blocks of scores: keys ca.. and cb..
-    load_block(base, half, 0, 0, n_max, xa, xb);
-#pragma unroll 1
+    m_out = m;
+    // pass 2, keys below 128: four blocks of 16, the next block read while one is computed
+    uint32_t ra[16], rb[16];
+    load16(base, c_lo, n_max, ra);
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk) {
+        const int ca = c_lo + 16 * blk;
+        ptx::tmem_ld_wait();
+        if (blk % 2 == 0) {
+            reg_fence<16>(ra);
+            if (blk + 1 < 4) load16(base, ca + 16, n_max, rb);
+            p_block16<kMask>(base, ca, n_max, ncol, scale, m, ra, pa, blk * 16);
+        } else {
+            reg_fence<16>(rb);
+            if (blk + 1 < 4) load16(base, ca + 16, n_max, ra);
+            p_block16<kMask>(base, ca, n_max, ncol, scale, m, rb, pa, blk * 16);
+        }
+    }
+}
+
+// Second phase: p of the thread's keys 128 + 32b + i, the group sums in the
+// decode routine's tree (pair sums pa + pb, the xor-butterfly), P words of
+// these keys to TMEM.  Leaves w01 (lower half: groups 0 + 1) or xsum (upper
+// half: groups 2 and 3).
+template <bool kMask, int DH>
+__device__ __forceinline__ void softmax_hi(Smem<DH>& sm, uint32_t tmem, int half, int row, int32_t n_max,
+                                           int32_t ncol, float scale, float m, const float (&pa)[64], float& w01) {
+    const int c_hi = 128 + 64 * half;
+    const uint32_t base = lane_addr(tmem, kColS);
+    float pb[64];
+    uint32_t ra[16], rb[16];
+    load16(base, c_hi, n_max, ra);
+#pragma unroll
+    for (int blk = 0; blk < 4; ++blk) {
+        const int cb = c_hi + 16 * blk;
+        ptx::tmem_ld_wait();
+        if (blk % 2 == 0) {
+            reg_fence<16>(ra);
+            if (blk + 1 < 4) load16(base, cb + 16, n_max, rb);
+            p_block16<kMask>(base, cb, n_max, ncol, scale, m, ra, pb, blk * 16);
+        } else {
+            reg_fence<16>(rb);
+            if (blk + 1 < 4) load16(base, cb + 16, n_max, ra);
+            p_block16<kMask>(base, cb, n_max, ncol, scale, m, rb, pb, blk * 16);
+        }
+    }
+    // group gi: pairs (pa, pb) of keys 32b + i, i = 0..31, summed pairwise then
+    // by the butterfly (16 first: i with i + 16, then 8, 4, 2, 1)
+    float w[2];
+#pragma unroll
     for (int gi = 0; gi < 2; ++gi) {
-        float u[16];  // after the second block: the butterfly's first level (i, i + 16)
-        ptx::tmem_ld_wait();
-        reg_fence<16>(xa);
-        reg_fence<16>(xb);
-        load_block(base, half, gi, 1, n_max, ya, yb);
-        p_block<kMask, true>(base, half, gi, 0, n_max, ncol, scale, m, xa, xb, u);
-        ptx::tmem_ld_wait();
-        reg_fence<16>(ya);
-        reg_fence<16>(yb);
-        if (gi == 0) load_block(base, half, 1, 0, n_max, xa, xb);
-        p_block<kMask, false>(base, half, gi, 1, n_max, ncol, scale, m, ya, yb, u);
+        float u[16];
+#pragma unroll
+        for (int i = 0; i < 16; ++i) {
+            const float p0 = __fadd_rn(pa[32 * gi + i], pb[32 * gi + i]);            // 0 + p = p exactly (p >= 0)
+            const float p1 = __fadd_rn(pa[32 * gi + 16 + i], pb[32 * gi + 16 + i]);
+            u[i] = __fadd_rn(p0, p1);
+        }
 #pragma unroll
         for (int off = 8; off >= 1; off >>= 1)
 #pragma unroll
             for (int i = 0; i < off; ++i) u[i] = __fadd_rn(u[i], u[i + off]);
-        if (gi == 0)
-            w0 = u[0];
-        else
-            w1 = u[0];
+        w[gi] = u[0];
     }
-    m_out = m;
     if (half == 0) {
-        w01 = __fadd_rn(w0, w1);
+        w01 = __fadd_rn(w[0], w[1]);
     } else {
-        sm.xsum[0][row] = w0;
-        sm.xsum[1][row] = w1;
+        sm.xsum[0][row] = w[0];
+        sm.xsum[1][row] = w[1];
         w01 = 0.0f;
     }
 }
@@ -390,7 +407,7 @@ struct PendingOut {
     int32_t t0, tokens, g;  // first token, tokens of the run, KV head
 };
 
-// out = O / L of a finished run, staged through shared memory and written
+// out = O * fl(1 / L) of a finished run, staged through shared memory and written
 // with 16-byte stores.  Every thread takes part: each writes its half of its
 // row (a row without keys: zeros), then all copy whole rows out.  bf16 rows
 // fit the stage at once, fp32 rows in two passes of half the dims.
@@ -400,6 +417,7 @@ __device__ __forceinline__ void write_out(Smem<DH>& sm, uint32_t tmem, const Att
     constexpr int kHalfDims = DH / 2;
     constexpr int kCPR = DH / 8;  // 16-byte chunks per stage row (DH * 2 bytes)
     const float L = half == 0 ? L_lower : sm.xL[row];
+    const float rl = __frcp_rn(L);  // out = O * fl(1 / L), as the decode merge computes it
     const int passes = geo.out_f32 ? 2 : 1;
     const int esize = geo.out_f32 ? 4 : 2;
     for (int p = 0; p < passes; ++p) {
@@ -412,7 +430,7 @@ __device__ __forceinline__ void write_out(Smem<DH>& sm, uint32_t tmem, const Att
                 reg_fence<32>(O);
                 float val[32];
 #pragma unroll
-                for (int x = 0; x < 32; ++x) val[x] = has ? __fdiv_rn(__uint_as_float(O[x]), L) : 0.0f;
+                for (int x = 0; x < 32; ++x) val[x] = has ? __fmul_rn(__uint_as_float(O[x]), rl) : 0.0f;
                 if (geo.out_f32) {
 #pragma unroll
                     for (int c = 0; c < 8; ++c) {
@@ -589,10 +607,72 @@ __device__ __forceinline__ void produce(Smem<DH>& sm, const CUtensorMap* tmK, co
     __syncwarp();
 }
 
+// The MMA thread (lane 0 of warp 9): per chunk S = Q K^T once the chunk's
+// keys (and the run's queries) have landed and the previous chunk's PV
+// product is done; PV of keys 0-127 once the consumers have written their P
+// and the values have landed; PV of keys 128-255 once that P is written.
+// Reads the run descriptors to know the chunk counts.  Before it returns no
+// product is in flight.
+template <int DH>
+__device__ __forceinline__ void issue_products(Smem<DH>& sm, uint32_t tmem) {
+    const uint32_t idesc_s = ptx::idesc_bf16_f32(kRows, kChunk);
+    const uint32_t idesc_pv = ptx::idesc_bf16_f32(kRows, DH) | (1u << 16);  // B (V) MN-major
+    volatile int32_t* abort = &sm.abort;
+    uint32_t runs = 0, chunks = 0, q_runs = 0;
+    bool ok = true, issued = false;
+    auto pv_steps = [&](int k_begin, int k_end) {  // 16-key steps: the hi part, then the lo part
+        for (int ks = k_begin; ks < k_end; ++ks) {
+            const uint64_t bd = desc(smem_u32(&sm.v[0][0]) + static_cast<uint32_t>(ks * 2048), kVLbo, kVSbo);
+            mma_ts(tmem + kColO, tmem + kColS + 16 * ks, bd, idesc_pv, 1u);
+            mma_ts(tmem + kColO, tmem + kColS + 16 * ks + 8, bd, idesc_pv, 1u);
+        }
+    };
+    while (ok) {
+        const int slot = runs & 1;
+        if (!(ok = ptx::mbar_wait_bounded(&sm.rd_full[slot], (runs >> 1) & 1u, abort))) break;
+        const int32_t tokens = sm.rd[slot].tokens, count = sm.rd[slot].count, s_max = sm.rd[slot].s_max;
+        mbar_arrive(&sm.rd_empty[slot]);
+        ++runs;
+        if (tokens < 0) break;
+        for (int32_t j = 0; j < count; ++j, ++chunks) {
+            const int32_t n_max = min(kChunk, s_max - j * kChunk);
+            const int steps = (n_max + 15) / 16;
+            if (j == 0 && !(ok = ptx::mbar_wait_bounded(&sm.q_full, (q_runs++) & 1u, abort))) break;
+            // the previous chunk's PV product has read its P (in the S columns)
+            if (issued && !(ok = ptx::mbar_wait_bounded(&sm.pv_done, (chunks - 1) & 1u, abort))) break;
+            if (!(ok = ptx::mbar_wait_bounded(&sm.k_full, chunks & 1u, abort))) break;
+            ptx::tc_fence_after();
+#pragma unroll
+            for (int ks = 0; ks < DH / 16; ++ks) {
+                const uint32_t step = static_cast<uint32_t>((ks % 4) * 32);
+                ptx::tc_mma_f16<1>(tmem + kColS, desc(smem_u32(&sm.q[ks / 4][0]) + step, 16, 1024),
+                                   desc(smem_u32(&sm.k[ks / 4][0]) + step, 16, 1024), idesc_s, ks > 0);
+            }
+            ptx::tc_commit<1>(&sm.s_done);
+            issued = true;
+            if (!(ok = ptx::mbar_wait_bounded(&sm.pa_ready, chunks & 1u, abort))) break;
+            if (!(ok = ptx::mbar_wait_bounded(&sm.v_full, chunks & 1u, abort))) break;
+            ptx::tc_fence_after();
+            pv_steps(0, min(steps, 8));
+            if (!(ok = ptx::mbar_wait_bounded(&sm.pb_ready, chunks & 1u, abort))) break;
+            ptx::tc_fence_after();
+            pv_steps(8, steps);
+            ptx::tc_commit<1>(&sm.pv_done);
+        }
+    }
+    if (!ok) *abort = 1;
+    // no product may be in flight when tensor memory is freed
+    if (issued) {
+        ptx::tc_commit<1>(&sm.drain);
+        volatile int32_t none = 0;
+        ptx::mbar_wait_bounded(&sm.drain, 0, &none);
+    }
+}
+
 // Persistent CTAs, one per SM: warps 0-7 consume runs (two threads per query
-// row: softmax, fold, output; thread 0 issues the MMAs), warp 8 produces them
-// (descriptors and copies); warps 9-11 complete warp 8's warpgroup, whose
-// registers go to the consumers.
+// row: softmax, fold, output), warp 8 produces them (descriptors and copies),
+// lane 0 of warp 9 issues the tensor-core products; warps 10 and 11 complete
+// that warpgroup, whose registers go to the consumers.
 template <int G, int DH>
 __global__ void __launch_bounds__(kThreads, 1)
 prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -613,9 +693,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
         ptx::mbar_init(&sm.v_full, 1);
         ptx::mbar_init(&sm.s_done, 1);
         ptx::mbar_init(&sm.pv_done, 1);
+        ptx::mbar_init(&sm.drain, 1);
+        ptx::mbar_init(&sm.pa_ready, kConsumers);
+        ptx::mbar_init(&sm.pb_ready, kConsumers);
         for (int i = 0; i < 2; ++i) {
             ptx::mbar_init(&sm.rd_full[i], 1);
-            ptx::mbar_init(&sm.rd_empty[i], kConsumers);
+            ptx::mbar_init(&sm.rd_empty[i], kConsumers + 1);  // the consumers and the MMA thread
         }
         ptx::fence_barrier_init();
     }
@@ -629,33 +712,29 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
     const uint32_t tmem = sm.tmem_base;
     if (warp >= kConsumers / 32) {
         asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kProducerRegs));
-        if (warp == kConsumers / 32) produce<G, DH>(sm, &tmK, &tmV, &tmQ, geo, em, n_entries);
+        if (warp == kConsumers / 32) {
+            produce<G, DH>(sm, &tmK, &tmV, &tmQ, geo, em, n_entries);
+        } else if (warp == kConsumers / 32 + 1 && lane == 0) {
+            issue_products<DH>(sm, tmem);
+        }
     } else {
         asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kConsumerRegs));
         const int half = warp >> 2;              // which half of the row's keys and dims
         const int row = 32 * (warp & 3) + lane;  // the row, = its TMEM lane
-        const uint32_t idesc_s = ptx::idesc_bf16_f32(kRows, kChunk);
-        const uint32_t idesc_pv = ptx::idesc_bf16_f32(kRows, DH) | (1u << 16);  // B (V) MN-major
         const uint32_t col_o = kColO + half * kHalfDims, col_run = kColRun + half * kHalfDims;
         volatile int32_t* abort = &sm.abort;
         zero_cols<kHalfDims>(lane_addr(tmem, col_o));  // o starts at zero (and is zeroed after every fold)
-        uint32_t runs = 0, chunks = 0, q_runs = 0;     // descriptors, chunks and queries consumed
-        bool s_pending = false, pv_pending = false;    // products in flight
+        uint32_t runs = 0, chunks = 0;
         bool ok = true;
         PendingOut po{false, 0, 0, 0};
         bool po_has = false;  // this thread's row of the pending run has keys
         float po_L = 0.0f;
-
-        auto issue_s = [&]() {  // thread 0: S = Q K^T of the chunk in sm.k
-#pragma unroll
-            for (int ks = 0; ks < DH / 16; ++ks) {
-                const uint32_t step = static_cast<uint32_t>((ks % 4) * 32);
-                ptx::tc_mma_f16<1>(tmem + kColS, desc(smem_u32(&sm.q[ks / 4][0]) + step, 16, 1024),
-                                   desc(smem_u32(&sm.k[ks / 4][0]) + step, 16, 1024), idesc_s, ks > 0);
-            }
-            ptx::tc_commit<1>(&sm.s_done);
+        // P written (TMEM stores and generic shared-memory writes done) before the products read it
+        auto p_ready = [&](uint64_t* bar) {
+            tmem_st_wait();
+            ptx::tc_fence_before();
+            mbar_arrive(bar);
         };
-
         while (ok) {
             // ---- the next run's descriptor ----
             const int slot = runs & 1;
@@ -668,14 +747,6 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             const bool mine = row / G < tokens;
             mbar_arrive(&sm.rd_empty[slot]);
             ++runs;
-            if (count > 0) {
-                if (!(ok = wait_all(&sm.q_full, q_runs & 1u, abort))) break;
-                ++q_runs;
-                if (!(ok = wait_all(&sm.k_full, chunks & 1u, abort))) break;
-                ptx::tc_fence_after();
-                if (tid == 0) issue_s();
-                s_pending = true;
-            }
             // the previous run's output, while this run's first scores are computed
             if (po.on) {
                 write_out<G, DH>(sm, tmem, geo, po, half, row, po_has, po_L);
@@ -688,13 +759,12 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 const int32_t ncol = mine ? min(max(keys - k0, 0), kChunk) : 0;
                 const bool masked = k0 + kChunk > s_min;  // some row of the run stops inside this chunk
                 if (!(ok = wait_all(&sm.s_done, chunks & 1u, abort))) break;
-                s_pending = false;
                 ptx::tc_fence_after();
-                float m, w01;
+                float m, w01, pa[64];
                 if (masked)
-                    softmax_half<true, DH>(sm, tmem, half, row, n_max, ncol, geo.scale, m, w01);
+                    softmax_lo<true, DH>(sm, tmem, half, row, n_max, ncol, geo.scale, m, pa);
                 else
-                    softmax_half<false, DH>(sm, tmem, half, row, n_max, ncol, geo.scale, m, w01);
+                    softmax_lo<false, DH>(sm, tmem, half, row, n_max, ncol, geo.scale, m, pa);
                 if (!(ok = wait_all(&sm.v_full, chunks & 1u, abort))) break;
                 // V rows past the last key up to the 16-key step meet p = 0 in the MMAs:
                 // zeros, not whatever the page holds there
@@ -707,34 +777,17 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                     }
                     ptx::fence_proxy_async_smem();
                 }
-                tmem_st_wait();
-                ptx::tc_fence_before();
-                consumer_sync();
-                ptx::tc_fence_after();
+                p_ready(&sm.pa_ready);  // PV of keys 0-127 runs during the second phase
+                if (masked)
+                    softmax_hi<true, DH>(sm, tmem, half, row, n_max, ncol, geo.scale, m, pa, w01);
+                else
+                    softmax_hi<false, DH>(sm, tmem, half, row, n_max, ncol, geo.scale, m, pa, w01);
+                p_ready(&sm.pb_ready);
+                consumer_sync();  // the upper half's group sums
                 // l in the decode routine's order: ((group 0 + group 1) + group 2) + group 3
                 const float l = half == 0 ? __fadd_rn(__fadd_rn(w01, sm.xsum[0][row]), sm.xsum[1][row]) : 0.0f;
-                // o = P V: per 16-key step the hi part, then the lo part
-                if (tid == 0) {
-                    const int steps = (n_max + 15) / 16;
-                    for (int ks = 0; ks < steps; ++ks) {
-                        const uint64_t bd =
-                            desc(smem_u32(&sm.v[0][0]) + static_cast<uint32_t>(ks * 2048), kVLbo, kVSbo);
-                        mma_ts(tmem + kColO, tmem + kColS + 16 * ks, bd, idesc_pv, 1u);
-                        mma_ts(tmem + kColO, tmem + kColS + 16 * ks + 8, bd, idesc_pv, 1u);
-                    }
-                    ptx::tc_commit<1>(&sm.pv_done);
-                }
-                pv_pending = true;
                 if (!(ok = wait_all(&sm.pv_done, chunks & 1u, abort))) break;
-                pv_pending = false;
                 ptx::tc_fence_after();
-                // the next chunk's scores while this chunk is folded
-                if (j + 1 < count) {
-                    if (!(ok = wait_all(&sm.k_full, (chunks + 1) & 1u, abort))) break;
-                    ptx::tc_fence_after();
-                    if (tid == 0) issue_s();
-                    s_pending = true;
-                }
                 // the decode merge's fold; a row without keys in this chunk keeps its state
                 const bool active = ncol > 0;
                 float a = 1.0f, bw = 1.0f;
@@ -770,8 +823,7 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                     }
                 }
                 zero_cols<kHalfDims>(lane_addr(tmem, col_o));  // the next chunk's o starts at zero
-                tmem_st_wait();
-                ptx::tc_fence_before();
+                tmem_st_wait();  // O before it is read again (next fold, or the output)
             }
             if (!ok) break;
             // the run's output is written while the next run's first scores are computed
@@ -784,16 +836,10 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
             consumer_sync();  // xL of the last run
             write_out<G, DH>(sm, tmem, geo, po, half, row, po_has, po_L);
         }
-        if (!ok) {
-            // a copy or an MMA did not complete in time: stop the producer,
-            // wait (bounded) for the products still in flight
-            if (tid == 0) {
-                report(geo.status, BI_DEV_TIMEOUT_ATTENTION);
-                *abort = 1;
-            }
-            volatile int32_t none = 0;
-            if (s_pending) wait_all(&sm.s_done, chunks & 1u, &none);
-            if (pv_pending) wait_all(&sm.pv_done, chunks & 1u, &none);
+        if (!ok && tid == 0) {
+            // a copy or a product did not complete in time: stop the other roles
+            report(geo.status, BI_DEV_TIMEOUT_ATTENTION);
+            *abort = 1;
         }
     }
     ptx::tc_fence_before();
