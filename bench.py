@@ -333,6 +333,54 @@ def prefill_measure(device: str, steps: int, bf16_peak: float, stream) -> dict:
                              "frac": round(gu_tf / bf16_peak, 3), "peak_tflops": bf16_peak}}
 
 
+def model32_measure(device: str, steps: int, hbm_peak: float, stream) -> dict:
+    """The full 32-layer Llama-3-8B-shaped model (random-init weights): one decode step (every layer, final
+    norm, LM head, greedy argmax) by CUDA-graph replay at bs 1, 16 and 64, invariant vs batch-variant.
+    Contexts U[128, 4096] (the prompt lengths of the 32-layer configuration), KV history N(0, 1) in every
+    layer, pages from the engine's shuffled pool.  Roofline bytes: every layer's weights, the LM head, each
+    request's KV in every layer and the activations (roofline.decode_step_bytes)."""
+    import torch
+    from invariant_fixed_order_gb300 import bi, roofline, synth
+    from invariant_fixed_order_gb300.config import LLAMA3_8B
+    from invariant_fixed_order_gb300.engine import Engine
+    from invariant_fixed_order_gb300.graphs import DecodeGraphs
+    cfg = LLAMA3_8B
+    B = 64
+    ctx = [int(x) for x in synth.uniform_ints(B, 128, 4096, DATA_SEED + 2)]
+    ids = synth.token_ids(B, cfg.V, DATA_SEED + 3)
+    max_pages = 4096 // 16 + 1
+    pages = sum((s + 15) // 16 for s in ctx)
+    eng = Engine(cfg, seed=WEIGHT_SEED, num_pages=pages + 8, max_pages=max_pages, max_T=B, max_B=B, max_R=B,
+                 max_seq=max_pages * 16, device=device)
+    table = np.zeros((B, max_pages), np.int32)
+    for i, s in enumerate(ctx):
+        pg = eng.pool.alloc((s + 15) // 16)
+        table[i, :len(pg)] = pg
+    g = torch.Generator(device=device).manual_seed(DATA_SEED * 7919)
+    for layer in range(cfg.n_layers):  # the KV history of every layer: N(0, 1) bf16
+        for t in (eng.k[layer], eng.v[layer]):
+            t.copy_(torch.randn(t.shape, generator=g, device=device, dtype=torch.float32).to(torch.bfloat16))
+    positions = [s - 1 for s in ctx]
+    out = {"layers": cfg.n_layers, "context": [128, 4096], "path": "bi_forward_step by CUDA-graph replay",
+           "weights_gb": round(roofline.step_weight_bytes(cfg) / 1e9, 2), "rows": []}
+    rows = {b: {"bs": b} for b in (1, 16, 64)}
+    for name, mode in (("invariant", bi.INVARIANT), ("variant", bi.VARIANT)):
+        graphs = DecodeGraphs(eng, max(ctx), ladder=(1, 16, 64), mode=mode)
+        for b in (1, 16, 64):
+            graphs.step(ids[:b], positions[:b], table[:b], bucket=b)
+            t = time_steps(graphs.buckets[b][0].replay, max(steps, 10), 3, stream)
+            nbytes = roofline.decode_step_bytes(cfg, ctx[:b])
+            rows[b][name + "_tok_s"] = round(b / (t * 1e-3), 1)
+            rows[b][name + "_ms"] = round(t, 3)
+            rows[b][name + "_hbm_frac"] = round(nbytes / (t * 1e-3) / 1e9 / hbm_peak, 3)
+            rows[b]["step_gb"] = round(nbytes / 1e9, 2)
+        graphs.close()
+    eng.check()
+    eng.close()
+    out["rows"] = [rows[b] for b in (1, 16, 64)]
+    return out
+
+
 def gemm_traffic(per_launch_bytes_of: str):
     """Per-launch DRAM traffic of gemm_tc_kernel from the committed ncu summary,
     if it was captured on the current kernel source (else None)."""
@@ -541,6 +589,9 @@ def run_ours(args):
     torch.cuda.empty_cache()
     _, bf16_peak, _ = peaks()
     pre = prefill_measure(device, args.steps, bf16_peak, stream) if not args.no_sweep else None
+    torch.cuda.empty_cache()
+    m32 = model32_measure(device, args.steps, hbm_peak, stream) if not args.no_sweep else None
+    torch.cuda.empty_cache()
     clocks = sampler.stop()
 
     cpu = None
@@ -572,6 +623,8 @@ def run_ours(args):
         }
         if pre is not None:
             line["prefill"] = pre
+        if m32 is not None:
+            line["model32"] = m32
         if cpu is not None:
             line["cpu_baseline"] = cpu
         print(json.dumps(line), flush=True)

@@ -142,6 +142,20 @@ bi_status bi_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype,
                   int64_t M, int32_t N, int32_t K, bi_mode mode,
                   void* ws, size_t ws_bytes, int32_t* dev_status, bi_stream stream);
 
+/* bi_gemm's failure-detection check (for tests; the pages have no
+ * counterpart).  Runs bi_gemm (BI_INVARIANT, no epilogue) with two changes:
+ * every bounded wait of the kernel gives up after wait_limit_ns (1 ms to 2 s),
+ * and the copies of ring stage skip_stage (counted in issue order from 0, in
+ * every CTA of a pair; -1: none) are never issued.  The MMA issuer's wait for
+ * that stage then runs out: the kernel writes BI_DEV_TIMEOUT_MMA into
+ * dev_status (DEVICE, required), every role stops, the copies and products
+ * in flight are drained, tensor memory is freed and the kernel returns; C
+ * holds no defined values.  Nothing faults or waits without a bound, and the
+ * stream stays usable. */
+bi_status bi_gemm_wait_test(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype, int64_t M,
+                            int32_t N, int32_t K, uint64_t wait_limit_ns, int32_t skip_stage,
+                            int32_t* dev_status, bi_stream stream);
+
 /* Packs logical gate [F, d] and up [F, d] weights into the interleaved [2F, d]
  * layout BI_EP_SWIGLU reads: rows 64j..64j+31 = gate rows 32j..32j+31, rows
  * 64j+32..64j+63 = up rows 32j..32j+31.  All DEVICE; F % 32 == 0. */

@@ -81,6 +81,7 @@ _proto("bi_rmsnorm", _i32, _vp, _vp, _vp, _i64, _i32, _f32, _vp)
 _proto("bi_gemm_workspace_size", _sz, _i64, _i32, _i32, _i32)
 _proto("bi_gemm", _i32, _vp, _vp, _vp, _i32, _vp, _i32, _i64, _i32, _i32, _i32, _vp, _sz, _vp, _vp)
 _proto("bi_pack_gate_up", _i32, _vp, _vp, _vp, _i32, _i32, _vp)
+_proto("bi_gemm_wait_test", _i32, _vp, _vp, _vp, _i32, _i64, _i32, _i32, ctypes.c_uint64, _i32, _vp, _vp)
 _proto("bi_rope_kv_append", _i32, _vp, _vp, _vp, _vp, _vp, _i32, _vp, _vp, _vp, _vp, _i32, _i32, _i32, _i32, _i32,
        _i32, _vp, _vp)
 _proto("bi_rope_table", _i32, _vp, _vp, _i32, _i32, _f64)
@@ -217,6 +218,19 @@ def gemm(A: torch.Tensor, W: torch.Tensor, out: torch.Tensor | None = None, c_dt
                         _d(ws, "ws", optional=True), 0 if ws is None else ws.numel() * ws.element_size(),
                         _d(status, "status", _I32, optional=True), _stream(stream)))
     return out
+
+
+def gemm_wait_test(A: torch.Tensor, W: torch.Tensor, out: torch.Tensor, status: torch.Tensor,
+                   wait_limit_ns: int = 1_000_000, skip_stage: int = 0, stream=None) -> None:
+    """bi_gemm_wait_test: the GEMM with a short wait limit and one ring stage's copies withheld (its bounded
+    wait runs out and the kernel reports through status)."""
+    _shape(A, "A", None, None)
+    M, K = A.shape
+    _shape(W, "W", None, K)
+    N = W.shape[0]
+    _shape(out, "out", M, N)
+    _check(_lib.bi_gemm_wait_test(_d(A, "A", _BF16), _d(W, "W", _BF16), _d(out, "out", _F32), F32, M, N, K,
+                                  wait_limit_ns, skip_stage, _d(status, "status", _I32), _stream(stream)))
 
 
 def pack_gate_up(w_gate: torch.Tensor, w_up: torch.Tensor, stream=None) -> torch.Tensor:

@@ -8,6 +8,7 @@
 #include <string>
 #include <vector>
 
+#include "common.cuh"
 #include "internal.h"
 
 namespace bi {
@@ -125,6 +126,19 @@ extern "C" bi_status bi_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dty
     if (st != BI_OK || M == 0) return st;
     return run_gemm(A, W, C, c_dtype, residual, ep, M, N, K, mode, ws, ws_bytes, dev_status,
                     static_cast<cudaStream_t>(stream));
+}
+
+extern "C" bi_status bi_gemm_wait_test(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype, int64_t M,
+                                       int32_t N, int32_t K, uint64_t wait_limit_ns, int32_t skip_stage,
+                                       int32_t* dev_status, bi_stream stream) {
+    bi_status st = check_gemm_args(A, W, C, c_dtype, nullptr, BI_EP_NONE, M, N, K, BI_INVARIANT);
+    if (st != BI_OK || M == 0) return st;
+    if (!dev_status) return fail(BI_ERR_INVALID, "bi_gemm_wait_test: needs dev_status");
+    if (wait_limit_ns < 1000000ull || wait_limit_ns > kWaitLimitNs)
+        return fail(BI_ERR_INVALID, "bi_gemm_wait_test: wait limit outside [1 ms, 2 s]");
+    const GemmWaitTest wt{wait_limit_ns, skip_stage};
+    return run_gemm(A, W, C, c_dtype, nullptr, BI_EP_NONE, M, N, K, BI_INVARIANT, nullptr, 0, dev_status,
+                    static_cast<cudaStream_t>(stream), false, nullptr, nullptr, &wt);
 }
 
 extern "C" bi_status bi_pack_gate_up(const bi_bf16* w_gate, const bi_bf16* w_up, bi_bf16* w_gu, int32_t F,

@@ -183,11 +183,18 @@ size_t gemm_ws_bytes(int64_t M, int32_t N, int32_t K, bi_mode mode);
 // earlier work on the stream), so W may be fetched before the dependency wait.
 // am (optional, fp32 output, no epilogue, plan without split-K): fused greedy
 // argmax over each row's N outputs; C may then be null (outputs not stored).
+// The GEMM's failure-detection check: every bounded wait gives up after
+// wait_ns, and the copies of ring stage skip_stage (in issue order, in every
+// CTA of a pair) are withheld, so the MMA issuer's wait for them runs out.
+struct GemmWaitTest {
+    uint64_t wait_ns;
+    int32_t skip_stage;
+};
 bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype,
                    const bi_bf16* residual, bi_epilogue ep, int64_t M, int32_t N, int32_t K,
                    bi_mode mode, void* ws, size_t ws_bytes, int32_t* status, cudaStream_t s,
                    bool weights_settled = false, const ArgmaxFuse* am = nullptr,
-                   const RopeFuse* rope = nullptr);
+                   const RopeFuse* rope = nullptr, const GemmWaitTest* wait_test = nullptr);
 // whether run_gemm can fuse RoPE + KV append for this shape and mode
 bool gemm_can_fuse_rope(int64_t M, int32_t N, int32_t K, bi_mode mode, int32_t Dh);
 

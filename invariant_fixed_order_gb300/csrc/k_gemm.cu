@@ -95,6 +95,8 @@ struct GemmArgs {
     int32_t rope_on;       // 1: the epilogue applies RoPE and appends K/V (rope) instead of storing C
     RopeFuse rope;
     int32_t* status;
+    uint64_t wait_ns;      // bound of every wait (2 s; shorter in the wait test)
+    int32_t skip_stage;    // wait test: the ring stage (in issue order) whose copies are withheld, else -1
 };
 
 __device__ __forceinline__ float silu_mul(float g, float u) {
@@ -406,15 +408,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         // armed, W already requested: only A is missing
                         load(sA + s * kps * args.a_stride, &tmA, s, a_row, kb0 + kb, pol_a);
                     } else {
-                        if (!ptx::mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag)) {
+                        if (!ptx::mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag, args.wait_ns)) {
                             if (!*abort_flag) report(args.status, BI_DEV_TIMEOUT_PRODUCER);
                             raise_abort();
                             ok = false;
                             break;
                         }
-                        if (rank == 0) ptx::mbar_arrive_expect_tx(&full[s], stage_tx);
-                        load(sA + s * kps * args.a_stride, &tmA, s, a_row, kb0 + kb, pol_a);
-                        load(sW + s * kps * kWBytes, &tmW, s, n_tile * BN + w_row0, kb0 + kb, pol_w);
+                        if (static_cast<int32_t>(issued) != args.skip_stage) {
+                            if (rank == 0) ptx::mbar_arrive_expect_tx(&full[s], stage_tx);
+                            load(sA + s * kps * args.a_stride, &tmA, s, a_row, kb0 + kb, pol_a);
+                            load(sW + s * kps * kWBytes, &tmW, s, n_tile * BN + w_row0, kb0 + kb, pol_w);
+                        }
                     }
                     ++issued;
                     if (++s == S) {
@@ -432,7 +436,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     const uint32_t qph = (q / S) & 1u;
                     const uint64_t t0 = globaltimer_ns();
                     while (!ptx::mbar_try_wait(smem_u32(&full[qs]), qph)) {
-                        if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                        if (globaltimer_ns() - t0 > args.wait_ns) {
                             report(args.status, BI_DEV_TIMEOUT_DRAIN);
                             break;
                         }
@@ -457,7 +461,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             bool ok = true;
             for (int32_t tile = unit; tile < args.total_tiles && ok; tile += nunits, ++i) {
                 const int b = i & 1;
-                if (!ptx::mbar_wait_bounded(&acc_empty[b], ((static_cast<uint32_t>(i) >> 1) & 1u) ^ 1u, abort_flag)) {
+                if (!ptx::mbar_wait_bounded(&acc_empty[b], ((static_cast<uint32_t>(i) >> 1) & 1u) ^ 1u, abort_flag,
+                                            args.wait_ns)) {
                     if (!*abort_flag) report(args.status, BI_DEV_TIMEOUT_MMA);
                     raise_abort();
                     break;
@@ -466,7 +471,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 const uint32_t acc = tmem + static_cast<uint32_t>(b * BN);
                 for (int32_t kb = 0; kb < nkb; kb += kps) {
                     const int cnt = min(kps, nkb - kb);
-                    if (!ptx::mbar_wait_bounded(&full[s], ph, abort_flag)) {
+                    if (!ptx::mbar_wait_bounded(&full[s], ph, abort_flag, args.wait_ns)) {
                         if (!*abort_flag) report(args.status, BI_DEV_TIMEOUT_MMA);
                         raise_abort();
                         ok = false;
@@ -499,7 +504,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         if (lane == 0) {
             const uint64_t t0 = globaltimer_ns();
             while (!ptx::mbar_try_wait(smem_u32(drain), 0)) {
-                if (globaltimer_ns() - t0 > kWaitLimitNs) {
+                if (globaltimer_ns() - t0 > args.wait_ns) {
                     report(args.status, BI_DEV_TIMEOUT_DRAIN);
                     break;
                 }
@@ -527,7 +532,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     }
                 }
             }
-            const bool ready = ptx::mbar_wait_bounded(&acc_full[b], (static_cast<uint32_t>(i) >> 1) & 1u, abort_flag);
+            const bool ready =
+                ptx::mbar_wait_bounded(&acc_full[b], (static_cast<uint32_t>(i) >> 1) & 1u, abort_flag, args.wait_ns);
             if (!ready && !*abort_flag) report(args.status, BI_DEV_TIMEOUT_EPILOGUE);
             if (!__all_sync(0xffffffffu, ready && !*abort_flag)) break;
             ptx::tc_fence_after();
@@ -820,7 +826,7 @@ bool gemm_can_fuse_rope(int64_t M, int32_t N, int32_t K, bi_mode mode, int32_t D
 bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype, const bi_bf16* residual,
                    bi_epilogue ep, int64_t M, int32_t N, int32_t K, bi_mode mode, void* ws, size_t ws_bytes,
                    int32_t* status, cudaStream_t s, bool weights_settled, const ArgmaxFuse* am,
-                   const RopeFuse* rope) {
+                   const RopeFuse* rope, const GemmWaitTest* wait_test) {
     if (M == 0) return BI_OK;
     const GemmPlan plan = gemm_plan(M, N, K, mode);
     const Layout L = choose_layout(M, N, K);
@@ -848,8 +854,10 @@ bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype
     a.a_region = L.a_region;
     a.stages = L.stages;
     a.kps = L.kps;
-    a.w_early = weights_settled ? 1 : 0;
+    a.w_early = weights_settled && wait_test == nullptr ? 1 : 0;
     a.status = status;
+    a.wait_ns = wait_test != nullptr ? wait_test->wait_ns : kWaitLimitNs;
+    a.skip_stage = wait_test != nullptr ? wait_test->skip_stage : -1;
     if (rope != nullptr) {
         if (!gemm_can_fuse_rope(M, N, K, mode, rope->Dh) || am != nullptr || ep != BI_EP_NONE ||
             N != (rope->H + 2 * rope->Hkv) * rope->Dh)

@@ -37,8 +37,9 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
     return ok != 0;
 }
 // Waits for the phase with the given parity to complete.  Gives up (returns
-// false) after kWaitLimitNs or once *abort is set by another role.
-__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int32_t* abort) {
+// false) after limit_ns or once *abort is set by another role.
+__device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int32_t* abort,
+                                                  uint64_t limit_ns = kWaitLimitNs) {
     const uint32_t addr = smem_u32(bar);
     if (mbar_try_wait(addr, parity)) return true;
     const uint64_t t0 = globaltimer_ns();
@@ -46,7 +47,7 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
         if (mbar_try_wait(addr, parity)) return true;
         if ((i & 255u) == 0u) {
             if (*abort) return false;
-            if (globaltimer_ns() - t0 > kWaitLimitNs) return false;
+            if (globaltimer_ns() - t0 > limit_ns) return false;
         }
     }
 }

@@ -59,6 +59,11 @@ def case_gemm_validation(lib):
     # misaligned pointer
     assert call(lib, "bi_gemm", P(0x10004), FAKE, FAKE, i32(1), None, i32(0), i64(4), i32(128), i32(128), i32(0),
                 None, sz(0), None, None) == BI_ERR_INVALID
+    # the wait test: a limit outside [1 ms, 2 s], no status word
+    assert call(lib, "bi_gemm_wait_test", FAKE, FAKE, FAKE, i32(1), i64(1), i32(128), i32(64),
+                ctypes.c_uint64(1000), i32(0), FAKE, None) == BI_ERR_INVALID
+    assert call(lib, "bi_gemm_wait_test", FAKE, FAKE, FAKE, i32(1), i64(1), i32(128), i32(64),
+                ctypes.c_uint64(1000000), i32(0), None, None) == BI_ERR_INVALID
     # M = 0 is a valid no-op
     assert call(lib, "bi_gemm", None, None, None, i32(1), None, i32(0), i64(0), i32(128), i32(128), i32(0),
                 None, sz(0), None, None) == BI_OK

@@ -62,3 +62,29 @@ def test_step_without_logit_rows(bi):
     assert torch.equal(h_with.view(torch.int16), h_without.view(torch.int16))
     eng.check()
     eng.close()
+
+
+def _int_bf16(shape, seed):
+    g = torch.Generator().manual_seed(seed)
+    return torch.randint(-8, 9, shape, generator=g).to(torch.bfloat16).cuda()
+
+
+@pytest.mark.parametrize("M,N,K,skip", [(1, 128, 64, 0), (300, 4096, 4096, 5), (64, 131072, 256, 3)])
+def test_gemm_bounded_wait_runs_out_and_the_stream_recovers(bi, M, N, K, skip):
+    """Failure detection of the GEMM without a fault: one ring stage's copies are withheld (in every CTA of a
+    pair), so the MMA issuer's bounded wait runs out after 1 ms; the kernel reports a timeout through the
+    status word, drains what is in flight, frees tensor memory and returns.  The next ordinary GEMM on the
+    same stream is integer-exact.  (The CTA-pair form for N <= 65536, the single-CTA form above.)"""
+    A, W = _int_bf16((M, K), 1 + M), _int_bf16((N, K), 2 + N)
+    out = torch.empty(M, N, dtype=torch.float32, device="cuda")
+    st = bi.new_status()
+    bi.gemm_wait_test(A, W, out, st, wait_limit_ns=1_000_000, skip_stage=skip)
+    with pytest.raises(bi.BIError) as e:
+        bi.check_status(st)
+    assert e.value.status == bi.BI_ERR_TIMEOUT
+    bi.reset_status(st)
+    A2, W2 = _int_bf16((37, 256), 3), _int_bf16((384, 256), 4)
+    C = bi.gemm(A2, W2, c_dtype=bi.F32, status=st)
+    bi.check_status(st)
+    ref = A2.double() @ W2.double().T  # |sums| < 2^24: exact in fp32 in any order
+    assert torch.equal(C.double(), ref)
