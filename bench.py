@@ -51,7 +51,8 @@ def parse():
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
-    p.add_argument("--ncu-target", choices=["gemm-decode64", "gemm-prefill8192", "prefill-attn16"], default=None,
+    p.add_argument("--ncu-target", choices=["gemm-decode64", "gemm-prefill8192", "prefill-attn16", "gemm-o-m1"],
+                   default=None,
                    help="launch only the named GEMMs (twice: warm-up, then the pass to capture) for an ncu "
                         "capture; prints no measurement")
     return p.parse_args()
@@ -666,6 +667,15 @@ def ncu_target(which: str) -> None:
         pos0 = torch.zeros(16, dtype=torch.int32, device="cuda")
         for _ in range(2):
             bi.prefill_attention(q, cu_q, pos0, kc, vc, table)
+        torch.cuda.synchronize()
+        print(json.dumps({"ncu_target": which, "done": True}))
+        return
+    if which == "gemm-o-m1":
+        # the decode-step o projection at M = 1 with its residual epilogue (launched twice)
+        A, W = rnd(1, c.H * c.Dh), rnd(c.d, c.H * c.Dh, std=0.02)
+        res = rnd(1, c.d)
+        for _ in range(2):
+            bi.gemm(A, W, out=res, residual=res, ep=bi.EP_RESIDUAL)
         torch.cuda.synchronize()
         print(json.dumps({"ncu_target": which, "done": True}))
         return

@@ -9,10 +9,9 @@
  * in one fixed order with split points that depend on the request alone:
  *   - RMSNorm: one warp per row, lane-serial over 16-byte chunks, then a fixed
  *     xor-butterfly;
- *   - GEMM: per weight matrix one tcgen05 MMA instruction form, chosen by
- *     the matrix's width N alone (N <= 65536: the two-SM pair form
- *     256x128x16; wider: the single-SM form 128x128x16), bf16 in, fp32
- *     accumulate in TMEM, one K tile (64), K loop in ascending order, no
+ *   - GEMM: tcgen05 MMAs (the two-SM pair form 256x128x16 or the single-SM
+ *     form 128x128x16, which give every element the same bits), bf16 in,
+ *     fp32 accumulate in TMEM, one K tile (64), K loop in ascending order, no
  *     split-K, whatever M is;
  *   - attention: keys cut into chunks of BI_KV_CHUNK positions aligned to key 0
  *     ("Batch invariance and reproducible inference", "1 · Split-K and

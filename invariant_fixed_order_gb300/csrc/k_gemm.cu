@@ -4,10 +4,11 @@
 // accumulation" and "3 · Kernel selection changing with shape": split-K and
 // M-dependent kernel choice are what make a GEMM's per-element order follow
 // the batch.  Here every output element of a weight matrix, for every M, is
-// produced by the same sequence: one tcgen05.mma instruction form (bf16 in,
-// fp32 accumulated in TMEM, N = 128, K = 16), K tiles of 64 in ascending
-// order, inside a K tile the four 16-deep MMAs in ascending order, all into
-// one accumulator.  The form is fixed by the matrix's width N alone:
+// produced by the same sequence: tcgen05.mma products (bf16 in, fp32
+// accumulated in TMEM, N = 128, K = 16), K tiles of 64 in ascending order,
+// inside a K tile the four 16-deep MMAs in ascending order, all into one
+// accumulator.  Two instruction forms give every element the same bits
+// (tested bit for bit), so which one runs is data movement:
 //   * N <= 65536 (the projections of a layer): the CTA-pair form, M = 256
 //     over a cluster of two CTAs on two SMs.  The pair's MMA takes 128 rows of
 //     A from each CTA's shared memory and 64 of its 128 weight rows from
@@ -724,14 +725,18 @@ struct Layout {
     size_t smem;
 };
 
-// The MMA instruction form of a weight matrix, from its width alone (never
-// from M): weight matrices up to kPairMaxN columns have few enough 128-wide
-// output tiles that a tile must be spread over two SMs to use the GPU, and
-// take the pair form (256x128x16 over two SMs, 2 KB of weights per SM per
-// MMA); wider ones (a vocabulary projection) fill every SM many times over
-// and are bound by how fast the tensor cores consume weights, which the
-// single-CTA form (128x128x16, 4 KB of weights per MMA) does faster.
+// The MMA instruction form: weight matrices up to kPairMaxN columns have few
+// enough 128-wide output tiles that a tile must be spread over two SMs to use
+// the GPU, and take the pair form (256x128x16 over two SMs, 2 KB of weights
+// per SM per MMA); wider ones (a vocabulary projection) fill every SM many
+// times over and are bound by how fast the tensor cores consume weights,
+// which the single-CTA form (128x128x16, 4 KB of weights per MMA) does faster.
 constexpr int32_t kPairMaxN = 65536;
+// The two forms give every element the same bits (tested: the same product
+// through either form, bit for bit, at decode and prefill sizes), so the
+// choice is data movement like the tile width.  (Taking the single-CTA form
+// for the gate/up projection at decode sizes, whose 224 tiles fill every SM,
+// was measured no faster: ~50 us either way at M = 64.)
 int mma_group(int32_t N) { return N <= kPairMaxN ? 2 : 1; }
 
 // Layout of one launch.  Only data movement depends on M here; the MMA

@@ -114,6 +114,22 @@ def test_gemm_bf16_and_residual_epilogue(bi):
     assert np.array_equal(bits(Rc), bits(C))
 
 
+@pytest.mark.parametrize("K", [4096, 14336])
+def test_gemm_pair_and_single_forms_give_identical_bits(bi, K):
+    """The CTA-pair MMA form (256x128x16 over two SMs) and the single-CTA form (128x128x16) give every
+    element the same bits, at decode and prefill sizes: the same columns computed by a 4096-wide product
+    (pair form) and by a 65792-wide one (single form).  This is what lets the form follow the tile count."""
+    W = rand_bf16((65792, K), 0.02, 600 + K)
+    for M in (1, 64, 300):
+        A = rand_bf16((M, K), 1.0, 601 + M)
+        pair = bi.gemm(A, W[:4096].contiguous(), c_dtype=bi.F32)
+        single = bi.gemm(A, W, c_dtype=bi.F32)[:, :4096].contiguous()
+        torch.cuda.synchronize()
+        assert np.array_equal(bits(pair), bits(single)), (M, K)
+    del W
+    torch.cuda.empty_cache()
+
+
 def test_gemm_swiglu_epilogue(bi):
     M, F, K = 40, 256, 512
     A = rand_bf16((M, K), 1.0, 500)
