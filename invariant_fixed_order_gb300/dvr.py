@@ -44,6 +44,8 @@ class DvrStats:
     t_decode: float = 0.0
     t_verify: float = 0.0
     verified: set = field(default_factory=set)  # request ids whose windows were verified
+    first_mismatch: list = field(default_factory=list)    # per rolled-back window: index of its first mismatch
+    window_committed: list = field(default_factory=list)  # per verified window: tokens it committed
 
     @property
     def rollback_rate(self) -> float:
@@ -54,12 +56,28 @@ class DvrStats:
         tot = self.t_decode + self.t_verify
         return self.t_verify / tot if tot else 0.0
 
-    def as_dict(self) -> dict:
+    def as_dict(self, window: int | None = None) -> dict:
+        """Counts, times and where windows break: the first-mismatch position of each rolled-back window (its
+        mean, median and a histogram) and the tokens each verified window committed (the verifier's token
+        included).  A window that commits c of its W candidates (plus the verifier's) pays for W fast-path
+        steps and one replay, which is why DVR only pays when mismatches are rare and late."""
         tot = self.t_prefill + self.t_decode + self.t_verify
-        return {"windows": self.windows, "mismatched_windows": self.mismatched_windows,
-                "rollback_rate": self.rollback_rate, "committed": self.committed, "discarded": self.discarded,
-                "committed_tok_s": self.committed / tot if tot else 0.0, "verify_overhead": self.verify_overhead,
-                "t_prefill_s": self.t_prefill, "t_decode_s": self.t_decode, "t_verify_s": self.t_verify}
+        fm = sorted(self.first_mismatch)
+        edges = [0, 1, 4, 16, 64, 1 << 30]
+        hist = {f"{a}-{b - 1}" if b - 1 < (1 << 29) else f"{a}+": sum(1 for k in fm if a <= k < b)
+                for a, b in zip(edges[:-1], edges[1:])}
+        wc = self.window_committed
+        d = {"windows": self.windows, "mismatched_windows": self.mismatched_windows,
+             "rollback_rate": self.rollback_rate, "committed": self.committed, "discarded": self.discarded,
+             "committed_tok_s": self.committed / tot if tot else 0.0, "verify_overhead": self.verify_overhead,
+             "t_prefill_s": self.t_prefill, "t_decode_s": self.t_decode, "t_verify_s": self.t_verify,
+             "first_mismatch_mean": sum(fm) / len(fm) if fm else None,
+             "first_mismatch_median": fm[len(fm) // 2] if fm else None,
+             "first_mismatch_hist": hist,
+             "committed_per_window_mean": sum(wc) / len(wc) if wc else None}
+        if window:
+            d["committed_fraction_mean"] = (sum(wc) / len(wc)) / window if wc else None
+        return d
 
 
 def _groups(seq, n):
@@ -134,9 +152,12 @@ def dvr_generate(runner: Runner, reqs: list, n_new: int, window: int = 64, verif
                 n_prompt = len(r.prompt)
                 if k is None:
                     r.n_cached = L + W - 1
+                    st.window_committed.append(W)
                 else:
                     st.mismatched_windows += 1
                     st.discarded += W - k
+                    st.first_mismatch.append(k)
+                    st.window_committed.append(k + 1)
                     r.generated = r.generated[:L + k - n_prompt] + [int(verified[k])]
                     r.n_cached = L + k
         st.t_verify += _now() - t1

@@ -203,7 +203,8 @@ class FuzzConfig:
 
 
 def fuzz_continuous(runner: Runner, requests: list, n_decode: int, rng: np.random.Generator,
-                    cfg: FuzzConfig, teacher: dict | None = None, all_prompt_logits: bool = True):
+                    cfg: FuzzConfig, teacher: dict | None = None, all_prompt_logits: bool = True,
+                    stats: dict | None = None):
     """A randomised continuous-batching run.  Requests arrive at random steps,
     prefill in random chunks (within the token budget, co-scheduled with the
     decodes of running requests), may be evicted (pages freed) and readmitted
@@ -212,7 +213,10 @@ def fuzz_continuous(runner: Runner, requests: list, n_decode: int, rng: np.rando
     appended instead of the argmax (so logits stay comparable after a
     divergence).  Returns {rid: {position: logits row}} for every position
     whose logits were produced (prompt positions during the first prefill and
-    each decode position)."""
+    each decode position).  stats (optional) receives the counts of steps, evictions and readmissions."""
+    if stats is not None:
+        for k in ("steps", "evictions", "readmissions", "prefill_tokens"):
+            stats.setdefault(k, 0)
     arrival = {r.rid: int(rng.integers(0, cfg.arrival_span)) for r in requests}
     order = list(requests)
     rng.shuffle(order)
@@ -232,6 +236,8 @@ def fuzz_continuous(runner: Runner, requests: list, n_decode: int, rng: np.rando
                 r = next(x for x in requests if x.rid == rid)
                 waiting.append(r)
                 del evicted_until[rid]
+                if stats is not None:
+                    stats["readmissions"] += 1
         items = []
         budget = cfg.token_budget
         rng.shuffle(running)
@@ -259,6 +265,9 @@ def fuzz_continuous(runner: Runner, requests: list, n_decode: int, rng: np.rando
         order_idx = rng.permutation(len(items))
         items = [items[i] for i in order_idx]
         logits, tokens, slices = runner.step(items)
+        if stats is not None:
+            stats["steps"] += 1
+            stats["prefill_tokens"] += sum(it.n_new for it in items if it.n_new > 1)
         for it, sl in zip(items, slices):
             r = it.req
             rows = logits[sl]
@@ -295,5 +304,7 @@ def fuzz_continuous(runner: Runner, requests: list, n_decode: int, rng: np.rando
                 running.remove(r)
                 runner.evict(r)
                 evicted_until[r.rid] = step_no + int(rng.integers(*cfg.readmit_delay))
+                if stats is not None:
+                    stats["evictions"] += 1
         step_no += 1
     return out

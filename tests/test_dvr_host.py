@@ -59,3 +59,38 @@ def test_dvr_forced_divergence_is_rolled_back():
     for r in reqs:
         assert r.generated == greedy(r.prompt, 30, INVARIANT), r.rid
     assert st.mismatched_windows == len(bad)
+
+
+def test_dvr_window_statistics():
+    """Forced divergences at known offsets inside the windows: each rolled-back window's first-mismatch index
+    is recorded, and each verified window commits its matching prefix plus the verifier's token."""
+    rng = np.random.default_rng(2)
+    prompts = [rng.integers(0, V, 20).astype(np.int32) for _ in range(4)]
+    runner = sched.Runner(FakeEngine(), mode=INVARIANT)
+    reqs = [sched.Request(i, p) for i, p in enumerate(prompts)]
+    # the first window of request i covers positions 21 .. 28 (prompt 20, first token from the prefill)
+    bad = {(i, 21 + 2 * i) for i in range(4)}
+    st = dvr.dvr_generate(runner, reqs, 30, window=8, verify_batch=2, fast_mode=INVARIANT,
+                          corrupt=lambda rid, pos: (rid, pos) in bad)
+    assert sorted(st.first_mismatch) == [0, 2, 4, 6]
+    d = st.as_dict(window=8)
+    assert d["first_mismatch_mean"] == 3.0 and d["first_mismatch_median"] == 4
+    assert d["first_mismatch_hist"]["0-0"] == 1 and d["first_mismatch_hist"]["1-3"] == 1
+    assert d["first_mismatch_hist"]["4-15"] == 2
+    # windows without a mismatch commit all 8; the four rolled-back ones commit k + 1
+    assert sorted(k for k in st.window_committed if k < 8) == [1, 3, 5, 7]
+    assert len(st.window_committed) == st.windows
+    assert 0 < d["committed_fraction_mean"] <= 1
+
+
+def test_results_record_is_atomic_and_complete(tmp_path, monkeypatch):
+    from invariant_fixed_order_gb300 import results
+    monkeypatch.setenv("BI_GIT_SHA", "0123abc")
+    assert results.record("x", {"a": 1}, directory=None) is None or "BI_RESULTS_DIR" in __import__("os").environ
+    path = results.record("unique", {"max_completions": 1, "bound": 0.0009}, directory=str(tmp_path))
+    import json
+    import os
+    j = json.load(open(path))
+    assert j["name"] == "unique" and j["result"]["max_completions"] == 1
+    assert j["environment"]["git_sha"] == "0123abc" and "time_utc" in j["environment"]
+    assert [f for f in os.listdir(tmp_path)] == ["unique.json"]  # no temporary left behind

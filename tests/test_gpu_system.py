@@ -12,12 +12,13 @@ Sizes are reduced from the full configurations so the suite stays within
 minutes; BI_SYSTEM_SCALE=full runs the full ones (32 layers, 64 prompts of
 128-4096 tokens, 256 generated tokens, 50 schedules)."""
 import os
+import time
 
 import numpy as np
 import pytest
 import torch
 
-from invariant_fixed_order_gb300 import synth
+from invariant_fixed_order_gb300 import results, synth
 from invariant_fixed_order_gb300.config import LLAMA3_8B
 
 pytestmark = pytest.mark.gpu
@@ -74,14 +75,18 @@ def test_unique_completions_under_random_schedules(mods):
     runner = sched.Runner(eng)
     solo = {rid: greedy_solo(sched, runner, p, rid, n_new, bi.INVARIANT) for rid, p in enumerate(prompts)}
     completions = {rid: {tuple(solo[rid])} for rid in solo}
-    # at full size an eviction recomputes up to 4k positions through 32 layers: evict less often
-    fz = sched.FuzzConfig(token_budget=4096, chunk_min=256, chunk_max=2048, p_evict=0.002 if FULL else 0.05,
+    # an eviction frees the request's pages; its readmission recomputes up to 4k positions through every
+    # layer by chunked prefill (at full size ~80 evictions per schedule)
+    fz = sched.FuzzConfig(token_budget=4096, chunk_min=256, chunk_max=2048, p_evict=0.005 if FULL else 0.05,
                           readmit_delay=(1, 3), arrival_span=6)
+    counts = {}
+    t_start = time.perf_counter()
     print(f"unique completions: {n_layers} layers, {n_prompts} prompts, {n_new} tokens, {n_sched} schedules",
           flush=True)
     for k in range(n_sched):
         reqs = [sched.Request(rid, p) for rid, p in enumerate(prompts)]
-        sched.fuzz_continuous(runner, reqs, n_new, np.random.default_rng(1000 + k), fz, all_prompt_logits=False)
+        sched.fuzz_continuous(runner, reqs, n_new, np.random.default_rng(1000 + k), fz, all_prompt_logits=False,
+                              stats=counts)
         eng.check()
         for r in reqs:
             completions[r.rid].add(tuple(r.generated[:n_new]))
@@ -89,7 +94,18 @@ def test_unique_completions_under_random_schedules(mods):
               flush=True)
     unique = {rid: len(c) for rid, c in completions.items()}
     bound = sched.rule_of_three(n_prompts * n_sched)
-    print(f"unique completions per prompt: max {max(unique.values())}; rule-of-three bound {bound:.4f}")
+    print(f"unique completions per prompt: max {max(unique.values())}; rule-of-three bound {bound:.4f}; "
+          f"{counts}")
+    results.record("unique_completions" + ("_full" if FULL else ""), {
+        "mode": "invariant", "layers": n_layers, "prompts": n_prompts, "prompt_len": [lo, hi], "new_tokens": n_new,
+        "schedules": n_sched, "seeds": {"prompt_lengths": 42 + 4, "prompt_tokens": "4000 + i", "weights": 1234,
+                                        "schedules": "1000 + k"},
+        "fuzz": {"token_budget": fz.token_budget, "chunk": [fz.chunk_min, fz.chunk_max], "p_evict": fz.p_evict,
+                 "readmit_delay": list(fz.readmit_delay), "arrival_span": fz.arrival_span},
+        "counts": counts, "max_completions_per_prompt": max(unique.values()),
+        "prompts_with_one_completion": sum(1 for u in unique.values() if u == 1),
+        "divergent_trials": sum(u - 1 for u in unique.values()), "trials": n_prompts * n_sched,
+        "rule_of_three_bound": bound, "seconds": round(time.perf_counter() - t_start, 1)})
     assert all(u == 1 for u in unique.values()), unique
     eng.close()
 
@@ -144,7 +160,11 @@ def test_decode_verify_rollback_commits_the_invariant_greedy_tokens(mods):
                  max_T=max(8 * window, 8 * 1024) + 64, max_B=n_prompts, max_R=8 * window)
     runner = sched.Runner(eng)
     # pure invariant greedy decoding (batched: invariant mode gives every request its solo bits)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
     truth = greedy_batched(sched, runner, prompts, n_new, bi.INVARIANT)
+    torch.cuda.synchronize()
+    t_invariant = time.perf_counter() - t0
 
     # plain run of the fast path
     reqs = [sched.Request(rid, p) for rid, p in enumerate(prompts)]
@@ -154,8 +174,15 @@ def test_decode_verify_rollback_commits_the_invariant_greedy_tokens(mods):
         assert r.generated == truth[r.rid], r.rid
         runner.evict(r)
     assert st.committed == n_prompts * n_new
-    print(f"dvr ({n_layers} layers, {n_prompts} prompts, {n_new} tokens, window {window}):", st.as_dict(),
-          flush=True)
+    summary = st.as_dict(window=window)
+    summary["invariant_greedy_tok_s"] = n_prompts * n_new / t_invariant
+    summary["committed_vs_invariant"] = summary["committed_tok_s"] / summary["invariant_greedy_tok_s"]
+    print(f"dvr ({n_layers} layers, {n_prompts} prompts, {n_new} tokens, window {window}):", summary, flush=True)
+    results.record("dvr" + ("_full" if FULL else ""), {
+        "layers": n_layers, "prompts": n_prompts, "prompt_len": [128, 1024], "new_tokens": n_new, "window": window,
+        "verify_batch": 8, "fast_mode": "variant", "verifier": "invariant teacher-forced replay",
+        "seeds": {"prompt_lengths": 42 + 5, "prompt_tokens": "5000 + i", "weights": 1234},
+        "committed_equals_invariant_greedy": True, "stats": summary})
 
     # a fast path that emits wrong candidates at chosen positions: the verifier
     # must catch each one, roll back and still commit exactly the greedy tokens
