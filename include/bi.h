@@ -384,15 +384,35 @@ typedef struct {
 
 typedef struct bi_model bi_model;
 
+/* bi_model_create ("Lockstep", "The fix": the engine whose output for a
+ * request does not depend on its batch; the decoder's steps are the plain
+ * Llama-style layer the forward step below lists).  Checks the shapes the
+ * kernels support (d, V and (H + 2 Hkv) Dh multiples of 128; F and H Dh
+ * multiples of 64; Dh in {64, 128}; H / Hkv in {1, 2, 4, 8}), borrows the
+ * weight pointers, copies the per-layer pointer arrays and allocates the
+ * model's device buffers: the RoPE cos and sin tables for max_pos positions
+ * (bi_rope_table's values).  Returns BI_ERR_SHAPE, BI_ERR_UNSUPPORTED or
+ * BI_ERR_INVALID without allocating on a bad config, BI_ERR_CUDA if the tables
+ * cannot be allocated.  *out is owned by the caller until bi_model_destroy,
+ * which frees the tables and the step's pinned staging buffers (NULL is
+ * accepted). */
 bi_status bi_model_create(const bi_model_config* cfg, const bi_model_weights* w, bi_model** out);
 void bi_model_destroy(bi_model* m);
 
-/* Workspace for bi_forward_step with at most max_T tokens, max_B requests,
- * max_R logit rows and contexts up to max_seq positions. */
+/* Workspace for bi_forward_step ("The fix": every intermediate of the step has
+ * a fixed place, so no allocation happens while a step runs) with at most
+ * max_T tokens, max_B requests, max_R logit rows and contexts up to max_seq
+ * positions.  Covers both modes (the batch-variant mode's split partials
+ * included).  0 on a bad argument. */
 size_t bi_forward_workspace_size(const bi_model_config* cfg, int32_t max_T, int32_t max_B,
                                  int32_t max_R, int32_t max_seq);
 
-/* Embedding -> n_layers x (RMSNorm, QKV GEMM, RoPE + KV append, attention,
+/* bi_forward_step ("Lockstep", "The fix" and "Proving it": one step of a
+ * ragged batch whose rows for a request are bit-identical whatever else the
+ * batch holds, whatever the order of its requests and however a prompt was
+ * cut into prefill chunks; the harness that checks this replays steps under
+ * every schedule it enumerates and compares the bits with the solo run).
+ * Embedding -> n_layers x (RMSNorm, QKV GEMM, RoPE + KV append, attention,
  * O GEMM + residual, RMSNorm, gate/up GEMM + SwiGLU, down GEMM + residual) ->
  * final RMSNorm of the logit rows -> LM head (fp32) -> greedy argmax (taken in
  * the LM head's epilogue: the same tokens as bi_argmax of the logits).
