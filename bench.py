@@ -51,7 +51,7 @@ def parse():
     p.add_argument("--no-sweep", action="store_true")
     p.add_argument("--no-cpu", action="store_true")
     p.add_argument("--cpu-seconds", type=float, default=15.0)
-    p.add_argument("--ncu-target", choices=["gemm-decode64", "gemm-prefill8192", "prefill-attn16", "gemm-o-m1"],
+    p.add_argument("--ncu-target", choices=["gemm-decode64", "gemm-prefill8192", "prefill-attn16", "gemm-o-m1", "decode-attn16"],
                    default=None,
                    help="launch only the named GEMMs (twice: warm-up, then the pass to capture) for an ncu "
                         "capture; prints no measurement")
@@ -256,6 +256,37 @@ def attention_time(w: GpuWorkload, steps: int, stream) -> dict:
     ms = time_steps(fn, max(steps, 10), 3, stream)
     kv = sum(2 * int(s) * cfg.Hkv * cfg.Dh * 2 for s in w.ctx)
     return {"us": round(ms * 1e3, 2), "GBps": round(kv / (ms * 1e-3) / 1e9, 1), "kv_bytes": kv}
+
+
+def gemm_chain(steps: int, stream) -> dict:
+    """The cost of one dependent MMA in the layer projections' form: one output tile (M = 1, N = 128, a single
+    CTA pair) at K = 1024 ... 65536.  Every K step of the tile's accumulator is one 256x128x16 pair MMA that
+    must follow the previous one, so the time's slope against K / 16 is the cost of a dependent MMA (the weights,
+    at most 16 MB, stay in L2 across the timed repeats: this measures the chain, not HBM).  The layer's floor
+    under one MMA form and no split of K follows: each projection's chain length (K / 16 per output tile, times
+    the waves of output tiles over the 76 CTA pairs) times that cost."""
+    import torch
+    from invariant_fixed_order_gb300 import bi
+    from invariant_fixed_order_gb300.config import LLAMA3_8B
+    g = torch.Generator(device="cuda").manual_seed(5)
+    ks = [1024, 2048, 4096, 8192, 16384, 32768, 65536]
+    us = []
+    for K in ks:
+        A = torch.randn(1, K, device="cuda", generator=g).to(torch.bfloat16)
+        W = (torch.randn(128, K, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+        C = torch.empty(1, 128, dtype=torch.float32, device="cuda")
+        us.append(time_steps(lambda: bi.gemm(A, W, out=C, c_dtype=bi.F32, stream=stream), max(steps, 20), 3,
+                             stream) * 1e3)
+    slope, icpt = np.polyfit(np.asarray(ks, np.float64) / 16.0, np.asarray(us), 1)
+    c = LLAMA3_8B
+    pairs = 76
+    chains = {"qkv": (c.d // 16) * -(-(c.qkv_dim // 128) // pairs), "o": (c.H * c.Dh // 16) * -(-(c.d // 128) // pairs),
+              "gate_up": (c.d // 16) * -(-(2 * c.F // 128) // pairs), "down": (c.F // 16) * -(-(c.d // 128) // pairs)}
+    floor = {k: round(v * slope * 1e-3 + icpt, 1) for k, v in chains.items()}
+    return {"shape": "M=1, N=128: one output tile, CTA-pair form 256x128x16", "k": ks, "us": [round(x, 2) for x in us],
+            "ns_per_dependent_mma": round(slope * 1e3, 2), "fixed_us": round(icpt, 2),
+            "layer_chain_mmas": chains, "layer_chain_floor_us": floor,
+            "layer_chain_floor_total_us": round(sum(floor.values()), 1)}
 
 
 def logits_ops_time(w: GpuWorkload, steps: int, stream, hbm_peak: float) -> dict:
@@ -585,6 +616,7 @@ def run_ours(args):
     g = gemm_roofline(w, args.steps, stream, hbm_peak)
     att = attention_time(w, args.steps, stream)
     lops = logits_ops_time(w, args.steps, stream, hbm_peak)
+    chain = gemm_chain(args.steps, stream) if not args.no_sweep else None
     step_bytes = w.step_bytes(B)
     del w
     torch.cuda.empty_cache()
@@ -622,6 +654,8 @@ def run_ours(args):
             "clocks": clocks,
             "sweep": sweep,
         }
+        if chain is not None:
+            line["gemm_chain"] = chain
         if pre is not None:
             line["prefill"] = pre
         if m32 is not None:
@@ -669,6 +703,30 @@ def ncu_target(which: str) -> None:
             bi.prefill_attention(q, cu_q, pos0, kc, vc, table)
         torch.cuda.synchronize()
         print(json.dumps({"ncu_target": which, "done": True}))
+        return
+    if which == "decode-attn16":
+        # decode attention of 16 requests with contexts U[128, 8192] (the bench's distribution) over paged K/V in
+        # a shuffled pool (launched twice)
+        from invariant_fixed_order_gb300 import synth
+        ctx = [int(x) for x in synth.uniform_ints(16, 128, 8192, DATA_SEED)]
+        max_pages = 8192 // 16 + 1
+        n_pages = sum((s + 15) // 16 for s in ctx)
+        kc = rnd(n_pages, c.Hkv, 16, c.Dh)
+        vc = rnd(n_pages, c.Hkv, 16, c.Dh)
+        perm = np.random.default_rng(DATA_SEED).permutation(n_pages).astype(np.int32)
+        table = np.zeros((16, max_pages), np.int32)
+        p0 = 0
+        for i, s in enumerate(ctx):
+            n = (s + 15) // 16
+            table[i, :n] = perm[p0:p0 + n]
+            p0 += n
+        q = rnd(16, c.H, c.Dh)
+        sl = torch.tensor(ctx, dtype=torch.int32, device="cuda")
+        d_table = torch.from_numpy(table).cuda()
+        for _ in range(2):
+            bi.decode_attention(q, kc, vc, d_table, sl, max(ctx))
+        torch.cuda.synchronize()
+        print(json.dumps({"ncu_target": which, "kv_bytes": sum(2 * s * c.Hkv * c.Dh * 2 for s in ctx), "done": True}))
         return
     if which == "gemm-o-m1":
         # the decode-step o projection at M = 1 with its residual epilogue (launched twice)
