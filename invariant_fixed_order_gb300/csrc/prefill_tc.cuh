@@ -121,6 +121,20 @@ __device__ __forceinline__ bool consumer_any(bool pred) {
     return r != 0;
 }
 
+// Every bounded wait of this kernel: each try may suspend the thread for up to
+// kHintNs (it resumes when the phase completes), so waiting warps take few
+// issue slots from the softmax warps that share their schedulers.
+constexpr uint32_t kHintNs = 20000;
+__device__ __forceinline__ bool wait_bounded(uint64_t* bar, uint32_t parity, volatile int32_t* abort) {
+    return ptx::mbar_wait_bounded_hint(bar, parity, abort, kHintNs);
+}
+// Every thread of a warp: a bounded wait whose outcome is the same in the
+// whole warp (a failure in one lane fails the warp), so the warp-collective
+// tensor-memory accesses that follow stay uniform.
+__device__ __forceinline__ bool warp_wait(uint64_t* bar, uint32_t parity, volatile int32_t* abort) {
+    return __all_sync(0xffffffffu, wait_bounded(bar, parity, abort));
+}
+
 // Byte offset of 16-byte chunk c (0..7) of row r in a 128-byte-swizzled region.
 __device__ __forceinline__ uint32_t sw128(int r, int c) {
     return static_cast<uint32_t>(r * 128 + (((c & 7) ^ (r & 7)) << 4));
@@ -205,15 +219,46 @@ __device__ __forceinline__ uint32_t lane_addr(uint32_t base, uint32_t col) {
     return base + (static_cast<uint32_t>(((threadIdx.x / 32) & 3) * 32) << 16) + col;
 }
 
+// Packed fp32 pairs (the f32x2 instructions): each lane is one IEEE
+// round-to-nearest operation, so the results are the bits of the scalar
+// __fadd_rn / __fsub_rn / __fmul_rn the decode routine uses (checked on GB300
+// against the scalar instructions).  Only additions, subtractions and
+// products whose result does not feed an addition use them: packed, the sum
+// of two products by per-row constants did not reproduce the scalar bits on
+// GB300, so the fold stays scalar.
+__device__ __forceinline__ float2 add2(float2 a, float2 b) {
+    float2 r;
+    asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+        "add.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+__device__ __forceinline__ float2 sub2(float2 a, float2 b) {
+    float2 r;
+    asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+        "sub.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+__device__ __forceinline__ float2 mul2(float2 a, float2 b) {
+    float2 r;
+    asm("{\n\t.reg .b64 x, y, z;\n\tmov.b64 x, {%2, %3};\n\tmov.b64 y, {%4, %5};\n\t"
+        "mul.rn.f32x2 z, x, y;\n\tmov.b64 {%0, %1}, z;\n\t}"
+        : "=f"(r.x), "=f"(r.y)
+        : "f"(a.x), "f"(a.y), "f"(b.x), "f"(b.y));
+    return r;
+}
+
 // p of two consecutive keys (the even one first) as packed bf16 hi and lo
 // pairs: hi = bf16(p) and lo = bf16(p - hi), rounded to nearest even as the
 // decode routine rounds them.
 __device__ __forceinline__ void pack_p(float p0, float p1, uint32_t& hi, uint32_t& lo) {
     __nv_bfloat162 h = __floats2bfloat162_rn(p0, p1);  // .x (low half) = p0
     hi = *reinterpret_cast<uint32_t*>(&h);
-    const float r0 = __fsub_rn(p0, __uint_as_float(hi << 16));
-    const float r1 = __fsub_rn(p1, __uint_as_float(hi & 0xffff0000u));
-    __nv_bfloat162 l = __floats2bfloat162_rn(r0, r1);
+    const float2 r = sub2(make_float2(p0, p1), make_float2(__uint_as_float(hi << 16), __uint_as_float(hi & 0xffff0000u)));
+    __nv_bfloat162 l = __floats2bfloat162_rn(r.x, r.y);
     lo = *reinterpret_cast<uint32_t*>(&l);
 }
 
@@ -242,25 +287,32 @@ __device__ __forceinline__ void load16(uint32_t base, int c0, int32_t n_max, uin
 template <bool kMask>
 __device__ __forceinline__ void p_block16(uint32_t base, int c0, int32_t n_max, int32_t ncol, float scale, float m,
                                           const uint32_t (&r)[16], float (&p)[64], int off) {
+    // score = fl(acc * scale) (or -inf), then attn_exp(score - m) = 2^(fl((score - m) log2 e))
+    const float2 sc2 = make_float2(scale, scale), m2 = make_float2(m, m);
+    const float2 l2e = make_float2(1.44269504088896341f, 1.44269504088896341f);
     uint32_t w[16];
 #pragma unroll
     for (int j = 0; j < 16; j += 2) {
-        float pv[2];
-#pragma unroll
-        for (int x = 0; x < 2; ++x) {
-            float sc = c0 < n_max ? __fmul_rn(__uint_as_float(r[j + x]), scale) : -INFINITY;
-            if (kMask && c0 + j + x >= ncol) sc = -INFINITY;
-            pv[x] = attn_exp(__fsub_rn(sc, m));
-            p[off + j + x] = pv[x];
+        float2 x = c0 < n_max ? mul2(make_float2(__uint_as_float(r[j]), __uint_as_float(r[j + 1])), sc2)
+                              : make_float2(-INFINITY, -INFINITY);
+        if (kMask) {
+            if (c0 + j >= ncol) x.x = -INFINITY;
+            if (c0 + j + 1 >= ncol) x.y = -INFINITY;
         }
-        pack_p(pv[0], pv[1], w[j / 2], w[8 + j / 2]);
+        x = mul2(sub2(x, m2), l2e);
+        float pv0, pv1;
+        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(pv0) : "f"(x.x));
+        asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(pv1) : "f"(x.y));
+        p[off + j] = pv0;
+        p[off + j + 1] = pv1;
+        pack_p(pv0, pv1, w[j / 2], w[8 + j / 2]);
     }
     if (c0 < n_max) tmem_st16(base + c0, w);
 }
 
 template <bool kMask, int DH>
-__device__ __forceinline__ void softmax_lo(Smem<DH>& sm, uint32_t tmem, int half, int row, int32_t n_max,
-                                           int32_t ncol, float scale, float& m_out, float (&pa)[64]) {
+__device__ __forceinline__ bool softmax_lo(Smem<DH>& sm, uint32_t tmem, int half, int row, int32_t n_max,
+                                           int32_t ncol, float scale, float& m_out, float (&pa)[64], bool good) {
     const int c_lo = 64 * half, c_hi = 128 + 64 * half;  // this thread's key ranges (64 keys each)
     const uint32_t base = lane_addr(tmem, kColS);
     // pass 1: the row's maximum over its keys, 64 at a time
@@ -268,7 +320,7 @@ __device__ __forceinline__ void softmax_lo(Smem<DH>& sm, uint32_t tmem, int half
 #pragma unroll
     for (int rg = 0; rg < 2; ++rg) {
         const int c0 = rg == 0 ? c_lo : c_hi;
-        if (c0 < n_max) {
+        if (good && c0 < n_max) {
             uint32_t r[64];
             tmem_ld32(base + c0, r);
             tmem_ld32(base + c0 + 32, r + 32);
@@ -280,7 +332,8 @@ __device__ __forceinline__ void softmax_lo(Smem<DH>& sm, uint32_t tmem, int half
         }
     }
     sm.xmax[half][row] = mx;
-    consumer_sync();
+    // the partial maxima meet, and every consumer learns whether the scores' wait succeeded everywhere
+    if (consumer_any(!good)) return false;
     const float m = ncol > 0 ? __fmul_rn(fmaxf(sm.xmax[0][row], sm.xmax[1][row]), scale) : 0.0f;
     m_out = m;
     // pass 2, keys below 128: four blocks of 16, the next block read while one is computed
@@ -300,6 +353,7 @@ __device__ __forceinline__ void softmax_lo(Smem<DH>& sm, uint32_t tmem, int half
             p_block16<kMask>(base, ca, n_max, ncol, scale, m, rb, pa, blk * 16);
         }
     }
+    return true;
 }
 
 // Second phase: p of the thread's keys 128 + 32b + i, the group sums in the
@@ -333,18 +387,23 @@ __device__ __forceinline__ void softmax_hi(Smem<DH>& sm, uint32_t tmem, int half
     float w[2];
 #pragma unroll
     for (int gi = 0; gi < 2; ++gi) {
-        float u[16];
+        float v[32];
 #pragma unroll
-        for (int i = 0; i < 16; ++i) {
-            const float p0 = __fadd_rn(pa[32 * gi + i], pb[32 * gi + i]);            // 0 + p = p exactly (p >= 0)
-            const float p1 = __fadd_rn(pa[32 * gi + 16 + i], pb[32 * gi + 16 + i]);
-            u[i] = __fadd_rn(p0, p1);
+        for (int i = 0; i < 32; i += 2) {  // 0 + p = p exactly (p >= 0)
+            const float2 t = add2(make_float2(pa[32 * gi + i], pa[32 * gi + i + 1]),
+                                  make_float2(pb[32 * gi + i], pb[32 * gi + i + 1]));
+            v[i] = t.x;
+            v[i + 1] = t.y;
         }
 #pragma unroll
-        for (int off = 8; off >= 1; off >>= 1)
+        for (int off = 16; off >= 2; off >>= 1)
 #pragma unroll
-            for (int i = 0; i < off; ++i) u[i] = __fadd_rn(u[i], u[i + off]);
-        w[gi] = u[0];
+            for (int i = 0; i < off; i += 2) {
+                const float2 t = add2(make_float2(v[i], v[i + 1]), make_float2(v[i + off], v[i + off + 1]));
+                v[i] = t.x;
+                v[i + 1] = t.y;
+            }
+        w[gi] = __fadd_rn(v[0], v[1]);
     }
     if (half == 0) {
         w01 = __fadd_rn(w[0], w[1]);
@@ -398,7 +457,7 @@ __device__ __forceinline__ void issue_chunk(uint8_t (*dst)[kKeyRegion], const CU
 // parity; the outcome is the same in every consumer thread (a failure
 // anywhere fails them all).
 __device__ __forceinline__ bool wait_all(uint64_t* bar, uint32_t parity, volatile int32_t* abort) {
-    return !consumer_any(!ptx::mbar_wait_bounded(bar, parity, abort));
+    return !consumer_any(!wait_bounded(bar, parity, abort));
 }
 
 // A finished run whose output is still in tensor memory (running O).
@@ -488,7 +547,7 @@ __device__ __forceinline__ void produce(Smem<DH>& sm, const CUtensorMap* tmK, co
     // lane 0 waits (bounded), the warp follows its outcome
     auto wait = [&](uint64_t* bar, uint32_t parity) {
         bool r = true;
-        if (lane == 0) r = ptx::mbar_wait_bounded(bar, parity, abort);
+        if (lane == 0) r = wait_bounded(bar, parity, abort);
         return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
     };
     auto take_slot = [&]() {  // the descriptor slot for run `runs`, once its previous run was read
@@ -629,7 +688,7 @@ __device__ __forceinline__ void issue_products(Smem<DH>& sm, uint32_t tmem) {
     };
     while (ok) {
         const int slot = runs & 1;
-        if (!(ok = ptx::mbar_wait_bounded(&sm.rd_full[slot], (runs >> 1) & 1u, abort))) break;
+        if (!(ok = wait_bounded(&sm.rd_full[slot], (runs >> 1) & 1u, abort))) break;
         const int32_t tokens = sm.rd[slot].tokens, count = sm.rd[slot].count, s_max = sm.rd[slot].s_max;
         mbar_arrive(&sm.rd_empty[slot]);
         ++runs;
@@ -637,10 +696,10 @@ __device__ __forceinline__ void issue_products(Smem<DH>& sm, uint32_t tmem) {
         for (int32_t j = 0; j < count; ++j, ++chunks) {
             const int32_t n_max = min(kChunk, s_max - j * kChunk);
             const int steps = (n_max + 15) / 16;
-            if (j == 0 && !(ok = ptx::mbar_wait_bounded(&sm.q_full, (q_runs++) & 1u, abort))) break;
+            if (j == 0 && !(ok = wait_bounded(&sm.q_full, (q_runs++) & 1u, abort))) break;
             // the previous chunk's PV product has read its P (in the S columns)
-            if (issued && !(ok = ptx::mbar_wait_bounded(&sm.pv_done, (chunks - 1) & 1u, abort))) break;
-            if (!(ok = ptx::mbar_wait_bounded(&sm.k_full, chunks & 1u, abort))) break;
+            if (issued && !(ok = wait_bounded(&sm.pv_done, (chunks - 1) & 1u, abort))) break;
+            if (!(ok = wait_bounded(&sm.k_full, chunks & 1u, abort))) break;
             ptx::tc_fence_after();
 #pragma unroll
             for (int ks = 0; ks < DH / 16; ++ks) {
@@ -650,11 +709,11 @@ __device__ __forceinline__ void issue_products(Smem<DH>& sm, uint32_t tmem) {
             }
             ptx::tc_commit<1>(&sm.s_done);
             issued = true;
-            if (!(ok = ptx::mbar_wait_bounded(&sm.pa_ready, chunks & 1u, abort))) break;
-            if (!(ok = ptx::mbar_wait_bounded(&sm.v_full, chunks & 1u, abort))) break;
+            if (!(ok = wait_bounded(&sm.pa_ready, chunks & 1u, abort))) break;
+            if (!(ok = wait_bounded(&sm.v_full, chunks & 1u, abort))) break;
             ptx::tc_fence_after();
             pv_steps(0, min(steps, 8));
-            if (!(ok = ptx::mbar_wait_bounded(&sm.pb_ready, chunks & 1u, abort))) break;
+            if (!(ok = wait_bounded(&sm.pb_ready, chunks & 1u, abort))) break;
             ptx::tc_fence_after();
             pv_steps(8, steps);
             ptx::tc_commit<1>(&sm.pv_done);
@@ -758,24 +817,28 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 const int32_t n_max = min(kChunk, s_max - k0);
                 const int32_t ncol = mine ? min(max(keys - k0, 0), kChunk) : 0;
                 const bool masked = k0 + kChunk > s_min;  // some row of the run stops inside this chunk
-                if (!(ok = wait_all(&sm.s_done, chunks & 1u, abort))) break;
+                bool good = warp_wait(&sm.s_done, chunks & 1u, abort);
                 ptx::tc_fence_after();
                 float m, w01, pa[64];
-                if (masked)
-                    softmax_lo<true, DH>(sm, tmem, half, row, n_max, ncol, geo.scale, m, pa);
-                else
-                    softmax_lo<false, DH>(sm, tmem, half, row, n_max, ncol, geo.scale, m, pa);
-                if (!(ok = wait_all(&sm.v_full, chunks & 1u, abort))) break;
+                const bool agreed = masked ? softmax_lo<true, DH>(sm, tmem, half, row, n_max, ncol, geo.scale, m, pa, good)
+                                           : softmax_lo<false, DH>(sm, tmem, half, row, n_max, ncol, geo.scale, m, pa, good);
+                if (!agreed) {
+                    ok = false;
+                    break;
+                }
                 // V rows past the last key up to the 16-key step meet p = 0 in the MMAs:
                 // zeros, not whatever the page holds there
                 if (n_max & 15) {
                     constexpr int kRegions = DH / 64;
-                    const int pad = ((n_max + 15) & ~15) - n_max;
-                    for (int i = tid; i < pad * 8 * kRegions; i += kConsumers) {
-                        const int r = n_max + i / (8 * kRegions), rem = i % (8 * kRegions);
-                        *reinterpret_cast<uint4*>(&sm.v[rem / 8][sw128(r, rem % 8)]) = make_uint4(0u, 0u, 0u, 0u);
+                    good = warp_wait(&sm.v_full, chunks & 1u, abort);
+                    if (good) {
+                        const int pad = ((n_max + 15) & ~15) - n_max;
+                        for (int i = tid; i < pad * 8 * kRegions; i += kConsumers) {
+                            const int r = n_max + i / (8 * kRegions), rem = i % (8 * kRegions);
+                            *reinterpret_cast<uint4*>(&sm.v[rem / 8][sw128(r, rem % 8)]) = make_uint4(0u, 0u, 0u, 0u);
+                        }
+                        ptx::fence_proxy_async_smem();
                     }
-                    ptx::fence_proxy_async_smem();
                 }
                 p_ready(&sm.pa_ready);  // PV of keys 0-127 runs during the second phase
                 if (masked)
@@ -783,11 +846,14 @@ prefill_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant
                 else
                     softmax_hi<false, DH>(sm, tmem, half, row, n_max, ncol, geo.scale, m, pa, w01);
                 p_ready(&sm.pb_ready);
-                consumer_sync();  // the upper half's group sums
+                good = good && warp_wait(&sm.pv_done, chunks & 1u, abort);
+                if (consumer_any(!good)) {  // also publishes the upper half's group sums
+                    ok = false;
+                    break;
+                }
+                ptx::tc_fence_after();
                 // l in the decode routine's order: ((group 0 + group 1) + group 2) + group 3
                 const float l = half == 0 ? __fadd_rn(__fadd_rn(w01, sm.xsum[0][row]), sm.xsum[1][row]) : 0.0f;
-                if (!(ok = wait_all(&sm.pv_done, chunks & 1u, abort))) break;
-                ptx::tc_fence_after();
                 // the decode merge's fold; a row without keys in this chunk keeps its state
                 const bool active = ncol > 0;
                 float a = 1.0f, bw = 1.0f;

@@ -36,6 +36,20 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar_addr, uint32_t parity
         : "memory");
     return ok != 0;
 }
+// As mbar_try_wait, but a thread whose phase is not complete may be
+// suspended for up to hint_ns (it resumes as soon as the phase completes)
+// instead of the system-dependent default.
+__device__ __forceinline__ bool mbar_try_wait_hint(uint32_t bar_addr, uint32_t parity, uint32_t hint_ns) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred P1;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 P1, [%1], %2, %3;\n\t"
+        "selp.b32 %0, 1, 0, P1;\n\t}"
+        : "=r"(ok)
+        : "r"(bar_addr), "r"(parity), "r"(hint_ns)
+        : "memory");
+    return ok != 0;
+}
 // Waits for the phase with the given parity to complete.  Gives up (returns
 // false) after limit_ns or once *abort is set by another role.
 __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity, volatile int32_t* abort,
@@ -49,6 +63,20 @@ __device__ __forceinline__ bool mbar_wait_bounded(uint64_t* bar, uint32_t parity
             if (*abort) return false;
             if (globaltimer_ns() - t0 > limit_ns) return false;
         }
+    }
+}
+// The same bound, with each try suspending the thread for up to hint_ns
+// (woken when the phase completes): a waiting warp takes few issue slots
+// from the warps that share its scheduler.
+__device__ __forceinline__ bool mbar_wait_bounded_hint(uint64_t* bar, uint32_t parity, volatile int32_t* abort,
+                                                       uint32_t hint_ns, uint64_t limit_ns = kWaitLimitNs) {
+    const uint32_t addr = smem_u32(bar);
+    if (mbar_try_wait_hint(addr, parity, hint_ns)) return true;
+    const uint64_t t0 = globaltimer_ns();
+    for (;;) {
+        if (mbar_try_wait_hint(addr, parity, hint_ns)) return true;
+        if (*abort) return false;
+        if (globaltimer_ns() - t0 > limit_ns) return false;
     }
 }
 
