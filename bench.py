@@ -282,7 +282,7 @@ def gemm_chain(steps: int, stream) -> dict:
     pairs = 76
     chains = {"qkv": (c.d // 16) * -(-(c.qkv_dim // 128) // pairs), "o": (c.H * c.Dh // 16) * -(-(c.d // 128) // pairs),
               "gate_up": (c.d // 16) * -(-(2 * c.F // 128) // pairs), "down": (c.F // 16) * -(-(c.d // 128) // pairs)}
-    floor = {k: round(v * slope * 1e-3 + icpt, 1) for k, v in chains.items()}
+    floor = {k: round(v * slope + icpt, 1) for k, v in chains.items()}  # slope: us per dependent MMA
     return {"shape": "M=1, N=128: one output tile, CTA-pair form 256x128x16", "k": ks, "us": [round(x, 2) for x in us],
             "ns_per_dependent_mma": round(slope * 1e3, 2), "fixed_us": round(icpt, 2),
             "layer_chain_mmas": chains, "layer_chain_floor_us": floor,
@@ -587,6 +587,31 @@ def run_ours(args):
     h2d = (pin_ids.numel() + pin_table.numel() + pin_meta.numel()) * 4
     d2h = B * 4
 
+    # ---- e2e through the C ABI alone: bi_forward_step launched eagerly, its per-token metadata staged by the
+    # library from host arrays (q_len, pos0, logit rows), token ids and page table copied in from pinned host
+    # memory, tokens copied back; no graph ----
+    d_ids_c = torch.empty_like(w.d_ids)
+    d_table_c = torch.empty_like(w.d_table)
+    tok_c = torch.empty(B, dtype=torch.int32, device=device)
+    rows = list(range(B))
+
+    def e2e_cabi_step():
+        d_ids_c.copy_(pin_ids, non_blocking=True)
+        d_table_c.copy_(pin_table, non_blocking=True)
+        w.eng.step([1] * B, positions, d_ids_c, d_table_c, rows, mode=bi.INVARIANT, want_logits=False,
+                   tokens_out=tok_c, stream=stream)
+        pin_tok.copy_(tok_c, non_blocking=True)
+
+    for _ in range(3):
+        e2e_cabi_step()
+    torch.cuda.synchronize()
+    t0 = time.perf_counter()
+    for _ in range(args.steps):
+        e2e_cabi_step()
+    torch.cuda.synchronize()
+    e2e_cabi_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    h2d_cabi = (pin_ids.numel() + pin_table.numel() + 3 * B + B) * 4  # ids, table, the library's metadata
+
     # ---- sweep: invariant vs variant over batch sizes ----
     sweep = []
     if not args.no_sweep:
@@ -649,7 +674,14 @@ def run_ours(args):
             "eager": {"ms_per_step": round(eager_ms, 4), "value": round(world * B / (eager_ms * 1e-3), 1),
                       "step_hbm_frac": round(step_bytes / (eager_ms * 1e-3) / 1e9 / hbm_peak, 3)},
             "e2e": {"value": round(world * B / (e2e_ms * 1e-3), 1), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-                    "d2h_bytes_per_step": d2h},
+                    "d2h_bytes_per_step": d2h,
+                    "path": "pinned host ids, page table and step metadata copied into the CUDA graph's buffers, "
+                            "graph replay, tokens copied back"},
+            "e2e_c_abi": {"value": round(world * B / (e2e_cabi_ms * 1e-3), 1), "unit": "tokens/s",
+                          "h2d_bytes_per_step": h2d_cabi, "d2h_bytes_per_step": d2h,
+                          "path": "bi_forward_step launched eagerly through the C ABI with host q_len/pos0/logit "
+                                  "rows (staged by the library), pinned host ids and page table copied in, tokens "
+                                  "copied back"},
             "gpu_launches": launches_per_step * args.steps,
             "clocks": clocks,
             "sweep": sweep,
