@@ -552,25 +552,47 @@ extern "C" bi_status bi_forward_step(bi_model* m, const bi_batch* batch, const b
     if (dec_splits > L.dec_splits) return fail(BI_ERR_SHAPE, "bi_forward_step: split plan exceeds workspace");
     float* dec_ml = dec_o + static_cast<size_t>(std::max(nd, 1)) * c.H * dec_splits * c.Dh;
 
+    // greedy tokens come straight out of the LM head's epilogue unless the
+    // batch-variant plan splits its K (then the argmax reads stored logits)
+    const bool lm_head = b.R > 0 && (logits_out || tokens_out);
+    const bool fuse = lm_head && tokens_out != nullptr && gemm_plan(b.R, c.V, c.d, mode).splits == 1;
+    ArgmaxFuse am{reinterpret_cast<unsigned long long*>(base + L.am_keys), tokens_out,
+                  reinterpret_cast<unsigned int*>(base + L.am_counter)};
+    // With few tokens the RMSNorms run inside the GEMMs that consume them (their A writers apply the norm
+    // kernel's arithmetic), which saves a launch and a round trip of y per norm; a row's bits are the same
+    // either way.  The gate/up GEMM streams the most weight per row of A, and above 4 rows its writers'
+    // per-stage pass shows on the step (8 rows: +10 us of 353), so it takes the norm only up to 4 rows.
+    constexpr int64_t kNormInGateUpMaxRows = 4;
+    const bool norm_in_qkv = gemm_can_fuse_norm(T, nqkv, c.d, mode);
+    const bool norm_in_gu = T <= kNormInGateUpMaxRows && gemm_can_fuse_norm(T, 2 * c.F, c.d, mode);
+    // (the LM head's rows are x's first R rows when every request contributes its one decode token)
+    bool rows_leading = true;
+    for (int32_t i = 0; i < b.R && rows_leading; ++i) rows_leading = b.logit_rows[i] == i;
+    const bool norm_in_lm = lm_head && rows_leading && gemm_can_fuse_norm(b.R, c.V, c.d, mode);
+
     // The step's first kernel waits for all earlier work on the stream; every
     // later kernel of the step starts after it, so weights (never written
     // within a step) may be fetched before each kernel's dependency wait.
-    // the embedding gather and the first norm in one kernel (it also writes the residual stream x)
+    // the embedding gather and the first norm in one kernel (it also writes the residual stream x, and
+    // initialises the fused argmax's keys)
     BI_TRY_CUDA(launch_embed_rmsnorm(m->embed, b.token_ids, c.V, m->gamma_attn[0], x, y, T, c.d, c.eps, dev_status,
-                                     s),
+                                     s, fuse ? &am : nullptr, b.R),
                 "embed + rmsnorm");
     for (int l = 0; l < c.n_layers; ++l) {
-        if (l > 0) BI_TRY_CUDA(launch_rmsnorm(x, m->gamma_attn[l], y, T, c.d, c.eps, s), "rmsnorm");
+        // layer 0's norm ran with the embedding gather; later layers' in their QKV GEMM when it takes few rows
+        const NormFuse qkv_norm{x, m->gamma_attn[l], nullptr, c.eps};
+        const NormFuse* qn = l > 0 && norm_in_qkv ? &qkv_norm : nullptr;
+        if (l > 0 && qn == nullptr) BI_TRY_CUDA(launch_rmsnorm(x, m->gamma_attn[l], y, T, c.d, c.eps, s), "rmsnorm");
         if (gemm_can_fuse_rope(T, nqkv, c.d, mode, c.Dh)) {
             // RoPE and the K/V append run in the QKV GEMM's epilogue (no fp32 qkv round trip)
             const RopeFuse rf{d_req, d_pos, m->rope_cos, m->rope_sin, reinterpret_cast<uint16_t*>(q),
                               reinterpret_cast<uint16_t*>(kv->k[l]), reinterpret_cast<uint16_t*>(kv->v[l]),
                               b.page_table, c.max_pos, b.max_pages, kv->num_pages, c.H, c.Hkv, c.Dh};
             BI_TRY(run_gemm(y, m->w_qkv[l], nullptr, BI_F32, nullptr, BI_EP_NONE, T, nqkv, c.d, mode, gws,
-                            gws_bytes, dev_status, s, true, nullptr, &rf));
+                            gws_bytes, dev_status, s, true, nullptr, &rf, nullptr, qn));
         } else {
             BI_TRY(run_gemm(y, m->w_qkv[l], qkv, BI_F32, nullptr, BI_EP_NONE, T, nqkv, c.d, mode, gws, gws_bytes,
-                            dev_status, s, true));
+                            dev_status, s, true, nullptr, nullptr, nullptr, qn));
             BI_TRY_CUDA(launch_rope_kv_append(qkv, d_req, d_pos, m->rope_cos, m->rope_sin, c.max_pos, q, kv->k[l],
                                               kv->v[l], b.page_table, b.max_pages, kv->num_pages, T, c.H, c.Hkv,
                                               c.Dh, dev_status, s),
@@ -590,27 +612,26 @@ extern "C" bi_status bi_forward_step(bi_model* m, const bi_batch* batch, const b
         }
         BI_TRY(run_gemm(attn, m->w_o[l], x, BI_BF16, x, BI_EP_RESIDUAL, T, c.d, c.H * c.Dh, mode, gws, gws_bytes,
                         dev_status, s, true));
-        BI_TRY_CUDA(launch_rmsnorm(x, m->gamma_ffn[l], y, T, c.d, c.eps, s), "rmsnorm");
+        const NormFuse ffn_norm{x, m->gamma_ffn[l], nullptr, c.eps};
+        if (!norm_in_gu) BI_TRY_CUDA(launch_rmsnorm(x, m->gamma_ffn[l], y, T, c.d, c.eps, s), "rmsnorm");
         BI_TRY(run_gemm(y, m->w_gu[l], h, BI_BF16, nullptr, BI_EP_SWIGLU, T, 2 * c.F, c.d, mode, gws, gws_bytes,
-                        dev_status, s, true));
+                        dev_status, s, true, nullptr, nullptr, nullptr, norm_in_gu ? &ffn_norm : nullptr));
         BI_TRY(run_gemm(h, m->w_down[l], x, BI_BF16, x, BI_EP_RESIDUAL, T, c.d, c.F, mode, gws, gws_bytes,
                         dev_status, s, true));
     }
     if (hidden_out)
         BI_TRY_CUDA(cudaMemcpyAsync(hidden_out, x, static_cast<size_t>(T) * c.d * 2, cudaMemcpyDeviceToDevice, s),
                     "hidden copy");
-    if (b.R > 0 && (logits_out || tokens_out)) {
+    if (lm_head) {
         bi_bf16* yr = reinterpret_cast<bi_bf16*>(base + L.yr);
-        // greedy tokens come straight out of the LM head's epilogue unless the
-        // batch-variant plan splits its K (then the argmax reads stored logits)
-        const bool fuse = tokens_out != nullptr && gemm_plan(b.R, c.V, c.d, mode).splits == 1;
-        ArgmaxFuse am{reinterpret_cast<unsigned long long*>(base + L.am_keys), tokens_out,
-                      reinterpret_cast<unsigned int*>(base + L.am_counter)};
         float* logits = logits_out ? logits_out : fuse ? nullptr : reinterpret_cast<float*>(base + L.logits);
-        BI_TRY_CUDA(launch_rmsnorm(x, m->gamma_final, yr, b.R, c.d, c.eps, s, d_rows, fuse ? &am : nullptr),
-                    "final rmsnorm");
+        // the final norm of the logit rows (gathered by d_rows), in the LM head when it has few rows
+        const NormFuse final_norm{x, m->gamma_final, nullptr, c.eps};
+        if (!norm_in_lm)
+            BI_TRY_CUDA(launch_rmsnorm(x, m->gamma_final, yr, b.R, c.d, c.eps, s, d_rows), "final rmsnorm");
         BI_TRY(run_gemm(yr, m->w_lm, logits, BI_F32, nullptr, BI_EP_NONE, b.R, c.V, c.d, mode, gws, gws_bytes,
-                        dev_status, s, true, fuse ? &am : nullptr));
+                        dev_status, s, true, fuse ? &am : nullptr, nullptr, nullptr,
+                        norm_in_lm ? &final_norm : nullptr));
         if (tokens_out && !fuse) BI_TRY_CUDA(launch_argmax(logits, tokens_out, b.R, c.V, s), "argmax");
     }
     return BI_OK;

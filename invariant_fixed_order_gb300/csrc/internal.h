@@ -98,12 +98,22 @@ struct RopeFuse {
 cudaError_t launch_rmsnorm(const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y, int64_t rows,
                            int32_t d, float eps, cudaStream_t s, const int32_t* src_rows = nullptr,
                            const ArgmaxFuse* am = nullptr);
+// RMSNorm fused into a GEMM's A operand (few rows): A row r = bf16((x[src] * rinv) * gamma)
+// with src = rows[r] (or r), rinv from x[src]'s sum of squares in the RMSNorm kernel's
+// order, so the GEMM reads exactly the bits the RMSNorm kernel would have written.
+struct NormFuse {
+    const bi_bf16* x;
+    const bi_bf16* gamma;
+    const int32_t* rows;  // device, optional
+    float eps;
+};
 // after_all: launch without programmatic serialisation, so the kernel (and
 // every kernel chained after it) starts only once all earlier work on the
 // stream has finished.
 // x[t] = E[ids[t]] and y[t] = rmsnorm(x[t]) in one kernel (the norm's arithmetic), waiting for all earlier work
 cudaError_t launch_embed_rmsnorm(const bi_bf16* E, const int32_t* ids, int32_t V, const bi_bf16* gamma, bi_bf16* x,
-                                 bi_bf16* y, int32_t T, int32_t d, float eps, int32_t* status, cudaStream_t s);
+                                 bi_bf16* y, int32_t T, int32_t d, float eps, int32_t* status, cudaStream_t s,
+                                 const ArgmaxFuse* am = nullptr, int64_t am_rows = 0);
 cudaError_t launch_embed(const bi_bf16* E, const int32_t* ids, bi_bf16* x, int32_t T, int32_t V,
                          int32_t d, int32_t* status, cudaStream_t s, bool after_all = false);
 cudaError_t launch_rope_kv_append(const float* qkv, const int32_t* tok_req, const int32_t* tok_pos,
@@ -194,7 +204,10 @@ bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype
                    const bi_bf16* residual, bi_epilogue ep, int64_t M, int32_t N, int32_t K,
                    bi_mode mode, void* ws, size_t ws_bytes, int32_t* status, cudaStream_t s,
                    bool weights_settled = false, const ArgmaxFuse* am = nullptr,
-                   const RopeFuse* rope = nullptr, const GemmWaitTest* wait_test = nullptr);
+                   const RopeFuse* rope = nullptr, const GemmWaitTest* wait_test = nullptr,
+                   const NormFuse* norm = nullptr);
+// whether run_gemm can take its A operand through a fused RMSNorm (norm) for this shape and mode
+bool gemm_can_fuse_norm(int64_t M, int32_t N, int32_t K, bi_mode mode);
 // whether run_gemm can fuse RoPE + KV append for this shape and mode
 bool gemm_can_fuse_rope(int64_t M, int32_t N, int32_t K, bi_mode mode, int32_t Dh);
 

@@ -48,6 +48,17 @@
 // and a device status code, every role winds down, copies and MMAs in flight
 // are drained and TMEM is freed.
 //
+// With a fused RMSNorm (a few contiguous rows: the forward step's norms at
+// small batch) the producer brings the raw rows x into the A ring as usual,
+// counted on a separate barrier; warps 2-3 of the issuing CTA then normalise
+// each landed stage in place and release it to the MMA issuer.  Each row's
+// rinv is taken first, by warps 2-7 of the issuing CTA, from x in global
+// memory in the RMSNorm kernel's order (a warp per row, lane l over 16-byte
+// chunks l, l + 32, ... with fused multiply-adds, then the xor-butterfly), and
+// every element becomes bf16((x * rinv) * gamma): the A operand is bit for bit
+// the RMSNorm kernel's output, so whether a step normalises in a kernel or in
+// the GEMM does not change a row's bits.
+//
 // BI_VARIANT splits K over CTAs into an fp32 workspace when the output has
 // fewer 128x128 tiles than SMs and adds the partials in split order in a
 // second kernel: deterministic run to run, but its order depends on M.
@@ -98,7 +109,17 @@ struct GemmArgs {
     int32_t* status;
     uint64_t wait_ns;      // bound of every wait (2 s; shorter in the wait test)
     int32_t skip_stage;    // wait test: the ring stage (in issue order) whose copies are withheld, else -1
+    int32_t norm_on;       // 1: A = bf16((x * rinv) * gamma) of x's first M rows (M <= kNormMaxM), A loads raw x
+    const uint4* norm_x;   // [M.., K / 8]
+    const uint4* norm_gamma;
+    float norm_eps;
 };
+
+// Rows up to which a GEMM may take its A operand through a fused RMSNorm:
+// warps 2-3 then rescale every landed A stage of every output tile they visit
+// in shared memory, M x 256 elements per stage, which stays below a stage's
+// MMA time for these rows.
+constexpr int64_t kNormMaxM = 8;
 
 __device__ __forceinline__ float silu_mul(float g, float u) {
     const float s = __fdiv_rn(g, __fadd_rn(1.0f, expf(-g)));
@@ -108,6 +129,7 @@ __device__ __forceinline__ float silu_mul(float g, float u) {
 __device__ __forceinline__ void mbar_arrive(uint64_t* bar) {
     asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(smem_u32(bar)) : "memory");
 }
+
 
 // Epilogue of one 64-column group (one MMA's worth) of one row: 64 fp32
 // accumulators in r, output columns n0 .. n0+63 of the GEMM.
@@ -180,47 +202,102 @@ __device__ __forceinline__ uint32_t acc_col(int32_t o) {
     }
 }
 
-// RoPE + KV append of one GEMM row (token) over the heads of one tile, the
-// arithmetic of rope_append_kernel: rotate-half pairs (i, i + Dh/2) of q and
-// k heads as r0 = x0 c - x1 s, r1 = x1 c + x0 s in fp32, one bf16 rounding;
-// q to q_out, k and v to the token's page slot.  Every lane loads (the TMEM
-// loads are warp-wide); only rows < M store.
-template <int BN, int CG>
-__device__ __forceinline__ void rope_epilogue(const GemmArgs& args, uint32_t taddr, int64_t row, int32_t n_tile) {
+// RoPE + KV append of one GEMM row (token), the arithmetic of rope_append_kernel: rotate-half pairs
+// (i, i + Dh/2) of q and k heads as r0 = x0 c - x1 s, r1 = x1 c + x0 s in fp32, one bf16 rounding; q to q_out,
+// k and v to the token's page slot.  The row's position and page are looked up once (bad ones reported).
+struct RopeRow {
+    bool ok;
+    int32_t pos, page, slot;
+    const float* crow;
+    const float* srow;
+};
+
+__device__ __forceinline__ RopeRow rope_row(const GemmArgs& args, int64_t row, bool live) {
     const RopeFuse& rp = args.rope;
-    const int32_t Dh = rp.Dh, half = Dh / 2;
-    const bool live = row < args.M;
-    int32_t pos = 0, page = 0;
-    bool ok = false;
+    RopeRow r{false, 0, 0, 0, nullptr, nullptr};
     if (live) {
-        pos = rp.tok_pos[row];
+        r.pos = rp.tok_pos[row];
         const int32_t req = rp.tok_req[row];
-        ok = pos >= 0 && pos < rp.max_pos && (pos / BI_PAGE) < rp.max_pages;
-        if (ok) {
-            page = rp.page_table[static_cast<int64_t>(req) * rp.max_pages + pos / BI_PAGE];
-            if (page < 0 || page >= rp.num_pages) {
+        r.ok = r.pos >= 0 && r.pos < rp.max_pos && (r.pos / BI_PAGE) < rp.max_pages;
+        if (r.ok) {
+            r.page = rp.page_table[static_cast<int64_t>(req) * rp.max_pages + r.pos / BI_PAGE];
+            if (r.page < 0 || r.page >= rp.num_pages) {
                 report(args.status, BI_DEV_BAD_PAGE);
-                ok = false;
+                r.ok = false;
             }
         } else {
             report(args.status, BI_DEV_BAD_POSITION);
         }
     }
-    const int32_t slot = pos & (BI_PAGE - 1);
-    const float* crow = rp.rc + static_cast<int64_t>(ok ? pos : 0) * half;
-    const float* srow = rp.rs + static_cast<int64_t>(ok ? pos : 0) * half;
+    const int32_t half = rp.Dh / 2;
+    r.slot = r.pos & (BI_PAGE - 1);
+    r.crow = rp.rc + static_cast<int64_t>(r.ok ? r.pos : 0) * half;
+    r.srow = rp.rs + static_cast<int64_t>(r.ok ? r.pos : 0) * half;
+    return r;
+}
+
+// Destination of one head of the row (q_out, or the K/V cache slot), or null (k/v of a row without a slot).
+__device__ __forceinline__ uint16_t* rope_dst(const RopeFuse& rp, const RopeRow& rr, int64_t row, int32_t head) {
+    if (head < rp.H) return rp.q_out + (row * rp.H + head) * rp.Dh;
+    if (!rr.ok) return nullptr;
+    const bool is_k = head < rp.H + rp.Hkv;
+    const int32_t g = is_k ? head - rp.H : head - rp.H - rp.Hkv;
+    return (is_k ? rp.kc : rp.vc) + ((static_cast<int64_t>(rr.page) * rp.Hkv + g) * BI_PAGE + rr.slot) * rp.Dh;
+}
+
+// Elements c .. c+15 of both halves of one head: ra = x[c..], rb = x[half + c..] (fp32 bits); rotated when rot
+// (q and k heads), stored to d[c..] and d[half + c..].
+__device__ __forceinline__ void rope_chunk16(const RopeRow& rr, int32_t half, int32_t c, bool rot,
+                                             const uint32_t (&ra)[16], const uint32_t (&rb)[16], uint16_t* dst) {
+    float cs16[16], sn16[16];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) {
+        const float4 cv = rr.ok ? reinterpret_cast<const float4*>(rr.crow + c)[v] : make_float4(1.f, 1.f, 1.f, 1.f);
+        const float4 sv = rr.ok ? reinterpret_cast<const float4*>(rr.srow + c)[v] : make_float4(0.f, 0.f, 0.f, 0.f);
+        cs16[4 * v] = cv.x; cs16[4 * v + 1] = cv.y; cs16[4 * v + 2] = cv.z; cs16[4 * v + 3] = cv.w;
+        sn16[4 * v] = sv.x; sn16[4 * v + 1] = sv.y; sn16[4 * v + 2] = sv.z; sn16[4 * v + 3] = sv.w;
+    }
+    uint32_t o0[8], o1[8];
+#pragma unroll
+    for (int e = 0; e < 16; e += 2) {
+        float r0[2], r1[2];
+#pragma unroll
+        for (int u = 0; u < 2; ++u) {
+            const float x0 = __uint_as_float(ra[e + u]), x1 = __uint_as_float(rb[e + u]);
+            if (rot) {
+                const float cs = cs16[e + u];
+                const float sn = sn16[e + u];
+                r0[u] = __fsub_rn(__fmul_rn(x0, cs), __fmul_rn(x1, sn));
+                r1[u] = __fadd_rn(__fmul_rn(x1, cs), __fmul_rn(x0, sn));
+            } else {
+                r0[u] = x0;
+                r1[u] = x1;
+            }
+        }
+        o0[e / 2] = pack_bf16x2(r0[0], r0[1]);
+        o1[e / 2] = pack_bf16x2(r1[0], r1[1]);
+    }
+    uint4* d0 = reinterpret_cast<uint4*>(dst + c);
+    uint4* d1 = reinterpret_cast<uint4*>(dst + half + c);
+    d0[0] = make_uint4(o0[0], o0[1], o0[2], o0[3]);
+    d0[1] = make_uint4(o0[4], o0[5], o0[6], o0[7]);
+    d1[0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
+    d1[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
+}
+
+// The row's heads of one tile from its TMEM lane.  Every lane loads (the TMEM loads are warp-wide); only
+// rows < M store.
+template <int BN, int CG>
+__device__ __forceinline__ void rope_epilogue(const GemmArgs& args, uint32_t taddr, int64_t row, int32_t n_tile) {
+    const RopeFuse& rp = args.rope;
+    const int32_t Dh = rp.Dh, half = Dh / 2;
+    const bool live = row < args.M;
+    const RopeRow rr = rope_row(args, row, live);
 #pragma unroll 1
     for (int32_t hs = 0; hs < BN / Dh; ++hs) {
         const int32_t head = (n_tile * BN + hs * Dh) / Dh;
         const bool rot = head < rp.H + rp.Hkv;
-        uint16_t* dst = nullptr;
-        if (head < rp.H) {
-            dst = rp.q_out + (row * rp.H + head) * Dh;
-        } else if (ok) {
-            const bool is_k = head < rp.H + rp.Hkv;
-            const int32_t g = is_k ? head - rp.H : head - rp.H - rp.Hkv;
-            dst = (is_k ? rp.kc : rp.vc) + ((static_cast<int64_t>(page) * rp.Hkv + g) * BI_PAGE + slot) * Dh;
-        }
+        uint16_t* dst = live ? rope_dst(rp, rr, row, head) : nullptr;
         const uint32_t ta = acc_col<BN, CG>(hs * Dh), tb = acc_col<BN, CG>(hs * Dh + half);
 #pragma unroll 1
         for (int32_t c = 0; c < half; c += 16) {
@@ -228,43 +305,43 @@ __device__ __forceinline__ void rope_epilogue(const GemmArgs& args, uint32_t tad
             ptx::tmem_ld16(taddr + ta + c, ra);
             ptx::tmem_ld16(taddr + tb + c, rb);
             ptx::tmem_ld_wait();
-            if (live && dst != nullptr) {
-                float cs16[16], sn16[16];
+            if (dst != nullptr) rope_chunk16(rr, half, c, rot, ra, rb, dst);
+        }
+    }
+}
+
+// Fused RMSNorm: rinv of the rows r = wi, wi + 6, ... (< M) of x, one warp per row (wi = 0..5: warps 2-7 of
+// the issuing CTA), in the RMSNorm kernel's order: lane l adds the squares of 16-byte chunks l, l + 32, ... in
+// ascending element order with fused multiply-adds, the lane sums meet in an xor-butterfly (16, 8, 4, 2, 1),
+// then rinv = 1 / sqrt(sum / K + eps).  A lane issues all its loads of a row before it uses any.
+__device__ __forceinline__ void norm_rinv_rows(const GemmArgs& args, float* rinv_out, int wi) {
+    const int lane = threadIdx.x & 31;
+    const int32_t d8 = args.K / 8;
+    constexpr int kMaxPerLane = 16;  // K <= 4096
+    for (int32_t r = wi; r < args.M; r += 6) {
+        const uint4* xr = args.norm_x + static_cast<int64_t>(r) * d8;
+        uint4 v[kMaxPerLane];
 #pragma unroll
-                for (int v = 0; v < 4; ++v) {
-                    const float4 cv = ok ? reinterpret_cast<const float4*>(crow + c)[v] : make_float4(1.f, 1.f, 1.f, 1.f);
-                    const float4 sv = ok ? reinterpret_cast<const float4*>(srow + c)[v] : make_float4(0.f, 0.f, 0.f, 0.f);
-                    cs16[4 * v] = cv.x; cs16[4 * v + 1] = cv.y; cs16[4 * v + 2] = cv.z; cs16[4 * v + 3] = cv.w;
-                    sn16[4 * v] = sv.x; sn16[4 * v + 1] = sv.y; sn16[4 * v + 2] = sv.z; sn16[4 * v + 3] = sv.w;
+        for (int i = 0; i < kMaxPerLane; ++i)
+            if (lane + 32 * i < d8) v[i] = xr[lane + 32 * i];
+        float ss = 0.0f;
+#pragma unroll
+        for (int i = 0; i < kMaxPerLane; ++i) {
+            if (lane + 32 * i < d8) {
+                const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+#pragma unroll
+                for (int e = 0; e < 4; ++e) {
+                    const float a = bf16_lo(w[e]);
+                    ss = __fmaf_rn(a, a, ss);
+                    const float b = bf16_hi(w[e]);
+                    ss = __fmaf_rn(b, b, ss);
                 }
-                uint32_t o0[8], o1[8];
-#pragma unroll
-                for (int e = 0; e < 16; e += 2) {
-                    float r0[2], r1[2];
-#pragma unroll
-                    for (int u = 0; u < 2; ++u) {
-                        const float x0 = __uint_as_float(ra[e + u]), x1 = __uint_as_float(rb[e + u]);
-                        if (rot) {
-                            const float cs = cs16[e + u];
-                            const float sn = sn16[e + u];
-                            r0[u] = __fsub_rn(__fmul_rn(x0, cs), __fmul_rn(x1, sn));
-                            r1[u] = __fadd_rn(__fmul_rn(x1, cs), __fmul_rn(x0, sn));
-                        } else {
-                            r0[u] = x0;
-                            r1[u] = x1;
-                        }
-                    }
-                    o0[e / 2] = pack_bf16x2(r0[0], r0[1]);
-                    o1[e / 2] = pack_bf16x2(r1[0], r1[1]);
-                }
-                uint4* d0 = reinterpret_cast<uint4*>(dst + c);
-                uint4* d1 = reinterpret_cast<uint4*>(dst + half + c);
-                d0[0] = make_uint4(o0[0], o0[1], o0[2], o0[3]);
-                d0[1] = make_uint4(o0[4], o0[5], o0[6], o0[7]);
-                d1[0] = make_uint4(o1[0], o1[1], o1[2], o1[3]);
-                d1[1] = make_uint4(o1[4], o1[5], o1[6], o1[7]);
             }
         }
+#pragma unroll
+        for (int off = 16; off >= 1; off >>= 1) ss = __fadd_rn(ss, __shfl_xor_sync(0xffffffffu, ss, off));
+        const float mean = __fdiv_rn(ss, static_cast<float>(args.K));
+        if (lane == 0) rinv_out[r] = __fdiv_rn(1.0f, __fsqrt_rn(__fadd_rn(mean, args.norm_eps)));
     }
 }
 
@@ -287,10 +364,12 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
     uint8_t* sW = smem + args.a_region;
     uint64_t* full = reinterpret_cast<uint64_t*>(sW + args.stages * args.kps * kWBytes);
     uint64_t* empty = full + kMaxStages;
-    uint64_t* acc_full = empty + kMaxStages;     // [2]
+    uint64_t* a_full = empty + kMaxStages;       // fused RMSNorm: the raw A rows of a stage landed
+    uint64_t* acc_full = a_full + kMaxStages;    // [2]
     uint64_t* acc_empty = acc_full + 2;          // [2]
     uint64_t* drain = acc_empty + 2;
     uint32_t* tmem_holder = reinterpret_cast<uint32_t*>(drain + 1);
+    __shared__ float norm_rinv[kNormMaxM];  // fused RMSNorm: each row's rinv
     int32_t* abort_word = reinterpret_cast<int32_t*>(tmem_holder + 1);
     volatile int32_t* abort_flag = abort_word;
 
@@ -323,8 +402,9 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         ptx::prefetch_tmap(&tmA);
         ptx::prefetch_tmap(&tmW);
         for (int s = 0; s < S; ++s) {
-            ptx::mbar_init(&full[s], 1);
+            ptx::mbar_init(&full[s], args.norm_on ? 2 : 1);  // + the A writers' arrival
             ptx::mbar_init(&empty[s], 1);
+            ptx::mbar_init(&a_full[s], 1);
         }
         for (int b = 0; b < 2; ++b) {
             ptx::mbar_init(&acc_full[b], 1);
@@ -370,7 +450,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             // boxes always land whole (out-of-range rows and K tiles are zero-filled); the
             // issuing CTA's full barrier counts the bytes of every CTA of the group
             const uint32_t stage_tx =
-                static_cast<uint32_t>(CG * kps) * (static_cast<uint32_t>(args.a_stride) + kWBytes);
+                static_cast<uint32_t>(CG * kps) * (static_cast<uint32_t>(args.norm_on ? 0 : args.a_stride) + kWBytes);
             const int32_t a_row0 = static_cast<int32_t>(rank) * kBM;     // this CTA's rows of the tile
             const int32_t w_row0 = static_cast<int32_t>(rank) * kWRows;  // this CTA's W rows of the tile
             auto load = [&](void* dst, const CUtensorMap* map, int s_, int32_t y, int32_t z, uint64_t pol) {
@@ -378,6 +458,17 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     ptx::tma_load_3d_pair(dst, map, ptx::mapa_shared(smem_u32(&full[s_]), 0), 0, y, z, pol);
                 else
                     ptx::tma_load_3d(dst, map, &full[s_], 0, y, z, pol);
+            };
+            // A of a stage: counted with W on the group's full barrier, or (fused RMSNorm) the issuing CTA's raw
+            // rows on a_full for the A writers, who then complete full themselves (the other CTA's rows lie
+            // past M and keep their zeros)
+            auto load_a = [&](int s_, int32_t y, int32_t z) {
+                if (!args.norm_on) {
+                    load(sA + s_ * kps * args.a_stride, &tmA, s_, y, z, pol_a);
+                } else if (rank == 0) {
+                    ptx::mbar_arrive_expect_tx(&a_full[s_], static_cast<uint32_t>(kps * args.a_stride));
+                    ptx::tma_load_3d(sA + s_ * kps * args.a_stride, &tmA, &a_full[s_], 0, y, z, pol_a);
+                }
             };
             // Weights do not depend on the kernel before this one: when the
             // caller guarantees that nothing still in flight writes them, the
@@ -407,7 +498,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 for (int32_t kb = 0; kb < nkb; kb += kps) {
                     if (issued < pre) {
                         // armed, W already requested: only A is missing
-                        load(sA + s * kps * args.a_stride, &tmA, s, a_row, kb0 + kb, pol_a);
+                        load_a(s, a_row, kb0 + kb);
                     } else {
                         if (!ptx::mbar_wait_bounded(&empty[s], ph ^ 1u, abort_flag, args.wait_ns)) {
                             if (!*abort_flag) report(args.status, BI_DEV_TIMEOUT_PRODUCER);
@@ -417,7 +508,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         }
                         if (static_cast<int32_t>(issued) != args.skip_stage) {
                             if (rank == 0) ptx::mbar_arrive_expect_tx(&full[s], stage_tx);
-                            load(sA + s * kps * args.a_stride, &tmA, s, a_row, kb0 + kb, pol_a);
+                            load_a(s, a_row, kb0 + kb);
                             load(sW + s * kps * kWBytes, &tmW, s, n_tile * BN + w_row0, kb0 + kb, pol_w);
                         }
                     }
@@ -436,7 +527,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                     const int qs = static_cast<int>(q % S);
                     const uint32_t qph = (q / S) & 1u;
                     const uint64_t t0 = globaltimer_ns();
-                    while (!ptx::mbar_try_wait(smem_u32(&full[qs]), qph)) {
+                    while (!ptx::mbar_try_wait(smem_u32(&full[qs]), qph) ||
+                           (args.norm_on && !ptx::mbar_try_wait(smem_u32(&a_full[qs]), qph))) {
                         if (globaltimer_ns() - t0 > args.wait_ns) {
                             report(args.status, BI_DEV_TIMEOUT_DRAIN);
                             break;
@@ -511,8 +603,76 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 }
             }
         }
+    } else if ((warp == 2 || warp == 3) && args.norm_on && rank == 0) {
+        // ---- A writers (fused RMSNorm): warps 2-3 of the issuing CTA; the tile's rows < M all lie in this
+        // CTA's 128 rows (the pair's other CTA keeps its zeroed A region) ----
+        norm_rinv_rows(args, norm_rinv, warp - 2);
+        asm volatile("bar.sync 2, 192;" ::: "memory");  // every row's rinv (warps 2-7)
+        const int t = threadIdx.x - 64;  // 0..63
+        const int32_t rows = static_cast<int32_t>(args.M);
+        int s = 0;
+        uint32_t ph = 0;
+        for (int32_t tile = unit; tile < args.total_tiles; tile += nunits) {
+            bool ok = true;
+            for (int32_t kb = 0; kb < nkb; kb += kps) {
+                if (!ptx::mbar_wait_bounded(&a_full[s], ph, abort_flag, args.wait_ns)) {
+                    if (!*abort_flag) report(args.status, BI_DEV_TIMEOUT_PRODUCER);
+                    raise_abort();
+                    ok = false;
+                    break;
+                }
+                // in place: chunk position p of row r of K tile j holds the 8 elements of chunk p ^ (r % 8)
+                // (the 128-byte swizzle of the TMA box)
+                const int32_t cnt = min(kps, nkb - kb);
+                const int32_t total = rows * cnt * 8;  // <= kNormMaxM * 4 * 8 (kps <= 4 for 128-wide tiles)
+                uint8_t* stage_a = sA + s * kps * args.a_stride;
+                constexpr int kIt = static_cast<int>(kNormMaxM) * 4 * 8 / 64;
+                uint4 v[kIt], g[kIt];
+                uint4* cell[kIt];
+                float rinv[kIt];
+                // every read of the stage first, then the arithmetic and the writes
+#pragma unroll
+                for (int u = 0; u < kIt; ++u) {
+                    const int32_t i = t + 64 * u;
+                    if (i < total) {
+                        const int32_t r = i / (cnt * 8), rem = i % (cnt * 8), j = rem / 8, pos = rem % 8;
+                        cell[u] = reinterpret_cast<uint4*>(stage_a + j * args.a_stride + r * 128 + pos * 16);
+                        v[u] = *cell[u];
+                        g[u] = __ldg(args.norm_gamma + (kb0 + kb + j) * 8 + (pos ^ (r & 7)));
+                        rinv[u] = norm_rinv[r];
+                    }
+                }
+#pragma unroll
+                for (int u = 0; u < kIt; ++u) {
+                    if (t + 64 * u < total) {
+                        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                        const uint32_t gw[4] = {g[u].x, g[u].y, g[u].z, g[u].w};
+                        uint32_t o[4];
+#pragma unroll
+                        for (int e = 0; e < 4; ++e) {
+                            const float x0 = __fmul_rn(__fmul_rn(bf16_lo(w[e]), rinv[u]), bf16_lo(gw[e]));
+                            const float x1 = __fmul_rn(__fmul_rn(bf16_hi(w[e]), rinv[u]), bf16_hi(gw[e]));
+                            o[e] = pack_bf16x2(x0, x1);
+                        }
+                        *cell[u] = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+                }
+                ptx::fence_proxy_async_smem();  // the generic writes before the MMAs (async proxy) read them
+                asm volatile("bar.sync 3, 64;" ::: "memory");
+                if (t == 0) mbar_arrive(&full[s]);
+                if (++s == S) {
+                    s = 0;
+                    ph ^= 1u;
+                }
+            }
+            if (!ok) break;
+        }
     } else if (warp >= 4) {
         // ---- epilogue: warps 4..7 of each CTA, on that CTA's 128 rows ----
+        if (args.norm_on && rank == 0) {  // first, rinv of some rows for the A writers
+            norm_rinv_rows(args, norm_rinv, warp - 2);
+            asm volatile("bar.sync 2, 192;" ::: "memory");
+        }
         const int q = warp & 3;
         int32_t i = 0;
         for (int32_t tile = unit; tile < args.total_tiles; tile += nunits, ++i) {
@@ -828,11 +988,20 @@ bool gemm_can_fuse_rope(int64_t M, int32_t N, int32_t K, bi_mode mode, int32_t D
     return M > 0 && N > 0 && gemm_plan(M, N, K, mode).splits == 1 && (Dh == 64 || Dh == 128);
 }
 
+bool gemm_can_fuse_norm(int64_t M, int32_t N, int32_t K, bi_mode mode) {
+    return M > 0 && M <= kNormMaxM && N > 0 && K % kBK == 0 && K <= 4096 && gemm_plan(M, N, K, mode).splits == 1;
+}
+
 bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype, const bi_bf16* residual,
                    bi_epilogue ep, int64_t M, int32_t N, int32_t K, bi_mode mode, void* ws, size_t ws_bytes,
                    int32_t* status, cudaStream_t s, bool weights_settled, const ArgmaxFuse* am,
-                   const RopeFuse* rope, const GemmWaitTest* wait_test) {
+                   const RopeFuse* rope, const GemmWaitTest* wait_test, const NormFuse* norm) {
     if (M == 0) return BI_OK;
+    if (norm != nullptr) {
+        if (!gemm_can_fuse_norm(M, N, K, mode) || wait_test != nullptr || norm->rows != nullptr)
+            return fail(BI_ERR_INVALID, "fused RMSNorm needs at most 8 contiguous rows, K <= 4096 and no split-K");
+        A = norm->x;  // the A ring receives the raw rows
+    }
     const GemmPlan plan = gemm_plan(M, N, K, mode);
     const Layout L = choose_layout(M, N, K);
 
@@ -863,6 +1032,12 @@ bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype
     a.status = status;
     a.wait_ns = wait_test != nullptr ? wait_test->wait_ns : kWaitLimitNs;
     a.skip_stage = wait_test != nullptr ? wait_test->skip_stage : -1;
+    if (norm != nullptr) {
+        a.norm_on = 1;
+        a.norm_x = reinterpret_cast<const uint4*>(norm->x);
+        a.norm_gamma = reinterpret_cast<const uint4*>(norm->gamma);
+        a.norm_eps = norm->eps;
+    }
     if (rope != nullptr) {
         if (!gemm_can_fuse_rope(M, N, K, mode, rope->Dh) || am != nullptr || ep != BI_EP_NONE ||
             N != (rope->H + 2 * rope->Hkv) * rope->Dh)

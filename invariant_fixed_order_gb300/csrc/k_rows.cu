@@ -27,13 +27,13 @@ template <int CPL, bool kEmbed>
 __global__ void __launch_bounds__(kNormWarps * 32)
 rmsnorm_kernel(const uint4* x, const uint4* __restrict__ gamma, uint4* y, int64_t rows, int32_t d8, float eps,
                float fd, const int32_t* __restrict__ src_rows, unsigned long long* am_keys, unsigned int* am_counter,
-               const int32_t* __restrict__ ids, int32_t V, uint4* x_out, int32_t* status) {
+               int64_t am_rows, const int32_t* __restrict__ ids, int32_t V, uint4* x_out, int32_t* status) {
     pdl_trigger();
     pdl_wait();
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kNormWarps + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;  // uniform per warp
-    if (am_keys != nullptr && lane == 0) {
+    if (am_keys != nullptr && lane == 0 && row < am_rows) {  // a fused argmax later in the stream
         am_keys[row] = kArgmaxKeyNone;
         if (row == 0) *am_counter = 0u;
     }
@@ -121,8 +121,8 @@ rmsnorm_kernel(const uint4* x, const uint4* __restrict__ gamma, uint4* y, int64_
 template <bool kEmbed>
 static cudaError_t launch_rmsnorm_t(bool pdl, const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y, int64_t rows,
                                     int32_t d, float eps, cudaStream_t s, const int32_t* src_rows,
-                                    const ArgmaxFuse* am, const int32_t* ids, int32_t V, bi_bf16* x_out,
-                                    int32_t* status) {
+                                    const ArgmaxFuse* am, int64_t am_rows, const int32_t* ids, int32_t V,
+                                    bi_bf16* x_out, int32_t* status) {
     if (rows <= 0) return cudaSuccess;
     const dim3 grid(static_cast<unsigned>((rows + kNormWarps - 1) / kNormWarps));
     const dim3 block(kNormWarps * 32);
@@ -130,8 +130,8 @@ static cudaError_t launch_rmsnorm_t(bool pdl, const bi_bf16* x, const bi_bf16* g
     auto go = [&](auto kernel) {
         return launch_k(pdl, kernel, grid, block, 0, s, reinterpret_cast<const uint4*>(x),
                         reinterpret_cast<const uint4*>(gamma), reinterpret_cast<uint4*>(y), rows, d8, eps,
-                        static_cast<float>(d), src_rows, am ? am->keys : nullptr, am ? am->counter : nullptr, ids, V,
-                        reinterpret_cast<uint4*>(x_out), status);
+                        static_cast<float>(d), src_rows, am ? am->keys : nullptr, am ? am->counter : nullptr, am_rows,
+                        ids, V, reinterpret_cast<uint4*>(x_out), status);
     };
     if (d8 <= 32) return go(rmsnorm_kernel<1, kEmbed>);
     if (d8 <= 64) return go(rmsnorm_kernel<2, kEmbed>);
@@ -142,13 +142,16 @@ static cudaError_t launch_rmsnorm_t(bool pdl, const bi_bf16* x, const bi_bf16* g
 
 cudaError_t launch_rmsnorm(const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y, int64_t rows, int32_t d, float eps,
                            cudaStream_t s, const int32_t* src_rows, const ArgmaxFuse* am) {
-    return launch_rmsnorm_t<false>(true, x, gamma, y, rows, d, eps, s, src_rows, am, nullptr, 0, nullptr, nullptr);
+    return launch_rmsnorm_t<false>(true, x, gamma, y, rows, d, eps, s, src_rows, am, rows, nullptr, 0, nullptr,
+                                   nullptr);
 }
 
 cudaError_t launch_embed_rmsnorm(const bi_bf16* E, const int32_t* ids, int32_t V, const bi_bf16* gamma, bi_bf16* x,
-                                 bi_bf16* y, int32_t T, int32_t d, float eps, int32_t* status, cudaStream_t s) {
-    // the step's first kernel: launched without programmatic serialisation, so it waits for all earlier work
-    return launch_rmsnorm_t<true>(false, E, gamma, y, T, d, eps, s, nullptr, nullptr, ids, V, x, status);
+                                 bi_bf16* y, int32_t T, int32_t d, float eps, int32_t* status, cudaStream_t s,
+                                 const ArgmaxFuse* am, int64_t am_rows) {
+    // the step's first kernel: launched without programmatic serialisation, so it waits for all earlier work;
+    // it also initialises the keys of the step's fused greedy argmax (rows < am_rows <= T)
+    return launch_rmsnorm_t<true>(false, E, gamma, y, T, d, eps, s, nullptr, am, am_rows, ids, V, x, status);
 }
 
 // ---------------------------------------------------------------------------

@@ -130,6 +130,32 @@ def test_gemm_pair_and_single_forms_give_identical_bits(bi, K):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("N,K", [(4096, 4096), (4096, 14336), (65792, 4096)])
+def test_gemm_rows_at_every_m_match_a_300_row_product(bi, N, K):
+    """How a product is laid out follows M (the A box height, the tile width, the ring), never the
+    arithmetic of an element: every row at every M up to 128 has the bits of the same row in a 300-row
+    product (256-wide tiles there), for fp32 output, the residual epilogue and the SwiGLU epilogue, in
+    the pair form (N <= 65536) and the single-CTA form (above)."""
+    A = rand_bf16((300, K), 1.0, 620 + K)
+    W = rand_bf16((N, K), 0.02, 621 + N)
+    R = rand_bf16((300, N), 1.0, 622)
+    full = bits(bi.gemm(A, W, c_dtype=bi.F32))
+    full_res = bits(bi.gemm(A, W, residual=R, ep=bi.EP_RESIDUAL))
+    full_glu = bits(bi.gemm(A, W, ep=bi.EP_SWIGLU)) if N <= 8192 else None
+    rng = np.random.default_rng(K + N)
+    for M in (1, 2, 7, 16, 17, 33, 64, 65, 100, 128):
+        rows = np.sort(rng.choice(300, size=M, replace=False))
+        idx = torch.from_numpy(rows).cuda()
+        sub = A[idx].contiguous()
+        assert np.array_equal(bits(bi.gemm(sub, W, c_dtype=bi.F32)), full[rows]), (M, N, K)
+        got = bits(bi.gemm(sub, W, residual=R[idx].contiguous(), ep=bi.EP_RESIDUAL))
+        assert np.array_equal(got, full_res[rows]), (M, N, K)
+        if full_glu is not None:
+            assert np.array_equal(bits(bi.gemm(sub, W, ep=bi.EP_SWIGLU)), full_glu[rows]), (M, N, K)
+    del A, W, R
+    torch.cuda.empty_cache()
+
+
 def test_gemm_swiglu_epilogue(bi):
     M, F, K = 40, 256, 512
     A = rand_bf16((M, K), 1.0, 500)
