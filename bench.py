@@ -55,6 +55,9 @@ def parse():
                    default=None,
                    help="launch only the named GEMMs (twice: warm-up, then the pass to capture) for an ncu "
                         "capture; prints no measurement")
+    p.add_argument("--floor", action="store_true",
+                   help="print the GEMM floor microbenchmarks (ns per MMA per tcgen05 form, per-SM ingest) and the "
+                        "floor they give each decode projection at M = 1, against its measured time")
     return p.parse_args()
 
 
@@ -287,6 +290,90 @@ def gemm_chain(steps: int, stream) -> dict:
             "ns_per_dependent_mma": round(slope * 1e3, 2), "fixed_us": round(icpt, 2),
             "layer_chain_mmas": chains, "layer_chain_floor_us": floor,
             "layer_chain_floor_total_us": round(sum(floor.values()), 1)}
+
+
+def gemm_floor(stream) -> dict:
+    """What bounds a decode projection at M = 1 (one token), measured.  libbi_probe.so times one tcgen05 MMA
+    per instruction form (operands resident in shared memory, unrolled issue) and how fast one SM takes in a
+    stream (TMA boxes, bulk copies; one CTA per SM).  In the CTA-pair form a 64-deep K tile costs each SM of
+    a pair four pair MMAs and bringing in 10 KB (its 64 W rows and the 16-row A box); a projection's tiles
+    run K / 64 such K tiles in a row, in waves over the 76 pairs.  The floor is that chain at the larger of
+    the two costs per K tile (no launch overhead); each projection is also timed standalone at M = 1 with
+    the L2 flushed before every launch."""
+    import ctypes
+    import torch
+    from invariant_fixed_order_gb300 import bi
+    from invariant_fixed_order_gb300 import build as B
+    from invariant_fixed_order_gb300.config import LLAMA3_8B
+    lib = ctypes.CDLL(B.PROBE_LIB)
+    dp = ctypes.POINTER(ctypes.c_double)
+    lib.bip_mma_ns.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int, dp]
+    lib.bip_ingest.argtypes = [ctypes.c_int, ctypes.c_int, dp, dp]
+
+    def mma(cg, m, n, nacc=1):
+        v = ctypes.c_double()
+        rc = lib.bip_mma_ns(cg, m, n, nacc, ctypes.byref(v))
+        if rc != 0:
+            raise RuntimeError(f"bip_mma_ns({cg}, {m}, {n}, {nacc}) returned {rc}")
+        return round(v.value, 2)
+
+    forms = {"single 128x16": mma(1, 128, 16), "single 128x32": mma(1, 128, 32), "single 128x64": mma(1, 128, 64),
+             "single 128x128": mma(1, 128, 128), "single 64x16": mma(1, 64, 16), "pair 256x64": mma(2, 256, 64),
+             "pair 256x128": mma(2, 256, 128), "pair 256x256": mma(2, 256, 256),
+             "single 128x64, 4 accumulators alternating": mma(1, 128, 64, 4),
+             "pair 256x128, 2 accumulators alternating": mma(2, 256, 128, 2)}
+    ingest = {}
+    for mode, name in ((0, "tma 2-D boxes, 128 rows x 128 B contiguous"), (1, "bulk 1-D copies of 16 KB"),
+                       (2, "tma 3-D weight-ring boxes: 64 rows x 4 K tiles of a 128 KB-row matrix")):
+        rows = []
+        for ctas in (1, 32, 64, 96, 128, 152):
+            a, t = ctypes.c_double(), ctypes.c_double()
+            rc = lib.bip_ingest(mode, ctas, ctypes.byref(a), ctypes.byref(t))
+            if rc != 0:
+                raise RuntimeError(f"bip_ingest({mode}, {ctas}) returned {rc}")
+            rows.append({"ctas": ctas, "gbps_per_cta": round(a.value, 1), "gbps_total": round(t.value, 1)})
+        ingest[name] = rows
+    per_cta = {r["ctas"]: r["gbps_per_cta"] for r in ingest["tma 3-D weight-ring boxes: 64 rows x 4 K tiles of a "
+                                                            "128 KB-row matrix"]}
+    c = LLAMA3_8B
+    pairs = 76
+    shapes = {"qkv": (c.qkv_dim, c.d, bi.EP_NONE), "o": (c.d, c.H * c.Dh, bi.EP_RESIDUAL),
+              "gate_up": (2 * c.F, c.d, bi.EP_SWIGLU), "down": (c.d, c.F, bi.EP_RESIDUAL)}
+    g = torch.Generator(device="cuda").manual_seed(9)
+    flush = torch.empty(256 << 20, dtype=torch.uint8, device="cuda")
+    proj = {}
+    for name, (N, K, ep) in shapes.items():
+        tiles = N // 128
+        waves = -(-tiles // pairs)
+        sms = 2 * min(tiles, pairs)
+        ktiles = (K // 64) * waves
+        mma_ns = 4 * forms["pair 256x128"]
+        ingest_ns = 10240 / per_cta[min((1, 32, 64, 96, 128, 152), key=lambda x: abs(x - sms))]
+        floor_us = ktiles * max(mma_ns, ingest_ns) / 1e3
+        W = (torch.randn(N, K, device="cuda", generator=g) * 0.02).to(torch.bfloat16)
+        A = torch.randn(1, K, device="cuda", generator=g).to(torch.bfloat16)
+        R = torch.randn(1, N, device="cuda", generator=g).to(torch.bfloat16)
+
+        def run(flush_only=False):
+            flush.zero_()
+            if flush_only:
+                return
+            if ep == bi.EP_RESIDUAL:
+                bi.gemm(A, W, residual=R, ep=ep, stream=stream)
+            elif ep == bi.EP_SWIGLU:
+                bi.gemm(A, W, ep=ep, stream=stream)
+            else:
+                bi.gemm(A, W, stream=stream)
+        t = min(time_steps(run, 30, 5, stream) for _ in range(3))
+        t0 = min(time_steps(lambda: run(True), 30, 5, stream) for _ in range(3))
+        measured = (t - t0) * 1e3
+        proj[name] = {"tiles": tiles, "sms": sms, "k_tiles_in_a_row": ktiles, "mma_ns_per_k_tile": round(mma_ns, 1),
+                      "ingest_ns_per_k_tile": round(ingest_ns, 1), "floor_us": round(floor_us, 1),
+                      "measured_us": round(measured, 1), "measured_over_floor": round(measured / floor_us, 2)}
+        del W
+    chain = gemm_chain(20, stream)
+    return {"mma_ns": forms, "ingest": ingest, "projections_m1": proj,
+            "chain_through_the_kernel": {k: chain[k] for k in ("ns_per_dependent_mma", "fixed_us")}}
 
 
 def logits_ops_time(w: GpuWorkload, steps: int, stream, hbm_peak: float) -> dict:
@@ -788,6 +875,12 @@ def ncu_target(which: str) -> None:
 
 def main():
     args = parse()
+    if args.floor:
+        import torch
+        from __graft_entry__ import build
+        build()
+        print(json.dumps({"gemm_floor": gemm_floor(torch.cuda.current_stream())}))
+        return
     if args.ncu_target:
         ncu_target(args.ncu_target)
         return

@@ -624,37 +624,40 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                 // in place: chunk position p of row r of K tile j holds the 8 elements of chunk p ^ (r % 8)
                 // (the 128-byte swizzle of the TMA box)
                 const int32_t cnt = min(kps, nkb - kb);
-                const int32_t total = rows * cnt * 8;  // <= kNormMaxM * 4 * 8 (kps <= 4 for 128-wide tiles)
+                const int32_t total = rows * cnt * 8;
                 uint8_t* stage_a = sA + s * kps * args.a_stride;
                 constexpr int kIt = static_cast<int>(kNormMaxM) * 4 * 8 / 64;
-                uint4 v[kIt], g[kIt];
-                uint4* cell[kIt];
-                float rinv[kIt];
-                // every read of the stage first, then the arithmetic and the writes
+                // passes of 64 * kIt cells over the stage (one pass for up to 4 K tiles of 8 rows); in each,
+                // every read first, then the arithmetic and the writes
+                for (int32_t base = 0; base < total; base += 64 * kIt) {
+                    uint4 v[kIt], g[kIt];
+                    uint4* cell[kIt];
+                    float rinv[kIt];
 #pragma unroll
-                for (int u = 0; u < kIt; ++u) {
-                    const int32_t i = t + 64 * u;
-                    if (i < total) {
-                        const int32_t r = i / (cnt * 8), rem = i % (cnt * 8), j = rem / 8, pos = rem % 8;
-                        cell[u] = reinterpret_cast<uint4*>(stage_a + j * args.a_stride + r * 128 + pos * 16);
-                        v[u] = *cell[u];
-                        g[u] = __ldg(args.norm_gamma + (kb0 + kb + j) * 8 + (pos ^ (r & 7)));
-                        rinv[u] = norm_rinv[r];
-                    }
-                }
-#pragma unroll
-                for (int u = 0; u < kIt; ++u) {
-                    if (t + 64 * u < total) {
-                        const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
-                        const uint32_t gw[4] = {g[u].x, g[u].y, g[u].z, g[u].w};
-                        uint32_t o[4];
-#pragma unroll
-                        for (int e = 0; e < 4; ++e) {
-                            const float x0 = __fmul_rn(__fmul_rn(bf16_lo(w[e]), rinv[u]), bf16_lo(gw[e]));
-                            const float x1 = __fmul_rn(__fmul_rn(bf16_hi(w[e]), rinv[u]), bf16_hi(gw[e]));
-                            o[e] = pack_bf16x2(x0, x1);
+                    for (int u = 0; u < kIt; ++u) {
+                        const int32_t i = base + t + 64 * u;
+                        if (i < total) {
+                            const int32_t r = i / (cnt * 8), rem = i % (cnt * 8), j = rem / 8, pos = rem % 8;
+                            cell[u] = reinterpret_cast<uint4*>(stage_a + j * args.a_stride + r * 128 + pos * 16);
+                            v[u] = *cell[u];
+                            g[u] = __ldg(args.norm_gamma + (kb0 + kb + j) * 8 + (pos ^ (r & 7)));
+                            rinv[u] = norm_rinv[r];
                         }
-                        *cell[u] = make_uint4(o[0], o[1], o[2], o[3]);
+                    }
+#pragma unroll
+                    for (int u = 0; u < kIt; ++u) {
+                        if (base + t + 64 * u < total) {
+                            const uint32_t w[4] = {v[u].x, v[u].y, v[u].z, v[u].w};
+                            const uint32_t gw[4] = {g[u].x, g[u].y, g[u].z, g[u].w};
+                            uint32_t o[4];
+#pragma unroll
+                            for (int e = 0; e < 4; ++e) {
+                                const float x0 = __fmul_rn(__fmul_rn(bf16_lo(w[e]), rinv[u]), bf16_lo(gw[e]));
+                                const float x1 = __fmul_rn(__fmul_rn(bf16_hi(w[e]), rinv[u]), bf16_hi(gw[e]));
+                                o[e] = pack_bf16x2(x0, x1);
+                            }
+                            *cell[u] = make_uint4(o[0], o[1], o[2], o[3]);
+                        }
                     }
                 }
                 ptx::fence_proxy_async_smem();  // the generic writes before the MMAs (async proxy) read them
@@ -899,6 +902,9 @@ constexpr int32_t kPairMaxN = 65536;
 // was measured no faster: ~50 us either way at M = 64.)
 int mma_group(int32_t N) { return N <= kPairMaxN ? 2 : 1; }
 
+// Rows up to which the pair form takes 8 K tiles per ring stage (below).
+constexpr int64_t kDeepStageMaxM = 16;
+
 // Layout of one launch.  Only data movement depends on M here; the MMA
 // sequence of every output element is the same for all layouts.
 Layout choose_layout(int64_t M, int32_t N, int32_t K) {
@@ -917,7 +923,12 @@ Layout choose_layout(int64_t M, int32_t N, int32_t K) {
     const int32_t budget = kRingBudget - pad;
     const int32_t per_k = L.a_stride + w_tile;  // bytes of one K tile of A and W
     // deep stages (one large copy per operand) while at least two still fit
-    L.kps = std::max(1, std::min({L.bn == 256 ? 2 : 4, K / kBK, budget / (2 * per_k)}));
+    // (few rows: 8 K tiles per stage in the pair form.  One SM's copy engine handles a few boxes per
+    // microsecond whatever their size up to tens of KB, so with 16-row A boxes the larger stages bring the
+    // weights in faster: measured 310 / 316 / 337 us per decode step at 1 / 4 / 8 tokens against 318 / 325 /
+    // 344 with 4 K tiles, and no better with 5-7; with more rows the A boxes grow and 4 stays best)
+    L.kps = std::max(1, std::min({L.bn == 256 ? 2 : (L.cg == 2 && M <= kDeepStageMaxM ? 8 : 4), K / kBK,
+                                  budget / (2 * per_k)}));
     int32_t stages = budget / (L.kps * per_k);
     stages = std::min(std::max(stages, 2), kMaxStages);
     L.stages = stages;
