@@ -561,7 +561,7 @@ extern "C" bi_status bi_forward_step(bi_model* m, const bi_batch* batch, const b
     // With few tokens the RMSNorms run inside the GEMMs that consume them (their A writers apply the norm
     // kernel's arithmetic), which saves a launch and a round trip of y per norm; a row's bits are the same
     // either way.  The gate/up GEMM streams the most weight per row of A, and above 4 rows its writers'
-    // per-stage pass shows on the step (8 rows: +10 us of 353), so it takes the norm only up to 4 rows.
+    // per-stage pass shows on the step (8 rows: 348 against 337 us), so it takes the norm only up to 4 rows.
     constexpr int64_t kNormInGateUpMaxRows = 4;
     const bool norm_in_qkv = gemm_can_fuse_norm(T, nqkv, c.d, mode);
     const bool norm_in_gu = T <= kNormInGateUpMaxRows && gemm_can_fuse_norm(T, 2 * c.F, c.d, mode);
