@@ -96,6 +96,7 @@ typedef enum {
 #define BI_DEV_BAD_PAGE 0x201
 #define BI_DEV_BAD_POSITION 0x202
 #define BI_DEV_BAD_TOKEN 0x203
+#define BI_DEV_BAD_LOGIT_ROWS 0x204  /* a replayed step's device logit rows are not the 0..R-1 its capture fused on */
 
 /* ---- diagnostics -------------------------------------------------------- */
 
@@ -378,7 +379,11 @@ typedef struct {
      * shapes (T, nd, R) and bounds: a replayed position must not exceed the
      * captured pos0[i] + q_len[i] - 1 of its request slot (the attention split
      * count and workspace were sized from it); larger positions are reported
-     * as BI_DEV_BAD_POSITION. */
+     * as BI_DEV_BAD_POSITION.  When logit_rows is 0..R-1 with R <= 8, the
+     * final RMSNorm runs inside the LM head on the first R rows of the
+     * residual stream (bit for bit the norm kernel's output), so the logit
+     * rows in meta must then be 0..R-1 too: any other list is reported as
+     * BI_DEV_BAD_LOGIT_ROWS (the logits then belong to rows 0..R-1). */
     const int32_t* meta;
 } bi_batch;
 

@@ -625,8 +625,9 @@ extern "C" bi_status bi_forward_step(bi_model* m, const bi_batch* batch, const b
     if (lm_head) {
         bi_bf16* yr = reinterpret_cast<bi_bf16*>(base + L.yr);
         float* logits = logits_out ? logits_out : fuse ? nullptr : reinterpret_cast<float*>(base + L.logits);
-        // the final norm of the logit rows (gathered by d_rows), in the LM head when it has few rows
-        const NormFuse final_norm{x, m->gamma_final, nullptr, c.eps};
+        // the final norm of the logit rows (gathered by d_rows), in the LM head when it has few rows; there it
+        // reads x's first R rows, and d_rows (which a replayed graph may have changed) is checked against them
+        const NormFuse final_norm{x, m->gamma_final, d_rows, c.eps};
         if (!norm_in_lm)
             BI_TRY_CUDA(launch_rmsnorm(x, m->gamma_final, yr, b.R, c.d, c.eps, s, d_rows), "final rmsnorm");
         BI_TRY(run_gemm(yr, m->w_lm, logits, BI_F32, nullptr, BI_EP_NONE, b.R, c.V, c.d, mode, gws, gws_bytes,

@@ -98,13 +98,15 @@ struct RopeFuse {
 cudaError_t launch_rmsnorm(const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y, int64_t rows,
                            int32_t d, float eps, cudaStream_t s, const int32_t* src_rows = nullptr,
                            const ArgmaxFuse* am = nullptr);
-// RMSNorm fused into a GEMM's A operand (few rows): A row r = bf16((x[src] * rinv) * gamma)
-// with src = rows[r] (or r), rinv from x[src]'s sum of squares in the RMSNorm kernel's
-// order, so the GEMM reads exactly the bits the RMSNorm kernel would have written.
+// RMSNorm fused into a GEMM's A operand (few rows): A row r = bf16((x[r] * rinv) * gamma)
+// for x's first M rows, rinv from x[r]'s sum of squares in the RMSNorm kernel's order, so
+// the GEMM reads exactly the bits the RMSNorm kernel would have written.  rows (device,
+// optional): the rows the caller means; where rows[r] != r the kernel reports
+// BI_DEV_BAD_LOGIT_ROWS (a replayed step whose rows no longer lead).
 struct NormFuse {
     const bi_bf16* x;
     const bi_bf16* gamma;
-    const int32_t* rows;  // device, optional
+    const int32_t* rows;
     float eps;
 };
 // after_all: launch without programmatic serialisation, so the kernel (and

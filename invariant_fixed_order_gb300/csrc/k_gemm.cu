@@ -113,6 +113,7 @@ struct GemmArgs {
     const uint4* norm_x;   // [M.., K / 8]
     const uint4* norm_gamma;
     float norm_eps;
+    const int32_t* norm_rows;  // the rows the caller means (must be 0..M-1), or null
 };
 
 // Rows up to which a GEMM may take its A operand through a fused RMSNorm:
@@ -607,6 +608,11 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
         // ---- A writers (fused RMSNorm): warps 2-3 of the issuing CTA; the tile's rows < M all lie in this
         // CTA's 128 rows (the pair's other CTA keeps its zeroed A region) ----
         norm_rinv_rows(args, norm_rinv, warp - 2);
+        if (args.norm_rows != nullptr && blockIdx.x == 0 && threadIdx.x == 64) {
+            // the fused norm reads x's first M rows: a caller's row list that says otherwise is reported
+            for (int32_t r = 0; r < static_cast<int32_t>(args.M); ++r)
+                if (args.norm_rows[r] != r) report(args.status, BI_DEV_BAD_LOGIT_ROWS);
+        }
         asm volatile("bar.sync 2, 192;" ::: "memory");  // every row's rinv (warps 2-7)
         const int t = threadIdx.x - 64;  // 0..63
         const int32_t rows = static_cast<int32_t>(args.M);
@@ -1009,8 +1015,8 @@ bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype
                    const RopeFuse* rope, const GemmWaitTest* wait_test, const NormFuse* norm) {
     if (M == 0) return BI_OK;
     if (norm != nullptr) {
-        if (!gemm_can_fuse_norm(M, N, K, mode) || wait_test != nullptr || norm->rows != nullptr)
-            return fail(BI_ERR_INVALID, "fused RMSNorm needs at most 8 contiguous rows, K <= 4096 and no split-K");
+        if (!gemm_can_fuse_norm(M, N, K, mode) || wait_test != nullptr)
+            return fail(BI_ERR_INVALID, "fused RMSNorm needs at most 8 rows, K <= 4096 and no split-K");
         A = norm->x;  // the A ring receives the raw rows
     }
     const GemmPlan plan = gemm_plan(M, N, K, mode);
@@ -1048,6 +1054,7 @@ bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype
         a.norm_x = reinterpret_cast<const uint4*>(norm->x);
         a.norm_gamma = reinterpret_cast<const uint4*>(norm->gamma);
         a.norm_eps = norm->eps;
+        a.norm_rows = norm->rows;
     }
     if (rope != nullptr) {
         if (!gemm_can_fuse_rope(M, N, K, mode, rope->Dh) || am != nullptr || ep != BI_EP_NONE ||

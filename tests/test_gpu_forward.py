@@ -195,6 +195,43 @@ def test_tiny_bad_token_reports_status(mods, tiny):
         eng.pool.free([int(table[0, 0]), int(table[1, 0])])
 
 
+def test_tiny_fused_final_norm_checks_replayed_logit_rows(mods, tiny):
+    """With at most 8 logit rows that are the step's first tokens, the final RMSNorm runs inside the LM head on
+    the residual stream's first R rows.  Device metadata (what a replay of such a captured step reads) must keep
+    those rows: kept, the step gives the host-metadata step's bits; changed, the step reports
+    BI_DEV_BAD_LOGIT_ROWS through the status word rather than answer silently for other rows."""
+    bi, sched, _ = mods
+    eng, prompts = tiny
+    B = 3
+    ids = [int(prompts[i][0]) for i in range(B)]
+    table = np.zeros((B, eng.max_pages), np.int32)
+    pages = [int(eng.pool.alloc(1)[0]) for _ in range(B)]
+    table[:, 0] = pages
+    try:
+        ref, _, _ = eng.step([1] * B, [0] * B, ids, table, list(range(B)))
+        ref = ref.clone()
+        eng.check()
+        d_ids = torch.tensor(ids, dtype=torch.int32, device="cuda")
+        d_table = torch.from_numpy(table).cuda()
+        for rows, ok in ((list(range(B)), True), ([2, 1, 0], False)):
+            meta = torch.tensor(list(range(B)) + [0] * B + list(range(B)) + rows, dtype=torch.int32, device="cuda")
+            logits = torch.empty(B, TINY.V, dtype=torch.float32, device="cuda")
+            tokens = torch.empty(B, dtype=torch.int32, device="cuda")
+            eng.model.forward_step([1] * B, [0] * B, d_ids, d_table, eng.k, eng.v, list(range(B)), eng.ws,
+                                   eng.status, logits_out=logits, tokens_out=tokens, meta=meta)
+            torch.cuda.synchronize()
+            if ok:
+                eng.check()
+                assert torch.equal(logits.view(torch.int32), ref.view(torch.int32))
+            else:
+                with pytest.raises(bi.BIError) as e:
+                    eng.check()
+                assert "0x204" in str(e.value)
+                bi.reset_status(eng.status)
+    finally:
+        eng.pool.free(pages)
+
+
 # ---------------------------------------------------------------------------
 # 8B-shaped single layer (decode steps over random compositions)
 # ---------------------------------------------------------------------------
