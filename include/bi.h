@@ -367,8 +367,10 @@ typedef struct {
     int32_t R;                  /* rows that need logits */
     const int32_t* logit_rows;  /* HOST [R] token indices in 0..T-1 */
     /* DEVICE [3T + R] or NULL.  NULL: the step derives its per-token metadata
-     * from q_len, pos0 and logit_rows and copies it host to device through a
-     * pinned staging buffer.  Non-NULL: the caller has written it on the
+     * from q_len, pos0 and logit_rows and hands it to its first kernel as a
+     * launch parameter (3T + R <= 1024: every decode step of up to 256
+     * tokens), or copies it host to device through a pinned staging buffer
+     * (larger steps).  Non-NULL: the caller has written it on the
      * device: [request of token t, T][position of token t, T][tokens with
      * q_len 1 in token order, nd][the other tokens in order, T - nd][logit
      * rows, R].  The step then reads no host memory after the call and calls

@@ -495,20 +495,29 @@ extern "C" bi_status bi_forward_step(bi_model* m, const bi_batch* batch, const b
     const size_t meta_n = static_cast<size_t>(T) * 3 + b.R;
     char* base = static_cast<char*>(ws);
     const int32_t* d_meta = b.meta;
+    // host metadata of a small step travels as the first kernel's parameter (no copy ahead of it)
+    StepMeta param_meta;
+    const bool meta_in_param = d_meta == nullptr && meta_n <= static_cast<size_t>(kStepMetaMax);
     if (d_meta == nullptr) {
-        // the step derives the metadata on the host and copies it through pinned staging
-        int slot = m->stage_next;
-        m->stage_next ^= 1;
-        BI_TRY_CUDA(cudaEventSynchronize(m->stage_done[slot]), "bi_forward_step: staging event");
-        if (m->stage_cap[slot] < meta_n) {
-            if (m->stage[slot]) cudaFreeHost(m->stage[slot]);
-            m->stage[slot] = nullptr;
-            m->stage_cap[slot] = 0;
-            const size_t cap = std::max<size_t>(meta_n * 2, 4096);
-            BI_TRY_CUDA(cudaHostAlloc(&m->stage[slot], cap * sizeof(int32_t), cudaHostAllocDefault), "cudaHostAlloc");
-            m->stage_cap[slot] = cap;
+        // the step derives the metadata on the host: into the first kernel's parameter, or (larger steps)
+        // through pinned staging and a copy
+        int32_t* hm = param_meta.v;
+        int slot = 0;
+        if (!meta_in_param) {
+            slot = m->stage_next;
+            m->stage_next ^= 1;
+            BI_TRY_CUDA(cudaEventSynchronize(m->stage_done[slot]), "bi_forward_step: staging event");
+            if (m->stage_cap[slot] < meta_n) {
+                if (m->stage[slot]) cudaFreeHost(m->stage[slot]);
+                m->stage[slot] = nullptr;
+                m->stage_cap[slot] = 0;
+                const size_t cap = std::max<size_t>(meta_n * 2, 4096);
+                BI_TRY_CUDA(cudaHostAlloc(&m->stage[slot], cap * sizeof(int32_t), cudaHostAllocDefault),
+                            "cudaHostAlloc");
+                m->stage_cap[slot] = cap;
+            }
+            hm = m->stage[slot];
         }
-        int32_t* hm = m->stage[slot];
         int32_t* h_req = hm;
         int32_t* h_pos = hm + T;
         int32_t* h_dec = hm + 2 * static_cast<size_t>(T);
@@ -525,8 +534,13 @@ extern "C" bi_status bi_forward_step(bi_model* m, const bi_batch* batch, const b
             std::memcpy(h_rows, b.logit_rows, sizeof(int32_t) * b.R);
         }
         int32_t* d_stage = reinterpret_cast<int32_t*>(base + L.meta);
-        BI_TRY_CUDA(cudaMemcpyAsync(d_stage, hm, meta_n * sizeof(int32_t), cudaMemcpyHostToDevice, s), "metadata copy");
-        BI_TRY_CUDA(cudaEventRecord(m->stage_done[slot], s), "cudaEventRecord");
+        if (meta_in_param) {
+            param_meta.n = static_cast<int32_t>(meta_n);
+        } else {
+            BI_TRY_CUDA(cudaMemcpyAsync(d_stage, hm, meta_n * sizeof(int32_t), cudaMemcpyHostToDevice, s),
+                        "metadata copy");
+            BI_TRY_CUDA(cudaEventRecord(m->stage_done[slot], s), "cudaEventRecord");
+        }
         d_meta = d_stage;
     }
     const int32_t* d_req = d_meta;
@@ -576,7 +590,8 @@ extern "C" bi_status bi_forward_step(bi_model* m, const bi_batch* batch, const b
     // the embedding gather and the first norm in one kernel (it also writes the residual stream x, and
     // initialises the fused argmax's keys)
     BI_TRY_CUDA(launch_embed_rmsnorm(m->embed, b.token_ids, c.V, m->gamma_attn[0], x, y, T, c.d, c.eps, dev_status,
-                                     s, fuse ? &am : nullptr, b.R),
+                                     s, fuse ? &am : nullptr, b.R, meta_in_param ? &param_meta : nullptr,
+                                     meta_in_param ? const_cast<int32_t*>(d_meta) : nullptr),
                 "embed + rmsnorm");
     for (int l = 0; l < c.n_layers; ++l) {
         // layer 0's norm ran with the embedding gather; later layers' in their QKV GEMM when it takes few rows

@@ -112,10 +112,20 @@ struct NormFuse {
 // after_all: launch without programmatic serialisation, so the kernel (and
 // every kernel chained after it) starts only once all earlier work on the
 // stream has finished.
-// x[t] = E[ids[t]] and y[t] = rmsnorm(x[t]) in one kernel (the norm's arithmetic), waiting for all earlier work
+// A forward step's per-token metadata small enough to travel as a kernel parameter (3T + R values: every
+// decode step of up to 256 tokens), so that a step with host metadata needs no host-to-device copy ahead of its
+// first kernel.
+constexpr int kStepMetaMax = 1024;
+struct StepMeta {
+    int32_t n;
+    int32_t v[kStepMetaMax];
+};
+// x[t] = E[ids[t]] and y[t] = rmsnorm(x[t]) in one kernel (the norm's arithmetic), waiting for all earlier work;
+// with meta, the kernel first writes meta->v[0 .. n) to meta_out for the kernels after it
 cudaError_t launch_embed_rmsnorm(const bi_bf16* E, const int32_t* ids, int32_t V, const bi_bf16* gamma, bi_bf16* x,
                                  bi_bf16* y, int32_t T, int32_t d, float eps, int32_t* status, cudaStream_t s,
-                                 const ArgmaxFuse* am = nullptr, int64_t am_rows = 0);
+                                 const ArgmaxFuse* am = nullptr, int64_t am_rows = 0, const StepMeta* meta = nullptr,
+                                 int32_t* meta_out = nullptr);
 cudaError_t launch_embed(const bi_bf16* E, const int32_t* ids, bi_bf16* x, int32_t T, int32_t V,
                          int32_t d, int32_t* status, cudaStream_t s, bool after_all = false);
 cudaError_t launch_rope_kv_append(const float* qkv, const int32_t* tok_req, const int32_t* tok_pos,

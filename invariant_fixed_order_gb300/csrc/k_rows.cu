@@ -24,12 +24,11 @@ constexpr int kNormWarps = 4;
 // the warp also writes it to x_out, the residual stream (an id outside the
 // vocabulary reports BI_DEV_BAD_TOKEN and reads as zeros, as embed_kernel).
 template <int CPL, bool kEmbed>
-__global__ void __launch_bounds__(kNormWarps * 32)
-rmsnorm_kernel(const uint4* x, const uint4* __restrict__ gamma, uint4* y, int64_t rows, int32_t d8, float eps,
-               float fd, const int32_t* __restrict__ src_rows, unsigned long long* am_keys, unsigned int* am_counter,
-               int64_t am_rows, const int32_t* __restrict__ ids, int32_t V, uint4* x_out, int32_t* status) {
-    pdl_trigger();
-    pdl_wait();
+__device__ __forceinline__ void rmsnorm_rows(const uint4* x, const uint4* __restrict__ gamma, uint4* y, int64_t rows,
+                                             int32_t d8, float eps, float fd, const int32_t* __restrict__ src_rows,
+                                             unsigned long long* am_keys, unsigned int* am_counter, int64_t am_rows,
+                                             const int32_t* __restrict__ ids, int32_t V, uint4* x_out,
+                                             int32_t* status) {
     const int64_t row = static_cast<int64_t>(blockIdx.x) * kNormWarps + threadIdx.x / 32;
     const int lane = threadIdx.x & 31;
     if (row >= rows) return;  // uniform per warp
@@ -118,6 +117,35 @@ rmsnorm_kernel(const uint4* x, const uint4* __restrict__ gamma, uint4* y, int64_
     }
 }
 
+template <int CPL, bool kEmbed>
+__global__ void __launch_bounds__(kNormWarps * 32)
+rmsnorm_kernel(const uint4* x, const uint4* __restrict__ gamma, uint4* y, int64_t rows, int32_t d8, float eps,
+               float fd, const int32_t* __restrict__ src_rows, unsigned long long* am_keys, unsigned int* am_counter,
+               int64_t am_rows, const int32_t* __restrict__ ids, int32_t V, uint4* x_out, int32_t* status) {
+    pdl_trigger();
+    pdl_wait();
+    rmsnorm_rows<CPL, kEmbed>(x, gamma, y, rows, d8, eps, fd, src_rows, am_keys, am_counter, am_rows, ids, V, x_out,
+                              status);
+}
+
+// The step's first kernel with its per-token metadata as a parameter: every thread first copies its share of
+// the values to meta_out (read by the step's later kernels after their dependency wait), then the embedding
+// gather and the norm as rmsnorm_kernel<CPL, true>.
+template <int CPL>
+__global__ void __launch_bounds__(kNormWarps * 32)
+embed_rmsnorm_meta_kernel(const __grid_constant__ StepMeta meta, int32_t* meta_out, const uint4* x,
+                          const uint4* __restrict__ gamma, uint4* y, int64_t rows, int32_t d8, float eps, float fd,
+                          unsigned long long* am_keys, unsigned int* am_counter, int64_t am_rows,
+                          const int32_t* __restrict__ ids, int32_t V, uint4* x_out, int32_t* status) {
+    pdl_trigger();
+    pdl_wait();
+    for (int32_t i = static_cast<int32_t>(blockIdx.x * blockDim.x + threadIdx.x); i < meta.n;
+         i += static_cast<int32_t>(gridDim.x * blockDim.x))
+        meta_out[i] = meta.v[i];
+    rmsnorm_rows<CPL, true>(x, gamma, y, rows, d8, eps, fd, nullptr, am_keys, am_counter, am_rows, ids, V, x_out,
+                            status);
+}
+
 template <bool kEmbed>
 static cudaError_t launch_rmsnorm_t(bool pdl, const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y, int64_t rows,
                                     int32_t d, float eps, cudaStream_t s, const int32_t* src_rows,
@@ -148,10 +176,26 @@ cudaError_t launch_rmsnorm(const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y, i
 
 cudaError_t launch_embed_rmsnorm(const bi_bf16* E, const int32_t* ids, int32_t V, const bi_bf16* gamma, bi_bf16* x,
                                  bi_bf16* y, int32_t T, int32_t d, float eps, int32_t* status, cudaStream_t s,
-                                 const ArgmaxFuse* am, int64_t am_rows) {
+                                 const ArgmaxFuse* am, int64_t am_rows, const StepMeta* meta, int32_t* meta_out) {
     // the step's first kernel: launched without programmatic serialisation, so it waits for all earlier work;
     // it also initialises the keys of the step's fused greedy argmax (rows < am_rows <= T)
-    return launch_rmsnorm_t<true>(false, E, gamma, y, T, d, eps, s, nullptr, am, am_rows, ids, V, x, status);
+    if (meta == nullptr)
+        return launch_rmsnorm_t<true>(false, E, gamma, y, T, d, eps, s, nullptr, am, am_rows, ids, V, x, status);
+    if (T <= 0 || meta_out == nullptr || meta->n < 0 || meta->n > kStepMetaMax) return cudaErrorInvalidValue;
+    const dim3 grid(static_cast<unsigned>((T + kNormWarps - 1) / kNormWarps));
+    const dim3 block(kNormWarps * 32);
+    const int32_t d8 = d / 8;
+    auto go = [&](auto kernel) {
+        return launch_k(false, kernel, grid, block, 0, s, *meta, meta_out, reinterpret_cast<const uint4*>(E),
+                        reinterpret_cast<const uint4*>(gamma), reinterpret_cast<uint4*>(y), static_cast<int64_t>(T),
+                        d8, eps, static_cast<float>(d), am ? am->keys : nullptr, am ? am->counter : nullptr, am_rows,
+                        ids, V, reinterpret_cast<uint4*>(x), status);
+    };
+    if (d8 <= 32) return go(embed_rmsnorm_meta_kernel<1>);
+    if (d8 <= 64) return go(embed_rmsnorm_meta_kernel<2>);
+    if (d8 <= 128) return go(embed_rmsnorm_meta_kernel<4>);
+    if (d8 <= 256) return go(embed_rmsnorm_meta_kernel<8>);
+    return go(embed_rmsnorm_meta_kernel<16>);
 }
 
 // ---------------------------------------------------------------------------
