@@ -5,17 +5,16 @@
 // M-dependent kernel choice are what make a GEMM's per-element order follow
 // the batch.  Here every output element of a weight matrix, for every M, is
 // produced by the same sequence: tcgen05.mma products (bf16 in, fp32
-// accumulated in TMEM, N = 128, K = 16), K tiles of 64 in ascending order,
-// inside a K tile the four 16-deep MMAs in ascending order, all into one
-// accumulator.  Two instruction forms give every element the same bits
+// accumulated in TMEM, K = 16), K tiles of 64 in ascending order, inside a K
+// tile the four 16-deep MMAs in ascending order, all into one accumulator.
+// The instruction forms and widths below give every element the same bits
 // (tested bit for bit), so which one runs is data movement:
 //   * N <= 65536 (the projections of a layer): the CTA-pair form, M = 256
 //     over a cluster of two CTAs on two SMs.  The pair's MMA takes 128 rows of
-//     A from each CTA's shared memory and 64 of its 128 weight rows from
-//     each, so a layer projection with only 32-48 output tiles of 128 columns
-//     keeps twice the SMs busy, and a prefill GEMM's tensor cores read less
-//     shared memory per multiply-add (measured: ~55 ns per pair MMA against
-//     ~65 ns for a single-CTA 128x128x16 MMA);
+//     A from each CTA's shared memory and half its weight rows from each, so
+//     a layer projection with only 32-48 output tiles of 128 columns keeps
+//     twice the SMs busy (one MMA costs the same in either form: 32.7 ns at
+//     N = 128, measured with resident operands);
 //   * N > 65536 (a vocabulary projection): the single-CTA form, M = 128.
 //     Its hundreds of tiles fill every SM many times over, and one SM then
 //     consumes 4 KB of weights per MMA instead of the pair's 2 KB, which is
@@ -23,8 +22,10 @@
 //
 // What may follow M is only how that work is laid out, never the arithmetic
 // of an element:
-//   * tile width: 128 columns (one MMA per 16-deep step) for M <= 256, and
-//     256 columns (two MMAs per step sharing A) for larger M;
+//   * tile width: 128 columns for M <= 256 and 256 for larger M, one MMA of
+//     that width per 16-deep step (N = 256: the A slice is read from shared
+//     memory once per step instead of once per 128 columns, which is what
+//     lets a prefill GEMM keep the tensor pipe busy: 63 -> 87 % active);
 //   * the TMA box of A covers the smallest power of two >= min(M, 128) rows
 //     (16..128); A stages are packed at that stride, so the MMA's rows past
 //     the box read neighbouring stages: those rows of the accumulator are
@@ -190,17 +191,12 @@ __device__ __forceinline__ void epilogue_group(const GemmArgs& args, int64_t row
 }
 
 // Accumulator column (within a tile's TMEM buffer) of output column o of the
-// tile: in a pair, an MMA's columns 0-63 are the even CTA's W rows (output
-// columns g*64.. of the tile's first half), 64-127 the odd CTA's (second half).
+// tile.  A tile is one MMA wide (N = BN): in a pair, the MMA's first BN/2
+// columns are the even CTA's W rows (the tile's first half) and the rest the
+// odd CTA's, so in either form the column is o itself.
 template <int BN, int CG>
 __device__ __forceinline__ uint32_t acc_col(int32_t o) {
-    if constexpr (CG == 2) {
-        const int32_t hi = o >= BN / 2 ? 1 : 0;
-        const int32_t oo = o - hi * (BN / 2);
-        return static_cast<uint32_t>((oo / 64) * 128 + hi * 64 + (oo % 64));
-    } else {
-        return static_cast<uint32_t>(o);
-    }
+    return static_cast<uint32_t>(o);
 }
 
 // RoPE + KV append of one GEMM row (token), the arithmetic of rope_append_kernel: rotate-half pairs
@@ -351,12 +347,13 @@ __global__ void __launch_bounds__(kGemmThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, GemmArgs args) {
     static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair");
     constexpr int kTileM = CG * kBM;           // rows of a tile (the MMA's M)
-    constexpr int kGroups = BN / kUN;          // MMAs per 16-deep step
+    constexpr int kMmaN = BN;                  // one MMA per 16-deep step covers the tile (N = 128 or 256)
+    constexpr int kGroups = BN / kMmaN;        // MMAs per 16-deep step
     constexpr int kWRows = BN / CG;            // W rows (output columns) this CTA holds per K tile
     constexpr int kWBytes = kWRows * kBK * 2;  // bytes of one K tile of W in this CTA
     constexpr int kChunks = BN / kEpi;         // epilogue chunks per tile
     constexpr uint32_t kTmemCols = 2 * BN;     // two accumulator buffers
-    constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM, kUN);
+    constexpr uint32_t kIdesc = ptx::idesc_bf16_f32(kTileM, kMmaN);
     extern __shared__ __align__(1024) uint8_t smem_raw[];
     // both CTAs of a pair use identical offsets: the MMA descriptors and the
     // cluster addresses below name the same offset in either CTA
@@ -548,7 +545,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const uint64_t w_desc0 = ptx::smem_desc_sw128(smem_u32(sW));
             const uint32_t a_step = static_cast<uint32_t>(args.a_stride) >> 4;
             constexpr uint32_t w_step = kWBytes >> 4;
-            constexpr uint32_t g_step = ((kUN / CG) * kBK * 2) >> 4;  // the next MMA's W rows in each CTA
+            constexpr uint32_t g_step = ((kMmaN / CG) * kBK * 2) >> 4;  // the next MMA's W rows in each CTA
             int s = 0;
             uint32_t ph = 0;
             int32_t i = 0;
@@ -580,7 +577,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
                         for (int k = 0; k < kBK / 16; ++k) {
 #pragma unroll
                             for (int g = 0; g < kGroups; ++g)
-                                ptx::tc_mma_f16<CG>(acc + g * kUN, ad + 2u * k, wd + g * g_step + 2u * k, kIdesc,
+                                ptx::tc_mma_f16<CG>(acc + g * kMmaN, ad + 2u * k, wd + g * g_step + 2u * k, kIdesc,
                                                     (kb + j > 0 || k > 0) ? 1u : 0u);
                         }
                     }
@@ -716,10 +713,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
 #pragma unroll
                 for (int c = 0; c < 4; ++c) ptx::tmem_ld16(taddr + j * kEpi + c * 16, r[c]);
                 ptx::tmem_ld_wait();
-                // accumulator columns 64j..64j+63 are MMA j/2's columns 64(j%2)..; in a
-                // pair, an MMA's columns 0-63 are W rows held by the even CTA, 64-127 by the odd
-                const int32_t n0 = CG == 2 ? n_tile * BN + (j & 1) * (BN / 2) + (j >> 1) * kEpi
-                                           : n_tile * BN + j * kEpi;
+                // accumulator columns 64j..64j+63 are the tile's output columns 64j..
+                const int32_t n0 = n_tile * BN + j * kEpi;
                 if (row < args.M && args.C != nullptr) epilogue_group(args, row, n0, split, r);
                 if (args.am_keys != nullptr) {
 #pragma unroll
@@ -916,9 +911,9 @@ constexpr int64_t kDeepStageMaxM = 16;
 Layout choose_layout(int64_t M, int32_t N, int32_t K) {
     Layout L{};
     L.cg = mma_group(N);
-    // 256-wide tiles (two MMAs per step sharing the A slice, half the A
-    // re-reads from L2) for M > 256; for fewer rows 128-wide tiles spread the
-    // output over twice the tiles
+    // 256-wide tiles (one 256-wide MMA per step: half the A re-reads from L2
+    // and from shared memory) for M > 256; for fewer rows 128-wide tiles
+    // spread the output over twice the tiles
     L.bn = (M > 2 * kBM && N % 256 == 0) ? 256 : kUN;
     int32_t box = 16;
     while (box < kBM && box < M) box *= 2;
