@@ -14,7 +14,9 @@
 //     A from each CTA's shared memory and half its weight rows from each, so
 //     a layer projection with only 32-48 output tiles of 128 columns keeps
 //     twice the SMs busy (one MMA costs the same in either form: 32.7 ns at
-//     N = 128, measured with resident operands);
+//     N = 128, measured with resident operands).  With at most 64 rows (and
+//     no fused RoPE) the pair takes M = 128 instead, 64 rows per CTA, so each
+//     tensor core reads half the A rows per MMA;
 //   * N > 65536 (a vocabulary projection): the single-CTA form, M = 128.
 //     Its hundreds of tiles fill every SM many times over, and one SM then
 //     consumes 4 KB of weights per MMA instead of the pair's 2 KB, which is
@@ -79,7 +81,6 @@ constexpr int kEpi = 64;               // epilogue column chunk (a SwiGLU gate|u
 constexpr int kBK = BI_GEMM_BLOCK_K;   // 64
 constexpr int kMaxStages = 16;
 constexpr int kGemmThreads = 256;
-constexpr int kAFull = kBM * kBK * 2;  // bytes the MMA reads for A per K tile in one CTA (16 KB)
 constexpr int kGroupM = 16;            // M tiles per rasterisation band
 constexpr int kBarrierBytes = 1024;
 constexpr int kRingBudget = 212 * 1024;  // shared memory for the A and W rings
@@ -342,11 +343,16 @@ __device__ __forceinline__ void norm_rinv_rows(const GemmArgs& args, float* rinv
     }
 }
 
-template <int BN, int CG>
+// HALF: the CTA-pair MMA with M = 128 (64 rows of A and of the accumulator per CTA).  Its accumulator holds, in
+// CTA c, lanes 0-63 = rows 64c + lane for the tile's first 64 columns and lanes 64-127 = the same rows for the
+// last 64 (measured), so warp q's lanes are rows 64c + 32 (q % 2) + lane of column half q / 2.
+template <int BN, int CG, bool HALF = false>
 __global__ void __launch_bounds__(kGemmThreads, 1)
 gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ CUtensorMap tmW, GemmArgs args) {
     static_assert(CG == 1 || CG == 2, "one CTA or a CTA pair");
-    constexpr int kTileM = CG * kBM;           // rows of a tile (the MMA's M)
+    static_assert(!HALF || (CG == 2 && BN == kUN), "the half-row pair form has 128-wide tiles");
+    constexpr int kRowsCta = HALF ? kBM / 2 : kBM;  // rows of A (and of the accumulator) in one CTA
+    constexpr int kTileM = CG * kRowsCta;     // rows of a tile (the MMA's M)
     constexpr int kMmaN = BN;                  // one MMA per 16-deep step covers the tile (N = 128 or 256)
     constexpr int kGroups = BN / kMmaN;        // MMAs per 16-deep step
     constexpr int kWRows = BN / CG;            // W rows (output columns) this CTA holds per K tile
@@ -449,7 +455,7 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             // issuing CTA's full barrier counts the bytes of every CTA of the group
             const uint32_t stage_tx =
                 static_cast<uint32_t>(CG * kps) * (static_cast<uint32_t>(args.norm_on ? 0 : args.a_stride) + kWBytes);
-            const int32_t a_row0 = static_cast<int32_t>(rank) * kBM;     // this CTA's rows of the tile
+            const int32_t a_row0 = static_cast<int32_t>(rank) * kRowsCta;  // this CTA's rows of the tile
             const int32_t w_row0 = static_cast<int32_t>(rank) * kWRows;  // this CTA's W rows of the tile
             auto load = [&](void* dst, const CUtensorMap* map, int s_, int32_t y, int32_t z, uint64_t pol) {
                 if constexpr (CG == 2)
@@ -685,7 +691,8 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             const int b = i & 1;
             int32_t m_tile, n_tile;
             tile_coords(tile, m_tile, n_tile);
-            const int64_t row = static_cast<int64_t>(m_tile) * kTileM + rank * kBM + q * 32 + lane;
+            const int64_t row = HALF ? static_cast<int64_t>(m_tile) * kTileM + rank * kRowsCta + (q & 1) * 32 + lane
+                                     : static_cast<int64_t>(m_tile) * kTileM + rank * kBM + q * 32 + lane;
             if (args.rope_on && row < args.M) {
                 // the row's cos/sin table rows are read after the MMAs: fetch them into L1 meanwhile
                 const int32_t pos = args.rope.tok_pos[row];
@@ -708,13 +715,14 @@ gemm_tc_kernel(const __grid_constant__ CUtensorMap tmA, const __grid_constant__ 
             unsigned long long best = kArgmaxKeyNone;
             if (args.rope_on) rope_epilogue<BN, CG>(args, taddr, row, n_tile);
 #pragma unroll 1
-            for (int j = 0; j < (args.rope_on ? 0 : kChunks); ++j) {
+            for (int j = 0; j < (args.rope_on ? 0 : (HALF ? 1 : kChunks)); ++j) {
                 uint32_t r[4][16];
 #pragma unroll
                 for (int c = 0; c < 4; ++c) ptx::tmem_ld16(taddr + j * kEpi + c * 16, r[c]);
                 ptx::tmem_ld_wait();
-                // accumulator columns 64j..64j+63 are the tile's output columns 64j..
-                const int32_t n0 = n_tile * BN + j * kEpi;
+                // accumulator columns 64j..64j+63 are the tile's output columns 64j.. (half form: this warp's
+                // lanes hold column half q / 2 in accumulator columns 0-63)
+                const int32_t n0 = HALF ? n_tile * BN + (q >> 1) * kEpi : n_tile * BN + j * kEpi;
                 if (row < args.M && args.C != nullptr) epilogue_group(args, row, n0, split, r);
                 if (args.am_keys != nullptr) {
 #pragma unroll
@@ -886,6 +894,7 @@ namespace {
 
 struct Layout {
     int32_t cg, bn, a_box, a_stride, a_region, stages, kps;
+    bool half;  // CTA-pair MMA with M = 128: 64 rows per CTA
     size_t smem;
 };
 
@@ -908,19 +917,26 @@ constexpr int64_t kDeepStageMaxM = 16;
 
 // Layout of one launch.  Only data movement depends on M here; the MMA
 // sequence of every output element is the same for all layouts.
-Layout choose_layout(int64_t M, int32_t N, int32_t K) {
+// Rows up to which a pair-form product with 128-wide tiles takes the half-row pair MMA (M = 128: 64 rows of A
+// per CTA).  Each CTA's tensor core then reads 64 rows of A per MMA instead of 128, most of them padding at
+// decode sizes; the per-element arithmetic is the same (tested bit for bit against the full pair form).
+constexpr int64_t kHalfMaxM = 64;
+
+Layout choose_layout(int64_t M, int32_t N, int32_t K, bool half_ok) {
     Layout L{};
     L.cg = mma_group(N);
     // 256-wide tiles (one 256-wide MMA per step: half the A re-reads from L2
     // and from shared memory) for M > 256; for fewer rows 128-wide tiles
     // spread the output over twice the tiles
     L.bn = (M > 2 * kBM && N % 256 == 0) ? 256 : kUN;
+    L.half = half_ok && L.cg == 2 && L.bn == kUN && M <= kHalfMaxM;
+    const int32_t rows_cta = L.half ? kBM / 2 : kBM;  // rows of A the MMA reads in one CTA
     int32_t box = 16;
-    while (box < kBM && box < M) box *= 2;
+    while (box < rows_cta && box < M) box *= 2;
     L.a_box = box;
     L.a_stride = box * kBK * 2;
     const int32_t w_tile = (L.bn / L.cg) * kBK * 2;  // one K tile of this CTA's W rows
-    const int32_t pad = kAFull - L.a_stride;  // the last slot's 128-row window reaches this far past it
+    const int32_t pad = rows_cta * kBK * 2 - L.a_stride;  // the last slot's MMA window reaches this far past it
     const int32_t budget = kRingBudget - pad;
     const int32_t per_k = L.a_stride + w_tile;  // bytes of one K tile of A and W
     // deep stages (one large copy per operand) while at least two still fit
@@ -938,13 +954,14 @@ Layout choose_layout(int64_t M, int32_t N, int32_t K) {
     return L;
 }
 
-template <int BN, int CG>
+template <int BN, int CG, bool HALF = false>
 cudaError_t prepare_tiles() {
     static_assert(BN % kUN == 0, "a tile is a whole number of MMAs wide");
     static std::once_flag once;
     static cudaError_t err = cudaSuccess;
     std::call_once(once, [] {
-        err = cudaFuncSetAttribute(gemm_tc_kernel<BN, CG>, cudaFuncAttributeMaxDynamicSharedMemorySize, kMaxSmem);
+        err = cudaFuncSetAttribute(gemm_tc_kernel<BN, CG, HALF>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   kMaxSmem);
     });
     return err;
 }
@@ -977,14 +994,14 @@ int resident_pairs() {
 }
 
 // Units (pairs or CTAs) launched: one per tile up to what fits at once.
-template <int BN, int CG>
+template <int BN, int CG, bool HALF = false>
 cudaError_t launch_tiles(const CUtensorMap& tmA, const CUtensorMap& tmW, const GemmArgs& a, int64_t tiles,
                          int splits, size_t smem, cudaStream_t s) {
-    cudaError_t e = prepare_tiles<BN, CG>();
+    cudaError_t e = prepare_tiles<BN, CG, HALF>();
     if (e != cudaSuccess) return e;
     if constexpr (CG == 2) {
         const int64_t pairs = std::min<int64_t>(tiles, std::max(1, resident_pairs() / splits));
-        return launch_pair_pdl(gemm_tc_kernel<BN, CG>, dim3(static_cast<unsigned>(2 * pairs), splits),
+        return launch_pair_pdl(gemm_tc_kernel<BN, CG, HALF>, dim3(static_cast<unsigned>(2 * pairs), splits),
                                dim3(kGemmThreads), smem, s, tmA, tmW, a);
     } else {
         const int64_t ctas = std::min<int64_t>(tiles, std::max(1, num_sms() / splits));
@@ -1015,7 +1032,8 @@ bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype
         A = norm->x;  // the A ring receives the raw rows
     }
     const GemmPlan plan = gemm_plan(M, N, K, mode);
-    const Layout L = choose_layout(M, N, K);
+    // (the fused RoPE rotates pairs (i, i + Dh/2) of one row, which the half-row form puts in two warps)
+    const Layout L = choose_layout(M, N, K, rope == nullptr);
 
     if (L.smem > static_cast<size_t>(kMaxSmem)) return fail(BI_ERR_UNSUPPORTED, "bi_gemm: no ring layout fits");
     const int32_t nkb = K / kBK;
@@ -1033,7 +1051,8 @@ bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype
     a.K = K;
     a.kb_per_split = per;
     a.nkb_total = nkb;
-    a.m_tiles = static_cast<int32_t>((M + L.cg * kBM - 1) / (L.cg * kBM));
+    const int64_t tile_m = L.half ? kBM : static_cast<int64_t>(L.cg) * kBM;
+    a.m_tiles = static_cast<int32_t>((M + tile_m - 1) / tile_m);
     a.n_tiles = N / L.bn;
     a.a_box_rows = L.a_box;
     a.a_stride = L.a_stride;
@@ -1087,6 +1106,7 @@ bi_status run_gemm(const bi_bf16* A, const bi_bf16* W, void* C, bi_dtype c_dtype
     cudaError_t e;
     if (L.cg == 2)
         e = L.bn == 256 ? launch_tiles<256, 2>(tmA, tmW, a, tiles, plan.splits, L.smem, s)
+            : L.half    ? launch_tiles<kUN, 2, true>(tmA, tmW, a, tiles, plan.splits, L.smem, s)
                         : launch_tiles<kUN, 2>(tmA, tmW, a, tiles, plan.splits, L.smem, s);
     else
         e = L.bn == 256 ? launch_tiles<256, 1>(tmA, tmW, a, tiles, plan.splits, L.smem, s)
