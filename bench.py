@@ -305,9 +305,9 @@ def gemm_chain(steps: int, stream) -> dict:
 def gemm_floor(stream) -> dict:
     """What bounds a decode projection at M = 1 (one token), measured.  libbi_probe.so times one tcgen05 MMA
     per instruction form (operands resident in shared memory, unrolled issue) and how fast one SM takes in a
-    stream (TMA boxes, bulk copies; one CTA per SM).  In the CTA-pair form a 64-deep K tile costs each SM of
-    a pair four pair MMAs and bringing in 10 KB (its 64 W rows and the 16-row A box); a projection's tiles
-    run K / 64 such K tiles in a row, in waves over the 76 pairs.  The floor is that chain at the larger of
+    stream (TMA boxes, bulk copies; one CTA per SM).  At M = 1 the projections take the CTA-pair MMA with
+    M = 128; a 64-deep K tile costs each SM of a pair four such MMAs and bringing in 10 KB (its 64 W rows and
+    the 16-row A box); a projection's tiles run K / 64 such K tiles in a row, in waves over the 76 pairs.  The floor is that chain at the larger of
     the two costs per K tile (no launch overhead); each projection is also timed standalone at M = 1 with
     the L2 flushed before every launch."""
     import ctypes
@@ -329,7 +329,7 @@ def gemm_floor(stream) -> dict:
 
     forms = {"single 128x16": mma(1, 128, 16), "single 128x32": mma(1, 128, 32), "single 128x64": mma(1, 128, 64),
              "single 128x128": mma(1, 128, 128), "single 64x16": mma(1, 64, 16), "pair 256x64": mma(2, 256, 64),
-             "pair 256x128": mma(2, 256, 128), "pair 256x256": mma(2, 256, 256),
+             "pair 256x128": mma(2, 256, 128), "pair 256x256": mma(2, 256, 256), "pair 128x128": mma(2, 128, 128),
              "single 128x64, 4 accumulators alternating": mma(1, 128, 64, 4),
              "pair 256x128, 2 accumulators alternating": mma(2, 256, 128, 2)}
     ingest = {}
@@ -357,7 +357,7 @@ def gemm_floor(stream) -> dict:
         waves = -(-tiles // pairs)
         sms = 2 * min(tiles, pairs)
         ktiles = (K // 64) * waves
-        mma_ns = 4 * forms["pair 256x128"]
+        mma_ns = 4 * forms["pair 128x128"]
         ingest_ns = 10240 / per_cta[min((1, 32, 64, 96, 128, 152), key=lambda x: abs(x - sms))]
         floor_us = ktiles * max(mma_ns, ingest_ns) / 1e3
         W = (torch.randn(N, K, device="cuda", generator=g) * 0.02).to(torch.bfloat16)

@@ -2,7 +2,7 @@
 // libbi: built beside it as libbi_probe.so and run by `bench.py --floor`.
 //
 //   bip_mma_ns   time per tcgen05.mma.kind::f16 instruction of one form
-//                (single CTA, M = 64 or 128; CTA pair, M = 256), with both
+//                (single CTA, M = 64 or 128; CTA pair, M = 128 or 256), with both
 //                operands resident in shared memory and the issue loop fully
 //                unrolled: a chain into one accumulator, or alternating over
 //                independent accumulators (each its own chain);
@@ -228,14 +228,15 @@ int run_mma(uint32_t idesc, int32_t ncols, double* ns_per_mma) {
 using namespace bi;
 using namespace bi::probe;
 
-// ns per MMA instruction.  cg = 1: M = 64 or 128, N a multiple of 16 (8 for M = 64) up to 128; cg = 2: M = 256,
-// N a multiple of 16 up to 256.  nacc = 1, 2 or 4 accumulators of N columns (nacc * N <= 512).  Returns 0, or
+// ns per MMA instruction.  cg = 1: M = 64 or 128, N a multiple of 16 (8 for M = 64) up to 128; cg = 2: M = 256
+// with N a multiple of 16 up to 256, or M = 128 with N a multiple of 32 up to 256.  nacc = 1, 2 or 4 accumulators of N columns (nacc * N <= 512).  Returns 0, or
 // -1 (bad arguments), 1 (CUDA error), 2 (a wait ran out).
 extern "C" int bip_mma_ns(int cg, int M, int N, int nacc, double* ns_per_mma) {
     if (ns_per_mma == nullptr) return -1;
     const bool shape_ok = cg == 1 ? ((M == 128 && N % 16 == 0 && N >= 16 && N <= 128) ||
                                      (M == 64 && N % 8 == 0 && N >= 8 && N <= 128))
-                                  : (cg == 2 && M == 256 && N % 16 == 0 && N >= 16 && N <= 256);
+                                  : (cg == 2 && ((M == 256 && N % 16 == 0 && N >= 16 && N <= 256) ||
+                                                 (M == 128 && N % 32 == 0 && N >= 32 && N <= 256)));
     if (!shape_ok || (nacc != 1 && nacc != 2 && nacc != 4) || nacc * N > 512) return -1;
     const uint32_t idesc = ptx::idesc_bf16_f32(static_cast<uint32_t>(M), static_cast<uint32_t>(N));
     if (cg == 1) {

@@ -23,7 +23,8 @@ bad_mma = [
     (1, 128, 8, 1),     # M = 128 needs N a multiple of 16
     (1, 128, 256, 1),   # a single CTA holds 128 rows of B
     (1, 96, 16, 1),     # M is 64 or 128 for one CTA
-    (2, 128, 64, 1),    # the pair form is M = 256
+    (2, 64, 64, 1),     # the pair form is M = 128 or 256
+    (2, 128, 48, 1),    # M = 128 in a pair needs N a multiple of 32
     (2, 256, 264, 1),   # N at most 256
     (1, 128, 128, 8),   # 1, 2 or 4 accumulators
     (1, 128, 128, 4 + 1),
