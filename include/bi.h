@@ -9,9 +9,10 @@
  * in one fixed order with split points that depend on the request alone:
  *   - RMSNorm: one warp per row, lane-serial over 16-byte chunks, then a fixed
  *     xor-butterfly;
- *   - GEMM: tcgen05 MMAs (the two-SM pair form 256x128x16 or the single-SM
- *     form 128x128x16, which give every element the same bits), bf16 in,
- *     fp32 accumulate in TMEM, one K tile (64), K loop in ascending order, no
+ *   - GEMM: tcgen05 MMAs (the two-SM pair form with M = 256 or, for at most
+ *     64 rows, 128, or the single-SM form with M = 128; N = the tile width,
+ *     128 or 256; all give every element the same bits), bf16 in, fp32
+ *     accumulate in TMEM, one K tile (64), K loop in ascending order, no
  *     split-K, whatever M is;
  *   - attention: keys cut into chunks of BI_KV_CHUNK positions aligned to key 0
  *     ("Batch invariance and reproducible inference", "1 · Split-K and
@@ -129,8 +130,8 @@ bi_status bi_rmsnorm(const bi_bf16* x, const bi_bf16* gamma, bi_bf16* y,
  * (BI_EP_RESIDUAL and BI_EP_SWIGLU need BI_BF16); residual: DEVICE [M, N] bf16
  * for BI_EP_RESIDUAL, else NULL.
  * BI_INVARIANT: every element's K sum, for every M, runs in ascending 64-wide K
- * tiles through 16-deep MMAs (M=128, N=128) into one TMEM accumulator; only
- * data movement (tile width, TMA box, ring depth) may follow M.
+ * tiles through 16-deep MMAs into one TMEM accumulator; only data movement
+ * (the MMA form and tile width, TMA box, ring depth) may follow M.
  * BI_VARIANT: when the output has fewer tiles than SMs, K is split over CTAs
  * into an fp32 workspace and the partials are added in split order.
  * Requires K % 64 == 0, N % 128 == 0, M >= 0, 16-byte aligned pointers.
