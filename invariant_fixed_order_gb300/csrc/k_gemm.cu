@@ -120,8 +120,7 @@ struct GemmArgs {
 
 // Rows up to which a GEMM may take its A operand through a fused RMSNorm:
 // warps 2-3 then rescale every landed A stage of every output tile they visit
-// in shared memory, M x 256 elements per stage, which stays below a stage's
-// MMA time for these rows.
+// in shared memory, M x 64 elements per K tile of the stage.
 constexpr int64_t kNormMaxM = 8;
 
 __device__ __forceinline__ float silu_mul(float g, float u) {
